@@ -1,0 +1,678 @@
+// Kitty CPU oracle -- TEST INFRASTRUCTURE ONLY.
+//
+// A plain, slow, single-source C++17 restatement of what the Kitty hot path
+// computes: per-page channel statistics, variance ranking with a top-k boost
+// set, asymmetric min/max quantization of Keys (2-bit, boosted channels 4-bit
+// split into two 2-bit planes) and Values (2-bit per-token groups of 32
+// channels), the packed page format, the append/flush step, and fp64 decode
+// attention over the dequantized pages.
+//
+// Only the test suite, the package's smoke check and the bench's CPU-baseline
+// leg may load this library.  It shares no code with the CUDA path.  Build with
+// -O2 -ffp-contract=off (no fused multiply-add): every fp32 operation below is
+// one IEEE round-to-nearest-even operation, in the order written.
+//
+// Sources (by page title and section):
+//  * "Kitty: Accurate and Efficient 2-bit KV Cache Quantization with Dynamic
+//    Channel-wise Precision Boost" (arXiv 2511.18643), Abstract: channel
+//    ranking with a small boosted fraction, each mixed-precision Key page
+//    decomposed into two uniform 2-bit tensors, page-centric layout.
+//  * "Kitty -- Dynamic Channel-wise Mixed-Precision Keys" (VeloxQuant-MLX docs),
+//    How it works / Prefill phase steps 1-3 (per-channel variance, top
+//    hi_fraction*D channels at hi_bit, asymmetric min/max groups of group_size
+//    tokens), Decode phase step 2 (running variance formula), Effective
+//    bit-width, Configuration reference.
+//  * PagedAttention / FlashAttention (cited by the paper) for the block table
+//    and softmax attention semantics.
+// Readings where the pages are silent are stated next to the code that takes
+// them.  Parity status of every function is pinned by the CPU test suite.
+
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <thread>
+#include <vector>
+
+namespace {
+
+constexpr int D = 128;        // head_dim (the only supported value)
+constexpr int P = 32;         // tokens per page = kitty_group_size
+constexpr int VG = 32;        // channels per Value group
+
+// ---------------------------------------------------------------- formats
+// IEEE binary16 / bfloat16 <-> binary32, written out from the encodings.
+
+float f16_to_f32(uint16_t h) {
+  const uint32_t sign = (uint32_t)(h & 0x8000u) << 16;
+  const uint32_t e = (h >> 10) & 0x1Fu;
+  const uint32_t m = h & 0x3FFu;
+  uint32_t bits;
+  if (e == 0) {
+    if (m == 0) {
+      bits = sign;
+    } else {  // subnormal: m * 2^-24, exact in fp32
+      float v = std::ldexp((float)m, -24);
+      std::memcpy(&bits, &v, 4);
+      bits |= sign;
+    }
+  } else if (e == 31) {
+    bits = sign | 0x7F800000u | (m << 13);
+  } else {
+    bits = sign | ((e - 15 + 127) << 23) | (m << 13);
+  }
+  float f;
+  std::memcpy(&f, &bits, 4);
+  return f;
+}
+
+float bf16_to_f32(uint16_t b) {
+  uint32_t bits = (uint32_t)b << 16;
+  float f;
+  std::memcpy(&f, &bits, 4);
+  return f;
+}
+
+// binary32 -> binary16, round to nearest, ties to even, with subnormals.
+uint16_t f32_to_f16(float f) {
+  uint32_t x;
+  std::memcpy(&x, &f, 4);
+  const uint32_t sign = (x >> 16) & 0x8000u;
+  const uint32_t ax = x & 0x7FFFFFFFu;
+  if (ax >= 0x7F800000u) return (uint16_t)(sign | 0x7C00u | (ax > 0x7F800000u ? 0x200u : 0u));
+  if (ax >= 0x477FF000u) return (uint16_t)(sign | 0x7C00u);  // >= 65520 rounds to inf
+  if (ax >= 0x38800000u) {                                     // normal half range
+    const uint32_t e = (ax >> 23) - 127 + 15;
+    const uint32_t mant = ax & 0x7FFFFFu;
+    uint32_t h = (e << 10) | (mant >> 13);
+    const uint32_t rem = mant & 0x1FFFu;
+    if (rem > 0x1000u || (rem == 0x1000u && (h & 1u))) h++;
+    return (uint16_t)(sign | h);
+  }
+  if (ax < 0x33000000u) return (uint16_t)sign;  // below 2^-25: rounds to zero
+  const uint32_t e = ax >> 23;                   // 102..112
+  const uint32_t M = (ax & 0x7FFFFFu) | 0x800000u;
+  const uint32_t s = 126 - e;                    // 14..24
+  uint32_t m = M >> s;
+  const uint32_t rem = M & ((1u << s) - 1u);
+  const uint32_t half = 1u << (s - 1);
+  if (rem > half || (rem == half && (m & 1u))) m++;
+  return (uint16_t)(sign | m);
+}
+
+float in_to_f32(uint16_t v, int dtype) { return dtype == 1 ? bf16_to_f32(v) : f16_to_f32(v); }
+
+// ---------------------------------------------------------------- page format
+// Byte layout of one (page, kv-head) blob, n_hi a multiple of 16 in [0, 128]:
+//   Kbase  1024 B   2-bit codes, all D channels x 32 tokens
+//   Kextra n_hi*8 B 2-bit low halves of the boosted channels' 4-bit codes
+//   KS     256 B    fp16 step per channel (boosted: the base-plane step)
+//   KM     256 B    fp16 minimum per channel
+//   Kch    n_hi B   boosted channel ids, ascending (row j of Kextra = Kch[j])
+//   Vbase  1024 B   2-bit codes, 32 tokens x D channels
+//   VS     256 B    fp16 step per (group, token), group-major [4][32]
+//   VM     256 B    fp16 minimum per (group, token), group-major [4][32]
+struct Layout {
+  int n_hi;
+  size_t kbase, kextra, ks, km, kch, vbase, vs, vm, bytes;
+  explicit Layout(int nh) : n_hi(nh) {
+    kbase = 0;
+    kextra = 1024;
+    ks = kextra + (size_t)nh * 8;
+    km = ks + 256;
+    kch = km + 256;
+    vbase = kch + (size_t)nh;
+    vs = vbase + 1024;
+    vm = vs + 256;
+    bytes = vm + 256;
+  }
+};
+
+// Position of one 2-bit code inside a plane: 32-bit little-endian word index
+// and bit offset.  Each plane is stored in "fragment order": the 32 bytes (8
+// words) of lane L hold exactly the codes that lane L of a 32-thread warp needs
+// as 16x16 operand tiles, and inside a word the code of element (row, col) sits
+// at bit 16*(col parity) + 8*(col half of the 16-wide tile) + 2*tau, where tau
+// names the row's 8-row block.  The mapping is a bijection (checked by tests).
+//
+// Key planes: row = token t, col = channel c (base) or boosted row j (extra).
+struct BitPos { int word; int bit; };
+
+BitPos key_pos(int col, int t, int words_per_lane) {
+  const int ks = col >> 4, cc = col & 15;
+  const int half = cc >> 3, qq = (cc & 7) >> 1, e = cc & 1;
+  const int mt = t >> 4, rh = (t >> 3) & 1, r = t & 7;
+  const int tau = 2 * mt + rh;
+  const int lane = 4 * r + qq;
+  return {lane * words_per_lane + ks, 16 * e + 8 * half + 2 * tau};
+}
+
+// Value plane: row = channel c, col = token t (the transposed operand).
+BitPos val_pos(int t, int c) {
+  const int mc = c >> 4, rh = (c >> 3) & 1, r = c & 7;
+  const int kt = t >> 4, half = (t >> 3) & 1, qq = (t & 7) >> 1, e = t & 1;
+  const int tau = 2 * (mc & 1) + rh;
+  const int lane = 4 * r + qq;
+  return {lane * 8 + (mc >> 1) * 2 + kt, 16 * e + 8 * half + 2 * tau};
+}
+
+void put2(uint8_t* plane, BitPos p, uint32_t code) {
+  uint32_t w;
+  std::memcpy(&w, plane + 4 * p.word, 4);
+  w |= (code & 3u) << p.bit;
+  std::memcpy(plane + 4 * p.word, &w, 4);
+}
+
+uint32_t get2(const uint8_t* plane, BitPos p) {
+  uint32_t w;
+  std::memcpy(&w, plane + 4 * p.word, 4);
+  return (w >> p.bit) & 3u;
+}
+
+uint16_t rd16(const uint8_t* p, size_t i) { uint16_t v; std::memcpy(&v, p + 2 * i, 2); return v; }
+void wr16(uint8_t* p, size_t i, uint16_t v) { std::memcpy(p + 2 * i, &v, 2); }
+
+}  // namespace
+
+// ---------------------------------------------------------------- status codes
+// Same numbering as the library's public header; defined here on their own.
+namespace {
+constexpr int ST_OK = 0, ST_EMPTY = 1, ST_RANGE = 2, ST_NONFINITE = 3, ST_BAD_PAGE = 4,
+              ST_BAD_LEN = 5, ST_TAIL_FULL = 6, ST_BAD_FLUSH = 7, ST_TABLE_FULL = 8,
+              ST_BAD_SEQ = 9;
+
+void note(int* st, int code) { if (*st == ST_OK) *st = code; }
+
+int g_threads = 1;
+
+// Run f(i) for i in [0, n) on g_threads std::threads (static interleaved split).
+template <class F>
+void parallel_for(int n, F f) {
+  const int nt = std::max(1, std::min(g_threads, n));
+  if (nt == 1) { for (int i = 0; i < n; ++i) f(i); return; }
+  std::vector<std::thread> ts;
+  for (int w = 0; w < nt; ++w)
+    ts.emplace_back([=]() { for (int i = w; i < n; i += nt) f(i); });
+  for (auto& t : ts) t.join();
+}
+
+// ---------------------------------------------------------------- statistics
+// Pairwise tree sum of 32 fp32 values: fold the upper half onto the lower half
+// 16, 8, 4, 2, 1 apart.  The pages fix no summation order; this one is chosen
+// and stated so that a GPU warp reduction can reproduce it bit for bit.
+float tree_sum(const float* x) {
+  float a[32];
+  for (int i = 0; i < 32; ++i) a[i] = x[i];
+  for (int w = 16; w >= 1; w >>= 1)
+    for (int i = 0; i < w; ++i) a[i] = a[i] + a[i + w];
+  return a[0];
+}
+
+struct PageStats { float mn[D], mx[D], s1[D], s2[D]; };
+
+// Per channel over the 32 tokens of one Key page: min, max, sum and sum of
+// squares (VeloxQuant-MLX docs, Prefill phase step 1 and step 5).
+void page_stats(const float* xk, PageStats& st) {
+  for (int c = 0; c < D; ++c) {
+    float col[P], sq[P];
+    float mn = xk[c], mx = xk[c];
+    for (int t = 0; t < P; ++t) {
+      const float x = xk[t * D + c];
+      col[t] = x;
+      sq[t] = x * x;
+      mn = std::min(mn, x);
+      mx = std::max(mx, x);
+    }
+    st.mn[c] = mn;
+    st.mx[c] = mx;
+    st.s1[c] = tree_sum(col);
+    st.s2[c] = tree_sum(sq);
+  }
+}
+
+// Running-variance estimate sigma^2 = (sum k^2)/n - ((sum k)/n)^2
+// (VeloxQuant-MLX docs, Decode phase step 2), three divisions/products and one
+// subtraction, each rounded once.
+float variance(float sum, float sumsq, float n) {
+  const float a = sumsq / n;
+  const float b = sum / n;
+  const float bb = b * b;
+  return a - bb;
+}
+
+// Top-k boost set (VeloxQuant-MLX docs, Prefill phase step 2): the n_hi
+// channels of largest variance; among equal variances the lower channel index
+// ranks first (reading).  rank_c counts the channels that beat channel c.
+void top_k(const float* var, int n_hi, bool* boosted) {
+  for (int c = 0; c < D; ++c) {
+    int rank = 0;
+    for (int o = 0; o < D; ++o)
+      if (var[o] > var[c] || (var[o] == var[c] && o < c)) ++rank;
+    boosted[c] = rank < n_hi;
+  }
+}
+
+// Asymmetric min/max quantization of one group (VeloxQuant-MLX docs, Prefill
+// phase step 3).  Readings: the minimum and the step are stored as fp16 and the
+// codes are computed against the STORED values, so encoder and decoder agree;
+// rounding is to nearest-even; codes are clamped to [0, 2^b - 1].  A boosted
+// Key channel stores the step of its high 2-bit plane, 4x the 4-bit step.
+void quant_group(const float* x, int stride, int n, float mn, float mx, int levels,
+                 bool boosted, uint16_t* S_out, uint16_t* M_out, uint8_t* code) {
+  const uint16_t M = f32_to_f16(mn);
+  const float Mf = f16_to_f32(M);
+  const float r = mx - mn;
+  const float s = r / (float)levels;
+  uint16_t S;
+  float u;
+  if (boosted) {
+    S = f32_to_f16(4.0f * s);
+    u = f16_to_f32(S) * 0.25f;
+  } else {
+    S = f32_to_f16(s);
+    u = f16_to_f32(S);
+  }
+  for (int i = 0; i < n; ++i) {
+    if (u == 0.0f) { code[i] = 0; continue; }
+    const float d = x[i * stride] - Mf;
+    const float y = d / u;
+    float q = std::nearbyint(y);
+    if (q < 0.0f) q = 0.0f;
+    if (q > (float)levels) q = (float)levels;
+    code[i] = (uint8_t)q;
+  }
+  *S_out = S;
+  *M_out = M;
+}
+
+// Input range rule: fp16 metadata must hold the values, so |x| <= 65504.
+int check_range(const float* x, int n) {
+  for (int i = 0; i < n; ++i) {
+    if (!std::isfinite(x[i])) return ST_NONFINITE;
+    if (std::fabs(x[i]) > 65504.0f) return ST_RANGE;
+  }
+  return ST_OK;
+}
+
+// Encode one (page, kv-head): Key planes with the given boost set, Value
+// planes, metadata and channel list, into `blob` (Layout(n_hi).bytes bytes).
+void encode_blob(const float* xk, const float* xv, const PageStats& st, const bool* boosted,
+                 int n_hi, uint8_t* blob) {
+  const Layout lay(n_hi);
+  std::memset(blob, 0, lay.bytes);
+  uint8_t* kbase = blob + lay.kbase;
+  uint8_t* kextra = blob + lay.kextra;
+  uint8_t* vbase = blob + lay.vbase;
+  int row_of[D];
+  int j = 0;
+  for (int c = 0; c < D; ++c) {
+    row_of[c] = -1;
+    if (boosted[c]) { blob[lay.kch + j] = (uint8_t)c; row_of[c] = j++; }
+  }
+  const int xw = n_hi / 16;  // Kextra words per lane
+  for (int c = 0; c < D; ++c) {
+    uint16_t S, M;
+    uint8_t code[P];
+    const bool b = boosted[c];
+    quant_group(xk + c, D, P, st.mn[c], st.mx[c], b ? 15 : 3, b, &S, &M, code);
+    wr16(blob + lay.ks, c, S);
+    wr16(blob + lay.km, c, M);
+    for (int t = 0; t < P; ++t) {
+      if (b) {
+        // 4-bit code c4 = 4*hi + lo: hi joins the uniform base plane, lo the
+        // extra plane row of this channel (two uniform 2-bit tensors).
+        put2(kbase, key_pos(c, t, 8), code[t] >> 2);
+        put2(kextra, key_pos(row_of[c], t, xw), code[t] & 3u);
+      } else {
+        put2(kbase, key_pos(c, t, 8), code[t]);
+      }
+    }
+  }
+  for (int t = 0; t < P; ++t) {
+    for (int g = 0; g < D / VG; ++g) {
+      const float* x = xv + t * D + g * VG;
+      float mn = x[0], mx = x[0];
+      for (int i = 1; i < VG; ++i) { mn = std::min(mn, x[i]); mx = std::max(mx, x[i]); }
+      uint16_t S, M;
+      uint8_t code[VG];
+      quant_group(x, 1, VG, mn, mx, 3, false, &S, &M, code);
+      wr16(blob + lay.vs, g * P + t, S);
+      wr16(blob + lay.vm, g * P + t, M);
+      for (int i = 0; i < VG; ++i) put2(vbase, val_pos(t, g * VG + i), code[i]);
+    }
+  }
+}
+
+// Quantize one page-head from fp32 token-major tiles xk, xv [32][D].  In
+// running mode the (sequence, head) accumulators are updated with this page's
+// sums before it is ranked; in page mode the page ranks on its own 32 tokens.
+int quantize_one(const float* xk, const float* xv, int n_hi, int running, float* rsum,
+                 float* rsq, int* rcount, uint8_t* blob) {
+  int st = check_range(xk, P * D);
+  if (st == ST_OK) st = check_range(xv, P * D);
+  PageStats ps;
+  page_stats(xk, ps);
+  float var[D];
+  if (running) {
+    *rcount += P;
+    const float n = (float)*rcount;
+    for (int c = 0; c < D; ++c) {
+      rsum[c] = rsum[c] + ps.s1[c];
+      rsq[c] = rsq[c] + ps.s2[c];
+      var[c] = variance(rsum[c], rsq[c], n);
+    }
+  } else {
+    for (int c = 0; c < D; ++c) var[c] = variance(ps.s1[c], ps.s2[c], (float)P);
+  }
+  bool boosted[D];
+  top_k(var, n_hi, boosted);
+  encode_blob(xk, xv, ps, boosted, n_hi, blob);
+  return st;
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------- decode side
+namespace {
+
+// Dequantize one page-head in fp64: k = M + S*hi + [boosted]*(S/4)*lo and
+// v = M + S*code, per the page format above.  Returns ST_BAD_PAGE if the
+// channel list is not a strictly ascending list of valid channel ids.
+int dequant(const uint8_t* blob, int n_hi, double* kh, double* vh) {
+  const Layout lay(n_hi);
+  int row_of[D];
+  for (int c = 0; c < D; ++c) row_of[c] = -1;
+  int prev = -1;
+  for (int j = 0; j < n_hi; ++j) {
+    const int ch = blob[lay.kch + j];
+    if (ch >= D || ch <= prev) return ST_BAD_PAGE;
+    row_of[ch] = j;
+    prev = ch;
+  }
+  const int xw = n_hi / 16;
+  for (int c = 0; c < D; ++c) {
+    const double S = f16_to_f32(rd16(blob + lay.ks, c));
+    const double M = f16_to_f32(rd16(blob + lay.km, c));
+    for (int t = 0; t < P; ++t) {
+      double v = M + S * (double)get2(blob + lay.kbase, key_pos(c, t, 8));
+      if (row_of[c] >= 0) v += (S / 4.0) * (double)get2(blob + lay.kextra, key_pos(row_of[c], t, xw));
+      kh[t * D + c] = v;
+    }
+  }
+  for (int t = 0; t < P; ++t)
+    for (int c = 0; c < D; ++c) {
+      const int g = c / VG;
+      const double S = f16_to_f32(rd16(blob + lay.vs, g * P + t));
+      const double M = f16_to_f32(rd16(blob + lay.vm, g * P + t));
+      vh[t * D + c] = M + S * (double)get2(blob + lay.vbase, val_pos(t, c));
+    }
+  return ST_OK;
+}
+
+struct AttnArgs {
+  int Hkv, Hq, n_hi, in_dtype;
+  const uint16_t* q;
+  const uint8_t* pool;
+  int pool_pages;
+  const int* block_table;
+  int max_pages;
+  const int* num_pages;
+  const uint16_t* tail_k;
+  const uint16_t* tail_v;
+  const int* tail_len;
+  double sm_scale;
+};
+
+// Softmax attention of the g query heads of kv head `kvh` of sequence b over
+// every cached token: the pages in block-table order, then the unquantized tail
+// (readings: no mask; grouped-query heads hq map to kv head hq / g).  fp64
+// throughout.  out has g*D entries.
+int attend_group(const AttnArgs& a, int b, int kvh, double* out) {
+  const int g = a.Hq / a.Hkv;
+  const Layout lay(a.n_hi);
+  const size_t page_stride = lay.bytes * (size_t)a.Hkv;
+  const int np = a.num_pages[b];
+  const int tl = a.tail_len[b];
+  for (int i = 0; i < g * D; ++i) out[i] = 0.0;
+  if (np < 0 || np > a.max_pages || tl < 0 || tl > P) return ST_BAD_LEN;
+  const int ntok = np * P + tl;
+  if (ntok == 0) return ST_EMPTY;
+  std::vector<double> kh((size_t)ntok * D), vh((size_t)ntok * D);
+  for (int p = 0; p < np; ++p) {
+    const int id = a.block_table[(size_t)b * a.max_pages + p];
+    if (id < 0 || id >= a.pool_pages) return ST_BAD_PAGE;
+    const uint8_t* blob = a.pool + (size_t)id * page_stride + (size_t)kvh * lay.bytes;
+    const int st = dequant(blob, a.n_hi, &kh[(size_t)p * P * D], &vh[(size_t)p * P * D]);
+    if (st != ST_OK) return st;
+  }
+  const size_t tail_base = ((size_t)b * a.Hkv + kvh) * P * D;
+  for (int t = 0; t < tl; ++t)
+    for (int c = 0; c < D; ++c) {
+      kh[(size_t)(np * P + t) * D + c] = in_to_f32(a.tail_k[tail_base + (size_t)t * D + c], a.in_dtype);
+      vh[(size_t)(np * P + t) * D + c] = in_to_f32(a.tail_v[tail_base + (size_t)t * D + c], a.in_dtype);
+    }
+  std::vector<double> s(ntok);
+  for (int h = 0; h < g; ++h) {
+    const int hq = kvh * g + h;
+    double q[D];
+    for (int c = 0; c < D; ++c) q[c] = in_to_f32(a.q[((size_t)b * a.Hq + hq) * D + c], a.in_dtype);
+    double m = -INFINITY;
+    for (int t = 0; t < ntok; ++t) {
+      double dot = 0.0;
+      for (int c = 0; c < D; ++c) dot += q[c] * kh[(size_t)t * D + c];
+      s[t] = a.sm_scale * dot;
+      m = std::max(m, s[t]);
+    }
+    double l = 0.0;
+    for (int t = 0; t < ntok; ++t) { s[t] = std::exp(s[t] - m); l += s[t]; }
+    for (int c = 0; c < D; ++c) {
+      double acc = 0.0;
+      for (int t = 0; t < ntok; ++t) acc += s[t] * vh[(size_t)t * D + c];
+      out[h * D + c] = acc / l;
+    }
+  }
+  return ST_OK;
+}
+
+bool valid_n_hi(int n_hi) { return n_hi >= 0 && n_hi <= D && n_hi % 16 == 0; }
+
+}  // namespace
+
+// ---------------------------------------------------------------- C entry points
+extern "C" {
+
+int orc_abi_version() { return 1; }
+
+void orc_set_threads(int n) { g_threads = n < 1 ? 1 : n; }
+
+// Bytes of one (page, kv-head) blob; -1 for an unsupported n_hi.
+long orc_page_bytes(int n_hi) { return valid_n_hi(n_hi) ? (long)Layout(n_hi).bytes : -1; }
+
+// Effective Key bits per element, codes only (VeloxQuant-MLX docs, Effective
+// bit-width): hi_fraction*hi_bit + (1 - hi_fraction)*lo_bit.
+double orc_avg_bits(double hi_fraction, int hi_bit, int lo_bit) {
+  return hi_fraction * hi_bit + (1.0 - hi_fraction) * lo_bit;
+}
+
+uint16_t orc_f32_to_f16(float f) { return f32_to_f16(f); }
+float orc_f16_to_f32(uint16_t h) { return f16_to_f32(h); }
+float orc_bf16_to_f32(uint16_t b) { return bf16_to_f32(b); }
+float orc_tree_sum(const float* x) { return tree_sum(x); }
+float orc_variance(float sum, float sumsq, float n) { return variance(sum, sumsq, n); }
+
+void orc_top_k(const float* var, int n_hi, uint8_t* boosted) {
+  bool b[D];
+  top_k(var, n_hi, b);
+  for (int c = 0; c < D; ++c) boosted[c] = b[c] ? 1 : 0;
+}
+
+void orc_key_pos(int col, int t, int words_per_lane, int* word, int* bit) {
+  const BitPos p = key_pos(col, t, words_per_lane);
+  *word = p.word;
+  *bit = p.bit;
+}
+
+void orc_val_pos(int t, int c, int* word, int* bit) {
+  const BitPos p = val_pos(t, c);
+  *word = p.word;
+  *bit = p.bit;
+}
+
+// One page-head from fp32 tiles [32][D] (token-major).  running != 0 updates
+// rsum/rsq [D] and *rcount before ranking.  Returns a status code.
+int orc_quantize_page_f32(const float* xk, const float* xv, int n_hi, int running, float* rsum,
+                          float* rsq, int* rcount, uint8_t* blob) {
+  if (!valid_n_hi(n_hi)) return -1;
+  return quantize_one(xk, xv, n_hi, running, rsum, rsq, rcount, blob);
+}
+
+void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int* status) {
+  *status = valid_n_hi(n_hi) ? dequant(blob, n_hi, kh, vh) : -1;
+}
+
+// Bulk quantization with the library's semantics.  k, v: [n_pages*32][Hkv][D]
+// 16-bit values (in_dtype 0 = fp16, 1 = bf16).  Page i is written at
+// pool + page_ids[i]*Hkv*blob.  rank_mode 0 = page, 1 = running; running mode
+// needs seq_of_page non-decreasing in [0, n_seqs) and accumulators
+// run_sum/run_sumsq [n_seqs][Hkv][D], run_count [n_seqs][Hkv].
+int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint16_t* k,
+                       const uint16_t* v, int n_pages, const int* page_ids, const int* seq_of_page,
+                       int n_seqs, float* run_sum, float* run_sumsq, int* run_count, uint8_t* pool,
+                       int pool_pages) {
+  if (!valid_n_hi(n_hi) || Hkv <= 0 || n_pages < 0) return -1;
+  const Layout lay(n_hi);
+  const size_t page_stride = lay.bytes * (size_t)Hkv;
+  int st = ST_OK;
+  if (rank_mode == 1) {
+    for (int i = 0; i < n_pages; ++i) {
+      const int s = seq_of_page[i];
+      if (s < 0 || s >= n_seqs || (i > 0 && s < seq_of_page[i - 1])) return ST_BAD_SEQ;
+    }
+  }
+  std::vector<int> sts(n_pages > 0 ? (size_t)n_pages * Hkv : 1, ST_OK);
+  auto one = [&](int i, int h) {
+    const int id = page_ids[i];
+    if (id < 0 || id >= pool_pages) { sts[(size_t)i * Hkv + h] = ST_BAD_PAGE; return; }
+    std::vector<float> xk(P * D), xv(P * D);
+    for (int t = 0; t < P; ++t)
+      for (int c = 0; c < D; ++c) {
+        const size_t src = (((size_t)i * P + t) * Hkv + h) * D + c;
+        xk[t * D + c] = in_to_f32(k[src], in_dtype);
+        xv[t * D + c] = in_to_f32(v[src], in_dtype);
+      }
+    float* rs = nullptr;
+    float* rq = nullptr;
+    int* rc = nullptr;
+    if (rank_mode == 1) {
+      const size_t sh = (size_t)seq_of_page[i] * Hkv + h;
+      rs = run_sum + sh * D;
+      rq = run_sumsq + sh * D;
+      rc = run_count + sh;
+    }
+    sts[(size_t)i * Hkv + h] = quantize_one(xk.data(), xv.data(), n_hi, rank_mode == 1, rs, rq, rc,
+                                            pool + (size_t)id * page_stride + (size_t)h * lay.bytes);
+  };
+  if (rank_mode == 1) {
+    // Each head's accumulators see that head's pages strictly in input order.
+    parallel_for(Hkv, [&](int h) { for (int i = 0; i < n_pages; ++i) one(i, h); });
+  } else {
+    parallel_for(n_pages * Hkv, [&](int ih) { one(ih / Hkv, ih % Hkv); });
+  }
+  for (int x : sts) note(&st, x);
+  return st;
+}
+
+// Append one token per sequence (VeloxQuant-MLX docs, Decode phase), with the
+// reading that a new token waits in an unquantized tail until 32 tokens form a
+// page: the token goes to tail[tail_len]; when the tail becomes full and the
+// caller named a page id for this sequence, the tail is quantized (running
+// statistics updated first in running mode), written at that page id, the id
+// is appended to the block table and the tail is emptied.
+// k_new, v_new: [B][Hkv][D]; tail_k, tail_v: [B][Hkv][32][D];
+// run_sum, run_sumsq: [B][Hkv][D]; run_count: [B][Hkv].
+int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint16_t* k_new,
+                     const uint16_t* v_new, uint16_t* tail_k, uint16_t* tail_v, int* tail_len,
+                     float* run_sum, float* run_sumsq, int* run_count, const int* flush_page_ids,
+                     int* block_table, int max_pages, int* num_pages, uint8_t* pool, int pool_pages,
+                     int B) {
+  if (!valid_n_hi(n_hi) || Hkv <= 0 || B < 0) return -1;
+  const Layout lay(n_hi);
+  const size_t page_stride = lay.bytes * (size_t)Hkv;
+  std::vector<int> sts(B > 0 ? B : 1, ST_OK);
+  parallel_for(B, [&](int b) {
+    const int len = tail_len[b];
+    if (len < 0 || len > P) { sts[b] = ST_BAD_LEN; return; }
+    if (len == P) { sts[b] = ST_TAIL_FULL; return; }
+    for (int h = 0; h < Hkv; ++h) {
+      const size_t dst = (((size_t)b * Hkv + h) * P + len) * D;
+      const size_t src = ((size_t)b * Hkv + h) * D;
+      for (int c = 0; c < D; ++c) {
+        tail_k[dst + c] = k_new[src + c];
+        tail_v[dst + c] = v_new[src + c];
+      }
+    }
+    const int n = len + 1;
+    const int fid = flush_page_ids[b];
+    if (fid >= 0 && n < P) { sts[b] = ST_BAD_FLUSH; tail_len[b] = n; return; }
+    if (n < P || fid < 0) { tail_len[b] = n; return; }
+    const int np = num_pages[b];
+    if (np < 0 || np >= max_pages) { sts[b] = ST_TABLE_FULL; tail_len[b] = n; return; }
+    if (fid >= pool_pages) { sts[b] = ST_BAD_PAGE; tail_len[b] = n; return; }
+    int st = ST_OK;
+    for (int h = 0; h < Hkv; ++h) {
+      std::vector<float> xk(P * D), xv(P * D);
+      const size_t base = ((size_t)b * Hkv + h) * P * D;
+      for (int i = 0; i < P * D; ++i) {
+        xk[i] = in_to_f32(tail_k[base + i], in_dtype);
+        xv[i] = in_to_f32(tail_v[base + i], in_dtype);
+      }
+      const size_t sh = (size_t)b * Hkv + h;
+      const bool running = rank_mode == 1;
+      note(&st, quantize_one(xk.data(), xv.data(), n_hi, running, running ? run_sum + sh * D : nullptr,
+                             running ? run_sumsq + sh * D : nullptr, running ? run_count + sh : nullptr,
+                             pool + (size_t)fid * page_stride + (size_t)h * lay.bytes));
+    }
+    block_table[(size_t)b * max_pages + np] = fid;
+    num_pages[b] = np + 1;
+    tail_len[b] = 0;
+    sts[b] = st;
+  });
+  int st = ST_OK;
+  for (int x : sts) note(&st, x);
+  return st;
+}
+
+// fp64 decode attention for every (sequence, query head); out: [B][Hq][D].
+// sm_scale multiplies q.k (callers pass 1/sqrt(D) unless they want another).
+int orc_decode_attention(int Hkv, int Hq, int n_hi, int in_dtype, const uint16_t* q,
+                         const uint8_t* pool, int pool_pages, const int* block_table, int max_pages,
+                         const int* num_pages, const uint16_t* tail_k, const uint16_t* tail_v,
+                         const int* tail_len, float sm_scale, int B, double* out) {
+  if (!valid_n_hi(n_hi) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B < 0) return -1;
+  const AttnArgs a{Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, max_pages,
+                   num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
+  const int g = Hq / Hkv;
+  std::vector<int> sts(B > 0 ? (size_t)B * Hkv : 1, ST_OK);
+  parallel_for(B * Hkv, [&](int i) {
+    const int b = i / Hkv, kvh = i % Hkv;
+    sts[i] = attend_group(a, b, kvh, out + ((size_t)b * Hq + (size_t)kvh * g) * D);
+  });
+  int st = ST_OK;
+  for (int x : sts) note(&st, x);
+  return st;
+}
+
+// The g query heads of one (sequence, kv head) only; out: [g][D].  For sampled
+// checks on workloads too large to run whole.
+int orc_decode_attention_one(int Hkv, int Hq, int n_hi, int in_dtype, const uint16_t* q,
+                             const uint8_t* pool, int pool_pages, const int* block_table,
+                             int max_pages, const int* num_pages, const uint16_t* tail_k,
+                             const uint16_t* tail_v, const int* tail_len, float sm_scale, int b,
+                             int kvh, double* out) {
+  if (!valid_n_hi(n_hi) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return -1;
+  const AttnArgs a{Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, max_pages,
+                   num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
+  return attend_group(a, b, kvh, out);
+}
+
+}  // extern "C"

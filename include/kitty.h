@@ -1,0 +1,189 @@
+/* kitty.h -- C ABI of the Kitty GB300 library (libkitty.so).
+ *
+ * Kitty keeps a paged KV cache at ~2 bits per element.  Key pages rank their
+ * channels by variance and store the top n_hi at 4 bits, split into two 2-bit
+ * planes, so every Key page is two uniform 2-bit tensors plus a channel list;
+ * Values use 2-bit per-token groups of 32 channels.  Decode attention reads the
+ * packed pages through a block table and dequantizes them in registers.
+ *
+ * Sources: "Kitty: Accurate and Efficient 2-bit KV Cache Quantization with
+ * Dynamic Channel-wise Precision Boost" (arXiv 2511.18643), Abstract; and
+ * "Kitty -- Dynamic Channel-wise Mixed-Precision Keys" (VeloxQuant-MLX docs),
+ * sections "How it works" (Prefill phase, Decode phase), "Effective bit-width"
+ * and "Configuration reference".
+ *
+ * Conventions for every entry point:
+ *  - Return value: KITTY_OK (0) or a negative KITTY_ERR_* code.  Arguments are
+ *    checked on the host before anything is launched; on an error nothing is
+ *    launched and no memory is touched.
+ *  - Device pointers are raw CUDA device addresses owned by the caller (the
+ *    library allocates no device memory and keeps no global state).  Work is
+ *    enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and the call returns without synchronizing.
+ *  - `d_status` (optional, may be NULL) is a caller-owned device int32.  Data
+ *    errors found on the device (bad page id, bad lengths, out-of-range input,
+ *    wait timeout) store a KITTY_ST_* code there if it still holds 0 (first
+ *    error wins); the affected work item is skipped.  The library never traps.
+ *  - 16-bit inputs are fp16 or bf16 per cfg->in_dtype.  Layouts are dense,
+ *    row-major, with the shapes given below.
+ */
+#ifndef KITTY_H_
+#define KITTY_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---------------------------------------------------------------- codes */
+#define KITTY_OK 0
+#define KITTY_ERR_INVALID_ARG -1 /* null pointer, bad size, misaligned pointer */
+#define KITTY_ERR_UNSUPPORTED -2 /* a configuration the kernels do not cover */
+#define KITTY_ERR_CUDA -3        /* a CUDA runtime call or launch failed */
+#define KITTY_ERR_WORKSPACE -4   /* workspace smaller than kitty_decode_workspace_bytes */
+#define KITTY_ERR_OOM -5         /* page allocator has too few free pages */
+
+/* device status codes (written to *d_status) */
+#define KITTY_ST_OK 0
+#define KITTY_ST_EMPTY 1      /* a sequence with no cached token: its output is 0 */
+#define KITTY_ST_RANGE 2      /* |input| > 65504: fp16 metadata cannot hold it */
+#define KITTY_ST_NONFINITE 3  /* NaN or Inf input */
+#define KITTY_ST_BAD_PAGE 4   /* page id outside [0, pool_pages) or corrupt page */
+#define KITTY_ST_BAD_LEN 5    /* num_pages outside [0, max_pages] or tail_len outside [0, 32] */
+#define KITTY_ST_TAIL_FULL 6  /* append to a tail that already holds 32 tokens */
+#define KITTY_ST_BAD_FLUSH 7  /* flush page id given although the tail did not fill */
+#define KITTY_ST_TABLE_FULL 8 /* flush with num_pages == max_pages */
+#define KITTY_ST_BAD_SEQ 9    /* seq_of_page not non-decreasing in [0, n_seqs) */
+#define KITTY_ST_TIMEOUT 10   /* a bounded wait on an in-flight copy gave up */
+
+#define KITTY_F16 0
+#define KITTY_BF16 1
+#define KITTY_F32 2 /* output only */
+
+#define KITTY_RANK_PAGE 0    /* rank each page on its own 32 tokens */
+#define KITTY_RANK_RUNNING 1 /* rank on running sum / sum of squares per (seq, head) */
+
+/* Configuration.  The parameters follow the VeloxQuant-MLX docs,
+ * "Configuration reference": kitty_hi_fraction (as n_hi = round(hf * D)),
+ * kitty_hi_bit, kitty_lo_bit, kitty_group_size, head_dim. */
+typedef struct {
+  int32_t head_dim;     /* D; must be 128 */
+  int32_t num_kv_heads; /* Hkv >= 1 */
+  int32_t num_q_heads;  /* Hq, a multiple of Hkv; decode needs Hq/Hkv <= 4 */
+  int32_t page_tokens;  /* tokens per page = Key quantization group; must be 32 */
+  int32_t n_hi;         /* boosted Key channels per page: 0, 16, 32, ..., 128 */
+  int32_t hi_bit;       /* must be 4 */
+  int32_t lo_bit;       /* must be 2 */
+  int32_t v_group;      /* channels per Value group; must be 32 */
+  int32_t rank_mode;    /* KITTY_RANK_PAGE or KITTY_RANK_RUNNING */
+  int32_t in_dtype;     /* KITTY_F16 or KITTY_BF16 for K, V, Q and the tails */
+  int32_t decode_pages_per_split; /* split-K chunk in pages; 0 = library's choice */
+} kitty_cfg;
+
+/* Library ABI version (this header: 1). */
+int kitty_abi_version(void);
+
+/* Packed page size.  A page holds Hkv blobs, one per kv head, in head order;
+ * physical page p starts at byte p * per_page of the pool.  Blob of one
+ * (page, kv head), in order: Key base plane 1024 B, Key extra plane n_hi*8 B,
+ * Key step fp16[128], Key minimum fp16[128], channel list uint8[n_hi]
+ * (ascending), Value plane 1024 B, Value step fp16[4][32], Value minimum
+ * fp16[4][32] (group-major).  = 3072 + 9*n_hi bytes (3360 at n_hi=32).  The
+ * bit positions inside the planes are the "fragment order" index maps
+ * documented in the oracle and DESIGN notes.  Paper: Abstract (page-centric
+ * layout, two uniform 2-bit tensors per Key page). */
+int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page);
+
+/* Effective Key bits per element, codes only: hf*hi_bit + (1-hf)*lo_bit with
+ * hf = n_hi/D (VeloxQuant-MLX docs, "Effective bit-width").  <0 on a bad cfg. */
+float kitty_avg_bits(const kitty_cfg* cfg);
+
+/* ---------------------------------------------------------------- page allocator
+ * Host-side free list of physical page ids [0, num_pages) (PagedAttention-style
+ * block table, cited by the paper).  LIFO and deterministic: a fresh allocator
+ * hands out 0, 1, 2, ...  Not thread-safe; one allocator per pool. */
+typedef struct kitty_alloc kitty_alloc;
+int kitty_alloc_create(int32_t num_pages, kitty_alloc** out);
+/* n ids into ids_out, all or nothing: KITTY_ERR_OOM if fewer than n are free. */
+int kitty_alloc_pages(kitty_alloc* a, int32_t n, int32_t* ids_out);
+/* Return ids; KITTY_ERR_INVALID_ARG (nothing freed) on an id out of range or
+ * not currently allocated. */
+int kitty_free_pages(kitty_alloc* a, int32_t n, const int32_t* ids);
+int32_t kitty_alloc_free_count(const kitty_alloc* a);
+void kitty_alloc_destroy(kitty_alloc* a);
+
+/* ---------------------------------------------------------------- quantize
+ * Quantize n_pages pages of 32 tokens into the pool.  Paper: Abstract (Dynamic
+ * Channel-wise Precision Boost, two-plane Key page); VeloxQuant-MLX docs,
+ * Prefill phase steps 1-3 and 5.
+ *   k, v        device [n_pages*32][Hkv][128] 16-bit; page i = tokens 32i..32i+31
+ *   page_ids    device int32 [n_pages]: page i is written at pool page page_ids[i]
+ *   Page mode: each page ranks its channels on its own 32 tokens; seq_of_page,
+ *   run_* may be NULL and n_seqs is ignored.
+ *   Running mode: seq_of_page device int32 [n_pages], non-decreasing, in
+ *   [0, n_seqs); run_sum, run_sumsq device f32 [n_seqs][Hkv][128] and run_count
+ *   device int32 [n_seqs][Hkv] are updated with each page's sums (in page order)
+ *   before that page is ranked.
+ *   pool        device, pool_pages * per_page bytes, 16-byte aligned. */
+int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const void* v, int32_t n_pages,
+                         const int32_t* page_ids, const int32_t* seq_of_page, int32_t n_seqs,
+                         float* run_sum, float* run_sumsq, int32_t* run_count, void* pool,
+                         int32_t pool_pages, int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------- append
+ * Append one token per sequence (VeloxQuant-MLX docs, Decode phase).  The token
+ * goes to tail[b][h][tail_len[b]]; when the tail becomes full (32 tokens) and
+ * flush_page_ids[b] >= 0, the tail is quantized as one page (running mode:
+ * accumulators updated first) into pool page flush_page_ids[b], that id is
+ * stored at block_table[b][num_pages[b]], num_pages[b] is incremented and the
+ * tail emptied.  The caller knows every tail length, so it prepares
+ * flush_page_ids without reading device memory.
+ *   k_new, v_new   device [B][Hkv][128] 16-bit
+ *   tail_k, tail_v device [B][Hkv][32][128] 16-bit
+ *   tail_len, num_pages device int32 [B]; block_table device int32 [B][max_pages]
+ *   run_sum, run_sumsq device f32 [B][Hkv][128], run_count int32 [B][Hkv]
+ *   (running mode only; may be NULL in page mode)
+ *   flush_page_ids device int32 [B], -1 = no flush for that sequence */
+int kitty_append_token(const kitty_cfg* cfg, const void* k_new, const void* v_new, void* tail_k,
+                       void* tail_v, int32_t* tail_len, float* run_sum, float* run_sumsq,
+                       int32_t* run_count, const int32_t* flush_page_ids, int32_t* block_table,
+                       int32_t max_pages, int32_t* num_pages, void* pool, int32_t pool_pages,
+                       int32_t B, int32_t* d_status, void* stream);
+
+/* ---------------------------------------------------------------- decode attention
+ * Workspace needed by kitty_decode_attention for this batch shape (0 when a
+ * single split suffices). */
+int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pages,
+                                 size_t* bytes);
+
+/* Split-K paged decode attention (paper: Abstract, page dequantization with a
+ * coalesced page-centric layout; FlashAttention-style online softmax).  For
+ * query head hq of sequence b (kv head hq / (Hq/Hkv)):
+ *   out[b][hq] = softmax_t(sm_scale * q.k_t) . v_t over the num_pages[b] pages
+ *   listed in block_table[b][0..num_pages[b]) followed by the tail_len[b] tail
+ *   tokens; an empty sequence gives 0 and KITTY_ST_EMPTY.
+ *   q       device [B][Hq][128] 16-bit (in_dtype)
+ *   pool    device, 16-byte aligned, pool_pages pages
+ *   tail_k, tail_v device [B][Hkv][32][128] 16-bit; may be NULL if all tails are 0
+ *   out     device [B][Hq][128] of out_dtype (KITTY_F32, KITTY_BF16, KITTY_F16)
+ *   workspace device, >= kitty_decode_workspace_bytes, 16-byte aligned (may be
+ *   NULL when that size is 0). */
+int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const void* pool,
+                           int32_t pool_pages, const int32_t* block_table, int32_t max_pages,
+                           const int32_t* num_pages, const void* tail_k, const void* tail_v,
+                           const int32_t* tail_len, float sm_scale, void* out, int32_t out_dtype,
+                           void* workspace, size_t workspace_bytes, int32_t B, int32_t* d_status,
+                           void* stream);
+
+/* Launch shape that kitty_decode_attention uses for this batch shape: number of
+ * splits per sequence and pages per split (for reporting and tests). */
+int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pages, int32_t* splits,
+                      int32_t* pages_per_split);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KITTY_H_ */

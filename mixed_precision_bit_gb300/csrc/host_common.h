@@ -1,0 +1,32 @@
+// Host-side argument checks shared by the Kitty entry points.
+#pragma once
+
+#include <stddef.h>
+#include <stdint.h>
+
+#include "kitty.h"
+
+namespace kitty {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Checks the fixed parameters; decode additionally needs Hq/Hkv <= 4.
+inline int check_cfg(const kitty_cfg* c, bool decode) {
+  if (c == nullptr) return KITTY_ERR_INVALID_ARG;
+  if (c->num_kv_heads <= 0 || c->num_q_heads <= 0 || c->num_q_heads % c->num_kv_heads != 0)
+    return KITTY_ERR_INVALID_ARG;
+  if (c->n_hi < 0 || c->n_hi > 128) return KITTY_ERR_INVALID_ARG;
+  if (c->head_dim != 128 || c->page_tokens != 32 || c->hi_bit != 4 || c->lo_bit != 2 ||
+      c->v_group != 32 || c->n_hi % 16 != 0)
+    return KITTY_ERR_UNSUPPORTED;
+  if (c->rank_mode != KITTY_RANK_PAGE && c->rank_mode != KITTY_RANK_RUNNING)
+    return KITTY_ERR_INVALID_ARG;
+  if (c->in_dtype != KITTY_F16 && c->in_dtype != KITTY_BF16) return KITTY_ERR_INVALID_ARG;
+  if (c->decode_pages_per_split < 0) return KITTY_ERR_INVALID_ARG;
+  if (decode && c->num_q_heads / c->num_kv_heads > 4) return KITTY_ERR_UNSUPPORTED;
+  return KITTY_OK;
+}
+
+inline size_t blob_bytes(int n_hi) { return 3072u + 9u * (size_t)n_hi; }
+
+}  // namespace kitty

@@ -1,0 +1,451 @@
+// Kitty page quantization for GB300 (sm_103a): channel statistics, variance
+// top-k boost selection, asymmetric min/max quantization of Keys (2-bit, boosted
+// channels 4-bit split into two 2-bit planes) and Values (2-bit per-token groups
+// of 32 channels), packed into the page-centric blob.
+//
+// Paper: "Kitty: Accurate and Efficient 2-bit KV Cache Quantization with
+// Dynamic Channel-wise Precision Boost", Abstract.  Steps: "Kitty -- Dynamic
+// Channel-wise Mixed-Precision Keys" (VeloxQuant-MLX docs), How it works,
+// Prefill phase steps 1-3 and 5, Decode phase steps 1-3.
+//
+// Every fp32 step uses an explicitly rounded intrinsic (no contraction), in the
+// order that defines the page bytes, so the packed pages are bit-exact with a
+// plain sequential implementation.  One CTA of 128 threads quantizes one
+// (page, kv-head): thread c owns Key channel c; thread 4t+G owns Value group G
+// of token t.
+#include "kitty_common.cuh"
+#include "host_common.h"
+
+namespace kitty {
+namespace {
+
+constexpr int kQThreads = 128;
+constexpr int kMaxBlobWords = (3072 + 9 * kD) / 4;
+
+struct QuantSmem {
+  float xk[kPage][kD];
+  float xv[kPage][kD / kVGroup][kVGroup + 1];  // padded: group reads hit 32 banks
+  float var[kD];
+  uint32_t blob[kMaxBlobWords];
+  int warp_cnt[kQThreads / 32];
+  int bad;
+};
+
+// Fixed pairwise tree over 32 values (upper half folded onto lower half, 16, 8,
+// 4, 2, 1 apart) -- the order the page bytes are defined with.
+__device__ __forceinline__ float tree32(float* a) {
+#pragma unroll
+  for (int w = 16; w >= 1; w >>= 1) {
+#pragma unroll
+    for (int i = 0; i < w; ++i) a[i] = __fadd_rn(a[i], a[i + w]);
+  }
+  return a[0];
+}
+
+// sigma^2 ~ sumsq/n - (sum/n)^2, each operation rounded once.
+__device__ __forceinline__ float running_var(float sum, float sumsq, float n) {
+  const float a = __fdiv_rn(sumsq, n);
+  const float b = __fdiv_rn(sum, n);
+  return __fsub_rn(a, __fmul_rn(b, b));
+}
+
+struct QuantParams {
+  float M, u;
+  uint16_t Sbits, Mbits;
+};
+
+// Asymmetric min/max group quantizer: fp16 minimum and step, codes computed
+// against the stored values; boosted Key channels store 4x the 4-bit step.
+__device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, bool boosted) {
+  QuantParams q;
+  const __half Mh = __float2half_rn(mn);
+  q.M = __half2float(Mh);
+  q.Mbits = __half_as_ushort(Mh);
+  const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
+  if (boosted) {
+    const __half Sh = __float2half_rn(__fmul_rn(4.0f, s));
+    q.Sbits = __half_as_ushort(Sh);
+    q.u = __fmul_rn(__half2float(Sh), 0.25f);
+  } else {
+    const __half Sh = __float2half_rn(s);
+    q.Sbits = __half_as_ushort(Sh);
+    q.u = __half2float(Sh);
+  }
+  return q;
+}
+
+__device__ __forceinline__ uint32_t qcode(float x, const QuantParams& q, int levels) {
+  if (q.u == 0.0f) return 0u;
+  int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, q.M), q.u));
+  c = c < 0 ? 0 : (c > levels ? levels : c);
+  return (uint32_t)c;
+}
+
+__device__ __forceinline__ bool in_range(float x, int* bad_code) {
+  if (!isfinite(x)) { *bad_code = KITTY_ST_NONFINITE; return false; }
+  if (fabsf(x) > 65504.0f) { *bad_code = KITTY_ST_RANGE; return false; }
+  return true;
+}
+
+// Quantize one (page, kv-head).  ksrc/vsrc point at token 0 of the tile; token t
+// is at +t*row_stride elements.  rsum/rsq/rcount: running accumulators of
+// channel `threadIdx.x` (running mode only).  Writes the blob to dst.
+template <int DT>
+__device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_t* vsrc,
+                              size_t row_stride, int n_hi, bool running, float& rsum, float& rsq,
+                              int& rcount, uint8_t* dst, int32_t* d_status) {
+  const int tid = threadIdx.x;
+  const int lane = tid & 31, warp = tid >> 5;
+  const BlobLayout lay(n_hi);
+  const int nwords = lay.bytes / 4;
+  if (tid == 0) sm.bad = 0;
+  for (int i = tid; i < nwords; i += kQThreads) sm.blob[i] = 0u;
+  __syncthreads();
+
+  int bad = 0;
+  for (int idx = tid; idx < kPage * (kD / 8); idx += kQThreads) {
+    const int t = idx >> 4, ch = (idx & 15) * 8;
+    const uint4 a = *reinterpret_cast<const uint4*>(ksrc + (size_t)t * row_stride + ch);
+    const uint4 b = *reinterpret_cast<const uint4*>(vsrc + (size_t)t * row_stride + ch);
+    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float k0 = bits16_to_f32((uint16_t)(aw[i] & 0xFFFFu), DT);
+      const float k1 = bits16_to_f32((uint16_t)(aw[i] >> 16), DT);
+      const float v0 = bits16_to_f32((uint16_t)(bw[i] & 0xFFFFu), DT);
+      const float v1 = bits16_to_f32((uint16_t)(bw[i] >> 16), DT);
+      in_range(k0, &bad); in_range(k1, &bad); in_range(v0, &bad); in_range(v1, &bad);
+      sm.xk[t][ch + 2 * i] = k0;
+      sm.xk[t][ch + 2 * i + 1] = k1;
+      sm.xv[t][(ch + 2 * i) >> 5][(ch + 2 * i) & 31] = v0;
+      sm.xv[t][(ch + 2 * i + 1) >> 5][(ch + 2 * i + 1) & 31] = v1;
+    }
+  }
+  if (bad) atomicCAS(&sm.bad, 0, bad);
+  __syncthreads();
+
+  // ---- Key channel statistics and variance (thread = channel c)
+  const int c = tid;
+  float x[kPage], tmp[kPage];
+  float mn, mx;
+  x[0] = sm.xk[0][c];
+  mn = mx = x[0];
+#pragma unroll
+  for (int t = 1; t < kPage; ++t) {
+    x[t] = sm.xk[t][c];
+    mn = fminf(mn, x[t]);
+    mx = fmaxf(mx, x[t]);
+  }
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
+  const float s1 = tree32(tmp);
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) tmp[t] = __fmul_rn(x[t], x[t]);
+  const float s2 = tree32(tmp);
+  float var;
+  if (running) {
+    rsum = __fadd_rn(rsum, s1);
+    rsq = __fadd_rn(rsq, s2);
+    rcount += kPage;
+    var = running_var(rsum, rsq, __int2float_rn(rcount));
+  } else {
+    var = running_var(s1, s2, (float)kPage);
+  }
+  sm.var[c] = var;
+  __syncthreads();
+
+  // ---- top-k: rank = #channels with larger variance, ties to the lower index
+  int rank = 0;
+#pragma unroll 8
+  for (int o = 0; o < kD; ++o) {
+    const float vo = sm.var[o];
+    rank += (vo > var || (vo == var && o < c)) ? 1 : 0;
+  }
+  const bool boosted = rank < n_hi;
+  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, boosted);
+  if (lane == 0) sm.warp_cnt[warp] = __popc(bal);
+  __syncthreads();
+  int row = __popc(bal & ((1u << lane) - 1u));
+  for (int w = 0; w < warp; ++w) row += sm.warp_cnt[w];
+
+  // ---- Key quantization of channel c and packing in fragment order
+  {
+    const int levels = boosted ? 15 : 3;
+    const QuantParams q = qparams(mn, mx, levels, boosted);
+    uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
+    b16[lay.ks / 2 + c] = q.Sbits;
+    b16[lay.km / 2 + c] = q.Mbits;
+    uint32_t code[kPage];
+#pragma unroll
+    for (int t = 0; t < kPage; ++t) code[t] = qcode(x[t], q, levels);
+    const int j = c >> 4, half = (c >> 3) & 1, qq = (c >> 1) & 3, e = c & 1;
+    const int bitbase = 16 * e + 8 * half;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int tau = 0; tau < 4; ++tau) {
+        const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
+        const uint32_t cb = boosted ? (code[t] >> 2) : code[t];
+        w |= cb << (bitbase + 2 * tau);
+      }
+      atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 8 + j], w);
+    }
+    if (boosted) {
+      const int wpl = n_hi / 16;
+      const int js = row >> 4, hx = (row >> 3) & 1, qx = (row >> 1) & 3, ex = row & 1;
+      const int bx = 16 * ex + 8 * hx;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        uint32_t w = 0;
+#pragma unroll
+        for (int tau = 0; tau < 4; ++tau) {
+          const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
+          w |= (code[t] & 3u) << (bx + 2 * tau);
+        }
+        atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w);
+      }
+      atomicOr(&sm.blob[(lay.kch + row) / 4], (uint32_t)c << (8 * (row & 3)));
+    }
+  }
+
+  // ---- Value quantization: thread 4t+G owns token t, channels 32G..32G+31
+  {
+    const int t = tid >> 2, G = tid & 3;
+    float v[kVGroup];
+    float vmn, vmx;
+#pragma unroll
+    for (int i = 0; i < kVGroup; ++i) v[i] = sm.xv[t][G][i];
+    vmn = vmx = v[0];
+#pragma unroll
+    for (int i = 1; i < kVGroup; ++i) { vmn = fminf(vmn, v[i]); vmx = fmaxf(vmx, v[i]); }
+    const QuantParams q = qparams(vmn, vmx, 3, false);
+    uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
+    b16[lay.vs / 2 + G * kPage + t] = q.Sbits;
+    b16[lay.vm / 2 + G * kPage + t] = q.Mbits;
+    const int qq = (t >> 1) & 3, kt = t >> 4, half = (t >> 3) & 1, e = t & 1;
+    const int bitbase = 16 * e + 8 * half;
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      uint32_t w = 0;
+#pragma unroll
+      for (int odd = 0; odd < 2; ++odd) {
+#pragma unroll
+        for (int rh = 0; rh < 2; ++rh) {
+          const int i = odd * 16 + rh * 8 + r;  // channel 32G + i has mc = 2G + odd
+          w |= qcode(v[i], q, 3) << (bitbase + 2 * (2 * odd + rh));
+        }
+      }
+      atomicOr(&sm.blob[lay.vbase / 4 + (4 * r + qq) * 8 + G * 2 + kt], w);
+    }
+  }
+  __syncthreads();
+
+  uint4* d4 = reinterpret_cast<uint4*>(dst);
+  const uint4* s4 = reinterpret_cast<const uint4*>(sm.blob);
+  for (int i = tid; i < lay.bytes / 16; i += kQThreads) d4[i] = s4[i];
+  if (tid == 0 && sm.bad) set_status(d_status, sm.bad);
+  __syncthreads();
+}
+
+// Page mode: one CTA per (input page i, kv head h).
+template <int DT>
+__global__ void __launch_bounds__(kQThreads) quantize_pages_kernel(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
+    int n_hi, int Hkv, uint8_t* pool, int pool_pages, int32_t* d_status) {
+  __shared__ QuantSmem sm;
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int pid = page_ids[i];
+  if (pid < 0 || pid >= pool_pages) {
+    if (threadIdx.x == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
+    return;
+  }
+  const BlobLayout lay(n_hi);
+  const size_t stride = (size_t)Hkv * kD;
+  const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
+  float dummy_s = 0.f, dummy_q = 0.f;
+  int dummy_c = 0;
+  quantize_tile<DT>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
+                    pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status);
+}
+
+__global__ void check_seq_kernel(const int32_t* seq_of_page, int n_pages, int n_seqs,
+                                 int32_t* d_status) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= n_pages) return;
+  const int s = seq_of_page[i];
+  if (s < 0 || s >= n_seqs || (i > 0 && s < seq_of_page[i - 1])) set_status(d_status, KITTY_ST_BAD_SEQ);
+}
+
+// Running mode: one CTA per (sequence s, kv head h) walks that sequence's pages
+// in order, carrying the channel accumulators in registers.
+template <int DT>
+__global__ void __launch_bounds__(kQThreads) quantize_running_kernel(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
+    const int32_t* seq_of_page, int n_pages, int n_hi, int Hkv, float* run_sum, float* run_sumsq,
+    int32_t* run_count, uint8_t* pool, int pool_pages, int32_t* d_status) {
+  __shared__ QuantSmem sm;
+  const int s = blockIdx.x, h = blockIdx.y;
+  // first page with seq >= s, and first with seq > s (binary search)
+  int lo = 0, hi = n_pages;
+  while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] < s) lo = m + 1; else hi = m; }
+  const int p0 = lo;
+  hi = n_pages;
+  while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] <= s) lo = m + 1; else hi = m; }
+  const int p1 = lo;
+  if (p0 >= p1) return;
+  const BlobLayout lay(n_hi);
+  const size_t stride = (size_t)Hkv * kD;
+  const size_t sh = (size_t)s * Hkv + h;
+  float rs = run_sum[sh * kD + threadIdx.x];
+  float rq = run_sumsq[sh * kD + threadIdx.x];
+  int rc = run_count[sh];
+  for (int i = p0; i < p1; ++i) {
+    const int pid = page_ids[i];
+    if (pid < 0 || pid >= pool_pages) {
+      if (threadIdx.x == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
+      continue;
+    }
+    const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
+    quantize_tile<DT>(sm, k + src, v + src, stride, n_hi, true, rs, rq, rc,
+                      pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status);
+  }
+  run_sum[sh * kD + threadIdx.x] = rs;
+  run_sumsq[sh * kD + threadIdx.x] = rq;
+  if (threadIdx.x == 0) run_count[sh] = rc;
+}
+
+// Append, part 1: one CTA per (sequence b, kv head h) writes the token into the
+// tail and, when the tail fills and a page id is given, quantizes the tail.
+template <int DT>
+__global__ void __launch_bounds__(kQThreads) append_heads_kernel(
+    const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new, uint16_t* tail_k,
+    uint16_t* tail_v, const int32_t* tail_len, float* run_sum, float* run_sumsq,
+    int32_t* run_count, const int32_t* flush_page_ids, int max_pages, const int32_t* num_pages,
+    uint8_t* pool, int pool_pages, int n_hi, int Hkv, int running, int32_t* d_status) {
+  __shared__ QuantSmem sm;
+  const int b = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int len = tail_len[b];
+  if (len < 0 || len > kPage) { if (c == 0) set_status(d_status, KITTY_ST_BAD_LEN); return; }
+  if (len == kPage) { if (c == 0) set_status(d_status, KITTY_ST_TAIL_FULL); return; }
+  const size_t sh = (size_t)b * Hkv + h;
+  tail_k[(sh * kPage + len) * kD + c] = k_new[sh * kD + c];
+  tail_v[(sh * kPage + len) * kD + c] = v_new[sh * kD + c];
+  const int n = len + 1;
+  const int fid = flush_page_ids[b];
+  if (fid >= 0 && n < kPage) { if (c == 0) set_status(d_status, KITTY_ST_BAD_FLUSH); return; }
+  if (n < kPage || fid < 0) return;
+  const int np = num_pages[b];
+  if (np < 0 || np >= max_pages) { if (c == 0) set_status(d_status, KITTY_ST_TABLE_FULL); return; }
+  if (fid >= pool_pages) { if (c == 0) set_status(d_status, KITTY_ST_BAD_PAGE); return; }
+  __syncthreads();  // the new token row is visible to the whole CTA
+  const BlobLayout lay(n_hi);
+  float rs = 0.f, rq = 0.f;
+  int rc = 0;
+  if (running) {
+    rs = run_sum[sh * kD + c];
+    rq = run_sumsq[sh * kD + c];
+    rc = run_count[sh];
+  }
+  quantize_tile<DT>(sm, tail_k + sh * kPage * kD, tail_v + sh * kPage * kD, kD, n_hi, running != 0,
+                    rs, rq, rc, pool + ((size_t)fid * Hkv + h) * lay.bytes, d_status);
+  if (running) {
+    run_sum[sh * kD + c] = rs;
+    run_sumsq[sh * kD + c] = rq;
+    if (c == 0) run_count[sh] = rc;
+  }
+}
+
+// Append, part 2: per-sequence bookkeeping (tail length, block table, page
+// count), after every head of the sequence has used the old values.
+__global__ void append_finalize_kernel(int32_t* tail_len, const int32_t* flush_page_ids,
+                                       int32_t* block_table, int max_pages, int32_t* num_pages,
+                                       int pool_pages, int B) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b >= B) return;
+  const int len = tail_len[b];
+  if (len < 0 || len >= kPage) return;
+  const int n = len + 1;
+  const int fid = flush_page_ids[b];
+  const int np = num_pages[b];
+  if (n == kPage && fid >= 0 && np >= 0 && np < max_pages && fid < pool_pages) {
+    block_table[(size_t)b * max_pages + np] = fid;
+    num_pages[b] = np + 1;
+    tail_len[b] = 0;
+  } else {
+    tail_len[b] = n;
+  }
+}
+
+}  // namespace
+}  // namespace kitty
+
+using namespace kitty;
+
+extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const void* v,
+                                    int32_t n_pages, const int32_t* page_ids,
+                                    const int32_t* seq_of_page, int32_t n_seqs, float* run_sum,
+                                    float* run_sumsq, int32_t* run_count, void* pool,
+                                    int32_t pool_pages, int32_t* d_status, void* stream) {
+  int rc = check_cfg(cfg, false);
+  if (rc != KITTY_OK) return rc;
+  if (n_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
+  if (n_pages == 0) return KITTY_OK;
+  if (!k || !v || !page_ids || !pool || !aligned16(k) || !aligned16(v) || !aligned16(pool))
+    return KITTY_ERR_INVALID_ARG;
+  const bool running = cfg->rank_mode == KITTY_RANK_RUNNING;
+  if (running && (!seq_of_page || n_seqs <= 0 || !run_sum || !run_sumsq || !run_count))
+    return KITTY_ERR_INVALID_ARG;
+  if (n_pages > 65535 * 1024) return KITTY_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int Hkv = cfg->num_kv_heads;
+  const auto* k16 = static_cast<const uint16_t*>(k);
+  const auto* v16 = static_cast<const uint16_t*>(v);
+  auto* p8 = static_cast<uint8_t*>(pool);
+  if (!running) {
+    dim3 grid(n_pages, Hkv);
+    if (cfg->in_dtype == KITTY_BF16)
+      quantize_pages_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, cfg->n_hi, Hkv, p8, pool_pages, d_status);
+    else
+      quantize_pages_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, cfg->n_hi, Hkv, p8, pool_pages, d_status);
+  } else {
+    check_seq_kernel<<<(n_pages + 255) / 256, 256, 0, s>>>(seq_of_page, n_pages, n_seqs, d_status);
+    dim3 grid(n_seqs, Hkv);
+    if (cfg->in_dtype == KITTY_BF16)
+      quantize_running_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+    else
+      quantize_running_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+  }
+  return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
+}
+
+extern "C" int kitty_append_token(const kitty_cfg* cfg, const void* k_new, const void* v_new,
+                                  void* tail_k, void* tail_v, int32_t* tail_len, float* run_sum,
+                                  float* run_sumsq, int32_t* run_count,
+                                  const int32_t* flush_page_ids, int32_t* block_table,
+                                  int32_t max_pages, int32_t* num_pages, void* pool,
+                                  int32_t pool_pages, int32_t B, int32_t* d_status, void* stream) {
+  int rc = check_cfg(cfg, false);
+  if (rc != KITTY_OK) return rc;
+  if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
+  if (B == 0) return KITTY_OK;
+  if (!k_new || !v_new || !tail_k || !tail_v || !tail_len || !flush_page_ids || !block_table ||
+      !num_pages || !pool || !aligned16(tail_k) || !aligned16(tail_v) || !aligned16(pool))
+    return KITTY_ERR_INVALID_ARG;
+  const bool running = cfg->rank_mode == KITTY_RANK_RUNNING;
+  if (running && (!run_sum || !run_sumsq || !run_count)) return KITTY_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int Hkv = cfg->num_kv_heads;
+  dim3 grid(B, Hkv);
+  auto* tk = static_cast<uint16_t*>(tail_k);
+  auto* tv = static_cast<uint16_t*>(tail_v);
+  const auto* kn = static_cast<const uint16_t*>(k_new);
+  const auto* vn = static_cast<const uint16_t*>(v_new);
+  auto* p8 = static_cast<uint8_t*>(pool);
+  if (cfg->in_dtype == KITTY_BF16)
+    append_heads_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(kn, vn, tk, tv, tail_len, run_sum, run_sumsq, run_count, flush_page_ids, max_pages, num_pages, p8, pool_pages, cfg->n_hi, Hkv, running ? 1 : 0, d_status);
+  else
+    append_heads_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(kn, vn, tk, tv, tail_len, run_sum, run_sumsq, run_count, flush_page_ids, max_pages, num_pages, p8, pool_pages, cfg->n_hi, Hkv, running ? 1 : 0, d_status);
+  append_finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(tail_len, flush_page_ids, block_table, max_pages, num_pages, pool_pages, B);
+  return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
+}

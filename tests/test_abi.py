@@ -1,0 +1,103 @@
+"""The C ABI library builds, loads and exports every declared entry point; its
+host-only parts (sizes, effective bits, page allocator, argument checks) work
+without a GPU."""
+
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def K():
+    from mixed_precision_bit_gb300 import kitty
+    kitty.load()
+    return kitty
+
+
+def _declared():
+    names = set()
+    for f in os.listdir(os.path.join(ROOT, "include")):
+        if f.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", f)).read()
+            names |= set(re.findall(r"^(?:int|int32_t|float|void)\s+\*?(kitty_[a-z_0-9]+)\s*\(",
+                                    src, re.M))
+    return names
+
+
+def test_exports_every_declared_symbol(K):
+    names = _declared()
+    assert {"kitty_quantize_pages", "kitty_append_token", "kitty_decode_attention"} <= names
+    lib = K.load()
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(K.EXPORTS) == names
+    assert lib.kitty_abi_version() == 1
+
+
+def test_page_bytes_and_avg_bits(K):
+    for n_hi, blob in ((32, 3360), (16, 3216), (0, 3072), (128, 4224)):
+        cfg = K.Config(num_kv_heads=8, num_q_heads=32, n_hi=n_hi)
+        assert K.page_bytes(cfg) == (blob, 8 * blob)
+    assert K.avg_bits(K.Config(8, 32, n_hi=32)) == 2.5
+    assert K.avg_bits(K.Config(8, 32, n_hi=0)) == 2.0
+    assert K.avg_bits(K.Config(8, 32, n_hi=64)) == 3.0
+
+
+def test_config_checks(K):
+    for bad, code in ((dict(n_hi=8), -2), (dict(head_dim=64), -2), (dict(hi_bit=8), -2),
+                      (dict(num_q_heads=12), -1), (dict(in_dtype=7), -1)):
+        cfg = K.Config(**{**dict(num_kv_heads=8, num_q_heads=32), **bad})
+        with pytest.raises(K.KittyError) as e:
+            K.page_bytes(cfg)
+        assert e.value.code == code
+    cfg = K.Config(num_kv_heads=8, num_q_heads=64)   # g = 8: quantize ok, decode unsupported
+    K.page_bytes(cfg)
+    with pytest.raises(K.KittyError):
+        K.decode_workspace_bytes(cfg, 4, 16)
+
+
+def test_allocator(K):
+    a = K.PageAllocator(6)
+    assert list(a.alloc(3)) == [0, 1, 2] and a.free_count == 3
+    with pytest.raises(K.KittyError) as e:
+        a.alloc(4)
+    assert e.value.code == -5 and a.free_count == 3
+    a.free([1])
+    assert list(a.alloc(1)) == [1]
+    with pytest.raises(K.KittyError):
+        a.free([5])          # not allocated
+    with pytest.raises(K.KittyError):
+        a.free([0, 0])       # duplicate
+    assert a.free_count == 3
+    a.free([0, 1, 2])
+    assert a.free_count == 6
+    a.close()
+
+
+def test_null_arguments_rejected_before_launch(K):
+    """Argument errors come back synchronously and nothing is launched."""
+    lib = K.load()
+    cfg = K.Config(num_kv_heads=1, num_q_heads=1).c()
+    rc = lib.kitty_quantize_pages(ctypes.byref(cfg), None, None, 1, None, None, 0, None, None,
+                                  None, None, 1, None, None)
+    assert rc == -1
+    rc = lib.kitty_decode_attention(ctypes.byref(cfg), None, None, 1, None, 1, None, None, None,
+                                    None, 0.1, None, 0, None, 0, 1, None, None)
+    assert rc == -1
+    assert lib.kitty_quantize_pages(ctypes.byref(cfg), None, None, 0, None, None, 0, None, None,
+                                    None, None, 0, None, None) == 0   # empty batch: no-op
+
+
+def test_decode_plan_and_workspace(K):
+    cfg = K.Config(num_kv_heads=8, num_q_heads=32)
+    s, c = K.decode_plan(cfg, 16, 128)
+    assert s * c >= 128 and c % 4 == 0 and c >= 16
+    assert K.decode_workspace_bytes(cfg, 16, 128) == (16 * 32 * s * 130 * 4 if s > 1 else 0)
+    cfg.decode_pages_per_split = 1000
+    assert K.decode_plan(cfg, 16, 128) == (1, 1000)
+    assert K.decode_workspace_bytes(cfg, 16, 128) == 0

@@ -1,0 +1,193 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle on the
+same seeded inputs.  Packed pages, channel lists, scales and running
+statistics must be bit-exact; attention within 2e-3 * RMS(oracle output)
+(+ half an output ulp for 16-bit outputs)."""
+
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+from mixed_precision_bit_gb300 import synth
+from tests.kitty_cases import (attn_error, gpu_decode, gpu_quantize, oracle_decode,
+                               oracle_quantize, dev16, dev32, cfg_for)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixed_precision_bit_gb300 import kitty
+    kitty.load()
+
+
+def _variant(name, **kw):
+    return dataclasses.replace(synth.workload(name), **kw)
+
+
+CASES = [
+    ("tiny", {}),
+    ("small_gqa", {}),
+    ("small_gqa", dict(n_hi=0)),
+    ("small_gqa", dict(n_hi=16)),
+    ("small_gqa", dict(n_hi=64)),
+    ("small_gqa", dict(n_hi=128)),
+    ("small_gqa", dict(dtype=synth.F16)),
+    ("small_gqa", dict(Hq=2, Hkv=2)),            # g = 1
+    ("small_gqa", dict(Hq=6, Hkv=3)),            # g = 2
+    ("small_gqa", dict(Hq=6, Hkv=2)),            # g = 3
+]
+
+
+def _ids(c):
+    return c[0] + "".join("-%s%s" % kv for kv in c[1].items())
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+def test_quantize_bit_exact(case):
+    w = _variant(case[0], **case[1])
+    inp = synth.host_inputs(w, seed=1)
+    pool, _ = gpu_quantize(w, inp)
+    ref, _, st = oracle_quantize(w, inp)
+    assert st == 0
+    got = pool.cpu().numpy()
+    assert got.shape == ref.shape
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, "first mismatching bytes at %s" % bad[:8]
+
+
+def test_quantize_running_bit_exact():
+    w = _variant("small_gqa", pages=np.array([5, 3, 9]))
+    inp = synth.host_inputs(w, seed=2)
+    pool, run = gpu_quantize(w, inp, running=True)
+    ref, (rs, rq, rc), st = oracle_quantize(w, inp, running=True)
+    assert st == 0
+    assert (pool.cpu().numpy() == ref).all()
+    assert (run[0].cpu().numpy().view(np.uint32) == rs.view(np.uint32)).all()
+    assert (run[1].cpu().numpy().view(np.uint32) == rq.view(np.uint32)).all()
+    assert (run[2].cpu().numpy() == rc).all()
+
+
+@pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_decode_attention(case, out_dtype):
+    w = _variant(case[0], **case[1])
+    inp = synth.host_inputs(w, seed=3)
+    pool, _ = gpu_quantize(w, inp)
+    got = gpu_decode(w, inp, pool, out_dtype)
+    ref, st = oracle_decode(w, inp, pool.cpu().numpy())
+    excess, rel = attn_error(got, ref, out_dtype)
+    assert excess <= 0, "max err %.3e of RMS" % rel
+
+
+def test_decode_split_invariance():
+    """Different split-K chunks give the same result up to fp32 rounding."""
+    w = _variant("small_gqa", pages=np.array([37, 1, 64]), tails=np.array([0, 5, 17]))
+    inp = synth.host_inputs(w, seed=4)
+    pool, _ = gpu_quantize(w, inp)
+    a = gpu_decode(w, inp, pool, pps=4)
+    b = gpu_decode(w, inp, pool, pps=64)
+    c = gpu_decode(w, inp, pool, pps=0)
+    scale = np.sqrt(np.mean(a ** 2))
+    assert np.abs(a - b).max() <= 1e-5 * scale and np.abs(a - c).max() <= 1e-5 * scale
+    ref, _ = oracle_decode(w, inp, pool.cpu().numpy())
+    assert attn_error(a, ref)[0] <= 0
+
+
+def test_decode_ragged_and_empty():
+    """Sequences with only a tail, only pages, nothing at all, and a full tail."""
+    w = _variant("small_gqa", B=5, pages=np.array([0, 3, 0, 6, 1]),
+                 tails=np.array([9, 0, 0, 32 - 1, 0]))
+    inp = synth.host_inputs(w, seed=5)
+    inp["tail_len"][3] = 31
+    pool, _ = gpu_quantize(w, inp)
+    import torch
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    got = gpu_decode(w, inp, pool, status=st)
+    ref, ost = oracle_decode(w, inp, pool.cpu().numpy())
+    assert ost == oracle.ST["EMPTY"] and int(st.item()) == oracle.ST["EMPTY"]
+    assert (got[2] == 0).all()
+    assert attn_error(got, ref)[0] <= 0
+
+
+def test_decode_bad_page_sets_status():
+    w = synth.workload("tiny")
+    inp = synth.host_inputs(w, seed=6)
+    pool, _ = gpu_quantize(w, inp)
+    inp["block_table"][0, 3] = 10 ** 6
+    import torch
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_decode(w, inp, pool, status=st)
+    assert int(st.item()) == oracle.ST["BAD_PAGE"]
+
+
+def test_quantize_range_status():
+    w = synth.workload("tiny")
+    inp = synth.host_inputs(w, seed=7)
+    inp["k"][5, 0, 9] = np.float32(70000.0).astype(np.float16).view(np.uint16)  # fp16 inf
+    import torch
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    gpu_quantize(w, inp, status=st)
+    assert int(st.item()) == oracle.ST["NONFINITE"]
+
+
+def test_append_matches_oracle():
+    """Token-by-token append with running statistics and flushes, bit-exact
+    pages/state, then decode over the resulting cache."""
+    import torch
+    from mixed_precision_bit_gb300 import kitty
+    B, Hkv, Hq, n_hi, steps = 3, 2, 8, 32, 70
+    w = synth.Workload("append", B, Hq, Hkv, n_hi, synth.BF16, np.zeros(B, np.int64),
+                       np.array([30, 0, 12]))
+    cfg = cfg_for(w, rank_mode=1)
+    r = np.random.default_rng(9)
+    max_pages = 4
+    pool_pages = B * max_pages
+    blob, per_page = kitty.page_bytes(cfg)
+    # oracle state
+    o = dict(tail_k=np.zeros((B, Hkv, 32, 128), np.uint16), tail_len=np.array([30, 0, 12], np.int32),
+             run_sum=np.zeros((B, Hkv, 128), np.float32), run_count=np.zeros((B, Hkv), np.int32),
+             block_table=np.full((B, max_pages), -1, np.int32), num_pages=np.zeros(B, np.int32),
+             pool=np.zeros(pool_pages * per_page, np.uint8))
+    o["tail_v"] = o["tail_k"].copy()
+    o["run_sumsq"] = o["run_sum"].copy()
+    pre = synth.to_bits(r.standard_normal((B, Hkv, 32, 128)), synth.BF16)
+    o["tail_k"][:] = pre
+    o["tail_v"][:] = pre[::-1]
+    g = {k: (torch.from_numpy(v.view(np.int16) if v.dtype == np.uint16 else v).cuda())
+         for k, v in o.items()}
+    alloc = kitty.PageAllocator(pool_pages)
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    sig = np.exp(r.standard_normal(128))
+    for step in range(steps):
+        kn = synth.to_bits(r.standard_normal((B, Hkv, 128)) * sig, synth.BF16)
+        vn = synth.to_bits(r.standard_normal((B, Hkv, 128)), synth.BF16)
+        fl = np.full(B, -1, np.int32)
+        for b in range(B):
+            if o["tail_len"][b] + 1 == 32 and o["num_pages"][b] < max_pages:
+                fl[b] = alloc.alloc(1)[0]
+        s1 = oracle.append_token(Hkv, n_hi, 1, synth.BF16, kn, vn, o["tail_k"], o["tail_v"],
+                                 o["tail_len"], o["run_sum"], o["run_sumsq"], o["run_count"], fl,
+                                 o["block_table"], max_pages, o["num_pages"], o["pool"], pool_pages)
+        assert s1 == 0
+        kitty.append_token(cfg, dev16(kn), dev16(vn), g["tail_k"], g["tail_v"], g["tail_len"],
+                           g["run_sum"], g["run_sumsq"], g["run_count"], dev32(fl),
+                           g["block_table"], g["num_pages"], g["pool"], pool_pages, status=st)
+    torch.cuda.synchronize()
+    assert int(st.item()) == 0
+    for k, v in o.items():
+        gv = g[k].cpu().numpy()
+        if v.dtype == np.uint16:
+            gv = gv.view(np.uint16)
+        assert (gv.view(np.uint8) == v.view(np.uint8)).all(), k
+    assert (o["num_pages"] > 0).all()
+    inp = dict(q=synth.to_bits(r.standard_normal((B, Hq, 128)), synth.BF16), pool_pages=pool_pages,
+               block_table=o["block_table"], num_pages=o["num_pages"], tail_k=o["tail_k"],
+               tail_v=o["tail_v"], tail_len=o["tail_len"])
+    got = gpu_decode(w, inp, g["pool"])
+    ref, _ = oracle_decode(w, inp, o["pool"])
+    assert attn_error(got, ref)[0] <= 0

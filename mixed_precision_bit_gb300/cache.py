@@ -1,0 +1,118 @@
+"""Paged Kitty KV cache state for a decode loop (the runtime around the kernels).
+
+Per layer: a pool of packed pages, a block table, per-sequence unquantized
+tails, running channel statistics and a host page allocator.  The host keeps a
+mirror of every tail length and page count, so it decides flushes (which
+sequences complete a 32-token page this step, and which physical page each one
+gets) without reading device memory; the device state is only ever changed by
+the library's kernels.  Paper: Abstract (page-centric layout, lightweight
+runtime pipeline); VeloxQuant-MLX docs, Decode phase.
+"""
+
+from __future__ import annotations
+
+import math
+
+import numpy as np
+import torch
+
+from . import kitty
+
+PAGE = 32
+D = 128
+
+
+class LayerCache:
+    def __init__(self, cfg: kitty.Config, B: int, max_pages: int, pool_pages: int,
+                 device="cuda"):
+        self.cfg, self.B, self.max_pages, self.pool_pages = cfg, B, max_pages, pool_pages
+        blob, per_page = kitty.page_bytes(cfg)
+        self.blob, self.per_page = blob, per_page
+        Hkv = cfg.num_kv_heads
+        dev = torch.device(device)
+        self.pool = torch.zeros(pool_pages * per_page, dtype=torch.uint8, device=dev)
+        self.block_table = torch.full((B, max_pages), -1, dtype=torch.int32, device=dev)
+        self.num_pages = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.tail_k = torch.zeros((B, Hkv, PAGE, D), dtype=torch.int16, device=dev)
+        self.tail_v = torch.zeros_like(self.tail_k)
+        self.tail_len = torch.zeros(B, dtype=torch.int32, device=dev)
+        running = cfg.rank_mode == kitty.RANK_RUNNING
+        self.run_sum = torch.zeros((B, Hkv, D), dtype=torch.float32, device=dev) if running else None
+        self.run_sumsq = torch.zeros_like(self.run_sum) if running else None
+        self.run_count = torch.zeros((B, Hkv), dtype=torch.int32, device=dev) if running else None
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.alloc = kitty.PageAllocator(pool_pages)
+        self.h_tail = np.zeros(B, np.int64)
+        self.h_pages = np.zeros(B, np.int64)
+        ws = kitty.decode_workspace_bytes(cfg, B, max_pages)
+        self.workspace = torch.empty(max(ws, 16) // 4, dtype=torch.float32, device=dev)
+
+    # -- prefill: n_pages[b] full pages and a tail of tails[b] tokens per sequence
+    def prefill(self, k_pages, v_pages, n_pages, k_tail=None, v_tail=None, tails=None,
+                page_order=None, stream=None):
+        """k_pages, v_pages: 16-bit tensors (int16 view) [sum(n_pages)*32, Hkv, D],
+        sequence-major; k_tail, v_tail: [B, Hkv, 32, D] with tails[b] valid rows.
+        page_order: optional permutation of the allocated ids (shuffled block table)."""
+        n_pages = np.asarray(n_pages, np.int64)
+        tails = np.zeros(self.B, np.int64) if tails is None else np.asarray(tails, np.int64)
+        tot = int(n_pages.sum())
+        dev = self.pool.device
+        ids = self.alloc.alloc(tot)
+        if page_order is not None:
+            ids = ids[np.asarray(page_order)]
+        bt = np.full((self.B, self.max_pages), -1, np.int32)
+        off = 0
+        for b in range(self.B):
+            bt[b, :n_pages[b]] = ids[off:off + n_pages[b]]
+            off += n_pages[b]
+        self.block_table.copy_(torch.from_numpy(bt))
+        self.num_pages.copy_(torch.from_numpy(n_pages.astype(np.int32)))
+        run = {}
+        if self.run_sum is not None:
+            seq = np.repeat(np.arange(self.B), n_pages).astype(np.int32)
+            run = dict(seq_of_page=torch.from_numpy(seq).to(dev), n_seqs=self.B,
+                       run_sum=self.run_sum, run_sumsq=self.run_sumsq, run_count=self.run_count)
+        if tot:
+            kitty.quantize_pages(self.cfg, k_pages, v_pages,
+                                 torch.from_numpy(ids.astype(np.int32)).to(dev), self.pool,
+                                 self.pool_pages, status=self.status, stream=stream, **run)
+        if k_tail is not None:
+            self.tail_k.copy_(k_tail)
+            self.tail_v.copy_(v_tail)
+        self.tail_len.copy_(torch.from_numpy(tails.astype(np.int32)))
+        self.h_tail[:] = tails
+        self.h_pages[:] = n_pages
+        return ids
+
+    def plan_flush(self) -> np.ndarray:
+        """Host decision for the next append: a fresh page id for each sequence whose
+        tail completes a page, -1 elsewhere; advances the host mirror."""
+        fl = np.full(self.B, -1, np.int32)
+        full = np.nonzero(self.h_tail + 1 == PAGE)[0]
+        full = full[self.h_pages[full] < self.max_pages]
+        if full.size:
+            fl[full] = self.alloc.alloc(full.size)
+        self.h_tail += 1
+        self.h_tail[full] = 0
+        self.h_pages[full] += 1
+        return fl
+
+    def append(self, k_new, v_new, flush_ids, stream=None):
+        kitty.append_token(self.cfg, k_new, v_new, self.tail_k, self.tail_v, self.tail_len,
+                           self.run_sum, self.run_sumsq, self.run_count, flush_ids,
+                           self.block_table, self.num_pages, self.pool, self.pool_pages,
+                           status=self.status, stream=stream)
+
+    def attend(self, q, out, sm_scale=None, stream=None):
+        sm = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+        kitty.decode_attention(self.cfg, q, self.pool, self.pool_pages, self.block_table,
+                               self.num_pages, self.tail_k, self.tail_v, self.tail_len, sm, out,
+                               workspace=self.workspace, status=self.status, stream=stream)
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes one decode call must move: packed pages + tails + Q + O + block
+        table entries (host mirror of the current lengths)."""
+        Hkv, Hq = self.cfg.num_kv_heads, self.cfg.num_q_heads
+        pages = int(self.h_pages.sum())
+        return (pages * Hkv * self.blob + int(self.h_tail.sum()) * Hkv * D * 2 * 2
+                + self.B * Hq * D * 2 * 2 + pages * 4)

@@ -225,3 +225,9 @@ def device_kv(w: Workload, b: int, seed: int, device, n_tok=None):
         hi = min(n, (s + 1) * w.drift) if w.drift else n
         z[lo:hi] *= sig
     return z.to(dt), vv.to(dt)
+
+
+def host_fast_normal(seed: int, shape) -> np.ndarray:
+    """N(0, 1) from numpy's seeded PCG64 (fast bulk draws for CPU timing samples,
+    where bit-reproducibility across the two paths is not needed)."""
+    return np.random.default_rng(seed).standard_normal(shape, dtype=np.float32)

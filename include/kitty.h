@@ -17,7 +17,8 @@
  *    checked on the host before anything is launched; on an error nothing is
  *    launched and no memory is touched.
  *  - Device pointers are raw CUDA device addresses owned by the caller (the
- *    library allocates no device memory and keeps no global state).  Work is
+ *    library allocates no device memory and keeps no global state, apart from
+ *    the fixed scratch array of kitty_decode_attention_noalloc).  Work is
  *    enqueued asynchronously on `stream` (a cudaStream_t; NULL = legacy default
  *    stream) and the call returns without synchronizing.
  *  - `d_status` (optional, may be NULL) is a caller-owned device int32.  Data
@@ -176,6 +177,31 @@ int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const void* pool
                            const int32_t* tail_len, float sm_scale, void* out, int32_t out_dtype,
                            void* workspace, size_t workspace_bytes, int32_t B, int32_t* d_status,
                            void* stream);
+
+/* Decode attention that allocates nothing and takes no workspace.  The paper has
+ * no counterpart: this entry point exists for callers that cannot allocate
+ * device memory while they run -- e.g. a serving process that reserved all of
+ * the GPU's memory for its page pool up front, or a host language runtime with
+ * no access to a CUDA allocator.  It computes exactly what
+ * kitty_decode_attention computes, with the split-K partials kept in a
+ * file-scope device array of KITTY_NOALLOC_SCRATCH_BYTES (8 MiB) that every
+ * GPU loading this library holds until the process exits.
+ *  - Returns KITTY_ERR_WORKSPACE, launching nothing, when this batch shape
+ *    needs more split-K scratch than that (kitty_decode_workspace_bytes tells).
+ *  - The first call on a device looks up the array's device address (once per
+ *    device, with that device current); make that first call before any stream
+ *    capture.
+ *  - All calls on a device share the one array and every call overwrites the
+ *    partials it reads, so nothing needs clearing between calls; calls whose
+ *    kernels overlap on the GPU (different streams, no ordering) race on it.
+ *  Arguments are those of kitty_decode_attention without the workspace. */
+#define KITTY_NOALLOC_SCRATCH_BYTES (8u << 20)
+int kitty_decode_attention_noalloc(const kitty_cfg* cfg, const void* q, const void* pool,
+                                   int32_t pool_pages, const int32_t* block_table,
+                                   int32_t max_pages, const int32_t* num_pages,
+                                   const void* tail_k, const void* tail_v,
+                                   const int32_t* tail_len, float sm_scale, void* out,
+                                   int32_t out_dtype, int32_t B, int32_t* d_status, void* stream);
 
 /* Launch shape that kitty_decode_attention uses for this batch shape: number of
  * splits per sequence and pages per split (for reporting and tests). */

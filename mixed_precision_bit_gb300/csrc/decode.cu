@@ -26,6 +26,7 @@
 #include "host_common.h"
 
 #include <cmath>
+#include <mutex>
 
 namespace kitty {
 namespace {
@@ -608,4 +609,55 @@ extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const
   if (sp > 1)
     combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p.ws, num_pages, max_pages, ch, sp, cfg->num_q_heads, out, out_dtype, d_status);
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+// Split-K partials in a fixed device array instead of a caller workspace.  Every
+// GPU that loads this library holds kNoAllocScratchBytes of it until exit.
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = size_t(8) << 20;  // 8 MiB
+static __device__ __align__(256) float g_noalloc_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void* g_scratch_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device, looked up once per
+// device (host code must not pass the symbol itself: it names a host stand-in).
+int scratch_on_current_device(void** out) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return KITTY_ERR_CUDA;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (g_scratch_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr)
+      return KITTY_ERR_CUDA;
+    g_scratch_ptr[dev] = p;
+  }
+  *out = g_scratch_ptr[dev];
+  return KITTY_OK;
+}
+
+}  // namespace
+
+extern "C" int kitty_decode_attention_noalloc(const kitty_cfg* cfg, const void* q, const void* pool,
+                                              int32_t pool_pages, const int32_t* block_table,
+                                              int32_t max_pages, const int32_t* num_pages,
+                                              const void* tail_k, const void* tail_v,
+                                              const int32_t* tail_len, float sm_scale, void* out,
+                                              int32_t out_dtype, int32_t B, int32_t* d_status,
+                                              void* stream) {
+  size_t need = 0;
+  int rc = kitty_decode_workspace_bytes(cfg, B, max_pages, &need);
+  if (rc != KITTY_OK) return rc;
+  if (need > kNoAllocScratchBytes) return KITTY_ERR_WORKSPACE;
+  void* scratch = nullptr;
+  if (need > 0) {
+    rc = scratch_on_current_device(&scratch);
+    if (rc != KITTY_OK) return rc;
+  }
+  return kitty_decode_attention(cfg, q, pool, pool_pages, block_table, max_pages, num_pages, tail_k,
+                                tail_v, tail_len, sm_scale, out, out_dtype, scratch,
+                                need > 0 ? kNoAllocScratchBytes : 0, B, d_status, stream);
 }

@@ -59,7 +59,9 @@ _lib = None
 EXPORTS = ("kitty_abi_version", "kitty_page_bytes", "kitty_avg_bits", "kitty_alloc_create",
            "kitty_alloc_pages", "kitty_free_pages", "kitty_alloc_free_count",
            "kitty_alloc_destroy", "kitty_quantize_pages", "kitty_append_token",
-           "kitty_decode_workspace_bytes", "kitty_decode_attention", "kitty_decode_plan")
+           "kitty_decode_workspace_bytes", "kitty_decode_attention", "kitty_decode_plan",
+           "kitty_decode_attention_noalloc")
+NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
 def lib_path() -> str:
@@ -89,6 +91,8 @@ def load():
             "kitty_decode_workspace_bytes": (ctypes.c_int, [C, i32, i32, ctypes.POINTER(sz)]),
             "kitty_decode_attention": (ctypes.c_int, [C, P, P, i32, P, i32, P, P, P, P,
                                                       ctypes.c_float, P, i32, P, sz, i32, P, P]),
+            "kitty_decode_attention_noalloc": (ctypes.c_int, [C, P, P, i32, P, i32, P, P, P, P,
+                                                              ctypes.c_float, P, i32, i32, P, P]),
             "kitty_decode_plan": (ctypes.c_int, [C, i32, i32, ctypes.POINTER(i32),
                                                  ctypes.POINTER(i32)]),
         }
@@ -216,3 +220,18 @@ def decode_attention(cfg: Config, q, pool, pool_pages: int, block_table, num_pag
         block_table.shape[1], _ptr(num_pages), _ptr(tail_k), _ptr(tail_v), _ptr(tail_len),
         float(sm_scale), _ptr(out), out_dtype, _ptr(workspace), ws_bytes, B, _ptr(status),
         _stream(stream)))
+
+
+def decode_attention_noalloc(cfg: Config, q, pool, pool_pages: int, block_table, num_pages,
+                             tail_k, tail_v, tail_len, sm_scale: float, out, status=None,
+                             stream=None, out_dtype=None):
+    """kitty_decode_attention without a workspace: the library keeps the split-K
+    partials in its own fixed device array (no allocation during the call)."""
+    import torch
+    B = num_pages.numel()
+    if out_dtype is None:
+        out_dtype = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}[out.dtype]
+    _chk("kitty_decode_attention_noalloc", load().kitty_decode_attention_noalloc(
+        ctypes.byref(cfg.c()), _ptr(q), _ptr(pool), pool_pages, _ptr(block_table),
+        block_table.shape[1], _ptr(num_pages), _ptr(tail_k), _ptr(tail_v), _ptr(tail_len),
+        float(sm_scale), _ptr(out), out_dtype, B, _ptr(status), _stream(stream)))

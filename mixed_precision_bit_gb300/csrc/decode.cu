@@ -11,10 +11,11 @@
 // with 1-D bulk copies (cp.async.bulk + mbarrier, 4 stages per warp), then
 // computes, for its g <= 4 query heads:
 //   scores  S^T[t][n] = sum_c code[t][c] * B[c][n] on the tensor cores
-//           (mma.m16n8k16, fp32 accumulate), B = q*S (per-channel Key step
-//           folded into the query) as an fp16 hi/lo pair in columns 0-3 / 4-7,
-//           plus the extra plane for the boosted channels (B = q*S/4 gathered
-//           through the channel list) and the q.M term as a one-row MMA;
+//           (mma.m16n8k16, fp32 accumulate) with B = q*S, the per-channel Key
+//           step folded into the query as an fp16 hi/lo pair (column 2h = hi,
+//           2h+1 = lo of head h), plus the extra plane of the boosted channels
+//           (B = q*S/4 gathered through the channel list) and the q.M term as
+//           a one-row MMA;
 //   softmax fp32 online (max, rescale, exp2) in registers;
 //   PV      O^T[c][n] = sum_t vcode[c][t] * P'[t][n] with P' = p*S_v per
 //           Value group as an fp16 hi/lo pair, plus the sum_t p*M_v term.
@@ -33,6 +34,7 @@ namespace {
 
 constexpr int kDWarps = 4;
 constexpr int kDStages = 4;
+constexpr int kDMinBlocks = 4;  // resident CTAs per SM the register budget is sized for
 constexpr int kDThreads = kDWarps * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of one barrier phase (~0.1-1 s)
 constexpr int kPartial = kD + 2;           // split partial: m, l, o[128]
@@ -58,13 +60,49 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
-// fp16 hi/lo split of q*S across lanes: lanes with lomask == 0 get fp16(q*S),
-// lanes with lomask == ~0 get fp16(q*S - fp16(q*S)) (the exact residual).
-__device__ __forceinline__ uint32_t hilo_mul(uint32_t q, uint32_t S, uint32_t lomask) {
-  const __half2 qh = bits_h2(q), Sh = bits_h2(S);
-  const uint32_t hi = h2_bits(__hmul2(qh, Sh));
-  const uint32_t negc = (hi ^ 0x80008000u) & lomask;
-  return h2_bits(__hfma2(qh, Sh, bits_h2(negc)));
+// Shared-memory loads from a 32-bit shared address plus a compile-time offset.
+template <int OFF>
+__device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
+  uint32_t v;
+  asm volatile("ld.shared.b32 %0, [%1+%2];" : "=r"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint32_t ld_s16(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1+%2];" : "=h"(v) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint2 ld_s64(uint32_t a) {
+  uint2 v;
+  asm volatile("ld.shared.v2.b32 {%0,%1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));
+  return v;
+}
+template <int OFF>
+__device__ __forceinline__ uint4 ld_s128(uint32_t a) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0,%1,%2,%3}, [%4+%5];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(a), "n"(OFF));
+  return v;
+}
+__device__ __forceinline__ uint16_t ld_s16r(uint32_t a) {
+  uint16_t v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(a));
+  return v;
+}
+__device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(bits_h2(a), bits_h2(b))); }
+__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
+  return h2_bits(__hfma2(bits_h2(a), bits_h2(b), bits_h2(c)));
+}
+
+// fp16 hi/lo split of q*S across the two columns of a head.  fneg is 0 on hi
+// lanes and -1 on lo lanes: hi lanes get fp16(q*S), lo lanes get the exact
+// residual fp16(q*S - fp16(q*S)).  Three FMA-pipe operations, no lane select.
+__device__ __forceinline__ uint32_t hilo_mul(uint32_t q, uint32_t S, uint32_t fneg) {
+  const uint32_t h = hmul2u(q, hmul2u(S, fneg));
+  return hfma2u(q, S, h);
 }
 
 __device__ __forceinline__ void store_out(void* out, int dt, size_t i, float v) {
@@ -73,168 +111,198 @@ __device__ __forceinline__ void store_out(void* out, int dt, size_t i, float v) 
   else static_cast<__half*>(out)[i] = __float2half_rn(v);
 }
 
-// Per-warp online-softmax state.  Thread (r = lane/4, qq = lane%4) holds heads
-// hA = 2*(qq&1), hB = hA+1; accumulator columns 2qq, 2qq+1 are the hi (qq<2) or
-// lo (qq>=2) parts of those heads.
+// Compile-time blob offsets for NX = n_hi/16 extra-plane k-steps.
+template <int NX>
+struct Off {
+  static constexpr int kx = 1024, ks = kx + 128 * NX, km = ks + 256, kch = km + 256;
+  static constexpr int vb = kch + 16 * NX, vs = vb + 1024, vm = vs + 256, bytes = vm + 256;
+};
+
+// Lane roles.  Thread (r = lane/4, qq = lane%4) owns head qq in the C
+// fragments (column 2qq = hi, 2qq+1 = lo) and, as a B-fragment lane, column
+// n = lane/4 = (head lane/8, part (lane/4)&1).
+struct Lane {
+  int lane, r, qq;
+  uint32_t fneg;  // fp16x2 0 (hi column) or -1 (lo column)
+  uint32_t fpos;  // fp16x2 0 (hi column) or +1 (lo column)
+  __device__ Lane() {
+    lane = threadIdx.x & 31;
+    r = lane >> 2;
+    qq = lane & 3;
+    const bool lo = (lane >> 2) & 1;
+    fneg = lo ? 0xBC00BC00u : 0u;
+    fpos = lo ? 0x3C003C00u : 0u;
+  }
+};
+
+// Per-warp online-softmax state of head qq.
 struct WarpState {
   float acc[8][4];  // O^T fragments, m-tile mc = channels 16mc..16mc+15
   float vm[4];      // sum_t p*M_v fragment (rows = Value groups)
-  float mA, mB;     // running max (log2 units), warp-uniform per head pair
-  float lA, lB;     // this thread's partial softmax denominators
+  float m;          // running max (log2 units), uniform over the lanes of a head
+  float l;          // this thread's partial softmax denominator
 };
 
-// Rescale the state when the running max of a head grows.
-__device__ __forceinline__ void update_max(WarpState& w, float pmA, float pmB) {
-  const float nA = fmaxf(w.mA, pmA), nB = fmaxf(w.mB, pmB);
-  if (__any_sync(0xFFFFFFFFu, nA > w.mA || nB > w.mB)) {
-    const float aA = ex2(w.mA - nA), aB = ex2(w.mB - nB);
+__device__ __forceinline__ void rescale(WarpState& w, float pm) {
+  const float nm = fmaxf(w.m, pm);
+  if (__any_sync(0xFFFFFFFFu, nm > w.m)) {
+    const float a = ex2(w.m - nm);
 #pragma unroll
-    for (int mc = 0; mc < 8; ++mc) {
-      w.acc[mc][0] *= aA; w.acc[mc][1] *= aB; w.acc[mc][2] *= aA; w.acc[mc][3] *= aB;
-    }
-    w.vm[0] *= aA; w.vm[1] *= aB; w.vm[2] *= aA; w.vm[3] *= aB;
-    w.lA *= aA;
-    w.lB *= aB;
-    w.mA = nA;
-    w.mB = nB;
+    for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w.acc[mc][i] *= a;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w.vm[i] *= a;
+    w.l *= a;
+    w.m = nm;
   }
 }
 
-// One staged (page, kv-head) blob: scores, online softmax, PV.
-//   qf[j][0..1]: this lane's B-fragment query pairs for k-step j (head (lane/4)%4)
-//   qs: query heads in fp16, [4][128] in shared memory
-__device__ __forceinline__ void compute_page(WarpState& w, const uint8_t* __restrict__ pg,
-                                             const uint32_t (&qf)[8][2], const __half* qs,
-                                             const BlobLayout& lay, const float (&kscale)[4],
-                                             float sm_log2) {
-  const int lane = threadIdx.x & 31, r = lane >> 2, qq = lane & 3;
-  const uint32_t lomask = lane >= 16 ? 0xFFFFFFFFu : 0u;
-  const __half* KS = reinterpret_cast<const __half*>(pg + lay.ks);
-  const __half* KM = reinterpret_cast<const __half*>(pg + lay.km);
+__device__ __forceinline__ void unpack_rows01(uint32_t x, uint32_t* a) {  // tau 0,1
+  const uint32_t x2 = x >> 8;
+  a[0] = x & 0x00030003u; a[1] = x & 0x000C000Cu; a[2] = x2 & 0x00030003u; a[3] = x2 & 0x000C000Cu;
+}
+__device__ __forceinline__ void unpack_rows23(uint32_t x, uint32_t* a) {  // tau 2,3
+  const uint32_t x2 = x >> 8;
+  a[0] = x & 0x00300030u; a[1] = x & 0x00C000C0u; a[2] = x2 & 0x00300030u; a[3] = x2 & 0x00C000C0u;
+}
 
-  // ---------------- scores
-  float cs[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-  float cm[4] = {0.f, 0.f, 0.f, 0.f};
-  const uint4 kb0 = *reinterpret_cast<const uint4*>(pg + lay.kbase + 32 * lane);
-  const uint4 kb1 = *reinterpret_cast<const uint4*>(pg + lay.kbase + 32 * lane + 16);
+// One staged (page, kv-head) blob: scores, online softmax, PV.
+//   pa: shared-space address of the staged blob
+//   qf[j][0..1]: this lane's B-fragment query pairs for k-step j (head lane/8)
+//   qxa: shared-space address of q/4 of head lane/8 (extra-plane gather)
+template <int NX>
+__device__ __forceinline__ void compute_page(WarpState& w, const uint32_t pa,
+                                             const uint32_t (&qf)[8][2], const uint32_t qxa,
+                                             const Lane& L, const float (&kscale)[4],
+                                             float sm_log2) {
+  using O = Off<NX>;
+  const int lane = L.lane, r = L.r, qq = L.qq;
+  const uint32_t a_lane = pa + 32 * lane;   // this lane's 32 bytes of each code plane
+  const uint32_t a_qq = pa + 4 * qq;        // this lane's fp16 pair in each 16-wide group
+
+  // ---------------- scores: base plane, q.M row, extra plane
+  // two accumulator sets (even / odd k-steps) halve the dependent MMA chains
+  float cs[2][2][4] = {};
+  float cm[2][4] = {};
+  const uint4 kb0 = ld_s128<0>(a_lane);
+  const uint4 kb1 = ld_s128<16>(a_lane);
   const uint32_t kw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    const int c0 = 16 * j + 2 * qq;
-    const uint32_t S0 = *reinterpret_cast<const uint32_t*>(KS + c0);
-    const uint32_t S1 = *reinterpret_cast<const uint32_t*>(KS + c0 + 8);
-    const uint32_t b0 = hilo_mul(qf[j][0], S0, lomask);
-    const uint32_t b1 = hilo_mul(qf[j][1], S1, lomask);
-    const uint32_t x = kw[j], x2 = x >> 8;
-    const uint32_t a0[4] = {x & 0x00030003u, x & 0x000C000Cu, x2 & 0x00030003u, x2 & 0x000C000Cu};
-    const uint32_t a1[4] = {x & 0x00300030u, x & 0x00C000C0u, x2 & 0x00300030u, x2 & 0x00C000C0u};
-    mma_f16(cs[0], a0, b0, b1);
-    mma_f16(cs[1], a1, b0, b1);
-    const uint32_t am[4] = {r == 0 ? *reinterpret_cast<const uint32_t*>(KM + c0) : 0u, 0u,
-                            r == 0 ? *reinterpret_cast<const uint32_t*>(KM + c0 + 8) : 0u, 0u};
-    mma_f16(cm, am, qf[j][0], qf[j][1]);
+    uint32_t S0, S1, M0, M1;
+    switch (j) {  // compile-time offsets (the loop is unrolled)
+#define KITTY_KS(J) case J: S0 = ld_s32<O::ks + 32 * J>(a_qq); S1 = ld_s32<O::ks + 32 * J + 16>(a_qq); \
+                            M0 = ld_s32<O::km + 32 * J>(a_qq); M1 = ld_s32<O::km + 32 * J + 16>(a_qq); break;
+      KITTY_KS(0) KITTY_KS(1) KITTY_KS(2) KITTY_KS(3) KITTY_KS(4) KITTY_KS(5) KITTY_KS(6) default: KITTY_KS(7)
+#undef KITTY_KS
+    }
+    const uint32_t b0 = hilo_mul(qf[j][0], S0, L.fneg);
+    const uint32_t b1 = hilo_mul(qf[j][1], S1, L.fneg);
+    uint32_t a[4];
+    unpack_rows01(kw[j], a);
+    mma_f16(cs[j & 1][0], a, b0, b1);
+    unpack_rows23(kw[j], a);
+    mma_f16(cs[j & 1][1], a, b0, b1);
+    // every row r < 8 carries the minima, so every lane reads beta of its head
+    const uint32_t am[4] = {M0, 0u, M1, 0u};
+    mma_f16(cm[j & 1], am, qf[j][0], qf[j][1]);
   }
-  // extra plane: low 2 bits of the boosted channels' 4-bit codes, step S/4
-  const int nx = lay.n_hi >> 4;
-  const uint8_t* kch = pg + lay.kch;
-  const uint32_t* xw = reinterpret_cast<const uint32_t*>(pg + lay.kextra) + lane * nx;
-  const __half* qh = qs + (r & 3) * kD;
-  const __half2 quarter = __float2half2_rn(0.25f);
-  for (int js = 0; js < nx; ++js) {
-    const int j0 = 16 * js + 2 * qq;
-    const int ch0 = kch[j0] & 127, ch1 = kch[j0 + 1] & 127;
-    const int ch2 = kch[j0 + 8] & 127, ch3 = kch[j0 + 9] & 127;
-    const __half2 q01 = __halves2half2(qh[ch0], qh[ch1]);
-    const __half2 q23 = __halves2half2(qh[ch2], qh[ch3]);
-    const __half2 s01 = __hmul2(__halves2half2(KS[ch0], KS[ch1]), quarter);
-    const __half2 s23 = __hmul2(__halves2half2(KS[ch2], KS[ch3]), quarter);
-    const uint32_t b0 = hilo_mul(h2_bits(q01), h2_bits(s01), lomask);
-    const uint32_t b1 = hilo_mul(h2_bits(q23), h2_bits(s23), lomask);
-    const uint32_t x = xw[js], x2 = x >> 8;
-    const uint32_t a0[4] = {x & 0x00030003u, x & 0x000C000Cu, x2 & 0x00030003u, x2 & 0x000C000Cu};
-    const uint32_t a1[4] = {x & 0x00300030u, x & 0x00C000C0u, x2 & 0x00300030u, x2 & 0x00C000C0u};
-    mma_f16(cs[0], a0, b0, b1);
-    mma_f16(cs[1], a1, b0, b1);
+  if (NX > 0) {
+    const uint32_t a_id = pa + 2 * qq;
+    const uint32_t a_x = pa + 4 * NX * lane;
+#pragma unroll
+    for (int js = 0; js < NX; ++js) {
+      uint32_t i01, i23, x;
+      switch (js) {
+#define KITTY_KX(J) case J: i01 = ld_s16<O::kch + 16 * J>(a_id); i23 = ld_s16<O::kch + 16 * J + 8>(a_id); \
+                            x = ld_s32<O::kx + 4 * J>(a_x); break;
+        KITTY_KX(0) KITTY_KX(1) KITTY_KX(2) KITTY_KX(3) KITTY_KX(4) KITTY_KX(5) KITTY_KX(6) default: KITTY_KX(7)
+#undef KITTY_KX
+      }
+      const uint32_t c0 = 2 * (i01 & 127), c1 = 2 * ((i01 >> 8) & 127);
+      const uint32_t c2 = 2 * (i23 & 127), c3 = 2 * ((i23 >> 8) & 127);
+      const uint32_t q01 = ld_s16r(qxa + c0) | ((uint32_t)ld_s16r(qxa + c1) << 16);
+      const uint32_t q23 = ld_s16r(qxa + c2) | ((uint32_t)ld_s16r(qxa + c3) << 16);
+      const uint32_t s01 = ld_s16r(pa + O::ks + c0) | ((uint32_t)ld_s16r(pa + O::ks + c1) << 16);
+      const uint32_t s23 = ld_s16r(pa + O::ks + c2) | ((uint32_t)ld_s16r(pa + O::ks + c3) << 16);
+      const uint32_t b0 = hilo_mul(q01, s01, L.fneg);
+      const uint32_t b1 = hilo_mul(q23, s23, L.fneg);
+      uint32_t a[4];
+      unpack_rows01(x, a);
+      mma_f16(cs[js & 1][0], a, b0, b1);
+      unpack_rows23(x, a);
+      mma_f16(cs[js & 1][1], a, b0, b1);
+    }
   }
-  // combine hi/lo columns (lane ^ 2 holds the other half), add q.M, scale
-  const float bA = __shfl_sync(0xFFFFFFFFu, cm[0], qq) * sm_log2;
-  const float bB = __shfl_sync(0xFFFFFFFFu, cm[1], qq) * sm_log2;
-  float s[2][4];
+
+  // ---------------- online softmax (head qq; hi + lo columns are this lane's pair)
+  const float beta = (cm[0][0] + cm[1][0]) * sm_log2;
+  float s[4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float v = cs[mt][i] + __shfl_xor_sync(0xFFFFFFFFu, cs[mt][i], 2);
-      s[mt][i] = fmaf(v, kscale[2 * mt + (i >> 1)], (i & 1) ? bB : bA);
-    }
-  float pmA = fmaxf(fmaxf(s[0][0], s[0][2]), fmaxf(s[1][0], s[1][2]));
-  float pmB = fmaxf(fmaxf(s[0][1], s[0][3]), fmaxf(s[1][1], s[1][3]));
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    pmA = fmaxf(pmA, __shfl_xor_sync(0xFFFFFFFFu, pmA, off));
-    pmB = fmaxf(pmB, __shfl_xor_sync(0xFFFFFFFFu, pmB, off));
-  }
-  update_max(w, pmA, pmB);
-
-  // ---------------- probabilities, hi/lo split, transpose to B fragments
-  const bool lo_pre = qq >= 2;
+    for (int rh = 0; rh < 2; ++rh)
+      s[2 * mt + rh] = fmaf((cs[0][mt][2 * rh] + cs[1][mt][2 * rh]) + (cs[0][mt][2 * rh + 1] + cs[1][mt][2 * rh + 1]),
+                            kscale[2 * mt + rh], beta);
+  float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
+  rescale(w, pm);
   uint32_t T[4];
 #pragma unroll
-  for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-    for (int rh = 0; rh < 2; ++rh) {
-      const float pA = ex2(s[mt][2 * rh] - w.mA);
-      const float pB = ex2(s[mt][2 * rh + 1] - w.mB);
-      w.lA += pA;
-      w.lB += pB;
-      const float tA = __uint_as_float(__float_as_uint(pA) & 0xFFFFE000u);
-      const float tB = __uint_as_float(__float_as_uint(pB) & 0xFFFFE000u);
-      const __half2 pk = __floats2half2_rn(lo_pre ? pA - tA : tA, lo_pre ? pB - tB : tB);
-      T[2 * mt + rh] = movmatrix_t(h2_bits(pk));
-    }
-  // lanes 0-15 hold p_hi (columns 0-3), lanes 16-31 p_lo (columns 4-7)
-
-  // ---------------- Value min term: rows = groups, k = tokens
-  const __half* VS = reinterpret_cast<const __half*>(pg + lay.vs);
-  const __half* VMv = reinterpret_cast<const __half*>(pg + lay.vm);
-#pragma unroll
-  for (int kt = 0; kt < 2; ++kt) {
-    const int t0 = 16 * kt + 2 * qq;
-    const uint32_t am[4] = {r < 4 ? *reinterpret_cast<const uint32_t*>(VMv + r * kPage + t0) : 0u, 0u,
-                            r < 4 ? *reinterpret_cast<const uint32_t*>(VMv + r * kPage + t0 + 8) : 0u, 0u};
-    mma_f16(w.vm, am, T[2 * kt], T[2 * kt + 1]);
+  for (int i = 0; i < 4; ++i) {
+    const float p = ex2(s[i] - w.m);
+    w.l += p;
+    const float t = __uint_as_float(__float_as_uint(p) & 0xFFFFE000u);  // 11 significant bits
+    T[i] = movmatrix_t(h2_bits(__floats2half2_rn(t, p - t)));          // (hi, lo) -> B columns
   }
 
-  // ---------------- PV with the Value step folded into P per group
-  uint32_t ph[4], pl[4];
+  // ---------------- Value minima: rows = groups (r & 3), k = tokens
+  {
+    const uint32_t a_vm = pa + 64 * (r & 3) + 4 * qq;
+    const uint32_t am0[4] = {ld_s32<O::vm>(a_vm), 0u, ld_s32<O::vm + 16>(a_vm), 0u};
+    mma_f16(w.vm, am0, T[0], T[1]);
+    const uint32_t am1[4] = {ld_s32<O::vm + 32>(a_vm), 0u, ld_s32<O::vm + 48>(a_vm), 0u};
+    mma_f16(w.vm, am1, T[2], T[3]);
+  }
+
+  // ---------------- PV with the Value step folded into P per group (hi/lo)
+  uint32_t ph[4], pl[4], phf[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    ph[i] = __shfl_sync(0xFFFFFFFFu, T[i], lane & 15);
-    pl[i] = T[i] & lomask;
+    ph[i] = __shfl_sync(0xFFFFFFFFu, T[i], lane & ~4);  // p_hi of this column's head
+    pl[i] = hmul2u(T[i], L.fpos);                        // p_lo on lo lanes, 0 on hi lanes
+    phf[i] = hmul2u(ph[i], L.fneg);                      // -p_hi on lo lanes, 0 on hi lanes
   }
-  const uint32_t* vw = reinterpret_cast<const uint32_t*>(pg + lay.vbase + 32 * lane);
 #pragma unroll
   for (int G = 0; G < 4; ++G) {
-    const uint2 vv = *reinterpret_cast<const uint2*>(vw + 2 * G);
-    const uint32_t vwords[2] = {vv.x, vv.y};
+    uint2 vv;
+    uint32_t S[4];
+    switch (G) {
+#define KITTY_VG(J) case J: vv = ld_s64<O::vb + 8 * J>(a_lane); \
+                            S[0] = ld_s32<O::vs + 64 * J>(a_qq); S[1] = ld_s32<O::vs + 64 * J + 16>(a_qq); \
+                            S[2] = ld_s32<O::vs + 64 * J + 32>(a_qq); S[3] = ld_s32<O::vs + 64 * J + 48>(a_qq); break;
+      KITTY_VG(0) KITTY_VG(1) KITTY_VG(2) default: KITTY_VG(3)
+#undef KITTY_VG
+    }
 #pragma unroll
     for (int kt = 0; kt < 2; ++kt) {
       uint32_t bg[2];
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
-        const int t0 = 16 * kt + 8 * k + 2 * qq;
-        const __half2 S = bits_h2(*reinterpret_cast<const uint32_t*>(VS + G * kPage + t0));
-        const __half2 a = bits_h2(ph[2 * kt + k]);
-        const uint32_t h = h2_bits(__hmul2(a, S));
-        const uint32_t negc = (h ^ 0x80008000u) & lomask;
-        const __half2 rr = __hfma2(a, S, bits_h2(negc));
-        bg[k] = h2_bits(__hfma2(bits_h2(pl[2 * kt + k]), S, rr));
+        const int i = 2 * kt + k;
+        const uint32_t h = hmul2u(phf[i], S[i]);    // lo: fp16(-p_hi*S); hi: 0
+        const uint32_t rr = hfma2u(ph[i], S[i], h);  // hi: fp16(p_hi*S); lo: exact residual
+        bg[k] = hfma2u(pl[i], S[i], rr);            // lo: + p_lo*S
       }
-      const uint32_t x = vwords[kt], x2 = x >> 8;
-      const uint32_t ae[4] = {x & 0x00030003u, x & 0x000C000Cu, x2 & 0x00030003u, x2 & 0x000C000Cu};
-      const uint32_t ao[4] = {x & 0x00300030u, x & 0x00C000C0u, x2 & 0x00300030u, x2 & 0x00C000C0u};
-      mma_f16(w.acc[2 * G], ae, bg[0], bg[1]);
-      mma_f16(w.acc[2 * G + 1], ao, bg[0], bg[1]);
+      const uint32_t x = kt ? vv.y : vv.x;
+      uint32_t a[4];
+      unpack_rows01(x, a);
+      mma_f16(w.acc[2 * G], a, bg[0], bg[1]);
+      unpack_rows23(x, a);
+      mma_f16(w.acc[2 * G + 1], a, bg[0], bg[1]);
     }
   }
 }
@@ -244,8 +312,8 @@ __device__ __forceinline__ void compute_page(WarpState& w, const uint8_t* __rest
 // the same per-row power of two as the paged codes.
 template <int DT>
 __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* qs, int b, int kvh,
-                            int tl, int wid) {
-  const int lane = threadIdx.x & 31, r = lane >> 2, qq = lane & 3;
+                            int tl, int wid, const Lane& L) {
+  const int lane = L.lane, r = L.r, qq = L.qq;
   const size_t base = ((size_t)b * p.Hkv + kvh) * kPage * kD;
   float qv[4][4];
 #pragma unroll
@@ -265,32 +333,29 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
 #pragma unroll
       for (int off = 16; off >= 1; off >>= 1) d[h] += __shfl_xor_sync(0xFFFFFFFFu, d[h], off);
     }
-    const int hA = 2 * (qq & 1);
-    const float sA = (hA == 0 ? d[0] : d[2]) * p.sm_log2;
-    const float sB = (hA == 0 ? d[1] : d[3]) * p.sm_log2;
-    update_max(w, sA, sB);
-    const float pA = ex2(sA - w.mA), pB = ex2(sB - w.mB);
-    if (r == 0) { w.lA += pA; w.lB += pB; }
-    if (qq < 2) {
+    const float sc = (qq == 0 ? d[0] : qq == 1 ? d[1] : qq == 2 ? d[2] : d[3]) * p.sm_log2;
+    rescale(w, sc);
+    const float pr = ex2(sc - w.m);
+    if (r == 0) w.l += pr;
 #pragma unroll
-      for (int mc = 0; mc < 8; ++mc)
+    for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
-        for (int rh = 0; rh < 2; ++rh) {
-          const int c = 16 * mc + 8 * rh + r;
-          const float sc = __uint_as_float((uint32_t)(127 - 24 + 2 * (2 * (mc & 1) + rh)) << 23);
-          const float v = load16<DT>(vr + c) * sc;
-          w.acc[mc][2 * rh] += pA * v;
-          w.acc[mc][2 * rh + 1] += pB * v;
-        }
-    }
+      for (int rh = 0; rh < 2; ++rh) {
+        const int c = 16 * mc + 8 * rh + r;
+        const float rs = __uint_as_float((uint32_t)(127 - 24 + 2 * (2 * (mc & 1) + rh)) << 23);
+        w.acc[mc][2 * rh] += pr * (load16<DT>(vr + c) * rs);
+      }
   }
 }
 
-template <int DT>
-__global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams p) {
+template <int DT, int NX>
+__global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
   const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, r = lane >> 2, qq = lane & 3;
+  const int tid = threadIdx.x, wid = tid >> 5;
+  const Lane L;
+  const int lane = L.lane, r = L.r, qq = L.qq;
+  constexpr int kBlob = Off<NX>::bytes;
   int np = p.num_pages[b];
   int tl = p.tail_len != nullptr ? p.tail_len[b] : 0;
   if (np < 0 || np > p.max_pages || tl < 0 || tl > kPage || (tl > 0 && p.tail_k == nullptr)) {
@@ -301,16 +366,19 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
   const int n_act = max(1, (np + p.chunk - 1) / p.chunk);
   if (s >= n_act) return;
   const int pbeg = s * p.chunk, pend = min(np, pbeg + p.chunk);
-  const BlobLayout lay(p.n_hi);
 
   uint8_t* stages = dsm;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + kDWarps * kDStages * p.blob);
-  __half* qs = reinterpret_cast<__half*>(bars + kDWarps * kDStages);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + kDWarps * kDStages * kBlob);
+  __half* qs = reinterpret_cast<__half*>(bars + kDWarps * kDStages);  // q      [4][128]
+  __half* qs4 = qs + 4 * kD;                                          // q / 4  [4][128]
+
   for (int i = tid; i < 4 * kD; i += kDThreads) {
     const int h = i >> 7, c = i & (kD - 1);
     float v = 0.f;
     if (h < p.g) v = load16<DT>(p.q + ((size_t)b * p.Hq + (size_t)kvh * p.g + h) * kD + c);
-    qs[i] = __float2half_rn(v);
+    const __half hv = __float2half_rn(v);
+    qs[i] = hv;
+    qs4[i] = __hmul(hv, __float2half_rn(0.25f));
   }
   if (lane == 0) {
     for (int st = 0; st < kDStages; ++st) mbar_init(&bars[wid * kDStages + st], 1);
@@ -320,13 +388,14 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
 
   uint32_t qf[8][2];
   {
-    const __half* qh = qs + (r & 3) * kD;
+    const __half* qh = qs + (lane >> 3) * kD;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
       qf[j][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * j + 2 * qq);
       qf[j][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * j + 2 * qq + 8);
     }
   }
+  const uint32_t qxa = smem_u32(qs4 + (lane >> 3) * kD);
   float kscale[4];
 #pragma unroll
   for (int tau = 0; tau < 4; ++tau)
@@ -339,17 +408,17 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
     for (int i = 0; i < 4; ++i) w.acc[mc][i] = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) w.vm[i] = 0.f;
-  w.mA = w.mB = -INFINITY;
-  w.lA = w.lB = 0.f;
+  w.m = -INFINITY;
+  w.l = 0.f;
 
   // ---- this warp's pages: pbeg + wid + kDWarps*i, i < npw
   const int first = pbeg + wid;
   const int npw = pend > first ? (pend - first + kDWarps - 1) / kDWarps : 0;
-  uint8_t* wst = stages + (size_t)wid * kDStages * p.blob;
+  uint8_t* wst = stages + (size_t)wid * kDStages * kBlob;
   uint64_t* wbar = bars + wid * kDStages;
   const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
-  const size_t head_off = (size_t)kvh * p.blob;
-  const size_t page_stride = (size_t)p.Hkv * p.blob;
+  const uint8_t* head_base = p.pool + (size_t)kvh * kBlob;
+  const size_t page_stride = (size_t)p.Hkv * kBlob;
   int bt_cache = -1, bt_base = -64;
   uint32_t valid_mask = 0;  // bit st: stage st holds a valid page
   auto issue = [&](int i) {
@@ -362,9 +431,9 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
     const bool ok = pid >= 0 && pid < p.pool_pages;
     if (lane == 0) {
       if (ok) {
-        mbar_arrive_expect_tx(&wbar[st], (uint32_t)p.blob);
-        bulk_g2s(wst + (size_t)st * p.blob, p.pool + (size_t)pid * page_stride + head_off,
-                 (uint32_t)p.blob, &wbar[st]);
+        mbar_arrive_expect_tx(&wbar[st], (uint32_t)kBlob);
+        bulk_g2s(wst + (size_t)st * kBlob, head_base + (size_t)pid * page_stride, (uint32_t)kBlob,
+                 &wbar[st]);
       } else {
         set_status(p.d_status, KITTY_ST_BAD_PAGE);
         mbar_arrive(&wbar[st]);
@@ -377,9 +446,15 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
   for (int i = 0; i < npw; ++i) {
     const int st = i % kDStages;
     const uint32_t par = (uint32_t)(i / kDStages) & 1u;
-    int ok = 0;
-    if (lane == 0) ok = mbar_wait_bounded(&wbar[st], par, kWaitLimit) ? 1 : 0;
-    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+    // every lane observes the phase completion itself (acquire of the copied
+    // bytes); the exit is warp-uniform and the wait is bounded
+    bool done = false;
+    for (uint32_t it = 0;; ++it) {
+      done = done || mbar_test(&wbar[st], par);
+      if (__all_sync(0xFFFFFFFFu, done) || it >= kWaitLimit) break;
+      if (it > 64) __nanosleep(32);
+    }
+    const bool ok = __all_sync(0xFFFFFFFFu, done);
     if (!ok) {
       // give up: report, then wait (bounded) for every copy still in flight
       if (lane == 0) {
@@ -391,27 +466,22 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
       break;
     }
     if (valid_mask & (1u << st))
-      compute_page(w, wst + (size_t)st * p.blob, qf, qs, lay, kscale, p.sm_log2);
+      compute_page<NX>(w, smem_u32(wst) + st * kBlob, qf, qxa, L, kscale, p.sm_log2);
     __syncwarp();
     if (i + kDStages < npw) issue(i + kDStages);
   }
-  if (s == 0 && tl > 0) {
-    if (p.in_dtype == KITTY_BF16) tail_tokens<KITTY_BF16>(w, p, qs, b, kvh, tl, wid);
-    else tail_tokens<KITTY_F16>(w, p, qs, b, kvh, tl, wid);
-  }
+  if (s == 0 && tl > 0) tail_tokens<DT>(w, p, qs, b, kvh, tl, wid, L);
 
   // ---- merge the 4 warps: per-warp (m, l, O) to shared memory, then per channel
-#pragma unroll
-  for (int off = 4; off < 32; off <<= 1) {
-    w.lA += __shfl_xor_sync(0xFFFFFFFFu, w.lA, off);
-    w.lB += __shfl_xor_sync(0xFFFFFFFFu, w.lB, off);
-  }
+  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 4);
+  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 8);
+  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 16);
   __syncthreads();
   constexpr int kMergeFloats = kD * 8 + 4 * 8 + 8;
   float* mw = reinterpret_cast<float*>(dsm) + wid * kMergeFloats;
-  float* Ow = mw;               // [128][8]
-  float* VMw = mw + kD * 8;     // [4][8]
-  float* MLw = VMw + 4 * 8;     // m[4], l[4]
+  float* Ow = mw;            // [128][8]: column 2h = hi, 2h+1 = lo part of head h
+  float* VMw = mw + kD * 8;  // [4][8]
+  float* MLw = VMw + 4 * 8;  // m[4], l[4]
 #pragma unroll
   for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
@@ -425,11 +495,9 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
     VMw[r * 8 + 2 * qq] = w.vm[0];
     VMw[r * 8 + 2 * qq + 1] = w.vm[1];
   }
-  if (r == 0 && qq < 2) {
-    MLw[2 * qq] = w.mA;
-    MLw[2 * qq + 1] = w.mB;
-    MLw[4 + 2 * qq] = w.lA;
-    MLw[4 + 2 * qq + 1] = w.lB;
+  if (r == 0) {
+    MLw[qq] = w.m;
+    MLw[4 + qq] = w.l;
   }
   __syncthreads();
   const int c = tid;
@@ -439,27 +507,27 @@ __global__ void __launch_bounds__(kDThreads, 4) decode_kernel(const DecodeParams
     float ms = -INFINITY;
 #pragma unroll
     for (int ww = 0; ww < kDWarps; ++ww) ms = fmaxf(ms, m0[ww * kMergeFloats + kD * 8 + 32 + h]);
-    float L = 0.f, O = 0.f;
+    float Lsum = 0.f, Osum = 0.f;
     if (ms != -INFINITY) {
 #pragma unroll
       for (int ww = 0; ww < kDWarps; ++ww) {
         const float* base = m0 + ww * kMergeFloats;
         const float mwv = base[kD * 8 + 32 + h];
         const float e = mwv == -INFINITY ? 0.f : ex2(mwv - ms);
-        L += base[kD * 8 + 32 + 4 + h] * e;
-        const float o = base[c * 8 + h] + base[c * 8 + h + 4] + base[kD * 8 + G * 8 + h] +
-                        base[kD * 8 + G * 8 + h + 4];
-        O += o * e;
+        Lsum += base[kD * 8 + 32 + 4 + h] * e;
+        const float o = base[c * 8 + 2 * h] + base[c * 8 + 2 * h + 1] + base[kD * 8 + G * 8 + 2 * h] +
+                        base[kD * 8 + G * 8 + 2 * h + 1];
+        Osum += o * e;
       }
     }
     const int hq = kvh * p.g + h;
     if (p.splits == 1) {
-      store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c, L > 0.f ? O / L : 0.f);
-      if (c == 0 && !(L > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
+      store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c, Lsum > 0.f ? Osum / Lsum : 0.f);
+      if (c == 0 && !(Lsum > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
     } else {
       float* part = p.ws + (((size_t)b * p.Hq + hq) * p.splits + s) * kPartial;
-      part[2 + c] = O;
-      if (c == 0) { part[0] = ms; part[1] = L; }
+      part[2 + c] = Osum;
+      if (c == 0) { part[0] = ms; part[1] = Lsum; }
     }
   }
 }
@@ -487,6 +555,30 @@ __global__ void __launch_bounds__(kD) combine_kernel(const float* __restrict__ w
   }
   store_out(out, out_dtype, (size_t)bh * kD + c, L > 0.f ? O / L : 0.f);
   if (c == 0 && !(L > 0.f)) set_status(d_status, KITTY_ST_EMPTY);
+}
+
+template <int DT, int NX>
+cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
+  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, NX>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  decode_kernel<DT, NX><<<grid, kDThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_decode_nx(int nx, dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
+  switch (nx) {
+    case 0: return launch_decode<DT, 0>(grid, smem, s, p);
+    case 1: return launch_decode<DT, 1>(grid, smem, s, p);
+    case 2: return launch_decode<DT, 2>(grid, smem, s, p);
+    case 3: return launch_decode<DT, 3>(grid, smem, s, p);
+    case 4: return launch_decode<DT, 4>(grid, smem, s, p);
+    case 5: return launch_decode<DT, 5>(grid, smem, s, p);
+    case 6: return launch_decode<DT, 6>(grid, smem, s, p);
+    case 7: return launch_decode<DT, 7>(grid, smem, s, p);
+    default: return launch_decode<DT, 8>(grid, smem, s, p);
+  }
 }
 
 }  // namespace
@@ -522,7 +614,7 @@ void plan(const kitty_cfg* cfg, int B, int max_pages, int* splits, int* chunk) {
 }
 
 size_t decode_smem(int blob) {
-  return (size_t)kDWarps * kDStages * blob + kDWarps * kDStages * sizeof(uint64_t) + 4 * kD * 2;
+  return (size_t)kDWarps * kDStages * blob + kDWarps * kDStages * sizeof(uint64_t) + 2 * 4 * kD * 2;
 }
 
 }  // namespace
@@ -599,13 +691,10 @@ extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const
   const size_t smem = decode_smem(p.blob);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid(sp, cfg->num_kv_heads, B);
-  if (cfg->in_dtype == KITTY_BF16) {
-    if (cudaFuncSetAttribute(decode_kernel<KITTY_BF16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return KITTY_ERR_CUDA;
-    decode_kernel<KITTY_BF16><<<grid, kDThreads, smem, s>>>(p);
-  } else {
-    if (cudaFuncSetAttribute(decode_kernel<KITTY_F16>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess) return KITTY_ERR_CUDA;
-    decode_kernel<KITTY_F16><<<grid, kDThreads, smem, s>>>(p);
-  }
+  const cudaError_t e = cfg->in_dtype == KITTY_BF16
+                            ? launch_decode_nx<KITTY_BF16>(cfg->n_hi / 16, grid, smem, s, p)
+                            : launch_decode_nx<KITTY_F16>(cfg->n_hi / 16, grid, smem, s, p);
+  if (e != cudaSuccess) return KITTY_ERR_CUDA;
   if (sp > 1)
     combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p.ws, num_pages, max_pages, ch, sp, cfg->num_q_heads, out, out_dtype, d_status);
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;

@@ -241,11 +241,7 @@ def run_kitty(args, rank, world, local_rank):
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        t = torch.tensor([ms], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = dist_max(t0.elapsed_time(t1), world)
     dec_ms = [ev[s][l][0].elapsed_time(ev[s][l][1]) for s in range(K) for l in range(L)]
     dec_bytes = [algo[W + s][l] for s in range(K) for l in range(L)]
     status = [int(lc.status.item()) for lc in layers]
@@ -275,11 +271,7 @@ def run_kitty(args, rank, world, local_rank):
             lc.attend(dq[l], out[l])
         hout.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
-    e2e_s = time.perf_counter() - w0
-    if world > 1:
-        t = torch.tensor([e2e_s], device="cuda")
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = dist_max(time.perf_counter() - w0, world)
     status = [int(lc.status.item()) for lc in layers]
     if any(status):
         raise RuntimeError("device status codes after e2e %s" % status)
@@ -373,6 +365,46 @@ def oracle_tokens_per_s(sample, steps, layers):
     return sample.S / (per * layers), per
 
 
+# ------------------------------------------------------------------ profiled traffic
+def profiled_traffic_ratio():
+    """DRAM traffic / algorithmic bytes of one decode launch, from the committed ncu
+    summary, if that capture was taken on the current kernel source; else None."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "decode_kernel_budget_layer.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    vals = dict(re.findall(r"^\s*(\w+) = (\w+)\s*$", text, re.M))
+    srcs = [os.path.join(ROOT, "mixed_precision_bit_gb300", "csrc", f)
+            for f in ("decode.cu", "kitty_common.cuh")]
+    sha = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
+    if vals.get("kernel_source_sha256_16") != sha:
+        return None
+    return float(vals["traffic_bytes_per_launch"]) / float(vals["algorithmic_bytes_per_launch"])
+
+
+# ------------------------------------------------------------------ multi-rank helpers
+def dist_max(x: float, world: int) -> float:
+    """Max of a per-rank scalar over all ranks (replicas are timed independently;
+    the slowest rank defines the job time)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, seqs_per_rank: int, steps: int, max_seconds: float) -> float:
+    """Whole-job decode tokens/s for replicas: every rank decodes seqs_per_rank
+    sequences per step, the job takes the slowest rank's time."""
+    return world * seqs_per_rank * steps / max_seconds
+
+
 # ------------------------------------------------------------------ JSON
 def config_block(spec, extra=None):
     c = {"workload": spec["name"],
@@ -437,11 +469,12 @@ def main():
     r = run_kitty(args, rank, world, local_rank)
     spec = r["spec"]
     B, L, K = spec["B"], spec["layers"], r["K"]
-    value = world * B * K / (r["ms"] / 1e3)
+    value = job_throughput(world, B, K, r["ms"] / 1e3)
     dec_s = statistics.mean(r["dec_ms"]) / 1e3
     dec_bytes = statistics.mean(r["dec_bytes"])
     achieved = dec_bytes / dec_s / 1e9
     hbm_peak = float(peaks["hbm_gbs"])
+    traffic_ratio = profiled_traffic_ratio()
     step_bytes = sum(r["dec_bytes"]) / K
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
@@ -456,14 +489,16 @@ def main():
                     "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
                     "pct_of_measured": 100.0 * achieved / hbm_peak},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
-                     "frac": achieved / hbm_peak, "traffic": None,
+                     "frac": achieved / hbm_peak,
+                     "traffic": (traffic_ratio * dec_bytes
+                                 if traffic_ratio is not None and spec["name"] == "budget" else None),
                      "kernel": "kitty_decode_attention (decode_kernel + split combine)",
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src,
                      "algorithmic_bytes_per_launch": dec_bytes,
                      "avg_launch_ms": dec_s * 1e3},
         "gpu_launches": r["gpu_launches"],
         "clocks": r["clocks"],
-        "e2e": {"value": world * B * r["E"] / r["e2e_s"], "unit": "tokens/s",
+        "e2e": {"value": job_throughput(world, B, r["E"], r["e2e_s"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -122,8 +122,10 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ kitty arm
-def build_layers(spec, steps_total, seed=0):
-    """Per-layer caches filled with seeded synthetic K/V (generated on the GPU)."""
+def build_layers(spec, steps_total, seed=0, keep=()):
+    """Per-layer caches filled with seeded synthetic K/V (generated on the GPU).
+    keep: sequences whose raw inputs are copied back to the host (for sampled
+    oracle checks); returned as raw[layer][b] = (k, v, tail_k, tail_v) uint16."""
     import numpy as np
     import torch
     from mixed_precision_bit_gb300 import kitty
@@ -137,8 +139,9 @@ def build_layers(spec, steps_total, seed=0):
                        in_dtype=kitty.BF16,
                        rank_mode=kitty.RANK_RUNNING if spec["running"] else kitty.RANK_PAGE)
     gen = torch.Generator(device="cuda")
-    layers = []
+    layers, raw = [], []
     tot = int(pages.sum())
+    starts = np.concatenate([[0], np.cumsum(pages)[:-1]]) * PAGE
     for l in range(L):
         lc = LayerCache(cfg, B, max_pages, pool_pages)
         gen.manual_seed(seed * 7919 + l)
@@ -170,9 +173,15 @@ def build_layers(spec, steps_total, seed=0):
         order = torch.randperm(tot, generator=torch.Generator().manual_seed(seed * 31 + l)).numpy()
         lc.prefill(kp.view(torch.int16), vp.view(torch.int16), pages, tk.view(torch.int16),
                    tv.view(torch.int16), tails, page_order=order)
+        host = lambda t: t.view(torch.int16).cpu().numpy().view(np.uint16)
+        raw.append({b: (host(kp[starts[b]:starts[b] + pages[b] * PAGE]),
+                        host(vp[starts[b]:starts[b] + pages[b] * PAGE]), host(tk[b]), host(tv[b]))
+                    for b in keep})
         del kp, vp
         layers.append(lc)
     torch.cuda.synchronize()
+    if keep:
+        return cfg, layers, raw
     return cfg, layers
 
 

@@ -122,7 +122,7 @@ class ClockSampler:
 
 
 # ------------------------------------------------------------------ kitty arm
-def build_layers(spec, steps_total, seed=0, keep=()):
+def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
     """Per-layer caches filled with seeded synthetic K/V (generated on the GPU).
     keep: sequences whose raw inputs are copied back to the host (for sampled
     oracle checks); returned as raw[layer][b] = (k, v, tail_k, tail_v) uint16."""
@@ -137,7 +137,8 @@ def build_layers(spec, steps_total, seed=0, keep=()):
     pool_pages = int(pages.sum()) + B * head
     cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
                        in_dtype=kitty.BF16,
-                       rank_mode=kitty.RANK_RUNNING if spec["running"] else kitty.RANK_PAGE)
+                       rank_mode=kitty.RANK_RUNNING if spec["running"] else kitty.RANK_PAGE,
+                       decode_pages_per_split=pages_per_split)
     gen = torch.Generator(device="cuda")
     layers, raw = [], []
     tot = int(pages.sum())
@@ -209,7 +210,7 @@ def run_kitty(args, rank, world, local_rank):
     if args.layers:
         spec["layers"] = args.layers
     L, B, Hq = spec["layers"], spec["B"], spec["Hq"]
-    cfg, layers = build_layers(spec, steps_total)
+    cfg, layers = build_layers(spec, steps_total, pages_per_split=args.pages_per_split)
     nsets = min(4, steps_total)
     q_all, kn_all, vn_all = token_inputs(spec, nsets)
     out = torch.empty((L, B, Hq, D), dtype=torch.bfloat16, device="cuda")
@@ -439,6 +440,8 @@ def main():
     ap.add_argument("--workload", default="budget",
                     choices=["budget", "budget_uniform", "llama3_8b", "qwen3_8b", "long"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
+    ap.add_argument("--pages-per-split", type=int, default=0,
+                    help="decode split-K chunk in pages (0: the library's choice)")
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -38,6 +38,8 @@ constexpr int kDMinBlocks = 4;  // resident CTAs per SM the register budget is s
 constexpr int kDThreads = kDWarps * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of one barrier phase (~0.1-1 s)
 constexpr int kPartial = kD + 2;           // split partial: m, l, o[128]
+// Running-max floor (log2 units): finite, so masked scores (-inf) give p = 0 exactly.
+constexpr float kNegBig = -1.0e30f;
 
 struct DecodeParams {
   const uint16_t* q;
@@ -167,33 +169,31 @@ __device__ __forceinline__ void unpack_rows23(uint32_t x, uint32_t* a) {  // tau
   a[0] = x & 0x00300030u; a[1] = x & 0x00C000C0u; a[2] = x2 & 0x00300030u; a[3] = x2 & 0x00C000C0u;
 }
 
-// One staged (page, kv-head) blob: scores, online softmax, PV.
+// Scores of one staged (page, kv-head) blob, in log2 units: s[2*mt + rh] is
+// token 16*mt + 8*rh + r of head qq.
 //   pa: shared-space address of the staged blob
 //   qf[j][0..1]: this lane's B-fragment query pairs for k-step j (head lane/8)
 //   qxa: shared-space address of q/4 of head lane/8 (extra-plane gather)
 template <int NX>
-__device__ __forceinline__ void compute_page(WarpState& w, const uint32_t pa,
-                                             const uint32_t (&qf)[8][2], const uint32_t qxa,
-                                             const Lane& L, const float (&kscale)[4],
-                                             float sm_log2) {
+__device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&qf)[8][2],
+                                            const uint32_t qxa, const Lane& L,
+                                            const float (&kscale)[4], float beta,
+                                            float (&s)[4]) {
   using O = Off<NX>;
-  const int lane = L.lane, r = L.r, qq = L.qq;
+  const int lane = L.lane, qq = L.qq;
   const uint32_t a_lane = pa + 32 * lane;   // this lane's 32 bytes of each code plane
   const uint32_t a_qq = pa + 4 * qq;        // this lane's fp16 pair in each 16-wide group
 
   // ---------------- scores: base plane, q.M row, extra plane
-  // two accumulator sets (even / odd k-steps) halve the dependent MMA chains
-  float cs[2][2][4] = {};
-  float cm[2][4] = {};
+  float cs[2][4] = {};
   const uint4 kb0 = ld_s128<0>(a_lane);
   const uint4 kb1 = ld_s128<16>(a_lane);
   const uint32_t kw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    uint32_t S0, S1, M0, M1;
+    uint32_t S0, S1;
     switch (j) {  // compile-time offsets (the loop is unrolled)
-#define KITTY_KS(J) case J: S0 = ld_s32<O::ks + 32 * J>(a_qq); S1 = ld_s32<O::ks + 32 * J + 16>(a_qq); \
-                            M0 = ld_s32<O::km + 32 * J>(a_qq); M1 = ld_s32<O::km + 32 * J + 16>(a_qq); break;
+#define KITTY_KS(J) case J: S0 = ld_s32<O::ks + 32 * J>(a_qq); S1 = ld_s32<O::ks + 32 * J + 16>(a_qq); break;
       KITTY_KS(0) KITTY_KS(1) KITTY_KS(2) KITTY_KS(3) KITTY_KS(4) KITTY_KS(5) KITTY_KS(6) default: KITTY_KS(7)
 #undef KITTY_KS
     }
@@ -201,12 +201,9 @@ __device__ __forceinline__ void compute_page(WarpState& w, const uint32_t pa,
     const uint32_t b1 = hilo_mul(qf[j][1], S1, L.fneg);
     uint32_t a[4];
     unpack_rows01(kw[j], a);
-    mma_f16(cs[j & 1][0], a, b0, b1);
+    mma_f16(cs[0], a, b0, b1);
     unpack_rows23(kw[j], a);
-    mma_f16(cs[j & 1][1], a, b0, b1);
-    // every row r < 8 carries the minima, so every lane reads beta of its head
-    const uint32_t am[4] = {M0, 0u, M1, 0u};
-    mma_f16(cm[j & 1], am, qf[j][0], qf[j][1]);
+    mma_f16(cs[1], a, b0, b1);
   }
   if (NX > 0) {
     const uint32_t a_id = pa + 2 * qq;
@@ -230,27 +227,49 @@ __device__ __forceinline__ void compute_page(WarpState& w, const uint32_t pa,
       const uint32_t b1 = hilo_mul(q23, s23, L.fneg);
       uint32_t a[4];
       unpack_rows01(x, a);
-      mma_f16(cs[js & 1][0], a, b0, b1);
+      mma_f16(cs[0], a, b0, b1);
       unpack_rows23(x, a);
-      mma_f16(cs[js & 1][1], a, b0, b1);
+      mma_f16(cs[1], a, b0, b1);
     }
   }
 
-  // ---------------- online softmax (head qq; hi + lo columns are this lane's pair)
-  const float beta = (cm[0][0] + cm[1][0]) * sm_log2;
-  float s[4];
 #pragma unroll
   for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
     for (int rh = 0; rh < 2; ++rh)
-      s[2 * mt + rh] = fmaf((cs[0][mt][2 * rh] + cs[1][mt][2 * rh]) + (cs[0][mt][2 * rh + 1] + cs[1][mt][2 * rh + 1]),
-                            kscale[2 * mt + rh], beta);
-  float pm = fmaxf(fmaxf(s[0], s[1]), fmaxf(s[2], s[3]));
-  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
-  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
-  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
-  rescale(w, pm);
-  uint32_t T[4];
+      s[2 * mt + rh] = fmaf(cs[mt][2 * rh] + cs[mt][2 * rh + 1], kscale[2 * mt + rh], beta);
+}
+
+// q.M bias (log2 units) of two pages with one set of one-row MMAs: B is the
+// plain query for every page, so A rows r even carry page A's Key minima and
+// odd rows page B's; each lane reads its own row and its neighbour's.
+template <int NX>
+__device__ __forceinline__ void pair_beta(const uint32_t paA, const uint32_t paB,
+                                          const uint32_t (&qf)[8][2], const Lane& L,
+                                          float sm_log2, float& bA, float& bB) {
+  using O = Off<NX>;
+  const uint32_t a_m = ((L.r & 1) ? paB : paA) + 4 * L.qq;
+  float cm[4] = {};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    uint32_t M0, M1;
+    switch (j) {
+#define KITTY_KM(J) case J: M0 = ld_s32<O::km + 32 * J>(a_m); M1 = ld_s32<O::km + 32 * J + 16>(a_m); break;
+      KITTY_KM(0) KITTY_KM(1) KITTY_KM(2) KITTY_KM(3) KITTY_KM(4) KITTY_KM(5) KITTY_KM(6) default: KITTY_KM(7)
+#undef KITTY_KM
+    }
+    const uint32_t am[4] = {M0, 0u, M1, 0u};
+    mma_f16(cm, am, qf[j][0], qf[j][1]);
+  }
+  const float mine = cm[0] * sm_log2;
+  const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 4);
+  bA = (L.r & 1) ? other : mine;
+  bB = (L.r & 1) ? mine : other;
+}
+
+// Probabilities of one page against the running max, split into fp16 (hi, lo)
+// and transposed into PV B fragments.
+__device__ __forceinline__ void page_probs(WarpState& w, const float (&s)[4], uint32_t (&T)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float p = ex2(s[i] - w.m);
@@ -258,7 +277,16 @@ __device__ __forceinline__ void compute_page(WarpState& w, const uint32_t pa,
     const float t = __uint_as_float(__float_as_uint(p) & 0xFFFFE000u);  // 11 significant bits
     T[i] = movmatrix_t(h2_bits(__floats2half2_rn(t, p - t)));          // (hi, lo) -> B columns
   }
+}
 
+// Value minima term and PV of one page with its probability fragments T.
+template <int NX>
+__device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const uint32_t (&T)[4],
+                                        const Lane& L) {
+  using O = Off<NX>;
+  const int lane = L.lane, r = L.r, qq = L.qq;
+  const uint32_t a_lane = pa + 32 * lane;
+  const uint32_t a_qq = pa + 4 * qq;
   // ---------------- Value minima: rows = groups (r & 3), k = tokens
   {
     const uint32_t a_vm = pa + 64 * (r & 3) + 4 * qq;
@@ -408,7 +436,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     for (int i = 0; i < 4; ++i) w.acc[mc][i] = 0.f;
 #pragma unroll
   for (int i = 0; i < 4; ++i) w.vm[i] = 0.f;
-  w.m = -INFINITY;
+  w.m = kNegBig;
   w.l = 0.f;
 
   // ---- this warp's pages: pbeg + wid + kDWarps*i, i < npw
@@ -443,32 +471,73 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   };
   const int pro = min(npw, kDStages);
   for (int i = 0; i < pro; ++i) issue(i);
-  for (int i = 0; i < npw; ++i) {
-    const int st = i % kDStages;
-    const uint32_t par = (uint32_t)(i / kDStages) & 1u;
+  const uint32_t stage0 = smem_u32(wst);
+  // Pages are taken two at a time: two independent score chains, one joint max
+  // and rescale, then both PVs.  A missing or invalid page is masked (score -inf).
+  for (int i = 0; i < npw; i += 2) {
+    const bool hasB = i + 1 < npw;
     // every lane observes the phase completion itself (acquire of the copied
     // bytes); the exit is warp-uniform and the wait is bounded
     bool done = false;
     for (uint32_t it = 0;; ++it) {
-      done = done || mbar_test(&wbar[st], par);
+      done = done || (mbar_test(&wbar[i % kDStages], (uint32_t)(i / kDStages) & 1u) &&
+                      (!hasB || mbar_test(&wbar[(i + 1) % kDStages], (uint32_t)((i + 1) / kDStages) & 1u)));
       if (__all_sync(0xFFFFFFFFu, done) || it >= kWaitLimit) break;
       if (it > 64) __nanosleep(32);
     }
-    const bool ok = __all_sync(0xFFFFFFFFu, done);
-    if (!ok) {
+    if (!__all_sync(0xFFFFFFFFu, done)) {
       // give up: report, then wait (bounded) for every copy still in flight
       if (lane == 0) {
         set_status(p.d_status, KITTY_ST_TIMEOUT);
-        for (int k = i + 1; k < min(npw, i + kDStages); ++k)
+        for (int k = i; k < min(npw, i + kDStages); ++k)
           mbar_wait_bounded(&wbar[k % kDStages], (uint32_t)(k / kDStages) & 1u, kWaitLimit);
       }
       __syncwarp();
       break;
     }
-    if (valid_mask & (1u << st))
-      compute_page<NX>(w, smem_u32(wst) + st * kBlob, qf, qxa, L, kscale, p.sm_log2);
+    const int stA = i % kDStages, stB = (i + 1) % kDStages;
+    const bool vA = (valid_mask >> stA) & 1u;
+    const uint32_t paA = stage0 + stA * kBlob;
+    const uint32_t paB = hasB ? stage0 + stB * kBlob : paA;
+    float bA, bB;
+    pair_beta<NX>(paA, paB, qf, L, p.sm_log2, bA, bB);
+    float sA[4];
+    page_scores<NX>(paA, qf, qxa, L, kscale, bA, sA);
+    if (hasB) {
+      const bool vB = (valid_mask >> stB) & 1u;
+      float sB[4];
+      page_scores<NX>(paB, qf, qxa, L, kscale, bB, sB);
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        sA[k] = vA ? sA[k] : -INFINITY;
+        sB[k] = vB ? sB[k] : -INFINITY;
+      }
+      float pm = fmaxf(fmaxf(fmaxf(sA[0], sA[1]), fmaxf(sA[2], sA[3])),
+                       fmaxf(fmaxf(sB[0], sB[1]), fmaxf(sB[2], sB[3])));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
+      rescale(w, pm);
+      uint32_t TA[4], TB[4];
+      page_probs(w, sA, TA);
+      page_probs(w, sB, TB);
+      page_pv<NX>(w, paA, TA, L);
+      page_pv<NX>(w, paB, TB, L);
+    } else {  // last page of an odd count
+#pragma unroll
+      for (int k = 0; k < 4; ++k) sA[k] = vA ? sA[k] : -INFINITY;
+      float pm = fmaxf(fmaxf(sA[0], sA[1]), fmaxf(sA[2], sA[3]));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
+      rescale(w, pm);
+      uint32_t TA[4];
+      page_probs(w, sA, TA);
+      page_pv<NX>(w, paA, TA, L);
+    }
     __syncwarp();
     if (i + kDStages < npw) issue(i + kDStages);
+    if (i + 1 + kDStages < npw) issue(i + 1 + kDStages);
   }
   if (s == 0 && tl > 0) tail_tokens<DT>(w, p, qs, b, kvh, tl, wid, L);
 

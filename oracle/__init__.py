@@ -60,6 +60,8 @@ def lib():
             "orc_val_pos": (None, [i, i, P, P]),
             "orc_quantize_page_f32": (i, [P, P, i, i, P, P, P, P]),
             "orc_dequant_page": (None, [P, i, P, P, P]),
+            "orc_page_channels": (None, [P, i, P]),
+            "orc_meta_pos": (None, [i, i, i, P]),
             "orc_quantize_pages": (i, [i, i, i, i, P, P, i, P, P, i, P, P, P, P, i]),
             "orc_append_token": (i, [i, i, i, i, P, P, P, P, P, P, P, P, P, P, i, P, P, i, i]),
             "orc_decode_attention": (i, [i, i, i, i, P, P, i, P, i, P, P, P, P, f, i, P]),
@@ -148,6 +150,22 @@ def quantize_page_f32(xk, xv, n_hi: int, running=None):
         rs, rq, rc = running
         st = lib().orc_quantize_page_f32(_p(xk), _p(xv), n_hi, 1, _p(rs), _p(rq), _p(rc), _p(blob))
     return blob, st
+
+
+def page_channels(blob, n_hi: int) -> np.ndarray:
+    """The boosted channel list of a blob, row order (ascending ids)."""
+    blob = _c(blob, np.uint8)
+    out = np.zeros(max(n_hi, 1), np.int32)
+    lib().orc_page_channels(_p(blob), n_hi, _p(out))
+    return out[:n_hi]
+
+
+def meta_pos(kind: str, a: int, b: int = 0) -> int:
+    """Storage index of Key minima ("km", channel a), Value metadata ("vmeta",
+    group a, token b) or channel-list rows ("kch", row a)."""
+    pos = ctypes.c_int()
+    lib().orc_meta_pos({"km": 0, "vmeta": 1, "kch": 2}[kind], a, b, ctypes.byref(pos))
+    return pos.value
 
 
 def dequant_page(blob, n_hi: int):

@@ -106,12 +106,13 @@ float in_to_f32(uint16_t v, int dtype) { return dtype == 1 ? bf16_to_f32(v) : f1
 // Byte layout of one (page, kv-head) blob, n_hi a multiple of 16 in [0, 128]:
 //   Kbase  1024 B   2-bit codes, all D channels x 32 tokens
 //   Kextra n_hi*8 B 2-bit low halves of the boosted channels' 4-bit codes
-//   KS     256 B    fp16 step per channel (boosted: the base-plane step)
-//   KM     256 B    fp16 minimum per channel
-//   Kch    n_hi B   boosted channel ids, ascending (row j of Kextra = Kch[j])
+//   KS     256 B    fp16 step per channel, channel order (boosted: the base-plane step)
+//   KM     256 B    fp16 minimum per channel, at km_pos(c)
+//   Kch    n_hi B   boosted channel ids; row j of Kextra (the j-th smallest
+//                   boosted channel) is stored at byte kch_pos(j)
 //   Vbase  1024 B   2-bit codes, 32 tokens x D channels
-//   VS     256 B    fp16 step per (group, token), group-major [4][32]
-//   VM     256 B    fp16 minimum per (group, token), group-major [4][32]
+//   VS     256 B    fp16 step per (group, token), at vmeta_pos(G, t)
+//   VM     256 B    fp16 minimum per (group, token), at vmeta_pos(G, t)
 struct Layout {
   int n_hi;
   size_t kbase, kextra, ks, km, kch, vbase, vs, vm, bytes;
@@ -154,6 +155,25 @@ BitPos val_pos(int t, int c) {
   const int tau = 2 * (mc & 1) + rh;
   const int lane = 4 * r + qq;
   return {lane * 8 + (mc >> 1) * 2 + kt, 16 * e + 8 * half + 2 * tau};
+}
+
+// Metadata read by the decode in 16-byte pieces is stored in the same
+// "fragment order" as the planes: the values lane group qq = (index % 8) / 2
+// needs are contiguous.
+//  km_pos(c):   channel c = 16j + 8h + 2qq + e  ->  ((qq*8 + j)*2 + h)*2 + e
+int km_pos(int c) {
+  const int j = c >> 4, h = (c >> 3) & 1, qq = (c >> 1) & 3, e = c & 1;
+  return ((qq * 8 + j) * 2 + h) * 2 + e;
+}
+//  vmeta_pos(G, t): token t = 16kt + 8h + 2qq + e  ->  G*32 + qq*8 + kt*4 + h*2 + e
+int vmeta_pos(int G, int t) {
+  const int kt = t >> 4, h = (t >> 3) & 1, qq = (t >> 1) & 3, e = t & 1;
+  return G * 32 + qq * 8 + kt * 4 + h * 2 + e;
+}
+//  kch_pos(j):  row j = 16js + 8h + 2qq + e  ->  js*16 + qq*4 + h*2 + e
+int kch_pos(int j) {
+  const int js = j >> 4, h = (j >> 3) & 1, qq = (j >> 1) & 3, e = j & 1;
+  return js * 16 + qq * 4 + h * 2 + e;
 }
 
 void put2(uint8_t* plane, BitPos p, uint32_t code) {
@@ -307,7 +327,7 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
   int j = 0;
   for (int c = 0; c < D; ++c) {
     row_of[c] = -1;
-    if (boosted[c]) { blob[lay.kch + j] = (uint8_t)c; row_of[c] = j++; }
+    if (boosted[c]) { blob[lay.kch + kch_pos(j)] = (uint8_t)c; row_of[c] = j++; }
   }
   const int xw = n_hi / 16;  // Kextra words per lane
   for (int c = 0; c < D; ++c) {
@@ -316,7 +336,7 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
     const bool b = boosted[c];
     quant_group(xk + c, D, P, st.mn[c], st.mx[c], b ? 15 : 3, b, &S, &M, code);
     wr16(blob + lay.ks, c, S);
-    wr16(blob + lay.km, c, M);
+    wr16(blob + lay.km, km_pos(c), M);
     for (int t = 0; t < P; ++t) {
       if (b) {
         // 4-bit code c4 = 4*hi + lo: hi joins the uniform base plane, lo the
@@ -336,8 +356,8 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
       uint16_t S, M;
       uint8_t code[VG];
       quant_group(x, 1, VG, mn, mx, 3, false, &S, &M, code);
-      wr16(blob + lay.vs, g * P + t, S);
-      wr16(blob + lay.vm, g * P + t, M);
+      wr16(blob + lay.vs, vmeta_pos(g, t), S);
+      wr16(blob + lay.vm, vmeta_pos(g, t), M);
       for (int i = 0; i < VG; ++i) put2(vbase, val_pos(t, g * VG + i), code[i]);
     }
   }
@@ -384,7 +404,7 @@ int dequant(const uint8_t* blob, int n_hi, double* kh, double* vh) {
   for (int c = 0; c < D; ++c) row_of[c] = -1;
   int prev = -1;
   for (int j = 0; j < n_hi; ++j) {
-    const int ch = blob[lay.kch + j];
+    const int ch = blob[lay.kch + kch_pos(j)];
     if (ch >= D || ch <= prev) return ST_BAD_PAGE;
     row_of[ch] = j;
     prev = ch;
@@ -392,7 +412,7 @@ int dequant(const uint8_t* blob, int n_hi, double* kh, double* vh) {
   const int xw = n_hi / 16;
   for (int c = 0; c < D; ++c) {
     const double S = f16_to_f32(rd16(blob + lay.ks, c));
-    const double M = f16_to_f32(rd16(blob + lay.km, c));
+    const double M = f16_to_f32(rd16(blob + lay.km, km_pos(c)));
     for (int t = 0; t < P; ++t) {
       double v = M + S * (double)get2(blob + lay.kbase, key_pos(c, t, 8));
       if (row_of[c] >= 0) v += (S / 4.0) * (double)get2(blob + lay.kextra, key_pos(row_of[c], t, xw));
@@ -402,8 +422,8 @@ int dequant(const uint8_t* blob, int n_hi, double* kh, double* vh) {
   for (int t = 0; t < P; ++t)
     for (int c = 0; c < D; ++c) {
       const int g = c / VG;
-      const double S = f16_to_f32(rd16(blob + lay.vs, g * P + t));
-      const double M = f16_to_f32(rd16(blob + lay.vm, g * P + t));
+      const double S = f16_to_f32(rd16(blob + lay.vs, vmeta_pos(g, t)));
+      const double M = f16_to_f32(rd16(blob + lay.vm, vmeta_pos(g, t)));
       vh[t * D + c] = M + S * (double)get2(blob + lay.vbase, val_pos(t, c));
     }
   return ST_OK;
@@ -524,6 +544,16 @@ int orc_quantize_page_f32(const float* xk, const float* xv, int n_hi, int runnin
                           float* rsq, int* rcount, uint8_t* blob) {
   if (!valid_n_hi(n_hi)) return -1;
   return quantize_one(xk, xv, n_hi, running, rsum, rsq, rcount, blob);
+}
+
+// The boosted channel list of a blob in row order (ascending channel ids).
+void orc_page_channels(const uint8_t* blob, int n_hi, int* out) {
+  const Layout lay(n_hi);
+  for (int j = 0; j < n_hi; ++j) out[j] = blob[lay.kch + kch_pos(j)];
+}
+
+void orc_meta_pos(int kind, int a, int b, int* pos) {
+  *pos = kind == 0 ? km_pos(a) : kind == 1 ? vmeta_pos(a, b) : kch_pos(a);
 }
 
 void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int* status) {

@@ -135,8 +135,7 @@ def test_planted_outlier_channels_are_boosted(orc):
     xv = _bf16(r.standard_normal((32, 128)))
     blob, st = orc.quantize_page_f32(xk, xv, 32)
     assert st == 0
-    lay_kch = 1024 + 32 * 8 + 512
-    assert (blob[lay_kch:lay_kch + 32] == planted).all()
+    assert (orc.page_channels(blob, 32) == planted).all()
 
 
 # ----------------------------------------------------------------- quantizer
@@ -219,7 +218,7 @@ def test_planes_recombine_to_4bit_code(orc):
     xk, xv = _kv(11)
     blob, _ = orc.quantize_page_f32(xk, xv, 32)
     base, extra = _planes(blob, 32)
-    kch = blob[1024 + 256 + 512:1024 + 256 + 512 + 32].astype(np.int64)
+    kch = orc.page_channels(blob, 32).astype(np.int64)
     assert (np.diff(kch) > 0).all()
     _, code4 = _np_uniform_quant(xk, 15)
     for j, c in enumerate(kch):
@@ -244,6 +243,9 @@ def test_plane_maps_are_bijections(orc):
     for nh in (16, 32, 64):
         seen = {orc.key_pos(j, t, nh // 16) for j in range(nh) for t in range(32)}
         assert len(seen) == nh * 32 and max(w for w, _ in seen) == nh * 2 - 1
+    assert sorted(orc.meta_pos("km", c) for c in range(128)) == list(range(128))
+    assert sorted(orc.meta_pos("vmeta", g, t) for g in range(4) for t in range(32)) == list(range(128))
+    assert sorted(orc.meta_pos("kch", j) for j in range(64)) == list(range(64))
 
 
 def test_closed_forms_exact_reconstruction(orc):
@@ -272,7 +274,7 @@ def test_closed_forms_exact_reconstruction(orc):
     xk2, xv2 = _kv(13)
     blob, _ = orc.quantize_page_f32(xk2, xv2, 32)
     base, extra = _planes(blob, 32)
-    kch = blob[1024 + 256 + 512:1024 + 256 + 512 + 32]
+    kch = orc.page_channels(blob, 32)
     code = base.copy()
     for j, c in enumerate(kch):
         code[:, c] = 4 * base[:, c] + extra[:, j]
@@ -288,7 +290,7 @@ def test_reconstruction_error_bound(orc):
         xk, xv = _kv(seed)
         blob, _ = orc.quantize_page_f32(xk, xv, 32)
         kh, vh, _ = orc.dequant_page(blob, 32)
-        kch = set(blob[1024 + 256 + 512:1024 + 256 + 512 + 32].tolist())
+        kch = set(orc.page_channels(blob, 32).tolist())
         for x, xh, groups in ((xk, kh, [(slice(None), c) for c in range(128)]),
                               (xv, vh, [(t, slice(32 * g, 32 * g + 32)) for t in range(32) for g in range(4)])):
             for sel in groups:
@@ -320,7 +322,7 @@ def test_boost_lowers_error(orc):
         assert (np.abs(kh - xk) <= np.abs(uni - xk) + 2e-3 * np.abs(xk).max()).all()
         tot_k += e_k.sum()
         tot_u += e_u.sum()
-        kch = blob[1024 + 256 + 512:1024 + 256 + 512 + 32]
+        kch = orc.page_channels(blob, 32)
         var = xk.astype(np.float64).var(0) + 1e-30
         norm = e_k.mean(0) / var
         mask = np.zeros(128, bool)

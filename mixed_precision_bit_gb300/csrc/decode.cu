@@ -206,19 +206,18 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
     mma_f16(cs[1], a, b0, b1);
   }
   if (NX > 0) {
-    const uint32_t a_id = pa + 2 * qq;
+    const uint32_t a_id = pa + 4 * qq;
     const uint32_t a_x = pa + 4 * NX * lane;
 #pragma unroll
     for (int js = 0; js < NX; ++js) {
-      uint32_t i01, i23, x;
-      switch (js) {
-#define KITTY_KX(J) case J: i01 = ld_s16<O::kch + 16 * J>(a_id); i23 = ld_s16<O::kch + 16 * J + 8>(a_id); \
-                            x = ld_s32<O::kx + 4 * J>(a_x); break;
+      uint32_t ids, x;
+      switch (js) {  // channel-list rows 2qq, 2qq+1, 2qq+8, 2qq+9 are one word (fragment order)
+#define KITTY_KX(J) case J: ids = ld_s32<O::kch + 16 * J>(a_id); x = ld_s32<O::kx + 4 * J>(a_x); break;
         KITTY_KX(0) KITTY_KX(1) KITTY_KX(2) KITTY_KX(3) KITTY_KX(4) KITTY_KX(5) KITTY_KX(6) default: KITTY_KX(7)
 #undef KITTY_KX
       }
-      const uint32_t c0 = 2 * (i01 & 127), c1 = 2 * ((i01 >> 8) & 127);
-      const uint32_t c2 = 2 * (i23 & 127), c3 = 2 * ((i23 >> 8) & 127);
+      const uint32_t c0 = (ids << 1) & 0xFEu, c1 = (ids >> 7) & 0xFEu;
+      const uint32_t c2 = (ids >> 15) & 0xFEu, c3 = (ids >> 23) & 0xFEu;
       const uint32_t q01 = ld_s16r(qxa + c0) | ((uint32_t)ld_s16r(qxa + c1) << 16);
       const uint32_t q23 = ld_s16r(qxa + c2) | ((uint32_t)ld_s16r(qxa + c3) << 16);
       const uint32_t s01 = ld_s16r(pa + O::ks + c0) | ((uint32_t)ld_s16r(pa + O::ks + c1) << 16);
@@ -248,17 +247,16 @@ __device__ __forceinline__ void pair_beta(const uint32_t paA, const uint32_t paB
                                           const uint32_t (&qf)[8][2], const Lane& L,
                                           float sm_log2, float& bA, float& bB) {
   using O = Off<NX>;
-  const uint32_t a_m = ((L.r & 1) ? paB : paA) + 4 * L.qq;
+  // this lane's 16 minima pairs are contiguous (fragment order): 4 x 16 bytes
+  const uint32_t a_m = ((L.r & 1) ? paB : paA) + 64 * L.qq;
+  const uint4 m0 = ld_s128<O::km>(a_m), m1 = ld_s128<O::km + 16>(a_m);
+  const uint4 m2 = ld_s128<O::km + 32>(a_m), m3 = ld_s128<O::km + 48>(a_m);
+  const uint32_t M[16] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w,
+                          m2.x, m2.y, m2.z, m2.w, m3.x, m3.y, m3.z, m3.w};
   float cm[4] = {};
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
-    uint32_t M0, M1;
-    switch (j) {
-#define KITTY_KM(J) case J: M0 = ld_s32<O::km + 32 * J>(a_m); M1 = ld_s32<O::km + 32 * J + 16>(a_m); break;
-      KITTY_KM(0) KITTY_KM(1) KITTY_KM(2) KITTY_KM(3) KITTY_KM(4) KITTY_KM(5) KITTY_KM(6) default: KITTY_KM(7)
-#undef KITTY_KM
-    }
-    const uint32_t am[4] = {M0, 0u, M1, 0u};
+    const uint32_t am[4] = {M[2 * j], 0u, M[2 * j + 1], 0u};
     mma_f16(cm, am, qf[j][0], qf[j][1]);
   }
   const float mine = cm[0] * sm_log2;
@@ -286,13 +284,13 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
   using O = Off<NX>;
   const int lane = L.lane, r = L.r, qq = L.qq;
   const uint32_t a_lane = pa + 32 * lane;
-  const uint32_t a_qq = pa + 4 * qq;
-  // ---------------- Value minima: rows = groups (r & 3), k = tokens
+  const uint32_t a_q16 = pa + 16 * qq;  // this lane group's Value steps (fragment order)
+  // ---------------- Value minima: rows = groups (r & 3), k = tokens (fragment order)
   {
-    const uint32_t a_vm = pa + 64 * (r & 3) + 4 * qq;
-    const uint32_t am0[4] = {ld_s32<O::vm>(a_vm), 0u, ld_s32<O::vm + 16>(a_vm), 0u};
+    const uint4 vm = ld_s128<O::vm>(pa + 64 * (r & 3) + 16 * qq);
+    const uint32_t am0[4] = {vm.x, 0u, vm.y, 0u};
     mma_f16(w.vm, am0, T[0], T[1]);
-    const uint32_t am1[4] = {ld_s32<O::vm + 32>(a_vm), 0u, ld_s32<O::vm + 48>(a_vm), 0u};
+    const uint32_t am1[4] = {vm.z, 0u, vm.w, 0u};
     mma_f16(w.vm, am1, T[2], T[3]);
   }
 
@@ -309,9 +307,9 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
     uint2 vv;
     uint32_t S[4];
     switch (G) {
-#define KITTY_VG(J) case J: vv = ld_s64<O::vb + 8 * J>(a_lane); \
-                            S[0] = ld_s32<O::vs + 64 * J>(a_qq); S[1] = ld_s32<O::vs + 64 * J + 16>(a_qq); \
-                            S[2] = ld_s32<O::vs + 64 * J + 32>(a_qq); S[3] = ld_s32<O::vs + 64 * J + 48>(a_qq); break;
+#define KITTY_VG(J) case J: { vv = ld_s64<O::vb + 8 * J>(a_lane); \
+                            const uint4 sv = ld_s128<O::vs + 64 * J>(a_q16); \
+                            S[0] = sv.x; S[1] = sv.y; S[2] = sv.z; S[3] = sv.w; } break;
       KITTY_VG(0) KITTY_VG(1) KITTY_VG(2) default: KITTY_VG(3)
 #undef KITTY_VG
     }

@@ -174,7 +174,8 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     const QuantParams q = qparams(mn, mx, levels, boosted);
     uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
     b16[lay.ks / 2 + c] = q.Sbits;
-    b16[lay.km / 2 + c] = q.Mbits;
+    // minima in fragment order: channel 16j + 8h + 2qq + e at ((qq*8 + j)*2 + h)*2 + e
+    b16[lay.km / 2 + (((((c >> 1) & 3) * 8 + (c >> 4)) * 2 + ((c >> 3) & 1)) * 2 + (c & 1))] = q.Mbits;
     uint32_t code[kPage];
 #pragma unroll
     for (int t = 0; t < kPage; ++t) code[t] = qcode(x[t], q, levels);
@@ -205,7 +206,9 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
         }
         atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w);
       }
-      atomicOr(&sm.blob[(lay.kch + row) / 4], (uint32_t)c << (8 * (row & 3)));
+      // channel-list row 16js + 8h + 2qq + e stored at byte js*16 + qq*4 + h*2 + e
+      const int pos = lay.kch + js * 16 + qx * 4 + hx * 2 + ex;
+      atomicOr(&sm.blob[pos / 4], (uint32_t)c << (8 * (pos & 3)));
     }
   }
 
@@ -221,8 +224,10 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     for (int i = 1; i < kVGroup; ++i) { vmn = fminf(vmn, v[i]); vmx = fmaxf(vmx, v[i]); }
     const QuantParams q = qparams(vmn, vmx, 3, false);
     uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
-    b16[lay.vs / 2 + G * kPage + t] = q.Sbits;
-    b16[lay.vm / 2 + G * kPage + t] = q.Mbits;
+    // Value metadata in fragment order: token 16kt + 8h + 2qq + e at G*32 + qq*8 + kt*4 + h*2 + e
+    const int vpos = G * kPage + ((t >> 1) & 3) * 8 + (t >> 4) * 4 + ((t >> 3) & 1) * 2 + (t & 1);
+    b16[lay.vs / 2 + vpos] = q.Sbits;
+    b16[lay.vm / 2 + vpos] = q.Mbits;
     const int qq = (t >> 1) & 3, kt = t >> 4, half = (t >> 3) & 1, e = t & 1;
     const int bitbase = 16 * e + 8 * half;
 #pragma unroll

@@ -186,6 +186,55 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
     return cfg, layers
 
 
+def measure_quantize(spec, reps=5, seed=3):
+    """Bulk page quantization throughput on one layer of the workload (inputs
+    resident): page mode and running mode, timed with CUDA events.  GB/s counts
+    the bf16 K+V read plus the packed pages written."""
+    import numpy as np
+    import torch
+    from mixed_precision_bit_gb300 import kitty
+    B, Hkv = spec["B"], spec["Hkv"]
+    pages = spec["pages"]
+    tot = int(pages.sum())
+    g = torch.Generator(device="cuda")
+    g.manual_seed(seed)
+    k = (torch.randn((tot * PAGE, Hkv, D), generator=g, device="cuda")
+         * torch.exp(torch.randn((Hkv, D), generator=g, device="cuda"))).to(torch.bfloat16)
+    v = torch.randn((tot * PAGE, Hkv, D), generator=g, device="cuda").to(torch.bfloat16)
+    ids = torch.from_numpy(np.random.default_rng(seed).permutation(tot).astype(np.int32)).cuda()
+    seq = torch.from_numpy(np.repeat(np.arange(B), pages).astype(np.int32)).cuda()
+    out = {}
+    for mode in (kitty.RANK_PAGE, kitty.RANK_RUNNING):
+        cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
+                           in_dtype=kitty.BF16, rank_mode=mode)
+        blob, per_page = kitty.page_bytes(cfg)
+        pool = torch.empty(tot * per_page, dtype=torch.uint8, device="cuda")
+        run = {}
+        if mode == kitty.RANK_RUNNING:
+            run = dict(seq_of_page=seq, n_seqs=B,
+                       run_sum=torch.zeros((B, Hkv, D), dtype=torch.float32, device="cuda"),
+                       run_sumsq=torch.zeros((B, Hkv, D), dtype=torch.float32, device="cuda"),
+                       run_count=torch.zeros((B, Hkv), dtype=torch.int32, device="cuda"))
+        call = lambda: kitty.quantize_pages(cfg, k.view(torch.int16), v.view(torch.int16), ids, pool,
+                                            tot, **run)
+        call()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(reps):
+            call()
+        e1.record()
+        torch.cuda.synchronize()
+        sec = e0.elapsed_time(e1) / 1e3 / reps
+        nbytes = 2 * k.numel() * 2 + tot * per_page
+        out["page_mode" if mode == kitty.RANK_PAGE else "running_mode"] = {
+            "gbs": nbytes / sec / 1e9, "ms": sec * 1e3, "page_heads_per_s": tot * Hkv / sec}
+    del k, v
+    torch.cuda.empty_cache()
+    out["unit"] = "GB/s (bf16 K+V read + packed pages written), one layer of the workload"
+    return out
+
+
 def token_inputs(spec, nsets, seed=1):
     """Per-step new tokens and queries for every layer: nsets distinct sets."""
     import torch
@@ -288,7 +337,9 @@ def run_kitty(args, rank, world, local_rank):
     h2d = (hq.numel() + hk.numel() + hv.numel()) * 2 + hfl.numel() * 4
     d2h = hout.numel() * 2
     launches_per_call = 1 + (1 if splits > 1 else 0)
+    quant = measure_quantize(spec) if args.measure_quantize else None
     return dict(spec=spec, cfg=cfg, ms=ms, K=K, W=W, E=E, dec_ms=dec_ms, dec_bytes=dec_bytes,
+                quantize=quant,
                 clocks=clk, e2e_s=e2e_s, h2d=h2d, d2h=d2h, splits=splits, chunk=chunk,
                 gpu_launches=K * L * (2 + launches_per_call), max_pages=layers[0].max_pages,
                 pool_bytes=sum(lc.pool.numel() for lc in layers))
@@ -445,6 +496,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--measure-quantize", type=int, default=1,
+                    help="also time bulk page quantization on one layer (1/0)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -509,6 +562,7 @@ def main():
                      "algorithmic_bytes_per_launch": dec_bytes,
                      "avg_launch_ms": dec_s * 1e3},
         "gpu_launches": r["gpu_launches"],
+        "quantize": r["quantize"],
         "clocks": r["clocks"],
         "e2e": {"value": job_throughput(world, B, r["E"], r["e2e_s"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

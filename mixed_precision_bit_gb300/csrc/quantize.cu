@@ -22,10 +22,11 @@ namespace {
 constexpr int kQThreads = 128;
 constexpr int kMaxBlobWords = (3072 + 9 * kD) / 4;
 
+constexpr int kRowH = kD + 8;  // 16-bit elements per staged row (16-byte pad: fewer bank conflicts)
+
 struct QuantSmem {
-  float xk[kPage][kD];
-  float xv[kPage][kD / kVGroup][kVGroup + 1];  // padded: group reads hit 32 banks
-  float var[kD];
+  uint16_t xk[kPage][kRowH];  // raw 16-bit inputs, token-major
+  uint16_t xv[kPage][kRowH];
   uint32_t blob[kMaxBlobWords];
   int warp_cnt[kQThreads / 32];
   int bad;
@@ -50,9 +51,15 @@ __device__ __forceinline__ float running_var(float sum, float sumsq, float n) {
 }
 
 struct QuantParams {
-  float M, u;
+  float M, u, ru;  // stored minimum and step as fp32, approximate 1/u
   uint16_t Sbits, Mbits;
 };
+
+__device__ __forceinline__ float rcp_approx(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Asymmetric min/max group quantizer: fp16 minimum and step, codes computed
 // against the stored values; boosted Key channels store 4x the 4-bit step.
@@ -71,20 +78,39 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
     q.Sbits = __half_as_ushort(Sh);
     q.u = __half2float(Sh);
   }
+  q.ru = rcp_approx(q.u);
   return q;
 }
 
+// code = clamp(rint(fl((x - M) / u)), 0, L), bit-exact with an IEEE division.
+// The quotient is taken as (x - M) * (1/u), within 2^-21 relative of the true
+// value; where that lands within 2^-15 of a rounding tie (and inside the clamp
+// range) the correctly rounded division decides.  u == 0 gives code 0.
 __device__ __forceinline__ uint32_t qcode(float x, const QuantParams& q, int levels) {
   if (q.u == 0.0f) return 0u;
-  int c = __float2int_rn(__fdiv_rn(__fsub_rn(x, q.M), q.u));
-  c = c < 0 ? 0 : (c > levels ? levels : c);
-  return (uint32_t)c;
+  const float d = __fsub_rn(x, q.M);
+  const float y = __fmul_rn(d, q.ru);
+  float n = rintf(y);
+  if (fabsf(fabsf(__fsub_rn(y, n)) - 0.5f) < 0x1p-15f && y > -1.5f && y < (float)levels + 1.5f)
+    n = rintf(__fdiv_rn(d, q.u));
+  n = fminf(fmaxf(n, 0.0f), (float)levels);
+  return (uint32_t)n;
 }
 
-__device__ __forceinline__ bool in_range(float x, int* bad_code) {
-  if (!isfinite(x)) { *bad_code = KITTY_ST_NONFINITE; return false; }
-  if (fabsf(x) > 65504.0f) { *bad_code = KITTY_ST_RANGE; return false; }
-  return true;
+// Largest |16-bit input| class in a 32-bit word pair: 0 ok, RANGE, NONFINITE.
+template <int DT>
+__device__ __forceinline__ int range_class(uint32_t w) {
+  const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
+  const uint32_t m = lo > hi ? lo : hi;
+  if (DT == KITTY_BF16) return m >= 0x7F80u ? KITTY_ST_NONFINITE : (m >= 0x4780u ? KITTY_ST_RANGE : 0);
+  return m >= 0x7C00u ? KITTY_ST_NONFINITE : 0;  // fp16 finite values never exceed 65504
+}
+
+// Order-preserving key of an fp32 variance (larger var -> larger key), with
+// -0 == +0 as in a float comparison.
+__device__ __forceinline__ uint32_t var_key(float v) {
+  const uint32_t b = __float_as_uint(v + 0.0f);
+  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
 // Quantize one (page, kv-head).  ksrc/vsrc point at token 0 of the tile; token t
@@ -100,39 +126,34 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
   const int nwords = lay.bytes / 4;
   if (tid == 0) sm.bad = 0;
   for (int i = tid; i < nwords; i += kQThreads) sm.blob[i] = 0u;
-  __syncthreads();
 
+  // ---- stage the raw 16-bit tile (16-byte loads and stores), classify the range
   int bad = 0;
-  for (int idx = tid; idx < kPage * (kD / 8); idx += kQThreads) {
+#pragma unroll
+  for (int it = 0; it < kPage * (kD / 8) / kQThreads; ++it) {
+    const int idx = tid + it * kQThreads;
     const int t = idx >> 4, ch = (idx & 15) * 8;
     const uint4 a = *reinterpret_cast<const uint4*>(ksrc + (size_t)t * row_stride + ch);
     const uint4 b = *reinterpret_cast<const uint4*>(vsrc + (size_t)t * row_stride + ch);
-    const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, bw[4] = {b.x, b.y, b.z, b.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float k0 = bits16_to_f32((uint16_t)(aw[i] & 0xFFFFu), DT);
-      const float k1 = bits16_to_f32((uint16_t)(aw[i] >> 16), DT);
-      const float v0 = bits16_to_f32((uint16_t)(bw[i] & 0xFFFFu), DT);
-      const float v1 = bits16_to_f32((uint16_t)(bw[i] >> 16), DT);
-      in_range(k0, &bad); in_range(k1, &bad); in_range(v0, &bad); in_range(v1, &bad);
-      sm.xk[t][ch + 2 * i] = k0;
-      sm.xk[t][ch + 2 * i + 1] = k1;
-      sm.xv[t][(ch + 2 * i) >> 5][(ch + 2 * i) & 31] = v0;
-      sm.xv[t][(ch + 2 * i + 1) >> 5][(ch + 2 * i + 1) & 31] = v1;
-    }
+    *reinterpret_cast<uint4*>(&sm.xk[t][ch]) = a;
+    *reinterpret_cast<uint4*>(&sm.xv[t][ch]) = b;
+    const int c = max(max(max(range_class<DT>(a.x), range_class<DT>(a.y)),
+                          max(range_class<DT>(a.z), range_class<DT>(a.w))),
+                      max(max(range_class<DT>(b.x), range_class<DT>(b.y)),
+                          max(range_class<DT>(b.z), range_class<DT>(b.w))));
+    bad = max(bad, c);
   }
+  __syncthreads();  // tile staged; sm.bad reset by thread 0 is visible
   if (bad) atomicCAS(&sm.bad, 0, bad);
-  __syncthreads();
 
   // ---- Key channel statistics and variance (thread = channel c)
   const int c = tid;
   float x[kPage], tmp[kPage];
-  float mn, mx;
-  x[0] = sm.xk[0][c];
-  mn = mx = x[0];
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) x[t] = bits16_to_f32(sm.xk[t][c], DT);
+  float mn = x[0], mx = x[0];
 #pragma unroll
   for (int t = 1; t < kPage; ++t) {
-    x[t] = sm.xk[t][c];
     mn = fminf(mn, x[t]);
     mx = fmaxf(mx, x[t]);
   }
@@ -151,17 +172,30 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
   } else {
     var = running_var(s1, s2, (float)kPage);
   }
-  sm.var[c] = var;
-  __syncthreads();
 
-  // ---- top-k: rank = #channels with larger variance, ties to the lower index
-  int rank = 0;
-#pragma unroll 8
-  for (int o = 0; o < kD; ++o) {
-    const float vo = sm.var[o];
-    rank += (vo > var || (vo == var && o < c)) ? 1 : 0;
+  // ---- top-k: boosted iff fewer than n_hi channels have a larger variance or an
+  // equal variance and a lower index.  The n_hi-th largest key T is found by a
+  // bitwise threshold search; ties at T go to the lowest channels.
+  bool boosted = false;
+  if (n_hi >= kD) {
+    boosted = true;
+  } else if (n_hi > 0) {
+    const uint32_t key = var_key(var);
+    uint32_t T = 0u;
+    for (int bit = 31; bit >= 0; --bit) {
+      const uint32_t cand = T | (1u << bit);
+      if (__syncthreads_count(key >= cand) >= n_hi) T = cand;
+    }
+    const int n_gt = __syncthreads_count(key > T);
+    const bool tie = key == T;
+    const uint32_t tb = __ballot_sync(0xFFFFFFFFu, tie);
+    if (lane == 0) sm.warp_cnt[warp] = __popc(tb);
+    __syncthreads();
+    int tie_rank = __popc(tb & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) tie_rank += sm.warp_cnt[w];
+    boosted = key > T || (tie && tie_rank < n_hi - n_gt);
+    __syncthreads();
   }
-  const bool boosted = rank < n_hi;
   const uint32_t bal = __ballot_sync(0xFFFFFFFFu, boosted);
   if (lane == 0) sm.warp_cnt[warp] = __popc(bal);
   __syncthreads();
@@ -216,10 +250,17 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
   {
     const int t = tid >> 2, G = tid & 3;
     float v[kVGroup];
-    float vmn, vmx;
 #pragma unroll
-    for (int i = 0; i < kVGroup; ++i) v[i] = sm.xv[t][G][i];
-    vmn = vmx = v[0];
+    for (int k = 0; k < 4; ++k) {
+      const uint4 w4 = *reinterpret_cast<const uint4*>(&sm.xv[t][G * kVGroup + 8 * k]);
+      const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        v[8 * k + 2 * i] = bits16_to_f32((uint16_t)(ww[i] & 0xFFFFu), DT);
+        v[8 * k + 2 * i + 1] = bits16_to_f32((uint16_t)(ww[i] >> 16), DT);
+      }
+    }
+    float vmn = v[0], vmx = v[0];
 #pragma unroll
     for (int i = 1; i < kVGroup; ++i) { vmn = fminf(vmn, v[i]); vmx = fmaxf(vmx, v[i]); }
     const QuantParams q = qparams(vmn, vmx, 3, false);

@@ -65,6 +65,8 @@ extern "C" {
 
 #define KITTY_RANK_PAGE 0    /* rank each page on its own 32 tokens */
 #define KITTY_RANK_RUNNING 1 /* rank on running sum / sum of squares per (seq, head) */
+#define KITTY_RANK_SEQUENCE 2 /* bulk quantize: one ranking per (seq, head) over all its
+                                 pages (prefill); appends then continue as running mode */
 
 /* Configuration.  The parameters follow the VeloxQuant-MLX docs,
  * "Configuration reference": kitty_hi_fraction (as n_hi = round(hf * D)),
@@ -78,7 +80,7 @@ typedef struct {
   int32_t hi_bit;       /* must be 4 */
   int32_t lo_bit;       /* must be 2 */
   int32_t v_group;      /* channels per Value group; must be 32 */
-  int32_t rank_mode;    /* KITTY_RANK_PAGE or KITTY_RANK_RUNNING */
+  int32_t rank_mode;    /* KITTY_RANK_PAGE, KITTY_RANK_RUNNING or KITTY_RANK_SEQUENCE */
   int32_t in_dtype;     /* KITTY_F16 or KITTY_BF16 for K, V, Q and the tails */
   int32_t decode_pages_per_split; /* split-K chunk in pages; 0 = library's choice */
 } kitty_cfg;
@@ -127,6 +129,10 @@ void kitty_alloc_destroy(kitty_alloc* a);
  *   [0, n_seqs); run_sum, run_sumsq device f32 [n_seqs][Hkv][128] and run_count
  *   device int32 [n_seqs][Hkv] are updated with each page's sums (in page order)
  *   before that page is ranked.
+ *   Sequence mode (same arguments): the accumulators take all of a sequence's
+ *   page sums first, the channels are ranked once on that variance, and every
+ *   page of the sequence is quantized with that one boost set (VeloxQuant-MLX
+ *   docs, Prefill phase: one ranking per head over the prompt).
  *   pool        device, pool_pages * per_page bytes, 16-byte aligned. */
 int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const void* v, int32_t n_pages,
                          const int32_t* page_ids, const int32_t* seq_of_page, int32_t n_seqs,

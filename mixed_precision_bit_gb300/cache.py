@@ -36,7 +36,7 @@ class LayerCache:
         self.tail_k = torch.zeros((B, Hkv, PAGE, D), dtype=torch.int16, device=dev)
         self.tail_v = torch.zeros_like(self.tail_k)
         self.tail_len = torch.zeros(B, dtype=torch.int32, device=dev)
-        running = cfg.rank_mode == kitty.RANK_RUNNING
+        running = cfg.rank_mode != kitty.RANK_PAGE  # running or sequence-wide ranking
         self.run_sum = torch.zeros((B, Hkv, D), dtype=torch.float32, device=dev) if running else None
         self.run_sumsq = torch.zeros_like(self.run_sum) if running else None
         self.run_count = torch.zeros((B, Hkv), dtype=torch.int32, device=dev) if running else None

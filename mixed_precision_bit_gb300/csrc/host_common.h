@@ -19,7 +19,8 @@ inline int check_cfg(const kitty_cfg* c, bool decode) {
   if (c->head_dim != 128 || c->page_tokens != 32 || c->hi_bit != 4 || c->lo_bit != 2 ||
       c->v_group != 32 || c->n_hi % 16 != 0)
     return KITTY_ERR_UNSUPPORTED;
-  if (c->rank_mode != KITTY_RANK_PAGE && c->rank_mode != KITTY_RANK_RUNNING)
+  if (c->rank_mode != KITTY_RANK_PAGE && c->rank_mode != KITTY_RANK_RUNNING &&
+      c->rank_mode != KITTY_RANK_SEQUENCE)
     return KITTY_ERR_INVALID_ARG;
   if (c->in_dtype != KITTY_F16 && c->in_dtype != KITTY_BF16) return KITTY_ERR_INVALID_ARG;
   if (c->decode_pages_per_split < 0) return KITTY_ERR_INVALID_ARG;

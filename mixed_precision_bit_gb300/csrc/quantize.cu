@@ -113,13 +113,65 @@ __device__ __forceinline__ uint32_t var_key(float v) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
+// Top-k boost flag of channel threadIdx.x: true iff fewer than n_hi channels have
+// a larger variance, or an equal variance and a lower index.  The n_hi-th
+// largest key T is found by a bitwise threshold search; ties at T go to the
+// lowest channels.  Called by all 128 threads.
+__device__ __forceinline__ bool topk_flag(QuantSmem& sm, float var, int n_hi) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  if (n_hi >= kD) return true;
+  if (n_hi <= 0) return false;
+  const uint32_t key = var_key(var);
+  uint32_t T = 0u;
+  for (int bit = 31; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    if (__syncthreads_count(key >= cand) >= n_hi) T = cand;
+  }
+  const int n_gt = __syncthreads_count(key > T);
+  const bool tie = key == T;
+  const uint32_t tb = __ballot_sync(0xFFFFFFFFu, tie);
+  if (lane == 0) sm.warp_cnt[warp] = __popc(tb);
+  __syncthreads();
+  int tie_rank = __popc(tb & ((1u << lane) - 1u));
+  for (int w = 0; w < warp; ++w) tie_rank += sm.warp_cnt[w];
+  __syncthreads();
+  return key > T || (tie && tie_rank < n_hi - n_gt);
+}
+
+// Tree-ordered sum and sum of squares of Key channel threadIdx.x over one
+// page's 32 tokens (ksrc at token 0, token t at +t*row_stride); stages only K.
+template <int DT>
+__device__ void tile_stats(QuantSmem& sm, const uint16_t* ksrc, size_t row_stride, float& s1,
+                           float& s2) {
+  const int tid = threadIdx.x;
+#pragma unroll
+  for (int it = 0; it < kPage * (kD / 8) / kQThreads; ++it) {
+    const int idx = tid + it * kQThreads;
+    const int t = idx >> 4, ch = (idx & 15) * 8;
+    *reinterpret_cast<uint4*>(&sm.xk[t][ch]) =
+        *reinterpret_cast<const uint4*>(ksrc + (size_t)t * row_stride + ch);
+  }
+  __syncthreads();
+  float a[kPage], b[kPage];
+#pragma unroll
+  for (int t = 0; t < kPage; ++t) {
+    a[t] = bits16_to_f32(sm.xk[t][tid], DT);
+    b[t] = __fmul_rn(a[t], a[t]);
+  }
+  s1 = tree32(a);
+  s2 = tree32(b);
+  __syncthreads();
+}
+
 // Quantize one (page, kv-head).  ksrc/vsrc point at token 0 of the tile; token t
 // is at +t*row_stride elements.  rsum/rsq/rcount: running accumulators of
 // channel `threadIdx.x` (running mode only).  Writes the blob to dst.
+// fixed: -1 ranks this page (page or running statistics); 0 / 1 imposes the
+// channel's boost flag (sequence-wide ranking), skipping the statistics.
 template <int DT>
 __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_t* vsrc,
                               size_t row_stride, int n_hi, bool running, float& rsum, float& rsq,
-                              int& rcount, uint8_t* dst, int32_t* d_status) {
+                              int& rcount, uint8_t* dst, int32_t* d_status, int fixed = -1) {
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const BlobLayout lay(n_hi);
@@ -157,45 +209,26 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     mn = fminf(mn, x[t]);
     mx = fmaxf(mx, x[t]);
   }
+  float var = 0.f;
+  if (fixed < 0) {
 #pragma unroll
-  for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
-  const float s1 = tree32(tmp);
+    for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
+    const float s1 = tree32(tmp);
 #pragma unroll
-  for (int t = 0; t < kPage; ++t) tmp[t] = __fmul_rn(x[t], x[t]);
-  const float s2 = tree32(tmp);
-  float var;
-  if (running) {
-    rsum = __fadd_rn(rsum, s1);
-    rsq = __fadd_rn(rsq, s2);
-    rcount += kPage;
-    var = running_var(rsum, rsq, __int2float_rn(rcount));
-  } else {
-    var = running_var(s1, s2, (float)kPage);
+    for (int t = 0; t < kPage; ++t) tmp[t] = __fmul_rn(x[t], x[t]);
+    const float s2 = tree32(tmp);
+    if (running) {
+      rsum = __fadd_rn(rsum, s1);
+      rsq = __fadd_rn(rsq, s2);
+      rcount += kPage;
+      var = running_var(rsum, rsq, __int2float_rn(rcount));
+    } else {
+      var = running_var(s1, s2, (float)kPage);
+    }
   }
 
-  // ---- top-k: boosted iff fewer than n_hi channels have a larger variance or an
-  // equal variance and a lower index.  The n_hi-th largest key T is found by a
-  // bitwise threshold search; ties at T go to the lowest channels.
-  bool boosted = false;
-  if (n_hi >= kD) {
-    boosted = true;
-  } else if (n_hi > 0) {
-    const uint32_t key = var_key(var);
-    uint32_t T = 0u;
-    for (int bit = 31; bit >= 0; --bit) {
-      const uint32_t cand = T | (1u << bit);
-      if (__syncthreads_count(key >= cand) >= n_hi) T = cand;
-    }
-    const int n_gt = __syncthreads_count(key > T);
-    const bool tie = key == T;
-    const uint32_t tb = __ballot_sync(0xFFFFFFFFu, tie);
-    if (lane == 0) sm.warp_cnt[warp] = __popc(tb);
-    __syncthreads();
-    int tie_rank = __popc(tb & ((1u << lane) - 1u));
-    for (int w = 0; w < warp; ++w) tie_rank += sm.warp_cnt[w];
-    boosted = key > T || (tie && tie_rank < n_hi - n_gt);
-    __syncthreads();
-  }
+  // ---- top-k (or the caller's fixed boost set)
+  const bool boosted = fixed >= 0 ? (fixed != 0) : topk_flag(sm, var, n_hi);
   const uint32_t bal = __ballot_sync(0xFFFFFFFFu, boosted);
   if (lane == 0) sm.warp_cnt[warp] = __popc(bal);
   __syncthreads();
@@ -296,7 +329,7 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
 
 // Page mode: one CTA per (input page i, kv head h).
 template <int DT>
-__global__ void __launch_bounds__(kQThreads) quantize_pages_kernel(
+__global__ void __launch_bounds__(kQThreads, 8) quantize_pages_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
     int n_hi, int Hkv, uint8_t* pool, int pool_pages, int32_t* d_status) {
   __shared__ QuantSmem sm;
@@ -326,7 +359,7 @@ __global__ void check_seq_kernel(const int32_t* seq_of_page, int n_pages, int n_
 // Running mode: one CTA per (sequence s, kv head h) walks that sequence's pages
 // in order, carrying the channel accumulators in registers.
 template <int DT>
-__global__ void __launch_bounds__(kQThreads) quantize_running_kernel(
+__global__ void __launch_bounds__(kQThreads, 8) quantize_running_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
     const int32_t* seq_of_page, int n_pages, int n_hi, int Hkv, float* run_sum, float* run_sumsq,
     int32_t* run_count, uint8_t* pool, int pool_pages, int32_t* d_status) {
@@ -355,6 +388,57 @@ __global__ void __launch_bounds__(kQThreads) quantize_running_kernel(
     const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
     quantize_tile<DT>(sm, k + src, v + src, stride, n_hi, true, rs, rq, rc,
                       pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status);
+  }
+  run_sum[sh * kD + threadIdx.x] = rs;
+  run_sumsq[sh * kD + threadIdx.x] = rq;
+  if (threadIdx.x == 0) run_count[sh] = rc;
+}
+
+// Sequence mode: one CTA per (sequence s, kv head h).  Pass 1 accumulates the
+// tree-ordered page sums of all the sequence's pages (in order) into the
+// running accumulators; the channels are ranked once on that variance; pass 2
+// quantizes every page with that fixed boost set.
+template <int DT>
+__global__ void __launch_bounds__(kQThreads, 8) quantize_sequence_kernel(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
+    const int32_t* seq_of_page, int n_pages, int n_hi, int Hkv, float* run_sum, float* run_sumsq,
+    int32_t* run_count, uint8_t* pool, int pool_pages, int32_t* d_status) {
+  __shared__ QuantSmem sm;
+  const int s = blockIdx.x, h = blockIdx.y;
+  int lo = 0, hi = n_pages;
+  while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] < s) lo = m + 1; else hi = m; }
+  const int p0 = lo;
+  hi = n_pages;
+  while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] <= s) lo = m + 1; else hi = m; }
+  const int p1 = lo;
+  if (p0 >= p1) return;
+  const BlobLayout lay(n_hi);
+  const size_t stride = (size_t)Hkv * kD;
+  const size_t sh = (size_t)s * Hkv + h;
+  float rs = run_sum[sh * kD + threadIdx.x];
+  float rq = run_sumsq[sh * kD + threadIdx.x];
+  int rc = run_count[sh];
+  for (int i = p0; i < p1; ++i) {
+    const int pid = page_ids[i];
+    if (pid < 0 || pid >= pool_pages) continue;
+    float s1, s2;
+    tile_stats<DT>(sm, k + (size_t)i * kPage * stride + (size_t)h * kD, stride, s1, s2);
+    rs = __fadd_rn(rs, s1);
+    rq = __fadd_rn(rq, s2);
+    rc += kPage;
+  }
+  const bool boosted = topk_flag(sm, running_var(rs, rq, __int2float_rn(rc)), n_hi);
+  float dummy_s = 0.f, dummy_q = 0.f;
+  int dummy_c = 0;
+  for (int i = p0; i < p1; ++i) {
+    const int pid = page_ids[i];
+    if (pid < 0 || pid >= pool_pages) {
+      if (threadIdx.x == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
+      continue;
+    }
+    const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
+    quantize_tile<DT>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
+                      pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status, boosted ? 1 : 0);
   }
   run_sum[sh * kD + threadIdx.x] = rs;
   run_sumsq[sh * kD + threadIdx.x] = rq;
@@ -439,7 +523,7 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
   if (n_pages == 0) return KITTY_OK;
   if (!k || !v || !page_ids || !pool || !aligned16(k) || !aligned16(v) || !aligned16(pool))
     return KITTY_ERR_INVALID_ARG;
-  const bool running = cfg->rank_mode == KITTY_RANK_RUNNING;
+  const bool running = cfg->rank_mode != KITTY_RANK_PAGE;  // running or sequence mode
   if (running && (!seq_of_page || n_seqs <= 0 || !run_sum || !run_sumsq || !run_count))
     return KITTY_ERR_INVALID_ARG;
   if (n_pages > 65535 * 1024) return KITTY_ERR_UNSUPPORTED;
@@ -457,7 +541,12 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
   } else {
     check_seq_kernel<<<(n_pages + 255) / 256, 256, 0, s>>>(seq_of_page, n_pages, n_seqs, d_status);
     dim3 grid(n_seqs, Hkv);
-    if (cfg->in_dtype == KITTY_BF16)
+    if (cfg->rank_mode == KITTY_RANK_SEQUENCE) {
+      if (cfg->in_dtype == KITTY_BF16)
+        quantize_sequence_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+      else
+        quantize_sequence_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+    } else if (cfg->in_dtype == KITTY_BF16)
       quantize_running_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
     else
       quantize_running_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
@@ -478,7 +567,7 @@ extern "C" int kitty_append_token(const kitty_cfg* cfg, const void* k_new, const
   if (!k_new || !v_new || !tail_k || !tail_v || !tail_len || !flush_page_ids || !block_table ||
       !num_pages || !pool || !aligned16(tail_k) || !aligned16(tail_v) || !aligned16(pool))
     return KITTY_ERR_INVALID_ARG;
-  const bool running = cfg->rank_mode == KITTY_RANK_RUNNING;
+  const bool running = cfg->rank_mode != KITTY_RANK_PAGE;  // sequence mode appends as running
   if (running && (!run_sum || !run_sumsq || !run_count)) return KITTY_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int Hkv = cfg->num_kv_heads;

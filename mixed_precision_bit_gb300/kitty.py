@@ -20,7 +20,7 @@ ERR = {-1: "KITTY_ERR_INVALID_ARG", -2: "KITTY_ERR_UNSUPPORTED", -3: "KITTY_ERR_
 ST = dict(OK=0, EMPTY=1, RANGE=2, NONFINITE=3, BAD_PAGE=4, BAD_LEN=5, TAIL_FULL=6,
           BAD_FLUSH=7, TABLE_FULL=8, BAD_SEQ=9, TIMEOUT=10)
 F16, BF16, F32 = 0, 1, 2
-RANK_PAGE, RANK_RUNNING = 0, 1
+RANK_PAGE, RANK_RUNNING, RANK_SEQUENCE = 0, 1, 2
 
 
 class KittyError(RuntimeError):

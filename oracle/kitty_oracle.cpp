@@ -390,6 +390,36 @@ int quantize_one(const float* xk, const float* xv, int n_hi, int running, float*
   return st;
 }
 
+// Sequence-wide ranking (VeloxQuant-MLX docs, Prefill phase steps 1-3 and 5):
+// one boost set per (sequence, head), ranked on the variance over all of the
+// sequence's pages, then every page quantized with that set.  The running
+// accumulators end with the sequence totals (page sums added in page order).
+// xk_pages/xv_pages: the pages' fp32 tiles in order; blobs: one per page.
+int quantize_sequence(const std::vector<std::vector<float>>& xk_pages,
+                      const std::vector<std::vector<float>>& xv_pages, int n_hi, float* rsum,
+                      float* rsq, int* rcount, const std::vector<uint8_t*>& blobs) {
+  int st = ST_OK;
+  std::vector<PageStats> ps(xk_pages.size());
+  for (size_t p = 0; p < xk_pages.size(); ++p) {
+    note(&st, check_range(xk_pages[p].data(), P * D));
+    note(&st, check_range(xv_pages[p].data(), P * D));
+    page_stats(xk_pages[p].data(), ps[p]);
+    *rcount += P;
+    for (int c = 0; c < D; ++c) {
+      rsum[c] = rsum[c] + ps[p].s1[c];
+      rsq[c] = rsq[c] + ps[p].s2[c];
+    }
+  }
+  float var[D];
+  const float n = (float)*rcount;
+  for (int c = 0; c < D; ++c) var[c] = variance(rsum[c], rsq[c], n);
+  bool boosted[D];
+  top_k(var, n_hi, boosted);
+  for (size_t p = 0; p < xk_pages.size(); ++p)
+    encode_blob(xk_pages[p].data(), xv_pages[p].data(), ps[p], boosted, n_hi, blobs[p]);
+  return st;
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- decode side
@@ -562,9 +592,10 @@ void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int
 
 // Bulk quantization with the library's semantics.  k, v: [n_pages*32][Hkv][D]
 // 16-bit values (in_dtype 0 = fp16, 1 = bf16).  Page i is written at
-// pool + page_ids[i]*Hkv*blob.  rank_mode 0 = page, 1 = running; running mode
-// needs seq_of_page non-decreasing in [0, n_seqs) and accumulators
-// run_sum/run_sumsq [n_seqs][Hkv][D], run_count [n_seqs][Hkv].
+// pool + page_ids[i]*Hkv*blob.  rank_mode 0 = page, 1 = running, 2 = sequence;
+// running and sequence modes need seq_of_page non-decreasing in [0, n_seqs) and
+// accumulators run_sum/run_sumsq [n_seqs][Hkv][D], run_count [n_seqs][Hkv].
+// Pages whose id is out of range are skipped (not counted, not written).
 int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint16_t* k,
                        const uint16_t* v, int n_pages, const int* page_ids, const int* seq_of_page,
                        int n_seqs, float* run_sum, float* run_sumsq, int* run_count, uint8_t* pool,
@@ -573,11 +604,45 @@ int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uin
   const Layout lay(n_hi);
   const size_t page_stride = lay.bytes * (size_t)Hkv;
   int st = ST_OK;
-  if (rank_mode == 1) {
+  if (rank_mode == 1 || rank_mode == 2) {
     for (int i = 0; i < n_pages; ++i) {
       const int s = seq_of_page[i];
       if (s < 0 || s >= n_seqs || (i > 0 && s < seq_of_page[i - 1])) return ST_BAD_SEQ;
     }
+  }
+  auto tile = [&](int i, int h, std::vector<float>& xk, std::vector<float>& xv) {
+    xk.assign(P * D, 0.f);
+    xv.assign(P * D, 0.f);
+    for (int t = 0; t < P; ++t)
+      for (int c = 0; c < D; ++c) {
+        const size_t src = (((size_t)i * P + t) * Hkv + h) * D + c;
+        xk[t * D + c] = in_to_f32(k[src], in_dtype);
+        xv[t * D + c] = in_to_f32(v[src], in_dtype);
+      }
+  };
+  if (rank_mode == 2) {
+    std::vector<int> sts2((size_t)Hkv * (n_seqs > 0 ? n_seqs : 1), ST_OK);
+    parallel_for(Hkv * n_seqs, [&](int sh) {
+      const int h = sh % Hkv, sq = sh / Hkv;
+      std::vector<std::vector<float>> xk, xv;
+      std::vector<uint8_t*> blobs;
+      int bad = ST_OK;
+      for (int i = 0; i < n_pages; ++i) {
+        if (seq_of_page[i] != sq) continue;
+        const int id = page_ids[i];
+        if (id < 0 || id >= pool_pages) { bad = ST_BAD_PAGE; continue; }
+        xk.emplace_back();
+        xv.emplace_back();
+        tile(i, h, xk.back(), xv.back());
+        blobs.push_back(pool + (size_t)id * page_stride + (size_t)h * lay.bytes);
+      }
+      if (xk.empty()) { sts2[sh] = bad; return; }
+      const size_t o = (size_t)sq * Hkv + h;
+      int r = quantize_sequence(xk, xv, n_hi, run_sum + o * D, run_sumsq + o * D, run_count + o, blobs);
+      sts2[sh] = r != ST_OK ? r : bad;
+    });
+    for (int x : sts2) note(&st, x);
+    return st;
   }
   std::vector<int> sts(n_pages > 0 ? (size_t)n_pages * Hkv : 1, ST_OK);
   auto one = [&](int i, int h) {
@@ -657,7 +722,7 @@ int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint1
         xv[i] = in_to_f32(tail_v[base + i], in_dtype);
       }
       const size_t sh = (size_t)b * Hkv + h;
-      const bool running = rank_mode == 1;
+      const bool running = rank_mode != 0;  // sequence mode continues with running statistics
       note(&st, quantize_one(xk.data(), xv.data(), n_hi, running, running ? run_sum + sh * D : nullptr,
                              running ? run_sumsq + sh * D : nullptr, running ? run_count + sh : nullptr,
                              pool + (size_t)fid * page_stride + (size_t)h * lay.bytes));

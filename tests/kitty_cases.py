@@ -29,11 +29,14 @@ def dev32(a):
     return torch.from_numpy(np.ascontiguousarray(a, np.int32)).cuda()
 
 
-def gpu_quantize(w, inp, running=False, status=None):
-    """Quantize every page on the GPU; returns (pool uint8 tensor, run state or None)."""
+def gpu_quantize(w, inp, running=False, status=None, mode=None):
+    """Quantize every page on the GPU; returns (pool uint8 tensor, run state or None).
+    mode: 0 page, 1 running, 2 sequence (default: running if `running` else page)."""
     import torch
     from mixed_precision_bit_gb300 import kitty
-    cfg = cfg_for(w, rank_mode=1 if running else 0)
+    mode = (1 if running else 0) if mode is None else mode
+    running = mode != 0
+    cfg = cfg_for(w, rank_mode=mode)
     blob, per_page = kitty.page_bytes(cfg)
     pool = torch.zeros(inp["pool_pages"] * per_page, dtype=torch.uint8, device="cuda")
     run = None
@@ -51,13 +54,15 @@ def gpu_quantize(w, inp, running=False, status=None):
     return pool, run
 
 
-def oracle_quantize(w, inp, running=False):
+def oracle_quantize(w, inp, running=False, mode=None):
+    mode = (1 if running else 0) if mode is None else mode
+    running = mode != 0
     pool = np.zeros(inp["pool_pages"] * w.Hkv * oracle.page_bytes(w.n_hi), np.uint8)
     if running:
         rs = np.zeros((w.B, w.Hkv, 128), np.float32)
         rq = np.zeros_like(rs)
         rc = np.zeros((w.B, w.Hkv), np.int32)
-        st = oracle.quantize_pages(w.Hkv, w.n_hi, 1, w.dtype, inp["k"], inp["v"], inp["page_ids"],
+        st = oracle.quantize_pages(w.Hkv, w.n_hi, mode, w.dtype, inp["k"], inp["v"], inp["page_ids"],
                                    pool, inp["pool_pages"], seq_of_page=inp["seq_of_page"],
                                    n_seqs=w.B, run_sum=rs, run_sumsq=rq, run_count=rc)
         return pool, (rs, rq, rc), st

@@ -60,11 +60,12 @@ def test_quantize_bit_exact(case):
     assert bad.size == 0, "first mismatching bytes at %s" % bad[:8]
 
 
-def test_quantize_running_bit_exact():
-    w = _variant("small_gqa", pages=np.array([5, 3, 9]))
+@pytest.mark.parametrize("mode", [1, 2], ids=["running", "sequence"])
+def test_quantize_running_bit_exact(mode):
+    w = _variant("small_gqa", pages=np.array([5, 3, 9]), drift=64)
     inp = synth.host_inputs(w, seed=2)
-    pool, run = gpu_quantize(w, inp, running=True)
-    ref, (rs, rq, rc), st = oracle_quantize(w, inp, running=True)
+    pool, run = gpu_quantize(w, inp, mode=mode)
+    ref, (rs, rq, rc), st = oracle_quantize(w, inp, mode=mode)
     assert st == 0
     assert (pool.cpu().numpy() == ref).all()
     assert (run[0].cpu().numpy().view(np.uint32) == rs.view(np.uint32)).all()

@@ -516,3 +516,59 @@ def test_quantize_range_status(orc):
     xk[4, 7] = np.nan
     _, st = orc.quantize_page_f32(xk, xv, 32)
     assert st == orc.ST["NONFINITE"]
+
+
+# ----------------------------------------------------------------- sequence-wide ranking
+def _seq_pages(seed, npg, offsets=None):
+    r = _rng(seed)
+    sig = np.exp(r.standard_normal(128))
+    k = r.standard_normal((npg * 32, 1, 128)) * sig
+    if offsets is not None:
+        k += offsets[:, None, :].repeat(32, axis=0)
+    return (synth.to_bits(k, synth.BF16), synth.to_bits(r.standard_normal((npg * 32, 1, 128)), synth.BF16))
+
+
+def _quant(orc, mode, k, v, npg):
+    pool = np.zeros(npg * orc.page_bytes(32), np.uint8)
+    rs = np.zeros((1, 1, 128), np.float32)
+    rq = np.zeros_like(rs)
+    rc = np.zeros((1, 1), np.int32)
+    st = orc.quantize_pages(1, 32, mode, synth.BF16, k, v, np.arange(npg), pool, npg,
+                            seq_of_page=np.zeros(npg, np.int32), n_seqs=1, run_sum=rs, run_sumsq=rq,
+                            run_count=rc)
+    assert st == 0
+    return pool, (rs, rq, rc)
+
+
+def test_sequence_mode_one_page_equals_other_modes(orc):
+    k, v = _seq_pages(30, 1)
+    a, _ = _quant(orc, 0, k, v, 1)
+    b, _ = _quant(orc, 1, k, v, 1)
+    c, _ = _quant(orc, 2, k, v, 1)
+    assert (a == b).all() and (a == c).all()
+
+
+def test_sequence_mode_ranks_over_the_whole_prompt(orc):
+    """VeloxQuant-MLX docs, Prefill phase step 1: variance across the sequence axis.
+    Channels that are constant inside each page but jump between pages have ~0
+    variance per page and a large variance over the sequence: the sequence mode
+    boosts exactly them, on every page; the page mode does not."""
+    r = _rng(31)
+    npg = 8
+    planted = np.sort(r.choice(128, 32, replace=False))
+    off = np.zeros((npg, 128))
+    off[:, planted] = r.standard_normal((npg, 32)) * 50.0
+    k, v = _seq_pages(32, npg, off)
+    k_view = synth.from_bits(k, synth.BF16)
+    k_view[:, :, planted] = synth.from_bits(synth.to_bits(off[:, None, planted].repeat(32, 0).reshape(-1, 1, 32),
+                                                          synth.BF16), synth.BF16)
+    k = synth.to_bits(k_view, synth.BF16)
+    pool, (rs, rq, rc) = _quant(orc, 2, k, v, npg)
+    blob = orc.page_bytes(32)
+    for p in range(npg):
+        assert (orc.page_channels(pool[p * blob:(p + 1) * blob], 32) == planted).all()
+    page_pool, _ = _quant(orc, 0, k, v, npg)
+    assert not all((orc.page_channels(page_pool[p * blob:(p + 1) * blob], 32) == planted).all()
+                   for p in range(npg))
+    run_pool, (rs1, rq1, rc1) = _quant(orc, 1, k, v, npg)
+    assert (rs == rs1).all() and (rq == rq1).all() and (rc == rc1).all() and rc[0, 0] == 32 * npg

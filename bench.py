@@ -60,14 +60,15 @@ def workload_spec(name: str, steps_total: int):
         tails = (synth.bits(0, "budget/tail", B) % np.uint64(32)).astype(np.int64)
         return dict(name=name, B=int(B), Hq=Hq, Hkv=Hkv, n_hi=n_hi, layers=layers,
                     running=running, pages=np.full(B, ctx_pages, np.int64), tails=tails,
-                    drift=0, budget_bytes=40 * 10 ** 9)
+                    drift=0, budget_bytes=40 * 10 ** 9, dtype=synth.BF16)
     w = synth.workload(name)
     # independent layer copies, rotated every step, so the working set exceeds 4x L2
     pool = w.total_pages * w.Hkv * (3072 + 9 * w.n_hi)
-    layers = max(1, math.ceil(4 * 129e6 / max(pool, 1)))
+    # (the tiny single-head case is latency-bound and stays L2-resident by design)
+    layers = 1 if name == "tiny" else max(1, math.ceil(4 * 129e6 / max(pool, 1)))
     return dict(name=name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, n_hi=w.n_hi, layers=layers, running=False,
                 pages=w.pages.astype(np.int64), tails=w.tails.astype(np.int64), drift=w.drift,
-                budget_bytes=None)
+                budget_bytes=None, dtype=w.dtype)
 
 
 def headroom_pages(tails, steps_total):
@@ -136,9 +137,10 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
     max_pages = int(pages.max()) + head
     pool_pages = int(pages.sum()) + B * head
     cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
-                       in_dtype=kitty.BF16,
+                       in_dtype=spec["dtype"],
                        rank_mode=kitty.RANK_RUNNING if spec["running"] else kitty.RANK_PAGE,
                        decode_pages_per_split=pages_per_split)
+    tdt = torch.float16 if spec["dtype"] == kitty.F16 else torch.bfloat16
     gen = torch.Generator(device="cuda")
     layers, raw = [], []
     tot = int(pages.sum())
@@ -147,7 +149,7 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
         lc = LayerCache(cfg, B, max_pages, pool_pages)
         gen.manual_seed(seed * 7919 + l)
         sig = torch.exp(torch.randn((Hkv, D), generator=gen, device="cuda"))
-        kp = torch.empty((tot * PAGE, Hkv, D), dtype=torch.bfloat16, device="cuda")
+        kp = torch.empty((tot * PAGE, Hkv, D), dtype=tdt, device="cuda")
         vp = torch.empty_like(kp)
         pos = None
         if spec["drift"]:
@@ -166,11 +168,11 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
                     z[m] = z[m] * sg
             else:
                 z = z * sig
-            kp[s0:s0 + n] = z.to(torch.bfloat16)
-            vp[s0:s0 + n] = torch.randn((n, Hkv, D), generator=gen, device="cuda").to(torch.bfloat16)
+            kp[s0:s0 + n] = z.to(tdt)
+            vp[s0:s0 + n] = torch.randn((n, Hkv, D), generator=gen, device="cuda").to(tdt)
         tk = (torch.randn((B, Hkv, PAGE, D), generator=gen, device="cuda") * sig[None, :, None, :]
-              ).to(torch.bfloat16)
-        tv = torch.randn((B, Hkv, PAGE, D), generator=gen, device="cuda").to(torch.bfloat16)
+              ).to(tdt)
+        tv = torch.randn((B, Hkv, PAGE, D), generator=gen, device="cuda").to(tdt)
         order = torch.randperm(tot, generator=torch.Generator().manual_seed(seed * 31 + l)).numpy()
         lc.prefill(kp.view(torch.int16), vp.view(torch.int16), pages, tk.view(torch.int16),
                    tv.view(torch.int16), tails, page_order=order)
@@ -198,15 +200,16 @@ def measure_quantize(spec, reps=5, seed=3):
     tot = int(pages.sum())
     g = torch.Generator(device="cuda")
     g.manual_seed(seed)
+    tdt = torch.float16 if spec["dtype"] == kitty.F16 else torch.bfloat16
     k = (torch.randn((tot * PAGE, Hkv, D), generator=g, device="cuda")
-         * torch.exp(torch.randn((Hkv, D), generator=g, device="cuda"))).to(torch.bfloat16)
-    v = torch.randn((tot * PAGE, Hkv, D), generator=g, device="cuda").to(torch.bfloat16)
+         * torch.exp(torch.randn((Hkv, D), generator=g, device="cuda"))).to(tdt)
+    v = torch.randn((tot * PAGE, Hkv, D), generator=g, device="cuda").to(tdt)
     ids = torch.from_numpy(np.random.default_rng(seed).permutation(tot).astype(np.int32)).cuda()
     seq = torch.from_numpy(np.repeat(np.arange(B), pages).astype(np.int32)).cuda()
     out = {}
     for mode in (kitty.RANK_PAGE, kitty.RANK_RUNNING):
         cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
-                           in_dtype=kitty.BF16, rank_mode=mode)
+                           in_dtype=spec["dtype"], rank_mode=mode)
         blob, per_page = kitty.page_bytes(cfg)
         pool = torch.empty(tot * per_page, dtype=torch.uint8, device="cuda")
         run = {}
@@ -241,8 +244,9 @@ def token_inputs(spec, nsets, seed=1):
     g = torch.Generator(device="cuda")
     g.manual_seed(seed)
     L, B, Hq, Hkv = spec["layers"], spec["B"], spec["Hq"], spec["Hkv"]
+    tdt = torch.float16 if spec["dtype"] == 0 else torch.bfloat16
     mk = lambda H: torch.randn((nsets, L, B, H, D), generator=g, device="cuda").to(
-        torch.bfloat16).view(torch.int16)
+        tdt).view(torch.int16)
     return mk(Hq), mk(Hkv), mk(Hkv)
 
 
@@ -258,11 +262,13 @@ def run_kitty(args, rank, world, local_rank):
     spec = workload_spec(args.workload, steps_total)
     if args.layers:
         spec["layers"] = args.layers
+
     L, B, Hq = spec["layers"], spec["B"], spec["Hq"]
     cfg, layers = build_layers(spec, steps_total, pages_per_split=args.pages_per_split)
     nsets = min(4, steps_total)
     q_all, kn_all, vn_all = token_inputs(spec, nsets)
-    out = torch.empty((L, B, Hq, D), dtype=torch.bfloat16, device="cuda")
+    out = torch.empty((L, B, Hq, D), dtype=torch.bfloat16 if spec["dtype"] else torch.float16,
+                      device="cuda")
     # flush plans for the warm-up and timed steps, decided on the host ahead of time
     plans, algo = [], []
     for s in range(W + K):
@@ -370,8 +376,8 @@ class OracleSample:
         tot = int(pages.sum())
         self.mode = 1 if spec["running"] else 0
         sig = np.exp(synth.host_fast_normal(seed, (Hkv, D)))
-        k = synth.to_bits(synth.host_fast_normal(seed + 1, (tot * PAGE, Hkv, D)) * sig, synth.BF16)
-        v = synth.to_bits(synth.host_fast_normal(seed + 2, (tot * PAGE, Hkv, D)), synth.BF16)
+        k = synth.to_bits(synth.host_fast_normal(seed + 1, (tot * PAGE, Hkv, D)) * sig, spec["dtype"])
+        v = synth.to_bits(synth.host_fast_normal(seed + 2, (tot * PAGE, Hkv, D)), spec["dtype"])
         self.max_pages = int(pages.max()) + 4
         self.pool_pages = tot + 4 * S
         self.pool = np.zeros(self.pool_pages * Hkv * oracle.page_bytes(n_hi), np.uint8)
@@ -385,16 +391,16 @@ class OracleSample:
         self.rq = np.zeros_like(self.rs)
         self.rc = np.zeros((S, Hkv), np.int32)
         oracle.set_threads(host_cores())
-        st = oracle.quantize_pages(Hkv, n_hi, self.mode, synth.BF16, k, v, ids, self.pool,
+        st = oracle.quantize_pages(Hkv, n_hi, self.mode, spec["dtype"], k, v, ids, self.pool,
                                    self.pool_pages, seq_of_page=np.repeat(np.arange(S), pages),
                                    n_seqs=S, run_sum=self.rs, run_sumsq=self.rq, run_count=self.rc)
         assert st == 0, st
-        self.tk = synth.to_bits(synth.host_fast_normal(seed + 3, (S, Hkv, PAGE, D)), synth.BF16)
-        self.tv = synth.to_bits(synth.host_fast_normal(seed + 4, (S, Hkv, PAGE, D)), synth.BF16)
+        self.tk = synth.to_bits(synth.host_fast_normal(seed + 3, (S, Hkv, PAGE, D)), spec["dtype"])
+        self.tv = synth.to_bits(synth.host_fast_normal(seed + 4, (S, Hkv, PAGE, D)), spec["dtype"])
         self.tl = tails.copy()
         self.np_ = pages.astype(np.int32).copy()
-        self.q = synth.to_bits(synth.host_fast_normal(seed + 5, (S, Hq, D)), synth.BF16)
-        self.kn = synth.to_bits(synth.host_fast_normal(seed + 6, (S, Hkv, D)), synth.BF16)
+        self.q = synth.to_bits(synth.host_fast_normal(seed + 5, (S, Hq, D)), spec["dtype"])
+        self.kn = synth.to_bits(synth.host_fast_normal(seed + 6, (S, Hkv, D)), spec["dtype"])
         self.next_id = tot
 
     def step(self):
@@ -406,10 +412,10 @@ class OracleSample:
             if self.tl[b] + 1 == PAGE and self.np_[b] < self.max_pages and self.next_id < self.pool_pages:
                 fl[b] = self.next_id
                 self.next_id += 1
-        st = self.o.append_token(spec["Hkv"], spec["n_hi"], self.mode, synth.BF16, self.kn, self.kn,
+        st = self.o.append_token(spec["Hkv"], spec["n_hi"], self.mode, spec["dtype"], self.kn, self.kn,
                                  self.tk, self.tv, self.tl, self.rs, self.rq, self.rc, fl, self.bt,
                                  self.max_pages, self.np_, self.pool, self.pool_pages)
-        _, st2 = self.o.decode_attention(spec["Hkv"], spec["Hq"], spec["n_hi"], synth.BF16, self.q,
+        _, st2 = self.o.decode_attention(spec["Hkv"], spec["Hq"], spec["n_hi"], spec["dtype"], self.q,
                                          self.pool, self.pool_pages, self.bt, self.np_, self.tk,
                                          self.tv, self.tl, 1.0 / math.sqrt(D))
         assert st in (0,) and st2 in (0,), (st, st2)
@@ -475,8 +481,9 @@ def config_block(spec, extra=None):
          "head_dim": D, "page_tokens": PAGE, "n_hi": spec["n_hi"],
          "rank_mode": "running" if spec["running"] else "page",
          "context_pages": int(spec["pages"].max()), "kv_budget_bytes": spec["budget_bytes"],
-         "l2": "inputs larger than L2: %d layer pools rotate every step, > 4x the 129 MB L2"
-               % spec["layers"]}
+         "l2": ("L2-resident (latency-bound tiny case, no roofline claim)" if spec["name"] == "tiny"
+                else "inputs larger than L2: %d layer pools rotate every step, > 4x the 129 MB L2"
+                % spec["layers"])}
     if extra:
         c.update(extra)
     return c
@@ -489,7 +496,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kitty", choices=["kitty", "reference"])
     ap.add_argument("--workload", default="budget",
-                    choices=["budget", "budget_uniform", "llama3_8b", "qwen3_8b", "long"])
+                    choices=["budget", "budget_uniform", "llama3_8b", "qwen3_8b", "long", "tiny"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")

@@ -82,7 +82,10 @@ typedef struct {
   int32_t v_group;      /* channels per Value group; must be 32 */
   int32_t rank_mode;    /* KITTY_RANK_PAGE, KITTY_RANK_RUNNING or KITTY_RANK_SEQUENCE */
   int32_t in_dtype;     /* KITTY_F16 or KITTY_BF16 for K, V, Q and the tails */
-  int32_t decode_pages_per_split; /* split-K chunk in pages; 0 = library's choice */
+  int32_t decode_pages_per_split; /* split-K: 0 = library's schedule (split sizes
+                                   shrinking towards the end of the grid), > 0 =
+                                   splits of this many pages, raised to
+                                   ceil(max_pages / 256) if smaller */
 } kitty_cfg;
 
 /* Library ABI version (this header: 1). */
@@ -173,7 +176,8 @@ int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pa
  *   tokens; an empty sequence gives 0 and KITTY_ST_EMPTY.
  *   q       device [B][Hq][128] 16-bit (in_dtype)
  *   pool    device, 16-byte aligned, pool_pages pages
- *   tail_k, tail_v device [B][Hkv][32][128] 16-bit; may be NULL if all tails are 0
+ *   tail_k, tail_v device [B][Hkv][32][128] 16-bit, 16-byte aligned; may be NULL
+ *           if all tails are 0
  *   out     device [B][Hq][128] of out_dtype (KITTY_F32, KITTY_BF16, KITTY_F16)
  *   workspace device, >= kitty_decode_workspace_bytes, 16-byte aligned (may be
  *   NULL when that size is 0). */
@@ -210,7 +214,9 @@ int kitty_decode_attention_noalloc(const kitty_cfg* cfg, const void* q, const vo
                                    int32_t out_dtype, int32_t B, int32_t* d_status, void* stream);
 
 /* Launch shape that kitty_decode_attention uses for this batch shape: number of
- * splits per sequence and pages per split (for reporting and tests). */
+ * splits per sequence (at most 256) and the pages in the largest split (for
+ * reporting and tests).  Splits are cut from the end of each sequence, so a
+ * sequence shorter than max_pages drops whole leading splits. */
 int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pages, int32_t* splits,
                       int32_t* pages_per_split);
 

@@ -6,8 +6,13 @@
 // FlashAttention-style online softmax and PagedAttention block tables (both
 // cited there).
 //
-// One CTA = (split, kv head, sequence); 4 warps, each streaming every 4th page
-// of the split.  A warp stages whole (page, kv-head) blobs into shared memory
+// One CTA = (kv head, sequence, split); 4 warps, each streaming every 4th page
+// of the split.  Split sizes shrink from the first split to the last and the
+// grid is split-major, so the CTAs dispatched last are the short ones
+// (longest-processing-time-first order: the grid ends with little idle time on
+// the SMs).  A split's page range does not depend on the sequence length, so a
+// CTA requests its lengths, query rows and block-table entries together and
+// starts its page copies one memory round trip after it starts.  A warp stages whole (page, kv-head) blobs into shared memory
 // with 1-D bulk copies (cp.async.bulk + mbarrier, 4 stages per warp), then
 // computes, for its g <= 4 query heads:
 //   scores  S^T[t][n] = sum_c code[t][c] * B[c][n] on the tensor cores
@@ -26,6 +31,7 @@
 #include "kitty_common.cuh"
 #include "host_common.h"
 
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -38,6 +44,7 @@ constexpr int kDMinBlocks = 4;  // resident CTAs per SM the register budget is s
 constexpr int kDThreads = kDWarps * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of one barrier phase (~0.1-1 s)
 constexpr int kPartial = kD + 2;           // split partial: m, l, o[128]
+constexpr int kMaxSplits = 256;            // splits per sequence, at most
 // Running-max floor (log2 units): finite, so masked scores (-inf) give p = 0 exactly.
 constexpr float kNegBig = -1.0e30f;
 
@@ -53,8 +60,18 @@ struct DecodeParams {
   float* ws;
   int32_t* d_status;
   float sm_log2;  // sm_scale * log2(e)
-  int pool_pages, max_pages, out_dtype, splits, chunk, Hkv, Hq, g, n_hi, blob, in_dtype;
+  int pool_pages, max_pages, out_dtype, splits, Hkv, Hq, g, n_hi, blob, in_dtype;
+  // Split s of a sequence with np pages covers pages [starts[s], min(np, starts[s+1]));
+  // starts[] rises from 0 to starts[splits] = max_pages.  A split holds work only
+  // when it holds a page, except split 0, which always runs (it takes the tail
+  // tokens and is the one an empty sequence reports from).
+  int32_t starts[kMaxSplits + 1];
 };
+
+// Split s holds work for a sequence of np pages.
+__device__ __forceinline__ bool split_active(const DecodeParams& p, int s, int np) {
+  return np > p.starts[s] || s == 0;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -333,43 +350,78 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
   }
 }
 
-// Unquantized tail tokens (0..31 per sequence), CUDA-core path: warp `wid`
-// takes tail tokens wid, wid+4, ...  Contributions go to the hi columns with
-// the same per-row power of two as the paged codes.
+// Unquantized tail tokens (0..31 per sequence) on the CUDA cores.  Warp wid
+// takes tokens wid, wid+4, ... (at most 8).  All of its K and V rows are
+// loaded at once (8 bytes a lane per row; the rows were prefetched into L2
+// when the CTA started); the 32 (token, head) dot products are reduced across
+// the warp in one transposing butterfly, after which lane 4i+h holds token i
+// of head h, i.e. lane (r, qq) holds token r of its own head; one rescale
+// covers them all.  The V rows pass through the warp's idle stage buffer to
+// reach the accumulator layout, and carry the same per-row power of two as the
+// paged codes.
 template <int DT>
 __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* qs, int b, int kvh,
-                            int tl, int wid, const Lane& L) {
+                            int tl, int wid, const Lane& L, uint8_t* vbuf) {
   const int lane = L.lane, r = L.r, qq = L.qq;
-  const size_t base = ((size_t)b * p.Hkv + kvh) * kPage * kD;
+  const int nw = tl > wid ? (tl - wid + kDWarps - 1) / kDWarps : 0;  // warp-uniform
+  if (nw == 0) return;
+  const size_t base = ((size_t)b * p.Hkv + kvh) * kPage * kD + 4 * lane;
+  uint2 kx[8], vx[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const size_t off = base + (size_t)(wid + kDWarps * i) * kD;
+    kx[i] = i < nw ? *reinterpret_cast<const uint2*>(p.tail_k + off) : make_uint2(0u, 0u);
+    vx[i] = i < nw ? *reinterpret_cast<const uint2*>(p.tail_v + off) : make_uint2(0u, 0u);
+  }
   float qv[4][4];
 #pragma unroll
   for (int h = 0; h < 4; ++h)
 #pragma unroll
-    for (int i = 0; i < 4; ++i) qv[h][i] = __half2float(qs[h * kD + 4 * lane + i]);
-  for (int t = wid; t < tl; t += kDWarps) {
-    const uint16_t* kr = p.tail_k + base + (size_t)t * kD;
-    const uint16_t* vr = p.tail_v + base + (size_t)t * kD;
-    float kx[4];
+    for (int e = 0; e < 4; ++e) qv[h][e] = __half2float(qs[h * kD + 4 * lane + e]);
+  float v[32];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) kx[i] = load16<DT>(kr + 4 * lane + i);
-    float d[4];
+  for (int i = 0; i < 8; ++i) {
+    const float k0 = bits16_to_f32((uint16_t)(kx[i].x & 0xFFFFu), DT);
+    const float k1 = bits16_to_f32((uint16_t)(kx[i].x >> 16), DT);
+    const float k2 = bits16_to_f32((uint16_t)(kx[i].y & 0xFFFFu), DT);
+    const float k3 = bits16_to_f32((uint16_t)(kx[i].y >> 16), DT);
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      d[h] = qv[h][0] * kx[0] + qv[h][1] * kx[1] + qv[h][2] * kx[2] + qv[h][3] * kx[3];
+    for (int h = 0; h < 4; ++h) v[4 * i + h] = qv[h][0] * k0 + qv[h][1] * k1 + qv[h][2] * k2 + qv[h][3] * k3;
+  }
+  // transposing butterfly: after the step with offset o, a lane keeps the half
+  // of the values whose index bit o matches its own lane bit o
 #pragma unroll
-      for (int off = 16; off >= 1; off >>= 1) d[h] += __shfl_xor_sync(0xFFFFFFFFu, d[h], off);
+  for (int st = 0; st < 5; ++st) {
+    const int o = 16 >> st;
+    const bool up = (lane & o) != 0;
+#pragma unroll
+    for (int k = 0; k < o; ++k) {
+      const float send = up ? v[k] : v[k + o];
+      const float keep = up ? v[k + o] : v[k];
+      v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
     }
-    const float sc = (qq == 0 ? d[0] : qq == 1 ? d[1] : qq == 2 ? d[2] : d[3]) * p.sm_log2;
-    rescale(w, sc);
-    const float pr = ex2(sc - w.m);
-    if (r == 0) w.l += pr;
+  }
+  const float sc = r < nw ? v[0] * p.sm_log2 : -INFINITY;
+  float pm = fmaxf(sc, __shfl_xor_sync(0xFFFFFFFFu, sc, 4));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
+  rescale(w, pm);
+  const float pr = r < nw ? ex2(sc - w.m) : 0.f;
+  w.l += pr;
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < nw) *reinterpret_cast<uint2*>(vbuf + i * 2 * kD + 8 * lane) = vx[i];
+  __syncwarp();
+  const uint32_t vb = smem_u32(vbuf) + 2 * r;
+  for (int i = 0; i < nw; ++i) {
+    const float pi = __shfl_sync(0xFFFFFFFFu, pr, 4 * i + qq);
 #pragma unroll
     for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
-        const int c = 16 * mc + 8 * rh + r;
+        const int c = 16 * mc + 8 * rh;
         const float rs = __uint_as_float((uint32_t)(127 - 24 + 2 * (2 * (mc & 1) + rh)) << 23);
-        w.acc[mc][2 * rh] += pr * (load16<DT>(vr + c) * rs);
+        w.acc[mc][2 * rh] += pi * (bits16_to_f32(ld_s16r(vb + i * 2 * kD + 2 * c), DT) * rs);
       }
   }
 }
@@ -377,38 +429,84 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
 template <int DT, int NX>
 __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
-  const int s = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int u = blockIdx.x, s = blockIdx.y;
+  const int b = u / p.Hkv, kvh = u - b * p.Hkv;
   const int tid = threadIdx.x, wid = tid >> 5;
   const Lane L;
   const int lane = L.lane, r = L.r, qq = L.qq;
   constexpr int kBlob = Off<NX>::bytes;
+  const int sbeg = p.starts[s], send = p.starts[s + 1];
+  // Independent loads first, all in flight together: the lengths, this warp's
+  // first 32 block-table entries (up to the split's nominal end, which is
+  // inside the row) and the query rows (thread tid = channel tid of 4 heads).
   int np = p.num_pages[b];
   int tl = p.tail_len != nullptr ? p.tail_len[b] : 0;
+  const int first = sbeg + wid;  // this warp's pages: first + kDWarps*i, i < npw
+  const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
+  int bt_cache = first + kDWarps * lane < send ? bt[first + kDWarps * lane] : -1;
+  float qv[4];
+#pragma unroll
+  for (int h = 0; h < 4; ++h)
+    qv[h] = h < p.g ? load16<DT>(p.q + ((size_t)b * p.Hq + (size_t)kvh * p.g + h) * kD + tid) : 0.f;
   if (np < 0 || np > p.max_pages || tl < 0 || tl > kPage || (tl > 0 && p.tail_k == nullptr)) {
     if (tid == 0 && s == 0 && kvh == 0) set_status(p.d_status, KITTY_ST_BAD_LEN);
     np = 0;
     tl = 0;
   }
-  const int n_act = max(1, (np + p.chunk - 1) / p.chunk);
-  if (s >= n_act) return;
-  const int pbeg = s * p.chunk, pend = min(np, pbeg + p.chunk);
+  if (!split_active(p, s, np)) return;
+  const int pbeg = sbeg, pend = min(np, send);
 
   uint8_t* stages = dsm;
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + kDWarps * kDStages * kBlob);
   __half* qs = reinterpret_cast<__half*>(bars + kDWarps * kDStages);  // q      [4][128]
   __half* qs4 = qs + 4 * kD;                                          // q / 4  [4][128]
 
-  for (int i = tid; i < 4 * kD; i += kDThreads) {
-    const int h = i >> 7, c = i & (kD - 1);
-    float v = 0.f;
-    if (h < p.g) v = load16<DT>(p.q + ((size_t)b * p.Hq + (size_t)kvh * p.g + h) * kD + c);
-    const __half hv = __float2half_rn(v);
-    qs[i] = hv;
-    qs4[i] = __hmul(hv, __float2half_rn(0.25f));
-  }
+  // ---- start this warp's page copies (its barriers are its own)
+  const int npw = pend > first ? (pend - first + kDWarps - 1) / kDWarps : 0;
+  uint8_t* wst = stages + (size_t)wid * kDStages * kBlob;
+  uint64_t* wbar = bars + wid * kDStages;
   if (lane == 0) {
-    for (int st = 0; st < kDStages; ++st) mbar_init(&bars[wid * kDStages + st], 1);
+    for (int st = 0; st < kDStages; ++st) mbar_init(&wbar[st], 1);
     fence_mbar_init();
+  }
+  const uint8_t* head_base = p.pool + (size_t)kvh * kBlob;
+  const size_t page_stride = (size_t)p.Hkv * kBlob;
+  int bt_base = 0;
+  uint32_t valid_mask = 0;  // bit st: stage st holds a valid page
+  auto issue = [&](int i) {
+    if (i - bt_base >= 32) {
+      bt_base = i;
+      bt_cache = (i + lane < npw) ? bt[first + (i + lane) * kDWarps] : -1;
+    }
+    const int pid = __shfl_sync(0xFFFFFFFFu, bt_cache, i - bt_base);
+    const int st = i % kDStages;
+    const bool ok = pid >= 0 && pid < p.pool_pages;
+    if (lane == 0) {
+      if (ok) {
+        mbar_arrive_expect_tx(&wbar[st], (uint32_t)kBlob);
+        bulk_g2s(wst + (size_t)st * kBlob, head_base + (size_t)pid * page_stride, (uint32_t)kBlob,
+                 &wbar[st]);
+      } else {
+        set_status(p.d_status, KITTY_ST_BAD_PAGE);
+        mbar_arrive(&wbar[st]);
+      }
+    }
+    valid_mask = ok ? (valid_mask | (1u << st)) : (valid_mask & ~(1u << st));
+  };
+  const int pro = min(npw, kDStages);
+  for (int i = 0; i < pro; ++i) issue(i);
+  // the tail rows are read after the pages: start pulling them into L2 now
+  if (pbeg == 0 && tl > 0 && tid == 0) {
+    const size_t off = ((size_t)b * p.Hkv + kvh) * kPage * kD;
+    l2_prefetch(p.tail_k + off, (uint32_t)tl * kD * 2);
+    l2_prefetch(p.tail_v + off, (uint32_t)tl * kD * 2);
+  }
+
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    const __half hv = __float2half_rn(qv[h]);
+    qs[h * kD + tid] = hv;
+    qs4[h * kD + tid] = __hmul(hv, __float2half_rn(0.25f));
   }
   __syncthreads();
 
@@ -436,39 +534,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   for (int i = 0; i < 4; ++i) w.vm[i] = 0.f;
   w.m = kNegBig;
   w.l = 0.f;
-
-  // ---- this warp's pages: pbeg + wid + kDWarps*i, i < npw
-  const int first = pbeg + wid;
-  const int npw = pend > first ? (pend - first + kDWarps - 1) / kDWarps : 0;
-  uint8_t* wst = stages + (size_t)wid * kDStages * kBlob;
-  uint64_t* wbar = bars + wid * kDStages;
-  const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
-  const uint8_t* head_base = p.pool + (size_t)kvh * kBlob;
-  const size_t page_stride = (size_t)p.Hkv * kBlob;
-  int bt_cache = -1, bt_base = -64;
-  uint32_t valid_mask = 0;  // bit st: stage st holds a valid page
-  auto issue = [&](int i) {
-    if (i - bt_base >= 32) {
-      bt_base = i;
-      bt_cache = (i + lane < npw) ? bt[first + (i + lane) * kDWarps] : -1;
-    }
-    const int pid = __shfl_sync(0xFFFFFFFFu, bt_cache, i - bt_base);
-    const int st = i % kDStages;
-    const bool ok = pid >= 0 && pid < p.pool_pages;
-    if (lane == 0) {
-      if (ok) {
-        mbar_arrive_expect_tx(&wbar[st], (uint32_t)kBlob);
-        bulk_g2s(wst + (size_t)st * kBlob, head_base + (size_t)pid * page_stride, (uint32_t)kBlob,
-                 &wbar[st]);
-      } else {
-        set_status(p.d_status, KITTY_ST_BAD_PAGE);
-        mbar_arrive(&wbar[st]);
-      }
-    }
-    valid_mask = ok ? (valid_mask | (1u << st)) : (valid_mask & ~(1u << st));
-  };
-  const int pro = min(npw, kDStages);
-  for (int i = 0; i < pro; ++i) issue(i);
+  bool timed_out = false;
   const uint32_t stage0 = smem_u32(wst);
   // Pages are taken two at a time: two independent score chains, one joint max
   // and rescale, then both PVs.  A missing or invalid page is masked (score -inf).
@@ -484,6 +550,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       if (it > 64) __nanosleep(32);
     }
     if (!__all_sync(0xFFFFFFFFu, done)) {
+      timed_out = true;
       // give up: report, then wait (bounded) for every copy still in flight
       if (lane == 0) {
         set_status(p.d_status, KITTY_ST_TIMEOUT);
@@ -537,7 +604,9 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     if (i + kDStages < npw) issue(i + kDStages);
     if (i + 1 + kDStages < npw) issue(i + 1 + kDStages);
   }
-  if (s == 0 && tl > 0) tail_tokens<DT>(w, p, qs, b, kvh, tl, wid, L);
+  // the tail tokens go with the sequence's first split (dispatched earliest);
+  // they reuse the stage buffers, which are idle unless a copy timed out
+  if (pbeg == 0 && tl > 0 && !timed_out) tail_tokens<DT>(w, p, qs, b, kvh, tl, wid, L, wst);
 
   // ---- merge the 4 warps: per-warp (m, l, O) to shared memory, then per channel
   w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 4);
@@ -600,28 +669,26 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
 }
 
 // Merge the split partials of one (sequence, query head); 128 threads = channels.
-__global__ void __launch_bounds__(kD) combine_kernel(const float* __restrict__ ws,
-                                                     const int32_t* num_pages, int max_pages,
-                                                     int chunk, int splits, int Hq, void* out,
-                                                     int out_dtype, int32_t* d_status) {
-  const int bh = blockIdx.x, b = bh / Hq, c = threadIdx.x;
-  int np = num_pages[b];
-  if (np < 0 || np > max_pages) np = 0;
-  const int n_act = max(1, (np + chunk - 1) / chunk);
-  const float* base = ws + (size_t)bh * splits * kPartial;
+__global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
+  const int bh = blockIdx.x, b = bh / p.Hq, c = threadIdx.x;
+  int np = p.num_pages[b];
+  if (np < 0 || np > p.max_pages) np = 0;
+  const float* base = p.ws + (size_t)bh * p.splits * kPartial;
   float ms = -INFINITY;
-  for (int s = 0; s < n_act; ++s) ms = fmaxf(ms, base[s * kPartial]);
+  for (int s = 0; s < p.splits; ++s)
+    if (split_active(p, s, np)) ms = fmaxf(ms, base[s * kPartial]);
   float L = 0.f, O = 0.f;
   if (ms != -INFINITY) {
-    for (int s = 0; s < n_act; ++s) {
+    for (int s = 0; s < p.splits; ++s) {
+      if (!split_active(p, s, np)) continue;
       const float m = base[s * kPartial];
       const float e = m == -INFINITY ? 0.f : ex2(m - ms);
       L += base[s * kPartial + 1] * e;
       O += base[s * kPartial + 2 + c] * e;
     }
   }
-  store_out(out, out_dtype, (size_t)bh * kD + c, L > 0.f ? O / L : 0.f);
-  if (c == 0 && !(L > 0.f)) set_status(d_status, KITTY_ST_EMPTY);
+  store_out(p.out, p.out_dtype, (size_t)bh * kD + c, L > 0.f ? O / L : 0.f);
+  if (c == 0 && !(L > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
 }
 
 template <int DT, int NX>
@@ -662,26 +729,91 @@ int sm_count() {
   return n;
 }
 
-// Split-K plan: enough CTAs for ~3 waves of 4 resident CTAs per SM, at least
-// 16 pages (4 per warp) per split unless the sequence is shorter.
-void plan(const kitty_cfg* cfg, int B, int max_pages, int* splits, int* chunk) {
-  int ch = cfg->decode_pages_per_split;
-  if (ch <= 0) {
-    const long units = (long)B * cfg->num_kv_heads;
-    const long target = 3L * sm_count() * 4;
-    const long want = units > 0 ? (target + units - 1) / units : 1;
-    long c = (max_pages + want - 1) / (want > 0 ? want : 1);
-    if (c < 16) c = 16;
-    c = (c + kDWarps - 1) / kDWarps * kDWarps;
-    ch = (int)c;
-  }
-  const int sp = max_pages > 0 ? (max_pages + ch - 1) / ch : 1;
-  *splits = sp < 1 ? 1 : sp;
-  *chunk = ch;
-}
-
 size_t decode_smem(int blob) {
   return (size_t)kDWarps * kDStages * blob + kDWarps * kDStages * sizeof(uint64_t) + 2 * 4 * kD * 2;
+}
+
+// CTAs of the decode kernel resident at once on the device: kDMinBlocks per SM
+// unless shared memory allows fewer (large n_hi).
+long resident_ctas(int blob) {
+  int dev = 0, smem_sm = 0;
+  int per_sm = kDMinBlocks;
+  if (cudaGetDevice(&dev) == cudaSuccess &&
+      cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
+      smem_sm > 0) {
+    const long fit = (long)smem_sm / (long)(decode_smem(blob) + 1024);
+    per_sm = (int)std::max(1L, std::min<long>(per_sm, fit));
+  }
+  return (long)sm_count() * per_sm;
+}
+
+struct Schedule {
+  int splits;     // splits per sequence
+  int largest;    // pages in the largest split
+  int32_t starts[kMaxSplits + 1];
+};
+
+// Split sizes, in dispatch order, for `units` (sequence, kv head) pairs of up to
+// M pages on `slots` resident CTAs.
+//  * fixed > 0: splits of `fixed` pages (raised to ceil(M / kMaxSplits) if that
+//    is larger), the remainder last.
+//  * fixed = 0: sizes that shrink towards the end of the grid.  Built from the
+//    last split backwards: the last split has m pages, and each earlier one is
+//    at most rho = units / slots times the pages that follow it, so a CTA
+//    dispatched in round s finishes no later than the work still queued behind
+//    it (rounded down to 8 pages; at least m).  The first split takes what is
+//    left; if that is smaller than the second, the two are merged and halved.
+//    m starts at 16 pages (2 pairs per warp) and doubles if more than
+//    kMaxSplits splits would be needed.
+void plan(const kitty_cfg* cfg, int B, int M, int blob, Schedule* sc) {
+  int sz[kMaxSplits];
+  int n = 0;
+  if (M <= 0) {
+    sz[n++] = 0;
+  } else if (cfg->decode_pages_per_split > 0) {
+    const int c = std::max(cfg->decode_pages_per_split, (M + kMaxSplits - 1) / kMaxSplits);
+    const int k = (M + c - 1) / c;
+    for (int i = 0; i < k; ++i) sz[n++] = i == k - 1 ? M - (k - 1) * c : c;
+  } else {
+    const double rho = (double)B * cfg->num_kv_heads / (double)resident_ctas(blob);
+    long T = 0;
+    for (int m = 16;; m *= 2) {
+      n = 0;
+      T = 0;
+      long c = m;
+      while (T < M && n < kMaxSplits) {
+        sz[n++] = (int)c;
+        T += c;
+        c = std::max<long>(m, (long)(rho * (double)T) / 8 * 8);
+      }
+      if (T >= M) break;
+    }
+    std::reverse(sz, sz + n);
+    sz[0] -= (int)(T - M);
+    if (n > 1 && sz[0] < sz[1]) {
+      const int tot = sz[0] + sz[1];
+      const int h = (tot / 2 + 7) / 8 * 8;
+      if (h >= tot) {
+        sz[0] = tot;
+        for (int i = 1; i + 1 < n; ++i) sz[i] = sz[i + 1];
+        --n;
+      } else {
+        sz[0] = h;
+        sz[1] = tot - h;
+      }
+    }
+  }
+  sc->splits = n;
+  sc->largest = 0;
+  sc->starts[0] = 0;
+  for (int i = 0; i < n; ++i) {
+    sc->starts[i + 1] = sc->starts[i] + sz[i];
+    sc->largest = std::max(sc->largest, sz[i]);
+  }
+}
+
+size_t workspace_bytes(const kitty_cfg* cfg, int B, const Schedule& sc) {
+  return sc.splits > 1 ? (size_t)B * cfg->num_q_heads * sc.splits * kPartial * sizeof(float) : 0;
 }
 
 }  // namespace
@@ -691,10 +823,10 @@ extern "C" int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pa
   int rc = check_cfg(cfg, true);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !splits || !pages_per_split) return KITTY_ERR_INVALID_ARG;
-  int sp, ch;
-  plan(cfg, B, max_pages, &sp, &ch);
-  *splits = sp;
-  *pages_per_split = ch;
+  Schedule sc;
+  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi), &sc);
+  *splits = sc.splits;
+  *pages_per_split = sc.largest;
   return KITTY_OK;
 }
 
@@ -703,9 +835,9 @@ extern "C" int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int
   int rc = check_cfg(cfg, true);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !bytes) return KITTY_ERR_INVALID_ARG;
-  int sp, ch;
-  plan(cfg, B, max_pages, &sp, &ch);
-  *bytes = sp > 1 ? (size_t)B * cfg->num_q_heads * sp * kPartial * sizeof(float) : 0;
+  Schedule sc;
+  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi), &sc);
+  *bytes = workspace_bytes(cfg, B, sc);
   return KITTY_OK;
 }
 
@@ -714,7 +846,7 @@ extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const
                                       int32_t max_pages, const int32_t* num_pages,
                                       const void* tail_k, const void* tail_v,
                                       const int32_t* tail_len, float sm_scale, void* out,
-                                      int32_t out_dtype, void* workspace, size_t workspace_bytes,
+                                      int32_t out_dtype, void* workspace, size_t workspace_bytes_in,
                                       int32_t B, int32_t* d_status, void* stream) {
   int rc = check_cfg(cfg, true);
   if (rc != KITTY_OK) return rc;
@@ -725,14 +857,17 @@ extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const
   if (B > 65535) return KITTY_ERR_UNSUPPORTED;
   if (!q || !out || !num_pages || (max_pages > 0 && (!block_table || !pool)) ||
       (pool && !aligned16(pool)) || ((tail_k == nullptr) != (tail_v == nullptr)) ||
+      (tail_k && (!aligned16(tail_k) || !aligned16(tail_v))) ||
       (tail_k && !tail_len) || !std::isfinite(sm_scale))
     return KITTY_ERR_INVALID_ARG;
-  int sp, ch;
-  plan(cfg, B, max_pages, &sp, &ch);
-  size_t need = sp > 1 ? (size_t)B * cfg->num_q_heads * sp * kPartial * sizeof(float) : 0;
-  if (workspace_bytes < need || (need > 0 && (!workspace || !aligned16(workspace))))
+  const int blob = (int)blob_bytes(cfg->n_hi);
+  DecodeParams p = {};
+  Schedule sc;
+  plan(cfg, B, max_pages, blob, &sc);
+  const size_t need = workspace_bytes(cfg, B, sc);
+  if (workspace_bytes_in < need || (need > 0 && (!workspace || !aligned16(workspace))))
     return KITTY_ERR_WORKSPACE;
-  DecodeParams p;
+  for (int i = 0; i <= sc.splits; ++i) p.starts[i] = sc.starts[i];
   p.q = static_cast<const uint16_t*>(q);
   p.pool = static_cast<const uint8_t*>(pool);
   p.block_table = block_table;
@@ -747,23 +882,21 @@ extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const
   p.pool_pages = pool_pages;
   p.max_pages = max_pages;
   p.out_dtype = out_dtype;
-  p.splits = sp;
-  p.chunk = ch;
+  p.splits = sc.splits;
   p.Hkv = cfg->num_kv_heads;
   p.Hq = cfg->num_q_heads;
   p.g = cfg->num_q_heads / cfg->num_kv_heads;
   p.n_hi = cfg->n_hi;
-  p.blob = (int)blob_bytes(cfg->n_hi);
+  p.blob = blob;
   p.in_dtype = cfg->in_dtype;
   const size_t smem = decode_smem(p.blob);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid(sp, cfg->num_kv_heads, B);
+  dim3 grid((unsigned)B * cfg->num_kv_heads, sc.splits);
   const cudaError_t e = cfg->in_dtype == KITTY_BF16
                             ? launch_decode_nx<KITTY_BF16>(cfg->n_hi / 16, grid, smem, s, p)
                             : launch_decode_nx<KITTY_F16>(cfg->n_hi / 16, grid, smem, s, p);
   if (e != cudaSuccess) return KITTY_ERR_CUDA;
-  if (sp > 1)
-    combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p.ws, num_pages, max_pages, ch, sp, cfg->num_q_heads, out, out_dtype, d_status);
+  if (sc.splits > 1) combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p);
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
 }
 

@@ -56,6 +56,12 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
                : "memory");
 }
 
+// Start pulling [ptr, ptr + bytes) into L2 (no completion to wait for);
+// ptr 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void l2_prefetch(const void* ptr, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(ptr), "r"(bytes) : "memory");
+}
+
 __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }

@@ -96,8 +96,15 @@ def test_null_arguments_rejected_before_launch(K):
 def test_decode_plan_and_workspace(K):
     cfg = K.Config(num_kv_heads=8, num_q_heads=32)
     s, c = K.decode_plan(cfg, 16, 128)
-    assert s * c >= 128 and c % 4 == 0 and c >= 16
+    assert 1 <= s <= 256 and s * c >= 128 and c % 8 == 0 and c >= 16
     assert K.decode_workspace_bytes(cfg, 16, 128) == (16 * 32 * s * 130 * 4 if s > 1 else 0)
+    for B, M in ((1, 4096), (177, 256), (4096, 256), (1, 3), (64, 65536)):
+        s, c = K.decode_plan(cfg, B, M)
+        assert 1 <= s <= 256 and c <= M and s * c >= M, (B, M, s, c)
+    assert K.decode_plan(cfg, 5, 0)[0] == 1
     cfg.decode_pages_per_split = 1000
-    assert K.decode_plan(cfg, 16, 128) == (1, 1000)
+    assert K.decode_plan(cfg, 16, 128) == (1, 128)
     assert K.decode_workspace_bytes(cfg, 16, 128) == 0
+    cfg.decode_pages_per_split = 4
+    assert K.decode_plan(cfg, 16, 128) == (32, 4)
+    assert K.decode_plan(cfg, 16, 4096) == (256, 16)

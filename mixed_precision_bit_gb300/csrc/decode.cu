@@ -636,34 +636,55 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     MLw[4 + qq] = w.l;
   }
   __syncthreads();
+  // per channel c: every warp's (m, l) and its O and Value-minima columns of c,
+  // read as 16-byte vectors; warps are combined in order 0..3
   const int c = tid;
   const int G = c >> 5;
   const float* m0 = reinterpret_cast<const float*>(dsm);
-  for (int h = 0; h < p.g; ++h) {
-    float ms = -INFINITY;
+  float mm[kDWarps][4], e[kDWarps][4], ms[4], Lsum[4], Osum[4];
 #pragma unroll
-    for (int ww = 0; ww < kDWarps; ++ww) ms = fmaxf(ms, m0[ww * kMergeFloats + kD * 8 + 32 + h]);
-    float Lsum = 0.f, Osum = 0.f;
-    if (ms != -INFINITY) {
+  for (int ww = 0; ww < kDWarps; ++ww) {
+    const float4 v = *reinterpret_cast<const float4*>(m0 + ww * kMergeFloats + kD * 8 + 32);
+    mm[ww][0] = v.x; mm[ww][1] = v.y; mm[ww][2] = v.z; mm[ww][3] = v.w;
+  }
 #pragma unroll
-      for (int ww = 0; ww < kDWarps; ++ww) {
-        const float* base = m0 + ww * kMergeFloats;
-        const float mwv = base[kD * 8 + 32 + h];
-        const float e = mwv == -INFINITY ? 0.f : ex2(mwv - ms);
-        Lsum += base[kD * 8 + 32 + 4 + h] * e;
-        const float o = base[c * 8 + 2 * h] + base[c * 8 + 2 * h + 1] + base[kD * 8 + G * 8 + 2 * h] +
-                        base[kD * 8 + G * 8 + 2 * h + 1];
-        Osum += o * e;
-      }
+  for (int h = 0; h < 4; ++h) {
+    ms[h] = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kDWarps; ++ww) ms[h] = fmaxf(ms[h], mm[ww][h]);
+    Lsum[h] = 0.f;
+    Osum[h] = 0.f;
+  }
+#pragma unroll
+  for (int ww = 0; ww < kDWarps; ++ww) {
+    const float* base = m0 + ww * kMergeFloats;
+    const float4 l4 = *reinterpret_cast<const float4*>(base + kD * 8 + 36);
+    const float4 o0 = *reinterpret_cast<const float4*>(base + c * 8);
+    const float4 o1 = *reinterpret_cast<const float4*>(base + c * 8 + 4);
+    const float4 v0 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8);
+    const float4 v1 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8 + 4);
+    const float lw[4] = {l4.x, l4.y, l4.z, l4.w};
+    const float o[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+    const float vmv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      e[ww][h] = (ms[h] == -INFINITY || mm[ww][h] == -INFINITY) ? 0.f : ex2(mm[ww][h] - ms[h]);
+      Lsum[h] += lw[h] * e[ww][h];
+      Osum[h] += (o[2 * h] + o[2 * h + 1] + vmv[2 * h] + vmv[2 * h + 1]) * e[ww][h];
     }
+  }
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    if (h >= p.g) break;
     const int hq = kvh * p.g + h;
     if (p.splits == 1) {
-      store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c, Lsum > 0.f ? Osum / Lsum : 0.f);
-      if (c == 0 && !(Lsum > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
+      store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c,
+                Lsum[h] > 0.f ? Osum[h] / Lsum[h] : 0.f);
+      if (c == 0 && !(Lsum[h] > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
     } else {
       float* part = p.ws + (((size_t)b * p.Hq + hq) * p.splits + s) * kPartial;
-      part[2 + c] = Osum;
-      if (c == 0) { part[0] = ms; part[1] = Lsum; }
+      part[2 + c] = Osum[h];
+      if (c == 0) { part[0] = ms[h]; part[1] = Lsum[h]; }
     }
   }
 }

@@ -277,14 +277,32 @@ def run_kitty(args, rank, world, local_rank):
     fl_dev = torch.from_numpy(np.stack(plans)).cuda()
     splits, chunk = kitty.decode_plan(cfg, B, layers[0].max_pages)
     stream = torch.cuda.current_stream()
+    # CUDA graphs: per input set and layer, one graph for the append and one for
+    # the decode call (the per-layer events stay outside the graphs); the step's
+    # flush ids are copied into one fixed buffer first
+    fl_st = torch.full((L, B), -1, dtype=torch.int32, device="cuda")
+    graphs = None
+    if args.graphs:
+        layers[0].attend(q_all[0, 0], out[0])   # first launch outside any capture
+        torch.cuda.synchronize()
+        graphs = [[lc.capture(kn_all[st, l], vn_all[st, l], fl_st[l], q_all[st, l], out[l])
+                   for l, lc in enumerate(layers)] for st in range(nsets)]
 
     def step(s, events=None):
         st = s % nsets
+        if graphs:
+            fl_st.copy_(fl_dev[s])
         for l, lc in enumerate(layers):
-            lc.append(kn_all[st, l], vn_all[st, l], fl_dev[s, l])
+            if graphs:
+                graphs[st][l][0].replay()
+            else:
+                lc.append(kn_all[st, l], vn_all[st, l], fl_dev[s, l])
             if events is not None:
                 events[l][0].record(stream)
-            lc.attend(q_all[st, l], out[l])
+            if graphs:
+                graphs[st][l][1].replay()
+            else:
+                lc.attend(q_all[st, l], out[l])
             if events is not None:
                 events[l][1].record(stream)
 
@@ -321,6 +339,9 @@ def run_kitty(args, rank, world, local_rank):
     dq, dk, dv = torch.empty_like(q_all[0]), torch.empty_like(kn_all[0]), torch.empty_like(vn_all[0])
     hfl = torch.empty((L, B), dtype=torch.int32).pin_memory()
     dfl = torch.empty((L, B), dtype=torch.int32, device="cuda")
+    e2e_graphs = None
+    if args.graphs:
+        e2e_graphs = [lc.capture(dk[l], dv[l], dfl[l], dq[l], out[l]) for l, lc in enumerate(layers)]
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -332,8 +353,12 @@ def run_kitty(args, rank, world, local_rank):
         dv.copy_(hv, non_blocking=True)
         dfl.copy_(hfl, non_blocking=True)
         for l, lc in enumerate(layers):
-            lc.append(dk[l], dv[l], dfl[l])
-            lc.attend(dq[l], out[l])
+            if e2e_graphs:
+                e2e_graphs[l][0].replay()
+                e2e_graphs[l][1].replay()
+            else:
+                lc.append(dk[l], dv[l], dfl[l])
+                lc.attend(dq[l], out[l])
         hout.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
     e2e_s = dist_max(time.perf_counter() - w0, world)
@@ -501,6 +526,8 @@ def main():
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--graphs", type=int, default=1,
+                    help="replay each layer's append and decode call as CUDA graphs (0: direct calls)")
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences in the oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--measure-quantize", type=int, default=1,
@@ -555,7 +582,9 @@ def main():
         "data": "synthetic (seeded, on device): K ~ N(0,1)*lognormal channel scales, V,Q ~ N(0,1), bf16",
         "config": config_block(spec, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "splits": r["splits"], "pages_per_split": r["chunk"],
-                                      "pool_bytes": r["pool_bytes"]}),
+                                      "pool_bytes": r["pool_bytes"],
+                                      "launch": ("CUDA graphs: one per layer for append, one for "
+                                                 "decode" if args.graphs else "direct calls")}),
         "hbm_gbs": {"decode_kernel": achieved,
                     "step_average": world * step_bytes * K / (r["ms"] / 1e3) / 1e9 / world,
                     "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,

@@ -97,6 +97,18 @@ class LayerCache:
         self.h_pages[full] += 1
         return fl
 
+    def capture(self, k_new, v_new, flush_ids, q, out, sm_scale=None):
+        """CUDA graphs of one append(k_new, v_new, flush_ids) and one attend(q, out)
+        on these tensors: replaying a graph runs the call on what the tensors hold
+        then, on the current stream.  Returns (append_graph, attend_graph).
+        Capturing runs nothing; the cache state changes only on replay."""
+        ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+        with torch.cuda.graph(ga):
+            self.append(k_new, v_new, flush_ids)
+        with torch.cuda.graph(gd):
+            self.attend(q, out, sm_scale)
+        return ga, gd
+
     def append(self, k_new, v_new, flush_ids, stream=None):
         kitty.append_token(self.cfg, k_new, v_new, self.tail_k, self.tail_v, self.tail_len,
                            self.run_sum, self.run_sumsq, self.run_count, flush_ids,

@@ -32,6 +32,7 @@
 #include "host_common.h"
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <mutex>
 
@@ -714,9 +715,18 @@ __global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
 
 template <int DT, int NX>
 cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
-  cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, NX>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
+  // the shared-memory opt-in is a per-device function attribute (smem is fixed
+  // per instantiation): set it on the first launch on each device only
+  static std::atomic<uint64_t> opted_in{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit == 0 || (opted_in.load() & bit) == 0) {
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, NX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    opted_in.fetch_or(bit);
+  }
   decode_kernel<DT, NX><<<grid, kDThreads, smem, s>>>(p);
   return cudaGetLastError();
 }

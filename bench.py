@@ -258,7 +258,7 @@ def run_kitty(args, rank, world, local_rank):
     kitty.load()
     K, W = args.steps, args.warmup
     E = max(1, min(K, args.e2e_steps))
-    steps_total = W + K + E
+    steps_total = W + K + E + 1   # + one untimed end-to-end step
     spec = workload_spec(args.workload, steps_total)
     if args.layers:
         spec["layers"] = args.layers
@@ -273,7 +273,10 @@ def run_kitty(args, rank, world, local_rank):
     plans, algo = [], []
     for s in range(W + K):
         plans.append(np.stack([lc.plan_flush() for lc in layers]))
-        algo.append([lc.algorithmic_bytes() for lc in layers])
+        # bytes of the timed call: the decode call, or the fused append + decode
+        algo.append([lc.algorithmic_bytes() + (lc.append_bytes(plans[-1][l], fused=True)
+                                               if args.fused else 0)
+                     for l, lc in enumerate(layers)])
     fl_dev = torch.from_numpy(np.stack(plans)).cuda()
     splits, chunk = kitty.decode_plan(cfg, B, layers[0].max_pages)
     stream = torch.cuda.current_stream()
@@ -285,22 +288,30 @@ def run_kitty(args, rank, world, local_rank):
     if args.graphs:
         layers[0].attend(q_all[0, 0], out[0])   # first launch outside any capture
         torch.cuda.synchronize()
-        graphs = [[lc.capture(kn_all[st, l], vn_all[st, l], fl_st[l], q_all[st, l], out[l])
-                   for l, lc in enumerate(layers)] for st in range(nsets)]
+        if args.fused:
+            graphs = [[(None, lc.capture_step(kn_all[st, l], vn_all[st, l], fl_st[l], q_all[st, l],
+                                              out[l]))
+                       for l, lc in enumerate(layers)] for st in range(nsets)]
+        else:
+            graphs = [[lc.capture(kn_all[st, l], vn_all[st, l], fl_st[l], q_all[st, l], out[l])
+                       for l, lc in enumerate(layers)] for st in range(nsets)]
 
     def step(s, events=None):
         st = s % nsets
         if graphs:
             fl_st.copy_(fl_dev[s])
         for l, lc in enumerate(layers):
-            if graphs:
-                graphs[st][l][0].replay()
-            else:
-                lc.append(kn_all[st, l], vn_all[st, l], fl_dev[s, l])
+            if not args.fused:
+                if graphs:
+                    graphs[st][l][0].replay()
+                else:
+                    lc.append(kn_all[st, l], vn_all[st, l], fl_dev[s, l])
             if events is not None:
                 events[l][0].record(stream)
             if graphs:
                 graphs[st][l][1].replay()
+            elif args.fused:
+                lc.step(kn_all[st, l], vn_all[st, l], fl_dev[s, l], q_all[st, l], out[l])
             else:
                 lc.attend(q_all[st, l], out[l])
             if events is not None:
@@ -340,13 +351,13 @@ def run_kitty(args, rank, world, local_rank):
     hfl = torch.empty((L, B), dtype=torch.int32).pin_memory()
     dfl = torch.empty((L, B), dtype=torch.int32, device="cuda")
     e2e_graphs = None
-    if args.graphs:
+    if args.graphs and args.fused:
+        e2e_graphs = [(None, lc.capture_step(dk[l], dv[l], dfl[l], dq[l], out[l]))
+                      for l, lc in enumerate(layers)]
+    elif args.graphs:
         e2e_graphs = [lc.capture(dk[l], dv[l], dfl[l], dq[l], out[l]) for l, lc in enumerate(layers)]
-    torch.cuda.synchronize()
-    if world > 1:
-        torch.distributed.barrier()
-    w0 = time.perf_counter()
-    for s in range(E):
+
+    def e2e_step():
         hfl.numpy()[:] = np.stack([lc.plan_flush() for lc in layers])
         dq.copy_(hq, non_blocking=True)
         dk.copy_(hk, non_blocking=True)
@@ -354,13 +365,24 @@ def run_kitty(args, rank, world, local_rank):
         dfl.copy_(hfl, non_blocking=True)
         for l, lc in enumerate(layers):
             if e2e_graphs:
-                e2e_graphs[l][0].replay()
+                if e2e_graphs[l][0] is not None:
+                    e2e_graphs[l][0].replay()
                 e2e_graphs[l][1].replay()
+            elif args.fused:
+                lc.step(dk[l], dv[l], dfl[l], dq[l], out[l])
             else:
                 lc.append(dk[l], dv[l], dfl[l])
                 lc.attend(dq[l], out[l])
         hout.copy_(out, non_blocking=True)
         torch.cuda.current_stream().synchronize()
+
+    e2e_step()   # untimed: the first replay of freshly captured graphs uploads them
+    torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    w0 = time.perf_counter()
+    for s in range(E):
+        e2e_step()
     e2e_s = dist_max(time.perf_counter() - w0, world)
     status = [int(lc.status.item()) for lc in layers]
     if any(status):
@@ -372,7 +394,8 @@ def run_kitty(args, rank, world, local_rank):
     return dict(spec=spec, cfg=cfg, ms=ms, K=K, W=W, E=E, dec_ms=dec_ms, dec_bytes=dec_bytes,
                 quantize=quant,
                 clocks=clk, e2e_s=e2e_s, h2d=h2d, d2h=d2h, splits=splits, chunk=chunk,
-                gpu_launches=K * L * (2 + launches_per_call), max_pages=layers[0].max_pages,
+                gpu_launches=K * L * (2 if args.fused else 2 + launches_per_call),
+                max_pages=layers[0].max_pages,
                 pool_bytes=sum(lc.pool.numel() for lc in layers))
 
 
@@ -526,6 +549,8 @@ def main():
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--fused", type=int, default=1,
+                    help="one fused append + decode call per layer (0: append, then decode)")
     ap.add_argument("--graphs", type=int, default=1,
                     help="replay each layer's append and decode call as CUDA graphs (0: direct calls)")
     ap.add_argument("--cpu-sample", type=int, default=16, help="sequences in the oracle sample")
@@ -583,8 +608,9 @@ def main():
         "config": config_block(spec, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "splits": r["splits"], "pages_per_split": r["chunk"],
                                       "pool_bytes": r["pool_bytes"],
-                                      "launch": ("CUDA graphs: one per layer for append, one for "
-                                                 "decode" if args.graphs else "direct calls")}),
+                                      "launch": ("fused append + decode per layer" if args.fused
+                                                 else "append, then decode, per layer") +
+                                                (", CUDA graphs" if args.graphs else ", direct calls")}),
         "hbm_gbs": {"decode_kernel": achieved,
                     "step_average": world * step_bytes * K / (r["ms"] / 1e3) / 1e9 / world,
                     "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,
@@ -593,7 +619,9 @@ def main():
                      "frac": achieved / hbm_peak,
                      "traffic": (traffic_ratio * dec_bytes
                                  if traffic_ratio is not None and spec["name"] == "budget" else None),
-                     "kernel": "kitty_decode_attention (decode_kernel + split combine)",
+                     "kernel": ("kitty_append_decode (decode_kernel with the append fused in + "
+                                "split combine)" if args.fused else
+                                "kitty_decode_attention (decode_kernel + split combine)"),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src,
                      "algorithmic_bytes_per_launch": dec_bytes,
                      "avg_launch_ms": dec_s * 1e3},

@@ -188,6 +188,25 @@ int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const void* pool
                            void* workspace, size_t workspace_bytes, int32_t B, int32_t* d_status,
                            void* stream);
 
+/* One decode step of a layer in one launch (plus the split combine): exactly
+ * kitty_append_token followed by kitty_decode_attention on the updated cache,
+ * with the same arguments, layouts, workspace size and status codes as those
+ * two calls.  The new token goes into the tail; a sequence whose tail fills
+ * and whose flush_page_ids entry is a page id gets that page quantized from
+ * its tail (paper: Abstract, page-centric layout; VeloxQuant-MLX docs, Decode
+ * phase steps 1-3) and attended from on-chip memory in the same launch; block
+ * table, page counts and tail lengths are updated after every head has read
+ * the old ones.  Invalid lengths (KITTY_ST_BAD_LEN) append nothing.
+ *   tail_k, tail_v device [B][Hkv][32][128], 16-byte aligned (required here)
+ *   workspace      >= kitty_decode_workspace_bytes(cfg, B, max_pages) */
+int kitty_append_decode(const kitty_cfg* cfg, const void* k_new, const void* v_new, const void* q,
+                        void* tail_k, void* tail_v, int32_t* tail_len, float* run_sum,
+                        float* run_sumsq, int32_t* run_count, const int32_t* flush_page_ids,
+                        int32_t* block_table, int32_t max_pages, int32_t* num_pages, void* pool,
+                        int32_t pool_pages, float sm_scale, void* out, int32_t out_dtype,
+                        void* workspace, size_t workspace_bytes, int32_t B, int32_t* d_status,
+                        void* stream);
+
 /* Decode attention that allocates nothing and takes no workspace.  The paper has
  * no counterpart: this entry point exists for callers that cannot allocate
  * device memory while they run -- e.g. a serving process that reserved all of

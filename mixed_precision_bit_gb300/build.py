@@ -26,7 +26,7 @@ def _nvcc():
 
 
 def _sources():
-    return [os.path.join(CSRC, f) for f in CU + CPP + ["kitty_common.cuh", "host_common.h"]] + [
+    return [os.path.join(CSRC, f) for f in CU + CPP + ["kitty_common.cuh", "quant_tile.cuh", "host_common.h"]] + [
         os.path.join(INCLUDE, "kitty.h")]
 
 

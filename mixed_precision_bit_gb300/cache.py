@@ -97,6 +97,23 @@ class LayerCache:
         self.h_pages[full] += 1
         return fl
 
+    def step(self, k_new, v_new, flush_ids, q, out, sm_scale=None, stream=None):
+        """append(k_new, v_new, flush_ids) then attend(q, out) as one fused launch
+        (plus the split combine)."""
+        sm = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+        kitty.append_decode(self.cfg, k_new, v_new, q, self.tail_k, self.tail_v, self.tail_len,
+                            self.run_sum, self.run_sumsq, self.run_count, flush_ids,
+                            self.block_table, self.num_pages, self.pool, self.pool_pages, sm, out,
+                            workspace=self.workspace, status=self.status, stream=stream)
+
+    def capture_step(self, k_new, v_new, flush_ids, q, out, sm_scale=None):
+        """A CUDA graph of one fused step(k_new, v_new, flush_ids, q, out) on these
+        tensors (see capture)."""
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            self.step(k_new, v_new, flush_ids, q, out, sm_scale)
+        return g
+
     def capture(self, k_new, v_new, flush_ids, q, out, sm_scale=None):
         """CUDA graphs of one append(k_new, v_new, flush_ids) and one attend(q, out)
         on these tensors: replaying a graph runs the call on what the tensors hold
@@ -120,6 +137,18 @@ class LayerCache:
         kitty.decode_attention(self.cfg, q, self.pool, self.pool_pages, self.block_table,
                                self.num_pages, self.tail_k, self.tail_v, self.tail_len, sm, out,
                                workspace=self.workspace, status=self.status, stream=stream)
+
+    def append_bytes(self, flush_ids, fused: bool = False) -> int:
+        """Bytes one append must move: the new K/V token read and written into the
+        tail and, per flushed (sequence, kv head), the full tail read, the page blob
+        written and the running statistics read and written.  fused: the flushed
+        page is attended from on-chip memory, so the read of it that
+        algorithmic_bytes counts is taken off here."""
+        Hkv = self.cfg.num_kv_heads
+        nf = int((np.asarray(flush_ids) >= 0).sum())
+        stats = 2 * 2 * D * 4 + 2 * 4 if self.run_sum is not None else 0
+        page = PAGE * D * 2 * 2 + self.blob + stats - (self.blob if fused else 0)
+        return self.B * Hkv * D * 2 * 2 * 2 + nf * Hkv * page
 
     def algorithmic_bytes(self) -> int:
         """Bytes one decode call must move: packed pages + tails + Q + O + block

@@ -29,6 +29,7 @@
 // code * 2^(2*tau - 24); the power of two depends only on the tile row and is
 // folded into the score scale (Keys) or the final output (Values).
 #include "kitty_common.cuh"
+#include "quant_tile.cuh"
 #include "host_common.h"
 
 #include <algorithm>
@@ -49,7 +50,27 @@ constexpr int kMaxSplits = 256;            // splits per sequence, at most
 // Running-max floor (log2 units): finite, so masked scores (-inf) give p = 0 exactly.
 constexpr float kNegBig = -1.0e30f;
 
+// Fused append (kitty_append_decode): the new token of every (sequence, kv
+// head), written into the tail by that pair's split-0 CTA, which also quantizes
+// a full tail into the caller's page.  k_new == nullptr: plain decode.
+struct AppendParams {
+  const uint16_t* k_new;  // [B][Hkv][128]
+  const uint16_t* v_new;
+  uint16_t* tail_k;       // the decode's tail_k / tail_v, writable
+  uint16_t* tail_v;
+  int32_t* tail_len;
+  int32_t* num_pages;
+  int32_t* block_table;
+  float* run_sum;         // running statistics (running or sequence mode), else null
+  float* run_sumsq;
+  int32_t* run_count;
+  const int32_t* flush_page_ids;
+  uint8_t* pool;
+  int running;
+};
+
 struct DecodeParams {
+  AppendParams ap;
   const uint16_t* q;
   const uint8_t* pool;
   const int32_t* block_table;
@@ -371,8 +392,9 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const size_t off = base + (size_t)(wid + kDWarps * i) * kD;
-    kx[i] = i < nw ? *reinterpret_cast<const uint2*>(p.tail_k + off) : make_uint2(0u, 0u);
-    vx[i] = i < nw ? *reinterpret_cast<const uint2*>(p.tail_v + off) : make_uint2(0u, 0u);
+    // L2-coherent loads: a fused append wrote the newest row in this launch
+    kx[i] = i < nw ? __ldcg(reinterpret_cast<const uint2*>(p.tail_k + off)) : make_uint2(0u, 0u);
+    vx[i] = i < nw ? __ldcg(reinterpret_cast<const uint2*>(p.tail_v + off)) : make_uint2(0u, 0u);
   }
   float qv[4][4];
 #pragma unroll
@@ -427,6 +449,32 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
   }
 }
 
+// Quantize the full tail of (sequence, kv head) sh into page fid with the
+// page quantizer (running statistics updated in running mode), staging through
+// sm.  Not inlined: it runs on a flush only (one call in 32 per sequence) and
+// keeps its registers out of the attention loop.  Called by all 128 threads.
+template <int DT>
+__device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, size_t sh, int fid,
+                                        int kvh, int Hkv, int n_hi, int32_t* d_status) {
+  const int c = threadIdx.x;
+  float rs = 0.f, rq = 0.f;
+  int rc = 0;
+  if (ap.running) {
+    rs = ap.run_sum[sh * kD + c];
+    rq = ap.run_sumsq[sh * kD + c];
+    rc = ap.run_count[sh];
+  }
+  const BlobLayout lay(n_hi);
+  quantize_tile<DT>(*sm, ap.tail_k + sh * kPage * kD, ap.tail_v + sh * kPage * kD, kD, n_hi,
+                    ap.running != 0, rs, rq, rc, ap.pool + ((size_t)fid * Hkv + kvh) * lay.bytes,
+                    d_status);
+  if (ap.running) {
+    ap.run_sum[sh * kD + c] = rs;
+    ap.run_sumsq[sh * kD + c] = rq;
+    if (c == 0) ap.run_count[sh] = rc;
+  }
+}
+
 template <int DT, int NX>
 __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
@@ -449,13 +497,41 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
 #pragma unroll
   for (int h = 0; h < 4; ++h)
     qv[h] = h < p.g ? load16<DT>(p.q + ((size_t)b * p.Hq + (size_t)kvh * p.g + h) * kD + tid) : 0.f;
-  if (np < 0 || np > p.max_pages || tl < 0 || tl > kPage || (tl > 0 && p.tail_k == nullptr)) {
+  const bool lens_ok =
+      !(np < 0 || np > p.max_pages || tl < 0 || tl > kPage || (tl > 0 && p.tail_k == nullptr));
+  if (!lens_ok) {  // nothing is appended either
     if (tid == 0 && s == 0 && kvh == 0) set_status(p.d_status, KITTY_ST_BAD_LEN);
     np = 0;
     tl = 0;
   }
-  if (!split_active(p, s, np)) return;
+  if (!split_active(p, s, np)) {
+    // no pages here: mark the partials empty (the combine then needs no lengths)
+    if (tid < p.g)
+      p.ws[(((size_t)b * p.Hq + (size_t)kvh * p.g + tid) * p.splits + s) * kPartial] = -INFINITY;
+    return;
+  }
   const int pbeg = sbeg, pend = min(np, send);
+  // ---- fused append (split 0 owns the (sequence, kv head) tail)
+  int flush_id = -1;  // >= 0: quantize the full tail into this page after the page loop
+  if (p.ap.k_new != nullptr && s == 0 && lens_ok && tl == kPage) {
+    if (tid == 0) set_status(p.d_status, KITTY_ST_TAIL_FULL);
+  } else if (p.ap.k_new != nullptr && s == 0 && lens_ok) {
+    const size_t sh = (size_t)b * p.Hkv + kvh;
+    p.ap.tail_k[(sh * kPage + tl) * kD + tid] = p.ap.k_new[sh * kD + tid];
+    p.ap.tail_v[(sh * kPage + tl) * kD + tid] = p.ap.v_new[sh * kD + tid];
+    const int n = tl + 1;
+    const int fid = p.ap.flush_page_ids[b];
+    if (fid >= 0 && n < kPage) {
+      if (tid == 0) set_status(p.d_status, KITTY_ST_BAD_FLUSH);
+    } else if (fid >= 0 && np >= p.max_pages) {
+      if (tid == 0) set_status(p.d_status, KITTY_ST_TABLE_FULL);
+    } else if (fid >= p.pool_pages) {
+      if (tid == 0) set_status(p.d_status, KITTY_ST_BAD_PAGE);
+    } else if (fid >= 0) {
+      flush_id = fid;
+    }
+    tl = flush_id >= 0 ? 0 : n;  // tokens the tail holds for this call's attention
+  }
 
   uint8_t* stages = dsm;
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + kDWarps * kDStages * kBlob);
@@ -605,6 +681,29 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     if (i + kDStages < npw) issue(i + kDStages);
     if (i + 1 + kDStages < npw) issue(i + 1 + kDStages);
   }
+  if (flush_id >= 0) {
+    // the full tail becomes page flush_id (quantized in the idle stage buffers),
+    // and this CTA attends to it from shared memory: the page the finalize step
+    // appends at index np
+    __syncthreads();
+    QuantSmem* qsm = reinterpret_cast<QuantSmem*>(dsm);
+    flush_tail<DT>(qsm, p.ap, (size_t)b * p.Hkv + kvh, flush_id, kvh, p.Hkv, p.n_hi, p.d_status);
+    if (wid == 0) {
+      const uint32_t pa = smem_u32(qsm->blob);
+      float bA, bB;
+      pair_beta<NX>(pa, pa, qf, L, p.sm_log2, bA, bB);
+      float sA[4];
+      page_scores<NX>(pa, qf, qxa, L, kscale, bA, sA);
+      float pm = fmaxf(fmaxf(sA[0], sA[1]), fmaxf(sA[2], sA[3]));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
+      pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
+      rescale(w, pm);
+      uint32_t TA[4];
+      page_probs(w, sA, TA);
+      page_pv<NX>(w, pa, TA, L);
+    }
+  }
   // the tail tokens go with the sequence's first split (dispatched earliest);
   // they reuse the stage buffers, which are idle unless a copy timed out
   if (pbeg == 0 && tl > 0 && !timed_out) tail_tokens<DT>(w, p, qs, b, kvh, tl, wid, L, wst);
@@ -691,26 +790,37 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
 }
 
 // Merge the split partials of one (sequence, query head); 128 threads = channels.
+// Splits without pages left m = -inf.  In a fused append, the CTA of query
+// head 0 then does the sequence's append bookkeeping (every decode CTA has read
+// the old lengths by now).
 __global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
   const int bh = blockIdx.x, b = bh / p.Hq, c = threadIdx.x;
-  int np = p.num_pages[b];
-  if (np < 0 || np > p.max_pages) np = 0;
   const float* base = p.ws + (size_t)bh * p.splits * kPartial;
   float ms = -INFINITY;
-  for (int s = 0; s < p.splits; ++s)
-    if (split_active(p, s, np)) ms = fmaxf(ms, base[s * kPartial]);
+  for (int s = 0; s < p.splits; ++s) ms = fmaxf(ms, base[s * kPartial]);
   float L = 0.f, O = 0.f;
   if (ms != -INFINITY) {
     for (int s = 0; s < p.splits; ++s) {
-      if (!split_active(p, s, np)) continue;
       const float m = base[s * kPartial];
-      const float e = m == -INFINITY ? 0.f : ex2(m - ms);
+      if (m == -INFINITY) continue;
+      const float e = ex2(m - ms);
       L += base[s * kPartial + 1] * e;
       O += base[s * kPartial + 2 + c] * e;
     }
   }
   store_out(p.out, p.out_dtype, (size_t)bh * kD + c, L > 0.f ? O / L : 0.f);
   if (c == 0 && !(L > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
+  if (p.ap.k_new != nullptr && c == 0 && bh - b * p.Hq == 0)
+    append_finalize_one(b, p.ap.tail_len, p.ap.flush_page_ids, p.ap.block_table, p.max_pages,
+                        p.ap.num_pages, p.pool_pages);
+}
+
+// Fused append bookkeeping when there is no combine step (one split).
+__global__ void finalize_kernel(const DecodeParams p, int B) {
+  const int b = blockIdx.x * blockDim.x + threadIdx.x;
+  if (b < B)
+    append_finalize_one(b, p.ap.tail_len, p.ap.flush_page_ids, p.ap.block_table, p.max_pages,
+                        p.ap.num_pages, p.pool_pages);
 }
 
 template <int DT, int NX>
@@ -872,13 +982,14 @@ extern "C" int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int
   return KITTY_OK;
 }
 
-extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const void* pool,
-                                      int32_t pool_pages, const int32_t* block_table,
-                                      int32_t max_pages, const int32_t* num_pages,
-                                      const void* tail_k, const void* tail_v,
-                                      const int32_t* tail_len, float sm_scale, void* out,
-                                      int32_t out_dtype, void* workspace, size_t workspace_bytes_in,
-                                      int32_t B, int32_t* d_status, void* stream) {
+namespace {
+
+// Checks and launch shared by the plain and the fused (append + decode) calls.
+int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t pool_pages,
+              const int32_t* block_table, int32_t max_pages, const int32_t* num_pages,
+              const void* tail_k, const void* tail_v, const int32_t* tail_len, float sm_scale,
+              void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes_in, int32_t B,
+              int32_t* d_status, void* stream, const AppendParams& ap) {
   int rc = check_cfg(cfg, true);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
@@ -899,6 +1010,7 @@ extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const
   if (workspace_bytes_in < need || (need > 0 && (!workspace || !aligned16(workspace))))
     return KITTY_ERR_WORKSPACE;
   for (int i = 0; i <= sc.splits; ++i) p.starts[i] = sc.starts[i];
+  p.ap = ap;
   p.q = static_cast<const uint16_t*>(q);
   p.pool = static_cast<const uint8_t*>(pool);
   p.block_table = block_table;
@@ -927,8 +1039,62 @@ extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const
                             ? launch_decode_nx<KITTY_BF16>(cfg->n_hi / 16, grid, smem, s, p)
                             : launch_decode_nx<KITTY_F16>(cfg->n_hi / 16, grid, smem, s, p);
   if (e != cudaSuccess) return KITTY_ERR_CUDA;
-  if (sc.splits > 1) combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p);
+  if (sc.splits > 1)
+    combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p);
+  else if (ap.k_new != nullptr)
+    finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(p, B);
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const void* pool,
+                                      int32_t pool_pages, const int32_t* block_table,
+                                      int32_t max_pages, const int32_t* num_pages,
+                                      const void* tail_k, const void* tail_v,
+                                      const int32_t* tail_len, float sm_scale, void* out,
+                                      int32_t out_dtype, void* workspace, size_t workspace_bytes_in,
+                                      int32_t B, int32_t* d_status, void* stream) {
+  const AppendParams none = {};
+  return attention(cfg, q, pool, pool_pages, block_table, max_pages, num_pages, tail_k, tail_v,
+                   tail_len, sm_scale, out, out_dtype, workspace, workspace_bytes_in, B, d_status,
+                   stream, none);
+}
+
+extern "C" int kitty_append_decode(const kitty_cfg* cfg, const void* k_new, const void* v_new,
+                                   const void* q, void* tail_k, void* tail_v, int32_t* tail_len,
+                                   float* run_sum, float* run_sumsq, int32_t* run_count,
+                                   const int32_t* flush_page_ids, int32_t* block_table,
+                                   int32_t max_pages, int32_t* num_pages, void* pool,
+                                   int32_t pool_pages, float sm_scale, void* out, int32_t out_dtype,
+                                   void* workspace, size_t workspace_bytes, int32_t B,
+                                   int32_t* d_status, void* stream) {
+  int rc = check_cfg(cfg, true);
+  if (rc != KITTY_OK) return rc;
+  if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
+  if (B == 0) return KITTY_OK;
+  if (!k_new || !v_new || !tail_k || !tail_v || !tail_len || !flush_page_ids || !block_table ||
+      !num_pages || !pool)
+    return KITTY_ERR_INVALID_ARG;
+  const bool running = cfg->rank_mode != KITTY_RANK_PAGE;  // sequence mode appends as running
+  if (running && (!run_sum || !run_sumsq || !run_count)) return KITTY_ERR_INVALID_ARG;
+  AppendParams ap = {};
+  ap.k_new = static_cast<const uint16_t*>(k_new);
+  ap.v_new = static_cast<const uint16_t*>(v_new);
+  ap.tail_k = static_cast<uint16_t*>(tail_k);
+  ap.tail_v = static_cast<uint16_t*>(tail_v);
+  ap.tail_len = tail_len;
+  ap.num_pages = num_pages;
+  ap.block_table = block_table;
+  ap.run_sum = running ? run_sum : nullptr;
+  ap.run_sumsq = running ? run_sumsq : nullptr;
+  ap.run_count = running ? run_count : nullptr;
+  ap.flush_page_ids = flush_page_ids;
+  ap.pool = static_cast<uint8_t*>(pool);
+  ap.running = running ? 1 : 0;
+  return attention(cfg, q, pool, pool_pages, block_table, max_pages, num_pages, tail_k, tail_v,
+                   tail_len, sm_scale, out, out_dtype, workspace, workspace_bytes, B, d_status,
+                   stream, ap);
 }
 
 // ------------------------------------------------------------------ no-allocation variant

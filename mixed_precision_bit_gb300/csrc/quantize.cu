@@ -13,319 +13,13 @@
 // plain sequential implementation.  One CTA of 128 threads quantizes one
 // (page, kv-head): thread c owns Key channel c; thread 4t+G owns Value group G
 // of token t.
-#include "kitty_common.cuh"
+//
+// Device-side quantizer: quant_tile.cuh.
+#include "quant_tile.cuh"
 #include "host_common.h"
 
 namespace kitty {
 namespace {
-
-constexpr int kQThreads = 128;
-constexpr int kMaxBlobWords = (3072 + 9 * kD) / 4;
-
-constexpr int kRowH = kD + 8;  // 16-bit elements per staged row (16-byte pad: fewer bank conflicts)
-
-struct QuantSmem {
-  uint16_t xk[kPage][kRowH];  // raw 16-bit inputs, token-major
-  uint16_t xv[kPage][kRowH];
-  uint32_t blob[kMaxBlobWords];
-  int warp_cnt[kQThreads / 32];
-  int bad;
-};
-
-// Fixed pairwise tree over 32 values (upper half folded onto lower half, 16, 8,
-// 4, 2, 1 apart) -- the order the page bytes are defined with.
-__device__ __forceinline__ float tree32(float* a) {
-#pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
-#pragma unroll
-    for (int i = 0; i < w; ++i) a[i] = __fadd_rn(a[i], a[i + w]);
-  }
-  return a[0];
-}
-
-// sigma^2 ~ sumsq/n - (sum/n)^2, each operation rounded once.
-__device__ __forceinline__ float running_var(float sum, float sumsq, float n) {
-  const float a = __fdiv_rn(sumsq, n);
-  const float b = __fdiv_rn(sum, n);
-  return __fsub_rn(a, __fmul_rn(b, b));
-}
-
-struct QuantParams {
-  float M, u, ru;  // stored minimum and step as fp32, approximate 1/u
-  uint16_t Sbits, Mbits;
-};
-
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
-
-// Asymmetric min/max group quantizer: fp16 minimum and step, codes computed
-// against the stored values; boosted Key channels store 4x the 4-bit step.
-__device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, bool boosted) {
-  QuantParams q;
-  const __half Mh = __float2half_rn(mn);
-  q.M = __half2float(Mh);
-  q.Mbits = __half_as_ushort(Mh);
-  const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
-  if (boosted) {
-    const __half Sh = __float2half_rn(__fmul_rn(4.0f, s));
-    q.Sbits = __half_as_ushort(Sh);
-    q.u = __fmul_rn(__half2float(Sh), 0.25f);
-  } else {
-    const __half Sh = __float2half_rn(s);
-    q.Sbits = __half_as_ushort(Sh);
-    q.u = __half2float(Sh);
-  }
-  q.ru = rcp_approx(q.u);
-  return q;
-}
-
-// code = clamp(rint(fl((x - M) / u)), 0, L), bit-exact with an IEEE division.
-// The quotient is taken as (x - M) * (1/u), within 2^-21 relative of the true
-// value; where that lands within 2^-15 of a rounding tie (and inside the clamp
-// range) the correctly rounded division decides.  u == 0 gives code 0.
-__device__ __forceinline__ uint32_t qcode(float x, const QuantParams& q, int levels) {
-  if (q.u == 0.0f) return 0u;
-  const float d = __fsub_rn(x, q.M);
-  const float y = __fmul_rn(d, q.ru);
-  float n = rintf(y);
-  if (fabsf(fabsf(__fsub_rn(y, n)) - 0.5f) < 0x1p-15f && y > -1.5f && y < (float)levels + 1.5f)
-    n = rintf(__fdiv_rn(d, q.u));
-  n = fminf(fmaxf(n, 0.0f), (float)levels);
-  return (uint32_t)n;
-}
-
-// Largest |16-bit input| class in a 32-bit word pair: 0 ok, RANGE, NONFINITE.
-template <int DT>
-__device__ __forceinline__ int range_class(uint32_t w) {
-  const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
-  const uint32_t m = lo > hi ? lo : hi;
-  if (DT == KITTY_BF16) return m >= 0x7F80u ? KITTY_ST_NONFINITE : (m >= 0x4780u ? KITTY_ST_RANGE : 0);
-  return m >= 0x7C00u ? KITTY_ST_NONFINITE : 0;  // fp16 finite values never exceed 65504
-}
-
-// Order-preserving key of an fp32 variance (larger var -> larger key), with
-// -0 == +0 as in a float comparison.
-__device__ __forceinline__ uint32_t var_key(float v) {
-  const uint32_t b = __float_as_uint(v + 0.0f);
-  return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
-}
-
-// Top-k boost flag of channel threadIdx.x: true iff fewer than n_hi channels have
-// a larger variance, or an equal variance and a lower index.  The n_hi-th
-// largest key T is found by a bitwise threshold search; ties at T go to the
-// lowest channels.  Called by all 128 threads.
-__device__ __forceinline__ bool topk_flag(QuantSmem& sm, float var, int n_hi) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (n_hi >= kD) return true;
-  if (n_hi <= 0) return false;
-  const uint32_t key = var_key(var);
-  uint32_t T = 0u;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    if (__syncthreads_count(key >= cand) >= n_hi) T = cand;
-  }
-  const int n_gt = __syncthreads_count(key > T);
-  const bool tie = key == T;
-  const uint32_t tb = __ballot_sync(0xFFFFFFFFu, tie);
-  if (lane == 0) sm.warp_cnt[warp] = __popc(tb);
-  __syncthreads();
-  int tie_rank = __popc(tb & ((1u << lane) - 1u));
-  for (int w = 0; w < warp; ++w) tie_rank += sm.warp_cnt[w];
-  __syncthreads();
-  return key > T || (tie && tie_rank < n_hi - n_gt);
-}
-
-// Tree-ordered sum and sum of squares of Key channel threadIdx.x over one
-// page's 32 tokens (ksrc at token 0, token t at +t*row_stride); stages only K.
-template <int DT>
-__device__ void tile_stats(QuantSmem& sm, const uint16_t* ksrc, size_t row_stride, float& s1,
-                           float& s2) {
-  const int tid = threadIdx.x;
-#pragma unroll
-  for (int it = 0; it < kPage * (kD / 8) / kQThreads; ++it) {
-    const int idx = tid + it * kQThreads;
-    const int t = idx >> 4, ch = (idx & 15) * 8;
-    *reinterpret_cast<uint4*>(&sm.xk[t][ch]) =
-        *reinterpret_cast<const uint4*>(ksrc + (size_t)t * row_stride + ch);
-  }
-  __syncthreads();
-  float a[kPage], b[kPage];
-#pragma unroll
-  for (int t = 0; t < kPage; ++t) {
-    a[t] = bits16_to_f32(sm.xk[t][tid], DT);
-    b[t] = __fmul_rn(a[t], a[t]);
-  }
-  s1 = tree32(a);
-  s2 = tree32(b);
-  __syncthreads();
-}
-
-// Quantize one (page, kv-head).  ksrc/vsrc point at token 0 of the tile; token t
-// is at +t*row_stride elements.  rsum/rsq/rcount: running accumulators of
-// channel `threadIdx.x` (running mode only).  Writes the blob to dst.
-// fixed: -1 ranks this page (page or running statistics); 0 / 1 imposes the
-// channel's boost flag (sequence-wide ranking), skipping the statistics.
-template <int DT>
-__device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_t* vsrc,
-                              size_t row_stride, int n_hi, bool running, float& rsum, float& rsq,
-                              int& rcount, uint8_t* dst, int32_t* d_status, int fixed = -1) {
-  const int tid = threadIdx.x;
-  const int lane = tid & 31, warp = tid >> 5;
-  const BlobLayout lay(n_hi);
-  const int nwords = lay.bytes / 4;
-  if (tid == 0) sm.bad = 0;
-  for (int i = tid; i < nwords; i += kQThreads) sm.blob[i] = 0u;
-
-  // ---- stage the raw 16-bit tile (16-byte loads and stores), classify the range
-  int bad = 0;
-#pragma unroll
-  for (int it = 0; it < kPage * (kD / 8) / kQThreads; ++it) {
-    const int idx = tid + it * kQThreads;
-    const int t = idx >> 4, ch = (idx & 15) * 8;
-    const uint4 a = *reinterpret_cast<const uint4*>(ksrc + (size_t)t * row_stride + ch);
-    const uint4 b = *reinterpret_cast<const uint4*>(vsrc + (size_t)t * row_stride + ch);
-    *reinterpret_cast<uint4*>(&sm.xk[t][ch]) = a;
-    *reinterpret_cast<uint4*>(&sm.xv[t][ch]) = b;
-    const int c = max(max(max(range_class<DT>(a.x), range_class<DT>(a.y)),
-                          max(range_class<DT>(a.z), range_class<DT>(a.w))),
-                      max(max(range_class<DT>(b.x), range_class<DT>(b.y)),
-                          max(range_class<DT>(b.z), range_class<DT>(b.w))));
-    bad = max(bad, c);
-  }
-  __syncthreads();  // tile staged; sm.bad reset by thread 0 is visible
-  if (bad) atomicCAS(&sm.bad, 0, bad);
-
-  // ---- Key channel statistics and variance (thread = channel c)
-  const int c = tid;
-  float x[kPage], tmp[kPage];
-#pragma unroll
-  for (int t = 0; t < kPage; ++t) x[t] = bits16_to_f32(sm.xk[t][c], DT);
-  float mn = x[0], mx = x[0];
-#pragma unroll
-  for (int t = 1; t < kPage; ++t) {
-    mn = fminf(mn, x[t]);
-    mx = fmaxf(mx, x[t]);
-  }
-  float var = 0.f;
-  if (fixed < 0) {
-#pragma unroll
-    for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
-    const float s1 = tree32(tmp);
-#pragma unroll
-    for (int t = 0; t < kPage; ++t) tmp[t] = __fmul_rn(x[t], x[t]);
-    const float s2 = tree32(tmp);
-    if (running) {
-      rsum = __fadd_rn(rsum, s1);
-      rsq = __fadd_rn(rsq, s2);
-      rcount += kPage;
-      var = running_var(rsum, rsq, __int2float_rn(rcount));
-    } else {
-      var = running_var(s1, s2, (float)kPage);
-    }
-  }
-
-  // ---- top-k (or the caller's fixed boost set)
-  const bool boosted = fixed >= 0 ? (fixed != 0) : topk_flag(sm, var, n_hi);
-  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, boosted);
-  if (lane == 0) sm.warp_cnt[warp] = __popc(bal);
-  __syncthreads();
-  int row = __popc(bal & ((1u << lane) - 1u));
-  for (int w = 0; w < warp; ++w) row += sm.warp_cnt[w];
-
-  // ---- Key quantization of channel c and packing in fragment order
-  {
-    const int levels = boosted ? 15 : 3;
-    const QuantParams q = qparams(mn, mx, levels, boosted);
-    uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
-    b16[lay.ks / 2 + c] = q.Sbits;
-    // minima in fragment order: channel 16j + 8h + 2qq + e at ((qq*8 + j)*2 + h)*2 + e
-    b16[lay.km / 2 + (((((c >> 1) & 3) * 8 + (c >> 4)) * 2 + ((c >> 3) & 1)) * 2 + (c & 1))] = q.Mbits;
-    uint32_t code[kPage];
-#pragma unroll
-    for (int t = 0; t < kPage; ++t) code[t] = qcode(x[t], q, levels);
-    const int j = c >> 4, half = (c >> 3) & 1, qq = (c >> 1) & 3, e = c & 1;
-    const int bitbase = 16 * e + 8 * half;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int tau = 0; tau < 4; ++tau) {
-        const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
-        const uint32_t cb = boosted ? (code[t] >> 2) : code[t];
-        w |= cb << (bitbase + 2 * tau);
-      }
-      atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 8 + j], w);
-    }
-    if (boosted) {
-      const int wpl = n_hi / 16;
-      const int js = row >> 4, hx = (row >> 3) & 1, qx = (row >> 1) & 3, ex = row & 1;
-      const int bx = 16 * ex + 8 * hx;
-#pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        uint32_t w = 0;
-#pragma unroll
-        for (int tau = 0; tau < 4; ++tau) {
-          const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
-          w |= (code[t] & 3u) << (bx + 2 * tau);
-        }
-        atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w);
-      }
-      // channel-list row 16js + 8h + 2qq + e stored at byte js*16 + qq*4 + h*2 + e
-      const int pos = lay.kch + js * 16 + qx * 4 + hx * 2 + ex;
-      atomicOr(&sm.blob[pos / 4], (uint32_t)c << (8 * (pos & 3)));
-    }
-  }
-
-  // ---- Value quantization: thread 4t+G owns token t, channels 32G..32G+31
-  {
-    const int t = tid >> 2, G = tid & 3;
-    float v[kVGroup];
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const uint4 w4 = *reinterpret_cast<const uint4*>(&sm.xv[t][G * kVGroup + 8 * k]);
-      const uint32_t ww[4] = {w4.x, w4.y, w4.z, w4.w};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        v[8 * k + 2 * i] = bits16_to_f32((uint16_t)(ww[i] & 0xFFFFu), DT);
-        v[8 * k + 2 * i + 1] = bits16_to_f32((uint16_t)(ww[i] >> 16), DT);
-      }
-    }
-    float vmn = v[0], vmx = v[0];
-#pragma unroll
-    for (int i = 1; i < kVGroup; ++i) { vmn = fminf(vmn, v[i]); vmx = fmaxf(vmx, v[i]); }
-    const QuantParams q = qparams(vmn, vmx, 3, false);
-    uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
-    // Value metadata in fragment order: token 16kt + 8h + 2qq + e at G*32 + qq*8 + kt*4 + h*2 + e
-    const int vpos = G * kPage + ((t >> 1) & 3) * 8 + (t >> 4) * 4 + ((t >> 3) & 1) * 2 + (t & 1);
-    b16[lay.vs / 2 + vpos] = q.Sbits;
-    b16[lay.vm / 2 + vpos] = q.Mbits;
-    const int qq = (t >> 1) & 3, kt = t >> 4, half = (t >> 3) & 1, e = t & 1;
-    const int bitbase = 16 * e + 8 * half;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int odd = 0; odd < 2; ++odd) {
-#pragma unroll
-        for (int rh = 0; rh < 2; ++rh) {
-          const int i = odd * 16 + rh * 8 + r;  // channel 32G + i has mc = 2G + odd
-          w |= qcode(v[i], q, 3) << (bitbase + 2 * (2 * odd + rh));
-        }
-      }
-      atomicOr(&sm.blob[lay.vbase / 4 + (4 * r + qq) * 8 + G * 2 + kt], w);
-    }
-  }
-  __syncthreads();
-
-  uint4* d4 = reinterpret_cast<uint4*>(dst);
-  const uint4* s4 = reinterpret_cast<const uint4*>(sm.blob);
-  for (int i = tid; i < lay.bytes / 16; i += kQThreads) d4[i] = s4[i];
-  if (tid == 0 && sm.bad) set_status(d_status, sm.bad);
-  __syncthreads();
-}
 
 // Page mode: one CTA per (input page i, kv head h).
 template <int DT>
@@ -493,18 +187,7 @@ __global__ void append_finalize_kernel(int32_t* tail_len, const int32_t* flush_p
                                        int pool_pages, int B) {
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
-  const int len = tail_len[b];
-  if (len < 0 || len >= kPage) return;
-  const int n = len + 1;
-  const int fid = flush_page_ids[b];
-  const int np = num_pages[b];
-  if (n == kPage && fid >= 0 && np >= 0 && np < max_pages && fid < pool_pages) {
-    block_table[(size_t)b * max_pages + np] = fid;
-    num_pages[b] = np + 1;
-    tail_len[b] = 0;
-  } else {
-    tail_len[b] = n;
-  }
+  append_finalize_one(b, tail_len, flush_page_ids, block_table, max_pages, num_pages, pool_pages);
 }
 
 }  // namespace

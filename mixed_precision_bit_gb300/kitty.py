@@ -60,7 +60,7 @@ EXPORTS = ("kitty_abi_version", "kitty_page_bytes", "kitty_avg_bits", "kitty_all
            "kitty_alloc_pages", "kitty_free_pages", "kitty_alloc_free_count",
            "kitty_alloc_destroy", "kitty_quantize_pages", "kitty_append_token",
            "kitty_decode_workspace_bytes", "kitty_decode_attention", "kitty_decode_plan",
-           "kitty_decode_attention_noalloc")
+           "kitty_decode_attention_noalloc", "kitty_append_decode")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -93,6 +93,8 @@ def load():
                                                       ctypes.c_float, P, i32, P, sz, i32, P, P]),
             "kitty_decode_attention_noalloc": (ctypes.c_int, [C, P, P, i32, P, i32, P, P, P, P,
                                                               ctypes.c_float, P, i32, i32, P, P]),
+            "kitty_append_decode": (ctypes.c_int, [C, P, P, P, P, P, P, P, P, P, P, P, i32, P, P, i32,
+                                                   ctypes.c_float, P, i32, P, sz, i32, P, P]),
             "kitty_decode_plan": (ctypes.c_int, [C, i32, i32, ctypes.POINTER(i32),
                                                  ctypes.POINTER(i32)]),
         }
@@ -235,3 +237,20 @@ def decode_attention_noalloc(cfg: Config, q, pool, pool_pages: int, block_table,
         ctypes.byref(cfg.c()), _ptr(q), _ptr(pool), pool_pages, _ptr(block_table),
         block_table.shape[1], _ptr(num_pages), _ptr(tail_k), _ptr(tail_v), _ptr(tail_len),
         float(sm_scale), _ptr(out), out_dtype, B, _ptr(status), _stream(stream)))
+
+
+def append_decode(cfg: Config, k_new, v_new, q, tail_k, tail_v, tail_len, run_sum, run_sumsq,
+                  run_count, flush_page_ids, block_table, num_pages, pool, pool_pages: int,
+                  sm_scale: float, out, workspace=None, status=None, stream=None, out_dtype=None):
+    """append_token followed by decode_attention, as one fused launch."""
+    import torch
+    B = tail_len.numel()
+    if out_dtype is None:
+        out_dtype = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}[out.dtype]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _chk("kitty_append_decode", load().kitty_append_decode(
+        ctypes.byref(cfg.c()), _ptr(k_new), _ptr(v_new), _ptr(q), _ptr(tail_k), _ptr(tail_v),
+        _ptr(tail_len), _ptr(run_sum), _ptr(run_sumsq), _ptr(run_count), _ptr(flush_page_ids),
+        _ptr(block_table), block_table.shape[1], _ptr(num_pages), _ptr(pool), pool_pages,
+        float(sm_scale), _ptr(out), out_dtype, _ptr(workspace), ws_bytes, B, _ptr(status),
+        _stream(stream)))

@@ -493,7 +493,7 @@ def profiled_traffic_ratio():
         return None
     vals = dict(re.findall(r"^\s*(\w+) = (\w+)\s*$", text, re.M))
     srcs = [os.path.join(ROOT, "mixed_precision_bit_gb300", "csrc", f)
-            for f in ("decode.cu", "kitty_common.cuh")]
+            for f in ("decode.cu", "kitty_common.cuh", "quant_tile.cuh")]
     sha = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
     if vals.get("kernel_source_sha256_16") != sha:
         return None

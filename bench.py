@@ -49,8 +49,11 @@ def workload_spec(name: str, steps_total: int):
     """Shapes of the benchmark workloads (one GPU)."""
     import numpy as np
     from mixed_precision_bit_gb300 import synth
-    if name in ("budget", "budget_uniform"):
-        n_hi = 32 if name == "budget" else 0
+    if name in ("budget", "budget_uniform", "budget_k4"):
+        # budget: Kitty (top 32 of 128 Key channels at 4 bits, running statistics);
+        # budget_uniform: every Key channel at 2 bits; budget_k4: every Key channel
+        # at 4 bits (n_hi = 128, two 2-bit planes).  Values are 2-bit in all three.
+        n_hi = {"budget": 32, "budget_uniform": 0, "budget_k4": 128}[name]
         running = name == "budget"
         blob = 3072 + 9 * n_hi
         Hkv, Hq, layers, ctx_pages = 8, 32, 32, 256
@@ -544,7 +547,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kitty", choices=["kitty", "reference"])
     ap.add_argument("--workload", default="budget",
-                    choices=["budget", "budget_uniform", "llama3_8b", "qwen3_8b", "long", "tiny"])
+                    choices=["budget", "budget_uniform", "budget_k4", "llama3_8b", "qwen3_8b", "long",
+                             "tiny"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")

@@ -2,8 +2,9 @@
 //
 // A plain, slow, single-source C++17 restatement of what the Kitty hot path
 // computes: per-page channel statistics, variance ranking with a top-k boost
-// set, asymmetric min/max quantization of Keys (2-bit, boosted channels 4-bit
-// split into two 2-bit planes) and Values (2-bit per-token groups of 32
+// set, asymmetric min/max quantization of Keys (lo_bit codes; boosted channels
+// hi_bit = 2*lo_bit, split into two uniform lo_bit planes; (hi_bit, lo_bit) =
+// (4, 2) by default or (8, 4)) and Values (2-bit per-token groups of 32
 // channels), the packed page format, the append/flush step, and fp64 decode
 // attention over the dequantized pages.
 //
@@ -21,7 +22,9 @@
 //    How it works / Prefill phase steps 1-3 (per-channel variance, top
 //    hi_fraction*D channels at hi_bit, asymmetric min/max groups of group_size
 //    tokens), Decode phase step 2 (running variance formula), Effective
-//    bit-width, Configuration reference.
+//    bit-width, Configuration reference, Tuning avg_bits (the (0.25, 8, 4) row:
+//    8-bit boosted and 4-bit other Key channels; Values keep their 2-bit
+//    format -- the table concerns Keys only, a reading).
 //  * PagedAttention / FlashAttention (cited by the paper) for the block table
 //    and softmax attention semantics.
 // Readings where the pages are silent are stated next to the code that takes
@@ -103,23 +106,26 @@ uint16_t f32_to_f16(float f) {
 float in_to_f32(uint16_t v, int dtype) { return dtype == 1 ? bf16_to_f32(v) : f16_to_f32(v); }
 
 // ---------------------------------------------------------------- page format
+// The Key planes are w bits wide: w = lo_bit, and hi_bit = 2*w (a boosted code
+// splits into two w-bit halves).  w = 2 is the paper's (4, 2) configuration,
+// w = 4 the (8, 4) row of the avg_bits table.
 // Byte layout of one (page, kv-head) blob, n_hi a multiple of 16 in [0, 128]:
-//   Kbase  1024 B   2-bit codes, all D channels x 32 tokens
-//   Kextra n_hi*8 B 2-bit low halves of the boosted channels' 4-bit codes
-//   KS     256 B    fp16 step per channel, channel order (boosted: the base-plane step)
-//   KM     256 B    fp16 minimum per channel, at km_pos(c)
-//   Kch    n_hi B   boosted channel ids; row j of Kextra (the j-th smallest
-//                   boosted channel) is stored at byte kch_pos(j)
-//   Vbase  1024 B   2-bit codes, 32 tokens x D channels
-//   VS     256 B    fp16 step per (group, token), at vmeta_pos(G, t)
-//   VM     256 B    fp16 minimum per (group, token), at vmeta_pos(G, t)
+//   Kbase  128*w B    w-bit codes, all D channels x 32 tokens (high halves of boosted codes)
+//   Kextra n_hi*4*w B w-bit low halves of the boosted channels' 2w-bit codes
+//   KS     256 B      fp16 step per channel, channel order (boosted: the base-plane step)
+//   KM     256 B      fp16 minimum per channel, at km_pos(c)
+//   Kch    n_hi B     boosted channel ids; row j of Kextra (the j-th smallest
+//                     boosted channel) is stored at byte kch_pos(j)
+//   Vbase  1024 B     2-bit codes, 32 tokens x D channels
+//   VS     256 B      fp16 step per (group, token), at vmeta_pos(G, t)
+//   VM     256 B      fp16 minimum per (group, token), at vmeta_pos(G, t)
 struct Layout {
-  int n_hi;
+  int n_hi, w;
   size_t kbase, kextra, ks, km, kch, vbase, vs, vm, bytes;
-  explicit Layout(int nh) : n_hi(nh) {
+  Layout(int nh, int w_) : n_hi(nh), w(w_) {
     kbase = 0;
-    kextra = 1024;
-    ks = kextra + (size_t)nh * 8;
+    kextra = (size_t)D * P * w / 8;
+    ks = kextra + (size_t)nh * P * w / 8;
     km = ks + 256;
     kch = km + 256;
     vbase = kch + (size_t)nh;
@@ -146,6 +152,23 @@ BitPos key_pos(int col, int t, int words_per_lane) {
   const int tau = 2 * mt + rh;
   const int lane = 4 * r + qq;
   return {lane * words_per_lane + ks, 16 * e + 8 * half + 2 * tau};
+}
+
+// 4-bit Key planes, same fragment order with nibbles: a lane holds two words
+// per 16-column tile (one per 16-token block mt), and inside a word element
+// (row, col) sits at bit 16*(col parity) + 8*(col half) + 4*(row's 8-row half).
+// words_per_lane = 2 * (columns / 16).
+BitPos key_pos4(int col, int t, int words_per_lane) {
+  const int ks = col >> 4, cc = col & 15;
+  const int half = cc >> 3, qq = (cc & 7) >> 1, e = cc & 1;
+  const int mt = t >> 4, rh = (t >> 3) & 1, r = t & 7;
+  const int lane = 4 * r + qq;
+  return {lane * words_per_lane + 2 * ks + mt, 16 * e + 8 * half + 4 * rh};
+}
+
+// Key code position for plane width w over `cols` columns (D or n_hi).
+BitPos kpos(int w, int col, int t, int cols) {
+  return w == 4 ? key_pos4(col, t, 2 * (cols / 16)) : key_pos(col, t, cols / 16);
 }
 
 // Value plane: row = channel c, col = token t (the transposed operand).
@@ -176,18 +199,22 @@ int kch_pos(int j) {
   return js * 16 + qq * 4 + h * 2 + e;
 }
 
-void put2(uint8_t* plane, BitPos p, uint32_t code) {
+// Write / read a `bits`-wide code at p.
+void putb(uint8_t* plane, BitPos p, uint32_t code, int bits) {
   uint32_t w;
   std::memcpy(&w, plane + 4 * p.word, 4);
-  w |= (code & 3u) << p.bit;
+  w |= (code & ((1u << bits) - 1u)) << p.bit;
   std::memcpy(plane + 4 * p.word, &w, 4);
 }
 
-uint32_t get2(const uint8_t* plane, BitPos p) {
+uint32_t getb(const uint8_t* plane, BitPos p, int bits) {
   uint32_t w;
   std::memcpy(&w, plane + 4 * p.word, 4);
-  return (w >> p.bit) & 3u;
+  return (w >> p.bit) & ((1u << bits) - 1u);
 }
+
+void put2(uint8_t* plane, BitPos p, uint32_t code) { putb(plane, p, code, 2); }
+uint32_t get2(const uint8_t* plane, BitPos p) { return getb(plane, p, 2); }
 
 uint16_t rd16(const uint8_t* p, size_t i) { uint16_t v; std::memcpy(&v, p + 2 * i, 2); return v; }
 void wr16(uint8_t* p, size_t i, uint16_t v) { std::memcpy(p + 2 * i, &v, 2); }
@@ -276,9 +303,10 @@ void top_k(const float* var, int n_hi, bool* boosted) {
 // phase step 3).  Readings: the minimum and the step are stored as fp16 and the
 // codes are computed against the STORED values, so encoder and decoder agree;
 // rounding is to nearest-even; codes are clamped to [0, 2^b - 1].  A boosted
-// Key channel stores the step of its high 2-bit plane, 4x the 4-bit step.
+// Key channel (2w-bit code) stores the step of its high w-bit plane, F = 2^w
+// times its own step (F = 4 for the (4, 2) configuration, 16 for (8, 4)).
 void quant_group(const float* x, int stride, int n, float mn, float mx, int levels,
-                 bool boosted, uint16_t* S_out, uint16_t* M_out, uint8_t* code) {
+                 bool boosted, uint16_t* S_out, uint16_t* M_out, uint16_t* code, float F = 4.0f) {
   const uint16_t M = f32_to_f16(mn);
   const float Mf = f16_to_f32(M);
   const float r = mx - mn;
@@ -286,8 +314,8 @@ void quant_group(const float* x, int stride, int n, float mn, float mx, int leve
   uint16_t S;
   float u;
   if (boosted) {
-    S = f32_to_f16(4.0f * s);
-    u = f16_to_f32(S) * 0.25f;
+    S = f32_to_f16(F * s);
+    u = f16_to_f32(S) * (1.0f / F);
   } else {
     S = f32_to_f16(s);
     u = f16_to_f32(S);
@@ -299,7 +327,7 @@ void quant_group(const float* x, int stride, int n, float mn, float mx, int leve
     float q = std::nearbyint(y);
     if (q < 0.0f) q = 0.0f;
     if (q > (float)levels) q = (float)levels;
-    code[i] = (uint8_t)q;
+    code[i] = (uint16_t)q;
   }
   *S_out = S;
   *M_out = M;
@@ -315,10 +343,10 @@ int check_range(const float* x, int n) {
 }
 
 // Encode one (page, kv-head): Key planes with the given boost set, Value
-// planes, metadata and channel list, into `blob` (Layout(n_hi).bytes bytes).
+// planes, metadata and channel list, into `blob` (Layout(n_hi, w).bytes bytes).
 void encode_blob(const float* xk, const float* xv, const PageStats& st, const bool* boosted,
-                 int n_hi, uint8_t* blob) {
-  const Layout lay(n_hi);
+                 int n_hi, int w, uint8_t* blob) {
+  const Layout lay(n_hi, w);
   std::memset(blob, 0, lay.bytes);
   uint8_t* kbase = blob + lay.kbase;
   uint8_t* kextra = blob + lay.kextra;
@@ -329,22 +357,22 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
     row_of[c] = -1;
     if (boosted[c]) { blob[lay.kch + kch_pos(j)] = (uint8_t)c; row_of[c] = j++; }
   }
-  const int xw = n_hi / 16;  // Kextra words per lane
+  const int Lw = (1 << w) - 1, Lhi = (1 << (2 * w)) - 1;
   for (int c = 0; c < D; ++c) {
     uint16_t S, M;
-    uint8_t code[P];
+    uint16_t code[P];
     const bool b = boosted[c];
-    quant_group(xk + c, D, P, st.mn[c], st.mx[c], b ? 15 : 3, b, &S, &M, code);
+    quant_group(xk + c, D, P, st.mn[c], st.mx[c], b ? Lhi : Lw, b, &S, &M, code, (float)(1 << w));
     wr16(blob + lay.ks, c, S);
     wr16(blob + lay.km, km_pos(c), M);
     for (int t = 0; t < P; ++t) {
       if (b) {
-        // 4-bit code c4 = 4*hi + lo: hi joins the uniform base plane, lo the
-        // extra plane row of this channel (two uniform 2-bit tensors).
-        put2(kbase, key_pos(c, t, 8), code[t] >> 2);
-        put2(kextra, key_pos(row_of[c], t, xw), code[t] & 3u);
+        // 2w-bit code = 2^w*hi + lo: hi joins the uniform base plane, lo the
+        // extra plane row of this channel (two uniform w-bit tensors).
+        putb(kbase, kpos(w, c, t, D), code[t] >> w, w);
+        putb(kextra, kpos(w, row_of[c], t, n_hi), code[t] & (uint32_t)Lw, w);
       } else {
-        put2(kbase, key_pos(c, t, 8), code[t]);
+        putb(kbase, kpos(w, c, t, D), code[t], w);
       }
     }
   }
@@ -354,7 +382,7 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
       float mn = x[0], mx = x[0];
       for (int i = 1; i < VG; ++i) { mn = std::min(mn, x[i]); mx = std::max(mx, x[i]); }
       uint16_t S, M;
-      uint8_t code[VG];
+      uint16_t code[VG];
       quant_group(x, 1, VG, mn, mx, 3, false, &S, &M, code);
       wr16(blob + lay.vs, vmeta_pos(g, t), S);
       wr16(blob + lay.vm, vmeta_pos(g, t), M);
@@ -366,7 +394,7 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
 // Quantize one page-head from fp32 token-major tiles xk, xv [32][D].  In
 // running mode the (sequence, head) accumulators are updated with this page's
 // sums before it is ranked; in page mode the page ranks on its own 32 tokens.
-int quantize_one(const float* xk, const float* xv, int n_hi, int running, float* rsum,
+int quantize_one(const float* xk, const float* xv, int n_hi, int w, int running, float* rsum,
                  float* rsq, int* rcount, uint8_t* blob) {
   int st = check_range(xk, P * D);
   if (st == ST_OK) st = check_range(xv, P * D);
@@ -386,7 +414,7 @@ int quantize_one(const float* xk, const float* xv, int n_hi, int running, float*
   }
   bool boosted[D];
   top_k(var, n_hi, boosted);
-  encode_blob(xk, xv, ps, boosted, n_hi, blob);
+  encode_blob(xk, xv, ps, boosted, n_hi, w, blob);
   return st;
 }
 
@@ -396,7 +424,7 @@ int quantize_one(const float* xk, const float* xv, int n_hi, int running, float*
 // accumulators end with the sequence totals (page sums added in page order).
 // xk_pages/xv_pages: the pages' fp32 tiles in order; blobs: one per page.
 int quantize_sequence(const std::vector<std::vector<float>>& xk_pages,
-                      const std::vector<std::vector<float>>& xv_pages, int n_hi, float* rsum,
+                      const std::vector<std::vector<float>>& xv_pages, int n_hi, int w, float* rsum,
                       float* rsq, int* rcount, const std::vector<uint8_t*>& blobs) {
   int st = ST_OK;
   std::vector<PageStats> ps(xk_pages.size());
@@ -416,7 +444,7 @@ int quantize_sequence(const std::vector<std::vector<float>>& xk_pages,
   bool boosted[D];
   top_k(var, n_hi, boosted);
   for (size_t p = 0; p < xk_pages.size(); ++p)
-    encode_blob(xk_pages[p].data(), xv_pages[p].data(), ps[p], boosted, n_hi, blobs[p]);
+    encode_blob(xk_pages[p].data(), xv_pages[p].data(), ps[p], boosted, n_hi, w, blobs[p]);
   return st;
 }
 
@@ -425,11 +453,11 @@ int quantize_sequence(const std::vector<std::vector<float>>& xk_pages,
 // ---------------------------------------------------------------- decode side
 namespace {
 
-// Dequantize one page-head in fp64: k = M + S*hi + [boosted]*(S/4)*lo and
+// Dequantize one page-head in fp64: k = M + S*hi + [boosted]*(S/2^w)*lo and
 // v = M + S*code, per the page format above.  Returns ST_BAD_PAGE if the
 // channel list is not a strictly ascending list of valid channel ids.
-int dequant(const uint8_t* blob, int n_hi, double* kh, double* vh) {
-  const Layout lay(n_hi);
+int dequant(const uint8_t* blob, int n_hi, int w, double* kh, double* vh) {
+  const Layout lay(n_hi, w);
   int row_of[D];
   for (int c = 0; c < D; ++c) row_of[c] = -1;
   int prev = -1;
@@ -439,13 +467,14 @@ int dequant(const uint8_t* blob, int n_hi, double* kh, double* vh) {
     row_of[ch] = j;
     prev = ch;
   }
-  const int xw = n_hi / 16;
+  const double F = (double)(1 << w);
   for (int c = 0; c < D; ++c) {
     const double S = f16_to_f32(rd16(blob + lay.ks, c));
     const double M = f16_to_f32(rd16(blob + lay.km, km_pos(c)));
     for (int t = 0; t < P; ++t) {
-      double v = M + S * (double)get2(blob + lay.kbase, key_pos(c, t, 8));
-      if (row_of[c] >= 0) v += (S / 4.0) * (double)get2(blob + lay.kextra, key_pos(row_of[c], t, xw));
+      double v = M + S * (double)getb(blob + lay.kbase, kpos(w, c, t, D), w);
+      if (row_of[c] >= 0)
+        v += (S / F) * (double)getb(blob + lay.kextra, kpos(w, row_of[c], t, n_hi), w);
       kh[t * D + c] = v;
     }
   }
@@ -460,7 +489,7 @@ int dequant(const uint8_t* blob, int n_hi, double* kh, double* vh) {
 }
 
 struct AttnArgs {
-  int Hkv, Hq, n_hi, in_dtype;
+  int Hkv, Hq, n_hi, w, in_dtype;
   const uint16_t* q;
   const uint8_t* pool;
   int pool_pages;
@@ -479,7 +508,7 @@ struct AttnArgs {
 // throughout.  out has g*D entries.
 int attend_group(const AttnArgs& a, int b, int kvh, double* out) {
   const int g = a.Hq / a.Hkv;
-  const Layout lay(a.n_hi);
+  const Layout lay(a.n_hi, a.w);
   const size_t page_stride = lay.bytes * (size_t)a.Hkv;
   const int np = a.num_pages[b];
   const int tl = a.tail_len[b];
@@ -492,7 +521,7 @@ int attend_group(const AttnArgs& a, int b, int kvh, double* out) {
     const int id = a.block_table[(size_t)b * a.max_pages + p];
     if (id < 0 || id >= a.pool_pages) return ST_BAD_PAGE;
     const uint8_t* blob = a.pool + (size_t)id * page_stride + (size_t)kvh * lay.bytes;
-    const int st = dequant(blob, a.n_hi, &kh[(size_t)p * P * D], &vh[(size_t)p * P * D]);
+    const int st = dequant(blob, a.n_hi, a.w, &kh[(size_t)p * P * D], &vh[(size_t)p * P * D]);
     if (st != ST_OK) return st;
   }
   const size_t tail_base = ((size_t)b * a.Hkv + kvh) * P * D;
@@ -525,6 +554,8 @@ int attend_group(const AttnArgs& a, int b, int kvh, double* out) {
 }
 
 bool valid_n_hi(int n_hi) { return n_hi >= 0 && n_hi <= D && n_hi % 16 == 0; }
+// Key plane width: lo_bit 2 ((hi, lo) = (4, 2)) or 4 ((8, 4)).
+bool valid_w(int w) { return w == 2 || w == 4; }
 
 }  // namespace
 
@@ -535,8 +566,10 @@ int orc_abi_version() { return 1; }
 
 void orc_set_threads(int n) { g_threads = n < 1 ? 1 : n; }
 
-// Bytes of one (page, kv-head) blob; -1 for an unsupported n_hi.
-long orc_page_bytes(int n_hi) { return valid_n_hi(n_hi) ? (long)Layout(n_hi).bytes : -1; }
+// Bytes of one (page, kv-head) blob; -1 for an unsupported n_hi or lo_bit.
+long orc_page_bytes(int n_hi, int lo_bit) {
+  return valid_n_hi(n_hi) && valid_w(lo_bit) ? (long)Layout(n_hi, lo_bit).bytes : -1;
+}
 
 // Effective Key bits per element, codes only (VeloxQuant-MLX docs, Effective
 // bit-width): hi_fraction*hi_bit + (1 - hi_fraction)*lo_bit.
@@ -562,6 +595,12 @@ void orc_key_pos(int col, int t, int words_per_lane, int* word, int* bit) {
   *bit = p.bit;
 }
 
+void orc_key_pos4(int col, int t, int words_per_lane, int* word, int* bit) {
+  const BitPos p = key_pos4(col, t, words_per_lane);
+  *word = p.word;
+  *bit = p.bit;
+}
+
 void orc_val_pos(int t, int c, int* word, int* bit) {
   const BitPos p = val_pos(t, c);
   *word = p.word;
@@ -571,14 +610,14 @@ void orc_val_pos(int t, int c, int* word, int* bit) {
 // One page-head from fp32 tiles [32][D] (token-major).  running != 0 updates
 // rsum/rsq [D] and *rcount before ranking.  Returns a status code.
 int orc_quantize_page_f32(const float* xk, const float* xv, int n_hi, int running, float* rsum,
-                          float* rsq, int* rcount, uint8_t* blob) {
-  if (!valid_n_hi(n_hi)) return -1;
-  return quantize_one(xk, xv, n_hi, running, rsum, rsq, rcount, blob);
+                          float* rsq, int* rcount, uint8_t* blob, int lo_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit)) return -1;
+  return quantize_one(xk, xv, n_hi, lo_bit, running, rsum, rsq, rcount, blob);
 }
 
 // The boosted channel list of a blob in row order (ascending channel ids).
-void orc_page_channels(const uint8_t* blob, int n_hi, int* out) {
-  const Layout lay(n_hi);
+void orc_page_channels(const uint8_t* blob, int n_hi, int* out, int lo_bit) {
+  const Layout lay(n_hi, lo_bit);
   for (int j = 0; j < n_hi; ++j) out[j] = blob[lay.kch + kch_pos(j)];
 }
 
@@ -586,8 +625,9 @@ void orc_meta_pos(int kind, int a, int b, int* pos) {
   *pos = kind == 0 ? km_pos(a) : kind == 1 ? vmeta_pos(a, b) : kch_pos(a);
 }
 
-void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int* status) {
-  *status = valid_n_hi(n_hi) ? dequant(blob, n_hi, kh, vh) : -1;
+void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int* status,
+                      int lo_bit) {
+  *status = valid_n_hi(n_hi) && valid_w(lo_bit) ? dequant(blob, n_hi, lo_bit, kh, vh) : -1;
 }
 
 // Bulk quantization with the library's semantics.  k, v: [n_pages*32][Hkv][D]
@@ -599,9 +639,10 @@ void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int
 int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint16_t* k,
                        const uint16_t* v, int n_pages, const int* page_ids, const int* seq_of_page,
                        int n_seqs, float* run_sum, float* run_sumsq, int* run_count, uint8_t* pool,
-                       int pool_pages) {
-  if (!valid_n_hi(n_hi) || Hkv <= 0 || n_pages < 0) return -1;
-  const Layout lay(n_hi);
+                       int pool_pages, int lo_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || n_pages < 0) return -1;
+  const int w = lo_bit;
+  const Layout lay(n_hi, w);
   const size_t page_stride = lay.bytes * (size_t)Hkv;
   int st = ST_OK;
   if (rank_mode == 1 || rank_mode == 2) {
@@ -638,7 +679,7 @@ int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uin
       }
       if (xk.empty()) { sts2[sh] = bad; return; }
       const size_t o = (size_t)sq * Hkv + h;
-      int r = quantize_sequence(xk, xv, n_hi, run_sum + o * D, run_sumsq + o * D, run_count + o, blobs);
+      int r = quantize_sequence(xk, xv, n_hi, w, run_sum + o * D, run_sumsq + o * D, run_count + o, blobs);
       sts2[sh] = r != ST_OK ? r : bad;
     });
     for (int x : sts2) note(&st, x);
@@ -664,7 +705,7 @@ int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uin
       rq = run_sumsq + sh * D;
       rc = run_count + sh;
     }
-    sts[(size_t)i * Hkv + h] = quantize_one(xk.data(), xv.data(), n_hi, rank_mode == 1, rs, rq, rc,
+    sts[(size_t)i * Hkv + h] = quantize_one(xk.data(), xv.data(), n_hi, w, rank_mode == 1, rs, rq, rc,
                                             pool + (size_t)id * page_stride + (size_t)h * lay.bytes);
   };
   if (rank_mode == 1) {
@@ -689,9 +730,9 @@ int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint1
                      const uint16_t* v_new, uint16_t* tail_k, uint16_t* tail_v, int* tail_len,
                      float* run_sum, float* run_sumsq, int* run_count, const int* flush_page_ids,
                      int* block_table, int max_pages, int* num_pages, uint8_t* pool, int pool_pages,
-                     int B) {
-  if (!valid_n_hi(n_hi) || Hkv <= 0 || B < 0) return -1;
-  const Layout lay(n_hi);
+                     int B, int lo_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || B < 0) return -1;
+  const Layout lay(n_hi, lo_bit);
   const size_t page_stride = lay.bytes * (size_t)Hkv;
   std::vector<int> sts(B > 0 ? B : 1, ST_OK);
   parallel_for(B, [&](int b) {
@@ -723,7 +764,7 @@ int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint1
       }
       const size_t sh = (size_t)b * Hkv + h;
       const bool running = rank_mode != 0;  // sequence mode continues with running statistics
-      note(&st, quantize_one(xk.data(), xv.data(), n_hi, running, running ? run_sum + sh * D : nullptr,
+      note(&st, quantize_one(xk.data(), xv.data(), n_hi, lo_bit, running, running ? run_sum + sh * D : nullptr,
                              running ? run_sumsq + sh * D : nullptr, running ? run_count + sh : nullptr,
                              pool + (size_t)fid * page_stride + (size_t)h * lay.bytes));
     }
@@ -742,9 +783,9 @@ int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint1
 int orc_decode_attention(int Hkv, int Hq, int n_hi, int in_dtype, const uint16_t* q,
                          const uint8_t* pool, int pool_pages, const int* block_table, int max_pages,
                          const int* num_pages, const uint16_t* tail_k, const uint16_t* tail_v,
-                         const int* tail_len, float sm_scale, int B, double* out) {
-  if (!valid_n_hi(n_hi) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B < 0) return -1;
-  const AttnArgs a{Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, max_pages,
+                         const int* tail_len, float sm_scale, int B, double* out, int lo_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B < 0) return -1;
+  const AttnArgs a{Hkv, Hq, n_hi, lo_bit, in_dtype, q, pool, pool_pages, block_table, max_pages,
                    num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
   const int g = Hq / Hkv;
   std::vector<int> sts(B > 0 ? (size_t)B * Hkv : 1, ST_OK);
@@ -763,9 +804,9 @@ int orc_decode_attention_one(int Hkv, int Hq, int n_hi, int in_dtype, const uint
                              const uint8_t* pool, int pool_pages, const int* block_table,
                              int max_pages, const int* num_pages, const uint16_t* tail_k,
                              const uint16_t* tail_v, const int* tail_len, float sm_scale, int b,
-                             int kvh, double* out) {
-  if (!valid_n_hi(n_hi) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return -1;
-  const AttnArgs a{Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, max_pages,
+                             int kvh, double* out, int lo_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return -1;
+  const AttnArgs a{Hkv, Hq, n_hi, lo_bit, in_dtype, q, pool, pool_pages, block_table, max_pages,
                    num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
   return attend_group(a, b, kvh, out);
 }

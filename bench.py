@@ -49,13 +49,16 @@ def workload_spec(name: str, steps_total: int):
     """Shapes of the benchmark workloads (one GPU)."""
     import numpy as np
     from mixed_precision_bit_gb300 import synth
-    if name in ("budget", "budget_uniform", "budget_k4"):
+    if name in ("budget", "budget_uniform", "budget_k4", "budget_84"):
         # budget: Kitty (top 32 of 128 Key channels at 4 bits, running statistics);
         # budget_uniform: every Key channel at 2 bits; budget_k4: every Key channel
-        # at 4 bits (n_hi = 128, two 2-bit planes).  Values are 2-bit in all three.
-        n_hi = {"budget": 32, "budget_uniform": 0, "budget_k4": 128}[name]
-        running = name == "budget"
-        blob = 3072 + 9 * n_hi
+        # at 4 bits (n_hi = 128, two 2-bit planes); budget_84: Kitty at (8, 4) bits
+        # (top 32 channels at 8 bits, the rest at 4, two 4-bit planes, running
+        # statistics).  Values are 2-bit in all four.
+        n_hi = {"budget": 32, "budget_uniform": 0, "budget_k4": 128, "budget_84": 32}[name]
+        lo_bit = 4 if name == "budget_84" else 2
+        running = name in ("budget", "budget_84")
+        blob = 512 * lo_bit + 4 * lo_bit * n_hi + 2048 + n_hi
         Hkv, Hq, layers, ctx_pages = 8, 32, 32, 256
         stat = Hkv * D * 2 * 4 + Hkv * 4 if running else 0
         tail_bytes = 2 * Hkv * PAGE * D * 2
@@ -63,15 +66,15 @@ def workload_spec(name: str, steps_total: int):
         tails = (synth.bits(0, "budget/tail", B) % np.uint64(32)).astype(np.int64)
         return dict(name=name, B=int(B), Hq=Hq, Hkv=Hkv, n_hi=n_hi, layers=layers,
                     running=running, pages=np.full(B, ctx_pages, np.int64), tails=tails,
-                    drift=0, budget_bytes=40 * 10 ** 9, dtype=synth.BF16)
+                    drift=0, budget_bytes=40 * 10 ** 9, dtype=synth.BF16, lo_bit=lo_bit)
     w = synth.workload(name)
     # independent layer copies, rotated every step, so the working set exceeds 4x L2
-    pool = w.total_pages * w.Hkv * (3072 + 9 * w.n_hi)
+    pool = w.total_pages * w.Hkv * (512 * w.lo_bit + 4 * w.lo_bit * w.n_hi + 2048 + w.n_hi)
     # (the tiny single-head case is latency-bound and stays L2-resident by design)
     layers = 1 if name == "tiny" else max(1, math.ceil(4 * 129e6 / max(pool, 1)))
     return dict(name=name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, n_hi=w.n_hi, layers=layers, running=False,
                 pages=w.pages.astype(np.int64), tails=w.tails.astype(np.int64), drift=w.drift,
-                budget_bytes=None, dtype=w.dtype)
+                budget_bytes=None, dtype=w.dtype, lo_bit=w.lo_bit)
 
 
 def headroom_pages(tails, steps_total):
@@ -140,7 +143,7 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
     max_pages = int(pages.max()) + head
     pool_pages = int(pages.sum()) + B * head
     cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
-                       in_dtype=spec["dtype"],
+                       in_dtype=spec["dtype"], hi_bit=2 * spec["lo_bit"], lo_bit=spec["lo_bit"],
                        rank_mode=kitty.RANK_RUNNING if spec["running"] else kitty.RANK_PAGE,
                        decode_pages_per_split=pages_per_split)
     tdt = torch.float16 if spec["dtype"] == kitty.F16 else torch.bfloat16
@@ -212,7 +215,8 @@ def measure_quantize(spec, reps=5, seed=3):
     out = {}
     for mode in (kitty.RANK_PAGE, kitty.RANK_RUNNING):
         cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
-                           in_dtype=spec["dtype"], rank_mode=mode)
+                           in_dtype=spec["dtype"], rank_mode=mode, hi_bit=2 * spec["lo_bit"],
+                           lo_bit=spec["lo_bit"])
         blob, per_page = kitty.page_bytes(cfg)
         pool = torch.empty(tot * per_page, dtype=torch.uint8, device="cuda")
         run = {}
@@ -530,6 +534,7 @@ def config_block(spec, extra=None):
                          "batch maximised" if spec["budget_bytes"] else "single decode layer"),
          "batch": spec["B"], "layers": spec["layers"], "q_heads": spec["Hq"], "kv_heads": spec["Hkv"],
          "head_dim": D, "page_tokens": PAGE, "n_hi": spec["n_hi"],
+         "key_bits": "(hi, lo) = (%d, %d)" % (2 * spec["lo_bit"], spec["lo_bit"]),
          "rank_mode": "running" if spec["running"] else "page",
          "context_pages": int(spec["pages"].max()), "kv_budget_bytes": spec["budget_bytes"],
          "l2": ("L2-resident (latency-bound tiny case, no roofline claim)" if spec["name"] == "tiny"
@@ -547,8 +552,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kitty", choices=["kitty", "reference"])
     ap.add_argument("--workload", default="budget",
-                    choices=["budget", "budget_uniform", "budget_k4", "llama3_8b", "qwen3_8b", "long",
-                             "tiny"])
+                    choices=["budget", "budget_uniform", "budget_k4", "budget_84", "llama3_8b",
+                             "qwen3_8b", "long", "tiny"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")

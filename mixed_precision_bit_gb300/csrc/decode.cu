@@ -41,7 +41,9 @@ namespace kitty {
 namespace {
 
 constexpr int kDWarps = 4;
-constexpr int kDStages = 4;
+// Page stages per warp: 4 for 2-bit Key planes; 3 for 4-bit planes, whose
+// larger blobs would otherwise allow only 2 CTAs per SM.
+__host__ __device__ constexpr int stages_for(int w) { return w == 4 ? 3 : 4; }
 constexpr int kDMinBlocks = 4;  // resident CTAs per SM the register budget is sized for
 constexpr int kDThreads = kDWarps * 32;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of one barrier phase (~0.1-1 s)
@@ -152,10 +154,11 @@ __device__ __forceinline__ void store_out(void* out, int dt, size_t i, float v) 
   else static_cast<__half*>(out)[i] = __float2half_rn(v);
 }
 
-// Compile-time blob offsets for NX = n_hi/16 extra-plane k-steps.
-template <int NX>
+// Compile-time blob offsets for NX = n_hi/16 extra-plane k-steps and Key plane
+// width W (2: (4, 2) configuration, 4: (8, 4)).
+template <int NX, int W>
 struct Off {
-  static constexpr int kx = 1024, ks = kx + 128 * NX, km = ks + 256, kch = km + 256;
+  static constexpr int kx = 512 * W, ks = kx + 64 * W * NX, km = ks + 256, kch = km + 256;
   static constexpr int vb = kch + 16 * NX, vs = vb + 1024, vm = vs + 256, bytes = vm + 256;
 };
 
@@ -203,6 +206,12 @@ __device__ __forceinline__ void unpack_rows01(uint32_t x, uint32_t* a) {  // tau
   const uint32_t x2 = x >> 8;
   a[0] = x & 0x00030003u; a[1] = x & 0x000C000Cu; a[2] = x2 & 0x00030003u; a[3] = x2 & 0x000C000Cu;
 }
+// 4-bit planes: one word is one A fragment (rows r, r+8 = nibbles 0, 1 of each
+// byte; the high byte holds the tile's columns 8..15).
+__device__ __forceinline__ void unpack_nib(uint32_t x, uint32_t* a) {
+  const uint32_t x2 = x >> 8;
+  a[0] = x & 0x000F000Fu; a[1] = x & 0x00F000F0u; a[2] = x2 & 0x000F000Fu; a[3] = x2 & 0x00F000F0u;
+}
 __device__ __forceinline__ void unpack_rows23(uint32_t x, uint32_t* a) {  // tau 2,3
   const uint32_t x2 = x >> 8;
   a[0] = x & 0x00300030u; a[1] = x & 0x00C000C0u; a[2] = x2 & 0x00300030u; a[3] = x2 & 0x00C000C0u;
@@ -212,22 +221,32 @@ __device__ __forceinline__ void unpack_rows23(uint32_t x, uint32_t* a) {  // tau
 // token 16*mt + 8*rh + r of head qq.
 //   pa: shared-space address of the staged blob
 //   qf[j][0..1]: this lane's B-fragment query pairs for k-step j (head lane/8)
-//   qxa: shared-space address of q/4 of head lane/8 (extra-plane gather)
-template <int NX>
+//   qxa: shared-space address of q/2^W of head lane/8 (extra-plane gather)
+template <int NX, int W>
 __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&qf)[8][2],
                                             const uint32_t qxa, const Lane& L,
                                             const float (&kscale)[4], float beta,
                                             float (&s)[4]) {
-  using O = Off<NX>;
+  using O = Off<NX, W>;
   const int lane = L.lane, qq = L.qq;
-  const uint32_t a_lane = pa + 32 * lane;   // this lane's 32 bytes of each code plane
-  const uint32_t a_qq = pa + 4 * qq;        // this lane's fp16 pair in each 16-wide group
+  const uint32_t a_lane = pa + 4 * W * 4 * lane;  // this lane's 16*W bytes of the base plane
+  const uint32_t a_qq = pa + 4 * qq;              // this lane's fp16 pair in each 16-wide group
 
   // ---------------- scores: base plane, q.M row, extra plane
   float cs[2][4] = {};
-  const uint4 kb0 = ld_s128<0>(a_lane);
-  const uint4 kb1 = ld_s128<16>(a_lane);
-  const uint32_t kw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+  uint32_t kw[4 * W];  // W = 2: one word per k-step; W = 4: two (16-token blocks 0, 1)
+  {
+    const uint4 kb0 = ld_s128<0>(a_lane);
+    const uint4 kb1 = ld_s128<16>(a_lane);
+    kw[0] = kb0.x; kw[1] = kb0.y; kw[2] = kb0.z; kw[3] = kb0.w;
+    kw[4] = kb1.x; kw[5] = kb1.y; kw[6] = kb1.z; kw[7] = kb1.w;
+    if (W == 4) {
+      const uint4 kb2 = ld_s128<32>(a_lane);
+      const uint4 kb3 = ld_s128<48>(a_lane);
+      kw[8 % (4 * W)] = kb2.x; kw[9 % (4 * W)] = kb2.y; kw[10 % (4 * W)] = kb2.z; kw[11 % (4 * W)] = kb2.w;
+      kw[12 % (4 * W)] = kb3.x; kw[13 % (4 * W)] = kb3.y; kw[14 % (4 * W)] = kb3.z; kw[15 % (4 * W)] = kb3.w;
+    }
+  }
 #pragma unroll
   for (int j = 0; j < 8; ++j) {
     uint32_t S0, S1;
@@ -239,19 +258,29 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
     const uint32_t b0 = hilo_mul(qf[j][0], S0, L.fneg);
     const uint32_t b1 = hilo_mul(qf[j][1], S1, L.fneg);
     uint32_t a[4];
-    unpack_rows01(kw[j], a);
-    mma_f16(cs[0], a, b0, b1);
-    unpack_rows23(kw[j], a);
-    mma_f16(cs[1], a, b0, b1);
+    if (W == 2) {
+      unpack_rows01(kw[j], a);
+      mma_f16(cs[0], a, b0, b1);
+      unpack_rows23(kw[j], a);
+      mma_f16(cs[1], a, b0, b1);
+    } else {
+      unpack_nib(kw[(2 * j) % (4 * W)], a);
+      mma_f16(cs[0], a, b0, b1);
+      unpack_nib(kw[(2 * j + 1) % (4 * W)], a);
+      mma_f16(cs[1], a, b0, b1);
+    }
   }
   if (NX > 0) {
     const uint32_t a_id = pa + 4 * qq;
-    const uint32_t a_x = pa + 4 * NX * lane;
+    const uint32_t a_x = pa + 2 * W * NX * lane;
 #pragma unroll
     for (int js = 0; js < NX; ++js) {
-      uint32_t ids, x;
+      uint32_t ids;
+      uint2 x = make_uint2(0u, 0u);  // W = 2: x.x; W = 4: x.x, x.y for 16-token blocks 0, 1
       switch (js) {  // channel-list rows 2qq, 2qq+1, 2qq+8, 2qq+9 are one word (fragment order)
-#define KITTY_KX(J) case J: ids = ld_s32<O::kch + 16 * J>(a_id); x = ld_s32<O::kx + 4 * J>(a_x); break;
+#define KITTY_KX(J) case J: ids = ld_s32<O::kch + 16 * J>(a_id); \
+                            if (W == 2) x.x = ld_s32<O::kx + 4 * J>(a_x); \
+                            else x = ld_s64<O::kx + 8 * J>(a_x); break;
         KITTY_KX(0) KITTY_KX(1) KITTY_KX(2) KITTY_KX(3) KITTY_KX(4) KITTY_KX(5) KITTY_KX(6) default: KITTY_KX(7)
 #undef KITTY_KX
       }
@@ -264,10 +293,17 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
       const uint32_t b0 = hilo_mul(q01, s01, L.fneg);
       const uint32_t b1 = hilo_mul(q23, s23, L.fneg);
       uint32_t a[4];
-      unpack_rows01(x, a);
-      mma_f16(cs[0], a, b0, b1);
-      unpack_rows23(x, a);
-      mma_f16(cs[1], a, b0, b1);
+      if (W == 2) {
+        unpack_rows01(x.x, a);
+        mma_f16(cs[0], a, b0, b1);
+        unpack_rows23(x.x, a);
+        mma_f16(cs[1], a, b0, b1);
+      } else {
+        unpack_nib(x.x, a);
+        mma_f16(cs[0], a, b0, b1);
+        unpack_nib(x.y, a);
+        mma_f16(cs[1], a, b0, b1);
+      }
     }
   }
 
@@ -281,11 +317,11 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
 // q.M bias (log2 units) of two pages with one set of one-row MMAs: B is the
 // plain query for every page, so A rows r even carry page A's Key minima and
 // odd rows page B's; each lane reads its own row and its neighbour's.
-template <int NX>
+template <int NX, int W>
 __device__ __forceinline__ void pair_beta(const uint32_t paA, const uint32_t paB,
                                           const uint32_t (&qf)[8][2], const Lane& L,
                                           float sm_log2, float& bA, float& bB) {
-  using O = Off<NX>;
+  using O = Off<NX, W>;
   // this lane's 16 minima pairs are contiguous (fragment order): 4 x 16 bytes
   const uint32_t a_m = ((L.r & 1) ? paB : paA) + 64 * L.qq;
   const uint4 m0 = ld_s128<O::km>(a_m), m1 = ld_s128<O::km + 16>(a_m);
@@ -317,10 +353,10 @@ __device__ __forceinline__ void page_probs(WarpState& w, const float (&s)[4], ui
 }
 
 // Value minima term and PV of one page with its probability fragments T.
-template <int NX>
+template <int NX, int W>
 __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const uint32_t (&T)[4],
                                         const Lane& L) {
-  using O = Off<NX>;
+  using O = Off<NX, W>;
   const int lane = L.lane, r = L.r, qq = L.qq;
   const uint32_t a_lane = pa + 32 * lane;
   const uint32_t a_q16 = pa + 16 * qq;  // this lane group's Value steps (fragment order)
@@ -453,7 +489,7 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
 // page quantizer (running statistics updated in running mode), staging through
 // sm.  Not inlined: it runs on a flush only (one call in 32 per sequence) and
 // keeps its registers out of the attention loop.  Called by all 128 threads.
-template <int DT>
+template <int DT, int W>
 __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, size_t sh, int fid,
                                         int kvh, int Hkv, int n_hi, int32_t* d_status) {
   const int c = threadIdx.x;
@@ -464,8 +500,8 @@ __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, si
     rq = ap.run_sumsq[sh * kD + c];
     rc = ap.run_count[sh];
   }
-  const BlobLayout lay(n_hi);
-  quantize_tile<DT>(*sm, ap.tail_k + sh * kPage * kD, ap.tail_v + sh * kPage * kD, kD, n_hi,
+  const BlobLayout lay(n_hi, W);
+  quantize_tile<DT, W>(*sm, ap.tail_k + sh * kPage * kD, ap.tail_v + sh * kPage * kD, kD, n_hi,
                     ap.running != 0, rs, rq, rc, ap.pool + ((size_t)fid * Hkv + kvh) * lay.bytes,
                     d_status);
   if (ap.running) {
@@ -475,7 +511,7 @@ __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, si
   }
 }
 
-template <int DT, int NX>
+template <int DT, int NX, int W>
 __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
   const int u = blockIdx.x, s = blockIdx.y;
@@ -483,7 +519,8 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   const int tid = threadIdx.x, wid = tid >> 5;
   const Lane L;
   const int lane = L.lane, r = L.r, qq = L.qq;
-  constexpr int kBlob = Off<NX>::bytes;
+  constexpr int kBlob = Off<NX, W>::bytes;
+  constexpr int kDStages = stages_for(W);
   const int sbeg = p.starts[s], send = p.starts[s + 1];
   // Independent loads first, all in flight together: the lengths, this warp's
   // first 32 block-table entries (up to the split's nominal end, which is
@@ -536,7 +573,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   uint8_t* stages = dsm;
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + kDWarps * kDStages * kBlob);
   __half* qs = reinterpret_cast<__half*>(bars + kDWarps * kDStages);  // q      [4][128]
-  __half* qs4 = qs + 4 * kD;                                          // q / 4  [4][128]
+  __half* qs4 = qs + 4 * kD;                                          // q / 2^W [4][128]
 
   // ---- start this warp's page copies (its barriers are its own)
   const int npw = pend > first ? (pend - first + kDWarps - 1) / kDWarps : 0;
@@ -583,7 +620,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   for (int h = 0; h < 4; ++h) {
     const __half hv = __float2half_rn(qv[h]);
     qs[h * kD + tid] = hv;
-    qs4[h * kD + tid] = __hmul(hv, __float2half_rn(0.25f));
+    qs4[h * kD + tid] = __hmul(hv, __float2half_rn(1.0f / (1 << W)));  // exact: power of two
   }
   __syncthreads();
 
@@ -600,7 +637,9 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   float kscale[4];
 #pragma unroll
   for (int tau = 0; tau < 4; ++tau)
-    kscale[tau] = p.sm_log2 * __uint_as_float((uint32_t)(127 + 24 - 2 * tau) << 23);
+    // a code sits at 2^(2 tau - 24) (2-bit planes) or 2^(4 (tau & 1) - 24) (4-bit)
+    kscale[tau] = p.sm_log2 *
+                  __uint_as_float((uint32_t)(127 + 24 - (W == 2 ? 2 * tau : 4 * (tau & 1))) << 23);
 
   WarpState w;
 #pragma unroll
@@ -642,13 +681,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     const uint32_t paA = stage0 + stA * kBlob;
     const uint32_t paB = hasB ? stage0 + stB * kBlob : paA;
     float bA, bB;
-    pair_beta<NX>(paA, paB, qf, L, p.sm_log2, bA, bB);
+    pair_beta<NX, W>(paA, paB, qf, L, p.sm_log2, bA, bB);
     float sA[4];
-    page_scores<NX>(paA, qf, qxa, L, kscale, bA, sA);
+    page_scores<NX, W>(paA, qf, qxa, L, kscale, bA, sA);
     if (hasB) {
       const bool vB = (valid_mask >> stB) & 1u;
       float sB[4];
-      page_scores<NX>(paB, qf, qxa, L, kscale, bB, sB);
+      page_scores<NX, W>(paB, qf, qxa, L, kscale, bB, sB);
 #pragma unroll
       for (int k = 0; k < 4; ++k) {
         sA[k] = vA ? sA[k] : -INFINITY;
@@ -663,8 +702,8 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       uint32_t TA[4], TB[4];
       page_probs(w, sA, TA);
       page_probs(w, sB, TB);
-      page_pv<NX>(w, paA, TA, L);
-      page_pv<NX>(w, paB, TB, L);
+      page_pv<NX, W>(w, paA, TA, L);
+      page_pv<NX, W>(w, paB, TB, L);
     } else {  // last page of an odd count
 #pragma unroll
       for (int k = 0; k < 4; ++k) sA[k] = vA ? sA[k] : -INFINITY;
@@ -675,7 +714,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       rescale(w, pm);
       uint32_t TA[4];
       page_probs(w, sA, TA);
-      page_pv<NX>(w, paA, TA, L);
+      page_pv<NX, W>(w, paA, TA, L);
     }
     __syncwarp();
     if (i + kDStages < npw) issue(i + kDStages);
@@ -687,13 +726,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     // appends at index np
     __syncthreads();
     QuantSmem* qsm = reinterpret_cast<QuantSmem*>(dsm);
-    flush_tail<DT>(qsm, p.ap, (size_t)b * p.Hkv + kvh, flush_id, kvh, p.Hkv, p.n_hi, p.d_status);
+    flush_tail<DT, W>(qsm, p.ap, (size_t)b * p.Hkv + kvh, flush_id, kvh, p.Hkv, p.n_hi, p.d_status);
     if (wid == 0) {
       const uint32_t pa = smem_u32(qsm->blob);
       float bA, bB;
-      pair_beta<NX>(pa, pa, qf, L, p.sm_log2, bA, bB);
+      pair_beta<NX, W>(pa, pa, qf, L, p.sm_log2, bA, bB);
       float sA[4];
-      page_scores<NX>(pa, qf, qxa, L, kscale, bA, sA);
+      page_scores<NX, W>(pa, qf, qxa, L, kscale, bA, sA);
       float pm = fmaxf(fmaxf(sA[0], sA[1]), fmaxf(sA[2], sA[3]));
       pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
       pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
@@ -701,7 +740,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       rescale(w, pm);
       uint32_t TA[4];
       page_probs(w, sA, TA);
-      page_pv<NX>(w, pa, TA, L);
+      page_pv<NX, W>(w, pa, TA, L);
     }
   }
   // the tail tokens go with the sequence's first split (dispatched earliest);
@@ -823,7 +862,7 @@ __global__ void finalize_kernel(const DecodeParams p, int B) {
                         p.ap.num_pages, p.pool_pages);
 }
 
-template <int DT, int NX>
+template <int DT, int NX, int W>
 cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
   // the shared-memory opt-in is a per-device function attribute (smem is fixed
   // per instantiation): set it on the first launch on each device only
@@ -832,27 +871,27 @@ cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodePa
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
   if (bit == 0 || (opted_in.load() & bit) == 0) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, NX>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, NX, W>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  decode_kernel<DT, NX><<<grid, kDThreads, smem, s>>>(p);
+  decode_kernel<DT, NX, W><<<grid, kDThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
-template <int DT>
+template <int DT, int W>
 cudaError_t launch_decode_nx(int nx, dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
   switch (nx) {
-    case 0: return launch_decode<DT, 0>(grid, smem, s, p);
-    case 1: return launch_decode<DT, 1>(grid, smem, s, p);
-    case 2: return launch_decode<DT, 2>(grid, smem, s, p);
-    case 3: return launch_decode<DT, 3>(grid, smem, s, p);
-    case 4: return launch_decode<DT, 4>(grid, smem, s, p);
-    case 5: return launch_decode<DT, 5>(grid, smem, s, p);
-    case 6: return launch_decode<DT, 6>(grid, smem, s, p);
-    case 7: return launch_decode<DT, 7>(grid, smem, s, p);
-    default: return launch_decode<DT, 8>(grid, smem, s, p);
+    case 0: return launch_decode<DT, 0, W>(grid, smem, s, p);
+    case 1: return launch_decode<DT, 1, W>(grid, smem, s, p);
+    case 2: return launch_decode<DT, 2, W>(grid, smem, s, p);
+    case 3: return launch_decode<DT, 3, W>(grid, smem, s, p);
+    case 4: return launch_decode<DT, 4, W>(grid, smem, s, p);
+    case 5: return launch_decode<DT, 5, W>(grid, smem, s, p);
+    case 6: return launch_decode<DT, 6, W>(grid, smem, s, p);
+    case 7: return launch_decode<DT, 7, W>(grid, smem, s, p);
+    default: return launch_decode<DT, 8, W>(grid, smem, s, p);
   }
 }
 
@@ -870,19 +909,20 @@ int sm_count() {
   return n;
 }
 
-size_t decode_smem(int blob) {
-  return (size_t)kDWarps * kDStages * blob + kDWarps * kDStages * sizeof(uint64_t) + 2 * 4 * kD * 2;
+size_t decode_smem(int blob, int w) {
+  const int st = stages_for(w);
+  return (size_t)kDWarps * st * blob + kDWarps * st * sizeof(uint64_t) + 2 * 4 * kD * 2;
 }
 
 // CTAs of the decode kernel resident at once on the device: kDMinBlocks per SM
 // unless shared memory allows fewer (large n_hi).
-long resident_ctas(int blob) {
+long resident_ctas(int blob, int w) {
   int dev = 0, smem_sm = 0;
   int per_sm = kDMinBlocks;
   if (cudaGetDevice(&dev) == cudaSuccess &&
       cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
       smem_sm > 0) {
-    const long fit = (long)smem_sm / (long)(decode_smem(blob) + 1024);
+    const long fit = (long)smem_sm / (long)(decode_smem(blob, w) + 1024);
     per_sm = (int)std::max(1L, std::min<long>(per_sm, fit));
   }
   return (long)sm_count() * per_sm;
@@ -916,7 +956,7 @@ void plan(const kitty_cfg* cfg, int B, int M, int blob, Schedule* sc) {
     const int k = (M + c - 1) / c;
     for (int i = 0; i < k; ++i) sz[n++] = i == k - 1 ? M - (k - 1) * c : c;
   } else {
-    const double rho = (double)B * cfg->num_kv_heads / (double)resident_ctas(blob);
+    const double rho = (double)B * cfg->num_kv_heads / (double)resident_ctas(blob, cfg->lo_bit);
     long T = 0;
     for (int m = 16;; m *= 2) {
       n = 0;
@@ -965,7 +1005,7 @@ extern "C" int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pa
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !splits || !pages_per_split) return KITTY_ERR_INVALID_ARG;
   Schedule sc;
-  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi), &sc);
+  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi, cfg->lo_bit), &sc);
   *splits = sc.splits;
   *pages_per_split = sc.largest;
   return KITTY_OK;
@@ -977,7 +1017,7 @@ extern "C" int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !bytes) return KITTY_ERR_INVALID_ARG;
   Schedule sc;
-  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi), &sc);
+  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi, cfg->lo_bit), &sc);
   *bytes = workspace_bytes(cfg, B, sc);
   return KITTY_OK;
 }
@@ -1002,7 +1042,7 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
       (tail_k && (!aligned16(tail_k) || !aligned16(tail_v))) ||
       (tail_k && !tail_len) || !std::isfinite(sm_scale))
     return KITTY_ERR_INVALID_ARG;
-  const int blob = (int)blob_bytes(cfg->n_hi);
+  const int blob = (int)blob_bytes(cfg->n_hi, cfg->lo_bit);
   DecodeParams p = {};
   Schedule sc;
   plan(cfg, B, max_pages, blob, &sc);
@@ -1032,12 +1072,14 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
   p.n_hi = cfg->n_hi;
   p.blob = blob;
   p.in_dtype = cfg->in_dtype;
-  const size_t smem = decode_smem(p.blob);
+  const size_t smem = decode_smem(p.blob, cfg->lo_bit);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)B * cfg->num_kv_heads, sc.splits);
   const cudaError_t e = cfg->in_dtype == KITTY_BF16
-                            ? launch_decode_nx<KITTY_BF16>(cfg->n_hi / 16, grid, smem, s, p)
-                            : launch_decode_nx<KITTY_F16>(cfg->n_hi / 16, grid, smem, s, p);
+      ? (cfg->lo_bit == 4 ? launch_decode_nx<KITTY_BF16, 4>(cfg->n_hi / 16, grid, smem, s, p)
+                          : launch_decode_nx<KITTY_BF16, 2>(cfg->n_hi / 16, grid, smem, s, p))
+      : (cfg->lo_bit == 4 ? launch_decode_nx<KITTY_F16, 4>(cfg->n_hi / 16, grid, smem, s, p)
+                          : launch_decode_nx<KITTY_F16, 2>(cfg->n_hi / 16, grid, smem, s, p));
   if (e != cudaSuccess) return KITTY_ERR_CUDA;
   if (sc.splits > 1)
     combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p);

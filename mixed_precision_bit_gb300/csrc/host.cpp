@@ -20,7 +20,7 @@ extern "C" int kitty_abi_version(void) { return 1; }
 extern "C" int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page) {
   const int rc = check_cfg(cfg, false);
   if (rc != KITTY_OK) return rc;
-  const size_t b = blob_bytes(cfg->n_hi);
+  const size_t b = blob_bytes(cfg->n_hi, cfg->lo_bit);
   if (per_head_blob) *per_head_blob = b;
   if (per_page) *per_page = b * (size_t)cfg->num_kv_heads;
   return KITTY_OK;

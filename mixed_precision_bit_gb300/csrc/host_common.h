@@ -16,8 +16,10 @@ inline int check_cfg(const kitty_cfg* c, bool decode) {
   if (c->num_kv_heads <= 0 || c->num_q_heads <= 0 || c->num_q_heads % c->num_kv_heads != 0)
     return KITTY_ERR_INVALID_ARG;
   if (c->n_hi < 0 || c->n_hi > 128) return KITTY_ERR_INVALID_ARG;
-  if (c->head_dim != 128 || c->page_tokens != 32 || c->hi_bit != 4 || c->lo_bit != 2 ||
-      c->v_group != 32 || c->n_hi % 16 != 0)
+  // Key planes: (hi_bit, lo_bit) = (4, 2), two 2-bit planes, or (8, 4), two 4-bit planes
+  const bool bits_ok = (c->hi_bit == 4 && c->lo_bit == 2) || (c->hi_bit == 8 && c->lo_bit == 4);
+  if (c->head_dim != 128 || c->page_tokens != 32 || !bits_ok || c->v_group != 32 ||
+      c->n_hi % 16 != 0)
     return KITTY_ERR_UNSUPPORTED;
   if (c->rank_mode != KITTY_RANK_PAGE && c->rank_mode != KITTY_RANK_RUNNING &&
       c->rank_mode != KITTY_RANK_SEQUENCE)
@@ -28,6 +30,9 @@ inline int check_cfg(const kitty_cfg* c, bool decode) {
   return KITTY_OK;
 }
 
-inline size_t blob_bytes(int n_hi) { return 3072u + 9u * (size_t)n_hi; }
+// Bytes of one (page, kv-head) blob; w = lo_bit (Key plane width, 2 or 4).
+inline size_t blob_bytes(int n_hi, int w) {
+  return 512u * (size_t)w + 4u * (size_t)w * (size_t)n_hi + 2048u + (size_t)n_hi;
+}
 
 }  // namespace kitty

@@ -19,7 +19,7 @@ namespace kitty {
 namespace {
 
 constexpr int kQThreads = 128;
-constexpr int kMaxBlobWords = (3072 + 9 * kD) / 4;
+constexpr int kMaxBlobWords = (4096 + 17 * kD) / 4;  // largest blob: (8, 4) planes, n_hi = 128
 
 constexpr int kRowH = kD + 8;  // 16-bit elements per staged row (16-byte pad: fewer bank conflicts)
 
@@ -61,17 +61,19 @@ __device__ __forceinline__ float rcp_approx(float x) {
 }
 
 // Asymmetric min/max group quantizer: fp16 minimum and step, codes computed
-// against the stored values; boosted Key channels store 4x the 4-bit step.
-__device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, bool boosted) {
+// against the stored values; a boosted Key channel (2w-bit code) stores
+// F = 2^w times its own step, the step of its high w-bit plane.
+__device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, bool boosted,
+                                               float F = 4.0f) {
   QuantParams q;
   const __half Mh = __float2half_rn(mn);
   q.M = __half2float(Mh);
   q.Mbits = __half_as_ushort(Mh);
   const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
   if (boosted) {
-    const __half Sh = __float2half_rn(__fmul_rn(4.0f, s));
+    const __half Sh = __float2half_rn(__fmul_rn(F, s));
     q.Sbits = __half_as_ushort(Sh);
-    q.u = __fmul_rn(__half2float(Sh), 0.25f);
+    q.u = __fmul_rn(__half2float(Sh), 1.0f / F);
   } else {
     const __half Sh = __float2half_rn(s);
     q.Sbits = __half_as_ushort(Sh);
@@ -83,14 +85,16 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
 
 // code = clamp(rint(fl((x - M) / u)), 0, L), bit-exact with an IEEE division.
 // The quotient is taken as (x - M) * (1/u), within 2^-21 relative of the true
-// value; where that lands within 2^-15 of a rounding tie (and inside the clamp
-// range) the correctly rounded division decides.  u == 0 gives code 0.
+// value (so within 2^-17 for L <= 15 and 2^-13 for L = 255 inside the clamp
+// range); where that lands within 2^-15 (L <= 15) or 2^-12 (L = 255) of a
+// rounding tie, the correctly rounded division decides.  u == 0 gives code 0.
 __device__ __forceinline__ uint32_t qcode(float x, const QuantParams& q, int levels) {
   if (q.u == 0.0f) return 0u;
   const float d = __fsub_rn(x, q.M);
   const float y = __fmul_rn(d, q.ru);
   float n = rintf(y);
-  if (fabsf(fabsf(__fsub_rn(y, n)) - 0.5f) < 0x1p-15f && y > -1.5f && y < (float)levels + 1.5f)
+  const float window = levels > 15 ? 0x1p-12f : 0x1p-15f;
+  if (fabsf(fabsf(__fsub_rn(y, n)) - 0.5f) < window && y > -1.5f && y < (float)levels + 1.5f)
     n = rintf(__fdiv_rn(d, q.u));
   n = fminf(fmaxf(n, 0.0f), (float)levels);
   return (uint32_t)n;
@@ -167,13 +171,15 @@ __device__ void tile_stats(QuantSmem& sm, const uint16_t* ksrc, size_t row_strid
 // channel `threadIdx.x` (running mode only).  Writes the blob to dst.
 // fixed: -1 ranks this page (page or running statistics); 0 / 1 imposes the
 // channel's boost flag (sequence-wide ranking), skipping the statistics.
-template <int DT>
+// W = Key plane width (lo_bit): 2 for the (4, 2) configuration, 4 for (8, 4).
+template <int DT, int W>
 __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_t* vsrc,
                               size_t row_stride, int n_hi, bool running, float& rsum, float& rsq,
                               int& rcount, uint8_t* dst, int32_t* d_status, int fixed = -1) {
+  static_assert(W == 2 || W == 4, "Key planes are 2 or 4 bits wide");
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const BlobLayout lay(n_hi);
+  const BlobLayout lay(n_hi, W);
   const int nwords = lay.bytes / 4;
   if (tid == 0) sm.bad = 0;
   for (int i = tid; i < nwords; i += kQThreads) sm.blob[i] = 0u;
@@ -236,8 +242,9 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
 
   // ---- Key quantization of channel c and packing in fragment order
   {
-    const int levels = boosted ? 15 : 3;
-    const QuantParams q = qparams(mn, mx, levels, boosted);
+    constexpr int kLw = (1 << W) - 1;  // w-bit levels; boosted channels have 2w bits
+    const int levels = boosted ? (1 << (2 * W)) - 1 : kLw;
+    const QuantParams q = qparams(mn, mx, levels, boosted, (float)(1 << W));
     uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
     b16[lay.ks / 2 + c] = q.Sbits;
     // minima in fragment order: channel 16j + 8h + 2qq + e at ((qq*8 + j)*2 + h)*2 + e
@@ -247,31 +254,60 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     for (int t = 0; t < kPage; ++t) code[t] = qcode(x[t], q, levels);
     const int j = c >> 4, half = (c >> 3) & 1, qq = (c >> 1) & 3, e = c & 1;
     const int bitbase = 16 * e + 8 * half;
-#pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int tau = 0; tau < 4; ++tau) {
-        const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
-        const uint32_t cb = boosted ? (code[t] >> 2) : code[t];
-        w |= cb << (bitbase + 2 * tau);
-      }
-      atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 8 + j], w);
-    }
-    if (boosted) {
-      const int wpl = n_hi / 16;
-      const int js = row >> 4, hx = (row >> 3) & 1, qx = (row >> 1) & 3, ex = row & 1;
-      const int bx = 16 * ex + 8 * hx;
+    const int js = row >> 4, hx = (row >> 3) & 1, qx = (row >> 1) & 3, ex = row & 1;
+    const int bx = 16 * ex + 8 * hx;
+    if (W == 2) {
+      // 2-bit codes: word (lane 4r+qq, tile j) holds tokens 16mt + 8rh + r at 2*(2mt + rh)
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
         uint32_t w = 0;
 #pragma unroll
         for (int tau = 0; tau < 4; ++tau) {
           const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
-          w |= (code[t] & 3u) << (bx + 2 * tau);
+          const uint32_t cb = boosted ? (code[t] >> 2) : code[t];
+          w |= cb << (bitbase + 2 * tau);
         }
-        atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w);
+        atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 8 + j], w);
       }
+      if (boosted) {
+        const int wpl = n_hi / 16;
+#pragma unroll
+        for (int r = 0; r < 8; ++r) {
+          uint32_t w = 0;
+#pragma unroll
+          for (int tau = 0; tau < 4; ++tau) {
+            const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
+            w |= (code[t] & 3u) << (bx + 2 * tau);
+          }
+          atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w);
+        }
+      }
+    } else {
+      // 4-bit codes: two words per (lane 4r+qq, tile j), one per 16-token block
+      // mt; token 16mt + 8rh + r at nibble 4rh
+#pragma unroll
+      for (int r = 0; r < 8; ++r)
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+          const int t0 = 16 * mt + r, t1 = t0 + 8;
+          const uint32_t c0 = boosted ? (code[t0] >> 4) : code[t0];
+          const uint32_t c1 = boosted ? (code[t1] >> 4) : code[t1];
+          atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 16 + 2 * j + mt],
+                   (c0 << bitbase) | (c1 << (bitbase + 4)));
+        }
+      if (boosted) {
+        const int wpl = 2 * (n_hi / 16);
+#pragma unroll
+        for (int r = 0; r < 8; ++r)
+#pragma unroll
+          for (int mt = 0; mt < 2; ++mt) {
+            const int t0 = 16 * mt + r, t1 = t0 + 8;
+            atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + 2 * js + mt],
+                     ((code[t0] & 15u) << bx) | ((code[t1] & 15u) << (bx + 4)));
+          }
+      }
+    }
+    if (boosted) {
       // channel-list row 16js + 8h + 2qq + e stored at byte js*16 + qq*4 + h*2 + e
       const int pos = lay.kch + js * 16 + qx * 4 + hx * 2 + ex;
       atomicOr(&sm.blob[pos / 4], (uint32_t)c << (8 * (pos & 3)));

@@ -22,7 +22,7 @@ namespace kitty {
 namespace {
 
 // Page mode: one CTA per (input page i, kv head h).
-template <int DT>
+template <int DT, int W>
 __global__ void __launch_bounds__(kQThreads, 8) quantize_pages_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
     int n_hi, int Hkv, uint8_t* pool, int pool_pages, int32_t* d_status) {
@@ -33,12 +33,12 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_pages_kernel(
     if (threadIdx.x == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
     return;
   }
-  const BlobLayout lay(n_hi);
+  const BlobLayout lay(n_hi, W);
   const size_t stride = (size_t)Hkv * kD;
   const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
   float dummy_s = 0.f, dummy_q = 0.f;
   int dummy_c = 0;
-  quantize_tile<DT>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
+  quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
                     pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status);
 }
 
@@ -52,7 +52,7 @@ __global__ void check_seq_kernel(const int32_t* seq_of_page, int n_pages, int n_
 
 // Running mode: one CTA per (sequence s, kv head h) walks that sequence's pages
 // in order, carrying the channel accumulators in registers.
-template <int DT>
+template <int DT, int W>
 __global__ void __launch_bounds__(kQThreads, 8) quantize_running_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
     const int32_t* seq_of_page, int n_pages, int n_hi, int Hkv, float* run_sum, float* run_sumsq,
@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_running_kernel(
   while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] <= s) lo = m + 1; else hi = m; }
   const int p1 = lo;
   if (p0 >= p1) return;
-  const BlobLayout lay(n_hi);
+  const BlobLayout lay(n_hi, W);
   const size_t stride = (size_t)Hkv * kD;
   const size_t sh = (size_t)s * Hkv + h;
   float rs = run_sum[sh * kD + threadIdx.x];
@@ -80,7 +80,7 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_running_kernel(
       continue;
     }
     const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
-    quantize_tile<DT>(sm, k + src, v + src, stride, n_hi, true, rs, rq, rc,
+    quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, true, rs, rq, rc,
                       pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status);
   }
   run_sum[sh * kD + threadIdx.x] = rs;
@@ -92,7 +92,7 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_running_kernel(
 // tree-ordered page sums of all the sequence's pages (in order) into the
 // running accumulators; the channels are ranked once on that variance; pass 2
 // quantizes every page with that fixed boost set.
-template <int DT>
+template <int DT, int W>
 __global__ void __launch_bounds__(kQThreads, 8) quantize_sequence_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
     const int32_t* seq_of_page, int n_pages, int n_hi, int Hkv, float* run_sum, float* run_sumsq,
@@ -106,7 +106,7 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_sequence_kernel(
   while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] <= s) lo = m + 1; else hi = m; }
   const int p1 = lo;
   if (p0 >= p1) return;
-  const BlobLayout lay(n_hi);
+  const BlobLayout lay(n_hi, W);
   const size_t stride = (size_t)Hkv * kD;
   const size_t sh = (size_t)s * Hkv + h;
   float rs = run_sum[sh * kD + threadIdx.x];
@@ -131,7 +131,7 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_sequence_kernel(
       continue;
     }
     const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
-    quantize_tile<DT>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
+    quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
                       pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status, boosted ? 1 : 0);
   }
   run_sum[sh * kD + threadIdx.x] = rs;
@@ -141,7 +141,7 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_sequence_kernel(
 
 // Append, part 1: one CTA per (sequence b, kv head h) writes the token into the
 // tail and, when the tail fills and a page id is given, quantizes the tail.
-template <int DT>
+template <int DT, int W>
 __global__ void __launch_bounds__(kQThreads) append_heads_kernel(
     const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new, uint16_t* tail_k,
     uint16_t* tail_v, const int32_t* tail_len, float* run_sum, float* run_sumsq,
@@ -163,7 +163,7 @@ __global__ void __launch_bounds__(kQThreads) append_heads_kernel(
   if (np < 0 || np >= max_pages) { if (c == 0) set_status(d_status, KITTY_ST_TABLE_FULL); return; }
   if (fid >= pool_pages) { if (c == 0) set_status(d_status, KITTY_ST_BAD_PAGE); return; }
   __syncthreads();  // the new token row is visible to the whole CTA
-  const BlobLayout lay(n_hi);
+  const BlobLayout lay(n_hi, W);
   float rs = 0.f, rq = 0.f;
   int rc = 0;
   if (running) {
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kQThreads) append_heads_kernel(
     rq = run_sumsq[sh * kD + c];
     rc = run_count[sh];
   }
-  quantize_tile<DT>(sm, tail_k + sh * kPage * kD, tail_v + sh * kPage * kD, kD, n_hi, running != 0,
+  quantize_tile<DT, W>(sm, tail_k + sh * kPage * kD, tail_v + sh * kPage * kD, kD, n_hi, running != 0,
                     rs, rq, rc, pool + ((size_t)fid * Hkv + h) * lay.bytes, d_status);
   if (running) {
     run_sum[sh * kD + c] = rs;
@@ -188,6 +188,24 @@ __global__ void append_finalize_kernel(int32_t* tail_len, const int32_t* flush_p
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b >= B) return;
   append_finalize_one(b, tail_len, flush_page_ids, block_table, max_pages, num_pages, pool_pages);
+}
+
+// Calls f(KernelTag<DT, W>{}) for the configuration's input dtype and Key plane
+// width (lo_bit).
+template <int DT_, int W_>
+struct KernelTag {
+  static constexpr int DT = DT_, W = W_;
+};
+
+template <class F>
+void dispatch(const kitty_cfg* cfg, F f) {
+  if (cfg->in_dtype == KITTY_BF16) {
+    if (cfg->lo_bit == 4) f(KernelTag<KITTY_BF16, 4>{});
+    else f(KernelTag<KITTY_BF16, 2>{});
+  } else {
+    if (cfg->lo_bit == 4) f(KernelTag<KITTY_F16, 4>{});
+    else f(KernelTag<KITTY_F16, 2>{});
+  }
 }
 
 }  // namespace
@@ -217,22 +235,21 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
   auto* p8 = static_cast<uint8_t*>(pool);
   if (!running) {
     dim3 grid(n_pages, Hkv);
-    if (cfg->in_dtype == KITTY_BF16)
-      quantize_pages_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, cfg->n_hi, Hkv, p8, pool_pages, d_status);
-    else
-      quantize_pages_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, cfg->n_hi, Hkv, p8, pool_pages, d_status);
+    dispatch(cfg, [&](auto tag) {
+      using T = decltype(tag);
+      quantize_pages_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, cfg->n_hi, Hkv, p8, pool_pages, d_status);
+    });
   } else {
     check_seq_kernel<<<(n_pages + 255) / 256, 256, 0, s>>>(seq_of_page, n_pages, n_seqs, d_status);
     dim3 grid(n_seqs, Hkv);
-    if (cfg->rank_mode == KITTY_RANK_SEQUENCE) {
-      if (cfg->in_dtype == KITTY_BF16)
-        quantize_sequence_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+    const bool seq = cfg->rank_mode == KITTY_RANK_SEQUENCE;
+    dispatch(cfg, [&](auto tag) {
+      using T = decltype(tag);
+      if (seq)
+        quantize_sequence_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
       else
-        quantize_sequence_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
-    } else if (cfg->in_dtype == KITTY_BF16)
-      quantize_running_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
-    else
-      quantize_running_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+        quantize_running_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+    });
   }
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
 }
@@ -260,10 +277,10 @@ extern "C" int kitty_append_token(const kitty_cfg* cfg, const void* k_new, const
   const auto* kn = static_cast<const uint16_t*>(k_new);
   const auto* vn = static_cast<const uint16_t*>(v_new);
   auto* p8 = static_cast<uint8_t*>(pool);
-  if (cfg->in_dtype == KITTY_BF16)
-    append_heads_kernel<KITTY_BF16><<<grid, kQThreads, 0, s>>>(kn, vn, tk, tv, tail_len, run_sum, run_sumsq, run_count, flush_page_ids, max_pages, num_pages, p8, pool_pages, cfg->n_hi, Hkv, running ? 1 : 0, d_status);
-  else
-    append_heads_kernel<KITTY_F16><<<grid, kQThreads, 0, s>>>(kn, vn, tk, tv, tail_len, run_sum, run_sumsq, run_count, flush_page_ids, max_pages, num_pages, p8, pool_pages, cfg->n_hi, Hkv, running ? 1 : 0, d_status);
+  dispatch(cfg, [&](auto tag) {
+    using T = decltype(tag);
+    append_heads_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(kn, vn, tk, tv, tail_len, run_sum, run_sumsq, run_count, flush_page_ids, max_pages, num_pages, p8, pool_pages, cfg->n_hi, Hkv, running ? 1 : 0, d_status);
+  });
   append_finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(tail_len, flush_page_ids, block_table, max_pages, num_pages, pool_pages, B);
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
 }

@@ -106,6 +106,7 @@ class Workload:
     tails: np.ndarray      # [B] unquantized tail tokens (0..31)
     drift: int = 0         # redraw K channel scales every `drift` tokens (0: never)
     layers: int = 1
+    lo_bit: int = 2        # Key plane width: 2 ((hi, lo) = (4, 2) bits) or 4 ((8, 4))
 
     @property
     def g(self):

@@ -46,10 +46,18 @@ def test_page_bytes_and_avg_bits(K):
     assert K.avg_bits(K.Config(8, 32, n_hi=32)) == 2.5
     assert K.avg_bits(K.Config(8, 32, n_hi=0)) == 2.0
     assert K.avg_bits(K.Config(8, 32, n_hi=64)) == 3.0
+    # (hi_bit, lo_bit) = (8, 4): two 4-bit Key planes; the table's (0.25, 8, 4) row is 5.0 bits
+    import oracle
+    for n_hi in (0, 16, 32, 128):
+        cfg = K.Config(num_kv_heads=8, num_q_heads=32, n_hi=n_hi, hi_bit=8, lo_bit=4)
+        blob = oracle.page_bytes(n_hi, 4)
+        assert K.page_bytes(cfg) == (blob, 8 * blob)
+    assert K.avg_bits(K.Config(8, 32, n_hi=32, hi_bit=8, lo_bit=4)) == 5.0
 
 
 def test_config_checks(K):
     for bad, code in ((dict(n_hi=8), -2), (dict(head_dim=64), -2), (dict(hi_bit=8), -2),
+                      (dict(lo_bit=4), -2), (dict(hi_bit=6, lo_bit=3), -2),
                       (dict(num_q_heads=12), -1), (dict(in_dtype=7), -1)):
         cfg = K.Config(**{**dict(num_kv_heads=8, num_q_heads=32), **bad})
         with pytest.raises(K.KittyError) as e:

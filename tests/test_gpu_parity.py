@@ -40,6 +40,13 @@ CASES = [
     ("small_gqa", dict(Hq=2, Hkv=2)),            # g = 1
     ("small_gqa", dict(Hq=6, Hkv=3)),            # g = 2
     ("small_gqa", dict(Hq=6, Hkv=2)),            # g = 3
+    # (hi_bit, lo_bit) = (8, 4): two 4-bit Key planes
+    ("tiny", dict(lo_bit=4)),
+    ("small_gqa", dict(lo_bit=4)),
+    ("small_gqa", dict(lo_bit=4, n_hi=0)),
+    ("small_gqa", dict(lo_bit=4, n_hi=48)),
+    ("small_gqa", dict(lo_bit=4, n_hi=128)),
+    ("small_gqa", dict(lo_bit=4, dtype=synth.F16, n_hi=16, Hq=6, Hkv=3)),
 ]
 
 
@@ -60,9 +67,10 @@ def test_quantize_bit_exact(case):
     assert bad.size == 0, "first mismatching bytes at %s" % bad[:8]
 
 
+@pytest.mark.parametrize("lo_bit", [2, 4])
 @pytest.mark.parametrize("mode", [1, 2], ids=["running", "sequence"])
-def test_quantize_running_bit_exact(mode):
-    w = _variant("small_gqa", pages=np.array([5, 3, 9]), drift=64)
+def test_quantize_running_bit_exact(mode, lo_bit):
+    w = _variant("small_gqa", pages=np.array([5, 3, 9]), drift=64, lo_bit=lo_bit)
     inp = synth.host_inputs(w, seed=2)
     pool, run = gpu_quantize(w, inp, mode=mode)
     ref, (rs, rq, rc), st = oracle_quantize(w, inp, mode=mode)

@@ -77,8 +77,10 @@ typedef struct {
   int32_t num_q_heads;  /* Hq, a multiple of Hkv; decode needs Hq/Hkv <= 4 */
   int32_t page_tokens;  /* tokens per page = Key quantization group; must be 32 */
   int32_t n_hi;         /* boosted Key channels per page: 0, 16, 32, ..., 128 */
-  int32_t hi_bit;       /* must be 4 */
-  int32_t lo_bit;       /* must be 2 */
+  int32_t hi_bit;       /* (hi_bit, lo_bit) = (4, 2): Key channels 2-bit, boosted 4-bit as */
+  int32_t lo_bit;       /* two 2-bit planes; or (8, 4): 4-bit, boosted 8-bit as two 4-bit
+                           planes (VeloxQuant-MLX docs, "Tuning avg_bits"); Values are
+                           2-bit in both */
   int32_t v_group;      /* channels per Value group; must be 32 */
   int32_t rank_mode;    /* KITTY_RANK_PAGE, KITTY_RANK_RUNNING or KITTY_RANK_SEQUENCE */
   int32_t in_dtype;     /* KITTY_F16 or KITTY_BF16 for K, V, Q and the tails */
@@ -93,10 +95,11 @@ int kitty_abi_version(void);
 
 /* Packed page size.  A page holds Hkv blobs, one per kv head, in head order;
  * physical page p starts at byte p * per_page of the pool.  Blob of one
- * (page, kv head), in order: Key base plane 1024 B, Key extra plane n_hi*8 B,
- * Key step fp16[128], Key minimum fp16[128], channel list uint8[n_hi]
- * (ascending), Value plane 1024 B, Value step fp16[4][32], Value minimum
- * fp16[4][32] (group-major).  = 3072 + 9*n_hi bytes (3360 at n_hi=32).  The
+ * (page, kv head), in order, with w = lo_bit: Key base plane 512*w B, Key extra
+ * plane 4*w*n_hi B, Key step fp16[128], Key minimum fp16[128], channel list
+ * uint8[n_hi] (ascending), Value plane 1024 B, Value step fp16[4][32], Value
+ * minimum fp16[4][32] (group-major).  = 3072 + 9*n_hi bytes at (4, 2) (3360 at
+ * n_hi=32), 4096 + 17*n_hi at (8, 4).  The
  * bit positions inside the planes are the "fragment order" index maps
  * documented in the oracle and DESIGN notes.  Paper: Abstract (page-centric
  * layout, two uniform 2-bit tensors per Key page). */
@@ -125,7 +128,11 @@ void kitty_alloc_destroy(kitty_alloc* a);
  * Channel-wise Precision Boost, two-plane Key page); VeloxQuant-MLX docs,
  * Prefill phase steps 1-3 and 5.
  *   k, v        device [n_pages*32][Hkv][128] 16-bit; page i = tokens 32i..32i+31
- *   page_ids    device int32 [n_pages]: page i is written at pool page page_ids[i]
+ *   page_ids    device int32 [n_pages]: page i is written at pool page page_ids[i];
+ *               the ids must be distinct (repeated ids give undefined pages;
+ *               running and sequence modes use each page's own blob as scratch
+ *               before writing it); out-of-range ids are skipped with
+ *               KITTY_ST_BAD_PAGE
  *   Page mode: each page ranks its channels on its own 32 tokens; seq_of_page,
  *   run_* may be NULL and n_seqs is ignored.
  *   Running mode: seq_of_page device int32 [n_pages], non-decreasing, in
@@ -136,6 +143,11 @@ void kitty_alloc_destroy(kitty_alloc* a);
  *   page sums first, the channels are ranked once on that variance, and every
  *   page of the sequence is quantized with that one boost set (VeloxQuant-MLX
  *   docs, Prefill phase: one ranking per head over the prompt).
+ *   Both modes run in three launches (page sums in parallel, a per-(sequence,
+ *   head) scan, quantization in parallel) with the fp32 additions in page
+ *   order, so they give the same bytes as quantizing one page at a time.
+ *   Pages whose seq_of_page entry is outside [0, n_seqs) are not written
+ *   (KITTY_ST_BAD_SEQ).
  *   pool        device, pool_pages * per_page bytes, 16-byte aligned. */
 int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const void* v, int32_t n_pages,
                          const int32_t* page_ids, const int32_t* seq_of_page, int32_t n_seqs,

@@ -170,7 +170,9 @@ __device__ void tile_stats(QuantSmem& sm, const uint16_t* ksrc, size_t row_strid
 // is at +t*row_stride elements.  rsum/rsq/rcount: running accumulators of
 // channel `threadIdx.x` (running mode only).  Writes the blob to dst.
 // fixed: -1 ranks this page (page or running statistics); 0 / 1 imposes the
-// channel's boost flag (sequence-wide ranking), skipping the statistics.
+// channel's boost flag (sequence-wide ranking), skipping the statistics; -2
+// ranks on rsum/rsq/rcount as given (running totals that already include this
+// page), leaving them unchanged.
 // W = Key plane width (lo_bit): 2 for the (4, 2) configuration, 4 for (8, 4).
 template <int DT, int W>
 __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_t* vsrc,
@@ -215,7 +217,9 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     mx = fmaxf(mx, x[t]);
   }
   float var = 0.f;
-  if (fixed < 0) {
+  if (fixed == -2) {
+    var = running_var(rsum, rsq, __int2float_rn(rcount));
+  } else if (fixed < 0) {
 #pragma unroll
     for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
     const float s1 = tree32(tmp);

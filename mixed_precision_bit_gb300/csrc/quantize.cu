@@ -50,93 +50,133 @@ __global__ void check_seq_kernel(const int32_t* seq_of_page, int n_pages, int n_
   if (s < 0 || s >= n_seqs || (i > 0 && s < seq_of_page[i - 1])) set_status(d_status, KITTY_ST_BAD_SEQ);
 }
 
-// Running mode: one CTA per (sequence s, kv head h) walks that sequence's pages
-// in order, carrying the channel accumulators in registers.
-template <int DT, int W>
-__global__ void __launch_bounds__(kQThreads, 8) quantize_running_kernel(
-    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
-    const int32_t* seq_of_page, int n_pages, int n_hi, int Hkv, float* run_sum, float* run_sumsq,
-    int32_t* run_count, uint8_t* pool, int pool_pages, int32_t* d_status) {
-  __shared__ QuantSmem sm;
-  const int s = blockIdx.x, h = blockIdx.y;
-  // first page with seq >= s, and first with seq > s (binary search)
+// Running and sequence modes, in three launches.  Only the fp32 accumulation
+// over a sequence's pages is sequential, so:
+//  A. page_sums_kernel (one CTA per (page, kv head)): the page's tree-ordered
+//     channel sums S1, S2, parked in the page's own output blob (scratch);
+//  B. seq_scan_kernel (one CTA per (sequence, kv head)): the same fp32 adds in
+//     page order as a sequential walk.  Running mode writes each page's
+//     running totals (including that page) back into its blob; sequence mode
+//     ranks once on the totals and writes the boost flags into every blob.
+//     The final totals go to run_sum / run_sumsq / run_count;
+//  C. quantize_given_kernel (one CTA per (page, kv head)): reads its blob's
+//     totals or flags, then overwrites the blob with the quantized page.
+// Every fp32 operation and its order are those of a one-page-at-a-time walk,
+// so the pages and accumulators are bit-identical to it.  Pages are distinct
+// pool pages (the caller's ids), so blobs do not collide.
+//
+// Scratch words in a blob: running mode S1/R1 [0,128), S2/R2 [128,256), count
+// [256]; sequence mode boost flags [0,128).
+
+__device__ __forceinline__ int first_page_of(const int32_t* seq_of_page, int n_pages, int s) {
   int lo = 0, hi = n_pages;
   while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] < s) lo = m + 1; else hi = m; }
-  const int p0 = lo;
-  hi = n_pages;
-  while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] <= s) lo = m + 1; else hi = m; }
-  const int p1 = lo;
-  if (p0 >= p1) return;
-  const BlobLayout lay(n_hi, W);
-  const size_t stride = (size_t)Hkv * kD;
-  const size_t sh = (size_t)s * Hkv + h;
-  float rs = run_sum[sh * kD + threadIdx.x];
-  float rq = run_sumsq[sh * kD + threadIdx.x];
-  int rc = run_count[sh];
-  for (int i = p0; i < p1; ++i) {
-    const int pid = page_ids[i];
-    if (pid < 0 || pid >= pool_pages) {
-      if (threadIdx.x == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
-      continue;
-    }
-    const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
-    quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, true, rs, rq, rc,
-                      pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status);
-  }
-  run_sum[sh * kD + threadIdx.x] = rs;
-  run_sumsq[sh * kD + threadIdx.x] = rq;
-  if (threadIdx.x == 0) run_count[sh] = rc;
+  return lo;
 }
 
-// Sequence mode: one CTA per (sequence s, kv head h).  Pass 1 accumulates the
-// tree-ordered page sums of all the sequence's pages (in order) into the
-// running accumulators; the channels are ranked once on that variance; pass 2
-// quantizes every page with that fixed boost set.
-template <int DT, int W>
-__global__ void __launch_bounds__(kQThreads, 8) quantize_sequence_kernel(
-    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
-    const int32_t* seq_of_page, int n_pages, int n_hi, int Hkv, float* run_sum, float* run_sumsq,
-    int32_t* run_count, uint8_t* pool, int pool_pages, int32_t* d_status) {
+template <int DT>
+__global__ void __launch_bounds__(kQThreads, 8) page_sums_kernel(
+    const uint16_t* __restrict__ k, const int32_t* page_ids, const int32_t* seq_of_page,
+    int n_seqs, int Hkv, uint8_t* pool, int pool_pages, int blob) {
   __shared__ QuantSmem sm;
-  const int s = blockIdx.x, h = blockIdx.y;
-  int lo = 0, hi = n_pages;
-  while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] < s) lo = m + 1; else hi = m; }
-  const int p0 = lo;
-  hi = n_pages;
-  while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] <= s) lo = m + 1; else hi = m; }
-  const int p1 = lo;
-  if (p0 >= p1) return;
-  const BlobLayout lay(n_hi, W);
+  const int i = blockIdx.x, h = blockIdx.y;
+  const int sq = seq_of_page[i];
+  const int pid = page_ids[i];
+  // a bad id is reported by pass C; a bad sequence by check_seq_kernel
+  if (pid < 0 || pid >= pool_pages || sq < 0 || sq >= n_seqs) return;
   const size_t stride = (size_t)Hkv * kD;
+  float s1, s2;
+  tile_stats<DT>(sm, k + (size_t)i * kPage * stride + (size_t)h * kD, stride, s1, s2);
+  float* sc = reinterpret_cast<float*>(pool + ((size_t)pid * Hkv + h) * blob);
+  sc[threadIdx.x] = s1;
+  sc[kD + threadIdx.x] = s2;
+}
+
+// Thread c = channel c.  Pages are read 8 at a time ahead of the adds.
+__global__ void __launch_bounds__(kQThreads) seq_scan_kernel(
+    const int32_t* page_ids, const int32_t* seq_of_page, int n_pages, int Hkv, float* run_sum,
+    float* run_sumsq, int32_t* run_count, uint8_t* pool, int pool_pages, int blob, int n_hi,
+    int sequence_mode) {
+  __shared__ QuantSmem sm;  // top-k warp counts (sequence mode)
+  const int s = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int p0 = first_page_of(seq_of_page, n_pages, s);
+  const int p1 = first_page_of(seq_of_page, n_pages, s + 1);
+  if (p0 >= p1) return;
   const size_t sh = (size_t)s * Hkv + h;
-  float rs = run_sum[sh * kD + threadIdx.x];
-  float rq = run_sumsq[sh * kD + threadIdx.x];
+  float rs = run_sum[sh * kD + c];
+  float rq = run_sumsq[sh * kD + c];
   int rc = run_count[sh];
-  for (int i = p0; i < p1; ++i) {
-    const int pid = page_ids[i];
-    if (pid < 0 || pid >= pool_pages) continue;
-    float s1, s2;
-    tile_stats<DT>(sm, k + (size_t)i * kPage * stride + (size_t)h * kD, stride, s1, s2);
-    rs = __fadd_rn(rs, s1);
-    rq = __fadd_rn(rq, s2);
-    rc += kPage;
-  }
-  const bool boosted = topk_flag(sm, running_var(rs, rq, __int2float_rn(rc)), n_hi);
-  float dummy_s = 0.f, dummy_q = 0.f;
-  int dummy_c = 0;
-  for (int i = p0; i < p1; ++i) {
-    const int pid = page_ids[i];
-    if (pid < 0 || pid >= pool_pages) {
-      if (threadIdx.x == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
-      continue;
+  constexpr int kAhead = 8;
+  for (int i0 = p0; i0 < p1; i0 += kAhead) {
+    float a1[kAhead], a2[kAhead];
+    float* sc[kAhead];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int i = i0 + u;
+      const int pid = i < p1 ? page_ids[i] : -1;
+      sc[u] = pid >= 0 && pid < pool_pages
+                  ? reinterpret_cast<float*>(pool + ((size_t)pid * Hkv + h) * blob) : nullptr;
+      a1[u] = sc[u] ? sc[u][c] : 0.f;
+      a2[u] = sc[u] ? sc[u][kD + c] : 0.f;
     }
-    const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
-    quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
-                      pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status, boosted ? 1 : 0);
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      if (sc[u] == nullptr) continue;  // invalid page: not counted
+      rs = __fadd_rn(rs, a1[u]);
+      rq = __fadd_rn(rq, a2[u]);
+      rc += kPage;
+      if (!sequence_mode) {
+        sc[u][c] = rs;
+        sc[u][kD + c] = rq;
+        if (c == 0) reinterpret_cast<int*>(sc[u])[2 * kD] = rc;
+      }
+    }
   }
-  run_sum[sh * kD + threadIdx.x] = rs;
-  run_sumsq[sh * kD + threadIdx.x] = rq;
-  if (threadIdx.x == 0) run_count[sh] = rc;
+  if (sequence_mode) {
+    const int flag = topk_flag(sm, running_var(rs, rq, __int2float_rn(rc)), n_hi) ? 1 : 0;
+    for (int i = p0; i < p1; ++i) {
+      const int pid = page_ids[i];
+      if (pid >= 0 && pid < pool_pages)
+        reinterpret_cast<int*>(pool + ((size_t)pid * Hkv + h) * blob)[c] = flag;
+    }
+  }
+  run_sum[sh * kD + c] = rs;
+  run_sumsq[sh * kD + c] = rq;
+  if (c == 0) run_count[sh] = rc;
+}
+
+template <int DT, int W>
+__global__ void __launch_bounds__(kQThreads, 8) quantize_given_kernel(
+    const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
+    const int32_t* seq_of_page, int n_seqs, int n_hi, int Hkv, uint8_t* pool, int pool_pages,
+    int sequence_mode, int32_t* d_status) {
+  __shared__ QuantSmem sm;
+  const int i = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int sq = seq_of_page[i];
+  if (sq < 0 || sq >= n_seqs) return;  // no sequence scanned it (KITTY_ST_BAD_SEQ is set)
+  const int pid = page_ids[i];
+  if (pid < 0 || pid >= pool_pages) {
+    if (c == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
+    return;
+  }
+  const BlobLayout lay(n_hi, W);
+  uint8_t* dst = pool + ((size_t)pid * Hkv + h) * lay.bytes;
+  const size_t stride = (size_t)Hkv * kD;
+  const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
+  const float* sc = reinterpret_cast<const float*>(dst);
+  float rs = 0.f, rq = 0.f;
+  int rc = 0, fixed;
+  if (sequence_mode) {
+    fixed = reinterpret_cast<const int*>(sc)[c] != 0 ? 1 : 0;
+  } else {
+    rs = sc[c];
+    rq = sc[kD + c];
+    rc = reinterpret_cast<const int*>(sc)[2 * kD];
+    fixed = -2;  // rank on these totals
+  }
+  // quantize_tile reads the scratch values above before it overwrites the blob
+  // (its only global write, after its last barrier)
+  quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, false, rs, rq, rc, dst, d_status, fixed);
 }
 
 // Append, part 1: one CTA per (sequence b, kv head h) writes the token into the
@@ -241,14 +281,18 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
     });
   } else {
     check_seq_kernel<<<(n_pages + 255) / 256, 256, 0, s>>>(seq_of_page, n_pages, n_seqs, d_status);
-    dim3 grid(n_seqs, Hkv);
-    const bool seq = cfg->rank_mode == KITTY_RANK_SEQUENCE;
+    const int blob = (int)blob_bytes(cfg->n_hi, cfg->lo_bit);
+    const int seq = cfg->rank_mode == KITTY_RANK_SEQUENCE ? 1 : 0;
+    dim3 pages(n_pages, Hkv), seqs(n_seqs, Hkv);
+    if (cfg->in_dtype == KITTY_BF16)
+      page_sums_kernel<KITTY_BF16><<<pages, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_seqs, Hkv, p8, pool_pages, blob);
+    else
+      page_sums_kernel<KITTY_F16><<<pages, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_seqs, Hkv, p8, pool_pages, blob);
+    seq_scan_kernel<<<seqs, kQThreads, 0, s>>>(page_ids, seq_of_page, n_pages, Hkv, run_sum, run_sumsq,
+                                               run_count, p8, pool_pages, blob, cfg->n_hi, seq);
     dispatch(cfg, [&](auto tag) {
       using T = decltype(tag);
-      if (seq)
-        quantize_sequence_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
-      else
-        quantize_running_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_pages, cfg->n_hi, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, d_status);
+      quantize_given_kernel<T::DT, T::W><<<pages, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_seqs, cfg->n_hi, Hkv, p8, pool_pages, seq, d_status);
     });
   }
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;

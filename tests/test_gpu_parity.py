@@ -81,6 +81,31 @@ def test_quantize_running_bit_exact(mode, lo_bit):
     assert (run[2].cpu().numpy() == rc).all()
 
 
+def test_quantize_bad_seq_status():
+    """A seq_of_page entry outside [0, n_seqs) is reported; the other pages of
+    the batch are quantized as usual (bit-exact with a batch without the bad
+    page)."""
+    import torch
+    from mixed_precision_bit_gb300 import kitty
+    w = _variant("small_gqa", pages=np.array([4, 2, 3]))
+    inp = synth.host_inputs(w, seed=6)
+    good, _ = gpu_quantize(w, inp, mode=1)
+    bad_seq = inp["seq_of_page"].copy()
+    bad_seq[-1] = w.B          # the last page claims a sequence that does not exist
+    st = torch.zeros(1, dtype=torch.int32, device="cuda")
+    inp2 = dict(inp, seq_of_page=bad_seq)
+    pool, _ = gpu_quantize(w, inp2, mode=1, status=st)
+    assert int(st.item()) == kitty.ST["BAD_SEQ"]
+    per_page = kitty.page_bytes(cfg_for(w, rank_mode=1))[1]
+    ids = inp["page_ids"]
+    g, p = good.cpu().numpy(), pool.cpu().numpy()
+    for i in range(ids.size - 1):
+        sl = slice(int(ids[i]) * per_page, (int(ids[i]) + 1) * per_page)
+        assert (g[sl] == p[sl]).all(), i
+    sl = slice(int(ids[-1]) * per_page, (int(ids[-1]) + 1) * per_page)
+    assert not p[sl].any()     # never written (the pool starts zeroed)
+
+
 @pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
 @pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
 def test_decode_attention(case, out_dtype):

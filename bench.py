@@ -285,7 +285,7 @@ def run_kitty(args, rank, world, local_rank):
                                                if args.fused else 0)
                      for l, lc in enumerate(layers)])
     fl_dev = torch.from_numpy(np.stack(plans)).cuda()
-    splits, chunk = kitty.decode_plan(cfg, B, layers[0].max_pages)
+    splits, chunk = kitty.decode_plan(layers[0].cfg, B, layers[0].max_pages)
     stream = torch.cuda.current_stream()
     # CUDA graphs: per input set and layer, one graph for the append and one for
     # the decode call (the per-layer events stay outside the graphs); the step's

@@ -88,9 +88,14 @@ typedef struct {
                                    shrinking towards the end of the grid), > 0 =
                                    splits of this many pages, raised to
                                    ceil(max_pages / 256) if smaller */
+  int32_t decode_total_pages;     /* optional planning hint for the library's split
+                                   schedule: the batch's total page count
+                                   (sum of num_pages); 0 = unknown.  Any value
+                                   gives correct results; it only shapes the
+                                   splits (and so the workspace size) */
 } kitty_cfg;
 
-/* Library ABI version (this header: 1). */
+/* Library ABI version (this header: 2; kitty_cfg gained decode_total_pages). */
 int kitty_abi_version(void);
 
 /* Packed page size.  A page holds Hkv blobs, one per kv head, in head order;

@@ -11,6 +11,7 @@ runtime pipeline); VeloxQuant-MLX docs, Decode phase.
 
 from __future__ import annotations
 
+import dataclasses
 import math
 
 import numpy as np
@@ -82,7 +83,19 @@ class LayerCache:
         self.tail_len.copy_(torch.from_numpy(tails.astype(np.int32)))
         self.h_tail[:] = tails
         self.h_pages[:] = n_pages
+        self.set_plan_hint()
         return ids
+
+    def set_plan_hint(self, total_pages=None):
+        """Give the decode split planner the batch's total page count (default:
+        the host mirror's) on this cache's own copy of the config, and grow the
+        workspace if that plan needs more.  Any value is correct; a close one
+        balances ragged batches better."""
+        total = int(self.h_pages.sum()) if total_pages is None else int(total_pages)
+        self.cfg = dataclasses.replace(self.cfg, decode_total_pages=total)
+        need = kitty.decode_workspace_bytes(self.cfg, self.B, self.max_pages)
+        if need > self.workspace.numel() * 4:
+            self.workspace = torch.empty(need // 4, dtype=torch.float32, device=self.pool.device)
 
     def plan_flush(self) -> np.ndarray:
         """Host decision for the next append: a fresh page id for each sequence whose

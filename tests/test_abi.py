@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(K):
     for n in names:
         assert hasattr(lib, n), n
     assert set(K.EXPORTS) == names
-    assert lib.kitty_abi_version() == 1
+    assert lib.kitty_abi_version() == 2
 
 
 def test_page_bytes_and_avg_bits(K):
@@ -110,6 +110,13 @@ def test_decode_plan_and_workspace(K):
         s, c = K.decode_plan(cfg, B, M)
         assert 1 <= s <= 256 and c <= M and s * c >= M, (B, M, s, c)
     assert K.decode_plan(cfg, 5, 0)[0] == 1
+    # planning hint: the batch's total pages; pieces stay within one slot's fair share
+    for B, M, tot in ((8, 2048, 8 * 1280), (64, 256, 64 * 256), (177, 257, 177 * 256)):
+        h = K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=tot)
+        s, c = K.decode_plan(h, B, M)
+        assert 1 <= s <= 256 and c <= M and s * c >= M, (B, M, s, c)
+    with pytest.raises(K.KittyError):
+        K.decode_plan(K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=-1), 4, 16)
     cfg.decode_pages_per_split = 1000
     assert K.decode_plan(cfg, 16, 128) == (1, 128)
     assert K.decode_workspace_bytes(cfg, 16, 128) == 0

@@ -81,6 +81,33 @@ def test_quantize_running_bit_exact(mode, lo_bit):
     assert (run[2].cpu().numpy() == rc).all()
 
 
+def test_decode_with_plan_hint():
+    """The total-pages planning hint changes only the split layout: a ragged
+    batch decodes within tolerance with the exact, a stale and a large hint."""
+    import torch
+    from mixed_precision_bit_gb300 import kitty
+    w = _variant("small_gqa", pages=np.array([37, 1, 90]), tails=np.array([0, 5, 17]))
+    inp = synth.host_inputs(w, seed=8)
+    pool, _ = gpu_quantize(w, inp)
+    ref, _ = oracle_decode(w, inp, pool.cpu().numpy())
+    for hint in (int(w.pages.sum()), 5, 100000):
+        cfg = cfg_for(w)
+        cfg.decode_total_pages = hint
+        bt = inp["block_table"]
+        ws = torch.empty(max(kitty.decode_workspace_bytes(cfg, w.B, bt.shape[1]), 16) // 4,
+                         dtype=torch.float32, device="cuda")
+        out = torch.empty((w.B, w.Hq, 128), dtype=torch.float32, device="cuda")
+        st = torch.zeros(1, dtype=torch.int32, device="cuda")
+        kitty.decode_attention(cfg, dev16(inp["q"]), pool, inp["pool_pages"], dev32(bt),
+                               dev32(inp["num_pages"]), dev16(inp["tail_k"]), dev16(inp["tail_v"]),
+                               dev32(inp["tail_len"]), float(np.float32(1 / np.sqrt(128))), out,
+                               workspace=ws, status=st)
+        torch.cuda.synchronize()
+        assert int(st.item()) == 0
+        excess, rel = attn_error(out.cpu().numpy().astype(np.float64), ref)
+        assert excess <= 0, "hint %d: max err %.3e of RMS" % (hint, rel)
+
+
 def test_quantize_bad_seq_status():
     """A seq_of_page entry outside [0, n_seqs) is reported; the other pages of
     the batch are quantized as usual (bit-exact with a batch without the bad

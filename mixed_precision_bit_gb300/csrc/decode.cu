@@ -836,15 +836,38 @@ __global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
   const int bh = blockIdx.x, b = bh / p.Hq, c = threadIdx.x;
   const float* base = p.ws + (size_t)bh * p.splits * kPartial;
   float ms = -INFINITY;
-  for (int s = 0; s < p.splits; ++s) ms = fmaxf(ms, base[s * kPartial]);
   float L = 0.f, O = 0.f;
-  if (ms != -INFINITY) {
-    for (int s = 0; s < p.splits; ++s) {
-      const float m = base[s * kPartial];
-      if (m == -INFINITY) continue;
-      const float e = ex2(m - ms);
-      L += base[s * kPartial + 1] * e;
-      O += base[s * kPartial + 2 + c] * e;
+  constexpr int kU = 8;
+  if (p.splits <= kU) {
+    // every split's (m, l, o[c]) in one round of independent loads
+    float m[kU], l[kU], o[kU];
+#pragma unroll
+    for (int s = 0; s < kU; ++s) {
+      m[s] = s < p.splits ? base[s * kPartial] : -INFINITY;
+      l[s] = s < p.splits ? base[s * kPartial + 1] : 0.f;
+      o[s] = s < p.splits ? base[s * kPartial + 2 + c] : 0.f;
+    }
+#pragma unroll
+    for (int s = 0; s < kU; ++s) ms = fmaxf(ms, m[s]);
+    if (ms != -INFINITY) {
+#pragma unroll
+      for (int s = 0; s < kU; ++s) {
+        if (m[s] == -INFINITY) continue;  // no pages: l, o were never written
+        const float e = ex2(m[s] - ms);
+        L += l[s] * e;
+        O += o[s] * e;
+      }
+    }
+  } else {
+    for (int s = 0; s < p.splits; ++s) ms = fmaxf(ms, base[s * kPartial]);
+    if (ms != -INFINITY) {
+      for (int s = 0; s < p.splits; ++s) {
+        const float m = base[s * kPartial];
+        if (m == -INFINITY) continue;
+        const float e = ex2(m - ms);
+        L += base[s * kPartial + 1] * e;
+        O += base[s * kPartial + 2 + c] * e;
+      }
     }
   }
   store_out(p.out, p.out_dtype, (size_t)bh * kD + c, L > 0.f ? O / L : 0.f);

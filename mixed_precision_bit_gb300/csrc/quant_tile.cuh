@@ -83,6 +83,10 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
   return q;
 }
 
+// rint(fl(d / u)): the correctly rounded division, out of line (it is taken
+// only near a rounding tie, and inlining it at every code site bloats the code).
+__device__ __noinline__ float rint_div(float d, float u) { return rintf(__fdiv_rn(d, u)); }
+
 // code = clamp(rint(fl((x - M) / u)), 0, L), bit-exact with an IEEE division.
 // The quotient is taken as (x - M) * (1/u), within 2^-21 relative of the true
 // value (so within 2^-17 for L <= 15 and 2^-13 for L = 255 inside the clamp
@@ -94,17 +98,16 @@ __device__ __forceinline__ uint32_t qcode(float x, const QuantParams& q, int lev
   const float y = __fmul_rn(d, q.ru);
   float n = rintf(y);
   const float window = levels > 15 ? 0x1p-12f : 0x1p-15f;
-  if (fabsf(fabsf(__fsub_rn(y, n)) - 0.5f) < window && y > -1.5f && y < (float)levels + 1.5f)
-    n = rintf(__fdiv_rn(d, q.u));
+  // near a tie the division decides (outside [0, L] the clamp makes it moot, but
+  // taking it there too is harmless)
+  if (fabsf(fabsf(__fsub_rn(y, n)) - 0.5f) < window) n = rint_div(d, q.u);
   n = fminf(fmaxf(n, 0.0f), (float)levels);
   return (uint32_t)n;
 }
 
-// Largest |16-bit input| class in a 32-bit word pair: 0 ok, RANGE, NONFINITE.
+// Class of the largest |16-bit input| m (sign bits cleared): 0 ok, RANGE, NONFINITE.
 template <int DT>
-__device__ __forceinline__ int range_class(uint32_t w) {
-  const uint32_t lo = w & 0x7FFFu, hi = (w >> 16) & 0x7FFFu;
-  const uint32_t m = lo > hi ? lo : hi;
+__device__ __forceinline__ int range_class_of(uint32_t m) {
   if (DT == KITTY_BF16) return m >= 0x7F80u ? KITTY_ST_NONFINITE : (m >= 0x4780u ? KITTY_ST_RANGE : 0);
   return m >= 0x7C00u ? KITTY_ST_NONFINITE : 0;  // fp16 finite values never exceed 65504
 }
@@ -187,7 +190,7 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
   for (int i = tid; i < nwords; i += kQThreads) sm.blob[i] = 0u;
 
   // ---- stage the raw 16-bit tile (16-byte loads and stores), classify the range
-  int bad = 0;
+  uint32_t amax = 0u;  // per 16-bit half: the largest |input| bits seen
 #pragma unroll
   for (int it = 0; it < kPage * (kD / 8) / kQThreads; ++it) {
     const int idx = tid + it * kQThreads;
@@ -196,13 +199,13 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     const uint4 b = *reinterpret_cast<const uint4*>(vsrc + (size_t)t * row_stride + ch);
     *reinterpret_cast<uint4*>(&sm.xk[t][ch]) = a;
     *reinterpret_cast<uint4*>(&sm.xv[t][ch]) = b;
-    const int c = max(max(max(range_class<DT>(a.x), range_class<DT>(a.y)),
-                          max(range_class<DT>(a.z), range_class<DT>(a.w))),
-                      max(max(range_class<DT>(b.x), range_class<DT>(b.y)),
-                          max(range_class<DT>(b.z), range_class<DT>(b.w))));
-    bad = max(bad, c);
+    amax = __vmaxu2(amax, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                   __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+    amax = __vmaxu2(amax, __vmaxu2(__vmaxu2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
+                                   __vmaxu2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
   }
   __syncthreads();  // tile staged; sm.bad reset by thread 0 is visible
+  const int bad = range_class_of<DT>(max(amax & 0xFFFFu, amax >> 16));
   if (bad) atomicCAS(&sm.bad, 0, bad);
 
   // ---- Key channel statistics and variance (thread = channel c)

@@ -98,11 +98,11 @@ __device__ __forceinline__ uint32_t qcode(float x, const QuantParams& q, int lev
   const float y = __fmul_rn(d, q.ru);
   float n = rintf(y);
   const float window = levels > 15 ? 0x1p-12f : 0x1p-15f;
-  // near a tie the division decides (outside [0, L] the clamp makes it moot, but
-  // taking it there too is harmless)
-  if (fabsf(fabsf(__fsub_rn(y, n)) - 0.5f) < window) n = rint_div(d, q.u);
-  n = fminf(fmaxf(n, 0.0f), (float)levels);
-  return (uint32_t)n;
+  // near a tie (|y - n| is at most 1/2) the division decides; outside [0, L] the
+  // clamp makes it moot, but taking it there too is harmless
+  if (fabsf(__fsub_rn(y, n)) > 0.5f - window) n = rint_div(d, q.u);
+  // n is integral: a saturating conversion clamps below at 0, min() above at L
+  return min(__float2uint_rz(n), (uint32_t)levels);
 }
 
 // Class of the largest |16-bit input| m (sign bits cleared): 0 ok, RANGE, NONFINITE.
@@ -267,26 +267,19 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
       // 2-bit codes: word (lane 4r+qq, tile j) holds tokens 16mt + 8rh + r at 2*(2mt + rh)
 #pragma unroll
       for (int r = 0; r < 8; ++r) {
-        uint32_t w = 0;
-#pragma unroll
-        for (int tau = 0; tau < 4; ++tau) {
-          const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
-          const uint32_t cb = boosted ? (code[t] >> 2) : code[t];
-          w |= cb << (bitbase + 2 * tau);
-        }
-        atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 8 + j], w);
+        // the four codes of this lane's byte, at 2*tau, then shifted into place once
+        const int sh = boosted ? 2 : 0;
+        const uint32_t w = (code[r] >> sh) | ((code[r + 8] >> sh) << 2) |
+                           ((code[r + 16] >> sh) << 4) | ((code[r + 24] >> sh) << 6);
+        atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 8 + j], w << bitbase);
       }
       if (boosted) {
         const int wpl = n_hi / 16;
 #pragma unroll
         for (int r = 0; r < 8; ++r) {
-          uint32_t w = 0;
-#pragma unroll
-          for (int tau = 0; tau < 4; ++tau) {
-            const int t = 16 * (tau >> 1) + 8 * (tau & 1) + r;
-            w |= (code[t] & 3u) << (bx + 2 * tau);
-          }
-          atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w);
+          const uint32_t w = (code[r] & 3u) | ((code[r + 8] & 3u) << 2) |
+                             ((code[r + 16] & 3u) << 4) | ((code[r + 24] & 3u) << 6);
+          atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w << bx);
         }
       }
     } else {
@@ -348,16 +341,11 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     const int bitbase = 16 * e + 8 * half;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      uint32_t w = 0;
-#pragma unroll
-      for (int odd = 0; odd < 2; ++odd) {
-#pragma unroll
-        for (int rh = 0; rh < 2; ++rh) {
-          const int i = odd * 16 + rh * 8 + r;  // channel 32G + i has mc = 2G + odd
-          w |= qcode(v[i], q, 3) << (bitbase + 2 * (2 * odd + rh));
-        }
-      }
-      atomicOr(&sm.blob[lay.vbase / 4 + (4 * r + qq) * 8 + G * 2 + kt], w);
+      // channel 32G + i (i = 16 odd + 8 rh + r) sits at 2*(2 odd + rh): codes of
+      // i = r, r + 8, r + 16, r + 24 at 0, 2, 4, 6, shifted into place once
+      const uint32_t w = qcode(v[r], q, 3) | (qcode(v[r + 8], q, 3) << 2) |
+                         (qcode(v[r + 16], q, 3) << 4) | (qcode(v[r + 24], q, 3) << 6);
+      atomicOr(&sm.blob[lay.vbase / 4 + (4 * r + qq) * 8 + G * 2 + kt], w << bitbase);
     }
   }
   __syncthreads();

@@ -12,22 +12,24 @@
 // (longest-processing-time-first order: the grid ends with little idle time on
 // the SMs).  A split's page range does not depend on the sequence length, so a
 // CTA requests its lengths, query rows and block-table entries together and
-// starts its page copies one memory round trip after it starts.  A warp stages whole (page, kv-head) blobs into shared memory
-// with 1-D bulk copies (cp.async.bulk + mbarrier, 4 stages per warp), then
-// computes, for its g <= 4 query heads:
+// starts its page copies one memory round trip after it starts.  A warp stages
+// whole (page, kv-head) blobs into shared memory with 1-D bulk copies
+// (cp.async.bulk + mbarrier; 4 stages per warp for 2-bit Key planes, 3 for 4-bit
+// planes), then computes, for its g <= 4 query heads:
 //   scores  S^T[t][n] = sum_c code[t][c] * B[c][n] on the tensor cores
 //           (mma.m16n8k16, fp32 accumulate) with B = q*S, the per-channel Key
 //           step folded into the query as an fp16 hi/lo pair (column 2h = hi,
 //           2h+1 = lo of head h), plus the extra plane of the boosted channels
-//           (B = q*S/4 gathered through the channel list) and the q.M term as
-//           a one-row MMA;
+//           (B = q*S/2^W gathered through the channel list, W = Key plane
+//           width) and the q.M term as a one-row MMA;
 //   softmax fp32 online (max, rescale, exp2) in registers;
 //   PV      O^T[c][n] = sum_t vcode[c][t] * P'[t][n] with P' = p*S_v per
 //           Value group as an fp16 hi/lo pair, plus the sum_t p*M_v term.
-// 2-bit codes are unpacked with one AND each: the planes are stored in
-// fragment order, so a masked 16-bit half is the fp16 subnormal
-// code * 2^(2*tau - 24); the power of two depends only on the tile row and is
-// folded into the score scale (Keys) or the final output (Values).
+// Codes are unpacked with one AND per two: the planes are stored in fragment
+// order, so a masked 16-bit half is the fp16 subnormal code * 2^(2*tau - 24)
+// (2-bit planes) or code * 2^(4*(tau & 1) - 24) (4-bit Key planes); the power of
+// two depends only on the tile row and is folded into the score scale (Keys) or
+// the final output (Values).
 #include "kitty_common.cuh"
 #include "quant_tile.cuh"
 #include "host_common.h"

@@ -255,3 +255,34 @@ def test_append_matches_oracle():
     got = gpu_decode(w, inp, g["pool"])
     ref, _ = oracle_decode(w, inp, o["pool"])
     assert attn_error(got, ref)[0] <= 0
+
+
+def test_determinism():
+    """Two runs of the same quantize and decode give bitwise-equal pools and outputs
+    (fixed split layout, fixed combine order, no atomics on data)."""
+    for mode in (0, 1):
+        w = _variant("small_gqa", pages=np.array([33, 2, 40]), tails=np.array([9, 0, 31]))
+        inp = synth.host_inputs(w, seed=12)
+        pa, _ = gpu_quantize(w, inp, mode=mode)
+        pb, _ = gpu_quantize(w, inp, mode=mode)
+        assert (pa.cpu().numpy() == pb.cpu().numpy()).all()
+        oa = gpu_decode(w, inp, pa, pps=8)
+        ob = gpu_decode(w, inp, pa, pps=8)
+        assert (oa.view(np.uint64) == ob.view(np.uint64)).all()
+
+
+def test_grouped_heads_equal_single_head_calls():
+    """A kv head's g query heads decoded together agree with g separate one-head
+    calls over the same kv cache: query head hq reads kv head hq / g."""
+    w = _variant("small_gqa", Hq=8, Hkv=2, pages=np.array([12, 5, 20]), tails=np.array([3, 30, 0]))
+    inp = synth.host_inputs(w, seed=13)
+    pool, _ = gpu_quantize(w, inp)
+    together = gpu_decode(w, inp, pool)
+    g = w.g
+    for h in range(g):
+        w1 = dataclasses.replace(w, Hq=w.Hkv)          # one query head per kv head
+        inp1 = dict(inp, q=np.ascontiguousarray(inp["q"][:, h::g]))
+        alone = gpu_decode(w1, inp1, pool)
+        ref = together[:, h::g]
+        scale = np.sqrt(np.mean(ref ** 2))
+        assert np.abs(alone - ref).max() <= 1e-6 * scale, h

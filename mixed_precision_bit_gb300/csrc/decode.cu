@@ -48,6 +48,11 @@ constexpr int kDWarps = 4;
 __host__ __device__ constexpr int stages_for(int w) { return w == 4 ? 3 : 4; }
 constexpr int kDMinBlocks = 4;  // resident CTAs per SM the register budget is sized for
 constexpr int kDThreads = kDWarps * 32;
+// a flush quantizes the tail in the stage buffers: they must hold the page
+// quantizer's shared state at the smallest blob (n_hi = 0) of either width
+static_assert(sizeof(QuantSmem) <= (size_t)kDWarps * stages_for(2) * 3072 &&
+                  sizeof(QuantSmem) <= (size_t)kDWarps * stages_for(4) * 4096,
+              "page quantizer state does not fit in the decode stage buffers");
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of one barrier phase (~0.1-1 s)
 constexpr int kPartial = kD + 2;           // split partial: m, l, o[128]
 constexpr int kMaxSplits = 256;            // splits per sequence, at most

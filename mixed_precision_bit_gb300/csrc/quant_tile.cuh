@@ -27,7 +27,9 @@ struct QuantSmem {
   uint16_t xk[kPage][kRowH];  // raw 16-bit inputs, token-major
   uint16_t xv[kPage][kRowH];
   uint32_t blob[kMaxBlobWords];
-  int warp_cnt[kQThreads / 32];
+  uint32_t key[kD];           // order-preserving variance key of each Key channel
+  uint32_t boost[kD / 32];    // boost flag of channel c: bit c & 31 of word c >> 5
+  float2 kmm[kD];             // Key channel minimum and maximum, kept over the Value phase
   int bad;
 };
 
@@ -79,7 +81,9 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
     q.Sbits = __half_as_ushort(Sh);
     q.u = __half2float(Sh);
   }
-  q.ru = rcp_approx(q.u);
+  // u == 0: ru = 0 makes every code of a finite input 0, and no quotient lands
+  // near a tie, so the division below is never taken
+  q.ru = q.u == 0.0f ? 0.0f : rcp_approx(q.u);
   return q;
 }
 
@@ -87,22 +91,37 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
 // only near a rounding tie, and inlining it at every code site bloats the code).
 __device__ __noinline__ float rint_div(float d, float u) { return rintf(__fdiv_rn(d, u)); }
 
-// code = clamp(rint(fl((x - M) / u)), 0, L), bit-exact with an IEEE division.
-// The quotient is taken as (x - M) * (1/u), within 2^-21 relative of the true
-// value (so within 2^-17 for L <= 15 and 2^-13 for L = 255 inside the clamp
-// range); where that lands within 2^-15 (L <= 15) or 2^-12 (L = 255) of a
-// rounding tie, the correctly rounded division decides.  u == 0 gives code 0.
-__device__ __forceinline__ uint32_t qcode(float x, const QuantParams& q, int levels) {
-  if (q.u == 0.0f) return 0u;
-  const float d = __fsub_rn(x, q.M);
-  const float y = __fmul_rn(d, q.ru);
-  float n = rintf(y);
-  const float window = levels > 15 ? 0x1p-12f : 0x1p-15f;
-  // near a tie (|y - n| is at most 1/2) the division decides; outside [0, L] the
-  // clamp makes it moot, but taking it there too is harmless
-  if (fabsf(__fsub_rn(y, n)) > 0.5f - window) n = rint_div(d, q.u);
+// Codes of four values: code = clamp(rint(fl((x - M) / u)), 0, L), bit-exact
+// with an IEEE division.  The quotient is taken as (x - M) * (1/u), within
+// 2^-21 relative of the true value (so within 2^-17 for L <= 15 and 2^-13 for
+// L = 255 inside the clamp range); where one lands within 2^-15 (L <= 15) or
+// 2^-12 (L = 255) of a rounding tie, the correctly rounded division decides
+// it.  One branch covers the four (a tie is rare).
+__device__ __forceinline__ void qcode4(const float (&x)[4], const QuantParams& q, int levels,
+                                       uint32_t (&code)[4]) {
+  const float edge = 0.5f - (levels > 15 ? 0x1p-12f : 0x1p-15f);
+  float d[4], n[4];
+  float worst = 0.0f;  // largest |y - rint(y)|; a NaN quotient never counts
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    d[k] = __fsub_rn(x[k], q.M);
+    const float y = __fmul_rn(d[k], q.ru);
+    n[k] = rintf(y);
+    worst = fmaxf(worst, fabsf(__fsub_rn(y, n[k])));
+  }
+  if (worst > edge) {
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+      if (fabsf(__fsub_rn(__fmul_rn(d[k], q.ru), n[k])) > edge) n[k] = rint_div(d[k], q.u);
+  }
   // n is integral: a saturating conversion clamps below at 0, min() above at L
-  return min(__float2uint_rz(n), (uint32_t)levels);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) code[k] = min(__float2uint_rz(n[k]), (uint32_t)levels);
+}
+
+// One byte of four 2-bit codes, at bits 0, 2, 4, 6.
+__device__ __forceinline__ uint8_t pack4x2(uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  return (uint8_t)(a | (b << 2) | (c << 4) | (d << 6));
 }
 
 // Class of the largest |16-bit input| m (sign bits cleared): 0 ok, RANGE, NONFINITE.
@@ -119,29 +138,83 @@ __device__ __forceinline__ uint32_t var_key(float v) {
   return (b & 0x80000000u) ? ~b : (b | 0x80000000u);
 }
 
-// Top-k boost flag of channel threadIdx.x: true iff fewer than n_hi channels have
-// a larger variance, or an equal variance and a lower index.  The n_hi-th
-// largest key T is found by a bitwise threshold search; ties at T go to the
-// lowest channels.  Called by all 128 threads.
-__device__ __forceinline__ bool topk_flag(QuantSmem& sm, float var, int n_hi) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (n_hi >= kD) return true;
-  if (n_hi <= 0) return false;
-  const uint32_t key = var_key(var);
-  uint32_t T = 0u;
-  for (int bit = 31; bit >= 0; --bit) {
-    const uint32_t cand = T | (1u << bit);
-    if (__syncthreads_count(key >= cand) >= n_hi) T = cand;
+// Boost masks of the n_hi largest keys of sm.key, ties going to the lowest
+// channels: channel c is boosted iff fewer than n_hi channels have a larger key,
+// or an equal key and a lower index.  Run by one full warp once sm.key is
+// visible; lane l holds the keys of channels l, l + 32, l + 64, l + 96.  A
+// bitwise threshold search for the n_hi-th largest key T starts below the
+// leading bits that every key shares and stops early once exactly n_hi keys
+// are >= the threshold so far (then they are the set); no block barrier is
+// taken.
+__device__ __forceinline__ void topk_masks(QuantSmem& sm, int n_hi) {
+  const int lane = threadIdx.x & 31;
+  constexpr uint32_t kAll = 0xFFFFFFFFu;
+  if (n_hi >= kD || n_hi <= 0) {
+    if (lane < kD / 32) sm.boost[lane] = n_hi > 0 ? kAll : 0u;
+    return;
   }
-  const int n_gt = __syncthreads_count(key > T);
-  const bool tie = key == T;
-  const uint32_t tb = __ballot_sync(0xFFFFFFFFu, tie);
-  if (lane == 0) sm.warp_cnt[warp] = __popc(tb);
+  uint32_t k[4];
+#pragma unroll
+  for (int m = 0; m < 4; ++m) k[m] = sm.key[lane + 32 * m];
+  const uint32_t kmax = __reduce_max_sync(kAll, max(max(k[0], k[1]), max(k[2], k[3])));
+  const uint32_t kmin = __reduce_min_sync(kAll, min(min(k[0], k[1]), min(k[2], k[3])));
+  const uint32_t diff = kmax ^ kmin;
+  // the shared leading bits, zeros below: every key is >= T, so >= n_hi of them
+  const int top = diff ? 31 - __clz(diff) : -1;
+  uint32_t T = top >= 0 ? (kmax & ~((2u << top) - 1u)) : kmax;
+  bool exact = false;  // exactly n_hi keys are >= T: they are the set
+  for (int bit = top; bit >= 0; --bit) {
+    const uint32_t cand = T | (1u << bit);
+    const int cnt = __reduce_add_sync(kAll, (int)(k[0] >= cand) + (int)(k[1] >= cand) +
+                                                (int)(k[2] >= cand) + (int)(k[3] >= cand));
+    if (cnt >= n_hi) {
+      T = cand;
+      if (cnt == n_hi) { exact = true; break; }
+    }
+  }
+  uint32_t mask[4];
+  if (exact) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) mask[m] = __ballot_sync(kAll, k[m] >= T);
+  } else {
+    // T is the n_hi-th largest key: fewer than n_hi keys exceed it, and the rest
+    // of the set are ties at T in channel order
+    int need = n_hi - __reduce_add_sync(kAll, (int)(k[0] > T) + (int)(k[1] > T) +
+                                                  (int)(k[2] > T) + (int)(k[3] > T));
+    const uint32_t below = (1u << lane) - 1u;
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const uint32_t tie = __ballot_sync(kAll, k[m] == T);
+      const uint32_t take = __ballot_sync(kAll, k[m] == T && __popc(tie & below) < need);
+      mask[m] = __ballot_sync(kAll, k[m] > T) | take;
+      need -= __popc(tie);
+    }
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int m = 0; m < 4; ++m) sm.boost[m] = mask[m];
+  }
+}
+
+// Boost flag of channel c and its row in the channel list (the number of
+// boosted channels below c), from sm.boost.
+__device__ __forceinline__ bool boost_of(const QuantSmem& sm, int c, int& row) {
+  const int g = c >> 5;
+  const uint32_t m = sm.boost[g];
+  row = __popc(m & ((1u << (c & 31)) - 1u));
+  for (int w = 0; w < g; ++w) row += __popc(sm.boost[w]);
+  return (m >> (c & 31)) & 1u;
+}
+
+// Top-k boost flag of channel threadIdx.x for a variance given per thread.
+// Called by all 128 threads.
+__device__ __forceinline__ bool topk_flag(QuantSmem& sm, float var, int n_hi) {
+  sm.key[threadIdx.x] = var_key(var);
   __syncthreads();
-  int tie_rank = __popc(tb & ((1u << lane) - 1u));
-  for (int w = 0; w < warp; ++w) tie_rank += sm.warp_cnt[w];
+  if (threadIdx.x < 32) topk_masks(sm, n_hi);
   __syncthreads();
-  return key > T || (tie && tie_rank < n_hi - n_gt);
+  int row;
+  return boost_of(sm, threadIdx.x, row);
 }
 
 // Tree-ordered sum and sum of squares of Key channel threadIdx.x over one
@@ -177,6 +250,11 @@ __device__ void tile_stats(QuantSmem& sm, const uint16_t* ksrc, size_t row_strid
 // ranks on rsum/rsq/rcount as given (running totals that already include this
 // page), leaving them unchanged.
 // W = Key plane width (lo_bit): 2 for the (4, 2) configuration, 4 for (8, 4).
+//
+// Order of work: Key statistics (thread = channel); then warp 0 ranks the
+// channels while the other warps start on the Values (thread 4t+G = token t,
+// group G); then the Key codes.  Every code byte of the blob is written once
+// by one thread with a byte store.
 template <int DT, int W>
 __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_t* vsrc,
                               size_t row_stride, int n_hi, bool running, float& rsum, float& rsq,
@@ -185,9 +263,15 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
   const BlobLayout lay(n_hi, W);
-  const int nwords = lay.bytes / 4;
+  uint8_t* b8 = reinterpret_cast<uint8_t*>(sm.blob);
+  uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
   if (tid == 0) sm.bad = 0;
-  for (int i = tid; i < nwords; i += kQThreads) sm.blob[i] = 0u;
+  // every byte of the blob is written below once the boost set has n_hi
+  // channels, as a ranking's always has; zeros keep the page deterministic
+  // should an imposed set be smaller
+  if (fixed >= 0)
+    for (int i = tid; i < lay.bytes / 16; i += kQThreads)
+      reinterpret_cast<uint4*>(sm.blob)[i] = make_uint4(0u, 0u, 0u, 0u);
 
   // ---- stage the raw 16-bit tile (16-byte loads and stores), classify the range
   uint32_t amax = 0u;  // per 16-bit half: the largest |input| bits seen
@@ -204,115 +288,50 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     amax = __vmaxu2(amax, __vmaxu2(__vmaxu2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
                                    __vmaxu2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
   }
-  __syncthreads();  // tile staged; sm.bad reset by thread 0 is visible
+  __syncthreads();  // tile staged (blob zeroed if so); sm.bad reset by thread 0 is visible
   const int bad = range_class_of<DT>(max(amax & 0xFFFFu, amax >> 16));
   if (bad) atomicCAS(&sm.bad, 0, bad);
 
   // ---- Key channel statistics and variance (thread = channel c)
   const int c = tid;
-  float x[kPage], tmp[kPage];
-#pragma unroll
-  for (int t = 0; t < kPage; ++t) x[t] = bits16_to_f32(sm.xk[t][c], DT);
-  float mn = x[0], mx = x[0];
-#pragma unroll
-  for (int t = 1; t < kPage; ++t) {
-    mn = fminf(mn, x[t]);
-    mx = fmaxf(mx, x[t]);
-  }
-  float var = 0.f;
-  if (fixed == -2) {
-    var = running_var(rsum, rsq, __int2float_rn(rcount));
-  } else if (fixed < 0) {
-#pragma unroll
-    for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
-    const float s1 = tree32(tmp);
-#pragma unroll
-    for (int t = 0; t < kPage; ++t) tmp[t] = __fmul_rn(x[t], x[t]);
-    const float s2 = tree32(tmp);
-    if (running) {
-      rsum = __fadd_rn(rsum, s1);
-      rsq = __fadd_rn(rsq, s2);
-      rcount += kPage;
-      var = running_var(rsum, rsq, __int2float_rn(rcount));
-    } else {
-      var = running_var(s1, s2, (float)kPage);
-    }
-  }
-
-  // ---- top-k (or the caller's fixed boost set)
-  const bool boosted = fixed >= 0 ? (fixed != 0) : topk_flag(sm, var, n_hi);
-  const uint32_t bal = __ballot_sync(0xFFFFFFFFu, boosted);
-  if (lane == 0) sm.warp_cnt[warp] = __popc(bal);
-  __syncthreads();
-  int row = __popc(bal & ((1u << lane) - 1u));
-  for (int w = 0; w < warp; ++w) row += sm.warp_cnt[w];
-
-  // ---- Key quantization of channel c and packing in fragment order
   {
-    constexpr int kLw = (1 << W) - 1;  // w-bit levels; boosted channels have 2w bits
-    const int levels = boosted ? (1 << (2 * W)) - 1 : kLw;
-    const QuantParams q = qparams(mn, mx, levels, boosted, (float)(1 << W));
-    uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
-    b16[lay.ks / 2 + c] = q.Sbits;
-    // minima in fragment order: channel 16j + 8h + 2qq + e at ((qq*8 + j)*2 + h)*2 + e
-    b16[lay.km / 2 + (((((c >> 1) & 3) * 8 + (c >> 4)) * 2 + ((c >> 3) & 1)) * 2 + (c & 1))] = q.Mbits;
-    uint32_t code[kPage];
+    float x[kPage], tmp[kPage], var = 0.f;
 #pragma unroll
-    for (int t = 0; t < kPage; ++t) code[t] = qcode(x[t], q, levels);
-    const int j = c >> 4, half = (c >> 3) & 1, qq = (c >> 1) & 3, e = c & 1;
-    const int bitbase = 16 * e + 8 * half;
-    const int js = row >> 4, hx = (row >> 3) & 1, qx = (row >> 1) & 3, ex = row & 1;
-    const int bx = 16 * ex + 8 * hx;
-    if (W == 2) {
-      // 2-bit codes: word (lane 4r+qq, tile j) holds tokens 16mt + 8rh + r at 2*(2mt + rh)
+    for (int t = 0; t < kPage; ++t) x[t] = bits16_to_f32(sm.xk[t][c], DT);
+    float mn = x[0], mx = x[0];
 #pragma unroll
-      for (int r = 0; r < 8; ++r) {
-        // the four codes of this lane's byte, at 2*tau, then shifted into place once
-        const int sh = boosted ? 2 : 0;
-        const uint32_t w = (code[r] >> sh) | ((code[r + 8] >> sh) << 2) |
-                           ((code[r + 16] >> sh) << 4) | ((code[r + 24] >> sh) << 6);
-        atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 8 + j], w << bitbase);
-      }
-      if (boosted) {
-        const int wpl = n_hi / 16;
+    for (int t = 1; t < kPage; ++t) {
+      mn = fminf(mn, x[t]);
+      mx = fmaxf(mx, x[t]);
+    }
+    if (fixed == -2) {
+      var = running_var(rsum, rsq, __int2float_rn(rcount));
+    } else if (fixed < 0) {
 #pragma unroll
-        for (int r = 0; r < 8; ++r) {
-          const uint32_t w = (code[r] & 3u) | ((code[r + 8] & 3u) << 2) |
-                             ((code[r + 16] & 3u) << 4) | ((code[r + 24] & 3u) << 6);
-          atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + js], w << bx);
-        }
-      }
-    } else {
-      // 4-bit codes: two words per (lane 4r+qq, tile j), one per 16-token block
-      // mt; token 16mt + 8rh + r at nibble 4rh
+      for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
+      const float s1 = tree32(tmp);
 #pragma unroll
-      for (int r = 0; r < 8; ++r)
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-          const int t0 = 16 * mt + r, t1 = t0 + 8;
-          const uint32_t c0 = boosted ? (code[t0] >> 4) : code[t0];
-          const uint32_t c1 = boosted ? (code[t1] >> 4) : code[t1];
-          atomicOr(&sm.blob[lay.kbase / 4 + (4 * r + qq) * 16 + 2 * j + mt],
-                   (c0 << bitbase) | (c1 << (bitbase + 4)));
-        }
-      if (boosted) {
-        const int wpl = 2 * (n_hi / 16);
-#pragma unroll
-        for (int r = 0; r < 8; ++r)
-#pragma unroll
-          for (int mt = 0; mt < 2; ++mt) {
-            const int t0 = 16 * mt + r, t1 = t0 + 8;
-            atomicOr(&sm.blob[lay.kextra / 4 + (4 * r + qx) * wpl + 2 * js + mt],
-                     ((code[t0] & 15u) << bx) | ((code[t1] & 15u) << (bx + 4)));
-          }
+      for (int t = 0; t < kPage; ++t) tmp[t] = __fmul_rn(x[t], x[t]);
+      const float s2 = tree32(tmp);
+      if (running) {
+        rsum = __fadd_rn(rsum, s1);
+        rsq = __fadd_rn(rsq, s2);
+        rcount += kPage;
+        var = running_var(rsum, rsq, __int2float_rn(rcount));
+      } else {
+        var = running_var(s1, s2, (float)kPage);
       }
     }
-    if (boosted) {
-      // channel-list row 16js + 8h + 2qq + e stored at byte js*16 + qq*4 + h*2 + e
-      const int pos = lay.kch + js * 16 + qx * 4 + hx * 2 + ex;
-      atomicOr(&sm.blob[pos / 4], (uint32_t)c << (8 * (pos & 3)));
+    sm.kmm[c] = make_float2(mn, mx);
+    if (fixed >= 0) {  // the caller's boost set
+      const uint32_t bal = __ballot_sync(0xFFFFFFFFu, fixed != 0);
+      if (lane == 0) sm.boost[warp] = bal;
+    } else {
+      sm.key[c] = var_key(var);
     }
   }
+  __syncthreads();  // keys (or imposed flags) visible
+  if (fixed < 0 && warp == 0) topk_masks(sm, n_hi);
 
   // ---- Value quantization: thread 4t+G owns token t, channels 32G..32G+31
   {
@@ -332,20 +351,78 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
 #pragma unroll
     for (int i = 1; i < kVGroup; ++i) { vmn = fminf(vmn, v[i]); vmx = fmaxf(vmx, v[i]); }
     const QuantParams q = qparams(vmn, vmx, 3, false);
-    uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
     // Value metadata in fragment order: token 16kt + 8h + 2qq + e at G*32 + qq*8 + kt*4 + h*2 + e
     const int vpos = G * kPage + ((t >> 1) & 3) * 8 + (t >> 4) * 4 + ((t >> 3) & 1) * 2 + (t & 1);
     b16[lay.vs / 2 + vpos] = q.Sbits;
     b16[lay.vm / 2 + vpos] = q.Mbits;
+    // channel 32G + i (i = 16 odd + 8 rh + r) of token t = 16kt + 8h + 2qq + e sits
+    // in word (4r + qq)*8 + 2G + kt, byte 2e + h, at bits 2*(2 odd + rh): the codes
+    // of i = r, r + 8, r + 16, r + 24 make one byte
     const int qq = (t >> 1) & 3, kt = t >> 4, half = (t >> 3) & 1, e = t & 1;
-    const int bitbase = 16 * e + 8 * half;
+    uint8_t* vb = b8 + lay.vbase + (qq * 8 + 2 * G + kt) * 4 + 2 * e + half;
 #pragma unroll
     for (int r = 0; r < 8; ++r) {
-      // channel 32G + i (i = 16 odd + 8 rh + r) sits at 2*(2 odd + rh): codes of
-      // i = r, r + 8, r + 16, r + 24 at 0, 2, 4, 6, shifted into place once
-      const uint32_t w = qcode(v[r], q, 3) | (qcode(v[r + 8], q, 3) << 2) |
-                         (qcode(v[r + 16], q, 3) << 4) | (qcode(v[r + 24], q, 3) << 6);
-      atomicOr(&sm.blob[lay.vbase / 4 + (4 * r + qq) * 8 + G * 2 + kt], w << bitbase);
+      const float xs[4] = {v[r], v[r + 8], v[r + 16], v[r + 24]};
+      uint32_t cd[4];
+      qcode4(xs, q, 3, cd);
+      vb[128 * r] = pack4x2(cd[0], cd[1], cd[2], cd[3]);
+    }
+  }
+  __syncthreads();  // boost masks visible
+
+  // ---- Key quantization of channel c and packing in fragment order
+  {
+    int row;
+    const bool boosted = boost_of(sm, c, row);
+    constexpr int kLw = (1 << W) - 1;  // w-bit levels; boosted channels have 2w bits
+    const int levels = boosted ? (1 << (2 * W)) - 1 : kLw;
+    const float2 mm = sm.kmm[c];
+    const QuantParams q = qparams(mm.x, mm.y, levels, boosted, (float)(1 << W));
+    b16[lay.ks / 2 + c] = q.Sbits;
+    // minima in fragment order: channel 16j + 8h + 2qq + e at ((qq*8 + j)*2 + h)*2 + e
+    b16[lay.km / 2 + (((((c >> 1) & 3) * 8 + (c >> 4)) * 2 + ((c >> 3) & 1)) * 2 + (c & 1))] = q.Mbits;
+    const int j = c >> 4, half = (c >> 3) & 1, qq = (c >> 1) & 3, e = c & 1;
+    const int js = row >> 4, hx = (row >> 3) & 1, qx = (row >> 1) & 3, ex = row & 1;
+    // channel-list row 16js + 8h + 2qq + e stored at byte js*16 + qq*4 + h*2 + e
+    if (boosted) b8[lay.kch + js * 16 + qx * 4 + hx * 2 + ex] = (uint8_t)c;
+    if (W == 2) {
+      // 2-bit codes: word (4r + qq)*8 + j, byte 2e + h holds tokens r, r + 8,
+      // r + 16, r + 24 at bits 0, 2, 4, 6; the extra plane uses the row's place
+      const int wpl = n_hi / 16;
+      uint8_t* kb = b8 + lay.kbase + (qq * 8 + j) * 4 + 2 * e + half;
+      uint8_t* kx = b8 + lay.kextra + (qx * wpl + js) * 4 + 2 * ex + hx;
+      const int sh = boosted ? 2 : 0;
+#pragma unroll 2
+      for (int r = 0; r < 8; ++r) {
+        float xs[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) xs[k] = bits16_to_f32(sm.xk[r + 8 * k][c], DT);
+        uint32_t cd[4];
+        qcode4(xs, q, levels, cd);
+        kb[128 * r] = pack4x2(cd[0] >> sh, cd[1] >> sh, cd[2] >> sh, cd[3] >> sh);
+        if (boosted) kx[16 * wpl * r] = pack4x2(cd[0] & 3u, cd[1] & 3u, cd[2] & 3u, cd[3] & 3u);
+      }
+    } else {
+      // 4-bit codes: word (4r + qq)*16 + 2j + mt, byte 2e + h holds tokens
+      // 16mt + r (low nibble) and 16mt + r + 8 (high nibble)
+      const int wpl = 2 * (n_hi / 16);
+      uint8_t* kb = b8 + lay.kbase + (qq * 16 + 2 * j) * 4 + 2 * e + half;
+      uint8_t* kx = b8 + lay.kextra + (qx * wpl + 2 * js) * 4 + 2 * ex + hx;
+      const int sh = boosted ? 4 : 0;
+#pragma unroll 2
+      for (int r = 0; r < 8; ++r) {
+        float xs[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) xs[k] = bits16_to_f32(sm.xk[r + 8 * k][c], DT);
+        uint32_t cd[4];
+        qcode4(xs, q, levels, cd);
+        kb[256 * r] = (uint8_t)((cd[0] >> sh) | ((cd[1] >> sh) << 4));
+        kb[256 * r + 4] = (uint8_t)((cd[2] >> sh) | ((cd[3] >> sh) << 4));
+        if (boosted) {
+          kx[16 * wpl * r] = (uint8_t)((cd[0] & 15u) | ((cd[1] & 15u) << 4));
+          kx[16 * wpl * r + 4] = (uint8_t)((cd[2] & 15u) | ((cd[3] & 15u) << 4));
+        }
+      }
     }
   }
   __syncthreads();

@@ -170,3 +170,103 @@ class LayerCache:
         pages = int(self.h_pages.sum())
         return (pages * Hkv * self.blob + int(self.h_tail.sum()) * Hkv * D * 2 * 2
                 + self.B * Hq * D * 2 * 2 + pages * 4)
+
+
+class ServingStep:
+    """One decode step of every layer from pinned host memory, with the copies
+    overlapped with the kernels.
+
+    Per layer, the query rows, the new Key/Value token and the flush ids sit
+    in one contiguous pinned block (views: q[l], k_new[l], v_new[l]; the caller
+    writes q, k_new and v_new before run()), copied up with one transfer on an
+    upload stream; the layer's call waits only for its own block, and its
+    output comes back on a download stream while later layers compute.  The
+    flush plan of layer l is made on the host just before its block goes up,
+    so planning overlaps the kernels of the layers before it.  run() returns
+    once every output is in `out` (pinned host, [L][B][Hq][D]).
+
+    graphs=True replays each layer's fused call as a CUDA graph captured on
+    the device buffers; fused=False runs append then attend per layer.
+    """
+
+    def __init__(self, layers, graphs: bool = True, fused: bool = True, sm_scale=None):
+        self.layers = layers
+        lc0 = layers[0]
+        L, B = len(layers), lc0.B
+        Hq, Hkv = lc0.cfg.num_q_heads, lc0.cfg.num_kv_heads
+        dev = lc0.pool.device
+        self.sizes = [B * Hq * D * 2, B * Hkv * D * 2, B * Hkv * D * 2, B * 4]
+        per = sum(self.sizes)
+        self.block = (per + 255) // 256 * 256  # 256-byte aligned per-layer blocks
+        self.h_in = torch.empty(L * self.block, dtype=torch.uint8).pin_memory()
+        self.d_in = torch.empty(L * self.block, dtype=torch.uint8, device=dev)
+        self.q, self.k_new, self.v_new, self.flush = [], [], [], []
+        self._dq, self._dk, self._dv, self._dfl = [], [], [], []
+        for l in range(L):
+            hv_, dv_ = self._views(self.h_in, l, B, Hq, Hkv), self._views(self.d_in, l, B, Hq, Hkv)
+            for lst, x in zip((self.q, self.k_new, self.v_new, self.flush), hv_):
+                lst.append(x)
+            for lst, x in zip((self._dq, self._dk, self._dv, self._dfl), dv_):
+                lst.append(x)
+        out_dt = torch.bfloat16 if lc0.cfg.in_dtype == kitty.BF16 else torch.float16
+        self.d_out = torch.empty((L, B, Hq, D), dtype=out_dt, device=dev)
+        self.out = torch.empty((L, B, Hq, D), dtype=out_dt).pin_memory()
+        self.up, self.down = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        self.ev_in = [torch.cuda.Event() for _ in range(L)]
+        self.ev_out = [torch.cuda.Event() for _ in range(L)]
+        self.fused, self.sm_scale = fused, sm_scale
+        self.graphs = None
+        if graphs:
+            if fused:
+                self.graphs = [(None, lc.capture_step(self._dk[l], self._dv[l], self._dfl[l],
+                                                      self._dq[l], self.d_out[l], sm_scale))
+                               for l, lc in enumerate(layers)]
+            else:
+                self.graphs = [lc.capture(self._dk[l], self._dv[l], self._dfl[l], self._dq[l],
+                                          self.d_out[l], sm_scale)
+                               for l, lc in enumerate(layers)]
+
+    def _views(self, buf, l, B, Hq, Hkv):
+        o = l * self.block
+        s = self.sizes
+        q = buf[o:o + s[0]].view(torch.int16).view(B, Hq, D)
+        k = buf[o + s[0]:o + s[0] + s[1]].view(torch.int16).view(B, Hkv, D)
+        v = buf[o + s[0] + s[1]:o + s[0] + s[1] + s[2]].view(torch.int16).view(B, Hkv, D)
+        f = buf[o + s[0] + s[1] + s[2]:o + s[0] + s[1] + s[2] + s[3]].view(torch.int32)
+        return q, k, v, f
+
+    def bytes_up(self) -> int:
+        return len(self.layers) * sum(self.sizes)
+
+    def bytes_down(self) -> int:
+        return self.out.numel() * self.out.element_size()
+
+    def run(self):
+        cur = torch.cuda.current_stream()
+        # the device input blocks and outputs may still be in use by work queued
+        # before this call
+        self.up.wait_stream(cur)
+        self.down.wait_stream(cur)
+        for l, lc in enumerate(self.layers):
+            self.flush[l].numpy()[:] = lc.plan_flush()
+            o = l * self.block
+            with torch.cuda.stream(self.up):
+                self.d_in[o:o + self.block].copy_(self.h_in[o:o + self.block], non_blocking=True)
+                self.ev_in[l].record(self.up)
+            cur.wait_event(self.ev_in[l])
+            if self.graphs is not None:
+                if self.graphs[l][0] is not None:
+                    self.graphs[l][0].replay()
+                self.graphs[l][1].replay()
+            elif self.fused:
+                lc.step(self._dk[l], self._dv[l], self._dfl[l], self._dq[l], self.d_out[l],
+                        self.sm_scale)
+            else:
+                lc.append(self._dk[l], self._dv[l], self._dfl[l])
+                lc.attend(self._dq[l], self.d_out[l], self.sm_scale)
+            self.ev_out[l].record(cur)
+            with torch.cuda.stream(self.down):
+                self.down.wait_event(self.ev_out[l])
+                self.out[l].copy_(self.d_out[l], non_blocking=True)
+        self.down.synchronize()
+        return self.out

@@ -110,6 +110,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Programmatic dependent launch: a dependent grid may start once every CTA of
+// this grid has called trigger_dependents (or exited); wait blocks until this
+// grid has completed and its memory is visible.  Both are no-ops for a grid
+// launched without the attribute.
+__device__ __forceinline__ void trigger_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void grid_dependency_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // Shared-memory loads from a 32-bit shared address plus a compile-time offset.
 template <int OFF>
 __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
@@ -521,6 +532,7 @@ __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, si
 template <int DT, int NX, int W>
 __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
+  trigger_dependents();  // the combine step may be scheduled once every CTA is running
   const int u = blockIdx.x, s = blockIdx.y;
   const int b = u / p.Hkv, kvh = u - b * p.Hkv;
   const int tid = threadIdx.x, wid = tid >> 5;
@@ -838,8 +850,11 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
 // Merge the split partials of one (sequence, query head); 128 threads = channels.
 // Splits without pages left m = -inf.  In a fused append, the CTA of query
 // head 0 then does the sequence's append bookkeeping (every decode CTA has read
-// the old lengths by now).
+// the old lengths by now).  Launched as a programmatic dependent of the decode
+// kernel: it may be scheduled while the decode grid drains, and waits for the
+// whole grid (and its memory) before reading the partials.
 __global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
+  grid_dependency_wait();
   const int bh = blockIdx.x, b = bh / p.Hq, c = threadIdx.x;
   const float* base = p.ws + (size_t)bh * p.splits * kPartial;
   float ms = -INFINITY;
@@ -866,14 +881,33 @@ __global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
       }
     }
   } else {
-    for (int s = 0; s < p.splits; ++s) ms = fmaxf(ms, base[s * kPartial]);
+    // many splits: rounds of kV independent loads, first for the maxima, then
+    // for the sums, which are added in split order as in the branch above
+    constexpr int kV = 16;
+    for (int s0 = 0; s0 < p.splits; s0 += kV) {
+      float m[kV];
+#pragma unroll
+      for (int k = 0; k < kV; ++k) m[k] = s0 + k < p.splits ? base[(s0 + k) * kPartial] : -INFINITY;
+#pragma unroll
+      for (int k = 0; k < kV; ++k) ms = fmaxf(ms, m[k]);
+    }
     if (ms != -INFINITY) {
-      for (int s = 0; s < p.splits; ++s) {
-        const float m = base[s * kPartial];
-        if (m == -INFINITY) continue;
-        const float e = ex2(m - ms);
-        L += base[s * kPartial + 1] * e;
-        O += base[s * kPartial + 2 + c] * e;
+      for (int s0 = 0; s0 < p.splits; s0 += kV) {
+        float m[kV], l[kV], o[kV];
+#pragma unroll
+        for (int k = 0; k < kV; ++k) {
+          const bool in = s0 + k < p.splits;
+          m[k] = in ? base[(s0 + k) * kPartial] : -INFINITY;
+          l[k] = in ? base[(s0 + k) * kPartial + 1] : 0.f;
+          o[k] = in ? base[(s0 + k) * kPartial + 2 + c] : 0.f;
+        }
+#pragma unroll
+        for (int k = 0; k < kV; ++k) {
+          if (m[k] == -INFINITY) continue;
+          const float e = ex2(m[k] - ms);
+          L += l[k] * e;
+          O += o[k] * e;
+        }
       }
     }
   }
@@ -886,6 +920,7 @@ __global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
 
 // Fused append bookkeeping when there is no combine step (one split).
 __global__ void finalize_kernel(const DecodeParams p, int B) {
+  grid_dependency_wait();
   const int b = blockIdx.x * blockDim.x + threadIdx.x;
   if (b < B)
     append_finalize_one(b, p.ap.tail_len, p.ap.flush_page_ids, p.ap.block_table, p.max_pages,
@@ -1120,11 +1155,25 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
       : (cfg->lo_bit == 4 ? launch_decode_nx<KITTY_F16, 4>(cfg->n_hi / 16, grid, smem, s, p)
                           : launch_decode_nx<KITTY_F16, 2>(cfg->n_hi / 16, grid, smem, s, p));
   if (e != cudaSuccess) return KITTY_ERR_CUDA;
-  if (sc.splits > 1)
-    combine_kernel<<<B * cfg->num_q_heads, kD, 0, s>>>(p);
-  else if (ap.k_new != nullptr)
-    finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(p, B);
-  return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
+  // the merge step follows the decode grid as a programmatic dependent
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t lc = {};
+  lc.stream = s;
+  lc.attrs = attr;
+  lc.numAttrs = 1;
+  cudaError_t e2 = cudaSuccess;
+  if (sc.splits > 1) {
+    lc.gridDim = dim3((unsigned)B * cfg->num_q_heads);
+    lc.blockDim = dim3(kD);
+    e2 = cudaLaunchKernelEx(&lc, combine_kernel, p);
+  } else if (ap.k_new != nullptr) {
+    lc.gridDim = dim3((unsigned)(B + 127) / 128);
+    lc.blockDim = dim3(128);
+    e2 = cudaLaunchKernelEx(&lc, finalize_kernel, p, (int)B);
+  }
+  return e2 == cudaSuccess && cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
 }
 
 }  // namespace

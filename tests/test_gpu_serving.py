@@ -1,0 +1,86 @@
+"""GPU check of the pipelined multi-layer serving step (cache.ServingStep).
+
+Its copies run on side streams, overlapped with the kernels. Over many decode
+steps with page flushes, it must give outputs and cache state bit-identical to
+the plain per-layer fused calls (LayerCache.step) on the same inputs. The fused
+call itself is checked against the oracle in test_gpu_fused.py."""
+
+import numpy as np
+import pytest
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _cuda():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixed_precision_bit_gb300 import kitty
+    kitty.load()
+
+
+def _layers(L, B, Hkv, Hq, n_hi, pages, tails, gen):
+    import torch
+    from mixed_precision_bit_gb300 import kitty
+    from mixed_precision_bit_gb300.cache import LayerCache
+    cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=Hq, n_hi=n_hi, in_dtype=kitty.BF16,
+                       rank_mode=kitty.RANK_RUNNING)
+    max_pages = int(max(pages)) + 4
+    pool_pages = int(sum(pages)) + B * 4
+    out = []
+    for _ in range(L):
+        lc = LayerCache(cfg, B, max_pages, pool_pages)
+        tot = int(sum(pages))
+        kp = (torch.randn((tot * 32, Hkv, 128), generator=gen, device="cuda") *
+              torch.exp(torch.randn((1, Hkv, 128), generator=gen, device="cuda")))
+        vp = torch.randn((tot * 32, Hkv, 128), generator=gen, device="cuda")
+        kt = torch.randn((B, Hkv, 32, 128), generator=gen, device="cuda")
+        vt = torch.randn((B, Hkv, 32, 128), generator=gen, device="cuda")
+        bf = lambda x: x.to(torch.bfloat16).view(torch.int16)
+        lc.prefill(bf(kp), bf(vp), pages, bf(kt), bf(vt), tails)
+        out.append(lc)
+    torch.cuda.synchronize()
+    return out
+
+
+@pytest.mark.parametrize("graphs", [True, False])
+def test_serving_step_matches_per_layer_calls(graphs):
+    import torch
+    from mixed_precision_bit_gb300.cache import ServingStep
+    L, B, Hkv, Hq, n_hi = 3, 5, 2, 8, 32
+    pages, tails = [3, 1, 0, 2, 4], [30, 31, 5, 0, 17]
+    ref = _layers(L, B, Hkv, Hq, n_hi, pages, tails, torch.Generator("cuda").manual_seed(3))
+    new = _layers(L, B, Hkv, Hq, n_hi, pages, tails, torch.Generator("cuda").manual_seed(3))
+    # a first plain call outside any graph capture
+    q0 = torch.zeros((B, Hq, 128), dtype=torch.int16, device="cuda")
+    o0 = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    new[0].attend(q0, o0)
+    torch.cuda.synchronize()
+    srv = ServingStep(new, graphs=graphs)
+    g = torch.Generator("cuda").manual_seed(5)
+    d_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    flushes = 0
+    for step in range(40):
+        q = torch.randn((L, B, Hq, 128), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+        k = torch.randn((L, B, Hkv, 128), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+        v = torch.randn((L, B, Hkv, 128), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+        for l in range(L):
+            srv.q[l].copy_(q[l].cpu())
+            srv.k_new[l].copy_(k[l].cpu())
+            srv.v_new[l].copy_(v[l].cpu())
+        got = srv.run().clone()
+        for l, lc in enumerate(ref):
+            fl = lc.plan_flush()
+            flushes += int((fl >= 0).sum())
+            lc.step(k[l], v[l], torch.from_numpy(fl).cuda(), q[l], d_out)
+            want = d_out.cpu()
+            assert torch.equal(got[l].view(torch.int16), want.view(torch.int16)), (step, l)
+    assert flushes >= 2 * L  # the steps crossed page boundaries
+    torch.cuda.synchronize()
+    for a, b in zip(ref, new):
+        for name in ("pool", "block_table", "num_pages", "tail_k", "tail_v", "tail_len",
+                     "run_sum", "run_sumsq", "run_count", "status"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), name
+        assert int(b.status.item()) == 0
+    assert srv.bytes_up() == L * (B * Hq * 128 * 2 + 2 * B * Hkv * 128 * 2 + B * 4)

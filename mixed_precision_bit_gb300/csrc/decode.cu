@@ -606,6 +606,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   const size_t page_stride = (size_t)p.Hkv * kBlob;
   int bt_base = 0;
   uint32_t valid_mask = 0;  // bit st: stage st holds a valid page
+  const uint32_t stage0 = smem_u32(wst), bar0 = smem_u32(wbar);  // 32-bit shared addresses
   auto issue = [&](int i) {
     if (i - bt_base >= 32) {
       bt_base = i;
@@ -615,16 +616,48 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     const int st = i % kDStages;
     const bool ok = pid >= 0 && pid < p.pool_pages;
     if (lane == 0) {
+      const uint32_t bar = bar0 + 8 * st;
       if (ok) {
-        mbar_arrive_expect_tx(&wbar[st], (uint32_t)kBlob);
-        bulk_g2s(wst + (size_t)st * kBlob, head_base + (size_t)pid * page_stride, (uint32_t)kBlob,
-                 &wbar[st]);
+        mbar_arrive_expect_tx_s(bar, (uint32_t)kBlob);
+        bulk_g2s_s(stage0 + st * kBlob, head_base + (size_t)pid * page_stride, (uint32_t)kBlob, bar);
       } else {
         set_status(p.d_status, KITTY_ST_BAD_PAGE);
-        mbar_arrive(&wbar[st]);
+        mbar_arrive_s(bar);
       }
     }
     valid_mask = ok ? (valid_mask | (1u << st)) : (valid_mask & ~(1u << st));
+  };
+  // refill of a pair: pages i and i + 1 (if any) under one elected-lane branch
+  auto issue2 = [&](int i) {
+    const bool has1 = i + 1 < npw;
+    if (i + 1 - bt_base >= 32) {
+      bt_base = i;
+      bt_cache = (i + lane < npw) ? bt[first + (i + lane) * kDWarps] : -1;
+    }
+    const int pid0 = __shfl_sync(0xFFFFFFFFu, bt_cache, i - bt_base);
+    const int pid1 = __shfl_sync(0xFFFFFFFFu, bt_cache, i + 1 - bt_base);
+    const int st0 = i % kDStages, st1 = (i + 1) % kDStages;
+    const bool ok0 = pid0 >= 0 && pid0 < p.pool_pages;
+    const bool ok1 = has1 && pid1 >= 0 && pid1 < p.pool_pages;
+    if (lane == 0) {
+      const uint32_t b0 = bar0 + 8 * st0, b1 = bar0 + 8 * st1;
+      if (ok0) {
+        mbar_arrive_expect_tx_s(b0, (uint32_t)kBlob);
+        bulk_g2s_s(stage0 + st0 * kBlob, head_base + (size_t)pid0 * page_stride, (uint32_t)kBlob, b0);
+      } else {
+        set_status(p.d_status, KITTY_ST_BAD_PAGE);
+        mbar_arrive_s(b0);
+      }
+      if (ok1) {
+        mbar_arrive_expect_tx_s(b1, (uint32_t)kBlob);
+        bulk_g2s_s(stage0 + st1 * kBlob, head_base + (size_t)pid1 * page_stride, (uint32_t)kBlob, b1);
+      } else if (has1) {
+        set_status(p.d_status, KITTY_ST_BAD_PAGE);
+        mbar_arrive_s(b1);
+      }
+    }
+    valid_mask = ok0 ? (valid_mask | (1u << st0)) : (valid_mask & ~(1u << st0));
+    if (has1) valid_mask = ok1 ? (valid_mask | (1u << st1)) : (valid_mask & ~(1u << st1));
   };
   const int pro = min(npw, kDStages);
   for (int i = 0; i < pro; ++i) issue(i);
@@ -670,7 +703,6 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   w.m = kNegBig;
   w.l = 0.f;
   bool timed_out = false;
-  const uint32_t stage0 = smem_u32(wst);
   // Pages are taken two at a time: two independent score chains, one joint max
   // and rescale, then both PVs.  A missing or invalid page is masked (score -inf).
   for (int i = 0; i < npw; i += 2) {
@@ -679,8 +711,9 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     // bytes); the exit is warp-uniform and the wait is bounded
     bool done = false;
     for (uint32_t it = 0;; ++it) {
-      done = done || (mbar_test(&wbar[i % kDStages], (uint32_t)(i / kDStages) & 1u) &&
-                      (!hasB || mbar_test(&wbar[(i + 1) % kDStages], (uint32_t)((i + 1) / kDStages) & 1u)));
+      done = done || (mbar_test_s(bar0 + 8 * (i % kDStages), (uint32_t)(i / kDStages) & 1u) &&
+                      (!hasB || mbar_test_s(bar0 + 8 * ((i + 1) % kDStages),
+                                            (uint32_t)((i + 1) / kDStages) & 1u)));
       if (__all_sync(0xFFFFFFFFu, done) || it >= kWaitLimit) break;
       if (it > 64) __nanosleep(32);
     }
@@ -736,8 +769,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       page_pv<NX, W>(w, paA, TA, L);
     }
     __syncwarp();
-    if (i + kDStages < npw) issue(i + kDStages);
-    if (i + 1 + kDStages < npw) issue(i + 1 + kDStages);
+    if (i + kDStages < npw) issue2(i + kDStages);
   }
   if (flush_id >= 0) {
     // the full tail becomes page flush_id (quantized in the idle stage buffers),

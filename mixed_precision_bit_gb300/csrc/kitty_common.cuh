@@ -146,6 +146,32 @@ __device__ __forceinline__ void bulk_g2s_s(uint32_t dst, const void* src, uint32
       : "memory");
 }
 
+// Packed fp32x2 arithmetic: two IEEE round-to-nearest operations (no flush to
+// zero) in one instruction, lane for lane the same results as __fadd_rn etc.
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t r, float& a, float& b) {
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(a), "=f"(b) : "l"(r));
+}
+__device__ __forceinline__ void add2_rn(float& a, float& b, float c, float d) {  // (a, b) += (c, d)
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(a, b)), "l"(f2pack(c, d)));
+  f2unpack(r, a, b);
+}
+__device__ __forceinline__ void sub2_rn(float& ra, float& rb, float a, float b, float c, float d) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(a, b)), "l"(f2pack(c, d)));
+  f2unpack(r, ra, rb);
+}
+__device__ __forceinline__ void mul2_rn(float& ra, float& rb, float a, float b, float c, float d) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(f2pack(a, b)), "l"(f2pack(c, d)));
+  f2unpack(r, ra, rb);
+}
+
 // D(16x8 f32) += A(16x16 f16) * B(16x8 f16), warp-wide.
 __device__ __forceinline__ void mma_f16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
   asm volatile(

@@ -34,14 +34,15 @@ struct QuantSmem {
 };
 
 // Fixed pairwise tree over 32 values (upper half folded onto lower half, 16, 8,
-// 4, 2, 1 apart) -- the order the page bytes are defined with.
+// 4, 2, 1 apart) -- the order the page bytes are defined with.  The adds of a
+// level run two at a time as packed fp32x2 operations (the same roundings).
 __device__ __forceinline__ float tree32(float* a) {
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
+  for (int w = 16; w >= 2; w >>= 1) {
 #pragma unroll
-    for (int i = 0; i < w; ++i) a[i] = __fadd_rn(a[i], a[i + w]);
+    for (int i = 0; i < w; i += 2) add2_rn(a[i], a[i + 1], a[i + w], a[i + w + 1]);
   }
-  return a[0];
+  return __fadd_rn(a[0], a[1]);
 }
 
 // sigma^2 ~ sumsq/n - (sum/n)^2, each operation rounded once.
@@ -100,19 +101,23 @@ __device__ __noinline__ float rint_div(float d, float u) { return rintf(__fdiv_r
 __device__ __forceinline__ void qcode4(const float (&x)[4], const QuantParams& q, int levels,
                                        uint32_t (&code)[4]) {
   const float edge = 0.5f - (levels > 15 ? 0x1p-12f : 0x1p-15f);
-  float d[4], n[4];
+  float d[4], y[4], n[4], e[4];
+  // (x - M), (x - M) * (1/u) and the rounding residual, two at a time
+  sub2_rn(d[0], d[1], x[0], x[1], q.M, q.M);
+  sub2_rn(d[2], d[3], x[2], x[3], q.M, q.M);
+  mul2_rn(y[0], y[1], d[0], d[1], q.ru, q.ru);
+  mul2_rn(y[2], y[3], d[2], d[3], q.ru, q.ru);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) n[k] = rintf(y[k]);
+  sub2_rn(e[0], e[1], y[0], y[1], n[0], n[1]);
+  sub2_rn(e[2], e[3], y[2], y[3], n[2], n[3]);
   float worst = 0.0f;  // largest |y - rint(y)|; a NaN quotient never counts
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    d[k] = __fsub_rn(x[k], q.M);
-    const float y = __fmul_rn(d[k], q.ru);
-    n[k] = rintf(y);
-    worst = fmaxf(worst, fabsf(__fsub_rn(y, n[k])));
-  }
+  for (int k = 0; k < 4; ++k) worst = fmaxf(worst, fabsf(e[k]));
   if (worst > edge) {
 #pragma unroll
     for (int k = 0; k < 4; ++k)
-      if (fabsf(__fsub_rn(__fmul_rn(d[k], q.ru), n[k])) > edge) n[k] = rint_div(d[k], q.u);
+      if (fabsf(e[k]) > edge) n[k] = rint_div(d[k], q.u);
   }
   // n is integral: a saturating conversion clamps below at 0, min() above at L
 #pragma unroll
@@ -233,10 +238,9 @@ __device__ void tile_stats(QuantSmem& sm, const uint16_t* ksrc, size_t row_strid
   __syncthreads();
   float a[kPage], b[kPage];
 #pragma unroll
-  for (int t = 0; t < kPage; ++t) {
-    a[t] = bits16_to_f32(sm.xk[t][tid], DT);
-    b[t] = __fmul_rn(a[t], a[t]);
-  }
+  for (int t = 0; t < kPage; ++t) a[t] = bits16_to_f32(sm.xk[t][tid], DT);
+#pragma unroll
+  for (int t = 0; t < kPage; t += 2) mul2_rn(b[t], b[t + 1], a[t], a[t + 1], a[t], a[t + 1]);
   s1 = tree32(a);
   s2 = tree32(b);
   __syncthreads();
@@ -311,7 +315,7 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
       for (int t = 0; t < kPage; ++t) tmp[t] = x[t];
       const float s1 = tree32(tmp);
 #pragma unroll
-      for (int t = 0; t < kPage; ++t) tmp[t] = __fmul_rn(x[t], x[t]);
+      for (int t = 0; t < kPage; t += 2) mul2_rn(tmp[t], tmp[t + 1], x[t], x[t + 1], x[t], x[t + 1]);
       const float s2 = tree32(tmp);
       if (running) {
         rsum = __fadd_rn(rsum, s1);
@@ -319,7 +323,9 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
         rcount += kPage;
         var = running_var(rsum, rsq, __int2float_rn(rcount));
       } else {
-        var = running_var(s1, s2, (float)kPage);
+        // n = 32: dividing by a power of two is multiplying by its inverse, exactly
+        const float a = __fmul_rn(s2, 1.0f / kPage), b = __fmul_rn(s1, 1.0f / kPage);
+        var = __fsub_rn(a, __fmul_rn(b, b));
       }
     }
     sm.kmm[c] = make_float2(mn, mx);

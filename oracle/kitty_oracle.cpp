@@ -257,6 +257,19 @@ float tree_sum(const float* x) {
 
 struct PageStats { float mn[D], mx[D], s1[D], s2[D]; };
 
+// Minimum and maximum of a group of values.  The pages say "min/max" and no
+// more; of two zeros, -0 is taken as the smaller (IEEE 754-2019 minimum and
+// maximum), so the result does not depend on the order of the values.  Inputs
+// are finite (others are reported, and their pages are not defined).
+float min_of(float a, float b) {
+  if (a == b) return std::signbit(a) ? a : b;
+  return b < a ? b : a;
+}
+float max_of(float a, float b) {
+  if (a == b) return std::signbit(a) ? b : a;
+  return b > a ? b : a;
+}
+
 // Per channel over the 32 tokens of one Key page: min, max, sum and sum of
 // squares (VeloxQuant-MLX docs, Prefill phase step 1 and step 5).
 void page_stats(const float* xk, PageStats& st) {
@@ -267,8 +280,8 @@ void page_stats(const float* xk, PageStats& st) {
       const float x = xk[t * D + c];
       col[t] = x;
       sq[t] = x * x;
-      mn = std::min(mn, x);
-      mx = std::max(mx, x);
+      mn = min_of(mn, x);
+      mx = max_of(mx, x);
     }
     st.mn[c] = mn;
     st.mx[c] = mx;
@@ -380,7 +393,7 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
     for (int g = 0; g < D / VG; ++g) {
       const float* x = xv + t * D + g * VG;
       float mn = x[0], mx = x[0];
-      for (int i = 1; i < VG; ++i) { mn = std::min(mn, x[i]); mx = std::max(mx, x[i]); }
+      for (int i = 1; i < VG; ++i) { mn = min_of(mn, x[i]); mx = max_of(mx, x[i]); }
       uint16_t S, M;
       uint16_t code[VG];
       quant_group(x, 1, VG, mn, mx, 3, false, &S, &M, code);

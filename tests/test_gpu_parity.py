@@ -67,6 +67,40 @@ def test_quantize_bit_exact(case):
     assert bad.size == 0, "first mismatching bytes at %s" % bad[:8]
 
 
+def _signed_zeros(inp):
+    """Plant +0 / -0 (16-bit 0x0000 / 0x8000) into Key channels and Value groups
+    of page 0, head 0, where they decide a minimum or a maximum."""
+    P, Z, N = 0x0000, 0x8000, None
+    k, v = inp["k"], inp["v"]
+    t = np.arange(32)
+    k[t, 0, 3] = np.where(t % 2 == 0, P, Z)          # all zeros, +0 first
+    k[t, 0, 4] = np.where(t % 2 == 0, Z, P)          # all zeros, -0 first
+    k[t, 0, 5] = np.where(t < 16, np.where(t % 2 == 0, P, Z), k[t, 0, 5] & 0x7FFF)  # min is a zero
+    k[t, 0, 6] = np.where(t < 16, np.where(t % 2 == 0, Z, P), k[t, 0, 6] | 0x8000)  # max is a zero
+    c = np.arange(32)
+    v[0, 0, c] = np.where(c % 2 == 0, P, Z)          # token 0, group 0: zeros, +0 first
+    v[1, 0, 32 + c] = np.where(c % 2 == 0, Z, P)     # token 1, group 1: zeros, -0 first
+    v[2, 0, 64 + c] = np.where(c < 8, np.where(c % 2 == 0, Z, P), v[2, 0, 64 + c] & 0x7FFF)
+    v[3, 0, 96 + c] = np.where(c < 8, np.where(c % 2 == 0, P, Z), v[3, 0, 96 + c] | 0x8000)
+    return inp
+
+
+@pytest.mark.parametrize("lo_bit", [2, 4])
+@pytest.mark.parametrize("mode", [0, 1], ids=["page", "running"])
+@pytest.mark.parametrize("dtype", [synth.BF16, synth.F16], ids=["bf16", "f16"])
+def test_quantize_signed_zeros_bit_exact(dtype, mode, lo_bit):
+    """A minimum or maximum that is a signed zero is stored with the sign the
+    oracle's in-order min/max picks (the first of equal values)."""
+    w = _variant("small_gqa", dtype=dtype, lo_bit=lo_bit)
+    inp = _signed_zeros(synth.host_inputs(w, seed=1))
+    pool, run = gpu_quantize(w, inp, mode=mode)
+    ref, ref_run, st = oracle_quantize(w, inp, mode=mode)
+    assert st == 0
+    got = pool.cpu().numpy()
+    bad = np.nonzero(got != ref)[0]
+    assert bad.size == 0, "first mismatching bytes at %s" % bad[:8]
+
+
 @pytest.mark.parametrize("lo_bit", [2, 4])
 @pytest.mark.parametrize("mode", [1, 2], ids=["running", "sequence"])
 def test_quantize_running_bit_exact(mode, lo_bit):

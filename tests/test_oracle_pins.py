@@ -283,6 +283,39 @@ def test_closed_forms_exact_reconstruction(orc):
         assert (np.diff(code[o, c]) >= 0).all()
 
 
+def test_signed_zero_min_max_is_order_free(orc):
+    """Of two zeros, -0 is the minimum and +0 the maximum (IEEE 754-2019
+    minimum/maximum; the pages say only "min/max"): a Key channel or Value group
+    whose minimum is a zero stores M = -0 (0x8000) whenever a -0 is present, in
+    any token order, and +0 (0x0000) when none is; a group of zeros has step +0."""
+    xk, xv = _kv(40)
+    r = _rng(41)
+    z = np.where(r.permutation(np.r_[np.zeros(16), np.ones(16)]) == 1,
+                 np.float32(-0.0), np.float32(0.0)).astype(np.float32)
+    xk[:, 3] = z                                   # zeros, random signs
+    xk[:, 4] = z[::-1]                             # the same, reversed order
+    xk[:, 5] = 0.0                                 # +0 only
+    xk[:, 6] = np.abs(xk[:, 6]) + 1.0
+    xk[7, 6], xk[19, 6] = 0.0, -0.0                # minimum a zero, both signs
+    xv[0, 0:32] = z
+    xv[1, 32:64] = z[::-1]
+    xv[2, 64:96] = 0.0
+    blob, st = orc.quantize_page_f32(xk, xv, 32)
+    assert st == 0
+    lay = dict(ks=1280, km=1536, vs=2848, vm=3104)   # n_hi = 32, 2-bit planes
+    u16 = lambda off, i: int(blob[off + 2 * i]) | (int(blob[off + 2 * i + 1]) << 8)
+    km = lambda c: u16(lay["km"], orc.meta_pos("km", c))
+    assert km(3) == 0x8000 and km(4) == 0x8000 and km(6) == 0x8000
+    assert km(5) == 0x0000
+    assert u16(lay["ks"], 3) == u16(lay["ks"], 4) == u16(lay["ks"], 5) == 0x0000
+    vm = lambda g, t: u16(lay["vm"], orc.meta_pos("vmeta", g, t))
+    vs = lambda g, t: u16(lay["vs"], orc.meta_pos("vmeta", g, t))
+    assert vm(0, 0) == 0x8000 and vm(1, 1) == 0x8000 and vm(2, 2) == 0x0000
+    assert vs(0, 0) == vs(1, 1) == vs(2, 2) == 0x0000
+    kh, vh, _ = orc.dequant_page(blob, 32)
+    assert (kh[:, 3:6] == 0).all() and (vh[0, 0:32] == 0).all()
+
+
 def test_reconstruction_error_bound(orc):
     """|x - xhat| <= step/2 inside the stored range; clamped values lose at most the
     fp16 rounding of the minimum / of the top of the range."""

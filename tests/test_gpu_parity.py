@@ -168,7 +168,7 @@ def test_quantize_bad_seq_status():
 
 
 @pytest.mark.parametrize("case", CASES, ids=[_ids(c) for c in CASES])
-@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16", "f16"])
 def test_decode_attention(case, out_dtype):
     w = _variant(case[0], **case[1])
     inp = synth.host_inputs(w, seed=3)

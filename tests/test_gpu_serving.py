@@ -2,8 +2,9 @@
 
 Its copies run on side streams, overlapped with the kernels. Over many decode
 steps with page flushes, it must give outputs and cache state bit-identical to
-the plain per-layer fused calls (LayerCache.step) on the same inputs. The fused
-call itself is checked against the oracle in test_gpu_fused.py."""
+the same per-layer calls made directly on the same inputs: the fused call
+(LayerCache.step), or append then attend. Those calls themselves are checked
+against the oracle in test_gpu_fused.py and test_gpu_parity.py."""
 
 import numpy as np
 import pytest
@@ -44,8 +45,9 @@ def _layers(L, B, Hkv, Hq, n_hi, pages, tails, gen):
     return out
 
 
-@pytest.mark.parametrize("graphs", [True, False])
-def test_serving_step_matches_per_layer_calls(graphs):
+@pytest.mark.parametrize("graphs,fused", [(True, True), (False, True), (True, False)],
+                         ids=["graphs", "direct", "graphs-unfused"])
+def test_serving_step_matches_per_layer_calls(graphs, fused):
     import torch
     from mixed_precision_bit_gb300.cache import ServingStep
     L, B, Hkv, Hq, n_hi = 3, 5, 2, 8, 32
@@ -57,7 +59,7 @@ def test_serving_step_matches_per_layer_calls(graphs):
     o0 = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
     new[0].attend(q0, o0)
     torch.cuda.synchronize()
-    srv = ServingStep(new, graphs=graphs)
+    srv = ServingStep(new, graphs=graphs, fused=fused)
     g = torch.Generator("cuda").manual_seed(5)
     d_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
     flushes = 0
@@ -73,7 +75,12 @@ def test_serving_step_matches_per_layer_calls(graphs):
         for l, lc in enumerate(ref):
             fl = lc.plan_flush()
             flushes += int((fl >= 0).sum())
-            lc.step(k[l], v[l], torch.from_numpy(fl).cuda(), q[l], d_out)
+            fd = torch.from_numpy(fl).cuda()
+            if fused:
+                lc.step(k[l], v[l], fd, q[l], d_out)
+            else:  # the same two calls (the fused call attends a flushed page in another order)
+                lc.append(k[l], v[l], fd)
+                lc.attend(q[l], d_out)
             want = d_out.cpu()
             assert torch.equal(got[l].view(torch.int16), want.view(torch.int16)), (step, l)
     assert flushes >= 2 * L  # the steps crossed page boundaries

@@ -12,7 +12,7 @@ Metric: decode tokens/s = sequences x steps / time; HBM GB/s of the decode
 kernel on algorithmic bytes (packed pages + tails + Q + O + block table).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kitty|reference]
-                       [--workload budget|budget_uniform|llama3_8b|qwen3_8b|long]
+                       [--workload budget|budget_uniform|budget_k4|budget_84|llama3_8b|qwen3_8b|qwen3_g1|qwen3_g2|long|tiny]
 """
 
 from __future__ import annotations
@@ -529,7 +529,7 @@ def main():
     ap.add_argument("--impl", default="kitty", choices=["kitty", "reference"])
     ap.add_argument("--workload", default="budget",
                     choices=["budget", "budget_uniform", "budget_k4", "budget_84", "llama3_8b",
-                             "qwen3_8b", "long", "tiny"])
+                             "qwen3_8b", "qwen3_g1", "qwen3_g2", "long", "tiny"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")

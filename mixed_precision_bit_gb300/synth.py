@@ -130,14 +130,18 @@ def workload(name: str, seed: int = 0) -> Workload:
     long       8 seqs, 32/8 heads, bf16, lengths U[16384, 65536], n_hi=32, channel
                scales redrawn every 4096 tokens
     small_gqa  parity-size GQA case: 3 seqs, 8/2 heads, bf16, ragged lengths
+    qwen3_g1, qwen3_g2
+               qwen3_8b with 8 / 16 query heads (query groups of 1 and 2): the
+               decode kernel's per-page cost does not depend on the group size
     """
     if name == "tiny":
         return Workload(name, 1, 1, 1, 32, F16, np.array([8]), np.array([0]))
     if name == "llama3_8b":
         return Workload(name, 16, 32, 8, 32, BF16, np.full(16, 128), np.zeros(16, np.int64))
-    if name == "qwen3_8b":
+    if name in ("qwen3_8b", "qwen3_g1", "qwen3_g2"):
         tails = (bits(seed, "qwen3_8b/tail", 64) % np.uint64(32)).astype(np.int64)
-        return Workload(name, 64, 32, 8, 16, BF16, np.full(64, 256), tails)
+        Hq = {"qwen3_8b": 32, "qwen3_g1": 8, "qwen3_g2": 16}[name]
+        return Workload(name, 64, Hq, 8, 16, BF16, np.full(64, 256), tails)
     if name == "long":
         L = 16384 + (bits(seed, "long/len", 8) % np.uint64(65536 - 16384 + 1)).astype(np.int64)
         return Workload(name, 8, 32, 8, 32, BF16, L // PAGE, L % PAGE, drift=4096)

@@ -277,9 +277,10 @@ def run_kitty(args, rank, world, local_rank):
     out = torch.empty((L, B, Hq, D), dtype=torch.bfloat16 if spec["dtype"] else torch.float16,
                       device="cuda")
     # flush plans for the warm-up and timed steps, decided on the host ahead of time
-    plans, algo = [], []
+    plans, algo, kvtok = [], [], []
     for s in range(W + K):
         plans.append(np.stack([lc.plan_flush() for lc in layers]))
+        kvtok.append([lc.kv_tokens() for lc in layers])  # tokens each layer's call attends to
         # bytes of the timed call: the decode call, or the fused append + decode
         algo.append([lc.algorithmic_bytes() + (lc.append_bytes(plans[-1][l], fused=True)
                                                if args.fused else 0)
@@ -345,6 +346,7 @@ def run_kitty(args, rank, world, local_rank):
     ms = dist_max(t0.elapsed_time(t1), world)
     dec_ms = [ev[s][l][0].elapsed_time(ev[s][l][1]) for s in range(K) for l in range(L)]
     dec_bytes = [algo[W + s][l] for s in range(K) for l in range(L)]
+    dec_tokens = [kvtok[W + s][l] for s in range(K) for l in range(L)]
     status = [int(lc.status.item()) for lc in layers]
     bad = [x for x in status if x not in (0,)]
     if bad:
@@ -375,6 +377,7 @@ def run_kitty(args, rank, world, local_rank):
     launches_per_call = 1 + (1 if splits > 1 else 0)
     quant = measure_quantize(spec) if args.measure_quantize else None
     return dict(spec=spec, cfg=cfg, ms=ms, K=K, W=W, E=E, dec_ms=dec_ms, dec_bytes=dec_bytes,
+                dec_tokens=dec_tokens,
                 quantize=quant,
                 clocks=clk, e2e_s=e2e_s, h2d=h2d, d2h=d2h, splits=splits, chunk=chunk,
                 gpu_launches=K * L * (2 if args.fused else 2 + launches_per_call),
@@ -596,6 +599,7 @@ def main():
                                       "launch": ("fused append + decode per layer" if args.fused
                                                  else "append, then decode, per layer") +
                                                 (", CUDA graphs" if args.graphs else ", direct calls")}),
+        "kv_tokens_per_s": sum(r["dec_tokens"]) / (sum(r["dec_ms"]) / 1e3),
         "hbm_gbs": {"decode_kernel": achieved,
                     "step_average": world * step_bytes * K / (r["ms"] / 1e3) / 1e9 / world,
                     "pct_of_8tbs": 100.0 * achieved / NOMINAL_HBM_GBS,

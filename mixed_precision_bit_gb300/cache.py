@@ -163,6 +163,11 @@ class LayerCache:
         page = PAGE * D * 2 * 2 + self.blob + stats - (self.blob if fused else 0)
         return self.B * Hkv * D * 2 * 2 * 2 + nf * Hkv * page
 
+    def kv_tokens(self) -> int:
+        """Cached tokens one decode call attends to, over the batch (host mirror):
+        full pages and unquantized tail tokens."""
+        return int(self.h_pages.sum()) * PAGE + int(self.h_tail.sum())
+
     def algorithmic_bytes(self) -> int:
         """Bytes one decode call must move: packed pages + tails + Q + O + block
         table entries (host mirror of the current lengths)."""

@@ -129,12 +129,6 @@ __device__ __forceinline__ uint32_t ld_s32(uint32_t a) {
   return v;
 }
 template <int OFF>
-__device__ __forceinline__ uint32_t ld_s16(uint32_t a) {
-  uint16_t v;
-  asm volatile("ld.shared.u16 %0, [%1+%2];" : "=h"(v) : "r"(a), "n"(OFF));
-  return v;
-}
-template <int OFF>
 __device__ __forceinline__ uint2 ld_s64(uint32_t a) {
   uint2 v;
   asm volatile("ld.shared.v2.b32 {%0,%1}, [%2+%3];" : "=r"(v.x), "=r"(v.y) : "r"(a), "n"(OFF));

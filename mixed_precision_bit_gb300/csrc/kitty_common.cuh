@@ -67,20 +67,7 @@ __device__ __forceinline__ void fence_mbar_init() {
   asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
 }
 
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\t"
-      "mbarrier.arrive.expect_tx.shared::cta.b64 st, [%0], %1;\n\t}" ::"r"(smem_u32(bar)),
-      "r"(bytes)
-      : "memory");
-}
 
-__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
-  asm volatile(
-      "{\n\t.reg .b64 st;\n\t"
-      "mbarrier.arrive.shared::cta.b64 st, [%0];\n\t}" ::"r"(smem_u32(bar))
-      : "memory");
-}
 
 __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
   uint32_t ok;
@@ -103,18 +90,11 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
   return false;
 }
 
-// 1-D bulk copy global -> shared, completion counted on `bar` (bytes % 16 == 0,
-// both addresses 16-byte aligned).
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar))
-      : "memory");
-}
 
-// The same barrier and copy operations on 32-bit shared-space addresses
-// (precomputed once, so the hot loop does no generic-to-shared conversion).
+// Barrier arrive / expect-tx and 1-D bulk copy on 32-bit shared-space
+// addresses (precomputed once, so the hot loop does no generic-to-shared
+// conversion).  bulk_g2s_s: global -> shared, completion counted on `bar`;
+// bytes % 16 == 0, both addresses 16-byte aligned.
 __device__ __forceinline__ void mbar_arrive_expect_tx_s(uint32_t bar, uint32_t bytes) {
   asm volatile(
       "{\n\t.reg .b64 st;\n\t"

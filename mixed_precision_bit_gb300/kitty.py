@@ -113,10 +113,18 @@ def _chk(name, rc):
 
 
 def _ptr(t):
+    """Device address of a tensor argument.  The library reads and writes plain
+    dense arrays in device memory, so a view with gaps or a host tensor is
+    refused here (it would be read wrongly, or fault)."""
     if t is None:
         return None
     if isinstance(t, int):
         return ctypes.c_void_p(t)
+    if not t.is_cuda:
+        raise ValueError("kitty: tensor arguments must be in device memory (got %s)" % t.device)
+    if not t.is_contiguous():
+        raise ValueError("kitty: tensor arguments must be contiguous (shape %s, strides %s)"
+                         % (tuple(t.shape), t.stride()))
     return ctypes.c_void_p(t.data_ptr())
 
 

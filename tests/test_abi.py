@@ -123,3 +123,24 @@ def test_decode_plan_and_workspace(K):
     cfg.decode_pages_per_split = 4
     assert K.decode_plan(cfg, 16, 128) == (32, 4)
     assert K.decode_plan(cfg, 16, 4096) == (256, 16)
+
+
+def test_binding_refuses_host_and_strided_tensors():
+    """The ctypes binding passes raw device addresses: a host tensor or a view
+    with gaps is refused before any call."""
+    import torch
+    from mixed_precision_bit_gb300 import kitty as K
+    with pytest.raises(ValueError, match="device memory"):
+        K._ptr(torch.zeros(4, 4))
+    assert K._ptr(None) is None
+    assert K._ptr(1024).value == 1024
+
+
+@pytest.mark.gpu
+def test_binding_refuses_strided_device_tensor():
+    torch = pytest.importorskip("torch")
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from mixed_precision_bit_gb300 import kitty as K
+    with pytest.raises(ValueError, match="contiguous"):
+        K._ptr(torch.zeros(4, 4, device="cuda").t())

@@ -197,7 +197,12 @@ int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pa
  *           if all tails are 0
  *   out     device [B][Hq][128] of out_dtype (KITTY_F32, KITTY_BF16, KITTY_F16)
  *   workspace device, >= kitty_decode_workspace_bytes, 16-byte aligned (may be
- *   NULL when that size is 0). */
+ *   NULL when that size is 0).
+ * Launches, in stream order: the decode kernel, then (with more than one split)
+ * the split combine as a programmatic dependent launch, which may start while
+ * the decode grid drains and waits for it before reading the partials.  Both
+ * can be captured in a CUDA graph; the first call on a device should come
+ * before any capture (it sets the kernel's shared-memory attributes). */
 int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const void* pool,
                            int32_t pool_pages, const int32_t* block_table, int32_t max_pages,
                            const int32_t* num_pages, const void* tail_k, const void* tail_v,

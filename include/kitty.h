@@ -93,9 +93,16 @@ typedef struct {
                                    (sum of num_pages); 0 = unknown.  Any value
                                    gives correct results; it only shapes the
                                    splits (and so the workspace size) */
+  int32_t decode_max_pages;       /* optional planning hint: the largest num_pages
+                                   of the batch; 0 = unknown (max_pages is
+                                   assumed).  Splits are sized over this many
+                                   pages, and the last one still reaches
+                                   max_pages, so any value gives correct
+                                   results */
 } kitty_cfg;
 
-/* Library ABI version (this header: 2; kitty_cfg gained decode_total_pages). */
+/* Library ABI version (this header: 3; kitty_cfg gained decode_total_pages in
+ * version 2 and decode_max_pages in version 3). */
 int kitty_abi_version(void);
 
 /* Packed page size.  A page holds Hkv blobs, one per kv head, in head order;

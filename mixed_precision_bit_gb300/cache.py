@@ -86,13 +86,14 @@ class LayerCache:
         self.set_plan_hint()
         return ids
 
-    def set_plan_hint(self, total_pages=None):
-        """Give the decode split planner the batch's total page count (default:
-        the host mirror's) on this cache's own copy of the config, and grow the
-        workspace if that plan needs more.  Any value is correct; a close one
-        balances ragged batches better."""
+    def set_plan_hint(self, total_pages=None, max_pages=None):
+        """Give the decode split planner the batch's total and largest page counts
+        (default: the host mirror's) on this cache's own copy of the config, and
+        grow the workspace if that plan needs more.  Any values are correct;
+        close ones balance the splits better."""
         total = int(self.h_pages.sum()) if total_pages is None else int(total_pages)
-        self.cfg = dataclasses.replace(self.cfg, decode_total_pages=total)
+        mx = int(self.h_pages.max()) if max_pages is None and self.B else int(max_pages or 0)
+        self.cfg = dataclasses.replace(self.cfg, decode_total_pages=total, decode_max_pages=mx)
         need = kitty.decode_workspace_bytes(self.cfg, self.B, self.max_pages)
         if need > self.workspace.numel() * 4:
             self.workspace = torch.empty(need // 4, dtype=torch.float32, device=self.pool.device)

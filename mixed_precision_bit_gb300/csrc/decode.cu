@@ -1035,8 +1035,15 @@ struct Schedule {
 //    dispatched in round s finishes no later than the work still queued behind
 //    it (rounded down to 8 pages; at least m).  The first split takes what is
 //    left; if that is smaller than the second, the two are merged and halved.
-//    m starts at 16 pages (2 pairs per warp) and doubles if more than
+//    m starts at 16 pages (2 pairs per warp), or at 32 when the batch holds
+//    fewer than 64 pages per resident CTA: there every CTA is short and its
+//    fixed start and merge cost outweighs the balance of the last round
+//    (measured on GB300: 16 x 4096-token Llama-3-8B-shaped layer +7%; the
+//    larger layers are 1-2% faster with 16).  m doubles if more than
 //    kMaxSplits splits would be needed.
+//    With cfg->decode_max_pages (the longest sequence's page count) the sizes
+//    are built over that many pages instead of M, and the last split is
+//    extended to M, so the table's headroom past every sequence adds no CTA.
 //    With cfg->decode_total_pages (the batch's page count) the growth factor is
 //    2 rho, and no split exceeds one resident CTA's fair share of the whole
 //    batch (Hkv * total / slots pages), which keeps ragged batches balanced;
@@ -1057,20 +1064,25 @@ void plan(const kitty_cfg* cfg, int B, int M, int blob, Schedule* sc) {
     const double rho = (hinted ? 2.0 : 1.0) * (double)B * cfg->num_kv_heads / (double)slots;
     const long fair = hinted ? (long)cfg->num_kv_heads * cfg->decode_total_pages / slots / 8 * 8
                              : (1L << 30);
+    const int Ms = cfg->decode_max_pages > 0 ? std::min(M, cfg->decode_max_pages) : M;
+    const double work = hinted ? (double)cfg->num_kv_heads * cfg->decode_total_pages
+                               : (double)B * cfg->num_kv_heads * Ms;  // page-heads (at most)
+    const int m0 = work < 64.0 * (double)slots ? 32 : 16;
     long T = 0;
-    for (int m = 16;; m *= 2) {
+    for (int m = m0;; m *= 2) {
       n = 0;
       T = 0;
       long c = m;
-      while (T < M && n < kMaxSplits) {
+      while (T < Ms && n < kMaxSplits) {
         sz[n++] = (int)c;
         T += c;
         c = std::max<long>(m, std::min<long>(fair, (long)(rho * (double)T) / 8 * 8));
       }
-      if (T >= M) break;
+      if (T >= Ms) break;
     }
     std::reverse(sz, sz + n);
-    sz[0] -= (int)(T - M);
+    sz[0] -= (int)(T - Ms);
+    sz[n - 1] += M - Ms;  // the last split reaches the end of the table
     if (n > 1 && sz[0] < sz[1]) {
       const int tot = sz[0] + sz[1];
       const int h = (tot / 2 + 7) / 8 * 8;

@@ -32,7 +32,8 @@ class KittyError(RuntimeError):
 class _Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "head_dim", "num_kv_heads", "num_q_heads", "page_tokens", "n_hi", "hi_bit", "lo_bit",
-        "v_group", "rank_mode", "in_dtype", "decode_pages_per_split", "decode_total_pages")]
+        "v_group", "rank_mode", "in_dtype", "decode_pages_per_split", "decode_total_pages",
+        "decode_max_pages")]
 
 
 @dataclasses.dataclass
@@ -44,6 +45,7 @@ class Config:
     rank_mode: int = RANK_PAGE
     decode_pages_per_split: int = 0
     decode_total_pages: int = 0     # planning hint: the batch's total page count (0: unknown)
+    decode_max_pages: int = 0       # planning hint: the longest sequence's page count (0: unknown)
     head_dim: int = 128
     page_tokens: int = 32
     hi_bit: int = 4
@@ -53,7 +55,8 @@ class Config:
     def c(self):
         return _Cfg(self.head_dim, self.num_kv_heads, self.num_q_heads, self.page_tokens,
                     self.n_hi, self.hi_bit, self.lo_bit, self.v_group, self.rank_mode,
-                    self.in_dtype, self.decode_pages_per_split, self.decode_total_pages)
+                    self.in_dtype, self.decode_pages_per_split, self.decode_total_pages,
+                    self.decode_max_pages)
 
 
 _lib = None

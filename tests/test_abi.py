@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(K):
     for n in names:
         assert hasattr(lib, n), n
     assert set(K.EXPORTS) == names
-    assert lib.kitty_abi_version() == 2
+    assert lib.kitty_abi_version() == 3
 
 
 def test_page_bytes_and_avg_bits(K):
@@ -117,6 +117,18 @@ def test_decode_plan_and_workspace(K):
         assert 1 <= s <= 256 and c <= M and s * c >= M, (B, M, s, c)
     with pytest.raises(K.KittyError):
         K.decode_plan(K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=-1), 4, 16)
+    # planning hint: the longest sequence; the splits still cover the whole table
+    for B, M, mx in ((16, 136, 128), (64, 264, 256), (8, 2048, 2000), (4, 100, 1000), (3, 50, 1)):
+        h = K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=B * min(M, mx),
+                     decode_max_pages=mx)
+        s, c = K.decode_plan(h, B, M)
+        assert 1 <= s <= 256 and c <= M, (B, M, mx, s, c)
+        assert K.decode_workspace_bytes(h, B, M) == (B * 32 * s * 130 * 4 if s > 1 else 0)
+    # a 16 x 128-page batch in a 136-page table: four 32-page splits, the last to the end
+    h = K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=16 * 128, decode_max_pages=128)
+    assert K.decode_plan(h, 16, 136) == (4, 40)
+    with pytest.raises(K.KittyError):
+        K.decode_plan(K.Config(num_kv_heads=8, num_q_heads=32, decode_max_pages=-1), 4, 16)
     cfg.decode_pages_per_split = 1000
     assert K.decode_plan(cfg, 16, 128) == (1, 128)
     assert K.decode_workspace_bytes(cfg, 16, 128) == 0

@@ -124,9 +124,12 @@ def test_decode_with_plan_hint():
     inp = synth.host_inputs(w, seed=8)
     pool, _ = gpu_quantize(w, inp)
     ref, _ = oracle_decode(w, inp, pool.cpu().numpy())
-    for hint in (int(w.pages.sum()), 5, 100000):
+    hints = [(int(w.pages.sum()), 0), (5, 0), (100000, 0),
+             (int(w.pages.sum()), int(w.pages.max())), (int(w.pages.sum()), 3), (0, 100000)]
+    for hint, mx in hints:
         cfg = cfg_for(w)
         cfg.decode_total_pages = hint
+        cfg.decode_max_pages = mx
         bt = inp["block_table"]
         ws = torch.empty(max(kitty.decode_workspace_bytes(cfg, w.B, bt.shape[1]), 16) // 4,
                          dtype=torch.float32, device="cuda")

@@ -993,13 +993,6 @@ using namespace kitty;
 
 namespace {
 
-int sm_count() {
-  int dev = 0, n = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
-  return n;
-}
-
 size_t decode_smem(int blob, int w) {
   const int st = stages_for(w);
   return (size_t)kDWarps * st * blob + kDWarps * st * sizeof(uint64_t) + 2 * 4 * kD * 2;

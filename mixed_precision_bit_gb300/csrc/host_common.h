@@ -31,6 +31,17 @@ inline int check_cfg(const kitty_cfg* c, bool decode) {
   return KITTY_OK;
 }
 
+#ifdef __CUDACC__
+// Streaming multiprocessors of the current device (148 if it cannot be read);
+// for the CUDA translation units (host.cpp is built without the CUDA headers).
+inline int sm_count() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 148;
+  return n;
+}
+#endif
+
 // Bytes of one (page, kv-head) blob; w = lo_bit (Key plane width, 2 or 4).
 inline size_t blob_bytes(int n_hi, int w) {
   return 512u * (size_t)w + 4u * (size_t)w * (size_t)n_hi + 2048u + (size_t)n_hi;

@@ -151,16 +151,16 @@ __device__ __forceinline__ uint32_t var_key(float v) {
 // leading bits that every key shares and stops early once exactly n_hi keys
 // are >= the threshold so far (then they are the set); no block barrier is
 // taken.
-__device__ __forceinline__ void topk_masks(QuantSmem& sm, int n_hi) {
+__device__ __forceinline__ void topk_masks(const uint32_t* key, uint32_t* boost, int n_hi) {
   const int lane = threadIdx.x & 31;
   constexpr uint32_t kAll = 0xFFFFFFFFu;
   if (n_hi >= kD || n_hi <= 0) {
-    if (lane < kD / 32) sm.boost[lane] = n_hi > 0 ? kAll : 0u;
+    if (lane < kD / 32) boost[lane] = n_hi > 0 ? kAll : 0u;
     return;
   }
   uint32_t k[4];
 #pragma unroll
-  for (int m = 0; m < 4; ++m) k[m] = sm.key[lane + 32 * m];
+  for (int m = 0; m < 4; ++m) k[m] = key[lane + 32 * m];
   const uint32_t kmax = __reduce_max_sync(kAll, max(max(k[0], k[1]), max(k[2], k[3])));
   const uint32_t kmin = __reduce_min_sync(kAll, min(min(k[0], k[1]), min(k[2], k[3])));
   const uint32_t diff = kmax ^ kmin;
@@ -197,7 +197,7 @@ __device__ __forceinline__ void topk_masks(QuantSmem& sm, int n_hi) {
   }
   if (lane == 0) {
 #pragma unroll
-    for (int m = 0; m < 4; ++m) sm.boost[m] = mask[m];
+    for (int m = 0; m < 4; ++m) boost[m] = mask[m];
   }
 }
 
@@ -216,7 +216,7 @@ __device__ __forceinline__ bool boost_of(const QuantSmem& sm, int c, int& row) {
 __device__ __forceinline__ bool topk_flag(QuantSmem& sm, float var, int n_hi) {
   sm.key[threadIdx.x] = var_key(var);
   __syncthreads();
-  if (threadIdx.x < 32) topk_masks(sm, n_hi);
+  if (threadIdx.x < 32) topk_masks(sm.key, sm.boost, n_hi);
   __syncthreads();
   int row;
   return boost_of(sm, threadIdx.x, row);
@@ -337,7 +337,7 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     }
   }
   __syncthreads();  // keys (or imposed flags) visible
-  if (fixed < 0 && warp == 0) topk_masks(sm, n_hi);
+  if (fixed < 0 && warp == 0) topk_masks(sm.key, sm.boost, n_hi);
 
   // ---- Value quantization: thread 4t+G owns token t, channels 32G..32G+31
   {

@@ -145,6 +145,98 @@ __global__ void __launch_bounds__(kQThreads) seq_scan_kernel(
   if (c == 0) run_count[sh] = rc;
 }
 
+// Passes A and B in one launch, for batches with many (sequence, kv head)
+// chains: one CTA per chain streams its pages' Key tiles through a two-stage
+// cp.async ring (16 bytes a thread, 4 per page) and computes each page's
+// tree-ordered sums on arrival; the running totals take the same fp32 adds in
+// page order as seq_scan_kernel, so the scratch words, the final totals and the
+// sequence-mode flags are bit-identical to passes A and B.  Thread c = channel c.
+constexpr int kWalkStages = 2;
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kQThreads) seq_walk_kernel(
+    const uint16_t* __restrict__ k, const int32_t* page_ids, const int32_t* seq_of_page,
+    int n_pages, int Hkv, float* run_sum, float* run_sumsq, int32_t* run_count, uint8_t* pool,
+    int pool_pages, int blob, int n_hi, int sequence_mode) {
+  __shared__ __align__(16) uint16_t tile[kWalkStages][kPage][kD];
+  __shared__ uint32_t key[kD];
+  __shared__ uint32_t boost[kD / 32];
+  const int s = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
+  const int p0 = first_page_of(seq_of_page, n_pages, s);
+  const int p1 = first_page_of(seq_of_page, n_pages, s + 1);
+  if (p0 >= p1) return;
+  const size_t sh = (size_t)s * Hkv + h;
+  const size_t stride = (size_t)Hkv * kD;
+  float rs = run_sum[sh * kD + c];
+  float rq = run_sumsq[sh * kD + c];
+  int rc = run_count[sh];
+  auto issue = [&](int i) {  // page i's Key tile into stage i % kWalkStages
+    const uint16_t* src = k + (size_t)i * kPage * stride + (size_t)h * kD;
+    const uint32_t dst = smem_u32(&tile[(i - p0) % kWalkStages][0][0]);
+#pragma unroll
+    for (int it = 0; it < kPage * (kD / 8) / kQThreads; ++it) {
+      const int idx = c + it * kQThreads;
+      const int t = idx >> 4, ch = (idx & 15) * 8;
+      cp_async16(dst + (uint32_t)(t * kD + ch) * 2, src + (size_t)t * stride + ch);
+    }
+  };
+  for (int j = 0; j < kWalkStages - 1; ++j) {
+    if (p0 + j < p1) issue(p0 + j);
+    cp_async_commit();
+  }
+  for (int i = p0; i < p1; ++i) {
+    if (i + kWalkStages - 1 < p1) issue(i + kWalkStages - 1);
+    cp_async_commit();  // one group per iteration, empty near the end
+    cp_async_wait<kWalkStages - 1>();
+    __syncthreads();  // page i's tile complete for every thread
+    const int pid = page_ids[i];
+    if (pid >= 0 && pid < pool_pages) {  // an invalid page is not counted (pass C reports it)
+      const int st = (i - p0) % kWalkStages;
+      float a[kPage], b[kPage];
+#pragma unroll
+      for (int t = 0; t < kPage; ++t) a[t] = bits16_to_f32(tile[st][t][c], DT);
+#pragma unroll
+      for (int t = 0; t < kPage; t += 2) mul2_rn(b[t], b[t + 1], a[t], a[t + 1], a[t], a[t + 1]);
+      const float s1 = tree32(a), s2 = tree32(b);
+      rs = __fadd_rn(rs, s1);
+      rq = __fadd_rn(rq, s2);
+      rc += kPage;
+      if (!sequence_mode) {
+        float* sc = reinterpret_cast<float*>(pool + ((size_t)pid * Hkv + h) * blob);
+        sc[c] = rs;
+        sc[kD + c] = rq;
+        if (c == 0) reinterpret_cast<int*>(sc)[2 * kD] = rc;
+      }
+    }
+    __syncthreads();  // every thread is done with this stage before it is refilled
+  }
+  if (sequence_mode) {
+    // the boost set of the whole sequence
+    key[c] = var_key(running_var(rs, rq, __int2float_rn(rc)));
+    __syncthreads();
+    if (c < 32) topk_masks(key, boost, n_hi);  // the page quantizer's ranking
+    __syncthreads();
+    const int flag = (boost[c >> 5] >> (c & 31)) & 1u;
+    for (int i = p0; i < p1; ++i) {
+      const int pid = page_ids[i];
+      if (pid >= 0 && pid < pool_pages)
+        reinterpret_cast<int*>(pool + ((size_t)pid * Hkv + h) * blob)[c] = flag;
+    }
+  }
+  run_sum[sh * kD + c] = rs;
+  run_sumsq[sh * kD + c] = rq;
+  if (c == 0) run_count[sh] = rc;
+}
+
 template <int DT, int W>
 __global__ void __launch_bounds__(kQThreads, 8) quantize_given_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
@@ -284,12 +376,20 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
     const int blob = (int)blob_bytes(cfg->n_hi, cfg->lo_bit);
     const int seq = cfg->rank_mode == KITTY_RANK_SEQUENCE ? 1 : 0;
     dim3 pages(n_pages, Hkv), seqs(n_seqs, Hkv);
-    if (cfg->in_dtype == KITTY_BF16)
-      page_sums_kernel<KITTY_BF16><<<pages, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_seqs, Hkv, p8, pool_pages, blob);
-    else
-      page_sums_kernel<KITTY_F16><<<pages, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_seqs, Hkv, p8, pool_pages, blob);
-    seq_scan_kernel<<<seqs, kQThreads, 0, s>>>(page_ids, seq_of_page, n_pages, Hkv, run_sum, run_sumsq,
-                                               run_count, p8, pool_pages, blob, cfg->n_hi, seq);
+    if ((long)n_seqs * Hkv >= 3L * sm_count()) {
+      // many chains: passes A and B fused, Key tiles read once
+      if (cfg->in_dtype == KITTY_BF16)
+        seq_walk_kernel<KITTY_BF16><<<seqs, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_pages, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, blob, cfg->n_hi, seq);
+      else
+        seq_walk_kernel<KITTY_F16><<<seqs, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_pages, Hkv, run_sum, run_sumsq, run_count, p8, pool_pages, blob, cfg->n_hi, seq);
+    } else {
+      if (cfg->in_dtype == KITTY_BF16)
+        page_sums_kernel<KITTY_BF16><<<pages, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_seqs, Hkv, p8, pool_pages, blob);
+      else
+        page_sums_kernel<KITTY_F16><<<pages, kQThreads, 0, s>>>(k16, page_ids, seq_of_page, n_seqs, Hkv, p8, pool_pages, blob);
+      seq_scan_kernel<<<seqs, kQThreads, 0, s>>>(page_ids, seq_of_page, n_pages, Hkv, run_sum, run_sumsq,
+                                                 run_count, p8, pool_pages, blob, cfg->n_hi, seq);
+    }
     dispatch(cfg, [&](auto tag) {
       using T = decltype(tag);
       quantize_given_kernel<T::DT, T::W><<<pages, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_seqs, cfg->n_hi, Hkv, p8, pool_pages, seq, d_status);

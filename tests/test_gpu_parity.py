@@ -115,6 +115,28 @@ def test_quantize_running_bit_exact(mode, lo_bit):
     assert (run[2].cpu().numpy() == rc).all()
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["running", "sequence"])
+def test_quantize_running_many_chains_bit_exact(mode):
+    """Enough (sequence, kv head) chains for the fused statistics walk (at least
+    3 per SM): pages, channel lists and accumulators bit-exact with the oracle,
+    as on the three-launch path the small cases take."""
+    import torch
+    chains = 3 * torch.cuda.get_device_properties(0).multi_processor_count
+    B = (chains + 1) // 2 + 8
+    pages = (synth.bits(9, "walk/pages", B) % np.uint64(4)).astype(np.int64) + 1
+    pages[5] = 0                                    # a sequence without pages
+    w = _variant("small_gqa", B=B, pages=pages, tails=np.zeros(B, np.int64), drift=64)
+    assert w.B * w.Hkv >= chains
+    inp = synth.host_inputs(w, seed=3)
+    pool, run = gpu_quantize(w, inp, mode=mode)
+    ref, (rs, rq, rc), st = oracle_quantize(w, inp, mode=mode)
+    assert st == 0
+    assert (pool.cpu().numpy() == ref).all()
+    assert (run[0].cpu().numpy().view(np.uint32) == rs.view(np.uint32)).all()
+    assert (run[1].cpu().numpy().view(np.uint32) == rq.view(np.uint32)).all()
+    assert (run[2].cpu().numpy() == rc).all()
+
+
 def test_decode_with_plan_hint():
     """The total-pages planning hint changes only the split layout: a ragged
     batch decodes within tolerance with the exact, a stale and a large hint."""

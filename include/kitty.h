@@ -208,8 +208,9 @@ int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pa
  * Launches, in stream order: the decode kernel, then (with more than one split)
  * the split combine as a programmatic dependent launch, which may start while
  * the decode grid drains and waits for it before reading the partials.  Both
- * can be captured in a CUDA graph; the first call on a device should come
- * before any capture (it sets the kernel's shared-memory attributes). */
+ * can be captured in a CUDA graph, also as the first call on a device (that
+ * call sets the kernel's shared-memory attributes, which is allowed during
+ * capture). */
 int kitty_decode_attention(const kitty_cfg* cfg, const void* q, const void* pool,
                            int32_t pool_pages, const int32_t* block_table, int32_t max_pages,
                            const int32_t* num_pages, const void* tail_k, const void* tail_v,

@@ -91,3 +91,45 @@ def test_serving_step_matches_per_layer_calls(graphs, fused):
             assert torch.equal(getattr(a, name), getattr(b, name)), name
         assert int(b.status.item()) == 0
     assert srv.bytes_up() == L * (B * Hq * 128 * 2 + 2 * B * Hkv * 128 * 2 + B * 4)
+
+
+_FRESH = r"""
+import sys, torch
+sys.path.insert(0, sys.argv[1])
+from mixed_precision_bit_gb300 import kitty
+from mixed_precision_bit_gb300.cache import LayerCache
+cfg = kitty.Config(num_kv_heads=2, num_q_heads=8, n_hi=32, in_dtype=kitty.BF16,
+                   rank_mode=kitty.RANK_RUNNING)
+g = torch.Generator("cuda").manual_seed(1)
+bf = lambda *s: torch.randn(s, generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+caches = []
+for _ in range(2):
+    lc = LayerCache(cfg, 3, 8, 32)
+    g.manual_seed(2)
+    lc.prefill(bf(3 * 32, 2, 128), bf(3 * 32, 2, 128), [1, 2, 0], bf(3, 2, 32, 128), bf(3, 2, 32, 128), [5, 31, 0])
+    caches.append(lc)
+torch.cuda.synchronize()
+q, k, v = bf(3, 8, 128), bf(3, 2, 128), bf(3, 2, 128)
+fl = torch.full((3,), -1, dtype=torch.int32, device="cuda")
+o1 = torch.empty((3, 8, 128), dtype=torch.bfloat16, device="cuda")
+o2 = torch.empty_like(o1)
+graph = caches[0].capture_step(k, v, fl, q, o1)   # the first decode launch of this process
+graph.replay()
+caches[1].step(k, v, fl, q, o2)
+torch.cuda.synchronize()
+assert torch.equal(o1.view(torch.int16), o2.view(torch.int16))
+assert int(caches[0].status.item()) == 0
+print("ok")
+"""
+
+
+def test_capture_as_first_call_in_a_fresh_process():
+    """A graph captured before any plain call (a new CUDA context: the library's
+    first launch happens inside the capture) replays like a plain call."""
+    import os
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, "-c", _FRESH, root], capture_output=True, text=True,
+                       timeout=300)
+    assert r.returncode == 0 and r.stdout.strip().endswith("ok"), r.stdout + r.stderr

@@ -211,17 +211,6 @@ __device__ __forceinline__ bool boost_of(const QuantSmem& sm, int c, int& row) {
   return (m >> (c & 31)) & 1u;
 }
 
-// Top-k boost flag of channel threadIdx.x for a variance given per thread.
-// Called by all 128 threads.
-__device__ __forceinline__ bool topk_flag(QuantSmem& sm, float var, int n_hi) {
-  sm.key[threadIdx.x] = var_key(var);
-  __syncthreads();
-  if (threadIdx.x < 32) topk_masks(sm.key, sm.boost, n_hi);
-  __syncthreads();
-  int row;
-  return boost_of(sm, threadIdx.x, row);
-}
-
 // Tree-ordered sum and sum of squares of Key channel threadIdx.x over one
 // page's 32 tokens (ksrc at token 0, token t at +t*row_stride); stages only K.
 template <int DT>

@@ -68,6 +68,16 @@ __global__ void check_seq_kernel(const int32_t* seq_of_page, int n_pages, int n_
 // Scratch words in a blob: running mode S1/R1 [0,128), S2/R2 [128,256), count
 // [256]; sequence mode boost flags [0,128).
 
+// Top-k boost flag of channel threadIdx.x for a variance given per thread, in
+// shared arrays key[128] and boost[4].  Called by all 128 threads.
+__device__ __forceinline__ bool topk_flag(uint32_t* key, uint32_t* boost, float var, int n_hi) {
+  key[threadIdx.x] = var_key(var);
+  __syncthreads();
+  if (threadIdx.x < 32) topk_masks(key, boost, n_hi);
+  __syncthreads();
+  return (boost[threadIdx.x >> 5] >> (threadIdx.x & 31)) & 1u;
+}
+
 __device__ __forceinline__ int first_page_of(const int32_t* seq_of_page, int n_pages, int s) {
   int lo = 0, hi = n_pages;
   while (lo < hi) { const int m = (lo + hi) >> 1; if (seq_of_page[m] < s) lo = m + 1; else hi = m; }
@@ -92,12 +102,12 @@ __global__ void __launch_bounds__(kQThreads, 8) page_sums_kernel(
   sc[kD + threadIdx.x] = s2;
 }
 
-// Thread c = channel c.  Pages are read 8 at a time ahead of the adds.
+// Thread c = channel c.  Pages are read 32 at a time ahead of the adds.
 __global__ void __launch_bounds__(kQThreads) seq_scan_kernel(
     const int32_t* page_ids, const int32_t* seq_of_page, int n_pages, int Hkv, float* run_sum,
     float* run_sumsq, int32_t* run_count, uint8_t* pool, int pool_pages, int blob, int n_hi,
     int sequence_mode) {
-  __shared__ QuantSmem sm;  // top-k warp counts (sequence mode)
+  __shared__ uint32_t key[kD], boost[kD / 32];  // sequence-mode ranking
   const int s = blockIdx.x, h = blockIdx.y, c = threadIdx.x;
   const int p0 = first_page_of(seq_of_page, n_pages, s);
   const int p1 = first_page_of(seq_of_page, n_pages, s + 1);
@@ -106,7 +116,7 @@ __global__ void __launch_bounds__(kQThreads) seq_scan_kernel(
   float rs = run_sum[sh * kD + c];
   float rq = run_sumsq[sh * kD + c];
   int rc = run_count[sh];
-  constexpr int kAhead = 8;
+  constexpr int kAhead = 32;  // pages whose sums are loaded ahead of the adds (a long chain is latency-bound)
   for (int i0 = p0; i0 < p1; i0 += kAhead) {
     float a1[kAhead], a2[kAhead];
     float* sc[kAhead];
@@ -133,7 +143,7 @@ __global__ void __launch_bounds__(kQThreads) seq_scan_kernel(
     }
   }
   if (sequence_mode) {
-    const int flag = topk_flag(sm, running_var(rs, rq, __int2float_rn(rc)), n_hi) ? 1 : 0;
+    const int flag = topk_flag(key, boost, running_var(rs, rq, __int2float_rn(rc)), n_hi) ? 1 : 0;
     for (int i = p0; i < p1; ++i) {
       const int pid = page_ids[i];
       if (pid >= 0 && pid < pool_pages)
@@ -220,12 +230,8 @@ __global__ void __launch_bounds__(kQThreads) seq_walk_kernel(
     __syncthreads();  // every thread is done with this stage before it is refilled
   }
   if (sequence_mode) {
-    // the boost set of the whole sequence
-    key[c] = var_key(running_var(rs, rq, __int2float_rn(rc)));
-    __syncthreads();
-    if (c < 32) topk_masks(key, boost, n_hi);  // the page quantizer's ranking
-    __syncthreads();
-    const int flag = (boost[c >> 5] >> (c & 31)) & 1u;
+    // the boost set of the whole sequence (the page quantizer's ranking)
+    const int flag = topk_flag(key, boost, running_var(rs, rq, __int2float_rn(rc)), n_hi) ? 1 : 0;
     for (int i = p0; i < p1; ++i) {
       const int pid = page_ids[i];
       if (pid >= 0 && pid < pool_pages)

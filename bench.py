@@ -294,8 +294,6 @@ def run_kitty(args, rank, world, local_rank):
     fl_st = torch.full((L, B), -1, dtype=torch.int32, device="cuda")
     graphs = None
     if args.graphs:
-        layers[0].attend(q_all[0, 0], out[0])   # first launch outside any capture
-        torch.cuda.synchronize()
         if args.fused:
             graphs = [[(None, lc.capture_step(kn_all[st, l], vn_all[st, l], fl_st[l], q_all[st, l],
                                               out[l]))

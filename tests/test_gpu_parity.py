@@ -204,19 +204,22 @@ def test_decode_attention(case, out_dtype):
     assert excess <= 0, "max err %.3e of RMS" % rel
 
 
-def test_decode_split_invariance():
+@pytest.mark.parametrize("pps", [1, 3, 4, 5, 64])
+def test_decode_split_invariance(pps):
     """Different split-K chunks agree to well inside the tolerance.  They are not
     identical: probabilities enter the tensor cores as fp16 hi/lo pairs relative to
     each warp's running max, so tiny weights fall in the fp16 subnormal range with
-    a different absolute rounding per split layout (~1e-5 of RMS observed)."""
+    a different absolute rounding per split layout (~1e-5 of RMS observed).  On
+    the 64-page sequence the chunk sizes give 64, 22, 16, 13 and 1 splits: the
+    merge's several-round path (full and ragged last round), its one-round path
+    and no merge at all; the shorter sequences leave splits without pages."""
     w = _variant("small_gqa", pages=np.array([37, 1, 64]), tails=np.array([0, 5, 17]))
     inp = synth.host_inputs(w, seed=4)
     pool, _ = gpu_quantize(w, inp)
-    a = gpu_decode(w, inp, pool, pps=4)
-    b = gpu_decode(w, inp, pool, pps=64)
+    a = gpu_decode(w, inp, pool, pps=pps)
     c = gpu_decode(w, inp, pool, pps=0)
-    scale = np.sqrt(np.mean(a ** 2))
-    assert np.abs(a - b).max() <= 1e-4 * scale and np.abs(a - c).max() <= 1e-4 * scale
+    scale = np.sqrt(np.mean(c ** 2))
+    assert np.abs(a - c).max() <= 1e-4 * scale
     ref, _ = oracle_decode(w, inp, pool.cpu().numpy())
     assert attn_error(a, ref)[0] <= 0
 

@@ -265,14 +265,14 @@ def run_kitty(args, rank, world, local_rank):
     kitty.load()
     K, W = args.steps, args.warmup
     E = max(1, min(K, args.e2e_steps))
-    steps_total = W + K + E + 1   # + one untimed end-to-end step
+    steps_total = W + K + E + 3   # + two untimed end-to-end steps, + the plan made one step ahead
     spec = workload_spec(args.workload, steps_total)
     if args.layers:
         spec["layers"] = args.layers
 
     L, B, Hq = spec["layers"], spec["B"], spec["Hq"]
     cfg, layers = build_layers(spec, steps_total, pages_per_split=args.pages_per_split)
-    nsets = min(4, steps_total)
+    nsets = max(1, min(4, W))  # every input set's graph is replayed (uploaded) in warm-up
     q_all, kn_all, vn_all = token_inputs(spec, nsets)
     out = torch.empty((L, B, Hq, D), dtype=torch.bfloat16 if spec["dtype"] else torch.float16,
                       device="cuda")
@@ -282,52 +282,45 @@ def run_kitty(args, rank, world, local_rank):
         plans.append(np.stack([lc.plan_flush() for lc in layers]))
         kvtok.append([lc.kv_tokens() for lc in layers])  # tokens each layer's call attends to
         # bytes of the timed call: the decode call, or the fused append + decode
-        algo.append([lc.algorithmic_bytes() + (lc.append_bytes(plans[-1][l], fused=True)
-                                               if args.fused else 0)
+        # (with graphs, a layer's call is timed with its append also when unfused)
+        algo.append([lc.algorithmic_bytes() + (lc.append_bytes(plans[-1][l], fused=bool(args.fused))
+                                               if args.fused or args.graphs else 0)
                      for l, lc in enumerate(layers)])
     fl_dev = torch.from_numpy(np.stack(plans)).cuda()
     splits, chunk = kitty.decode_plan(layers[0].cfg, B, layers[0].max_pages)
     stream = torch.cuda.current_stream()
-    # CUDA graphs: per input set and layer, one graph for the append and one for
-    # the decode call (the per-layer events stay outside the graphs); the step's
-    # flush ids are copied into one fixed buffer first
+    # CUDA graphs: per input set, one graph of the whole step (every layer's
+    # call, in layer order); the step's flush ids are copied into one fixed
+    # buffer first.  Without graphs the calls are made directly, with events
+    # around each layer's decode call.
     fl_st = torch.full((L, B), -1, dtype=torch.int32, device="cuda")
     graphs = None
     if args.graphs:
-        if args.fused:
-            graphs = [[(None, lc.capture_step(kn_all[st, l], vn_all[st, l], fl_st[l], q_all[st, l],
-                                              out[l]))
-                       for l, lc in enumerate(layers)] for st in range(nsets)]
-        else:
-            graphs = [[lc.capture(kn_all[st, l], vn_all[st, l], fl_st[l], q_all[st, l], out[l])
-                       for l, lc in enumerate(layers)] for st in range(nsets)]
+        from mixed_precision_bit_gb300.cache import capture_layers_step
+        graphs = [capture_layers_step(layers, kn_all[st], vn_all[st], fl_st, q_all[st], out,
+                                      fused=bool(args.fused)) for st in range(nsets)]
 
-    def step(s, events=None):
+    def step(s, events):
         st = s % nsets
         if graphs:
             fl_st.copy_(fl_dev[s])
+            graphs[st].replay()
+            return
         for l, lc in enumerate(layers):
             if not args.fused:
-                if graphs:
-                    graphs[st][l][0].replay()
-                else:
-                    lc.append(kn_all[st, l], vn_all[st, l], fl_dev[s, l])
-            if events is not None:
-                events[l][0].record(stream)
-            if graphs:
-                graphs[st][l][1].replay()
-            elif args.fused:
+                lc.append(kn_all[st, l], vn_all[st, l], fl_dev[s, l])
+            events[l][0].record(stream)
+            if args.fused:
                 lc.step(kn_all[st, l], vn_all[st, l], fl_dev[s, l], q_all[st, l], out[l])
             else:
                 lc.attend(q_all[st, l], out[l])
-            if events is not None:
-                events[l][1].record(stream)
+            events[l][1].record(stream)
 
-    for s in range(W):
-        step(s)
-    torch.cuda.synchronize()
     ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-           for _ in range(L)] for _ in range(K)]
+           for _ in range(L)] for _ in range(W + K)]
+    for s in range(W):
+        step(s, ev[s])
+    torch.cuda.synchronize()
     t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     if world > 1:
         torch.distributed.barrier()
@@ -335,14 +328,20 @@ def run_kitty(args, rank, world, local_rank):
     clocks = ClockSampler(local_rank) if rank == 0 else None
     t0.record(stream)
     for s in range(K):
-        step(W + s, ev[s])
+        step(W + s, ev[W + s])
     t1.record(stream)
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
     clk = clocks.stop() if clocks else None
     ms = dist_max(t0.elapsed_time(t1), world)
-    dec_ms = [ev[s][l][0].elapsed_time(ev[s][l][1]) for s in range(K) for l in range(L)]
+    if graphs:
+        # one graph per step: a layer's call is timed as the step's time over
+        # its layers (an upper bound: the gaps between layers count against it)
+        dec_ms = [ms / (K * L)] * (K * L)
+    else:
+        dec_ms = [ev[W + s][l][0].elapsed_time(ev[W + s][l][1])
+                  for s in range(K) for l in range(L)]
     dec_bytes = [algo[W + s][l] for s in range(K) for l in range(L)]
     dec_tokens = [kvtok[W + s][l] for s in range(K) for l in range(L)]
     status = [int(lc.status.item()) for lc in layers]
@@ -359,7 +358,8 @@ def run_kitty(args, rank, world, local_rank):
         srv.q[l].copy_(q_all[0, l].cpu())
         srv.k_new[l].copy_(kn_all[0, l].cpu())
         srv.v_new[l].copy_(vn_all[0, l].cpu())
-    srv.run()   # untimed: the first replay of freshly captured graphs uploads them
+    for _ in range(2):   # untimed: the first replay of each freshly captured graph uploads it
+        srv.run()
     torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
@@ -596,7 +596,7 @@ def main():
                                       "pool_bytes": r["pool_bytes"],
                                       "launch": ("fused append + decode per layer" if args.fused
                                                  else "append, then decode, per layer") +
-                                                (", CUDA graphs" if args.graphs else ", direct calls")}),
+                                                (", one CUDA graph per step" if args.graphs else ", direct calls")}),
         "kv_tokens_per_s": sum(r["dec_tokens"]) / (sum(r["dec_ms"]) / 1e3),
         "hbm_gbs": {"decode_kernel": achieved,
                     "step_average": world * step_bytes * K / (r["ms"] / 1e3) / 1e9 / world,
@@ -608,10 +608,13 @@ def main():
                                  if traffic_ratio is not None and spec["name"] == "budget" else None),
                      "kernel": ("kitty_append_decode (decode_kernel with the append fused in + "
                                 "split combine)" if args.fused else
+                                "kitty_append_token + kitty_decode_attention" if args.graphs else
                                 "kitty_decode_attention (decode_kernel + split combine)"),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src,
                      "algorithmic_bytes_per_launch": dec_bytes,
-                     "avg_launch_ms": dec_s * 1e3},
+                     "avg_launch_ms": dec_s * 1e3,
+                     "launch_timing": ("timed step / layers (one CUDA graph per step)" if args.graphs
+                                       else "CUDA events around each call")},
         "gpu_launches": r["gpu_launches"],
         "quantize": r["quantize"],
         "clocks": r["clocks"],

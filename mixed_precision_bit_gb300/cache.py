@@ -178,21 +178,46 @@ class LayerCache:
                 + self.B * Hq * D * 2 * 2 + pages * 4)
 
 
+def capture_layers_step(layers, k_new, v_new, flush_ids, q, out, sm_scale=None,
+                        fused: bool = True):
+    """One CUDA graph of a decode step over every layer: per layer l in order, the
+    fused step(k_new[l], v_new[l], flush_ids[l], q[l], out[l]) (fused=False:
+    append then attend).  Each argument is indexed by layer (a list, or a tensor
+    with a leading layer dimension).  The layers' kernels run back to back inside
+    one graph, so a step costs one graph launch instead of one per layer.
+    Capturing runs nothing; replaying runs the calls on what the tensors hold then,
+    on the current stream."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for l, lc in enumerate(layers):
+            if fused:
+                lc.step(k_new[l], v_new[l], flush_ids[l], q[l], out[l], sm_scale)
+            else:
+                lc.append(k_new[l], v_new[l], flush_ids[l])
+                lc.attend(q[l], out[l], sm_scale)
+    return g
+
+
 class ServingStep:
     """One decode step of every layer from pinned host memory, with the copies
     overlapped with the kernels.
 
-    Per layer, the query rows, the new Key/Value token and the flush ids sit
-    in one contiguous pinned block (views: q[l], k_new[l], v_new[l]; the caller
-    writes q, k_new and v_new before run()), copied up with one transfer on an
-    upload stream; the layer's call waits only for its own block, and its
-    output comes back on a download stream while later layers compute.  The
-    flush plan of layer l is made on the host just before its block goes up,
-    so planning overlaps the kernels of the layers before it.  run() returns
-    once every output is in `out` (pinned host, [L][B][Hq][D]).
+    Per layer, the query rows and the new Key/Value token sit in one contiguous
+    pinned block (views: q[l], k_new[l], v_new[l]; the caller writes them before
+    run()), copied up with one transfer on an upload stream; the layer's call
+    waits only for its own block, and its output comes back on a download stream
+    while later layers compute.  run() returns once every output is in `out`
+    (pinned host, [L][B][Hq][D]).
 
-    graphs=True replays each layer's fused call as a CUDA graph captured on
-    the device buffers; fused=False runs append then attend per layer.
+    graphs=True: the whole step (uploads, every layer's call, downloads) is one
+    CUDA graph, so a step costs one graph launch.  The flush ids of the next
+    step are planned on the host while the graph of this one runs (the host
+    mirrors of the layers run one step ahead between calls); two graphs read
+    the plans from alternating pinned buffers.  Between run() calls the layers
+    must not be driven by other calls.
+    graphs=False: direct calls; the flush plan of layer l is made just before
+    its block goes up, so planning overlaps the kernels of the layers before it.
+    fused=False runs append then attend per layer.
     """
 
     def __init__(self, layers, graphs: bool = True, fused: bool = True, sm_scale=None):
@@ -223,14 +248,12 @@ class ServingStep:
         self.fused, self.sm_scale = fused, sm_scale
         self.graphs = None
         if graphs:
-            if fused:
-                self.graphs = [(None, lc.capture_step(self._dk[l], self._dv[l], self._dfl[l],
-                                                      self._dq[l], self.d_out[l], sm_scale))
-                               for l, lc in enumerate(layers)]
-            else:
-                self.graphs = [lc.capture(self._dk[l], self._dv[l], self._dfl[l], self._dq[l],
-                                          self.d_out[l], sm_scale)
-                               for l, lc in enumerate(layers)]
+            # flush plans of two consecutive steps, and their device copy
+            self.h_fl = [torch.empty((L, B), dtype=torch.int32).pin_memory() for _ in range(2)]
+            self.d_fl = torch.empty((L, B), dtype=torch.int32, device=dev)
+            self.graphs = [self._capture(p) for p in range(2)]
+            self._parity = 0
+            self._planned = False
 
     def _views(self, buf, l, B, Hq, Hkv):
         o = l * self.block
@@ -241,6 +264,43 @@ class ServingStep:
         f = buf[o + s[0] + s[1] + s[2]:o + s[0] + s[1] + s[2] + s[3]].view(torch.int32)
         return q, k, v, f
 
+    def _call(self, l, flush_ids):
+        lc = self.layers[l]
+        if self.fused:
+            lc.step(self._dk[l], self._dv[l], flush_ids, self._dq[l], self.d_out[l], self.sm_scale)
+        else:
+            lc.append(self._dk[l], self._dv[l], flush_ids)
+            lc.attend(self._dq[l], self.d_out[l], self.sm_scale)
+
+    def _capture(self, parity):
+        """The graph of one step reading its flush plan from h_fl[parity]."""
+        qkv = sum(self.sizes[:3])
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            cap = torch.cuda.current_stream()
+            self.up.wait_stream(cap)
+            self.down.wait_stream(cap)
+            with torch.cuda.stream(self.up):
+                self.d_fl.copy_(self.h_fl[parity], non_blocking=True)
+                for l in range(len(self.layers)):
+                    o = l * self.block
+                    self.d_in[o:o + qkv].copy_(self.h_in[o:o + qkv], non_blocking=True)
+                    self.ev_in[l].record(self.up)
+            for l in range(len(self.layers)):
+                cap.wait_event(self.ev_in[l])
+                self._call(l, self.d_fl[l])
+                self.ev_out[l].record(cap)
+                with torch.cuda.stream(self.down):
+                    self.down.wait_event(self.ev_out[l])
+                    self.out[l].copy_(self.d_out[l], non_blocking=True)
+            cap.wait_stream(self.down)
+        return g
+
+    def _plan(self, parity):
+        fl = self.h_fl[parity].numpy()
+        for l, lc in enumerate(self.layers):
+            fl[l] = lc.plan_flush()
+
     def bytes_up(self) -> int:
         return len(self.layers) * sum(self.sizes)
 
@@ -249,6 +309,15 @@ class ServingStep:
 
     def run(self):
         cur = torch.cuda.current_stream()
+        if self.graphs is not None:
+            if not self._planned:
+                self._plan(self._parity)
+                self._planned = True
+            self.graphs[self._parity].replay()
+            self._parity ^= 1
+            self._plan(self._parity)  # the next step's flushes, while this one runs
+            cur.synchronize()
+            return self.out
         # the device input blocks and outputs may still be in use by work queued
         # before this call
         self.up.wait_stream(cur)
@@ -260,16 +329,7 @@ class ServingStep:
                 self.d_in[o:o + self.block].copy_(self.h_in[o:o + self.block], non_blocking=True)
                 self.ev_in[l].record(self.up)
             cur.wait_event(self.ev_in[l])
-            if self.graphs is not None:
-                if self.graphs[l][0] is not None:
-                    self.graphs[l][0].replay()
-                self.graphs[l][1].replay()
-            elif self.fused:
-                lc.step(self._dk[l], self._dv[l], self._dfl[l], self._dq[l], self.d_out[l],
-                        self.sm_scale)
-            else:
-                lc.append(self._dk[l], self._dv[l], self._dfl[l])
-                lc.attend(self._dq[l], self.d_out[l], self.sm_scale)
+            self._call(l, self._dfl[l])
             self.ev_out[l].record(cur)
             with torch.cuda.stream(self.down):
                 self.down.wait_event(self.ev_out[l])

@@ -1,4 +1,5 @@
-"""GPU check of the pipelined multi-layer serving step (cache.ServingStep).
+"""GPU check of the pipelined multi-layer serving step (cache.ServingStep), and
+of the one-graph step over every layer (cache.capture_layers_step).
 
 Its copies run on side streams, overlapped with the kernels. Over many decode
 steps with page flushes, it must give outputs and cache state bit-identical to
@@ -91,6 +92,56 @@ def test_serving_step_matches_per_layer_calls(graphs, fused):
             assert torch.equal(getattr(a, name), getattr(b, name)), name
         assert int(b.status.item()) == 0
     assert srv.bytes_up() == L * (B * Hq * 128 * 2 + 2 * B * Hkv * 128 * 2 + B * 4)
+
+
+@pytest.mark.parametrize("fused", [True, False], ids=["fused", "unfused"])
+def test_layers_step_graph_matches_per_layer_calls(fused):
+    """One graph over every layer's call of a step (capture_layers_step), replayed
+    on new inputs each step, against the same calls made directly: outputs and
+    cache state bit-identical, across page flushes."""
+    import torch
+    from mixed_precision_bit_gb300.cache import capture_layers_step
+    L, B, Hkv, Hq, n_hi = 3, 5, 2, 8, 32
+    pages, tails = [3, 1, 0, 2, 4], [30, 31, 5, 0, 17]
+    ref = _layers(L, B, Hkv, Hq, n_hi, pages, tails, torch.Generator("cuda").manual_seed(3))
+    new = _layers(L, B, Hkv, Hq, n_hi, pages, tails, torch.Generator("cuda").manual_seed(3))
+    q_in = torch.empty((L, B, Hq, 128), dtype=torch.int16, device="cuda")
+    k_in = torch.empty((L, B, Hkv, 128), dtype=torch.int16, device="cuda")
+    v_in = torch.empty_like(k_in)
+    fl_in = torch.full((L, B), -1, dtype=torch.int32, device="cuda")
+    out = torch.empty((L, B, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    graph = capture_layers_step(new, k_in, v_in, fl_in, q_in, out, fused=fused)
+    g = torch.Generator("cuda").manual_seed(5)
+    d_out = torch.empty((B, Hq, 128), dtype=torch.bfloat16, device="cuda")
+    flushes = 0
+    for step in range(40):
+        q = torch.randn((L, B, Hq, 128), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+        k = torch.randn((L, B, Hkv, 128), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+        v = torch.randn((L, B, Hkv, 128), generator=g, device="cuda").to(torch.bfloat16).view(torch.int16)
+        plans = [lc.plan_flush() for lc in new]
+        q_in.copy_(q)
+        k_in.copy_(k)
+        v_in.copy_(v)
+        fl_in.copy_(torch.from_numpy(np.stack(plans)))
+        graph.replay()
+        for l, lc in enumerate(ref):
+            fl = lc.plan_flush()
+            assert (fl == plans[l]).all()
+            flushes += int((fl >= 0).sum())
+            fd = torch.from_numpy(fl).cuda()
+            if fused:
+                lc.step(k[l], v[l], fd, q[l], d_out)
+            else:
+                lc.append(k[l], v[l], fd)
+                lc.attend(q[l], d_out)
+            assert torch.equal(out[l].view(torch.int16), d_out.view(torch.int16)), (step, l)
+    assert flushes >= 2 * L
+    torch.cuda.synchronize()
+    for a, b in zip(ref, new):
+        for name in ("pool", "block_table", "num_pages", "tail_k", "tail_v", "tail_len",
+                     "run_sum", "run_sumsq", "run_count", "status"):
+            assert torch.equal(getattr(a, name), getattr(b, name)), name
+        assert int(b.status.item()) == 0
 
 
 _FRESH = r"""

@@ -253,7 +253,7 @@ class ServingStep:
             self.d_fl = torch.empty((L, B), dtype=torch.int32, device=dev)
             self.graphs = [self._capture(p) for p in range(2)]
             self._parity = 0
-            self._planned = False
+            self._planned = 0  # layers whose flushes of the pending step are planned
 
     def _views(self, buf, l, B, Hq, Hkv):
         o = l * self.block
@@ -297,9 +297,13 @@ class ServingStep:
         return g
 
     def _plan(self, parity):
+        """Plans the pending step's flushes into h_fl[parity], from the first layer
+        not yet planned: a layer whose page allocation fails raises, and the next
+        call resumes at that layer."""
         fl = self.h_fl[parity].numpy()
-        for l, lc in enumerate(self.layers):
-            fl[l] = lc.plan_flush()
+        while self._planned < len(self.layers):
+            fl[self._planned] = self.layers[self._planned].plan_flush()
+            self._planned += 1
 
     def bytes_up(self) -> int:
         return len(self.layers) * sum(self.sizes)
@@ -310,12 +314,14 @@ class ServingStep:
     def run(self):
         cur = torch.cuda.current_stream()
         if self.graphs is not None:
-            if not self._planned:
-                self._plan(self._parity)
-                self._planned = True
+            self._plan(self._parity)  # nothing left to do unless the look-ahead stopped
             self.graphs[self._parity].replay()
             self._parity ^= 1
-            self._plan(self._parity)  # the next step's flushes, while this one runs
+            self._planned = 0
+            try:
+                self._plan(self._parity)  # the next step's flushes, while this one runs
+            except kitty.KittyError:
+                pass  # e.g. the pool is full: raised by the next run(), before its step
             cur.synchronize()
             return self.out
         # the device input blocks and outputs may still be in use by work queued

@@ -122,23 +122,13 @@ class LayerCache:
 
     def capture_step(self, k_new, v_new, flush_ids, q, out, sm_scale=None):
         """A CUDA graph of one fused step(k_new, v_new, flush_ids, q, out) on these
-        tensors (see capture)."""
+        tensors: replaying it runs the call on what the tensors hold then, on the
+        current stream.  Capturing runs nothing; the cache state changes only on
+        replay."""
         g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g):
             self.step(k_new, v_new, flush_ids, q, out, sm_scale)
         return g
-
-    def capture(self, k_new, v_new, flush_ids, q, out, sm_scale=None):
-        """CUDA graphs of one append(k_new, v_new, flush_ids) and one attend(q, out)
-        on these tensors: replaying a graph runs the call on what the tensors hold
-        then, on the current stream.  Returns (append_graph, attend_graph).
-        Capturing runs nothing; the cache state changes only on replay."""
-        ga, gd = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-        with torch.cuda.graph(ga):
-            self.append(k_new, v_new, flush_ids)
-        with torch.cuda.graph(gd):
-            self.attend(q, out, sm_scale)
-        return ga, gd
 
     def append(self, k_new, v_new, flush_ids, stream=None):
         kitty.append_token(self.cfg, k_new, v_new, self.tail_k, self.tail_v, self.tail_len,

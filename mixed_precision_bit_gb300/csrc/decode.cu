@@ -54,7 +54,7 @@ static_assert(sizeof(QuantSmem) <= (size_t)kDWarps * stages_for(2) * 3072 &&
                   sizeof(QuantSmem) <= (size_t)kDWarps * stages_for(4) * 4096,
               "page quantizer state does not fit in the decode stage buffers");
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of one barrier phase (~0.1-1 s)
-constexpr int kPartial = kD + 2;           // split partial: m, l, o[128]
+constexpr int kPartial = kD + 4;           // split partial: m, l, 2 unused, o[128] (16-byte aligned)
 constexpr int kMaxSplits = 256;            // splits per sequence, at most
 // Running-max floor (log2 units): finite, so masked scores (-inf) give p = 0 exactly.
 constexpr float kNegBig = -1.0e30f;
@@ -158,6 +158,36 @@ __device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
 __device__ __forceinline__ uint32_t hilo_mul(uint32_t q, uint32_t S, uint32_t fneg) {
   const uint32_t h = hmul2u(q, hmul2u(S, fneg));
   return hfma2u(q, S, h);
+}
+
+// Four consecutive channels i..i+3 (i % 4 == 0): one vector store when the
+// output array is 16-byte aligned, else four scalar stores.
+__device__ __forceinline__ void store_out4(void* out, int dt, size_t i, float4 v) {
+  if ((reinterpret_cast<uintptr_t>(out) & 15u) == 0) {
+    if (dt == KITTY_F32) {
+      *reinterpret_cast<float4*>(static_cast<float*>(out) + i) = v;
+    } else if (dt == KITTY_BF16) {
+      const __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), c = __floats2bfloat162_rn(v.z, v.w);
+      *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(out) + i) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&a), *reinterpret_cast<const uint32_t*>(&c));
+    } else {
+      *reinterpret_cast<uint2*>(static_cast<__half*>(out) + i) =
+          make_uint2(h2_bits(__floats2half2_rn(v.x, v.y)), h2_bits(__floats2half2_rn(v.z, v.w)));
+    }
+    return;
+  }
+  if (dt == KITTY_F32) {
+    float* o = static_cast<float*>(out) + i;
+    o[0] = v.x; o[1] = v.y; o[2] = v.z; o[3] = v.w;
+  } else if (dt == KITTY_BF16) {
+    __nv_bfloat16* o = static_cast<__nv_bfloat16*>(out) + i;
+    o[0] = __float2bfloat16_rn(v.x); o[1] = __float2bfloat16_rn(v.y);
+    o[2] = __float2bfloat16_rn(v.z); o[3] = __float2bfloat16_rn(v.w);
+  } else {
+    __half* o = static_cast<__half*>(out) + i;
+    o[0] = __float2half_rn(v.x); o[1] = __float2half_rn(v.y);
+    o[2] = __float2half_rn(v.z); o[3] = __float2half_rn(v.w);
+  }
 }
 
 __device__ __forceinline__ void store_out(void* out, int dt, size_t i, float v) {
@@ -867,48 +897,61 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       if (c == 0 && !(Lsum[h] > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
     } else {
       float* part = p.ws + (((size_t)b * p.Hq + hq) * p.splits + s) * kPartial;
-      part[2 + c] = Osum[h];
+      part[4 + c] = Osum[h];
       if (c == 0) { part[0] = ms[h]; part[1] = Lsum[h]; }
     }
   }
 }
 
-// Merge the split partials of one (sequence, query head); 128 threads = channels.
-// Splits without pages left m = -inf.  In a fused append, the CTA of query
-// head 0 then does the sequence's append bookkeeping (every decode CTA has read
-// the old lengths by now).  Launched as a programmatic dependent of the decode
-// kernel: it may be scheduled while the decode grid drains, and waits for the
-// whole grid (and its memory) before reading the partials.
-__global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
+// Merge the split partials: 32 threads per (sequence, query head) row, four
+// channels a thread (16-byte loads), four rows per 128-thread CTA.  Splits
+// without pages left m = -inf.  In a fused append, the row of query head 0 then
+// does the sequence's append bookkeeping (every decode CTA has read the old
+// lengths by now).  Launched as a programmatic dependent of the decode kernel:
+// it may be scheduled while the decode grid drains, and waits for the whole
+// grid (and its memory) before reading the partials.
+__device__ __forceinline__ void merge_split(float m, float l, float4 o, float ms, float& L,
+                                            float4& O) {
+  if (m == -INFINITY) return;  // no pages: l, o were never written
+  const float e = ex2(m - ms);
+  L += l * e;
+  O.x += o.x * e;
+  O.y += o.y * e;
+  O.z += o.z * e;
+  O.w += o.w * e;
+}
+
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int rows) {
   grid_dependency_wait();
-  const int bh = blockIdx.x, b = bh / p.Hq, c = threadIdx.x;
+  const int bh = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (bh >= rows) return;
+  const int b = bh / p.Hq;
   const float* base = p.ws + (size_t)bh * p.splits * kPartial;
-  float ms = -INFINITY;
-  float L = 0.f, O = 0.f;
+  const float4* obase = reinterpret_cast<const float4*>(base + 4) + lane;  // kPartial / 4 apart
+  constexpr int kQ = kPartial / 4;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float ms = -INFINITY, L = 0.f;
+  float4 O = zero;
   constexpr int kU = 8;
   if (p.splits <= kU) {
-    // every split's (m, l, o[c]) in one round of independent loads
-    float m[kU], l[kU], o[kU];
+    // every split's (m, l, o[4 lane..4 lane+3]) in one round of independent loads
+    float m[kU], l[kU];
+    float4 o[kU];
 #pragma unroll
     for (int s = 0; s < kU; ++s) {
       m[s] = s < p.splits ? base[s * kPartial] : -INFINITY;
       l[s] = s < p.splits ? base[s * kPartial + 1] : 0.f;
-      o[s] = s < p.splits ? base[s * kPartial + 2 + c] : 0.f;
+      o[s] = s < p.splits ? obase[s * kQ] : zero;
     }
 #pragma unroll
     for (int s = 0; s < kU; ++s) ms = fmaxf(ms, m[s]);
     if (ms != -INFINITY) {
 #pragma unroll
-      for (int s = 0; s < kU; ++s) {
-        if (m[s] == -INFINITY) continue;  // no pages: l, o were never written
-        const float e = ex2(m[s] - ms);
-        L += l[s] * e;
-        O += o[s] * e;
-      }
+      for (int s = 0; s < kU; ++s) merge_split(m[s], l[s], o[s], ms, L, O);
     }
   } else {
-    // many splits: rounds of kV independent loads, first for the maxima, then
-    // for the sums, which are added in split order as in the branch above
+    // many splits: rounds of independent loads, first for the maxima, then for
+    // the sums, which are added in split order as in the branch above
     constexpr int kV = 16;
     for (int s0 = 0; s0 < p.splits; s0 += kV) {
       float m[kV];
@@ -918,28 +961,26 @@ __global__ void __launch_bounds__(kD) combine_kernel(const DecodeParams p) {
       for (int k = 0; k < kV; ++k) ms = fmaxf(ms, m[k]);
     }
     if (ms != -INFINITY) {
-      for (int s0 = 0; s0 < p.splits; s0 += kV) {
-        float m[kV], l[kV], o[kV];
+      for (int s0 = 0; s0 < p.splits; s0 += kU) {
+        float m[kU], l[kU];
+        float4 o[kU];
 #pragma unroll
-        for (int k = 0; k < kV; ++k) {
+        for (int k = 0; k < kU; ++k) {
           const bool in = s0 + k < p.splits;
           m[k] = in ? base[(s0 + k) * kPartial] : -INFINITY;
           l[k] = in ? base[(s0 + k) * kPartial + 1] : 0.f;
-          o[k] = in ? base[(s0 + k) * kPartial + 2 + c] : 0.f;
+          o[k] = in ? obase[(s0 + k) * kQ] : zero;
         }
 #pragma unroll
-        for (int k = 0; k < kV; ++k) {
-          if (m[k] == -INFINITY) continue;
-          const float e = ex2(m[k] - ms);
-          L += l[k] * e;
-          O += o[k] * e;
-        }
+        for (int k = 0; k < kU; ++k) merge_split(m[k], l[k], o[k], ms, L, O);
       }
     }
   }
-  store_out(p.out, p.out_dtype, (size_t)bh * kD + c, L > 0.f ? O / L : 0.f);
-  if (c == 0 && !(L > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
-  if (p.ap.k_new != nullptr && c == 0 && bh - b * p.Hq == 0)
+  const bool ok = L > 0.f;
+  const float4 r = ok ? make_float4(O.x / L, O.y / L, O.z / L, O.w / L) : zero;
+  store_out4(p.out, p.out_dtype, (size_t)bh * kD + 4 * lane, r);
+  if (lane == 0 && !ok) set_status(p.d_status, KITTY_ST_EMPTY);
+  if (p.ap.k_new != nullptr && lane == 0 && bh - b * p.Hq == 0)
     append_finalize_one(b, p.ap.tail_len, p.ap.flush_page_ids, p.ap.block_table, p.max_pages,
                         p.ap.num_pages, p.pool_pages);
 }
@@ -1196,9 +1237,10 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
   lc.numAttrs = 1;
   cudaError_t e2 = cudaSuccess;
   if (sc.splits > 1) {
-    lc.gridDim = dim3((unsigned)B * cfg->num_q_heads);
-    lc.blockDim = dim3(kD);
-    e2 = cudaLaunchKernelEx(&lc, combine_kernel, p);
+    const int rows = B * cfg->num_q_heads;
+    lc.gridDim = dim3((unsigned)(rows + 3) / 4);
+    lc.blockDim = dim3(128);
+    e2 = cudaLaunchKernelEx(&lc, combine_kernel, p, rows);
   } else if (ap.k_new != nullptr) {
     lc.gridDim = dim3((unsigned)(B + 127) / 128);
     lc.blockDim = dim3(128);

@@ -105,7 +105,7 @@ def test_decode_plan_and_workspace(K):
     cfg = K.Config(num_kv_heads=8, num_q_heads=32)
     s, c = K.decode_plan(cfg, 16, 128)
     assert 1 <= s <= 256 and s * c >= 128 and c % 8 == 0 and c >= 16
-    assert K.decode_workspace_bytes(cfg, 16, 128) == (16 * 32 * s * 130 * 4 if s > 1 else 0)
+    assert K.decode_workspace_bytes(cfg, 16, 128) == (16 * 32 * s * 132 * 4 if s > 1 else 0)
     for B, M in ((1, 4096), (177, 256), (4096, 256), (1, 3), (64, 65536)):
         s, c = K.decode_plan(cfg, B, M)
         assert 1 <= s <= 256 and c <= M and s * c >= M, (B, M, s, c)
@@ -123,7 +123,7 @@ def test_decode_plan_and_workspace(K):
                      decode_max_pages=mx)
         s, c = K.decode_plan(h, B, M)
         assert 1 <= s <= 256 and c <= M, (B, M, mx, s, c)
-        assert K.decode_workspace_bytes(h, B, M) == (B * 32 * s * 130 * 4 if s > 1 else 0)
+        assert K.decode_workspace_bytes(h, B, M) == (B * 32 * s * 132 * 4 if s > 1 else 0)
     # a 16 x 128-page batch in a 136-page table: four 32-page splits, the last to the end
     h = K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=16 * 128, decode_max_pages=128)
     assert K.decode_plan(h, 16, 136) == (4, 40)

@@ -66,7 +66,7 @@ def test_noalloc_matches_workspace_entry_point(out_dtype):
 def test_noalloc_rejects_batches_beyond_its_scratch():
     from mixed_precision_bit_gb300 import kitty
     lib = kitty.load()
-    # 64 sequences x 32 heads x 256 splits of 130 floats is far beyond 8 MiB
+    # 64 sequences x 32 heads x 256 splits of 132 floats is far beyond 8 MiB
     cfg = kitty.Config(num_kv_heads=8, num_q_heads=32, decode_pages_per_split=4)
     need = kitty.decode_workspace_bytes(cfg, 64, 1024)
     assert need > kitty.NOALLOC_SCRATCH_BYTES

@@ -73,12 +73,15 @@ def oracle_quantize(w, inp, running=False, mode=None):
     return pool, None, st
 
 
-def gpu_decode(w, inp, pool, out_dtype="f32", pps=0, status=None, sm_scale=None):
+def gpu_decode(w, inp, pool, out_dtype="f32", pps=0, status=None, sm_scale=None, out_offset=0):
+    """out_offset: the output array starts that many elements into its buffer."""
     import torch
     from mixed_precision_bit_gb300 import kitty
     cfg = cfg_for(w, pps=pps)
     dt = {"f32": torch.float32, "bf16": torch.bfloat16, "f16": torch.float16}[out_dtype]
-    out = torch.full((w.B, w.Hq, 128), float("nan"), dtype=dt, device="cuda")
+    n = w.B * w.Hq * 128
+    out = torch.full((n + out_offset,), float("nan"), dtype=dt, device="cuda")[out_offset:]
+    out = out.view(w.B, w.Hq, 128)
     bt = inp["block_table"]
     nbytes = kitty.decode_workspace_bytes(cfg, w.B, bt.shape[1])
     ws = torch.empty(max(nbytes, 16) // 4, dtype=torch.float32, device="cuda")

@@ -204,6 +204,21 @@ def test_decode_attention(case, out_dtype):
     assert excess <= 0, "max err %.3e of RMS" % rel
 
 
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16", "f16"])
+def test_decode_unaligned_output(out_dtype):
+    """An output array that starts one element past a 16-byte boundary (a plain
+    contiguous view) gets the same values as an aligned one: the split merge
+    stores vectors only into aligned arrays, and the one-split path stores
+    scalars."""
+    w = _variant("small_gqa", pages=np.array([37, 1, 64]), tails=np.array([0, 5, 17]))
+    inp = synth.host_inputs(w, seed=4)
+    pool, _ = gpu_quantize(w, inp)
+    for pps in (4, 0, 64):  # a 16-split merge, the planner's splits, one split
+        a = gpu_decode(w, inp, pool, out_dtype, pps=pps)
+        b = gpu_decode(w, inp, pool, out_dtype, pps=pps, out_offset=1)
+        assert not np.isnan(a).any() and np.array_equal(a, b), pps
+
+
 @pytest.mark.parametrize("pps", [1, 3, 4, 5, 64])
 def test_decode_split_invariance(pps):
     """Different split-K chunks agree to well inside the tolerance.  They are not

@@ -265,7 +265,14 @@ def test_closed_forms_exact_reconstruction(orc):
         else:
             xk[:, c] = off + delta * r.integers(0, 4, 32) * 0.25
             xk[0, c], xk[1, c] = off, off + delta * 0.75
-    xv = np.tile(np.array([0, 1, 2, 3] * 32, np.float32) * 0.5, (32, 1))
+    # Values: every (token, group of 32 channels) has its own offset and
+    # power-of-two step, so only the right group's metadata decodes them exactly
+    xv = np.zeros((32, 128), np.float32)
+    for t in range(32):
+        for G in range(4):
+            q = r.integers(0, 4, 32)
+            q[0], q[1] = 0, 3
+            xv[t, 32 * G:32 * G + 32] = float(r.integers(-8, 8)) + 2.0 ** int(r.integers(-4, 3)) * q
     blob, st = orc.quantize_page_f32(xk, xv, 32)
     kh, vh, _ = orc.dequant_page(blob, 32)
     assert st == 0

@@ -257,19 +257,14 @@ def token_inputs(spec, nsets, seed=1):
     return mk(Hq), mk(Hkv), mk(Hkv)
 
 
-def run_kitty(args, rank, world, local_rank):
+def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
+    """Builds the workload's layers, then times K steps (after W warm-up steps) of
+    one fused append + decode call per layer, replayed as one CUDA graph per
+    step (or as direct calls), with CUDA events on the launching stream and the
+    clocks sampled over the timed region."""
     import numpy as np
     import torch
     from mixed_precision_bit_gb300 import kitty
-    torch.cuda.set_device(local_rank)
-    kitty.load()
-    K, W = args.steps, args.warmup
-    E = max(1, min(K, args.e2e_steps))
-    steps_total = W + K + E + 3   # + two untimed end-to-end steps, + the plan made one step ahead
-    spec = workload_spec(args.workload, steps_total)
-    if args.layers:
-        spec["layers"] = args.layers
-
     L, B, Hq = spec["layers"], spec["B"], spec["Hq"]
     cfg, layers = build_layers(spec, steps_total, pages_per_split=args.pages_per_split)
     nsets = max(1, min(4, W))  # every input set's graph is replayed (uploaded) in warm-up
@@ -342,12 +337,60 @@ def run_kitty(args, rank, world, local_rank):
     else:
         dec_ms = [ev[W + s][l][0].elapsed_time(ev[W + s][l][1])
                   for s in range(K) for l in range(L)]
-    dec_bytes = [algo[W + s][l] for s in range(K) for l in range(L)]
-    dec_tokens = [kvtok[W + s][l] for s in range(K) for l in range(L)]
     status = [int(lc.status.item()) for lc in layers]
     bad = [x for x in status if x not in (0,)]
     if bad:
         raise RuntimeError("device status codes %s" % bad)
+    return dict(cfg=cfg, layers=layers, graphs=graphs, q_all=q_all, kn_all=kn_all, vn_all=vn_all,
+                ms=ms, dec_ms=dec_ms,
+                dec_bytes=[algo[W + s][l] for s in range(K) for l in range(L)],
+                dec_tokens=[kvtok[W + s][l] for s in range(K) for l in range(L)],
+                clocks=clk, splits=splits, chunk=chunk)
+
+
+def target_measure(name, args, world, rank, local_rank, K=20, W=3):
+    """The decode call of one single-layer workload (Qwen3-8B-shaped layer,
+    long-context layer), timed in the same run as the headline: its call time,
+    algorithmic bytes and GB/s against 8 TB/s and the measured copy peak, with
+    its own clock samples."""
+    import torch
+    spec = workload_spec(name, W + K + 2)
+    r = device_run(args, spec, K, W, W + K + 2, world, rank, local_rank)
+    dec_s = statistics.mean(r["dec_ms"]) / 1e3
+    nbytes = statistics.mean(r["dec_bytes"])
+    gbs = nbytes / dec_s / 1e9
+    peak = float(measured_peaks()[0]["hbm_gbs"])
+    res = {"workload": name, "batch": spec["B"], "layers": spec["layers"], "n_hi": spec["n_hi"],
+           "context_pages_max": int(spec["pages"].max()), "splits": r["splits"],
+           "pages_per_split": r["chunk"], "steps": K, "warmup": W,
+           "call_us": dec_s * 1e6, "algorithmic_bytes_per_call": nbytes, "gbs": gbs,
+           "pct_of_8tbs": 100.0 * gbs / NOMINAL_HBM_GBS, "pct_of_measured": 100.0 * gbs / peak,
+           "decode_tokens_per_s_per_layer": spec["B"] / dec_s,
+           "kv_tokens_per_s": sum(r["dec_tokens"]) / (sum(r["dec_ms"]) / 1e3),
+           "clocks": r["clocks"]}
+    del r
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return res
+
+
+def run_kitty(args, rank, world, local_rank):
+    import torch
+    from mixed_precision_bit_gb300 import kitty
+    torch.cuda.set_device(local_rank)
+    kitty.load()
+    K, W = args.steps, args.warmup
+    E = max(1, min(K, args.e2e_steps))
+    steps_total = W + K + E + 3   # + two untimed end-to-end steps, + the plan made one step ahead
+    spec = workload_spec(args.workload, steps_total)
+    if args.layers:
+        spec["layers"] = args.layers
+    L, B = spec["layers"], spec["B"]
+    r0 = device_run(args, spec, K, W, steps_total, world, rank, local_rank)
+    layers, graphs = r0["layers"], r0["graphs"]
+    cfg, ms, clk, splits, chunk = r0["cfg"], r0["ms"], r0["clocks"], r0["splits"], r0["chunk"]
+    q_all, kn_all, vn_all = r0["q_all"], r0["kn_all"], r0["vn_all"]
+    dec_ms, dec_bytes, dec_tokens = r0["dec_ms"], r0["dec_bytes"], r0["dec_tokens"]
 
     # ---- end to end through the public API: host inputs in, outputs back out.
     # ServingStep copies each layer's inputs up and its output back on side
@@ -373,14 +416,21 @@ def run_kitty(args, rank, world, local_rank):
     h2d = srv.bytes_up()
     d2h = srv.bytes_down()
     launches_per_call = 1 + (1 if splits > 1 else 0)
+    pool_bytes = sum(lc.pool.numel() for lc in layers)
+    max_pages = layers[0].max_pages
+    del srv, layers, graphs, r0, q_all, kn_all, vn_all
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
     quant = measure_quantize(spec) if args.measure_quantize else None
-    return dict(spec=spec, cfg=cfg, ms=ms, K=K, W=W, E=E, dec_ms=dec_ms, dec_bytes=dec_bytes,
+    targets = {}
+    for name in [t for t in args.targets.split(",") if t]:
+        targets[name] = target_measure(name, args, world, rank, local_rank)
+    return dict(targets=targets, spec=spec, cfg=cfg, ms=ms, K=K, W=W, E=E, dec_ms=dec_ms, dec_bytes=dec_bytes,
                 dec_tokens=dec_tokens,
                 quantize=quant,
                 clocks=clk, e2e_s=e2e_s, h2d=h2d, d2h=d2h, splits=splits, chunk=chunk,
                 gpu_launches=K * L * (2 if args.fused else 2 + launches_per_call),
-                max_pages=layers[0].max_pages,
-                pool_bytes=sum(lc.pool.numel() for lc in layers))
+                max_pages=max_pages, pool_bytes=pool_bytes)
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
@@ -543,6 +593,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--measure-quantize", type=int, default=1,
                     help="also time bulk page quantization on one layer (1/0)")
+    ap.add_argument("--targets", default="long,qwen3_8b",
+                    help="single-layer workloads whose decode call is also timed in this run "
+                         "(comma-separated; empty: none)")
     args = ap.parse_args()
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -589,7 +642,9 @@ def main():
     line = {
         "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": r["W"], "ms_per_step": r["ms"] / K, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "arithmetic": ("bf16 inputs; 2-bit codes as exact fp16 tensor-core operands against fp16 "
+                       "hi/lo pairs of the folded scales; fp32 accumulation and online softmax"),
         "data": "synthetic (seeded, on device): K ~ N(0,1)*lognormal channel scales, V,Q ~ N(0,1), bf16",
         "config": config_block(spec, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "splits": r["splits"], "pages_per_split": r["chunk"],
@@ -617,6 +672,7 @@ def main():
                                        else "CUDA events around each call")},
         "gpu_launches": r["gpu_launches"],
         "quantize": r["quantize"],
+        "targets": r["targets"],
         "clocks": r["clocks"],
         "e2e": {"value": job_throughput(world, B, r["E"], r["e2e_s"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},

@@ -99,10 +99,20 @@ typedef struct {
                                    pages, and the last one still reaches
                                    max_pages, so any value gives correct
                                    results */
+  int32_t decode_wait_polls;      /* bound of the decode page loop's waits for a
+                                   staged page, in polls of its barrier;
+                                   0 = the library's bound (2^22 polls, about
+                                   0.1-1 s).  A wait that runs out sets
+                                   KITTY_ST_TIMEOUT, waits (with the library's
+                                   bound) for the CTA's copies still in flight
+                                   and ends the CTA's page loop; its outputs are
+                                   then undefined.  A small value makes ordinary
+                                   copies outlast the wait, which is how the
+                                   timeout path is tested */
 } kitty_cfg;
 
-/* Library ABI version (this header: 3; kitty_cfg gained decode_total_pages in
- * version 2 and decode_max_pages in version 3). */
+/* Library ABI version (this header: 4; kitty_cfg gained decode_total_pages in
+ * version 2, decode_max_pages in version 3 and decode_wait_polls in version 4). */
 int kitty_abi_version(void);
 
 /* Packed page size.  A page holds Hkv blobs, one per kv head, in head order;
@@ -111,10 +121,11 @@ int kitty_abi_version(void);
  * plane 4*w*n_hi B, Key step fp16[128], Key minimum fp16[128], channel list
  * uint8[n_hi] (ascending), Value plane 1024 B, Value step fp16[4][32], Value
  * minimum fp16[4][32] (group-major).  = 3072 + 9*n_hi bytes at (4, 2) (3360 at
- * n_hi=32), 4096 + 17*n_hi at (8, 4).  The
- * bit positions inside the planes are the "fragment order" index maps
- * documented in the oracle and DESIGN notes.  Paper: Abstract (page-centric
- * layout, two uniform 2-bit tensors per Key page). */
+ * n_hi=32), 4096 + 17*n_hi at (8, 4).  Inside the planes, codes sit in
+ * "fragment order": the 32 bytes at offset 32*L of a 2-bit plane hold what lane
+ * L of a warp takes as its tensor-core operand fragments (the oracle's key_pos,
+ * key_pos4 and val_pos index functions spell the maps out).  Paper: Abstract
+ * (page-centric layout, two uniform 2-bit tensors per Key page). */
 int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page);
 
 /* Effective Key bits per element, codes only: hf*hi_bit + (1-hf)*lo_bit with
@@ -155,9 +166,12 @@ void kitty_alloc_destroy(kitty_alloc* a);
  *   page sums first, the channels are ranked once on that variance, and every
  *   page of the sequence is quantized with that one boost set (VeloxQuant-MLX
  *   docs, Prefill phase: one ranking per head over the prompt).
- *   Both modes run in three launches (page sums in parallel, a per-(sequence,
- *   head) scan, quantization in parallel) with the fp32 additions in page
- *   order, so they give the same bytes as quantizing one page at a time.
+ *   Both modes keep the fp32 additions in page order, so they give the same
+ *   bytes as quantizing one page at a time.  With at least 3 (sequence, kv
+ *   head) chains per SM they run in two launches (a per-chain walk that reads
+ *   each Key tile once and keeps the running totals, then quantization in
+ *   parallel); with fewer chains in three (page sums in parallel, a
+ *   per-(sequence, head) scan, quantization in parallel).
  *   Pages whose seq_of_page entry is outside [0, n_seqs) are not written
  *   (KITTY_ST_BAD_SEQ).
  *   pool        device, pool_pages * per_page bytes, 16-byte aligned. */
@@ -198,7 +212,10 @@ int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pa
  *   out[b][hq] = softmax_t(sm_scale * q.k_t) . v_t over the num_pages[b] pages
  *   listed in block_table[b][0..num_pages[b]) followed by the tail_len[b] tail
  *   tokens; an empty sequence gives 0 and KITTY_ST_EMPTY.
- *   q       device [B][Hq][128] 16-bit (in_dtype)
+ *   q       device [B][Hq][128] 16-bit (in_dtype).  The tensor cores take the
+ *           query as fp16: a bf16 query element with |q| > 65504 sets
+ *           KITTY_ST_RANGE (NaN or Inf: KITTY_ST_NONFINITE), and the outputs of
+ *           its kv head's query group are then undefined
  *   pool    device, 16-byte aligned, pool_pages pages
  *   tail_k, tail_v device [B][Hkv][32][128] 16-bit, 16-byte aligned; may be NULL
  *           if all tails are 0
@@ -264,8 +281,11 @@ int kitty_decode_attention_noalloc(const kitty_cfg* cfg, const void* q, const vo
 
 /* Launch shape that kitty_decode_attention uses for this batch shape: number of
  * splits per sequence (at most 256) and the pages in the largest split (for
- * reporting and tests).  Splits are cut from the end of each sequence, so a
- * sequence shorter than max_pages drops whole leading splits. */
+ * reporting and tests).  Split s covers block-table positions [start_s,
+ * start_(s+1)), from position 0 upwards with the largest split first.  A
+ * sequence shorter than max_pages leaves its later splits without pages: they
+ * write an empty partial, which the merge skips.  Split 0 always runs; it also
+ * takes the tail tokens. */
 int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pages, int32_t* splits,
                       int32_t* pages_per_split);
 

@@ -91,6 +91,7 @@ struct DecodeParams {
   float* ws;
   int32_t* d_status;
   float sm_log2;  // sm_scale * log2(e)
+  uint32_t wait_polls;  // bound of a page wait, in polls of its barrier
   int pool_pages, max_pages, out_dtype, splits, Hkv, Hq, g, n_hi, blob, in_dtype;
   // Split s of a sequence with np pages covers pages [starts[s], min(np, starts[s+1]));
   // starts[] rises from 0 to starts[splits] = max_pages.  A split holds work only
@@ -577,6 +578,14 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
 #pragma unroll
   for (int h = 0; h < 4; ++h)
     qv[h] = h < p.g ? load16<DT>(p.q + ((size_t)b * p.Hq + (size_t)kvh * p.g + h) * kD + tid) : 0.f;
+  // the tensor cores take the query as fp16: a value it cannot hold is reported
+  // (it would turn the scores of the query group into inf or NaN)
+  if (s == 0) {
+#pragma unroll
+    for (int h = 0; h < 4; ++h)
+      if (!(fabsf(qv[h]) <= 65504.0f))
+        set_status(p.d_status, fabsf(qv[h]) < INFINITY ? KITTY_ST_RANGE : KITTY_ST_NONFINITE);
+  }
   const bool lens_ok =
       !(np < 0 || np > p.max_pages || tl < 0 || tl > kPage || (tl > 0 && p.tail_k == nullptr));
   if (!lens_ok) {  // nothing is appended either
@@ -738,7 +747,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       done = done || (mbar_test_s(bar0 + 8 * (i % kDStages), (uint32_t)(i / kDStages) & 1u) &&
                       (!hasB || mbar_test_s(bar0 + 8 * ((i + 1) % kDStages),
                                             (uint32_t)((i + 1) / kDStages) & 1u)));
-      if (__all_sync(0xFFFFFFFFu, done) || it >= kWaitLimit) break;
+      if (__all_sync(0xFFFFFFFFu, done) || it >= p.wait_polls) break;
       if (it > 64) __nanosleep(32);
     }
     if (!__all_sync(0xFFFFFFFFu, done)) {
@@ -1208,6 +1217,7 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
   p.ws = static_cast<float*>(workspace);
   p.d_status = d_status;
   p.sm_log2 = sm_scale * 1.4426950408889634f;
+  p.wait_polls = cfg->decode_wait_polls > 0 ? (uint32_t)cfg->decode_wait_polls : kWaitLimit;
   p.pool_pages = pool_pages;
   p.max_pages = max_pages;
   p.out_dtype = out_dtype;

@@ -15,7 +15,7 @@ struct kitty_alloc {
   std::vector<uint8_t> in_use;
 };
 
-extern "C" int kitty_abi_version(void) { return 3; }
+extern "C" int kitty_abi_version(void) { return 4; }
 
 extern "C" int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page) {
   const int rc = check_cfg(cfg, false);

@@ -25,7 +25,8 @@ inline int check_cfg(const kitty_cfg* c, bool decode) {
       c->rank_mode != KITTY_RANK_SEQUENCE)
     return KITTY_ERR_INVALID_ARG;
   if (c->in_dtype != KITTY_F16 && c->in_dtype != KITTY_BF16) return KITTY_ERR_INVALID_ARG;
-  if (c->decode_pages_per_split < 0 || c->decode_total_pages < 0 || c->decode_max_pages < 0)
+  if (c->decode_pages_per_split < 0 || c->decode_total_pages < 0 || c->decode_max_pages < 0 ||
+      c->decode_wait_polls < 0)
     return KITTY_ERR_INVALID_ARG;
   if (decode && c->num_q_heads / c->num_kv_heads > 4) return KITTY_ERR_UNSUPPORTED;
   return KITTY_OK;

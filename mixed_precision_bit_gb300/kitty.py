@@ -33,7 +33,7 @@ class _Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "head_dim", "num_kv_heads", "num_q_heads", "page_tokens", "n_hi", "hi_bit", "lo_bit",
         "v_group", "rank_mode", "in_dtype", "decode_pages_per_split", "decode_total_pages",
-        "decode_max_pages")]
+        "decode_max_pages", "decode_wait_polls")]
 
 
 @dataclasses.dataclass
@@ -46,6 +46,7 @@ class Config:
     decode_pages_per_split: int = 0
     decode_total_pages: int = 0     # planning hint: the batch's total page count (0: unknown)
     decode_max_pages: int = 0       # planning hint: the longest sequence's page count (0: unknown)
+    decode_wait_polls: int = 0      # bound of the decode page waits in polls (0: the library's)
     head_dim: int = 128
     page_tokens: int = 32
     hi_bit: int = 4
@@ -56,7 +57,7 @@ class Config:
         return _Cfg(self.head_dim, self.num_kv_heads, self.num_q_heads, self.page_tokens,
                     self.n_hi, self.hi_bit, self.lo_bit, self.v_group, self.rank_mode,
                     self.in_dtype, self.decode_pages_per_split, self.decode_total_pages,
-                    self.decode_max_pages)
+                    self.decode_max_pages, self.decode_wait_polls)
 
 
 _lib = None

@@ -90,7 +90,8 @@ def _signed_zeros(inp):
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.F16], ids=["bf16", "f16"])
 def test_quantize_signed_zeros_bit_exact(dtype, mode, lo_bit):
     """A minimum or maximum that is a signed zero is stored with the sign the
-    oracle's in-order min/max picks (the first of equal values)."""
+    IEEE 754-2019 minimum and maximum give, whatever the token order: of +0 and
+    -0 the minimum is -0 and the maximum +0."""
     w = _variant("small_gqa", dtype=dtype, lo_bit=lo_bit)
     inp = _signed_zeros(synth.host_inputs(w, seed=1))
     pool, run = gpu_quantize(w, inp, mode=mode)

@@ -174,16 +174,107 @@ def test_hf0_equals_uniform_2bit(orc):
         assert (kh == want).all()
 
 
+def _np_uniform_4bit(x):
+    """Textbook per-channel 4-bit asymmetric min/max quantizer that stores its own
+    step: fp16 minimum, step u4 = fp16((max - min) / 15), codes
+    clamp(rint((x - M) / u4), 0, 15).  Returns (dequantized, u4 as fp32)."""
+    x = x.astype(np.float32)
+    mn, mx = x.min(0), x.max(0)
+    M = mn.astype(np.float16).astype(np.float32)
+    s4 = ((mx - mn).astype(np.float32) / np.float32(15)).astype(np.float32)
+    u4 = s4.astype(np.float16).astype(np.float32)
+    with np.errstate(divide="ignore", invalid="ignore"):
+        code = np.clip(np.rint(((x - M).astype(np.float32) / u4).astype(np.float32)), 0, 15)
+    code = np.where(u4 == 0, 0, code)
+    return M.astype(np.float64) + u4.astype(np.float64) * code, s4
+
+
 def test_hf1_equals_uniform_4bit(orc):
-    """hi_fraction = 1 is uniform 4-bit per-channel quantization: the base-plane
-    step 4*s4 stored in fp16, decoded as S/4, equals fp16(s4) when 4*s4 is a
-    normal half (power-of-two scaling commutes with rounding)."""
-    for seed in range(10):
+    """hi_fraction = 1 is uniform 4-bit per-channel quantization.  Kitty stores a
+    boosted channel's high-plane step fp16(4*s4) and decodes the 4-bit code with
+    a quarter of it; an independent 4-bit quantizer stores fp16(s4).  The two
+    steps agree whenever s4 is a normal half (s4 >= 2^-14: scaling by a power of
+    two commutes with rounding there), so the decoded pages are identical on
+    those channels.  Channels whose s4 is an fp16 subnormal are excluded from
+    the identity (fp16(s4) keeps fewer bits than fp16(4*s4)) and held to the
+    quantizer's error bound instead; the last seeds plant such channels."""
+    tiny_seen = 0
+    for seed in range(12):
         xk, xv = _kv(seed)
-        blob, _ = orc.quantize_page_f32(xk, xv, 128)
-        kh, _, _ = orc.dequant_page(blob, 128)
-        want, _ = _np_uniform_quant(xk, 15)
-        assert (kh == want).all()
+        if seed >= 10:   # channels whose range is a few fp16 subnormal steps
+            r = _rng(100 + seed)
+            cols = r.choice(128, 16, replace=False)
+            xk[:, cols] = _bf16(r.standard_normal((32, 16)) * 2.0 ** -14)
+        blob, st = orc.quantize_page_f32(xk, xv, 128)
+        kh, _, st2 = orc.dequant_page(blob, 128)
+        assert st == 0 and st2 == 0
+        want, s4 = _np_uniform_4bit(xk)
+        normal = s4 >= np.float32(2.0 ** -14)
+        assert (kh[:, normal] == want[:, normal]).all(), seed
+        tiny = ~normal
+        tiny_seen += int(tiny.sum())
+        if tiny.any():
+            x = xk[:, tiny].astype(np.float64)
+            rng_ = x.max(0) - x.min(0)
+            # within half a step (and an fp16 subnormal ulp of the stored step, times 15)
+            bound = rng_ / 15 / 2 + 15 * 2.0 ** -24 + 2.0 ** -25
+            assert (np.abs(kh[:, tiny] - x) <= bound[None, :] + 1e-12).all(), seed
+    assert tiny_seen >= 16
+
+
+def test_exact_rounding_ties_round_half_even(orc):
+    """Values exactly halfway between two quantization levels, at steps 3*2^-m
+    that are not powers of two, take the even level (round half to even,
+    numpy's rint), for 3 levels (2-bit channels and Value groups), 15 (4-bit
+    boosted channels of the (4, 2) configuration and 4-bit channels of (8, 4))
+    and 255 (8-bit boosted channels of (8, 4)).  The planted columns have exact
+    minima and steps, so the decoded value is minimum + step * rint(quotient)."""
+    from tests.edge_inputs import half_way_column
+    r = _rng(21)
+    for lo_bit, n_hi, lv in ((2, 0, (3, 15)), (2, 128, (3, 15)), (4, 0, (15, 255)),
+                             (4, 128, (15, 255))):
+        levels = lv[1] if n_hi else lv[0]
+        xk = np.zeros((32, 128))
+        want_k = np.zeros((32, 128))
+        for c in range(128):
+            m, a = int(r.integers(2, 6)), int(r.integers(0, 3))
+            col = half_way_column(levels, m, a)[r.permutation(32)]
+            u = 3.0 * 2.0 ** -m
+            mn = col.min()
+            xk[:, c] = col
+            want_k[:, c] = mn + u * np.rint((col - mn) / u)
+        xv = np.zeros((32, 128))
+        want_v = np.zeros((32, 128))
+        for t in range(32):
+            for G in range(4):
+                m, a = int(r.integers(2, 6)), int(r.integers(0, 3))
+                col = half_way_column(3, m, a)[r.permutation(32)]
+                u = 3.0 * 2.0 ** -m
+                xv[t, 32 * G:32 * G + 32] = col
+                want_v[t, 32 * G:32 * G + 32] = col.min() + u * np.rint((col - col.min()) / u)
+        assert (_bf16(xk) == xk).all() and (_bf16(xv) == xv).all()
+        blob, st = orc.quantize_page_f32(xk, xv, n_hi, lo_bit=lo_bit)
+        kh, vh, st2 = orc.dequant_page(blob, n_hi, lo_bit=lo_bit)
+        assert st == 0 and st2 == 0
+        assert (kh == want_k).all(), (lo_bit, n_hi)
+        assert (vh == want_v).all(), (lo_bit, n_hi)
+
+
+def test_equal_variances_at_the_cut_go_to_lower_channels(orc):
+    """Channels with equal variance straddling the n_hi cut (columns x or -x of
+    one shared column): the boosted set is every larger-variance channel plus
+    the lowest-indexed tied channels (brute force over the planted roles)."""
+    from tests.edge_inputs import tie_columns, tie_tile
+    r = _rng(22)
+    for n_distinct, n_tied, n_hi in ((0, 40, 32), (20, 30, 32), (5, 20, 16), (10, 60, 64)):
+        for lo_bit in (2, 4):
+            d, t, sg = tie_columns(r, n_distinct, n_tied)
+            xk = synth.from_bits(tie_tile(r, d, t, sg, synth.BF16), synth.BF16)
+            xv = _bf16(r.standard_normal((32, 128)))
+            blob, st = orc.quantize_page_f32(xk, xv, n_hi, lo_bit=lo_bit)
+            assert st == 0
+            want = np.sort(np.concatenate([d, t[:n_hi - n_distinct]]))
+            assert (orc.page_channels(blob, n_hi, lo_bit=lo_bit) == want).all()
 
 
 def _planes(blob, n_hi):

@@ -51,6 +51,7 @@ def lib():
             "orc_page_bytes": (ctypes.c_long, [i, i]),
             "orc_avg_bits": (d, [d, i, i]),
             "orc_f32_to_f16": (ctypes.c_uint16, [f]),
+            "orc_step_f16": (ctypes.c_uint16, [f]),
             "orc_f16_to_f32": (f, [ctypes.c_uint16]),
             "orc_bf16_to_f32": (f, [ctypes.c_uint16]),
             "orc_tree_sum": (f, [P]),
@@ -101,6 +102,11 @@ def avg_bits(hf: float, hi_bit: int, lo_bit: int) -> float:
 
 def f32_to_f16_bits(x: float) -> int:
     return int(lib().orc_f32_to_f16(float(x)))
+
+
+def step_f16(s: float) -> int:
+    """fp16 bits of the stored quantization step for the exact step s >= 0."""
+    return int(lib().orc_step_f16(float(s)))
 
 
 def f16_bits_to_f32(h: int) -> float:

@@ -312,12 +312,31 @@ void top_k(const float* var, int n_hi, bool* boosted) {
   }
 }
 
+// Stored step of a group: the smallest fp16 value that is >= s and whose
+// significand has at most 7 bits (s >= 0).  First s is rounded up to 7
+// significant bits (s = m * 2^e with m in [1/2, 1): ceil(m * 2^7) / 2^7 * 2^e),
+// then up to the fp16 grid, which changes it only below the fp16 normal range.
+// Reading: the pages fix neither the precision of the metadata nor its
+// rounding.  Seven bits let a 4-bit half of a query or probability multiply the
+// step exactly in fp16 (4 + 7 = 11 significant bits); rounding up keeps the
+// step >= (max - min) / levels, so no value lies above the top level.
+uint16_t step_f16(float s) {
+  if (s == 0.0f) return 0;
+  int e = 0;
+  const double m = std::frexp((double)s, &e);
+  const float v = (float)std::ldexp(std::ceil(std::ldexp(m, 7)), e - 7);
+  uint16_t h = f32_to_f16(v);
+  if (f16_to_f32(h) < v) ++h;  // positive fp16: the next pattern is the next value up
+  return h;
+}
+
 // Asymmetric min/max quantization of one group (VeloxQuant-MLX docs, Prefill
-// phase step 3).  Readings: the minimum and the step are stored as fp16 and the
-// codes are computed against the STORED values, so encoder and decoder agree;
-// rounding is to nearest-even; codes are clamped to [0, 2^b - 1].  A boosted
-// Key channel (2w-bit code) stores the step of its high w-bit plane, F = 2^w
-// times its own step (F = 4 for the (4, 2) configuration, 16 for (8, 4)).
+// phase step 3).  Readings: the minimum is stored as fp16 (nearest), the step
+// as step_f16 above, and the codes are computed against the STORED values, so
+// encoder and decoder agree; rounding is to nearest-even; codes are clamped to
+// [0, 2^b - 1].  A boosted Key channel (2w-bit code) stores the step of its
+// high w-bit plane, F = 2^w times its own step (F = 4 for the (4, 2)
+// configuration, 16 for (8, 4)).
 void quant_group(const float* x, int stride, int n, float mn, float mx, int levels,
                  bool boosted, uint16_t* S_out, uint16_t* M_out, uint16_t* code, float F = 4.0f) {
   const uint16_t M = f32_to_f16(mn);
@@ -327,10 +346,10 @@ void quant_group(const float* x, int stride, int n, float mn, float mx, int leve
   uint16_t S;
   float u;
   if (boosted) {
-    S = f32_to_f16(F * s);
+    S = step_f16(F * s);
     u = f16_to_f32(S) * (1.0f / F);
   } else {
-    S = f32_to_f16(s);
+    S = step_f16(s);
     u = f16_to_f32(S);
   }
   for (int i = 0; i < n; ++i) {
@@ -591,6 +610,7 @@ double orc_avg_bits(double hi_fraction, int hi_bit, int lo_bit) {
 }
 
 uint16_t orc_f32_to_f16(float f) { return f32_to_f16(f); }
+uint16_t orc_step_f16(float s) { return step_f16(s); }
 float orc_f16_to_f32(uint16_t h) { return f16_to_f32(h); }
 float orc_bf16_to_f32(uint16_t b) { return bf16_to_f32(b); }
 float orc_tree_sum(const float* x) { return tree_sum(x); }

@@ -139,17 +139,52 @@ def test_planted_outlier_channels_are_boosted(orc):
 
 
 # ----------------------------------------------------------------- quantizer
+def np_step(s):
+    """Stored step for exact steps s >= 0 (float32 array): s rounded up to 7
+    significant bits (numpy frexp / ceil / ldexp in float64), then up to the
+    next fp16 value if it falls between two (only below the fp16 normal
+    range).  Returned as float32 values."""
+    s = np.asarray(s, np.float32).astype(np.float64)
+    m, e = np.frexp(s)
+    v = np.ldexp(np.ceil(np.ldexp(m, 7)), e - 7)
+    h = v.astype(np.float16)
+    h = np.where(h.astype(np.float64) < v, np.nextafter(h, np.float16(np.inf)), h)
+    return h.astype(np.float32)
+
+
+def test_step_rule(orc):
+    """The stored step: the smallest fp16 value >= s with at most 7 significant
+    bits.  Checked against numpy on random steps over the fp16 range, powers of
+    two, values just above and below 7-bit boundaries, and fp16 subnormals."""
+    r = _rng(3)
+    s = (r.random(3000) * 10.0 ** r.integers(-9, 5, 3000)).astype(np.float32)
+    edge = np.float32(1.0 + 2.0 ** -6)
+    s = np.concatenate([s, np.float32(2.0) ** np.arange(-24, 15, dtype=np.float32),
+                        [edge, np.nextafter(edge, np.float32(0)), np.nextafter(edge, np.float32(9)),
+                         np.float32(3 * 2.0 ** -20), np.float32(1e-7), np.float32(0.0)]]).astype(np.float32)
+    want = np_step(s)
+    for x, w in zip(s, want):
+        got = orc.f16_bits_to_f32(orc.step_f16(float(x)))
+        assert got == w, (float(x), got, float(w))
+        assert got >= x
+        if x >= 2.0 ** -14:   # normal fp16: at most 7 significant bits, within 2^-6 above s
+            assert (int(np.float16(got).view(np.uint16)) & 0xF) == 0
+            assert got <= x * (1 + 2.0 ** -6)
+
+
 def _np_uniform_quant(x, levels):
     """Per-channel asymmetric min/max quantizer over tokens (KIVI-style, fp16
-    minimum and step, nearest-even codes, clamp): the textbook special case."""
+    minimum, step np_step(s) (a boosted 4-bit channel stores np_step(4 s) and
+    uses a quarter of it), nearest-even codes, clamp): the textbook special
+    case."""
     x = x.astype(np.float32)
     mn, mx = x.min(0), x.max(0)
     M = mn.astype(np.float16).astype(np.float32)
     s = ((mx - mn).astype(np.float32) / np.float32(levels)).astype(np.float32)
     if levels == 15:
-        u = (s * np.float32(4)).astype(np.float16).astype(np.float32) * np.float32(0.25)
+        u = np_step(s * np.float32(4)) * np.float32(0.25)
     else:
-        u = s.astype(np.float16).astype(np.float32)
+        u = np_step(s)
     with np.errstate(divide="ignore", invalid="ignore"):
         code = np.clip(np.rint(((x - M).astype(np.float32) / u).astype(np.float32)), 0, levels)
     code = np.where(u == 0, 0, code)
@@ -176,13 +211,13 @@ def test_hf0_equals_uniform_2bit(orc):
 
 def _np_uniform_4bit(x):
     """Textbook per-channel 4-bit asymmetric min/max quantizer that stores its own
-    step: fp16 minimum, step u4 = fp16((max - min) / 15), codes
-    clamp(rint((x - M) / u4), 0, 15).  Returns (dequantized, u4 as fp32)."""
+    step: fp16 minimum, step u4 = np_step((max - min) / 15), codes
+    clamp(rint((x - M) / u4), 0, 15).  Returns (dequantized, the exact step s4)."""
     x = x.astype(np.float32)
     mn, mx = x.min(0), x.max(0)
     M = mn.astype(np.float16).astype(np.float32)
     s4 = ((mx - mn).astype(np.float32) / np.float32(15)).astype(np.float32)
-    u4 = s4.astype(np.float16).astype(np.float32)
+    u4 = np_step(s4)
     with np.errstate(divide="ignore", invalid="ignore"):
         code = np.clip(np.rint(((x - M).astype(np.float32) / u4).astype(np.float32)), 0, 15)
     code = np.where(u4 == 0, 0, code)
@@ -191,13 +226,14 @@ def _np_uniform_4bit(x):
 
 def test_hf1_equals_uniform_4bit(orc):
     """hi_fraction = 1 is uniform 4-bit per-channel quantization.  Kitty stores a
-    boosted channel's high-plane step fp16(4*s4) and decodes the 4-bit code with
-    a quarter of it; an independent 4-bit quantizer stores fp16(s4).  The two
-    steps agree whenever s4 is a normal half (s4 >= 2^-14: scaling by a power of
-    two commutes with rounding there), so the decoded pages are identical on
-    those channels.  Channels whose s4 is an fp16 subnormal are excluded from
-    the identity (fp16(s4) keeps fewer bits than fp16(4*s4)) and held to the
-    quantizer's error bound instead; the last seeds plant such channels."""
+    boosted channel's high-plane step as the step of 4*s4 and decodes the 4-bit
+    code with a quarter of it; an independent 4-bit quantizer stores the step of
+    s4.  The two agree whenever s4 is a normal half (s4 >= 2^-14: scaling by a
+    power of two commutes with both roundings there), so the decoded pages are
+    identical on those channels.  Channels whose s4 lies below the fp16 normal
+    range are excluded from the identity (there the fp16 grid is coarser
+    relative to s4 than to 4*s4) and held to the quantizer's error bound
+    instead; the last seeds plant such channels."""
     tiny_seen = 0
     for seed in range(12):
         xk, xv = _kv(seed)
@@ -216,8 +252,10 @@ def test_hf1_equals_uniform_4bit(orc):
         if tiny.any():
             x = xk[:, tiny].astype(np.float64)
             rng_ = x.max(0) - x.min(0)
-            # within half a step (and an fp16 subnormal ulp of the stored step, times 15)
-            bound = rng_ / 15 / 2 + 15 * 2.0 ** -24 + 2.0 ** -25
+            # within half a step: Kitty's step is S/4 with S at most 2^-6 above
+            # 4*s4 and then at most 2^-24 (one fp16 subnormal ulp) above that;
+            # plus the fp16 rounding of the minimum (half an ulp, 2^-25)
+            bound = (rng_ / 15 * (1 + 2.0 ** -6) + 2.0 ** -26) / 2 + 2.0 ** -25
             assert (np.abs(kh[:, tiny] - x) <= bound[None, :] + 1e-12).all(), seed
     assert tiny_seen >= 16
 
@@ -431,8 +469,8 @@ def test_reconstruction_error_bound(orc):
                 M = float(np.float32(mn).astype(np.float16))
                 boosted = x is xk and sel[1] in kch
                 L = 15 if boosted else 3
-                s = float(np.float32(np.float32(mx - mn) / np.float32(L)))
-                u = float(np.float16(4 * s)) / 4 if boosted else float(np.float16(s))
+                s = np.float32(np.float32(mx - mn) / np.float32(L))
+                u = float(np_step(4 * s)) / 4 if boosted else float(np_step(s))
                 bound = max(u / 2 * (1 + 1e-6), M - mn, mx - (M + L * u)) + 1e-6 * abs(a).max()
                 assert np.abs(ah - a).max() <= bound + 1e-12
 
@@ -450,7 +488,11 @@ def test_boost_lowers_error(orc):
         uni, _ = _np_uniform_quant(xk, 3)
         e_k = (kh - xk) ** 2
         e_u = (uni - xk) ** 2
-        assert (np.abs(kh - xk) <= np.abs(uni - xk) + 2e-3 * np.abs(xk).max()).all()
+        # grid inclusion (j = 5k) up to the rounding of the two stored steps: each
+        # is at most 2^-6 above its exact step, so grid point k moves by at most
+        # 3 * 2^-6 * (max - min) / 3
+        rng_ = xk.astype(np.float64).max(0) - xk.astype(np.float64).min(0)
+        assert (np.abs(kh - xk) <= np.abs(uni - xk) + 2.0 ** -6 * rng_ + 1e-6).all()
         tot_k += e_k.sum()
         tot_u += e_u.sum()
         kch = orc.page_channels(blob, 32)

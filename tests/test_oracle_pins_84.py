@@ -12,6 +12,7 @@ errors of the two configurations.
 import numpy as np
 
 from mixed_precision_bit_gb300 import synth
+from tests.test_oracle_pins import np_step
 
 
 def _rng(seed):
@@ -30,13 +31,13 @@ def _kv(seed):
 
 def _np_quant(x, levels, factor=1):
     """Per-channel asymmetric min/max quantizer over 32 tokens: fp16 minimum,
-    step stored as fp16(factor * s) and used as that / factor, nearest-even
+    step stored as np_step(factor * s) and used as that / factor, nearest-even
     codes, clamp to [0, levels]."""
     x = x.astype(np.float32)
     mn, mx = x.min(0), x.max(0)
     M = mn.astype(np.float16).astype(np.float32)
     s = ((mx - mn).astype(np.float32) / np.float32(levels)).astype(np.float32)
-    u = (s * np.float32(factor)).astype(np.float16).astype(np.float32) / np.float32(factor)
+    u = np_step(s * np.float32(factor)) / np.float32(factor)
     with np.errstate(divide="ignore", invalid="ignore"):
         code = np.clip(np.rint(((x - M).astype(np.float32) / u).astype(np.float32)), 0, levels)
     code = np.where(u == 0, 0, code)
@@ -148,7 +149,9 @@ def test_wider_planes_never_lose(orc):
         k84, v84, _ = orc.dequant_page(b84, 32, lo_bit=4)
         x = xk.astype(np.float64)
         e42, e84 = np.abs(k42 - x), np.abs(k84 - x)
-        slack = 2e-3 * (x.max(0) - x.min(0))      # fp16 rounding of the steps
+        # rounding of the stored steps: each is at most 2^-6 above its exact
+        # step, which moves the coarser grid's top point by at most 2^-6 * range
+        slack = 2.0 ** -6 * (x.max(0) - x.min(0)) + 1e-6
         assert (e84 <= e42 + slack).all()
         assert (v42 == v84).all()
         tot42 += float((e42 ** 2).sum())

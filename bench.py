@@ -83,15 +83,21 @@ def headroom_pages(tails, steps_total):
 
 # ------------------------------------------------------------------ clocks
 class ClockSampler:
-    """nvidia-smi sampling of SM clock and throttle reasons during the timed region."""
+    """nvidia-smi sampling of SM clock and throttle reasons during the timed region.
 
-    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    start() waits for the first sample before the region opens and stamps the
+    region's start; stop() stamps its end and keeps the samples taken inside
+    it.  A region shorter than the 50 ms period keeps the first sample taken
+    after it began ("window" says which)."""
+
+    Q = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
          "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
          "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
     def __init__(self, gpu_index: int):
         self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
         self.p = None
+        self.t0 = self.t1 = None
         try:
             self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), "--query-gpu=" + self.Q,
                                        "--format=csv,noheader,nounits", "-lms", "50"],
@@ -99,33 +105,57 @@ class ClockSampler:
         except OSError:
             self.p = None
 
+    def start(self):
+        """Waits (at most 5 s) for the first sample, then stamps the region start."""
+        if self.p is not None:
+            t = time.time()
+            while time.time() - t < 5.0 and os.path.getsize(self.f.name) == 0:
+                time.sleep(0.01)
+        self.t0 = time.time()
+
+    def _rows(self):
+        import datetime
+        out = []
+        self.f.flush()
+        self.f.seek(0)
+        for line in self.f.read().splitlines():
+            r = [x.strip() for x in line.split(", ")]
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                out.append((ts, float(r[2]), float(r[3]), r[6:10]))
+            except (ValueError, IndexError):
+                continue
+        return out
+
     def stop(self):
+        self.t1 = time.time()
         if self.p is None:
             return None
+        time.sleep(0.06)   # one more period: the sample that covers the region's end
         self.p.terminate()
         try:
             self.p.wait(timeout=5)
         except subprocess.TimeoutExpired:
             self.p.kill()
-        self.f.flush()
-        self.f.seek(0)
-        rows = [l.strip().split(", ") for l in self.f.read().splitlines() if l.strip()]
+        rows = self._rows()
         os.unlink(self.f.name)
-        sm, mx, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
-            try:
-                sm.append(float(r[1]))
-                mx.append(float(r[2]))
-            except (ValueError, IndexError):
-                continue
-            for n, v in zip(names, r[5:9]):
-                if v.strip().lower() == "active":
-                    reasons.add(n)
-        if not sm:
+        t0 = self.t0 if self.t0 is not None else -1.0
+        inside = [r for r in rows if t0 <= r[0] <= self.t1]
+        window = "samples inside the timed region"
+        if not inside:
+            inside = [r for r in rows if r[0] >= t0][:1]
+            window = "first sample after the timed region began (region shorter than the period)"
+        if not inside:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "samples": len(sm),
-                "reasons": sorted(reasons)}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = set()
+        for r in inside:
+            for n, v in zip(names, r[3]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median([r[1] for r in inside]),
+                "sm_max_mhz": max(r[2] for r in inside), "samples": len(inside),
+                "reasons": sorted(reasons), "window": window}
 
 
 # ------------------------------------------------------------------ kitty arm
@@ -321,6 +351,8 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
         torch.distributed.barrier()
     torch.cuda.synchronize()
     clocks = ClockSampler(local_rank) if rank == 0 else None
+    if clocks:
+        clocks.start()
     t0.record(stream)
     for s in range(K):
         step(W + s, ev[W + s])
@@ -348,7 +380,7 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
                 clocks=clk, splits=splits, chunk=chunk)
 
 
-def target_measure(name, args, world, rank, local_rank, K=20, W=3):
+def target_measure(name, args, world, rank, local_rank, K=200, W=3):
     """The decode call of one single-layer workload (Qwen3-8B-shaped layer,
     long-context layer), timed in the same run as the headline: its call time,
     algorithmic bytes and GB/s against 8 TB/s and the measured copy peak, with

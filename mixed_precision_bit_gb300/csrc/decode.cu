@@ -18,13 +18,16 @@
 // planes), then computes, for its g <= 4 query heads:
 //   scores  S^T[t][n] = sum_c code[t][c] * B[c][n] on the tensor cores
 //           (mma.m16n8k16, fp32 accumulate) with B = q*S, the per-channel Key
-//           step folded into the query as an fp16 hi/lo pair (column 2h = hi,
-//           2h+1 = lo of head h), plus the extra plane of the boosted channels
-//           (B = q*S/2^W gathered through the channel list, W = Key plane
-//           width) and the q.M term as a one-row MMA;
+//           step folded into the query: the query is split into a high part
+//           (4 significant bits, column 2h of head h) and the rest (column
+//           2h+1), and a stored step has at most 7 significant bits, so each
+//           column is one exact fp16 multiply; plus the extra plane of the
+//           boosted channels (B = q*S/2^W gathered through the channel list,
+//           W = Key plane width) and the q.M term as a one-row MMA;
 //   softmax fp32 online (max, rescale, exp2) in registers;
 //   PV      O^T[c][n] = sum_t vcode[c][t] * P'[t][n] with P' = p*S_v per
-//           Value group as an fp16 hi/lo pair, plus the sum_t p*M_v term.
+//           Value group, p split the same way (high part exact times S_v, the
+//           rest rounded once), plus the sum_t p*M_v term.
 // Codes are unpacked with one AND per two: the planes are stored in fragment
 // order, so a masked 16-bit half is the fp16 subnormal code * 2^(2*tau - 24)
 // (2-bit planes) or code * 2^(4*(tau & 1) - 24) (4-bit Key planes); the power of
@@ -53,6 +56,11 @@ constexpr int kDThreads = kDWarps * 32;
 static_assert(sizeof(QuantSmem) <= (size_t)kDWarps * stages_for(2) * 3072 &&
                   sizeof(QuantSmem) <= (size_t)kDWarps * stages_for(4) * 4096,
               "page quantizer state does not fit in the decode stage buffers");
+// Row stride (halves) of the extra-plane query tables: 130 rather than 128, so
+// that the eight tables (4 heads x high/low part) put one channel's entries in
+// eight different shared-memory banks, and the lanes of a warp gathering the
+// same channel for different heads and parts do not conflict.
+constexpr int kQx = kD + 2;
 constexpr uint32_t kWaitLimit = 1u << 22;  // polls of one barrier phase (~0.1-1 s)
 constexpr int kPartial = kD + 4;           // split partial: m, l, 2 unused, o[128] (16-byte aligned)
 constexpr int kMaxSplits = 256;            // splits per sequence, at most
@@ -149,17 +157,14 @@ __device__ __forceinline__ uint16_t ld_s16r(uint32_t a) {
   return v;
 }
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(bits_h2(a), bits_h2(b))); }
-__device__ __forceinline__ uint32_t hfma2u(uint32_t a, uint32_t b, uint32_t c) {
-  return h2_bits(__hfma2(bits_h2(a), bits_h2(b), bits_h2(c)));
+// The high part of an fp16 value: sign, exponent and the top 3 mantissa bits
+// (4 significant bits).  Times a step of at most 7 significant bits it is exact
+// in fp16, and the rest (value - high part, exact) has at most 7 significant
+// bits left.
+__device__ __forceinline__ __half high_part(__half x) {
+  return __ushort_as_half((uint16_t)(__half_as_ushort(x) & 0xFF80u));
 }
 
-// fp16 hi/lo split of q*S across the two columns of a head.  fneg is 0 on hi
-// lanes and -1 on lo lanes: hi lanes get fp16(q*S), lo lanes get the exact
-// residual fp16(q*S - fp16(q*S)).  Three FMA-pipe operations, no lane select.
-__device__ __forceinline__ uint32_t hilo_mul(uint32_t q, uint32_t S, uint32_t fneg) {
-  const uint32_t h = hmul2u(q, hmul2u(S, fneg));
-  return hfma2u(q, S, h);
-}
 
 // Four consecutive channels i..i+3 (i % 4 == 0): one vector store when the
 // output array is 16-byte aligned, else four scalar stores.
@@ -206,19 +211,14 @@ struct Off {
 };
 
 // Lane roles.  Thread (r = lane/4, qq = lane%4) owns head qq in the C
-// fragments (column 2qq = hi, 2qq+1 = lo) and, as a B-fragment lane, column
-// n = lane/4 = (head lane/8, part (lane/4)&1).
+// fragments (column 2qq = high part, 2qq+1 = low part) and, as a B-fragment
+// lane, column n = lane/4 = (head lane/8, part (lane/4)&1).
 struct Lane {
   int lane, r, qq;
-  uint32_t fneg;  // fp16x2 0 (hi column) or -1 (lo column)
-  uint32_t fpos;  // fp16x2 0 (hi column) or +1 (lo column)
   __device__ Lane() {
     lane = threadIdx.x & 31;
     r = lane >> 2;
     qq = lane & 3;
-    const bool lo = (lane >> 2) & 1;
-    fneg = lo ? 0xBC00BC00u : 0u;
-    fpos = lo ? 0x3C003C00u : 0u;
   }
 };
 
@@ -263,8 +263,10 @@ __device__ __forceinline__ void unpack_rows23(uint32_t x, uint32_t* a) {  // tau
 // Scores of one staged (page, kv-head) blob, in log2 units: s[2*mt + rh] is
 // token 16*mt + 8*rh + r of head qq.
 //   pa: shared-space address of the staged blob
-//   qf[j][0..1]: this lane's B-fragment query pairs for k-step j (head lane/8)
-//   qxa: shared-space address of q/2^W of head lane/8 (extra-plane gather)
+//   qf[j][0..1]: this lane's B-fragment query pairs for k-step j: the high or
+//                the low part (column parity) of the query of head lane/8
+//   qxa: shared-space address of the same part of q/2^W of head lane/8, in
+//        channel order (extra-plane gather)
 template <int NX, int W>
 __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&qf)[8][2],
                                             const uint32_t qxa, const Lane& L,
@@ -298,8 +300,9 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
       KITTY_KS(0) KITTY_KS(1) KITTY_KS(2) KITTY_KS(3) KITTY_KS(4) KITTY_KS(5) KITTY_KS(6) default: KITTY_KS(7)
 #undef KITTY_KS
     }
-    const uint32_t b0 = hilo_mul(qf[j][0], S0, L.fneg);
-    const uint32_t b1 = hilo_mul(qf[j][1], S1, L.fneg);
+    // this lane's part of q (high or low) times the step: exact in fp16
+    const uint32_t b0 = hmul2u(qf[j][0], S0);
+    const uint32_t b1 = hmul2u(qf[j][1], S1);
     uint32_t a[4];
     if (W == 2) {
       unpack_rows01(kw[j], a);
@@ -333,8 +336,8 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
       const uint32_t q23 = ld_s16r(qxa + c2) | ((uint32_t)ld_s16r(qxa + c3) << 16);
       const uint32_t s01 = ld_s16r(pa + O::ks + c0) | ((uint32_t)ld_s16r(pa + O::ks + c1) << 16);
       const uint32_t s23 = ld_s16r(pa + O::ks + c2) | ((uint32_t)ld_s16r(pa + O::ks + c3) << 16);
-      const uint32_t b0 = hilo_mul(q01, s01, L.fneg);
-      const uint32_t b1 = hilo_mul(q23, s23, L.fneg);
+      const uint32_t b0 = hmul2u(q01, s01);
+      const uint32_t b1 = hmul2u(q23, s23);
       uint32_t a[4];
       if (W == 2) {
         unpack_rows01(x.x, a);
@@ -358,8 +361,9 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
 }
 
 // q.M bias (log2 units) of two pages with one set of one-row MMAs: B is the
-// plain query for every page, so A rows r even carry page A's Key minima and
-// odd rows page B's; each lane reads its own row and its neighbour's.
+// split query (the same for every page), whose two columns of a head add up to
+// q.M; A rows r even carry page A's Key minima and odd rows page B's; each lane
+// reads its own row and its neighbour's.
 template <int NX, int W>
 __device__ __forceinline__ void pair_beta(const uint32_t paA, const uint32_t paB,
                                           const uint32_t (&qf)[8][2], const Lane& L,
@@ -377,21 +381,22 @@ __device__ __forceinline__ void pair_beta(const uint32_t paA, const uint32_t paB
     const uint32_t am[4] = {M[2 * j], 0u, M[2 * j + 1], 0u};
     mma_f16(cm, am, qf[j][0], qf[j][1]);
   }
-  const float mine = cm[0] * sm_log2;
+  const float mine = (cm[0] + cm[1]) * sm_log2;
   const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 4);
   bA = (L.r & 1) ? other : mine;
   bB = (L.r & 1) ? mine : other;
 }
 
-// Probabilities of one page against the running max, split into fp16 (hi, lo)
-// and transposed into PV B fragments.
+// Probabilities of one page against the running max, split into a high part
+// with 4 significant bits (exact times a 7-bit Value step) and the rest, as
+// fp16, and transposed into PV B fragments (column 2h = high, 2h+1 = rest).
 __device__ __forceinline__ void page_probs(WarpState& w, const float (&s)[4], uint32_t (&T)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float p = ex2(s[i] - w.m);
     w.l += p;
-    const float t = __uint_as_float(__float_as_uint(p) & 0xFFFFE000u);  // 11 significant bits
-    T[i] = movmatrix_t(h2_bits(__floats2half2_rn(t, p - t)));          // (hi, lo) -> B columns
+    const float t = __uint_as_float(__float_as_uint(p) & 0xFFF00000u);  // 4 significant bits
+    T[i] = movmatrix_t(h2_bits(__floats2half2_rn(t, p - t)));          // (high, rest) -> B columns
   }
 }
 
@@ -412,14 +417,9 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
     mma_f16(w.vm, am1, T[2], T[3]);
   }
 
-  // ---------------- PV with the Value step folded into P per group (hi/lo)
-  uint32_t ph[4], pl[4], phf[4];
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    ph[i] = __shfl_sync(0xFFFFFFFFu, T[i], lane & ~4);  // p_hi of this column's head
-    pl[i] = hmul2u(T[i], L.fpos);                        // p_lo on lo lanes, 0 on hi lanes
-    phf[i] = hmul2u(ph[i], L.fneg);                      // -p_hi on lo lanes, 0 on hi lanes
-  }
+  // ---------------- PV with the Value step folded into this lane's part of P
+  // (high part: exact product; the rest: rounded once, relative 2^-12 of a
+  // term below 2^-3 of p)
 #pragma unroll
   for (int G = 0; G < 4; ++G) {
     uint2 vv;
@@ -437,9 +437,7 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
 #pragma unroll
       for (int k = 0; k < 2; ++k) {
         const int i = 2 * kt + k;
-        const uint32_t h = hmul2u(phf[i], S[i]);    // lo: fp16(-p_hi*S); hi: 0
-        const uint32_t rr = hfma2u(ph[i], S[i], h);  // hi: fp16(p_hi*S); lo: exact residual
-        bg[k] = hfma2u(pl[i], S[i], rr);            // lo: + p_lo*S
+        bg[k] = hmul2u(T[i], S[i]);
       }
       const uint32_t x = kt ? vv.y : vv.x;
       uint32_t a[4];
@@ -625,7 +623,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   uint8_t* stages = dsm;
   uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + kDWarps * kDStages * kBlob);
   __half* qs = reinterpret_cast<__half*>(bars + kDWarps * kDStages);  // q      [4][128]
-  __half* qs4 = qs + 4 * kD;                                          // q / 2^W [4][128]
+  __half* qs4 = qs + 4 * kD;  // q / 2^W split: high parts [4][kQx], then low parts [4][kQx]
 
   // ---- start this warp's page copies (its barriers are its own)
   const int npw = pend > first ? (pend - first + kDWarps - 1) / kDWarps : 0;
@@ -705,20 +703,29 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   for (int h = 0; h < 4; ++h) {
     const __half hv = __float2half_rn(qv[h]);
     qs[h * kD + tid] = hv;
-    qs4[h * kD + tid] = __hmul(hv, __float2half_rn(1.0f / (1 << W)));  // exact: power of two
+    const __half hx = __hmul(hv, __float2half_rn(1.0f / (1 << W)));  // exact: power of two
+    const __half hh = high_part(hx);
+    qs4[h * kQx + tid] = hh;
+    qs4[(4 + h) * kQx + tid] = __hsub(hx, hh);  // exact
   }
   __syncthreads();
 
+  // B-fragment query pairs: column 2h takes the high part of q, 2h+1 the rest
+  const bool low_col = (lane >> 2) & 1;
   uint32_t qf[8][2];
   {
     const __half* qh = qs + (lane >> 3) * kD;
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-      qf[j][0] = *reinterpret_cast<const uint32_t*>(qh + 16 * j + 2 * qq);
-      qf[j][1] = *reinterpret_cast<const uint32_t*>(qh + 16 * j + 2 * qq + 8);
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const __half2 q2 = *reinterpret_cast<const __half2*>(qh + 16 * j + 2 * qq + 8 * e);
+        const __half2 h2 = __halves2half2(high_part(__low2half(q2)), high_part(__high2half(q2)));
+        qf[j][e] = h2_bits(low_col ? __hsub2(q2, h2) : h2);
+      }
     }
   }
-  const uint32_t qxa = smem_u32(qs4 + (lane >> 3) * kD);
+  const uint32_t qxa = smem_u32(qs4 + ((low_col ? 4 : 0) + (lane >> 3)) * kQx);
   float kscale[4];
 #pragma unroll
   for (int tau = 0; tau < 4; ++tau)
@@ -773,10 +780,12 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       const bool vB = (valid_mask >> stB) & 1u;
       float sB[4];
       page_scores<NX, W>(paB, qf, qxa, L, kscale, bB, sB);
+      if (!(vA && vB)) {  // a page id was out of range (warp-uniform, rare)
 #pragma unroll
-      for (int k = 0; k < 4; ++k) {
-        sA[k] = vA ? sA[k] : -INFINITY;
-        sB[k] = vB ? sB[k] : -INFINITY;
+        for (int k = 0; k < 4; ++k) {
+          sA[k] = vA ? sA[k] : -INFINITY;
+          sB[k] = vB ? sB[k] : -INFINITY;
+        }
       }
       float pm = fmaxf(fmaxf(fmaxf(sA[0], sA[1]), fmaxf(sA[2], sA[3])),
                        fmaxf(fmaxf(sB[0], sB[1]), fmaxf(sB[2], sB[3])));
@@ -1045,7 +1054,7 @@ namespace {
 
 size_t decode_smem(int blob, int w) {
   const int st = stages_for(w);
-  return (size_t)kDWarps * st * blob + kDWarps * st * sizeof(uint64_t) + 2 * 4 * kD * 2;
+  return (size_t)kDWarps * st * blob + kDWarps * st * sizeof(uint64_t) + (4 * kD + 8 * kQx) * 2;
 }
 
 // CTAs of the decode kernel resident at once on the device: kDMinBlocks per SM

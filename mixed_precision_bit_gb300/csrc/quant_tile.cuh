@@ -63,9 +63,23 @@ __device__ __forceinline__ float rcp_approx(float x) {
   return y;
 }
 
-// Asymmetric min/max group quantizer: fp16 minimum and step, codes computed
-// against the stored values; a boosted Key channel (2w-bit code) stores
-// F = 2^w times its own step, the step of its high w-bit plane.
+// Stored step for the exact step s >= 0: the smallest fp16 value >= s whose
+// significand has at most 7 bits.  The fp32 pattern is rounded up to 6
+// explicit mantissa bits (for s >= 0 the pattern order is the value order, and
+// a carry moves on into the exponent), then the value is rounded up to the
+// fp16 grid, which only changes values below the fp16 normal range.  A 4-bit
+// half of a query or probability times such a step is exact in fp16.
+__device__ __forceinline__ uint16_t step_f16(float s) {
+  const float v = __uint_as_float((__float_as_uint(s) + 0x1FFFFu) & ~0x1FFFFu);
+  const __half h = __float2half_rn(v);
+  const uint16_t b = __half_as_ushort(h);
+  return __half2float(h) < v ? (uint16_t)(b + 1u) : b;  // next fp16 up (v > 0)
+}
+
+// Asymmetric min/max group quantizer: fp16 minimum (nearest) and step
+// (step_f16), codes computed against the stored values; a boosted Key channel
+// (2w-bit code) stores the step of F = 2^w times its own step, the step of its
+// high w-bit plane.
 __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, bool boosted,
                                                float F = 4.0f) {
   QuantParams q;
@@ -74,13 +88,11 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
   q.Mbits = __half_as_ushort(Mh);
   const float s = __fdiv_rn(__fsub_rn(mx, mn), (float)levels);
   if (boosted) {
-    const __half Sh = __float2half_rn(__fmul_rn(F, s));
-    q.Sbits = __half_as_ushort(Sh);
-    q.u = __fmul_rn(__half2float(Sh), 1.0f / F);
+    q.Sbits = step_f16(__fmul_rn(F, s));
+    q.u = __fmul_rn(__half2float(__ushort_as_half(q.Sbits)), 1.0f / F);
   } else {
-    const __half Sh = __float2half_rn(s);
-    q.Sbits = __half_as_ushort(Sh);
-    q.u = __half2float(Sh);
+    q.Sbits = step_f16(s);
+    q.u = __half2float(__ushort_as_half(q.Sbits));
   }
   // u == 0: ru = 0 makes every code of a finite input 0, and no quotient lands
   // near a tie, so the division below is never taken
@@ -88,16 +100,16 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
   return q;
 }
 
-// rint(fl(d / u)): the correctly rounded division, out of line (it is taken
-// only near a rounding tie, and inlining it at every code site bloats the code).
-__device__ __noinline__ float rint_div(float d, float u) { return rintf(__fdiv_rn(d, u)); }
-
-// Codes of four values: code = clamp(rint(fl((x - M) / u)), 0, L), bit-exact
-// with an IEEE division.  The quotient is taken as (x - M) * (1/u), within
+// Codes of four values: code = clamp(the integer nearest to d / u, ties to
+// even, 0, L) with d = fl(x - M).  The quotient is taken as d * (1/u), within
 // 2^-21 relative of the true value (so within 2^-17 for L <= 15 and 2^-13 for
 // L = 255 inside the clamp range); where one lands within 2^-15 (L <= 15) or
-// 2^-12 (L = 255) of a rounding tie, the correctly rounded division decides
-// it.  One branch covers the four (a tie is rare).
+// 2^-12 (L = 255) of a halfway point k0 + 1/2, the sign of d - (k0 + 1/2) u
+// decides it: (k0 + 1/2) u is exact in fp32 (at most 10 x 11 significant
+// bits), so one fused multiply-add gives that sign exactly, and a zero is an
+// exact tie.  (For fp32 d and u this equals rounding the correctly rounded
+// fp32 quotient: that quotient lands on a halfway point only when the exact one
+// does.)  One branch covers the four.
 __device__ __forceinline__ void qcode4(const float (&x)[4], const QuantParams& q, int levels,
                                        uint32_t (&code)[4]) {
   const float edge = 0.5f - (levels > 15 ? 0x1p-12f : 0x1p-15f);
@@ -116,8 +128,14 @@ __device__ __forceinline__ void qcode4(const float (&x)[4], const QuantParams& q
   for (int k = 0; k < 4; ++k) worst = fmaxf(worst, fabsf(e[k]));
   if (worst > edge) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k)
-      if (fabsf(e[k]) > edge) n[k] = rint_div(d[k], q.u);
+    for (int k = 0; k < 4; ++k) {
+      const float k0 = rintf(y[k] - 0.5f);               // the halfway point is k0 + 1/2
+      const float r = fmaf(-(k0 + 0.5f), q.u, d[k]);     // exact sign of d - (k0 + 1/2) u
+      const float up = k0 + 1.0f;
+      const float tie = (__float2int_rz(k0) & 1) ? up : k0;  // to even
+      const float m = r > 0.0f ? up : (r < 0.0f ? k0 : tie);
+      n[k] = fabsf(e[k]) > edge ? m : n[k];
+    }
   }
   // n is integral: a saturating conversion clamps below at 0, min() above at L
 #pragma unroll

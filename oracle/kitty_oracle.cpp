@@ -333,8 +333,12 @@ uint16_t step_f16(float s) {
 // Asymmetric min/max quantization of one group (VeloxQuant-MLX docs, Prefill
 // phase step 3).  Readings: the minimum is stored as fp16 (nearest), the step
 // as step_f16 above, and the codes are computed against the STORED values, so
-// encoder and decoder agree; rounding is to nearest-even; codes are clamped to
-// [0, 2^b - 1].  A boosted Key channel (2w-bit code) stores the step of its
+// encoder and decoder agree: d = x - M rounded to fp32, and the code is the
+// integer nearest to the exact quotient d / u, ties to even, clamped to
+// [0, 2^b - 1].  The quotient is formed in fp64: d has at most 24 significant
+// bits and u at most 11, so a quotient that is not exactly halfway lies at
+// least 2^-35 (relative) from the halfway point, far outside the fp64
+// rounding, and an exact halfway quotient is computed exactly.  A boosted Key channel (2w-bit code) stores the step of its
 // high w-bit plane, F = 2^w times its own step (F = 4 for the (4, 2)
 // configuration, 16 for (8, 4)).
 void quant_group(const float* x, int stride, int n, float mn, float mx, int levels,
@@ -355,8 +359,7 @@ void quant_group(const float* x, int stride, int n, float mn, float mx, int leve
   for (int i = 0; i < n; ++i) {
     if (u == 0.0f) { code[i] = 0; continue; }
     const float d = x[i * stride] - Mf;
-    const float y = d / u;
-    float q = std::nearbyint(y);
+    float q = (float)std::nearbyint((double)d / (double)u);
     if (q < 0.0f) q = 0.0f;
     if (q > (float)levels) q = (float)levels;
     code[i] = (uint16_t)q;

@@ -186,7 +186,8 @@ def _np_uniform_quant(x, levels):
     else:
         u = np_step(s)
     with np.errstate(divide="ignore", invalid="ignore"):
-        code = np.clip(np.rint(((x - M).astype(np.float32) / u).astype(np.float32)), 0, levels)
+        # nearest level to the quotient (d = x - M in fp32, the quotient in fp64)
+        code = np.clip(np.rint((x - M).astype(np.float32).astype(np.float64) / u), 0, levels)
     code = np.where(u == 0, 0, code)
     return M.astype(np.float64) + u.astype(np.float64) * code, code.astype(np.int64)
 
@@ -219,7 +220,7 @@ def _np_uniform_4bit(x):
     s4 = ((mx - mn).astype(np.float32) / np.float32(15)).astype(np.float32)
     u4 = np_step(s4)
     with np.errstate(divide="ignore", invalid="ignore"):
-        code = np.clip(np.rint(((x - M).astype(np.float32) / u4).astype(np.float32)), 0, 15)
+        code = np.clip(np.rint((x - M).astype(np.float32).astype(np.float64) / u4), 0, 15)
     code = np.where(u4 == 0, 0, code)
     return M.astype(np.float64) + u4.astype(np.float64) * code, s4
 

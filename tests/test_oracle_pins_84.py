@@ -39,7 +39,7 @@ def _np_quant(x, levels, factor=1):
     s = ((mx - mn).astype(np.float32) / np.float32(levels)).astype(np.float32)
     u = np_step(s * np.float32(factor)) / np.float32(factor)
     with np.errstate(divide="ignore", invalid="ignore"):
-        code = np.clip(np.rint(((x - M).astype(np.float32) / u).astype(np.float32)), 0, levels)
+        code = np.clip(np.rint((x - M).astype(np.float32).astype(np.float64) / u), 0, levels)
     code = np.where(u == 0, 0, code)
     return M.astype(np.float64) + u.astype(np.float64) * code, code.astype(np.int64)
 

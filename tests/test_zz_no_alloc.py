@@ -12,7 +12,7 @@ import numpy as np
 import pytest
 
 from mixed_precision_bit_gb300 import synth
-from tests.kitty_cases import attn_error, cfg_for, dev16, dev32, gpu_quantize
+from tests.kitty_cases import cfg_for, dev16, dev32, gpu_quantize
 
 pytestmark = pytest.mark.gpu
 
@@ -63,7 +63,6 @@ def test_noalloc_matches_workspace_entry_point(out_dtype):
     for cfg, ref in ((many, ref_many), (few, ref_few), (many, ref_many), (few, ref_few)):
         got = _run(kitty, cfg, w, inp, pool, True, out_dtype)
         assert np.array_equal(got, ref), "no-alloc output differs from the workspace path"
-    assert attn_error(ref_many, ref_few, out_dtype)[0] <= 0
 
     t = synth.workload("tiny")                           # one split: no scratch used
     tin = synth.host_inputs(t, seed=11)

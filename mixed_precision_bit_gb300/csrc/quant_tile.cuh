@@ -53,15 +53,9 @@ __device__ __forceinline__ float running_var(float sum, float sumsq, float n) {
 }
 
 struct QuantParams {
-  float M, u, ru;  // stored minimum and step as fp32, approximate 1/u
+  float M, u, ru;  // stored minimum and step as fp32, 1/u rounded to nearest
   uint16_t Sbits, Mbits;
 };
-
-__device__ __forceinline__ float rcp_approx(float x) {
-  float y;
-  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return y;
-}
 
 // Stored step for the exact step s >= 0: the smallest fp16 value >= s whose
 // significand has at most 7 bits.  The fp32 pattern is rounded up to 6
@@ -94,52 +88,25 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
     q.Sbits = step_f16(s);
     q.u = __half2float(__ushort_as_half(q.Sbits));
   }
-  // u == 0: ru = 0 makes every code of a finite input 0, and no quotient lands
-  // near a tie, so the division below is never taken
-  q.ru = q.u == 0.0f ? 0.0f : rcp_approx(q.u);
+  // u == 0: ru = 0 makes every code of a finite input 0
+  q.ru = q.u == 0.0f ? 0.0f : __frcp_rn(q.u);
   return q;
 }
 
-// Codes of four values: code = clamp(the integer nearest to d / u, ties to
-// even, 0, L) with d = fl(x - M).  The quotient is taken as d * (1/u), within
-// 2^-21 relative of the true value (so within 2^-17 for L <= 15 and 2^-13 for
-// L = 255 inside the clamp range); where one lands within 2^-15 (L <= 15) or
-// 2^-12 (L = 255) of a halfway point k0 + 1/2, the sign of d - (k0 + 1/2) u
-// decides it: (k0 + 1/2) u is exact in fp32 (at most 10 x 11 significant
-// bits), so one fused multiply-add gives that sign exactly, and a zero is an
-// exact tie.  (For fp32 d and u this equals rounding the correctly rounded
-// fp32 quotient: that quotient lands on a halfway point only when the exact one
-// does.)  One branch covers the four.
+// Codes of four values: code = clamp(rint((x - M) * (1/u)), 0, L), the
+// subtraction and the product rounded to nearest fp32 (two at a time as packed
+// fp32x2 operations, the same roundings), 1/u the correctly rounded
+// reciprocal, rint to the nearest integer (ties to even).  A saturating
+// conversion clamps below at 0, min() above at L.
 __device__ __forceinline__ void qcode4(const float (&x)[4], const QuantParams& q, int levels,
                                        uint32_t (&code)[4]) {
-  const float edge = 0.5f - (levels > 15 ? 0x1p-12f : 0x1p-15f);
-  float d[4], y[4], n[4], e[4];
-  // (x - M), (x - M) * (1/u) and the rounding residual, two at a time
+  float d[4], y[4];
   sub2_rn(d[0], d[1], x[0], x[1], q.M, q.M);
   sub2_rn(d[2], d[3], x[2], x[3], q.M, q.M);
   mul2_rn(y[0], y[1], d[0], d[1], q.ru, q.ru);
   mul2_rn(y[2], y[3], d[2], d[3], q.ru, q.ru);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) n[k] = rintf(y[k]);
-  sub2_rn(e[0], e[1], y[0], y[1], n[0], n[1]);
-  sub2_rn(e[2], e[3], y[2], y[3], n[2], n[3]);
-  float worst = 0.0f;  // largest |y - rint(y)|; a NaN quotient never counts
-#pragma unroll
-  for (int k = 0; k < 4; ++k) worst = fmaxf(worst, fabsf(e[k]));
-  if (worst > edge) {
-#pragma unroll
-    for (int k = 0; k < 4; ++k) {
-      const float k0 = rintf(y[k] - 0.5f);               // the halfway point is k0 + 1/2
-      const float r = fmaf(-(k0 + 0.5f), q.u, d[k]);     // exact sign of d - (k0 + 1/2) u
-      const float up = k0 + 1.0f;
-      const float tie = (__float2int_rz(k0) & 1) ? up : k0;  // to even
-      const float m = r > 0.0f ? up : (r < 0.0f ? k0 : tie);
-      n[k] = fabsf(e[k]) > edge ? m : n[k];
-    }
-  }
-  // n is integral: a saturating conversion clamps below at 0, min() above at L
-#pragma unroll
-  for (int k = 0; k < 4; ++k) code[k] = min(__float2uint_rz(n[k]), (uint32_t)levels);
+  for (int k = 0; k < 4; ++k) code[k] = min(__float2uint_rz(rintf(y[k])), (uint32_t)levels);
 }
 
 // One byte of four 2-bit codes, at bits 0, 2, 4, 6.

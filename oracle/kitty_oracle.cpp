@@ -333,12 +333,14 @@ uint16_t step_f16(float s) {
 // Asymmetric min/max quantization of one group (VeloxQuant-MLX docs, Prefill
 // phase step 3).  Readings: the minimum is stored as fp16 (nearest), the step
 // as step_f16 above, and the codes are computed against the STORED values, so
-// encoder and decoder agree: d = x - M rounded to fp32, and the code is the
-// integer nearest to the exact quotient d / u, ties to even, clamped to
-// [0, 2^b - 1].  The quotient is formed in fp64: d has at most 24 significant
-// bits and u at most 11, so a quotient that is not exactly halfway lies at
-// least 2^-35 (relative) from the halfway point, far outside the fp64
-// rounding, and an exact halfway quotient is computed exactly.  A boosted Key channel (2w-bit code) stores the step of its
+// encoder and decoder agree.  The code is the integer nearest to
+// (x - M) * (1 / u), each of the subtraction, the reciprocal and the product
+// rounded to nearest fp32 (integer ties to even), clamped to [0, 2^b - 1]:
+// "round((x - min) / scale)" with the division done as a multiplication by the
+// reciprocal of the step, as quantizers are commonly written.  It picks the
+// level nearest to the exact quotient except where that quotient lies within
+// about 2^-22 (relative) of a halfway point; there, and at exact halfway
+// values, the rounding of the reciprocal decides between the two neighbours.  A boosted Key channel (2w-bit code) stores the step of its
 // high w-bit plane, F = 2^w times its own step (F = 4 for the (4, 2)
 // configuration, 16 for (8, 4)).
 void quant_group(const float* x, int stride, int n, float mn, float mx, int levels,
@@ -356,10 +358,12 @@ void quant_group(const float* x, int stride, int n, float mn, float mx, int leve
     S = step_f16(s);
     u = f16_to_f32(S);
   }
+  const float ru = u == 0.0f ? 0.0f : 1.0f / u;
   for (int i = 0; i < n; ++i) {
     if (u == 0.0f) { code[i] = 0; continue; }
     const float d = x[i * stride] - Mf;
-    float q = (float)std::nearbyint((double)d / (double)u);
+    const float y = d * ru;
+    float q = std::nearbyint(y);
     if (q < 0.0f) q = 0.0f;
     if (q > (float)levels) q = (float)levels;
     code[i] = (uint16_t)q;

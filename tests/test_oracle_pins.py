@@ -175,8 +175,8 @@ def test_step_rule(orc):
 def _np_uniform_quant(x, levels):
     """Per-channel asymmetric min/max quantizer over tokens (KIVI-style, fp16
     minimum, step np_step(s) (a boosted 4-bit channel stores np_step(4 s) and
-    uses a quarter of it), nearest-even codes, clamp): the textbook special
-    case."""
+    uses a quarter of it), codes rint((x - M) * (1/u)) in fp32, clamp): the
+    textbook special case."""
     x = x.astype(np.float32)
     mn, mx = x.min(0), x.max(0)
     M = mn.astype(np.float16).astype(np.float32)
@@ -186,8 +186,9 @@ def _np_uniform_quant(x, levels):
     else:
         u = np_step(s)
     with np.errstate(divide="ignore", invalid="ignore"):
-        # nearest level to the quotient (d = x - M in fp32, the quotient in fp64)
-        code = np.clip(np.rint((x - M).astype(np.float32).astype(np.float64) / u), 0, levels)
+        # nearest integer to (x - M) times the reciprocal of the step, each rounded to fp32
+        ru = np.where(u == 0, np.float32(0), np.float32(1) / np.where(u == 0, np.float32(1), u))
+        code = np.clip(np.rint((x - M).astype(np.float32) * ru.astype(np.float32)), 0, levels)
     code = np.where(u == 0, 0, code)
     return M.astype(np.float64) + u.astype(np.float64) * code, code.astype(np.int64)
 
@@ -213,14 +214,16 @@ def test_hf0_equals_uniform_2bit(orc):
 def _np_uniform_4bit(x):
     """Textbook per-channel 4-bit asymmetric min/max quantizer that stores its own
     step: fp16 minimum, step u4 = np_step((max - min) / 15), codes
-    clamp(rint((x - M) / u4), 0, 15).  Returns (dequantized, the exact step s4)."""
+    clamp(rint((x - M) * (1/u4)), 0, 15) in fp32.  Returns (dequantized, the
+    exact step s4)."""
     x = x.astype(np.float32)
     mn, mx = x.min(0), x.max(0)
     M = mn.astype(np.float16).astype(np.float32)
     s4 = ((mx - mn).astype(np.float32) / np.float32(15)).astype(np.float32)
     u4 = np_step(s4)
     with np.errstate(divide="ignore", invalid="ignore"):
-        code = np.clip(np.rint((x - M).astype(np.float32).astype(np.float64) / u4), 0, 15)
+        ru = np.where(u4 == 0, np.float32(0), np.float32(1) / np.where(u4 == 0, np.float32(1), u4))
+        code = np.clip(np.rint((x - M).astype(np.float32) * ru.astype(np.float32)), 0, 15)
     code = np.where(u4 == 0, 0, code)
     return M.astype(np.float64) + u4.astype(np.float64) * code, s4
 
@@ -261,42 +264,48 @@ def test_hf1_equals_uniform_4bit(orc):
     assert tiny_seen >= 16
 
 
-def test_exact_rounding_ties_round_half_even(orc):
+def test_halfway_values_take_a_neighbouring_level(orc):
     """Values exactly halfway between two quantization levels, at steps 3*2^-m
-    that are not powers of two, take the even level (round half to even,
-    numpy's rint), for 3 levels (2-bit channels and Value groups), 15 (4-bit
-    boosted channels of the (4, 2) configuration and 4-bit channels of (8, 4))
-    and 255 (8-bit boosted channels of (8, 4)).  The planted columns have exact
-    minima and steps, so the decoded value is minimum + step * rint(quotient)."""
+    that are not powers of two (1/u is then inexact), for 3 levels (2-bit
+    channels and Value groups), 15 (4-bit boosted channels of the (4, 2)
+    configuration and 4-bit channels of (8, 4)) and 255 (8-bit boosted channels
+    of (8, 4)): each decodes to one of its two neighbouring levels, the group
+    ends decode exactly, and equal values get equal codes.  The planted columns
+    have exact minima and steps, so the levels are minimum + step * k."""
     from tests.edge_inputs import half_way_column
     r = _rng(21)
     for lo_bit, n_hi, lv in ((2, 0, (3, 15)), (2, 128, (3, 15)), (4, 0, (15, 255)),
                              (4, 128, (15, 255))):
         levels = lv[1] if n_hi else lv[0]
         xk = np.zeros((32, 128))
-        want_k = np.zeros((32, 128))
+        steps_k = np.zeros(128)
         for c in range(128):
             m, a = int(r.integers(2, 6)), int(r.integers(0, 3))
-            col = half_way_column(levels, m, a)[r.permutation(32)]
-            u = 3.0 * 2.0 ** -m
-            mn = col.min()
-            xk[:, c] = col
-            want_k[:, c] = mn + u * np.rint((col - mn) / u)
+            xk[:, c] = half_way_column(levels, m, a)[r.permutation(32)]
+            steps_k[c] = 3.0 * 2.0 ** -m
         xv = np.zeros((32, 128))
-        want_v = np.zeros((32, 128))
+        steps_v = np.zeros((32, 4))
         for t in range(32):
             for G in range(4):
                 m, a = int(r.integers(2, 6)), int(r.integers(0, 3))
-                col = half_way_column(3, m, a)[r.permutation(32)]
-                u = 3.0 * 2.0 ** -m
-                xv[t, 32 * G:32 * G + 32] = col
-                want_v[t, 32 * G:32 * G + 32] = col.min() + u * np.rint((col - col.min()) / u)
+                xv[t, 32 * G:32 * G + 32] = half_way_column(3, m, a)[r.permutation(32)]
+                steps_v[t, G] = 3.0 * 2.0 ** -m
         assert (_bf16(xk) == xk).all() and (_bf16(xv) == xv).all()
         blob, st = orc.quantize_page_f32(xk, xv, n_hi, lo_bit=lo_bit)
         kh, vh, st2 = orc.dequant_page(blob, n_hi, lo_bit=lo_bit)
         assert st == 0 and st2 == 0
-        assert (kh == want_k).all(), (lo_bit, n_hi)
-        assert (vh == want_v).all(), (lo_bit, n_hi)
+        groups = [(xk[:, c], kh[:, c], steps_k[c]) for c in range(128)]
+        groups += [(xv[t, 32 * G:32 * G + 32], vh[t, 32 * G:32 * G + 32], steps_v[t, G])
+                   for t in range(32) for G in range(4)]
+        for x, xh, u in groups:
+            mn = x.min()
+            q = (x - mn) / u                      # exact: k + 1/2, or 0 / levels at the ends
+            lo_, hi_ = mn + u * np.floor(q), mn + u * np.ceil(q)
+            assert ((xh == lo_) | (xh == hi_)).all(), (lo_bit, n_hi)
+            ends = (q == np.floor(q))
+            assert (xh[ends] == x[ends]).all()
+            for v in np.unique(x):
+                assert len(set(xh[x == v].tolist())) == 1
 
 
 def test_equal_variances_at_the_cut_go_to_lower_channels(orc):

@@ -31,15 +31,16 @@ def _kv(seed):
 
 def _np_quant(x, levels, factor=1):
     """Per-channel asymmetric min/max quantizer over 32 tokens: fp16 minimum,
-    step stored as np_step(factor * s) and used as that / factor, nearest-even
-    codes, clamp to [0, levels]."""
+    step stored as np_step(factor * s) and used as that / factor, codes
+    rint((x - M) * (1/u)) in fp32, clamp to [0, levels]."""
     x = x.astype(np.float32)
     mn, mx = x.min(0), x.max(0)
     M = mn.astype(np.float16).astype(np.float32)
     s = ((mx - mn).astype(np.float32) / np.float32(levels)).astype(np.float32)
     u = np_step(s * np.float32(factor)) / np.float32(factor)
     with np.errstate(divide="ignore", invalid="ignore"):
-        code = np.clip(np.rint((x - M).astype(np.float32).astype(np.float64) / u), 0, levels)
+        ru = np.where(u == 0, np.float32(0), np.float32(1) / np.where(u == 0, np.float32(1), u))
+        code = np.clip(np.rint((x - M).astype(np.float32) * ru.astype(np.float32)), 0, levels)
     code = np.where(u == 0, 0, code)
     return M.astype(np.float64) + u.astype(np.float64) * code, code.astype(np.int64)
 

@@ -49,6 +49,16 @@ def workload_spec(name: str, steps_total: int):
     """Shapes of the benchmark workloads (one GPU)."""
     import numpy as np
     from mixed_precision_bit_gb300 import synth
+    if name == "budget_fp16":
+        # the unquantized 16-bit paged layout on the same 40 GB budget (16 KB per
+        # (page, kv head), no tail or statistics): the comparison layout of the
+        # paper's batch and throughput claims
+        Hkv, Hq, layers, ctx_pages = 8, 32, 32, 256
+        B = synth.budget_batch(40 * 10 ** 9, layers, Hkv, ctx_pages, 2 * PAGE * D * 2, 0, 0)
+        tails = (synth.bits(0, "budget/tail", B) % np.uint64(32)).astype(np.int64)
+        return dict(name=name, B=int(B), Hq=Hq, Hkv=Hkv, n_hi=0, layers=layers, running=False,
+                    pages=np.full(B, ctx_pages, np.int64), tails=tails, drift=0,
+                    budget_bytes=40 * 10 ** 9, dtype=synth.BF16, lo_bit=2, f16kv=True)
     if name in ("budget", "budget_uniform", "budget_k4", "budget_84"):
         # budget: Kitty (top 32 of 128 Key channels at 4 bits, running statistics);
         # budget_uniform: every Key channel at 2 bits; budget_k4: every Key channel
@@ -166,7 +176,8 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
     import numpy as np
     import torch
     from mixed_precision_bit_gb300 import kitty
-    from mixed_precision_bit_gb300.cache import LayerCache
+    from mixed_precision_bit_gb300.cache import F16LayerCache, LayerCache
+    Cache = F16LayerCache if spec.get("f16kv") else LayerCache
     B, Hkv, L = spec["B"], spec["Hkv"], spec["layers"]
     pages, tails = spec["pages"], spec["tails"]
     head = headroom_pages(tails, steps_total)
@@ -182,7 +193,7 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
     tot = int(pages.sum())
     starts = np.concatenate([[0], np.cumsum(pages)[:-1]]) * PAGE
     for l in range(L):
-        lc = LayerCache(cfg, B, max_pages, pool_pages)
+        lc = Cache(cfg, B, max_pages, pool_pages)
         gen.manual_seed(seed * 7919 + l)
         sig = torch.exp(torch.randn((Hkv, D), generator=gen, device="cuda"))
         kp = torch.empty((tot * PAGE, Hkv, D), dtype=tdt, device="cuda")
@@ -312,7 +323,8 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
                                                if args.fused or args.graphs else 0)
                      for l, lc in enumerate(layers)])
     fl_dev = torch.from_numpy(np.stack(plans)).cuda()
-    splits, chunk = kitty.decode_plan(layers[0].cfg, B, layers[0].max_pages)
+    splits, chunk = ((0, 0) if spec.get("f16kv")
+                     else kitty.decode_plan(layers[0].cfg, B, layers[0].max_pages))
     stream = torch.cuda.current_stream()
     # CUDA graphs: per input set, one graph of the whole step (every layer's
     # call, in layer order); the step's flush ids are copied into one fixed
@@ -453,7 +465,7 @@ def run_kitty(args, rank, world, local_rank):
     del srv, layers, graphs, r0, q_all, kn_all, vn_all
     torch.cuda.synchronize()
     torch.cuda.empty_cache()
-    quant = measure_quantize(spec) if args.measure_quantize else None
+    quant = measure_quantize(spec) if args.measure_quantize and not spec.get("f16kv") else None
     targets = {}
     for name in [t for t in args.targets.split(",") if t]:
         targets[name] = target_measure(name, args, world, rank, local_rank)
@@ -611,7 +623,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kitty", choices=["kitty", "reference"])
     ap.add_argument("--workload", default="budget",
-                    choices=["budget", "budget_uniform", "budget_k4", "budget_84", "llama3_8b",
+                    choices=["budget", "budget_uniform", "budget_k4", "budget_84", "budget_fp16", "llama3_8b",
                              "qwen3_8b", "qwen3_g1", "qwen3_g2", "long", "tiny"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--pages-per-split", type=int, default=0,
@@ -709,7 +721,12 @@ def main():
         "e2e": {"value": job_throughput(world, B, r["E"], r["e2e_s"]), "unit": "tokens/s",
                 "h2d_bytes_per_step": r["h2d"], "d2h_bytes_per_step": r["d2h"]},
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if spec.get("f16kv"):
+        line["roofline"]["kernel"] = ("kitty_f16kv_append + kitty_f16kv_decode (16-bit paged "
+                                      "baseline: decode kernel + split combine)")
+        line["config"]["key_bits"] = "16 (unquantized bf16 K and V)"
+        line["gpu_launches"] = K * L * 4
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not spec.get("f16kv"):
         sample = OracleSample(spec, args.cpu_sample)
         sample.step()
         steps = 1

@@ -279,6 +279,47 @@ int kitty_decode_attention_noalloc(const kitty_cfg* cfg, const void* q, const vo
                                    const int32_t* tail_len, float sm_scale, void* out,
                                    int32_t out_dtype, int32_t B, int32_t* d_status, void* stream);
 
+/* ---------------------------------------------------------------- 16-bit paged baseline
+ * The unquantized paged KV cache that Kitty's memory budget and throughput are
+ * compared against (paper: Abstract, "up to 8x larger batches and 2.1x-4.1x
+ * higher throughput under the same memory budget").  Keys and Values stay in
+ * the input dtype (cfg->in_dtype); cfg's quantization fields are ignored.
+ * A (page, kv head) blob is K [32 tokens][128] followed by V [32][128], 16 KB; a
+ * page holds Hkv blobs in head order.  Sequence b holds ctx_len[b] tokens, token
+ * t in slot t % 32 of pool page block_table[b][t / 32]; there is no tail.
+ * Conventions (status codes, streams, ownership) are those above. */
+int kitty_f16kv_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page);
+
+/* Write n_pages full pages: page i of k, v (device [n_pages*32][Hkv][128],
+ * 16-byte aligned) goes to pool page page_ids[i] (out-of-range ids are skipped
+ * with KITTY_ST_BAD_PAGE). */
+int kitty_f16kv_write_pages(const kitty_cfg* cfg, const void* k, const void* v, int32_t n_pages,
+                            const int32_t* page_ids, void* pool, int32_t pool_pages,
+                            int32_t* d_status, void* stream);
+
+/* Append one token per sequence (k_new, v_new device [B][Hkv][128]) at position
+ * ctx_len[b]; a token that starts a page (ctx_len[b] % 32 == 0) goes to the
+ * caller's page new_page_ids[b], which is stored in the block table.  Then
+ * ctx_len[b] is incremented.  A full table gives KITTY_ST_TABLE_FULL. */
+int kitty_f16kv_append(const kitty_cfg* cfg, const void* k_new, const void* v_new, void* pool,
+                       int32_t pool_pages, int32_t* block_table, int32_t max_pages,
+                       int32_t* ctx_len, const int32_t* new_page_ids, int32_t B,
+                       int32_t* d_status, void* stream);
+
+/* Split-K workspace of kitty_f16kv_decode for this batch shape (0: one split). */
+int kitty_f16kv_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pages,
+                                size_t* bytes);
+
+/* Decode attention over the 16-bit pages: for query head hq of sequence b,
+ * out[b][hq] = softmax_t(sm_scale * q.k_t) . v_t over its ctx_len[b] tokens
+ * (kv head hq / (Hq/Hkv)); an empty sequence gives 0 and KITTY_ST_EMPTY.  q
+ * device [B][Hq][128] in_dtype; out [B][Hq][128] of out_dtype; workspace
+ * >= kitty_f16kv_workspace_bytes, 16-byte aligned. */
+int kitty_f16kv_decode(const kitty_cfg* cfg, const void* q, const void* pool, int32_t pool_pages,
+                       const int32_t* block_table, int32_t max_pages, const int32_t* ctx_len,
+                       float sm_scale, void* out, int32_t out_dtype, void* workspace,
+                       size_t workspace_bytes, int32_t B, int32_t* d_status, void* stream);
+
 /* Launch shape that kitty_decode_attention uses for this batch shape: number of
  * splits per sequence (at most 256) and the pages in the largest split (for
  * reporting and tests).  Split s covers block-table positions [start_s,

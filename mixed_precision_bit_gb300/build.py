@@ -13,7 +13,7 @@ OUT_DIR = os.path.join(PKG, "_build")
 LIB = os.path.join(OUT_DIR, "libkitty.so")
 INCLUDE = os.path.join(ROOT, "include")
 
-CU = ["quantize.cu", "decode.cu"]
+CU = ["quantize.cu", "decode.cu", "fp16kv.cu"]
 CPP = ["host.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -168,6 +168,106 @@ class LayerCache:
                 + self.B * Hq * D * 2 * 2 + pages * 4)
 
 
+class F16LayerCache:
+    """The unquantized 16-bit paged KV cache of one layer (the paper's comparison
+    layout for its same-budget claims, Abstract), with the same decode-loop
+    interface as LayerCache: every token lives in a 32-token page (no tail), a
+    token that starts a page gets a fresh page id from the host allocator, and
+    the host mirrors every length."""
+
+    def __init__(self, cfg: kitty.Config, B: int, max_pages: int, pool_pages: int,
+                 device="cuda"):
+        self.cfg, self.B, self.max_pages, self.pool_pages = cfg, B, max_pages, pool_pages
+        blob, per_page = kitty.f16kv_page_bytes(cfg)
+        self.blob, self.per_page = blob, per_page
+        dev = torch.device(device)
+        self.pool = torch.zeros(pool_pages * per_page, dtype=torch.uint8, device=dev)
+        self.block_table = torch.full((B, max_pages), -1, dtype=torch.int32, device=dev)
+        self.ctx_len = torch.zeros(B, dtype=torch.int32, device=dev)
+        self.status = torch.zeros(1, dtype=torch.int32, device=dev)
+        self.alloc = kitty.PageAllocator(pool_pages)
+        self.h_len = np.zeros(B, np.int64)
+        ws = kitty.f16kv_workspace_bytes(cfg, B, max_pages)
+        self.workspace = torch.empty(max(ws, 16) // 4, dtype=torch.float32, device=dev)
+
+    def prefill(self, k_pages, v_pages, n_pages, k_tail=None, v_tail=None, tails=None,
+                page_order=None, stream=None):
+        """As LayerCache.prefill: n_pages[b] full pages (k_pages, v_pages 16-bit
+        [sum(n_pages)*32, Hkv, D], sequence-major) and tails[b] more tokens
+        (k_tail, v_tail [B, Hkv, 32, D]), which go to a last, partial page."""
+        n_pages = np.asarray(n_pages, np.int64)
+        tails = np.zeros(self.B, np.int64) if tails is None else np.asarray(tails, np.int64)
+        tot = int(n_pages.sum())
+        dev = self.pool.device
+        ids = self.alloc.alloc(tot)
+        if page_order is not None:
+            ids = ids[np.asarray(page_order)]
+        with_tail = np.nonzero(tails > 0)[0]
+        tail_ids = self.alloc.alloc(with_tail.size) if with_tail.size else np.zeros(0, np.int32)
+        bt = np.full((self.B, self.max_pages), -1, np.int32)
+        off = 0
+        for b in range(self.B):
+            bt[b, :n_pages[b]] = ids[off:off + n_pages[b]]
+            off += n_pages[b]
+        for i, b in enumerate(with_tail):
+            bt[b, n_pages[b]] = tail_ids[i]
+        self.block_table.copy_(torch.from_numpy(bt))
+        if tot:
+            kitty.f16kv_write_pages(self.cfg, k_pages, v_pages,
+                                    torch.from_numpy(ids.astype(np.int32)).to(dev), self.pool,
+                                    self.pool_pages, status=self.status, stream=stream)
+        if with_tail.size:
+            sel = torch.from_numpy(with_tail).to(dev)
+            kt = k_tail.index_select(0, sel).transpose(1, 2).contiguous()  # [n, 32, Hkv, D]
+            vt = v_tail.index_select(0, sel).transpose(1, 2).contiguous()
+            kitty.f16kv_write_pages(self.cfg, kt, vt,
+                                    torch.from_numpy(tail_ids.astype(np.int32)).to(dev),
+                                    self.pool, self.pool_pages, status=self.status, stream=stream)
+        self.h_len[:] = n_pages * PAGE + tails
+        self.ctx_len.copy_(torch.from_numpy(self.h_len.astype(np.int32)))
+        return ids
+
+    def plan_flush(self) -> np.ndarray:
+        """Host decision for the next append: a fresh page id for each sequence whose
+        next token starts a page, -1 elsewhere; advances the host mirror."""
+        fl = np.full(self.B, -1, np.int32)
+        new = np.nonzero(self.h_len % PAGE == 0)[0]
+        new = new[self.h_len[new] // PAGE < self.max_pages]
+        if new.size:
+            fl[new] = self.alloc.alloc(new.size)
+        self.h_len += 1
+        return fl
+
+    def append(self, k_new, v_new, new_page_ids, stream=None):
+        kitty.f16kv_append(self.cfg, k_new, v_new, self.pool, self.pool_pages, self.block_table,
+                           self.ctx_len, new_page_ids, status=self.status, stream=stream)
+
+    def attend(self, q, out, sm_scale=None, stream=None):
+        sm = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
+        kitty.f16kv_decode(self.cfg, q, self.pool, self.pool_pages, self.block_table,
+                           self.ctx_len, sm, out, workspace=self.workspace, status=self.status,
+                           stream=stream)
+
+    def step(self, k_new, v_new, new_page_ids, q, out, sm_scale=None, stream=None):
+        """append then attend (the append's two kernels, the decode and its combine)."""
+        self.append(k_new, v_new, new_page_ids, stream=stream)
+        self.attend(q, out, sm_scale, stream=stream)
+
+    def append_bytes(self, new_page_ids, fused: bool = False) -> int:
+        """The new K/V token read and written into its page."""
+        return self.B * self.cfg.num_kv_heads * D * 2 * 2 * 2
+
+    def kv_tokens(self) -> int:
+        return int(self.h_len.sum())
+
+    def algorithmic_bytes(self) -> int:
+        """Bytes one decode call must move: the K and V rows of every cached token,
+        Q, O and the block-table entries (host mirror of the lengths)."""
+        Hkv, Hq = self.cfg.num_kv_heads, self.cfg.num_q_heads
+        pages = int(((self.h_len + PAGE - 1) // PAGE).sum())
+        return (int(self.h_len.sum()) * Hkv * D * 2 * 2 + self.B * Hq * D * 2 * 2 + pages * 4)
+
+
 def capture_layers_step(layers, k_new, v_new, flush_ids, q, out, sm_scale=None,
                         fused: bool = True):
     """One CUDA graph of a decode step over every layer: per layer l in order, the

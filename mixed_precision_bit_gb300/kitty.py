@@ -65,7 +65,9 @@ EXPORTS = ("kitty_abi_version", "kitty_page_bytes", "kitty_avg_bits", "kitty_all
            "kitty_alloc_pages", "kitty_free_pages", "kitty_alloc_free_count",
            "kitty_alloc_destroy", "kitty_quantize_pages", "kitty_append_token",
            "kitty_decode_workspace_bytes", "kitty_decode_attention", "kitty_decode_plan",
-           "kitty_decode_attention_noalloc", "kitty_append_decode")
+           "kitty_decode_attention_noalloc", "kitty_append_decode", "kitty_f16kv_page_bytes",
+           "kitty_f16kv_write_pages", "kitty_f16kv_append", "kitty_f16kv_workspace_bytes",
+           "kitty_f16kv_decode")
 NOALLOC_SCRATCH_BYTES = 8 << 20
 
 
@@ -102,6 +104,12 @@ def load():
                                                    ctypes.c_float, P, i32, P, sz, i32, P, P]),
             "kitty_decode_plan": (ctypes.c_int, [C, i32, i32, ctypes.POINTER(i32),
                                                  ctypes.POINTER(i32)]),
+            "kitty_f16kv_page_bytes": (ctypes.c_int, [C, ctypes.POINTER(sz), ctypes.POINTER(sz)]),
+            "kitty_f16kv_write_pages": (ctypes.c_int, [C, P, P, i32, P, P, i32, P, P]),
+            "kitty_f16kv_append": (ctypes.c_int, [C, P, P, P, i32, P, i32, P, P, i32, P, P]),
+            "kitty_f16kv_workspace_bytes": (ctypes.c_int, [C, i32, i32, ctypes.POINTER(sz)]),
+            "kitty_f16kv_decode": (ctypes.c_int, [C, P, P, i32, P, i32, P, ctypes.c_float, P, i32,
+                                                  P, sz, i32, P, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -267,3 +275,46 @@ def append_decode(cfg: Config, k_new, v_new, q, tail_k, tail_v, tail_len, run_su
         _ptr(block_table), block_table.shape[1], _ptr(num_pages), _ptr(pool), pool_pages,
         float(sm_scale), _ptr(out), out_dtype, _ptr(workspace), ws_bytes, B, _ptr(status),
         _stream(stream)))
+
+
+# ------------------------------------------------------------------ 16-bit paged baseline
+def f16kv_page_bytes(cfg: Config):
+    b, p = ctypes.c_size_t(), ctypes.c_size_t()
+    _chk("kitty_f16kv_page_bytes", load().kitty_f16kv_page_bytes(
+        ctypes.byref(cfg.c()), ctypes.byref(b), ctypes.byref(p)))
+    return b.value, p.value
+
+
+def f16kv_write_pages(cfg: Config, k, v, page_ids, pool, pool_pages: int, status=None,
+                      stream=None):
+    _chk("kitty_f16kv_write_pages", load().kitty_f16kv_write_pages(
+        ctypes.byref(cfg.c()), _ptr(k), _ptr(v), page_ids.numel(), _ptr(page_ids), _ptr(pool),
+        pool_pages, _ptr(status), _stream(stream)))
+
+
+def f16kv_append(cfg: Config, k_new, v_new, pool, pool_pages: int, block_table, ctx_len,
+                 new_page_ids, status=None, stream=None):
+    _chk("kitty_f16kv_append", load().kitty_f16kv_append(
+        ctypes.byref(cfg.c()), _ptr(k_new), _ptr(v_new), _ptr(pool), pool_pages,
+        _ptr(block_table), block_table.shape[1], _ptr(ctx_len), _ptr(new_page_ids),
+        ctx_len.numel(), _ptr(status), _stream(stream)))
+
+
+def f16kv_workspace_bytes(cfg: Config, B: int, max_pages: int) -> int:
+    n = ctypes.c_size_t()
+    _chk("kitty_f16kv_workspace_bytes", load().kitty_f16kv_workspace_bytes(
+        ctypes.byref(cfg.c()), B, max_pages, ctypes.byref(n)))
+    return n.value
+
+
+def f16kv_decode(cfg: Config, q, pool, pool_pages: int, block_table, ctx_len, sm_scale: float,
+                 out, workspace=None, status=None, stream=None, out_dtype=None):
+    import torch
+    B = ctx_len.numel()
+    if out_dtype is None:
+        out_dtype = {torch.float32: F32, torch.bfloat16: BF16, torch.float16: F16}[out.dtype]
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _chk("kitty_f16kv_decode", load().kitty_f16kv_decode(
+        ctypes.byref(cfg.c()), _ptr(q), _ptr(pool), pool_pages, _ptr(block_table),
+        block_table.shape[1], _ptr(ctx_len), float(sm_scale), _ptr(out), out_dtype,
+        _ptr(workspace), ws_bytes, B, _ptr(status), _stream(stream)))

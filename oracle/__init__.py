@@ -68,6 +68,7 @@ def lib():
             "orc_append_token": (i, [i, i, i, i, P, P, P, P, P, P, P, P, P, P, i, P, P, i, i, i]),
             "orc_decode_attention": (i, [i, i, i, i, P, P, i, P, i, P, P, P, P, f, i, P, i]),
             "orc_decode_attention_one": (i, [i, i, i, i, P, P, i, P, i, P, P, P, P, f, i, i, P, i]),
+            "orc_decode_f16kv": (i, [i, i, i, P, P, i, P, i, P, f, i, P]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(L, name)
@@ -238,6 +239,21 @@ def decode_attention(Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, 
     st = lib().orc_decode_attention(Hkv, Hq, n_hi, in_dtype, _p(q), _p(pool), pool_pages,
                                     _p(block_table), max_pages, _p(num_pages), _p(tail_k),
                                     _p(tail_v), _p(tail_len), float(sm_scale), B, _p(out), lo_bit)
+    return out, st
+
+
+def decode_f16kv(Hkv, Hq, in_dtype, q, pool, pool_pages, block_table, ctx_len, sm_scale):
+    """16-bit paged KV baseline: pool uint16 [pool_pages, Hkv, 2, 32, 128] (K then V);
+    returns (out float64 [B, Hq, 128], status)."""
+    q = _c(q, np.uint16)
+    pool = _c(pool, np.uint16)
+    block_table = _c(block_table, np.int32)
+    ctx_len = _c(ctx_len, np.int32)
+    B = ctx_len.size
+    max_pages = block_table.shape[1] if block_table.ndim == 2 else 0
+    out = np.zeros((B, Hq, 128), np.float64)
+    st = lib().orc_decode_f16kv(Hkv, Hq, in_dtype, _p(q), _p(pool), pool_pages, _p(block_table),
+                                max_pages, _p(ctx_len), float(sm_scale), B, _p(out))
     return out, st
 
 

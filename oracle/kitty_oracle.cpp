@@ -838,6 +838,60 @@ int orc_decode_attention(int Hkv, int Hq, int n_hi, int in_dtype, const uint16_t
   return st;
 }
 
+// 16-bit paged KV baseline (the unquantized layout Kitty is compared against on
+// one memory budget; paper: Abstract).  A (page, kv head) blob holds K [32][D]
+// then V [32][D] in the input dtype; sequence b holds ctx_len[b] tokens, token
+// t in slot t % 32 of page block_table[b][t / 32].  fp64 attention with no
+// quantization: out[b][hq] = softmax_t(sm_scale * q.k_t) . v_t, query head hq
+// reading kv head hq / (Hq / Hkv); an empty sequence gives 0 and ST_EMPTY.
+int orc_decode_f16kv(int Hkv, int Hq, int in_dtype, const uint16_t* q, const uint16_t* pool,
+                     int pool_pages, const int* block_table, int max_pages, const int* ctx_len,
+                     float sm_scale, int B, double* out) {
+  if (Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B < 0) return -1;
+  const int g = Hq / Hkv;
+  const size_t blob = 2 * (size_t)P * D;  // 16-bit elements per (page, kv head)
+  std::vector<int> sts(B > 0 ? (size_t)B * Hkv : 1, ST_OK);
+  parallel_for(B * Hkv, [&](int i) {
+    const int b = i / Hkv, kvh = i % Hkv;
+    const int len = ctx_len[b];
+    double* o = out + ((size_t)b * Hq + (size_t)kvh * g) * D;
+    if (len < 0 || len > max_pages * P) { sts[i] = ST_BAD_LEN; return; }
+    std::vector<const uint16_t*> krow(len), vrow(len);
+    for (int t = 0; t < len; ++t) {
+      const int pid = block_table[(size_t)b * max_pages + t / P];
+      if (pid < 0 || pid >= pool_pages) { sts[i] = ST_BAD_PAGE; return; }
+      const uint16_t* base = pool + ((size_t)pid * Hkv + kvh) * blob;
+      krow[t] = base + (size_t)(t % P) * D;
+      vrow[t] = base + (size_t)(P + t % P) * D;
+    }
+    for (int h = 0; h < g; ++h) {
+      const uint16_t* qh = q + ((size_t)b * Hq + (size_t)kvh * g + h) * D;
+      double* oh = o + (size_t)h * D;
+      for (int c = 0; c < D; ++c) oh[c] = 0.0;
+      if (len == 0) { sts[i] = ST_EMPTY; continue; }
+      std::vector<double> sc(len);
+      double mx = -INFINITY;
+      for (int t = 0; t < len; ++t) {
+        double acc = 0.0;
+        for (int c = 0; c < D; ++c)
+          acc += (double)in_to_f32(qh[c], in_dtype) * (double)in_to_f32(krow[t][c], in_dtype);
+        sc[t] = acc * (double)sm_scale;
+        mx = std::max(mx, sc[t]);
+      }
+      double den = 0.0;
+      for (int t = 0; t < len; ++t) {
+        sc[t] = std::exp(sc[t] - mx);
+        den += sc[t];
+      }
+      for (int t = 0; t < len; ++t)
+        for (int c = 0; c < D; ++c) oh[c] += sc[t] / den * (double)in_to_f32(vrow[t][c], in_dtype);
+    }
+  });
+  int st = ST_OK;
+  for (int x : sts) note(&st, x);
+  return st;
+}
+
 // The g query heads of one (sequence, kv head) only; out: [g][D].  For sampled
 // checks on workloads too large to run whole.
 int orc_decode_attention_one(int Hkv, int Hq, int n_hi, int in_dtype, const uint16_t* q,

@@ -755,3 +755,43 @@ def test_sequence_mode_ranks_over_the_whole_prompt(orc):
                    for p in range(npg))
     run_pool, (rs1, rq1, rc1) = _quant(orc, 1, k, v, npg)
     assert (rs == rs1).all() and (rq == rq1).all() and (rc == rc1).all() and rc[0, 0] == 32 * npg
+
+
+# ----------------------------------------------------------------- 16-bit paged baseline
+def test_f16kv_attention_against_numpy(orc):
+    """The unquantized 16-bit paged layout (the comparison layout of the paper's
+    same-budget claims, Abstract): the oracle's fp64 attention over pages in
+    block-table order equals numpy's softmax attention over the token rows,
+    with ragged lengths (a partial last page), grouped heads (query head h
+    reads kv head h / g), an empty sequence (0 and EMPTY) and a bad page id."""
+    r = _rng(31)
+    Hkv, Hq, D, P = 2, 6, 128, 32
+    lens = np.array([70, 1, 0, 64], np.int32)
+    max_pages = 3
+    pool_pages = 12
+    for dt in (synth.BF16, synth.F16):
+        pool = synth.to_bits(r.standard_normal((pool_pages, Hkv, 2, P, D)), dt)
+        ids = r.permutation(pool_pages)[:len(lens) * max_pages].reshape(len(lens), max_pages).astype(np.int32)
+        q = synth.to_bits(r.standard_normal((len(lens), Hq, D)), dt)
+        scale = float(np.float32(1 / np.sqrt(D)))
+        out, st = orc.decode_f16kv(Hkv, Hq, dt, q, pool, pool_pages, ids, lens, scale)
+        assert st == orc.ST["EMPTY"]
+        kv = synth.from_bits(pool, dt).astype(np.float64)
+        qf = synth.from_bits(q, dt).astype(np.float64)
+        for b, L in enumerate(lens):
+            for hq in range(Hq):
+                h = hq // (Hq // Hkv)
+                if L == 0:
+                    assert (out[b, hq] == 0).all()
+                    continue
+                t = np.arange(L)
+                K = kv[ids[b, t // P], h, 0, t % P]
+                V = kv[ids[b, t // P], h, 1, t % P]
+                s = K @ qf[b, hq] * scale
+                w = np.exp(s - s.max())
+                ref = (w / w.sum()) @ V
+                assert np.abs(out[b, hq] - ref).max() <= 1e-12 * max(1.0, np.abs(ref).max())
+        bad = ids.copy()
+        bad[0, 1] = pool_pages + 3
+        _, st = orc.decode_f16kv(Hkv, Hq, dt, q, pool, pool_pages, bad, lens, scale)
+        assert st == orc.ST["BAD_PAGE"]

@@ -48,7 +48,7 @@ def lib():
         sig = {
             "orc_abi_version": (i, []),
             "orc_set_threads": (None, [i]),
-            "orc_page_bytes": (ctypes.c_long, [i, i]),
+            "orc_page_bytes": (ctypes.c_long, [i, i, i]),
             "orc_avg_bits": (d, [d, i, i]),
             "orc_f32_to_f16": (ctypes.c_uint16, [f]),
             "orc_step_f16": (ctypes.c_uint16, [f]),
@@ -60,14 +60,15 @@ def lib():
             "orc_key_pos": (None, [i, i, i, P, P]),
             "orc_key_pos4": (None, [i, i, i, P, P]),
             "orc_val_pos": (None, [i, i, P, P]),
-            "orc_quantize_page_f32": (i, [P, P, i, i, P, P, P, P, i]),
-            "orc_dequant_page": (None, [P, i, P, P, P, i]),
+            "orc_val_pos4": (None, [i, i, P, P]),
+            "orc_quantize_page_f32": (i, [P, P, i, i, P, P, P, P, i, i]),
+            "orc_dequant_page": (None, [P, i, P, P, P, i, i]),
             "orc_page_channels": (None, [P, i, P, i]),
             "orc_meta_pos": (None, [i, i, i, P]),
-            "orc_quantize_pages": (i, [i, i, i, i, P, P, i, P, P, i, P, P, P, P, i, i]),
-            "orc_append_token": (i, [i, i, i, i, P, P, P, P, P, P, P, P, P, P, i, P, P, i, i, i]),
-            "orc_decode_attention": (i, [i, i, i, i, P, P, i, P, i, P, P, P, P, f, i, P, i]),
-            "orc_decode_attention_one": (i, [i, i, i, i, P, P, i, P, i, P, P, P, P, f, i, i, P, i]),
+            "orc_quantize_pages": (i, [i, i, i, i, P, P, i, P, P, i, P, P, P, P, i, i, i]),
+            "orc_append_token": (i, [i, i, i, i, P, P, P, P, P, P, P, P, P, P, i, P, P, i, i, i, i]),
+            "orc_decode_attention": (i, [i, i, i, i, P, P, i, P, i, P, P, P, P, f, i, P, i, i]),
+            "orc_decode_attention_one": (i, [i, i, i, i, P, P, i, P, i, P, P, P, P, f, i, i, P, i, i]),
             "orc_decode_f16kv": (i, [i, i, i, P, P, i, P, i, P, f, i, P]),
         }
         for name, (res, args) in sig.items():
@@ -91,10 +92,10 @@ def set_threads(n: int) -> None:
     lib().orc_set_threads(int(n))
 
 
-def page_bytes(n_hi: int, lo_bit: int = 2) -> int:
+def page_bytes(n_hi: int, lo_bit: int = 2, v_bit: int = 2) -> int:
     """Bytes of one (page, kv-head) blob; lo_bit = Key plane width (2: (4, 2)
-    configuration, 4: (8, 4))."""
-    return int(lib().orc_page_bytes(n_hi, lo_bit))
+    configuration, 4: (8, 4)), v_bit = Value code width (2, or 4 with lo_bit 4)."""
+    return int(lib().orc_page_bytes(n_hi, lo_bit, v_bit))
 
 
 def avg_bits(hf: float, hi_bit: int, lo_bit: int) -> float:
@@ -154,19 +155,27 @@ def val_pos(t: int, c: int):
     return w.value, b.value
 
 
-def quantize_page_f32(xk, xv, n_hi: int, running=None, lo_bit: int = 2):
+def val_pos4(t: int, c: int):
+    """4-bit Value plane: (word, bit) of token t, channel c."""
+    w, b = ctypes.c_int(), ctypes.c_int()
+    lib().orc_val_pos4(t, c, ctypes.byref(w), ctypes.byref(b))
+    return w.value, b.value
+
+
+def quantize_page_f32(xk, xv, n_hi: int, running=None, lo_bit: int = 2, v_bit: int = 2):
     """One page-head from fp32 [32,128] tiles.  running = (sum[128], sumsq[128],
     count[1]) arrays updated in place, or None for page mode.  Returns
     (blob bytes, status)."""
     xk = _c(xk, np.float32)
     xv = _c(xv, np.float32)
-    blob = np.zeros(page_bytes(n_hi, lo_bit), np.uint8)
+    blob = np.zeros(page_bytes(n_hi, lo_bit, v_bit), np.uint8)
     if running is None:
-        st = lib().orc_quantize_page_f32(_p(xk), _p(xv), n_hi, 0, None, None, None, _p(blob), lo_bit)
+        st = lib().orc_quantize_page_f32(_p(xk), _p(xv), n_hi, 0, None, None, None, _p(blob), lo_bit,
+                                         v_bit)
     else:
         rs, rq, rc = running
         st = lib().orc_quantize_page_f32(_p(xk), _p(xv), n_hi, 1, _p(rs), _p(rq), _p(rc), _p(blob),
-                                         lo_bit)
+                                         lo_bit, v_bit)
     return blob, st
 
 
@@ -186,18 +195,18 @@ def meta_pos(kind: str, a: int, b: int = 0) -> int:
     return pos.value
 
 
-def dequant_page(blob, n_hi: int, lo_bit: int = 2):
+def dequant_page(blob, n_hi: int, lo_bit: int = 2, v_bit: int = 2):
     blob = _c(blob, np.uint8)
     kh = np.zeros((32, 128), np.float64)
     vh = np.zeros((32, 128), np.float64)
     st = ctypes.c_int()
-    lib().orc_dequant_page(_p(blob), n_hi, _p(kh), _p(vh), ctypes.byref(st), lo_bit)
+    lib().orc_dequant_page(_p(blob), n_hi, _p(kh), _p(vh), ctypes.byref(st), lo_bit, v_bit)
     return kh, vh, st.value
 
 
 def quantize_pages(Hkv, n_hi, rank_mode, in_dtype, k, v, page_ids, pool, pool_pages,
                    seq_of_page=None, n_seqs=0, run_sum=None, run_sumsq=None, run_count=None,
-                   lo_bit=2):
+                   lo_bit=2, v_bit=2):
     """k, v: uint16 [n_pages*32, Hkv, 128]; pool: uint8 array updated in place."""
     k = _c(k, np.uint16)
     v = _c(v, np.uint16)
@@ -207,12 +216,12 @@ def quantize_pages(Hkv, n_hi, rank_mode, in_dtype, k, v, page_ids, pool, pool_pa
     assert pool.flags.c_contiguous and pool.dtype == np.uint8
     return lib().orc_quantize_pages(Hkv, n_hi, rank_mode, in_dtype, _p(k), _p(v), n_pages,
                                     _p(page_ids), _p(sop), n_seqs, _p(run_sum), _p(run_sumsq),
-                                    _p(run_count), _p(pool), pool_pages, lo_bit)
+                                    _p(run_count), _p(pool), pool_pages, lo_bit, v_bit)
 
 
 def append_token(Hkv, n_hi, rank_mode, in_dtype, k_new, v_new, tail_k, tail_v, tail_len,
                  run_sum, run_sumsq, run_count, flush_page_ids, block_table, max_pages,
-                 num_pages, pool, pool_pages, lo_bit=2):
+                 num_pages, pool, pool_pages, lo_bit=2, v_bit=2):
     """All state arrays are numpy arrays updated in place."""
     k_new = _c(k_new, np.uint16)
     v_new = _c(v_new, np.uint16)
@@ -221,11 +230,12 @@ def append_token(Hkv, n_hi, rank_mode, in_dtype, k_new, v_new, tail_k, tail_v, t
     return lib().orc_append_token(Hkv, n_hi, rank_mode, in_dtype, _p(k_new), _p(v_new),
                                   _p(tail_k), _p(tail_v), _p(tail_len), _p(run_sum),
                                   _p(run_sumsq), _p(run_count), _p(fl), _p(block_table),
-                                  max_pages, _p(num_pages), _p(pool), pool_pages, B, lo_bit)
+                                  max_pages, _p(num_pages), _p(pool), pool_pages, B, lo_bit,
+                                  v_bit)
 
 
 def decode_attention(Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, num_pages,
-                     tail_k, tail_v, tail_len, sm_scale, lo_bit=2):
+                     tail_k, tail_v, tail_len, sm_scale, lo_bit=2, v_bit=2):
     """Returns (out float64 [B, Hq, 128], status)."""
     q = _c(q, np.uint16)
     block_table = _c(block_table, np.int32)
@@ -238,7 +248,8 @@ def decode_attention(Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, 
     out = np.zeros((B, Hq, 128), np.float64)
     st = lib().orc_decode_attention(Hkv, Hq, n_hi, in_dtype, _p(q), _p(pool), pool_pages,
                                     _p(block_table), max_pages, _p(num_pages), _p(tail_k),
-                                    _p(tail_v), _p(tail_len), float(sm_scale), B, _p(out), lo_bit)
+                                    _p(tail_v), _p(tail_len), float(sm_scale), B, _p(out), lo_bit,
+                                    v_bit)
     return out, st
 
 
@@ -258,7 +269,7 @@ def decode_f16kv(Hkv, Hq, in_dtype, q, pool, pool_pages, block_table, ctx_len, s
 
 
 def decode_attention_one(Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_table, num_pages,
-                         tail_k, tail_v, tail_len, sm_scale, b, kvh, lo_bit=2):
+                         tail_k, tail_v, tail_len, sm_scale, b, kvh, lo_bit=2, v_bit=2):
     """The g = Hq/Hkv query heads of (sequence b, kv head kvh): (out [g, 128], status)."""
     g = Hq // Hkv
     out = np.zeros((g, 128), np.float64)
@@ -266,5 +277,5 @@ def decode_attention_one(Hkv, Hq, n_hi, in_dtype, q, pool, pool_pages, block_tab
     st = lib().orc_decode_attention_one(Hkv, Hq, n_hi, in_dtype, _p(q), _p(pool), pool_pages,
                                         _p(block_table), max_pages, _p(num_pages), _p(tail_k),
                                         _p(tail_v), _p(tail_len), float(sm_scale), b, kvh, _p(out),
-                                        lo_bit)
+                                        lo_bit, v_bit)
     return out, st

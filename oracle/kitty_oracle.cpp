@@ -4,9 +4,9 @@
 // computes: per-page channel statistics, variance ranking with a top-k boost
 // set, asymmetric min/max quantization of Keys (lo_bit codes; boosted channels
 // hi_bit = 2*lo_bit, split into two uniform lo_bit planes; (hi_bit, lo_bit) =
-// (4, 2) by default or (8, 4)) and Values (2-bit per-token groups of 32
-// channels), the packed page format, the append/flush step, and fp64 decode
-// attention over the dequantized pages.
+// (4, 2) by default or (8, 4)) and Values (per-token groups of 32 channels,
+// 2-bit, or 4-bit with 4-bit Key planes), the packed page format, the
+// append/flush step, and fp64 decode attention over the dequantized pages.
 //
 // Only the test suite, the package's smoke check and the bench's CPU-baseline
 // leg may load this library.  It shares no code with the CUDA path.  Build with
@@ -24,7 +24,11 @@
 //    tokens), Decode phase step 2 (running variance formula), Effective
 //    bit-width, Configuration reference, Tuning avg_bits (the (0.25, 8, 4) row:
 //    8-bit boosted and 4-bit other Key channels; Values keep their 2-bit
-//    format -- the table concerns Keys only, a reading).
+//    format -- the table concerns Keys only, a reading).  The same paper's
+//    Abstract names 4-bit KV quantization as the accuracy-preserving point
+//    Kitty is measured against: with n_hi = 0, 4-bit Key planes and 4-bit
+//    Values (v_bit = 4) this format is that uniform 4-bit KV cache (a reading:
+//    the same per-channel Key and per-token Value groups at 15 levels).
 //  * PagedAttention / FlashAttention (cited by the paper) for the block table
 //    and softmax attention semantics.
 // Readings where the pages are silent are stated next to the code that takes
@@ -116,20 +120,20 @@ float in_to_f32(uint16_t v, int dtype) { return dtype == 1 ? bf16_to_f32(v) : f1
 //   KM     256 B      fp16 minimum per channel, at km_pos(c)
 //   Kch    n_hi B     boosted channel ids; row j of Kextra (the j-th smallest
 //                     boosted channel) is stored at byte kch_pos(j)
-//   Vbase  1024 B     2-bit codes, 32 tokens x D channels
+//   Vbase  128*v B    v-bit codes (v = v_bit, 2 or 4), 32 tokens x D channels
 //   VS     256 B      fp16 step per (group, token), at vmeta_pos(G, t)
 //   VM     256 B      fp16 minimum per (group, token), at vmeta_pos(G, t)
 struct Layout {
-  int n_hi, w;
+  int n_hi, w, vw;
   size_t kbase, kextra, ks, km, kch, vbase, vs, vm, bytes;
-  Layout(int nh, int w_) : n_hi(nh), w(w_) {
+  Layout(int nh, int w_, int vw_) : n_hi(nh), w(w_), vw(vw_) {
     kbase = 0;
     kextra = (size_t)D * P * w / 8;
     ks = kextra + (size_t)nh * P * w / 8;
     km = ks + 256;
     kch = km + 256;
     vbase = kch + (size_t)nh;
-    vs = vbase + 1024;
+    vs = vbase + (size_t)P * D * vw_ / 8;
     vm = vs + 256;
     bytes = vm + 256;
   }
@@ -180,6 +184,20 @@ BitPos val_pos(int t, int c) {
   return {lane * 8 + (mc >> 1) * 2 + kt, 16 * e + 8 * half + 2 * tau};
 }
 
+// 4-bit Value plane, same rows and columns with nibbles: a lane holds four
+// words per 32-channel group G (16-token block kt, 16-channel tile parity), and
+// inside a word element (row, col) sits at bit 16*(col parity) + 8*(col half) +
+// 4*(row's 8-row half).
+BitPos val_pos4(int t, int c) {
+  const int mc = c >> 4, rh = (c >> 3) & 1, r = c & 7;
+  const int kt = t >> 4, half = (t >> 3) & 1, qq = (t & 7) >> 1, e = t & 1;
+  const int lane = 4 * r + qq;
+  return {lane * 16 + (mc >> 1) * 4 + kt * 2 + (mc & 1), 16 * e + 8 * half + 4 * rh};
+}
+
+// Value code position for Value width vw.
+BitPos vpos(int vw, int t, int c) { return vw == 4 ? val_pos4(t, c) : val_pos(t, c); }
+
 // Metadata read by the decode in 16-byte pieces is stored in the same
 // "fragment order" as the planes: the values lane group qq = (index % 8) / 2
 // needs are contiguous.
@@ -213,8 +231,6 @@ uint32_t getb(const uint8_t* plane, BitPos p, int bits) {
   return (w >> p.bit) & ((1u << bits) - 1u);
 }
 
-void put2(uint8_t* plane, BitPos p, uint32_t code) { putb(plane, p, code, 2); }
-uint32_t get2(const uint8_t* plane, BitPos p) { return getb(plane, p, 2); }
 
 uint16_t rd16(const uint8_t* p, size_t i) { uint16_t v; std::memcpy(&v, p + 2 * i, 2); return v; }
 void wr16(uint8_t* p, size_t i, uint16_t v) { std::memcpy(p + 2 * i, &v, 2); }
@@ -382,10 +398,10 @@ int check_range(const float* x, int n) {
 }
 
 // Encode one (page, kv-head): Key planes with the given boost set, Value
-// planes, metadata and channel list, into `blob` (Layout(n_hi, w).bytes bytes).
+// plane, metadata and channel list, into `blob` (Layout(n_hi, w, vw).bytes bytes).
 void encode_blob(const float* xk, const float* xv, const PageStats& st, const bool* boosted,
-                 int n_hi, int w, uint8_t* blob) {
-  const Layout lay(n_hi, w);
+                 int n_hi, int w, int vw, uint8_t* blob) {
+  const Layout lay(n_hi, w, vw);
   std::memset(blob, 0, lay.bytes);
   uint8_t* kbase = blob + lay.kbase;
   uint8_t* kextra = blob + lay.kextra;
@@ -422,10 +438,10 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
       for (int i = 1; i < VG; ++i) { mn = min_of(mn, x[i]); mx = max_of(mx, x[i]); }
       uint16_t S, M;
       uint16_t code[VG];
-      quant_group(x, 1, VG, mn, mx, 3, false, &S, &M, code);
+      quant_group(x, 1, VG, mn, mx, (1 << vw) - 1, false, &S, &M, code);
       wr16(blob + lay.vs, vmeta_pos(g, t), S);
       wr16(blob + lay.vm, vmeta_pos(g, t), M);
-      for (int i = 0; i < VG; ++i) put2(vbase, val_pos(t, g * VG + i), code[i]);
+      for (int i = 0; i < VG; ++i) putb(vbase, vpos(vw, t, g * VG + i), code[i], vw);
     }
   }
 }
@@ -433,8 +449,8 @@ void encode_blob(const float* xk, const float* xv, const PageStats& st, const bo
 // Quantize one page-head from fp32 token-major tiles xk, xv [32][D].  In
 // running mode the (sequence, head) accumulators are updated with this page's
 // sums before it is ranked; in page mode the page ranks on its own 32 tokens.
-int quantize_one(const float* xk, const float* xv, int n_hi, int w, int running, float* rsum,
-                 float* rsq, int* rcount, uint8_t* blob) {
+int quantize_one(const float* xk, const float* xv, int n_hi, int w, int vw, int running,
+                 float* rsum, float* rsq, int* rcount, uint8_t* blob) {
   int st = check_range(xk, P * D);
   if (st == ST_OK) st = check_range(xv, P * D);
   PageStats ps;
@@ -453,7 +469,7 @@ int quantize_one(const float* xk, const float* xv, int n_hi, int w, int running,
   }
   bool boosted[D];
   top_k(var, n_hi, boosted);
-  encode_blob(xk, xv, ps, boosted, n_hi, w, blob);
+  encode_blob(xk, xv, ps, boosted, n_hi, w, vw, blob);
   return st;
 }
 
@@ -463,8 +479,8 @@ int quantize_one(const float* xk, const float* xv, int n_hi, int w, int running,
 // accumulators end with the sequence totals (page sums added in page order).
 // xk_pages/xv_pages: the pages' fp32 tiles in order; blobs: one per page.
 int quantize_sequence(const std::vector<std::vector<float>>& xk_pages,
-                      const std::vector<std::vector<float>>& xv_pages, int n_hi, int w, float* rsum,
-                      float* rsq, int* rcount, const std::vector<uint8_t*>& blobs) {
+                      const std::vector<std::vector<float>>& xv_pages, int n_hi, int w, int vw,
+                      float* rsum, float* rsq, int* rcount, const std::vector<uint8_t*>& blobs) {
   int st = ST_OK;
   std::vector<PageStats> ps(xk_pages.size());
   for (size_t p = 0; p < xk_pages.size(); ++p) {
@@ -483,7 +499,7 @@ int quantize_sequence(const std::vector<std::vector<float>>& xk_pages,
   bool boosted[D];
   top_k(var, n_hi, boosted);
   for (size_t p = 0; p < xk_pages.size(); ++p)
-    encode_blob(xk_pages[p].data(), xv_pages[p].data(), ps[p], boosted, n_hi, w, blobs[p]);
+    encode_blob(xk_pages[p].data(), xv_pages[p].data(), ps[p], boosted, n_hi, w, vw, blobs[p]);
   return st;
 }
 
@@ -495,8 +511,8 @@ namespace {
 // Dequantize one page-head in fp64: k = M + S*hi + [boosted]*(S/2^w)*lo and
 // v = M + S*code, per the page format above.  Returns ST_BAD_PAGE if the
 // channel list is not a strictly ascending list of valid channel ids.
-int dequant(const uint8_t* blob, int n_hi, int w, double* kh, double* vh) {
-  const Layout lay(n_hi, w);
+int dequant(const uint8_t* blob, int n_hi, int w, int vw, double* kh, double* vh) {
+  const Layout lay(n_hi, w, vw);
   int row_of[D];
   for (int c = 0; c < D; ++c) row_of[c] = -1;
   int prev = -1;
@@ -522,13 +538,13 @@ int dequant(const uint8_t* blob, int n_hi, int w, double* kh, double* vh) {
       const int g = c / VG;
       const double S = f16_to_f32(rd16(blob + lay.vs, vmeta_pos(g, t)));
       const double M = f16_to_f32(rd16(blob + lay.vm, vmeta_pos(g, t)));
-      vh[t * D + c] = M + S * (double)get2(blob + lay.vbase, val_pos(t, c));
+      vh[t * D + c] = M + S * (double)getb(blob + lay.vbase, vpos(vw, t, c), vw);
     }
   return ST_OK;
 }
 
 struct AttnArgs {
-  int Hkv, Hq, n_hi, w, in_dtype;
+  int Hkv, Hq, n_hi, w, vw, in_dtype;
   const uint16_t* q;
   const uint8_t* pool;
   int pool_pages;
@@ -547,7 +563,7 @@ struct AttnArgs {
 // throughout.  out has g*D entries.
 int attend_group(const AttnArgs& a, int b, int kvh, double* out) {
   const int g = a.Hq / a.Hkv;
-  const Layout lay(a.n_hi, a.w);
+  const Layout lay(a.n_hi, a.w, a.vw);
   const size_t page_stride = lay.bytes * (size_t)a.Hkv;
   const int np = a.num_pages[b];
   const int tl = a.tail_len[b];
@@ -560,7 +576,7 @@ int attend_group(const AttnArgs& a, int b, int kvh, double* out) {
     const int id = a.block_table[(size_t)b * a.max_pages + p];
     if (id < 0 || id >= a.pool_pages) return ST_BAD_PAGE;
     const uint8_t* blob = a.pool + (size_t)id * page_stride + (size_t)kvh * lay.bytes;
-    const int st = dequant(blob, a.n_hi, a.w, &kh[(size_t)p * P * D], &vh[(size_t)p * P * D]);
+    const int st = dequant(blob, a.n_hi, a.w, a.vw, &kh[(size_t)p * P * D], &vh[(size_t)p * P * D]);
     if (st != ST_OK) return st;
   }
   const size_t tail_base = ((size_t)b * a.Hkv + kvh) * P * D;
@@ -593,8 +609,9 @@ int attend_group(const AttnArgs& a, int b, int kvh, double* out) {
 }
 
 bool valid_n_hi(int n_hi) { return n_hi >= 0 && n_hi <= D && n_hi % 16 == 0; }
-// Key plane width: lo_bit 2 ((hi, lo) = (4, 2)) or 4 ((8, 4)).
-bool valid_w(int w) { return w == 2 || w == 4; }
+// Key plane width: lo_bit 2 ((hi, lo) = (4, 2)) or 4 ((8, 4)); Value width:
+// 2, or 4 with 4-bit Key planes.
+bool valid_w(int w, int vw) { return (w == 2 || w == 4) && (vw == 2 || (vw == 4 && w == 4)); }
 
 }  // namespace
 
@@ -605,9 +622,9 @@ int orc_abi_version() { return 1; }
 
 void orc_set_threads(int n) { g_threads = n < 1 ? 1 : n; }
 
-// Bytes of one (page, kv-head) blob; -1 for an unsupported n_hi or lo_bit.
-long orc_page_bytes(int n_hi, int lo_bit) {
-  return valid_n_hi(n_hi) && valid_w(lo_bit) ? (long)Layout(n_hi, lo_bit).bytes : -1;
+// Bytes of one (page, kv-head) blob; -1 for an unsupported n_hi, lo_bit or v_bit.
+long orc_page_bytes(int n_hi, int lo_bit, int v_bit) {
+  return valid_n_hi(n_hi) && valid_w(lo_bit, v_bit) ? (long)Layout(n_hi, lo_bit, v_bit).bytes : -1;
 }
 
 // Effective Key bits per element, codes only (VeloxQuant-MLX docs, Effective
@@ -647,17 +664,23 @@ void orc_val_pos(int t, int c, int* word, int* bit) {
   *bit = p.bit;
 }
 
+void orc_val_pos4(int t, int c, int* word, int* bit) {
+  const BitPos p = val_pos4(t, c);
+  *word = p.word;
+  *bit = p.bit;
+}
+
 // One page-head from fp32 tiles [32][D] (token-major).  running != 0 updates
 // rsum/rsq [D] and *rcount before ranking.  Returns a status code.
 int orc_quantize_page_f32(const float* xk, const float* xv, int n_hi, int running, float* rsum,
-                          float* rsq, int* rcount, uint8_t* blob, int lo_bit) {
-  if (!valid_n_hi(n_hi) || !valid_w(lo_bit)) return -1;
-  return quantize_one(xk, xv, n_hi, lo_bit, running, rsum, rsq, rcount, blob);
+                          float* rsq, int* rcount, uint8_t* blob, int lo_bit, int v_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit, v_bit)) return -1;
+  return quantize_one(xk, xv, n_hi, lo_bit, v_bit, running, rsum, rsq, rcount, blob);
 }
 
 // The boosted channel list of a blob in row order (ascending channel ids).
 void orc_page_channels(const uint8_t* blob, int n_hi, int* out, int lo_bit) {
-  const Layout lay(n_hi, lo_bit);
+  const Layout lay(n_hi, lo_bit, 2);  // the list precedes the Value plane
   for (int j = 0; j < n_hi; ++j) out[j] = blob[lay.kch + kch_pos(j)];
 }
 
@@ -666,8 +689,9 @@ void orc_meta_pos(int kind, int a, int b, int* pos) {
 }
 
 void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int* status,
-                      int lo_bit) {
-  *status = valid_n_hi(n_hi) && valid_w(lo_bit) ? dequant(blob, n_hi, lo_bit, kh, vh) : -1;
+                      int lo_bit, int v_bit) {
+  *status = valid_n_hi(n_hi) && valid_w(lo_bit, v_bit) ? dequant(blob, n_hi, lo_bit, v_bit, kh, vh)
+                                                       : -1;
 }
 
 // Bulk quantization with the library's semantics.  k, v: [n_pages*32][Hkv][D]
@@ -679,10 +703,10 @@ void orc_dequant_page(const uint8_t* blob, int n_hi, double* kh, double* vh, int
 int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint16_t* k,
                        const uint16_t* v, int n_pages, const int* page_ids, const int* seq_of_page,
                        int n_seqs, float* run_sum, float* run_sumsq, int* run_count, uint8_t* pool,
-                       int pool_pages, int lo_bit) {
-  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || n_pages < 0) return -1;
-  const int w = lo_bit;
-  const Layout lay(n_hi, w);
+                       int pool_pages, int lo_bit, int v_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit, v_bit) || Hkv <= 0 || n_pages < 0) return -1;
+  const int w = lo_bit, vw = v_bit;
+  const Layout lay(n_hi, w, vw);
   const size_t page_stride = lay.bytes * (size_t)Hkv;
   int st = ST_OK;
   if (rank_mode == 1 || rank_mode == 2) {
@@ -719,7 +743,8 @@ int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uin
       }
       if (xk.empty()) { sts2[sh] = bad; return; }
       const size_t o = (size_t)sq * Hkv + h;
-      int r = quantize_sequence(xk, xv, n_hi, w, run_sum + o * D, run_sumsq + o * D, run_count + o, blobs);
+      int r = quantize_sequence(xk, xv, n_hi, w, vw, run_sum + o * D, run_sumsq + o * D,
+                                run_count + o, blobs);
       sts2[sh] = r != ST_OK ? r : bad;
     });
     for (int x : sts2) note(&st, x);
@@ -745,8 +770,8 @@ int orc_quantize_pages(int Hkv, int n_hi, int rank_mode, int in_dtype, const uin
       rq = run_sumsq + sh * D;
       rc = run_count + sh;
     }
-    sts[(size_t)i * Hkv + h] = quantize_one(xk.data(), xv.data(), n_hi, w, rank_mode == 1, rs, rq, rc,
-                                            pool + (size_t)id * page_stride + (size_t)h * lay.bytes);
+    sts[(size_t)i * Hkv + h] = quantize_one(xk.data(), xv.data(), n_hi, w, vw, rank_mode == 1, rs, rq,
+                                            rc, pool + (size_t)id * page_stride + (size_t)h * lay.bytes);
   };
   if (rank_mode == 1) {
     // Each head's accumulators see that head's pages strictly in input order.
@@ -770,9 +795,9 @@ int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint1
                      const uint16_t* v_new, uint16_t* tail_k, uint16_t* tail_v, int* tail_len,
                      float* run_sum, float* run_sumsq, int* run_count, const int* flush_page_ids,
                      int* block_table, int max_pages, int* num_pages, uint8_t* pool, int pool_pages,
-                     int B, int lo_bit) {
-  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || B < 0) return -1;
-  const Layout lay(n_hi, lo_bit);
+                     int B, int lo_bit, int v_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit, v_bit) || Hkv <= 0 || B < 0) return -1;
+  const Layout lay(n_hi, lo_bit, v_bit);
   const size_t page_stride = lay.bytes * (size_t)Hkv;
   std::vector<int> sts(B > 0 ? B : 1, ST_OK);
   parallel_for(B, [&](int b) {
@@ -804,7 +829,8 @@ int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint1
       }
       const size_t sh = (size_t)b * Hkv + h;
       const bool running = rank_mode != 0;  // sequence mode continues with running statistics
-      note(&st, quantize_one(xk.data(), xv.data(), n_hi, lo_bit, running, running ? run_sum + sh * D : nullptr,
+      note(&st, quantize_one(xk.data(), xv.data(), n_hi, lo_bit, v_bit, running,
+                             running ? run_sum + sh * D : nullptr,
                              running ? run_sumsq + sh * D : nullptr, running ? run_count + sh : nullptr,
                              pool + (size_t)fid * page_stride + (size_t)h * lay.bytes));
     }
@@ -823,10 +849,12 @@ int orc_append_token(int Hkv, int n_hi, int rank_mode, int in_dtype, const uint1
 int orc_decode_attention(int Hkv, int Hq, int n_hi, int in_dtype, const uint16_t* q,
                          const uint8_t* pool, int pool_pages, const int* block_table, int max_pages,
                          const int* num_pages, const uint16_t* tail_k, const uint16_t* tail_v,
-                         const int* tail_len, float sm_scale, int B, double* out, int lo_bit) {
-  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B < 0) return -1;
-  const AttnArgs a{Hkv, Hq, n_hi, lo_bit, in_dtype, q, pool, pool_pages, block_table, max_pages,
-                   num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
+                         const int* tail_len, float sm_scale, int B, double* out, int lo_bit,
+                         int v_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit, v_bit) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0 || B < 0)
+    return -1;
+  const AttnArgs a{Hkv, Hq, n_hi, lo_bit, v_bit, in_dtype, q, pool, pool_pages, block_table,
+                   max_pages, num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
   const int g = Hq / Hkv;
   std::vector<int> sts(B > 0 ? (size_t)B * Hkv : 1, ST_OK);
   parallel_for(B * Hkv, [&](int i) {
@@ -898,10 +926,10 @@ int orc_decode_attention_one(int Hkv, int Hq, int n_hi, int in_dtype, const uint
                              const uint8_t* pool, int pool_pages, const int* block_table,
                              int max_pages, const int* num_pages, const uint16_t* tail_k,
                              const uint16_t* tail_v, const int* tail_len, float sm_scale, int b,
-                             int kvh, double* out, int lo_bit) {
-  if (!valid_n_hi(n_hi) || !valid_w(lo_bit) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return -1;
-  const AttnArgs a{Hkv, Hq, n_hi, lo_bit, in_dtype, q, pool, pool_pages, block_table, max_pages,
-                   num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
+                             int kvh, double* out, int lo_bit, int v_bit) {
+  if (!valid_n_hi(n_hi) || !valid_w(lo_bit, v_bit) || Hkv <= 0 || Hq <= 0 || Hq % Hkv != 0) return -1;
+  const AttnArgs a{Hkv, Hq, n_hi, lo_bit, v_bit, in_dtype, q, pool, pool_pages, block_table,
+                   max_pages, num_pages, tail_k, tail_v, tail_len, (double)sm_scale};
   return attend_group(a, b, kvh, out);
 }
 

@@ -12,7 +12,8 @@ Metric: decode tokens/s = sequences x steps / time; HBM GB/s of the decode
 kernel on algorithmic bytes (packed pages + tails + Q + O + block table).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kitty|reference]
-                       [--workload budget|budget_uniform|budget_k4|budget_84|llama3_8b|qwen3_8b|qwen3_g1|qwen3_g2|long|tiny]
+                       [--workload budget|budget_uniform|budget_k4|budget_84|budget_kv4|budget_fp16|
+                                   llama3_8b|qwen3_8b|qwen3_g1|qwen3_g2|long|tiny]
 """
 
 from __future__ import annotations
@@ -59,16 +60,19 @@ def workload_spec(name: str, steps_total: int):
         return dict(name=name, B=int(B), Hq=Hq, Hkv=Hkv, n_hi=0, layers=layers, running=False,
                     pages=np.full(B, ctx_pages, np.int64), tails=tails, drift=0,
                     budget_bytes=40 * 10 ** 9, dtype=synth.BF16, lo_bit=2, f16kv=True)
-    if name in ("budget", "budget_uniform", "budget_k4", "budget_84"):
+    if name in ("budget", "budget_uniform", "budget_k4", "budget_84", "budget_kv4"):
         # budget: Kitty (top 32 of 128 Key channels at 4 bits, running statistics);
         # budget_uniform: every Key channel at 2 bits; budget_k4: every Key channel
         # at 4 bits (n_hi = 128, two 2-bit planes); budget_84: Kitty at (8, 4) bits
         # (top 32 channels at 8 bits, the rest at 4, two 4-bit planes, running
-        # statistics).  Values are 2-bit in all four.
-        n_hi = {"budget": 32, "budget_uniform": 0, "budget_k4": 128, "budget_84": 32}[name]
-        lo_bit = 4 if name == "budget_84" else 2
+        # statistics).  Values are 2-bit in these four.  budget_kv4: uniform 4-bit
+        # KV (every Key channel at 4 bits in one 4-bit plane, 4-bit Values).
+        n_hi = {"budget": 32, "budget_uniform": 0, "budget_k4": 128, "budget_84": 32,
+                "budget_kv4": 0}[name]
+        lo_bit = 4 if name in ("budget_84", "budget_kv4") else 2
+        v_bit = 4 if name == "budget_kv4" else 2
         running = name in ("budget", "budget_84")
-        blob = 512 * lo_bit + 4 * lo_bit * n_hi + 2048 + n_hi
+        blob = 512 * lo_bit + 4 * lo_bit * n_hi + n_hi + 512 * v_bit + 1024
         Hkv, Hq, layers, ctx_pages = 8, 32, 32, 256
         stat = Hkv * D * 2 * 4 + Hkv * 4 if running else 0
         tail_bytes = 2 * Hkv * PAGE * D * 2
@@ -76,15 +80,17 @@ def workload_spec(name: str, steps_total: int):
         tails = (synth.bits(0, "budget/tail", B) % np.uint64(32)).astype(np.int64)
         return dict(name=name, B=int(B), Hq=Hq, Hkv=Hkv, n_hi=n_hi, layers=layers,
                     running=running, pages=np.full(B, ctx_pages, np.int64), tails=tails,
-                    drift=0, budget_bytes=40 * 10 ** 9, dtype=synth.BF16, lo_bit=lo_bit)
+                    drift=0, budget_bytes=40 * 10 ** 9, dtype=synth.BF16, lo_bit=lo_bit,
+                    v_bit=v_bit)
     w = synth.workload(name)
     # independent layer copies, rotated every step, so the working set exceeds 4x L2
-    pool = w.total_pages * w.Hkv * (512 * w.lo_bit + 4 * w.lo_bit * w.n_hi + 2048 + w.n_hi)
+    pool = w.total_pages * w.Hkv * (512 * w.lo_bit + 4 * w.lo_bit * w.n_hi + w.n_hi
+                                    + 512 * w.v_bit + 1024)
     # (the tiny single-head case is latency-bound and stays L2-resident by design)
     layers = 1 if name == "tiny" else max(1, math.ceil(4 * 129e6 / max(pool, 1)))
     return dict(name=name, B=w.B, Hq=w.Hq, Hkv=w.Hkv, n_hi=w.n_hi, layers=layers, running=False,
                 pages=w.pages.astype(np.int64), tails=w.tails.astype(np.int64), drift=w.drift,
-                budget_bytes=None, dtype=w.dtype, lo_bit=w.lo_bit)
+                budget_bytes=None, dtype=w.dtype, lo_bit=w.lo_bit, v_bit=w.v_bit)
 
 
 def headroom_pages(tails, steps_total):
@@ -185,6 +191,7 @@ def build_layers(spec, steps_total, seed=0, keep=(), pages_per_split=0):
     pool_pages = int(pages.sum()) + B * head
     cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
                        in_dtype=spec["dtype"], hi_bit=2 * spec["lo_bit"], lo_bit=spec["lo_bit"],
+                       v_bit=spec.get("v_bit", 2),
                        rank_mode=kitty.RANK_RUNNING if spec["running"] else kitty.RANK_PAGE,
                        decode_pages_per_split=pages_per_split)
     tdt = torch.float16 if spec["dtype"] == kitty.F16 else torch.bfloat16
@@ -257,7 +264,7 @@ def measure_quantize(spec, reps=5, seed=3):
     for mode in (kitty.RANK_PAGE, kitty.RANK_RUNNING):
         cfg = kitty.Config(num_kv_heads=Hkv, num_q_heads=spec["Hq"], n_hi=spec["n_hi"],
                            in_dtype=spec["dtype"], rank_mode=mode, hi_bit=2 * spec["lo_bit"],
-                           lo_bit=spec["lo_bit"])
+                           lo_bit=spec["lo_bit"], v_bit=spec.get("v_bit", 2))
         blob, per_page = kitty.page_bytes(cfg)
         pool = torch.empty(tot * per_page, dtype=torch.uint8, device="cuda")
         run = {}
@@ -506,7 +513,8 @@ class OracleSample:
         v = synth.to_bits(synth.host_fast_normal(seed + 2, (tot * PAGE, Hkv, D)), spec["dtype"])
         self.max_pages = int(pages.max()) + 4
         self.pool_pages = tot + 4 * S
-        self.pool = np.zeros(self.pool_pages * Hkv * oracle.page_bytes(n_hi), np.uint8)
+        self.fmt = dict(lo_bit=spec["lo_bit"], v_bit=spec.get("v_bit", 2))
+        self.pool = np.zeros(self.pool_pages * Hkv * oracle.page_bytes(n_hi, **self.fmt), np.uint8)
         ids = np.arange(tot, dtype=np.int32)
         self.bt = np.full((S, self.max_pages), -1, np.int32)
         off = 0
@@ -519,7 +527,8 @@ class OracleSample:
         oracle.set_threads(host_cores())
         st = oracle.quantize_pages(Hkv, n_hi, self.mode, spec["dtype"], k, v, ids, self.pool,
                                    self.pool_pages, seq_of_page=np.repeat(np.arange(S), pages),
-                                   n_seqs=S, run_sum=self.rs, run_sumsq=self.rq, run_count=self.rc)
+                                   n_seqs=S, run_sum=self.rs, run_sumsq=self.rq, run_count=self.rc,
+                                   **self.fmt)
         assert st == 0, st
         self.tk = synth.to_bits(synth.host_fast_normal(seed + 3, (S, Hkv, PAGE, D)), spec["dtype"])
         self.tv = synth.to_bits(synth.host_fast_normal(seed + 4, (S, Hkv, PAGE, D)), spec["dtype"])
@@ -540,10 +549,10 @@ class OracleSample:
                 self.next_id += 1
         st = self.o.append_token(spec["Hkv"], spec["n_hi"], self.mode, spec["dtype"], self.kn, self.kn,
                                  self.tk, self.tv, self.tl, self.rs, self.rq, self.rc, fl, self.bt,
-                                 self.max_pages, self.np_, self.pool, self.pool_pages)
+                                 self.max_pages, self.np_, self.pool, self.pool_pages, **self.fmt)
         _, st2 = self.o.decode_attention(spec["Hkv"], spec["Hq"], spec["n_hi"], spec["dtype"], self.q,
                                          self.pool, self.pool_pages, self.bt, self.np_, self.tk,
-                                         self.tv, self.tl, 1.0 / math.sqrt(D))
+                                         self.tv, self.tl, 1.0 / math.sqrt(D), **self.fmt)
         assert st in (0,) and st2 in (0,), (st, st2)
 
 
@@ -606,6 +615,7 @@ def config_block(spec, extra=None):
          "batch": spec["B"], "layers": spec["layers"], "q_heads": spec["Hq"], "kv_heads": spec["Hkv"],
          "head_dim": D, "page_tokens": PAGE, "n_hi": spec["n_hi"],
          "key_bits": "(hi, lo) = (%d, %d)" % (2 * spec["lo_bit"], spec["lo_bit"]),
+         "value_bits": spec.get("v_bit", 2) if not spec.get("f16kv") else 16,
          "rank_mode": "running" if spec["running"] else "page",
          "context_pages": int(spec["pages"].max()), "kv_budget_bytes": spec["budget_bytes"],
          "l2": ("L2-resident (latency-bound tiny case, no roofline claim)" if spec["name"] == "tiny"
@@ -623,8 +633,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", default="kitty", choices=["kitty", "reference"])
     ap.add_argument("--workload", default="budget",
-                    choices=["budget", "budget_uniform", "budget_k4", "budget_84", "budget_fp16", "llama3_8b",
-                             "qwen3_8b", "qwen3_g1", "qwen3_g2", "long", "tiny"])
+                    choices=["budget", "budget_uniform", "budget_k4", "budget_84", "budget_kv4",
+                             "budget_fp16", "llama3_8b", "qwen3_8b", "qwen3_g1", "qwen3_g2", "long",
+                             "tiny"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")

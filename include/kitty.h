@@ -3,7 +3,8 @@
  * Kitty keeps a paged KV cache at ~2 bits per element.  Key pages rank their
  * channels by variance and store the top n_hi at 4 bits, split into two 2-bit
  * planes, so every Key page is two uniform 2-bit tensors plus a channel list;
- * Values use 2-bit per-token groups of 32 channels.  Decode attention reads the
+ * Values use 2-bit per-token groups of 32 channels (4-bit as an option, for the
+ * uniform 4-bit KV comparison layout).  Decode attention reads the
  * packed pages through a block table and dequantizes them in registers.
  *
  * Sources: "Kitty: Accurate and Efficient 2-bit KV Cache Quantization with
@@ -109,22 +110,31 @@ typedef struct {
                                    then undefined.  A small value makes ordinary
                                    copies outlast the wait, which is how the
                                    timeout path is tested */
+  int32_t v_bit;                  /* Value code width: 2 (0 = 2) or 4.  4-bit
+                                   Values need lo_bit = 4; with n_hi = 0 that
+                                   is a uniform 4-bit KV cache (per-channel
+                                   4-bit Keys, per-token 4-bit Value groups),
+                                   the accuracy-preserving point the paper's
+                                   Abstract names ("4-bit KV quantization") */
 } kitty_cfg;
 
-/* Library ABI version (this header: 4; kitty_cfg gained decode_total_pages in
- * version 2, decode_max_pages in version 3 and decode_wait_polls in version 4). */
+/* Library ABI version (this header: 5; kitty_cfg gained decode_total_pages in
+ * version 2, decode_max_pages in version 3, decode_wait_polls in version 4 and
+ * v_bit in version 5). */
 int kitty_abi_version(void);
 
 /* Packed page size.  A page holds Hkv blobs, one per kv head, in head order;
  * physical page p starts at byte p * per_page of the pool.  Blob of one
- * (page, kv head), in order, with w = lo_bit: Key base plane 512*w B, Key extra
- * plane 4*w*n_hi B, Key step fp16[128], Key minimum fp16[128], channel list
- * uint8[n_hi] (ascending), Value plane 1024 B, Value step fp16[4][32], Value
- * minimum fp16[4][32] (group-major).  = 3072 + 9*n_hi bytes at (4, 2) (3360 at
- * n_hi=32), 4096 + 17*n_hi at (8, 4).  Inside the planes, codes sit in
- * "fragment order": the 32 bytes at offset 32*L of a 2-bit plane hold what lane
- * L of a warp takes as its tensor-core operand fragments (the oracle's key_pos,
- * key_pos4 and val_pos index functions spell the maps out).  Paper: Abstract
+ * (page, kv head), in order, with w = lo_bit and v = v_bit: Key base plane
+ * 512*w B, Key extra plane 4*w*n_hi B, Key step fp16[128], Key minimum
+ * fp16[128], channel list uint8[n_hi] (ascending), Value plane 512*v B, Value
+ * step fp16[4][32], Value minimum fp16[4][32] (group-major).  = 3072 + 9*n_hi
+ * bytes at (4, 2) (3360 at n_hi=32), 4096 + 17*n_hi at (8, 4), 5120 + 17*n_hi
+ * at (8, 4) with 4-bit Values.  Inside the planes, codes sit in "fragment
+ * order": the 32*w (Keys) or 32*v (Values) bytes at offset 32*w*L (32*v*L) of
+ * a plane hold what lane L of a warp takes as its tensor-core operand
+ * fragments (the oracle's key_pos, key_pos4, val_pos and val_pos4 index
+ * functions spell the maps out).  Paper: Abstract
  * (page-centric layout, two uniform 2-bit tensors per Key page). */
 int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page);
 

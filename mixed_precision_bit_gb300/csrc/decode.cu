@@ -202,13 +202,20 @@ __device__ __forceinline__ void store_out(void* out, int dt, size_t i, float v) 
   else static_cast<__half*>(out)[i] = __float2half_rn(v);
 }
 
-// Compile-time blob offsets for NX = n_hi/16 extra-plane k-steps and Key plane
-// width W (2: (4, 2) configuration, 4: (8, 4)).
-template <int NX, int W>
+// Compile-time blob offsets for NX = n_hi/16 extra-plane k-steps, Key plane
+// width W (2: (4, 2) configuration, 4: (8, 4)) and Value code width V (2 or 4).
+template <int NX, int W, int V>
 struct Off {
   static constexpr int kx = 512 * W, ks = kx + 64 * W * NX, km = ks + 256, kch = km + 256;
-  static constexpr int vb = kch + 16 * NX, vs = vb + 1024, vm = vs + 256, bytes = vm + 256;
+  static constexpr int vb = kch + 16 * NX, vs = vb + 512 * V, vm = vs + 256, bytes = vm + 256;
 };
+
+// Power of two (exponent + 24) that an unpacked Value code of channel-tile row
+// (m-tile mc, 8-row half rh) carries: 2-bit planes place rows at bit 2*tau
+// (tau = 2*(mc & 1) + rh), 4-bit planes at bit 4*rh.
+__host__ __device__ constexpr int vrow_exp(int V, int mc, int rh) {
+  return V == 4 ? 4 * rh : 2 * (2 * (mc & 1) + rh);
+}
 
 // Lane roles.  Thread (r = lane/4, qq = lane%4) owns head qq in the C
 // fragments (column 2qq = high part, 2qq+1 = low part) and, as a B-fragment
@@ -267,12 +274,12 @@ __device__ __forceinline__ void unpack_rows23(uint32_t x, uint32_t* a) {  // tau
 //                the low part (column parity) of the query of head lane/8
 //   qxa: shared-space address of the same part of q/2^W of head lane/8, in
 //        channel order (extra-plane gather)
-template <int NX, int W>
+template <int NX, int W, int V>
 __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&qf)[8][2],
                                             const uint32_t qxa, const Lane& L,
                                             const float (&kscale)[4], float beta,
                                             float (&s)[4]) {
-  using O = Off<NX, W>;
+  using O = Off<NX, W, V>;
   const int lane = L.lane, qq = L.qq;
   const uint32_t a_lane = pa + 4 * W * 4 * lane;  // this lane's 16*W bytes of the base plane
   const uint32_t a_qq = pa + 4 * qq;              // this lane's fp16 pair in each 16-wide group
@@ -364,11 +371,11 @@ __device__ __forceinline__ void page_scores(const uint32_t pa, const uint32_t (&
 // split query (the same for every page), whose two columns of a head add up to
 // q.M; A rows r even carry page A's Key minima and odd rows page B's; each lane
 // reads its own row and its neighbour's.
-template <int NX, int W>
+template <int NX, int W, int V>
 __device__ __forceinline__ void pair_beta(const uint32_t paA, const uint32_t paB,
                                           const uint32_t (&qf)[8][2], const Lane& L,
                                           float sm_log2, float& bA, float& bB) {
-  using O = Off<NX, W>;
+  using O = Off<NX, W, V>;
   // this lane's 16 minima pairs are contiguous (fragment order): 4 x 16 bytes
   const uint32_t a_m = ((L.r & 1) ? paB : paA) + 64 * L.qq;
   const uint4 m0 = ld_s128<O::km>(a_m), m1 = ld_s128<O::km + 16>(a_m);
@@ -401,10 +408,10 @@ __device__ __forceinline__ void page_probs(WarpState& w, const float (&s)[4], ui
 }
 
 // Value minima term and PV of one page with its probability fragments T.
-template <int NX, int W>
+template <int NX, int W, int V>
 __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const uint32_t (&T)[4],
                                         const Lane& L) {
-  using O = Off<NX, W>;
+  using O = Off<NX, W, V>;
   const int lane = L.lane, r = L.r, qq = L.qq;
   const uint32_t a_lane = pa + 32 * lane;
   const uint32_t a_q16 = pa + 16 * qq;  // this lane group's Value steps (fragment order)
@@ -420,12 +427,18 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
   // ---------------- PV with the Value step folded into this lane's part of P
   // (high part: exact product; the rest: rounded once, relative 2^-12 of a
   // term below 2^-3 of p)
+  // 2-bit Values: a lane's 8 bytes of group G are words (kt = 0, 1), each
+  // holding both m-tiles; 4-bit Values: its 16 bytes are words (kt, m-tile
+  // parity), each one A fragment
+  const uint32_t a_lane4 = pa + 64 * lane;
 #pragma unroll
   for (int G = 0; G < 4; ++G) {
-    uint2 vv;
+    uint4 vv;
     uint32_t S[4];
     switch (G) {
-#define KITTY_VG(J) case J: { vv = ld_s64<O::vb + 8 * J>(a_lane); \
+#define KITTY_VG(J) case J: { if (V == 4) { vv = ld_s128<O::vb + 16 * J>(a_lane4); } \
+                            else { const uint2 v2 = ld_s64<O::vb + 8 * J>(a_lane); \
+                                   vv = make_uint4(v2.x, v2.y, 0u, 0u); } \
                             const uint4 sv = ld_s128<O::vs + 64 * J>(a_q16); \
                             S[0] = sv.x; S[1] = sv.y; S[2] = sv.z; S[3] = sv.w; } break;
       KITTY_VG(0) KITTY_VG(1) KITTY_VG(2) default: KITTY_VG(3)
@@ -439,12 +452,19 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
         const int i = 2 * kt + k;
         bg[k] = hmul2u(T[i], S[i]);
       }
-      const uint32_t x = kt ? vv.y : vv.x;
       uint32_t a[4];
-      unpack_rows01(x, a);
-      mma_f16(w.acc[2 * G], a, bg[0], bg[1]);
-      unpack_rows23(x, a);
-      mma_f16(w.acc[2 * G + 1], a, bg[0], bg[1]);
+      if (V == 4) {
+        unpack_nib(kt ? vv.z : vv.x, a);
+        mma_f16(w.acc[2 * G], a, bg[0], bg[1]);
+        unpack_nib(kt ? vv.w : vv.y, a);
+        mma_f16(w.acc[2 * G + 1], a, bg[0], bg[1]);
+      } else {
+        const uint32_t x = kt ? vv.y : vv.x;
+        unpack_rows01(x, a);
+        mma_f16(w.acc[2 * G], a, bg[0], bg[1]);
+        unpack_rows23(x, a);
+        mma_f16(w.acc[2 * G + 1], a, bg[0], bg[1]);
+      }
     }
   }
 }
@@ -458,7 +478,7 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
 // covers them all.  The V rows pass through the warp's idle stage buffer to
 // reach the accumulator layout, and carry the same per-row power of two as the
 // paged codes.
-template <int DT>
+template <int DT, int V>
 __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* qs, int b, int kvh,
                             int tl, int wid, const Lane& L, uint8_t* vbuf) {
   const int lane = L.lane, r = L.r, qq = L.qq;
@@ -520,7 +540,7 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
         const int c = 16 * mc + 8 * rh;
-        const float rs = __uint_as_float((uint32_t)(127 - 24 + 2 * (2 * (mc & 1) + rh)) << 23);
+        const float rs = __uint_as_float((uint32_t)(127 - 24 + vrow_exp(V, mc, rh)) << 23);
         w.acc[mc][2 * rh] += pi * (bits16_to_f32(ld_s16r(vb + i * 2 * kD + 2 * c), DT) * rs);
       }
   }
@@ -530,7 +550,7 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
 // page quantizer (running statistics updated in running mode), staging through
 // sm.  Not inlined: it runs on a flush only (one call in 32 per sequence) and
 // keeps its registers out of the attention loop.  Called by all 128 threads.
-template <int DT, int W>
+template <int DT, int W, int V>
 __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, size_t sh, int fid,
                                         int kvh, int Hkv, int n_hi, int32_t* d_status) {
   const int c = threadIdx.x;
@@ -541,8 +561,8 @@ __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, si
     rq = ap.run_sumsq[sh * kD + c];
     rc = ap.run_count[sh];
   }
-  const BlobLayout lay(n_hi, W);
-  quantize_tile<DT, W>(*sm, ap.tail_k + sh * kPage * kD, ap.tail_v + sh * kPage * kD, kD, n_hi,
+  const BlobLayout lay(n_hi, W, V);
+  quantize_tile<DT, W, V>(*sm, ap.tail_k + sh * kPage * kD, ap.tail_v + sh * kPage * kD, kD, n_hi,
                     ap.running != 0, rs, rq, rc, ap.pool + ((size_t)fid * Hkv + kvh) * lay.bytes,
                     d_status);
   if (ap.running) {
@@ -552,7 +572,7 @@ __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, si
   }
 }
 
-template <int DT, int NX, int W>
+template <int DT, int NX, int W, int V>
 __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
   trigger_dependents();  // the combine step may be scheduled once every CTA is running
@@ -561,7 +581,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   const int tid = threadIdx.x, wid = tid >> 5;
   const Lane L;
   const int lane = L.lane, r = L.r, qq = L.qq;
-  constexpr int kBlob = Off<NX, W>::bytes;
+  constexpr int kBlob = Off<NX, W, V>::bytes;
   constexpr int kDStages = stages_for(W);
   const int sbeg = p.starts[s], send = p.starts[s + 1];
   // Independent loads first, all in flight together: the lengths, this warp's
@@ -773,13 +793,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     const uint32_t paA = stage0 + stA * kBlob;
     const uint32_t paB = hasB ? stage0 + stB * kBlob : paA;
     float bA, bB;
-    pair_beta<NX, W>(paA, paB, qf, L, p.sm_log2, bA, bB);
+    pair_beta<NX, W, V>(paA, paB, qf, L, p.sm_log2, bA, bB);
     float sA[4];
-    page_scores<NX, W>(paA, qf, qxa, L, kscale, bA, sA);
+    page_scores<NX, W, V>(paA, qf, qxa, L, kscale, bA, sA);
     if (hasB) {
       const bool vB = (valid_mask >> stB) & 1u;
       float sB[4];
-      page_scores<NX, W>(paB, qf, qxa, L, kscale, bB, sB);
+      page_scores<NX, W, V>(paB, qf, qxa, L, kscale, bB, sB);
       if (!(vA && vB)) {  // a page id was out of range (warp-uniform, rare)
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -796,8 +816,8 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       uint32_t TA[4], TB[4];
       page_probs(w, sA, TA);
       page_probs(w, sB, TB);
-      page_pv<NX, W>(w, paA, TA, L);
-      page_pv<NX, W>(w, paB, TB, L);
+      page_pv<NX, W, V>(w, paA, TA, L);
+      page_pv<NX, W, V>(w, paB, TB, L);
     } else {  // last page of an odd count
 #pragma unroll
       for (int k = 0; k < 4; ++k) sA[k] = vA ? sA[k] : -INFINITY;
@@ -808,7 +828,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       rescale(w, pm);
       uint32_t TA[4];
       page_probs(w, sA, TA);
-      page_pv<NX, W>(w, paA, TA, L);
+      page_pv<NX, W, V>(w, paA, TA, L);
     }
     __syncwarp();
     if (i + kDStages < npw) issue2(i + kDStages);
@@ -819,13 +839,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     // appends at index np
     __syncthreads();
     QuantSmem* qsm = reinterpret_cast<QuantSmem*>(dsm);
-    flush_tail<DT, W>(qsm, p.ap, (size_t)b * p.Hkv + kvh, flush_id, kvh, p.Hkv, p.n_hi, p.d_status);
+    flush_tail<DT, W, V>(qsm, p.ap, (size_t)b * p.Hkv + kvh, flush_id, kvh, p.Hkv, p.n_hi, p.d_status);
     if (wid == 0) {
       const uint32_t pa = smem_u32(qsm->blob);
       float bA, bB;
-      pair_beta<NX, W>(pa, pa, qf, L, p.sm_log2, bA, bB);
+      pair_beta<NX, W, V>(pa, pa, qf, L, p.sm_log2, bA, bB);
       float sA[4];
-      page_scores<NX, W>(pa, qf, qxa, L, kscale, bA, sA);
+      page_scores<NX, W, V>(pa, qf, qxa, L, kscale, bA, sA);
       float pm = fmaxf(fmaxf(sA[0], sA[1]), fmaxf(sA[2], sA[3]));
       pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
       pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
@@ -833,12 +853,12 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
       rescale(w, pm);
       uint32_t TA[4];
       page_probs(w, sA, TA);
-      page_pv<NX, W>(w, pa, TA, L);
+      page_pv<NX, W, V>(w, pa, TA, L);
     }
   }
   // the tail tokens go with the sequence's first split (dispatched earliest);
   // they reuse the stage buffers, which are idle unless a copy timed out
-  if (pbeg == 0 && tl > 0 && !timed_out) tail_tokens<DT>(w, p, qs, b, kvh, tl, wid, L, wst);
+  if (pbeg == 0 && tl > 0 && !timed_out) tail_tokens<DT, V>(w, p, qs, b, kvh, tl, wid, L, wst);
 
   // ---- merge the 4 warps: per-warp (m, l, O) to shared memory, then per channel
   w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 4);
@@ -856,7 +876,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     for (int i = 0; i < 4; ++i) {
       const int rh = i >> 1;
       const int row = 16 * mc + 8 * rh + r;
-      const float sc = __uint_as_float((uint32_t)(127 + 24 - 2 * (2 * (mc & 1) + rh)) << 23);
+      const float sc = __uint_as_float((uint32_t)(127 + 24 - vrow_exp(V, mc, rh)) << 23);
       Ow[row * 8 + 2 * qq + (i & 1)] = w.acc[mc][i] * sc;
     }
   if (r < 4) {
@@ -1012,7 +1032,7 @@ __global__ void finalize_kernel(const DecodeParams p, int B) {
                         p.ap.num_pages, p.pool_pages);
 }
 
-template <int DT, int NX, int W>
+template <int DT, int NX, int W, int V>
 cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
   // the shared-memory opt-in is a per-device function attribute (smem is fixed
   // per instantiation): set it on the first launch on each device only
@@ -1021,27 +1041,27 @@ cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodePa
   if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
   const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
   if (bit == 0 || (opted_in.load() & bit) == 0) {
-    cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, NX, W>,
+    cudaError_t e = cudaFuncSetAttribute(decode_kernel<DT, NX, W, V>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     opted_in.fetch_or(bit);
   }
-  decode_kernel<DT, NX, W><<<grid, kDThreads, smem, s>>>(p);
+  decode_kernel<DT, NX, W, V><<<grid, kDThreads, smem, s>>>(p);
   return cudaGetLastError();
 }
 
-template <int DT, int W>
+template <int DT, int W, int V>
 cudaError_t launch_decode_nx(int nx, dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
   switch (nx) {
-    case 0: return launch_decode<DT, 0, W>(grid, smem, s, p);
-    case 1: return launch_decode<DT, 1, W>(grid, smem, s, p);
-    case 2: return launch_decode<DT, 2, W>(grid, smem, s, p);
-    case 3: return launch_decode<DT, 3, W>(grid, smem, s, p);
-    case 4: return launch_decode<DT, 4, W>(grid, smem, s, p);
-    case 5: return launch_decode<DT, 5, W>(grid, smem, s, p);
-    case 6: return launch_decode<DT, 6, W>(grid, smem, s, p);
-    case 7: return launch_decode<DT, 7, W>(grid, smem, s, p);
-    default: return launch_decode<DT, 8, W>(grid, smem, s, p);
+    case 0: return launch_decode<DT, 0, W, V>(grid, smem, s, p);
+    case 1: return launch_decode<DT, 1, W, V>(grid, smem, s, p);
+    case 2: return launch_decode<DT, 2, W, V>(grid, smem, s, p);
+    case 3: return launch_decode<DT, 3, W, V>(grid, smem, s, p);
+    case 4: return launch_decode<DT, 4, W, V>(grid, smem, s, p);
+    case 5: return launch_decode<DT, 5, W, V>(grid, smem, s, p);
+    case 6: return launch_decode<DT, 6, W, V>(grid, smem, s, p);
+    case 7: return launch_decode<DT, 7, W, V>(grid, smem, s, p);
+    default: return launch_decode<DT, 8, W, V>(grid, smem, s, p);
   }
 }
 
@@ -1169,7 +1189,7 @@ extern "C" int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pa
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !splits || !pages_per_split) return KITTY_ERR_INVALID_ARG;
   Schedule sc;
-  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi, cfg->lo_bit), &sc);
+  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi, cfg->lo_bit, v_bits(cfg)), &sc);
   *splits = sc.splits;
   *pages_per_split = sc.largest;
   return KITTY_OK;
@@ -1181,7 +1201,7 @@ extern "C" int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !bytes) return KITTY_ERR_INVALID_ARG;
   Schedule sc;
-  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi, cfg->lo_bit), &sc);
+  plan(cfg, B, max_pages, (int)blob_bytes(cfg->n_hi, cfg->lo_bit, v_bits(cfg)), &sc);
   *bytes = workspace_bytes(cfg, B, sc);
   return KITTY_OK;
 }
@@ -1206,7 +1226,7 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
       (tail_k && (!aligned16(tail_k) || !aligned16(tail_v))) ||
       (tail_k && !tail_len) || !std::isfinite(sm_scale))
     return KITTY_ERR_INVALID_ARG;
-  const int blob = (int)blob_bytes(cfg->n_hi, cfg->lo_bit);
+  const int blob = (int)blob_bytes(cfg->n_hi, cfg->lo_bit, v_bits(cfg));
   DecodeParams p = {};
   Schedule sc;
   plan(cfg, B, max_pages, blob, &sc);
@@ -1240,11 +1260,14 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
   const size_t smem = decode_smem(p.blob, cfg->lo_bit);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)B * cfg->num_kv_heads, sc.splits);
+  const int nx = cfg->n_hi / 16, v = v_bits(cfg);
   const cudaError_t e = cfg->in_dtype == KITTY_BF16
-      ? (cfg->lo_bit == 4 ? launch_decode_nx<KITTY_BF16, 4>(cfg->n_hi / 16, grid, smem, s, p)
-                          : launch_decode_nx<KITTY_BF16, 2>(cfg->n_hi / 16, grid, smem, s, p))
-      : (cfg->lo_bit == 4 ? launch_decode_nx<KITTY_F16, 4>(cfg->n_hi / 16, grid, smem, s, p)
-                          : launch_decode_nx<KITTY_F16, 2>(cfg->n_hi / 16, grid, smem, s, p));
+      ? (cfg->lo_bit == 4 ? (v == 4 ? launch_decode_nx<KITTY_BF16, 4, 4>(nx, grid, smem, s, p)
+                                    : launch_decode_nx<KITTY_BF16, 4, 2>(nx, grid, smem, s, p))
+                          : launch_decode_nx<KITTY_BF16, 2, 2>(nx, grid, smem, s, p))
+      : (cfg->lo_bit == 4 ? (v == 4 ? launch_decode_nx<KITTY_F16, 4, 4>(nx, grid, smem, s, p)
+                                    : launch_decode_nx<KITTY_F16, 4, 2>(nx, grid, smem, s, p))
+                          : launch_decode_nx<KITTY_F16, 2, 2>(nx, grid, smem, s, p));
   if (e != cudaSuccess) return KITTY_ERR_CUDA;
   // the merge step follows the decode grid as a programmatic dependent
   cudaLaunchAttribute attr[1];

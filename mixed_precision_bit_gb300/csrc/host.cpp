@@ -15,12 +15,12 @@ struct kitty_alloc {
   std::vector<uint8_t> in_use;
 };
 
-extern "C" int kitty_abi_version(void) { return 4; }
+extern "C" int kitty_abi_version(void) { return 5; }
 
 extern "C" int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page) {
   const int rc = check_cfg(cfg, false);
   if (rc != KITTY_OK) return rc;
-  const size_t b = blob_bytes(cfg->n_hi, cfg->lo_bit);
+  const size_t b = blob_bytes(cfg->n_hi, cfg->lo_bit, kitty::v_bits(cfg));
   if (per_head_blob) *per_head_blob = b;
   if (per_page) *per_page = b * (size_t)cfg->num_kv_heads;
   return KITTY_OK;

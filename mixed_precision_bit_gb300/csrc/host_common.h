@@ -21,6 +21,9 @@ inline int check_cfg(const kitty_cfg* c, bool decode) {
   if (c->head_dim != 128 || c->page_tokens != 32 || !bits_ok || c->v_group != 32 ||
       c->n_hi % 16 != 0)
     return KITTY_ERR_UNSUPPORTED;
+  // Value codes: 2-bit (0 = the default), or 4-bit with 4-bit Key planes
+  if (c->v_bit != 0 && c->v_bit != 2 && !(c->v_bit == 4 && c->lo_bit == 4))
+    return KITTY_ERR_UNSUPPORTED;
   if (c->rank_mode != KITTY_RANK_PAGE && c->rank_mode != KITTY_RANK_RUNNING &&
       c->rank_mode != KITTY_RANK_SEQUENCE)
     return KITTY_ERR_INVALID_ARG;
@@ -43,9 +46,13 @@ inline int sm_count() {
 }
 #endif
 
-// Bytes of one (page, kv-head) blob; w = lo_bit (Key plane width, 2 or 4).
-inline size_t blob_bytes(int n_hi, int w) {
-  return 512u * (size_t)w + 4u * (size_t)w * (size_t)n_hi + 2048u + (size_t)n_hi;
+// Value code width of a configuration: 2 or 4.
+inline int v_bits(const kitty_cfg* c) { return c->v_bit == 4 ? 4 : 2; }
+
+// Bytes of one (page, kv-head) blob; w = lo_bit (Key plane width, 2 or 4),
+// v = Value code width (2 or 4).
+inline size_t blob_bytes(int n_hi, int w, int v) {
+  return 512u * (size_t)w + 4u * (size_t)w * (size_t)n_hi + (size_t)n_hi + 512u * (size_t)v + 1024u;
 }
 
 }  // namespace kitty

@@ -14,19 +14,20 @@ constexpr int kD = 128;      // head_dim
 constexpr int kPage = 32;    // tokens per page
 constexpr int kVGroup = 32;  // channels per Value group
 
-// Byte offsets inside one (page, kv-head) blob for a given n_hi (multiple of 16)
-// and Key plane width w = lo_bit (2: the (4, 2) configuration, 4: (8, 4)).
+// Byte offsets inside one (page, kv-head) blob for a given n_hi (multiple of 16),
+// Key plane width w = lo_bit (2: the (4, 2) configuration, 4: (8, 4)) and Value
+// code width v (2, or 4 with w = 4).
 struct BlobLayout {
   int n_hi;
   int kbase, kextra, ks, km, kch, vbase, vs, vm, bytes;
-  __host__ __device__ BlobLayout(int nh, int w) : n_hi(nh) {
+  __host__ __device__ BlobLayout(int nh, int w, int v) : n_hi(nh) {
     kbase = 0;
     kextra = 512 * w;
     ks = kextra + nh * 4 * w;
     km = ks + 256;
     kch = km + 256;
     vbase = kch + nh;
-    vs = vbase + 1024;
+    vs = vbase + 512 * v;
     vm = vs + 256;
     bytes = vm + 256;
   }

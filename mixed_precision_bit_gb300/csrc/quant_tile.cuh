@@ -19,7 +19,7 @@ namespace kitty {
 namespace {
 
 constexpr int kQThreads = 128;
-constexpr int kMaxBlobWords = (4096 + 17 * kD) / 4;  // largest blob: (8, 4) planes, n_hi = 128
+constexpr int kMaxBlobWords = (5120 + 17 * kD) / 4;  // largest blob: (8, 4), 4-bit Values, n_hi = 128
 
 constexpr int kRowH = kD + 8;  // 16-bit elements per staged row (16-byte pad: fewer bank conflicts)
 
@@ -227,20 +227,22 @@ __device__ void tile_stats(QuantSmem& sm, const uint16_t* ksrc, size_t row_strid
 // channel's boost flag (sequence-wide ranking), skipping the statistics; -2
 // ranks on rsum/rsq/rcount as given (running totals that already include this
 // page), leaving them unchanged.
-// W = Key plane width (lo_bit): 2 for the (4, 2) configuration, 4 for (8, 4).
+// W = Key plane width (lo_bit): 2 for the (4, 2) configuration, 4 for (8, 4);
+// V = Value code width: 2, or 4 (with W = 4).
 //
 // Order of work: Key statistics (thread = channel); then warp 0 ranks the
 // channels while the other warps start on the Values (thread 4t+G = token t,
 // group G); then the Key codes.  Every code byte of the blob is written once
 // by one thread with a byte store.
-template <int DT, int W>
+template <int DT, int W, int V>
 __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_t* vsrc,
                               size_t row_stride, int n_hi, bool running, float& rsum, float& rsq,
                               int& rcount, uint8_t* dst, int32_t* d_status, int fixed = -1) {
   static_assert(W == 2 || W == 4, "Key planes are 2 or 4 bits wide");
+  static_assert(V == 2 || (V == 4 && W == 4), "Values are 2-bit, or 4-bit with 4-bit Key planes");
   const int tid = threadIdx.x;
   const int lane = tid & 31, warp = tid >> 5;
-  const BlobLayout lay(n_hi, W);
+  const BlobLayout lay(n_hi, W, V);
   uint8_t* b8 = reinterpret_cast<uint8_t*>(sm.blob);
   uint16_t* b16 = reinterpret_cast<uint16_t*>(sm.blob);
   if (tid == 0) sm.bad = 0;
@@ -330,22 +332,38 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     float vmn = v[0], vmx = v[0];
 #pragma unroll
     for (int i = 1; i < kVGroup; ++i) { vmn = fminf(vmn, v[i]); vmx = fmaxf(vmx, v[i]); }
-    const QuantParams q = qparams(vmn, vmx, 3, false);
+    constexpr int kVLevels = (1 << V) - 1;
+    const QuantParams q = qparams(vmn, vmx, kVLevels, false);
     // Value metadata in fragment order: token 16kt + 8h + 2qq + e at G*32 + qq*8 + kt*4 + h*2 + e
     const int vpos = G * kPage + ((t >> 1) & 3) * 8 + (t >> 4) * 4 + ((t >> 3) & 1) * 2 + (t & 1);
     b16[lay.vs / 2 + vpos] = q.Sbits;
     b16[lay.vm / 2 + vpos] = q.Mbits;
-    // channel 32G + i (i = 16 odd + 8 rh + r) of token t = 16kt + 8h + 2qq + e sits
-    // in word (4r + qq)*8 + 2G + kt, byte 2e + h, at bits 2*(2 odd + rh): the codes
-    // of i = r, r + 8, r + 16, r + 24 make one byte
     const int qq = (t >> 1) & 3, kt = t >> 4, half = (t >> 3) & 1, e = t & 1;
-    uint8_t* vb = b8 + lay.vbase + (qq * 8 + 2 * G + kt) * 4 + 2 * e + half;
+    if (V == 2) {
+      // channel 32G + i (i = 16 odd + 8 rh + r) of token t = 16kt + 8h + 2qq + e sits
+      // in word (4r + qq)*8 + 2G + kt, byte 2e + h, at bits 2*(2 odd + rh): the codes
+      // of i = r, r + 8, r + 16, r + 24 make one byte
+      uint8_t* vb = b8 + lay.vbase + (qq * 8 + 2 * G + kt) * 4 + 2 * e + half;
 #pragma unroll
-    for (int r = 0; r < 8; ++r) {
-      const float xs[4] = {v[r], v[r + 8], v[r + 16], v[r + 24]};
-      uint32_t cd[4];
-      qcode4(xs, q, 3, cd);
-      vb[128 * r] = pack4x2(cd[0], cd[1], cd[2], cd[3]);
+      for (int r = 0; r < 8; ++r) {
+        const float xs[4] = {v[r], v[r + 8], v[r + 16], v[r + 24]};
+        uint32_t cd[4];
+        qcode4(xs, q, kVLevels, cd);
+        vb[128 * r] = pack4x2(cd[0], cd[1], cd[2], cd[3]);
+      }
+    } else {
+      // 4-bit: channel 32G + i (i = 16 odd + 8 rh + r) sits in word
+      // (4r + qq)*16 + 4G + 2kt + odd, byte 2e + h, nibble rh: the codes of
+      // i = r, r + 8 make one byte, those of i = r + 16, r + 24 the byte one word on
+      uint8_t* vb = b8 + lay.vbase + (qq * 16 + 4 * G + 2 * kt) * 4 + 2 * e + half;
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const float xs[4] = {v[r], v[r + 8], v[r + 16], v[r + 24]};
+        uint32_t cd[4];
+        qcode4(xs, q, kVLevels, cd);
+        vb[256 * r] = (uint8_t)(cd[0] | (cd[1] << 4));
+        vb[256 * r + 4] = (uint8_t)(cd[2] | (cd[3] << 4));
+      }
     }
   }
   __syncthreads();  // boost masks visible

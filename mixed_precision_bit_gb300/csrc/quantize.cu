@@ -22,7 +22,7 @@ namespace kitty {
 namespace {
 
 // Page mode: one CTA per (input page i, kv head h).
-template <int DT, int W>
+template <int DT, int W, int V>
 __global__ void __launch_bounds__(kQThreads, 8) quantize_pages_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
     int n_hi, int Hkv, uint8_t* pool, int pool_pages, int32_t* d_status) {
@@ -33,12 +33,12 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_pages_kernel(
     if (threadIdx.x == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
     return;
   }
-  const BlobLayout lay(n_hi, W);
+  const BlobLayout lay(n_hi, W, V);
   const size_t stride = (size_t)Hkv * kD;
   const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
   float dummy_s = 0.f, dummy_q = 0.f;
   int dummy_c = 0;
-  quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
+  quantize_tile<DT, W, V>(sm, k + src, v + src, stride, n_hi, false, dummy_s, dummy_q, dummy_c,
                     pool + ((size_t)pid * Hkv + h) * lay.bytes, d_status);
 }
 
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kQThreads) seq_walk_kernel(
   if (c == 0) run_count[sh] = rc;
 }
 
-template <int DT, int W>
+template <int DT, int W, int V>
 __global__ void __launch_bounds__(kQThreads, 8) quantize_given_kernel(
     const uint16_t* __restrict__ k, const uint16_t* __restrict__ v, const int32_t* page_ids,
     const int32_t* seq_of_page, int n_seqs, int n_hi, int Hkv, uint8_t* pool, int pool_pages,
@@ -257,7 +257,7 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_given_kernel(
     if (c == 0) set_status(d_status, KITTY_ST_BAD_PAGE);
     return;
   }
-  const BlobLayout lay(n_hi, W);
+  const BlobLayout lay(n_hi, W, V);
   uint8_t* dst = pool + ((size_t)pid * Hkv + h) * lay.bytes;
   const size_t stride = (size_t)Hkv * kD;
   const size_t src = (size_t)i * kPage * stride + (size_t)h * kD;
@@ -274,12 +274,12 @@ __global__ void __launch_bounds__(kQThreads, 8) quantize_given_kernel(
   }
   // quantize_tile reads the scratch values above before it overwrites the blob
   // (its only global write, after its last barrier)
-  quantize_tile<DT, W>(sm, k + src, v + src, stride, n_hi, false, rs, rq, rc, dst, d_status, fixed);
+  quantize_tile<DT, W, V>(sm, k + src, v + src, stride, n_hi, false, rs, rq, rc, dst, d_status, fixed);
 }
 
 // Append, part 1: one CTA per (sequence b, kv head h) writes the token into the
 // tail and, when the tail fills and a page id is given, quantizes the tail.
-template <int DT, int W>
+template <int DT, int W, int V>
 __global__ void __launch_bounds__(kQThreads) append_heads_kernel(
     const uint16_t* __restrict__ k_new, const uint16_t* __restrict__ v_new, uint16_t* tail_k,
     uint16_t* tail_v, const int32_t* tail_len, float* run_sum, float* run_sumsq,
@@ -301,7 +301,7 @@ __global__ void __launch_bounds__(kQThreads) append_heads_kernel(
   if (np < 0 || np >= max_pages) { if (c == 0) set_status(d_status, KITTY_ST_TABLE_FULL); return; }
   if (fid >= pool_pages) { if (c == 0) set_status(d_status, KITTY_ST_BAD_PAGE); return; }
   __syncthreads();  // the new token row is visible to the whole CTA
-  const BlobLayout lay(n_hi, W);
+  const BlobLayout lay(n_hi, W, V);
   float rs = 0.f, rq = 0.f;
   int rc = 0;
   if (running) {
@@ -309,7 +309,7 @@ __global__ void __launch_bounds__(kQThreads) append_heads_kernel(
     rq = run_sumsq[sh * kD + c];
     rc = run_count[sh];
   }
-  quantize_tile<DT, W>(sm, tail_k + sh * kPage * kD, tail_v + sh * kPage * kD, kD, n_hi, running != 0,
+  quantize_tile<DT, W, V>(sm, tail_k + sh * kPage * kD, tail_v + sh * kPage * kD, kD, n_hi, running != 0,
                     rs, rq, rc, pool + ((size_t)fid * Hkv + h) * lay.bytes, d_status);
   if (running) {
     run_sum[sh * kD + c] = rs;
@@ -328,21 +328,24 @@ __global__ void append_finalize_kernel(int32_t* tail_len, const int32_t* flush_p
   append_finalize_one(b, tail_len, flush_page_ids, block_table, max_pages, num_pages, pool_pages);
 }
 
-// Calls f(KernelTag<DT, W>{}) for the configuration's input dtype and Key plane
-// width (lo_bit).
-template <int DT_, int W_>
+// Calls f(KernelTag<DT, W, V>{}) for the configuration's input dtype, Key plane
+// width (lo_bit) and Value code width (v_bit; 4 only with 4-bit Key planes).
+template <int DT_, int W_, int V_>
 struct KernelTag {
-  static constexpr int DT = DT_, W = W_;
+  static constexpr int DT = DT_, W = W_, V = V_;
 };
 
 template <class F>
 void dispatch(const kitty_cfg* cfg, F f) {
+  const int v = v_bits(cfg);
   if (cfg->in_dtype == KITTY_BF16) {
-    if (cfg->lo_bit == 4) f(KernelTag<KITTY_BF16, 4>{});
-    else f(KernelTag<KITTY_BF16, 2>{});
+    if (cfg->lo_bit == 4 && v == 4) f(KernelTag<KITTY_BF16, 4, 4>{});
+    else if (cfg->lo_bit == 4) f(KernelTag<KITTY_BF16, 4, 2>{});
+    else f(KernelTag<KITTY_BF16, 2, 2>{});
   } else {
-    if (cfg->lo_bit == 4) f(KernelTag<KITTY_F16, 4>{});
-    else f(KernelTag<KITTY_F16, 2>{});
+    if (cfg->lo_bit == 4 && v == 4) f(KernelTag<KITTY_F16, 4, 4>{});
+    else if (cfg->lo_bit == 4) f(KernelTag<KITTY_F16, 4, 2>{});
+    else f(KernelTag<KITTY_F16, 2, 2>{});
   }
 }
 
@@ -375,11 +378,11 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
     dim3 grid(n_pages, Hkv);
     dispatch(cfg, [&](auto tag) {
       using T = decltype(tag);
-      quantize_pages_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, cfg->n_hi, Hkv, p8, pool_pages, d_status);
+      quantize_pages_kernel<T::DT, T::W, T::V><<<grid, kQThreads, 0, s>>>(k16, v16, page_ids, cfg->n_hi, Hkv, p8, pool_pages, d_status);
     });
   } else {
     check_seq_kernel<<<(n_pages + 255) / 256, 256, 0, s>>>(seq_of_page, n_pages, n_seqs, d_status);
-    const int blob = (int)blob_bytes(cfg->n_hi, cfg->lo_bit);
+    const int blob = (int)blob_bytes(cfg->n_hi, cfg->lo_bit, v_bits(cfg));
     const int seq = cfg->rank_mode == KITTY_RANK_SEQUENCE ? 1 : 0;
     dim3 pages(n_pages, Hkv), seqs(n_seqs, Hkv);
     if ((long)n_seqs * Hkv >= 3L * sm_count()) {
@@ -398,7 +401,7 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
     }
     dispatch(cfg, [&](auto tag) {
       using T = decltype(tag);
-      quantize_given_kernel<T::DT, T::W><<<pages, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_seqs, cfg->n_hi, Hkv, p8, pool_pages, seq, d_status);
+      quantize_given_kernel<T::DT, T::W, T::V><<<pages, kQThreads, 0, s>>>(k16, v16, page_ids, seq_of_page, n_seqs, cfg->n_hi, Hkv, p8, pool_pages, seq, d_status);
     });
   }
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;
@@ -429,7 +432,7 @@ extern "C" int kitty_append_token(const kitty_cfg* cfg, const void* k_new, const
   auto* p8 = static_cast<uint8_t*>(pool);
   dispatch(cfg, [&](auto tag) {
     using T = decltype(tag);
-    append_heads_kernel<T::DT, T::W><<<grid, kQThreads, 0, s>>>(kn, vn, tk, tv, tail_len, run_sum, run_sumsq, run_count, flush_page_ids, max_pages, num_pages, p8, pool_pages, cfg->n_hi, Hkv, running ? 1 : 0, d_status);
+    append_heads_kernel<T::DT, T::W, T::V><<<grid, kQThreads, 0, s>>>(kn, vn, tk, tv, tail_len, run_sum, run_sumsq, run_count, flush_page_ids, max_pages, num_pages, p8, pool_pages, cfg->n_hi, Hkv, running ? 1 : 0, d_status);
   });
   append_finalize_kernel<<<(B + 127) / 128, 128, 0, s>>>(tail_len, flush_page_ids, block_table, max_pages, num_pages, pool_pages, B);
   return cudaGetLastError() == cudaSuccess ? KITTY_OK : KITTY_ERR_CUDA;

@@ -33,7 +33,7 @@ class _Cfg(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "head_dim", "num_kv_heads", "num_q_heads", "page_tokens", "n_hi", "hi_bit", "lo_bit",
         "v_group", "rank_mode", "in_dtype", "decode_pages_per_split", "decode_total_pages",
-        "decode_max_pages", "decode_wait_polls")]
+        "decode_max_pages", "decode_wait_polls", "v_bit")]
 
 
 @dataclasses.dataclass
@@ -52,12 +52,13 @@ class Config:
     hi_bit: int = 4
     lo_bit: int = 2
     v_group: int = 32
+    v_bit: int = 2                  # Value code width: 2, or 4 with lo_bit 4
 
     def c(self):
         return _Cfg(self.head_dim, self.num_kv_heads, self.num_q_heads, self.page_tokens,
                     self.n_hi, self.hi_bit, self.lo_bit, self.v_group, self.rank_mode,
                     self.in_dtype, self.decode_pages_per_split, self.decode_total_pages,
-                    self.decode_max_pages, self.decode_wait_polls)
+                    self.decode_max_pages, self.decode_wait_polls, self.v_bit)
 
 
 _lib = None

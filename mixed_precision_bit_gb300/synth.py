@@ -107,6 +107,7 @@ class Workload:
     drift: int = 0         # redraw K channel scales every `drift` tokens (0: never)
     layers: int = 1
     lo_bit: int = 2        # Key plane width: 2 ((hi, lo) = (4, 2) bits) or 4 ((8, 4))
+    v_bit: int = 2         # Value code width: 2, or 4 (with lo_bit 4)
 
     @property
     def g(self):

@@ -88,11 +88,12 @@ def half_way_column(levels, m, a, boosted_w=None):
     return vals
 
 
-def plant_half_way(inp, w, key_levels, boosted, seed):
+def plant_half_way(inp, w, key_levels, boosted, seed, value_levels=3):
     """Rounding ties in every Key channel and Value group of every page
     (in place).  key_levels: (levels of a normal channel, levels of a boosted
     one); boosted: channel indices given the larger scale, so that a ranking
-    of n_hi = len(boosted) boosts exactly them."""
+    of n_hi = len(boosted) boosts exactly them; value_levels: 3 (2-bit Values)
+    or 15 (4-bit)."""
     rng = np.random.default_rng(seed)
     tot = int(w.pages.sum())
     is_b = np.zeros(D, bool)
@@ -110,7 +111,8 @@ def plant_half_way(inp, w, key_levels, boosted, seed):
             vt = np.zeros((PAGE, D))
             for t in range(PAGE):
                 for G in range(4):
-                    col = half_way_column(3, int(rng.integers(2, 7)), int(rng.integers(0, 3)))
+                    col = half_way_column(value_levels, int(rng.integers(2, 7)),
+                                          int(rng.integers(0, 3)))
                     vt[t, 32 * G:32 * G + 32] = col[rng.permutation(32)]
             inp["v"][t0:t0 + PAGE, h, :] = _bits(vt, w.dtype)
     return inp

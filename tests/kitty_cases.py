@@ -17,7 +17,7 @@ def cfg_for(w, rank_mode=0, pps=0):
     from mixed_precision_bit_gb300 import kitty
     return kitty.Config(num_kv_heads=w.Hkv, num_q_heads=w.Hq, n_hi=w.n_hi, in_dtype=w.dtype,
                         rank_mode=rank_mode, decode_pages_per_split=pps,
-                        hi_bit=2 * w.lo_bit, lo_bit=w.lo_bit)
+                        hi_bit=2 * w.lo_bit, lo_bit=w.lo_bit, v_bit=w.v_bit)
 
 
 def dev16(a):
@@ -58,7 +58,7 @@ def gpu_quantize(w, inp, running=False, status=None, mode=None):
 def oracle_quantize(w, inp, running=False, mode=None):
     mode = (1 if running else 0) if mode is None else mode
     running = mode != 0
-    pool = np.zeros(inp["pool_pages"] * w.Hkv * oracle.page_bytes(w.n_hi, w.lo_bit), np.uint8)
+    pool = np.zeros(inp["pool_pages"] * w.Hkv * oracle.page_bytes(w.n_hi, w.lo_bit, w.v_bit), np.uint8)
     if running:
         rs = np.zeros((w.B, w.Hkv, 128), np.float32)
         rq = np.zeros_like(rs)
@@ -66,10 +66,10 @@ def oracle_quantize(w, inp, running=False, mode=None):
         st = oracle.quantize_pages(w.Hkv, w.n_hi, mode, w.dtype, inp["k"], inp["v"], inp["page_ids"],
                                    pool, inp["pool_pages"], seq_of_page=inp["seq_of_page"],
                                    n_seqs=w.B, run_sum=rs, run_sumsq=rq, run_count=rc,
-                                   lo_bit=w.lo_bit)
+                                   lo_bit=w.lo_bit, v_bit=w.v_bit)
         return pool, (rs, rq, rc), st
     st = oracle.quantize_pages(w.Hkv, w.n_hi, 0, w.dtype, inp["k"], inp["v"], inp["page_ids"],
-                               pool, inp["pool_pages"], lo_bit=w.lo_bit)
+                               pool, inp["pool_pages"], lo_bit=w.lo_bit, v_bit=w.v_bit)
     return pool, None, st
 
 
@@ -98,7 +98,7 @@ def oracle_decode(w, inp, pool, sm_scale=None):
     return oracle.decode_attention(w.Hkv, w.Hq, w.n_hi, w.dtype, inp["q"], pool,
                                    inp["pool_pages"], inp["block_table"], inp["num_pages"],
                                    inp["tail_k"], inp["tail_v"], inp["tail_len"], sm,
-                                   lo_bit=w.lo_bit)
+                                   lo_bit=w.lo_bit, v_bit=w.v_bit)
 
 
 def half_ulp(ref, out_dtype):

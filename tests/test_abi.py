@@ -36,7 +36,7 @@ def test_exports_every_declared_symbol(K):
     for n in names:
         assert hasattr(lib, n), n
     assert set(K.EXPORTS) == names
-    assert lib.kitty_abi_version() == 4
+    assert lib.kitty_abi_version() == 5
 
 
 def test_page_bytes_and_avg_bits(K):

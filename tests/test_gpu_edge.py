@@ -81,20 +81,22 @@ def test_quantize_ties_bit_exact(roles, mode, lo_bit):
 
 
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.F16], ids=["bf16", "f16"])
-@pytest.mark.parametrize("lo_bit,n_hi", [(2, 0), (2, 32), (2, 128), (4, 0), (4, 32), (4, 128)])
-def test_quantize_rounding_ties_bit_exact(lo_bit, n_hi, dtype):
+@pytest.mark.parametrize("lo_bit,n_hi,v_bit", [(2, 0, 2), (2, 32, 2), (2, 128, 2), (4, 0, 2),
+                                               (4, 32, 2), (4, 128, 2), (4, 0, 4), (4, 32, 4)])
+def test_quantize_rounding_ties_bit_exact(lo_bit, n_hi, v_bit, dtype):
     """Every Key channel and Value group holds values exactly halfway between two
-    levels (3 and 15 levels at (4, 2); 15 and 255 at (8, 4)): bit-exact pools in
-    page and running mode, then decode within tolerance."""
+    levels (3 and 15 levels at (4, 2); 15 and 255 at (8, 4); 3 or 15 for 2-bit or
+    4-bit Values): bit-exact pools in page and running mode, then decode within
+    tolerance."""
     levels = (3, 15) if lo_bit == 2 else (15, 255)
-    w = _w(n_hi=n_hi, lo_bit=lo_bit, dtype=dtype)
+    w = _w(n_hi=n_hi, lo_bit=lo_bit, dtype=dtype, v_bit=v_bit)
     inp = synth.host_inputs(w, seed=33)
     boosted = np.sort(np.random.default_rng(34).permutation(128)[:n_hi])
-    plant_half_way(inp, w, levels, boosted, seed=35)
+    plant_half_way(inp, w, levels, boosted, seed=35, value_levels=(1 << v_bit) - 1)
     for mode in (0, 1):
         pool, ref = _same_pool(w, inp, mode)
         if mode == 0 and 0 < n_hi < 128:
-            blob = oracle.page_bytes(n_hi, lo_bit)
+            blob = oracle.page_bytes(n_hi, lo_bit, v_bit)
             assert (oracle.page_channels(ref[:blob], n_hi, lo_bit) == boosted).all()
     got = gpu_decode(w, inp, pool)
     want, _ = oracle_decode(w, inp, pool.cpu().numpy())

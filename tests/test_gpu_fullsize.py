@@ -29,18 +29,20 @@ def _oracle_seq_pool(spec, k, v, running):
     """The oracle's pages for one sequence (local ids 0..np-1)."""
     n_hi, Hkv, lo_bit = spec["n_hi"], spec["Hkv"], spec["lo_bit"]
     npg = k.shape[0] // 32
-    pool = np.zeros(max(npg, 1) * Hkv * oracle.page_bytes(n_hi, lo_bit), np.uint8)
+    pool = np.zeros(max(npg, 1) * Hkv * oracle.page_bytes(n_hi, lo_bit, spec.get("v_bit", 2)), np.uint8)
     rs = np.zeros((1, Hkv, 128), np.float32)
     rq = np.zeros_like(rs)
     rc = np.zeros((1, Hkv), np.int32)
     st = oracle.quantize_pages(Hkv, n_hi, 1 if running else 0, 1, k, v, np.arange(npg, dtype=np.int32),
                                pool, max(npg, 1), seq_of_page=np.zeros(npg, np.int32), n_seqs=1,
-                               run_sum=rs, run_sumsq=rq, run_count=rc, lo_bit=lo_bit)
+                               run_sum=rs, run_sumsq=rq, run_count=rc, lo_bit=lo_bit,
+                               v_bit=spec.get("v_bit", 2))
     assert st == 0
     return pool, (rs, rq, rc)
 
 
-@pytest.mark.parametrize("name", ["llama3_8b", "qwen3_8b", "long", "budget", "budget_84"])
+@pytest.mark.parametrize("name", ["llama3_8b", "qwen3_8b", "long", "budget", "budget_84",
+                                  "budget_kv4"])
 def test_fullsize_sampled(name):
     import torch
     import bench
@@ -52,7 +54,7 @@ def test_fullsize_sampled(name):
     keep = sorted({0, B // 2, B - 1} | ({int(np.argmax(spec["tails"]))} if B > 1 else set()))
     cfg, layers, raw = bench.build_layers(spec, 8, keep=keep)
     lc = layers[0]
-    blob = oracle.page_bytes(spec["n_hi"], spec["lo_bit"])
+    blob = oracle.page_bytes(spec["n_hi"], spec["lo_bit"], spec.get("v_bit", 2))
     gpool = lc.pool.cpu().numpy()
     bt = lc.block_table.cpu().numpy()      # host-chosen page ids (an input)
     gen = torch.Generator(device="cuda").manual_seed(77)
@@ -76,7 +78,8 @@ def test_fullsize_sampled(name):
         ref, st = oracle.decode_attention(
             spec["Hkv"], spec["Hq"], spec["n_hi"], 1, qh[b:b + 1], opool, max(npg, 1),
             np.arange(max(npg, 1), dtype=np.int32)[None, :], np.array([npg], np.int32),
-            tk[None], tv[None], np.array([tl], np.int32), SM, lo_bit=spec["lo_bit"])
+            tk[None], tv[None], np.array([tl], np.int32), SM, lo_bit=spec["lo_bit"],
+            v_bit=spec.get("v_bit", 2))
         assert st == 0
         excess, rel = attn_error(got_all[b:b + 1], ref)
         print("%s sequence %d: max |gpu - oracle| = %.3e of RMS" % (name, b, rel))
@@ -105,7 +108,7 @@ def test_fullsize_serving_append_steps():
     torch.cuda.synchronize()
     assert int(lc.status.item()) == 0
     gpool = lc.pool.cpu().numpy()
-    per_page = oracle.page_bytes(spec["n_hi"], spec["lo_bit"]) * Hkv
+    per_page = oracle.page_bytes(spec["n_hi"], spec["lo_bit"], spec.get("v_bit", 2)) * Hkv
     g_sum = lc.run_sum.cpu().numpy()
     g_cnt = lc.run_count.cpu().numpy()
     g_np = lc.num_pages.cpu().numpy()

@@ -27,17 +27,17 @@ def _cuda():
     kitty.load()
 
 
-def _initial(mode, dtype, pages, tails, Hkv=2, Hq=8, n_hi=32, extra=3, seed=11, lo_bit=2):
+def _initial(mode, dtype, pages, tails, Hkv=2, Hq=8, n_hi=32, extra=3, seed=11, lo_bit=2, v_bit=2):
     """Oracle-built cache (prefilled pages quantized by the oracle, tails) with
     `extra` free block-table slots per sequence, as host arrays."""
     B = len(pages)
     w = synth.Workload("fused", B, Hq, Hkv, n_hi, dtype, np.asarray(pages), np.asarray(tails),
-                       lo_bit=lo_bit)
+                       lo_bit=lo_bit, v_bit=v_bit)
     inp = synth.host_inputs(w, seed=seed)
     max_pages = int(max(pages)) + extra
     tot = int(np.sum(pages))
     pool_pages = tot + B * extra
-    per_page = oracle.page_bytes(n_hi, lo_bit) * Hkv
+    per_page = oracle.page_bytes(n_hi, lo_bit, v_bit) * Hkv
     st = dict(pool=np.zeros(pool_pages * per_page, np.uint8),
               block_table=np.full((B, max_pages), -1, np.int32),
               num_pages=np.asarray(pages, np.int32).copy(),
@@ -52,7 +52,7 @@ def _initial(mode, dtype, pages, tails, Hkv=2, Hq=8, n_hi=32, extra=3, seed=11, 
             kw = dict(seq_of_page=inp["seq_of_page"], n_seqs=B, run_sum=st["run_sum"],
                       run_sumsq=st["run_sumsq"], run_count=st["run_count"])
         assert oracle.quantize_pages(Hkv, n_hi, mode, dtype, inp["k"], inp["v"], inp["page_ids"],
-                                     st["pool"], pool_pages, lo_bit=lo_bit, **kw) == 0
+                                     st["pool"], pool_pages, lo_bit=lo_bit, v_bit=v_bit, **kw) == 0
     return w, st, max_pages, pool_pages, tot
 
 
@@ -78,16 +78,20 @@ def _compare_state(o, g, keys=("pool", "tail_k", "tail_v", "tail_len", "num_page
         assert (gv.view(np.uint8) == o[k].view(np.uint8)).all(), k
 
 
-@pytest.mark.parametrize("mode,dtype,pps,lo_bit", [(1, synth.BF16, 0, 2), (0, synth.BF16, 4, 2),
-                                                   (1, synth.F16, 1000, 2), (2, synth.BF16, 2, 2),
-                                                   (1, synth.BF16, 4, 4), (0, synth.F16, 1000, 4)],
+@pytest.mark.parametrize("mode,dtype,pps,lo_bit,v_bit",
+                         [(1, synth.BF16, 0, 2, 2), (0, synth.BF16, 4, 2, 2),
+                          (1, synth.F16, 1000, 2, 2), (2, synth.BF16, 2, 2, 2),
+                          (1, synth.BF16, 4, 4, 2), (0, synth.F16, 1000, 4, 2),
+                          (0, synth.BF16, 4, 4, 4), (1, synth.F16, 0, 4, 4)],
                          ids=["running-bf16", "page-bf16-splits", "running-f16-one-split",
-                              "sequence-bf16-splits", "running-bf16-84", "page-f16-one-split-84"])
-def test_fused_matches_oracle(mode, dtype, pps, lo_bit):
+                              "sequence-bf16-splits", "running-bf16-84", "page-f16-one-split-84",
+                              "page-bf16-splits-kv4", "running-f16-84-v4"])
+def test_fused_matches_oracle(mode, dtype, pps, lo_bit, v_bit):
     import torch
     from mixed_precision_bit_gb300 import kitty
     w, o, max_pages, pool_pages, next_id = _initial(mode, dtype, [5, 0, 9], [29, 31, 3],
-                                                    lo_bit=lo_bit)
+                                                    lo_bit=lo_bit, v_bit=v_bit,
+                                                    n_hi=0 if (mode, v_bit) == (0, 4) else 32)
     B, Hkv, Hq = w.B, w.Hkv, w.Hq
     cfg = cfg_for(w, rank_mode=mode, pps=pps)
     g = _to_gpu(o)
@@ -107,10 +111,11 @@ def test_fused_matches_oracle(mode, dtype, pps, lo_bit):
         assert oracle.append_token(Hkv, w.n_hi, mode, dtype, kn, vn, o["tail_k"], o["tail_v"],
                                    o["tail_len"], o["run_sum"], o["run_sumsq"], o["run_count"], fl,
                                    o["block_table"], max_pages, o["num_pages"], o["pool"],
-                                   pool_pages, lo_bit=lo_bit) == 0
+                                   pool_pages, lo_bit=lo_bit, v_bit=v_bit) == 0
         ref, st = oracle.decode_attention(Hkv, Hq, w.n_hi, dtype, q, o["pool"], pool_pages,
                                           o["block_table"], o["num_pages"], o["tail_k"],
-                                          o["tail_v"], o["tail_len"], SM, lo_bit=lo_bit)
+                                          o["tail_v"], o["tail_len"], SM, lo_bit=lo_bit,
+                                          v_bit=v_bit)
         assert st == 0
         kitty.append_decode(cfg, dev16(kn), dev16(vn), dev16(q), g["tail_k"], g["tail_v"],
                             g["tail_len"], g["run_sum"], g["run_sumsq"], g["run_count"], dev32(fl),

@@ -47,6 +47,12 @@ CASES = [
     ("small_gqa", dict(lo_bit=4, n_hi=48)),
     ("small_gqa", dict(lo_bit=4, n_hi=128)),
     ("small_gqa", dict(lo_bit=4, dtype=synth.F16, n_hi=16, Hq=6, Hkv=3)),
+    # 4-bit Values: uniform 4-bit KV (n_hi = 0) and Kitty (8, 4) Keys
+    ("tiny", dict(lo_bit=4, v_bit=4)),
+    ("small_gqa", dict(lo_bit=4, v_bit=4, n_hi=0)),
+    ("small_gqa", dict(lo_bit=4, v_bit=4)),
+    ("small_gqa", dict(lo_bit=4, v_bit=4, n_hi=128, dtype=synth.F16)),
+    ("small_gqa", dict(lo_bit=4, v_bit=4, n_hi=16, Hq=6, Hkv=2)),
 ]
 
 

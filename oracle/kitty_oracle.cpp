@@ -143,11 +143,20 @@ struct Layout {
 // and bit offset.  Each plane is stored in "fragment order": the 32 bytes (8
 // words) of lane L hold exactly the codes that lane L of a 32-thread warp needs
 // as 16x16 operand tiles, and inside a word the code of element (row, col) sits
-// at bit 16*(col parity) + 8*(col half of the 16-wide tile) + 2*tau, where tau
-// names the row's 8-row block.  The mapping is a bijection (checked by tests).
+// at bit 16*(col parity) + 8*(col half of the 16-wide tile) + 2*tau + 2,
+// modulo 32, where tau names the row's 8-row block.  (Reading: the pages fix
+// no bit layout.  The +2 -- every word rotated left by two bits against the
+// plain order -- places a code, once masked out of its 16-bit half, in
+// mantissa bits 2..9 of an fp16 subnormal rather than 0..7; on the GB300 the
+// tensor cores keep measurably less of a product's low bits the further
+// below the top of the mantissa its code sits.)  The mapping is a bijection
+// (checked by tests).
 //
 // Key planes: row = token t, col = channel c (base) or boosted row j (extra).
 struct BitPos { int word; int bit; };
+
+// The rotation of a plane word's bit positions (see above).
+int rot_bit(int b) { return (b + 2) & 31; }
 
 BitPos key_pos(int col, int t, int words_per_lane) {
   const int ks = col >> 4, cc = col & 15;
@@ -155,19 +164,20 @@ BitPos key_pos(int col, int t, int words_per_lane) {
   const int mt = t >> 4, rh = (t >> 3) & 1, r = t & 7;
   const int tau = 2 * mt + rh;
   const int lane = 4 * r + qq;
-  return {lane * words_per_lane + ks, 16 * e + 8 * half + 2 * tau};
+  return {lane * words_per_lane + ks, rot_bit(16 * e + 8 * half + 2 * tau)};
 }
 
 // 4-bit Key planes, same fragment order with nibbles: a lane holds two words
 // per 16-column tile (one per 16-token block mt), and inside a word element
-// (row, col) sits at bit 16*(col parity) + 8*(col half) + 4*(row's 8-row half).
+// (row, col) sits at bit 16*(col parity) + 8*(col half) + 4*(row's 8-row half)
+// + 2, modulo 32 (a nibble may wrap from bit 31 to bit 0).
 // words_per_lane = 2 * (columns / 16).
 BitPos key_pos4(int col, int t, int words_per_lane) {
   const int ks = col >> 4, cc = col & 15;
   const int half = cc >> 3, qq = (cc & 7) >> 1, e = cc & 1;
   const int mt = t >> 4, rh = (t >> 3) & 1, r = t & 7;
   const int lane = 4 * r + qq;
-  return {lane * words_per_lane + 2 * ks + mt, 16 * e + 8 * half + 4 * rh};
+  return {lane * words_per_lane + 2 * ks + mt, rot_bit(16 * e + 8 * half + 4 * rh)};
 }
 
 // Key code position for plane width w over `cols` columns (D or n_hi).
@@ -181,18 +191,18 @@ BitPos val_pos(int t, int c) {
   const int kt = t >> 4, half = (t >> 3) & 1, qq = (t & 7) >> 1, e = t & 1;
   const int tau = 2 * (mc & 1) + rh;
   const int lane = 4 * r + qq;
-  return {lane * 8 + (mc >> 1) * 2 + kt, 16 * e + 8 * half + 2 * tau};
+  return {lane * 8 + (mc >> 1) * 2 + kt, rot_bit(16 * e + 8 * half + 2 * tau)};
 }
 
 // 4-bit Value plane, same rows and columns with nibbles: a lane holds four
 // words per 32-channel group G (16-token block kt, 16-channel tile parity), and
 // inside a word element (row, col) sits at bit 16*(col parity) + 8*(col half) +
-// 4*(row's 8-row half).
+// 4*(row's 8-row half) + 2, modulo 32.
 BitPos val_pos4(int t, int c) {
   const int mc = c >> 4, rh = (c >> 3) & 1, r = c & 7;
   const int kt = t >> 4, half = (t >> 3) & 1, qq = (t & 7) >> 1, e = t & 1;
   const int lane = 4 * r + qq;
-  return {lane * 16 + (mc >> 1) * 4 + kt * 2 + (mc & 1), 16 * e + 8 * half + 4 * rh};
+  return {lane * 16 + (mc >> 1) * 4 + kt * 2 + (mc & 1), rot_bit(16 * e + 8 * half + 4 * rh)};
 }
 
 // Value code position for Value width vw.
@@ -217,18 +227,21 @@ int kch_pos(int j) {
   return js * 16 + qq * 4 + h * 2 + e;
 }
 
-// Write / read a `bits`-wide code at p.
+// Write / read a `bits`-wide code at p; a code starting at bit 30 of a word
+// continues at bit 0 of the same word.
+uint32_t rotl32(uint32_t x, int k) { return k == 0 ? x : (x << k) | (x >> (32 - k)); }
+
 void putb(uint8_t* plane, BitPos p, uint32_t code, int bits) {
   uint32_t w;
   std::memcpy(&w, plane + 4 * p.word, 4);
-  w |= (code & ((1u << bits) - 1u)) << p.bit;
+  w |= rotl32(code & ((1u << bits) - 1u), p.bit);
   std::memcpy(plane + 4 * p.word, &w, 4);
 }
 
 uint32_t getb(const uint8_t* plane, BitPos p, int bits) {
   uint32_t w;
   std::memcpy(&w, plane + 4 * p.word, 4);
-  return (w >> p.bit) & ((1u << bits) - 1u);
+  return rotl32(w, (32 - p.bit) & 31) & ((1u << bits) - 1u);
 }
 
 

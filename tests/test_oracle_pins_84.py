@@ -56,7 +56,7 @@ def test_page_bytes_84(orc):
 def test_nibble_maps_are_bijections(orc):
     seen = {orc.key_pos4(c, t, 16) for c in range(128) for t in range(32)}
     assert len(seen) == 4096 and {w for w, _ in seen} == set(range(512))
-    assert {b for _, b in seen} == set(range(0, 32, 4))
+    assert {b for _, b in seen} == set(range(2, 32, 4))   # nibble starts, rotated by 2
     for nh in (16, 32, 128):
         seen = {orc.key_pos4(j, t, 2 * (nh // 16)) for j in range(nh) for t in range(32)}
         assert len(seen) == nh * 32 and max(w for w, _ in seen) == nh * 4 - 1
@@ -87,7 +87,8 @@ def test_hf1_is_uniform_8bit(orc):
 
 def _planes4(orc, blob, n_hi):
     def nib(off, w, b):
-        return (int.from_bytes(bytes(blob[off + 4 * w:off + 4 * w + 4]), "little") >> b) & 15
+        x = int.from_bytes(bytes(blob[off + 4 * w:off + 4 * w + 4]), "little")
+        return ((x >> b) | (x << (32 - b))) & 15   # a nibble at bit 30 wraps to bit 0
     base = np.array([[nib(0, *orc.key_pos4(c, t, 16)) for c in range(128)] for t in range(32)])
     extra = np.array([[nib(2048, *orc.key_pos4(j, t, 2 * (n_hi // 16))) for j in range(n_hi)]
                       for t in range(32)]).reshape(32, n_hi)

@@ -60,7 +60,7 @@ def test_value_nibble_map_is_a_bijection(orc):
     seen = {orc.val_pos4(t, c) for t in range(32) for c in range(128)}
     assert len(seen) == 4096
     assert {w for w, _ in seen} == set(range(512))
-    assert {b for _, b in seen} == set(range(0, 32, 4))
+    assert {b for _, b in seen} == set(range(2, 32, 4))   # nibble starts, rotated by 2
     # fragment order: lane L = 4r + qq (words 16L..16L+15) holds channels with
     # c % 8 == r and tokens with (t % 8) // 2 == qq, and the 8 nibbles of a word
     # are one m16n8k16 A fragment: rows r, r + 8 of one 16-channel tile times
@@ -78,7 +78,8 @@ def _value_codes(orc, blob, n_hi):
     vbase = 2048 + 16 * n_hi + 512 + n_hi
 
     def nib(w, b):
-        return (int.from_bytes(bytes(blob[vbase + 4 * w:vbase + 4 * w + 4]), "little") >> b) & 15
+        x = int.from_bytes(bytes(blob[vbase + 4 * w:vbase + 4 * w + 4]), "little")
+        return ((x >> b) | (x << (32 - b))) & 15   # a nibble at bit 30 wraps to bit 0
     return np.array([[nib(*orc.val_pos4(t, c)) for c in range(128)] for t in range(32)])
 
 

@@ -13,7 +13,7 @@ kernel on algorithmic bytes (packed pages + tails + Q + O + block table).
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kitty|reference]
                        [--workload budget|budget_uniform|budget_k4|budget_84|budget_kv4|budget_fp16|
-                                   llama3_8b|qwen3_8b|qwen3_g1|qwen3_g2|long|tiny]
+                                   llama3_8b|llama3_70b|qwen3_8b|qwen3_g1|qwen3_g2|long|tiny]
 """
 
 from __future__ import annotations
@@ -314,6 +314,8 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
     import torch
     from mixed_precision_bit_gb300 import kitty
     L, B, Hq = spec["layers"], spec["B"], spec["Hq"]
+    # the fused append + decode takes query groups of at most 4
+    fused = bool(args.fused) and Hq // spec["Hkv"] <= 4
     cfg, layers = build_layers(spec, steps_total, pages_per_split=args.pages_per_split)
     nsets = max(1, min(4, W))  # every input set's graph is replayed (uploaded) in warm-up
     q_all, kn_all, vn_all = token_inputs(spec, nsets)
@@ -326,8 +328,8 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
         kvtok.append([lc.kv_tokens() for lc in layers])  # tokens each layer's call attends to
         # bytes of the timed call: the decode call, or the fused append + decode
         # (with graphs, a layer's call is timed with its append also when unfused)
-        algo.append([lc.algorithmic_bytes() + (lc.append_bytes(plans[-1][l], fused=bool(args.fused))
-                                               if args.fused or args.graphs else 0)
+        algo.append([lc.algorithmic_bytes() + (lc.append_bytes(plans[-1][l], fused=fused)
+                                               if fused or args.graphs else 0)
                      for l, lc in enumerate(layers)])
     fl_dev = torch.from_numpy(np.stack(plans)).cuda()
     splits, chunk = ((0, 0) if spec.get("f16kv")
@@ -342,7 +344,7 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
     if args.graphs:
         from mixed_precision_bit_gb300.cache import capture_layers_step
         graphs = [capture_layers_step(layers, kn_all[st], vn_all[st], fl_st, q_all[st], out,
-                                      fused=bool(args.fused)) for st in range(nsets)]
+                                      fused=fused) for st in range(nsets)]
 
     def step(s, events):
         st = s % nsets
@@ -351,10 +353,10 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
             graphs[st].replay()
             return
         for l, lc in enumerate(layers):
-            if not args.fused:
+            if not fused:
                 lc.append(kn_all[st, l], vn_all[st, l], fl_dev[s, l])
             events[l][0].record(stream)
-            if args.fused:
+            if fused:
                 lc.step(kn_all[st, l], vn_all[st, l], fl_dev[s, l], q_all[st, l], out[l])
             else:
                 lc.attend(q_all[st, l], out[l])
@@ -396,7 +398,7 @@ def device_run(args, spec, K, W, steps_total, world, rank, local_rank):
                 ms=ms, dec_ms=dec_ms,
                 dec_bytes=[algo[W + s][l] for s in range(K) for l in range(L)],
                 dec_tokens=[kvtok[W + s][l] for s in range(K) for l in range(L)],
-                clocks=clk, splits=splits, chunk=chunk)
+                clocks=clk, splits=splits, chunk=chunk, fused=fused)
 
 
 def target_measure(name, args, world, rank, local_rank, K=200, W=3):
@@ -447,7 +449,8 @@ def run_kitty(args, rank, world, local_rank):
     # ServingStep copies each layer's inputs up and its output back on side
     # streams, overlapped with the other layers' kernels.
     from mixed_precision_bit_gb300.cache import ServingStep
-    srv = ServingStep(layers, graphs=bool(args.graphs), fused=bool(args.fused))
+    fused = r0["fused"]
+    srv = ServingStep(layers, graphs=bool(args.graphs), fused=fused)
     for l in range(L):
         srv.q[l].copy_(q_all[0, l].cpu())
         srv.k_new[l].copy_(kn_all[0, l].cpu())
@@ -480,8 +483,8 @@ def run_kitty(args, rank, world, local_rank):
                 dec_tokens=dec_tokens,
                 quantize=quant,
                 clocks=clk, e2e_s=e2e_s, h2d=h2d, d2h=d2h, splits=splits, chunk=chunk,
-                gpu_launches=K * L * (2 if args.fused else 2 + launches_per_call),
-                max_pages=max_pages, pool_bytes=pool_bytes)
+                gpu_launches=K * L * (2 if fused else 2 + launches_per_call),
+                max_pages=max_pages, pool_bytes=pool_bytes, fused=fused)
 
 
 # ------------------------------------------------------------------ oracle (CPU) arm
@@ -634,8 +637,8 @@ def main():
     ap.add_argument("--impl", default="kitty", choices=["kitty", "reference"])
     ap.add_argument("--workload", default="budget",
                     choices=["budget", "budget_uniform", "budget_k4", "budget_84", "budget_kv4",
-                             "budget_fp16", "llama3_8b", "qwen3_8b", "qwen3_g1", "qwen3_g2", "long",
-                             "tiny"])
+                             "budget_fp16", "llama3_8b", "llama3_70b", "qwen3_8b", "qwen3_g1",
+                             "qwen3_g2", "long", "tiny"])
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (profiling)")
     ap.add_argument("--pages-per-split", type=int, default=0,
                     help="decode split-K chunk in pages (0: the library's choice)")
@@ -704,7 +707,7 @@ def main():
         "config": config_block(spec, {"parallelism": "replicas" if world > 1 else "single GPU",
                                       "splits": r["splits"], "pages_per_split": r["chunk"],
                                       "pool_bytes": r["pool_bytes"],
-                                      "launch": ("fused append + decode per layer" if args.fused
+                                      "launch": ("fused append + decode per layer" if r["fused"]
                                                  else "append, then decode, per layer") +
                                                 (", one CUDA graph per step" if args.graphs else ", direct calls")}),
         "kv_tokens_per_s": sum(r["dec_tokens"]) / (sum(r["dec_ms"]) / 1e3),
@@ -717,7 +720,7 @@ def main():
                      "traffic": (traffic_ratio * dec_bytes
                                  if traffic_ratio is not None and spec["name"] == "budget" else None),
                      "kernel": ("kitty_append_decode (decode_kernel with the append fused in + "
-                                "split combine)" if args.fused else
+                                "split combine)" if r["fused"] else
                                 "kitty_append_token + kitty_decode_attention" if args.graphs else
                                 "kitty_decode_attention (decode_kernel + split combine)"),
                      "peak_source": "%s (MEASURED_PEAKS.json hbm_gbs)" % peak_src,

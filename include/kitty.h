@@ -75,7 +75,10 @@ extern "C" {
 typedef struct {
   int32_t head_dim;     /* D; must be 128 */
   int32_t num_kv_heads; /* Hkv >= 1 */
-  int32_t num_q_heads;  /* Hq, a multiple of Hkv; decode needs Hq/Hkv <= 4 */
+  int32_t num_q_heads;  /* Hq, a multiple of Hkv.  Decode attention takes
+                           Hq/Hkv <= 32 (groups above 4 run as CTAs of 4
+                           query heads over the same pages); the fused append
+                           + decode and the 16-bit baseline take Hq/Hkv <= 4 */
   int32_t page_tokens;  /* tokens per page = Key quantization group; must be 32 */
   int32_t n_hi;         /* boosted Key channels per page: 0, 16, 32, ..., 128 */
   int32_t hi_bit;       /* (hi_bit, lo_bit) = (4, 2): Key channels 2-bit, boosted 4-bit as */

@@ -29,10 +29,14 @@
 //           Value group, p split the same way (high part exact times S_v, the
 //           rest rounded once), plus the sum_t p*M_v term.
 // Codes are unpacked with one AND per two: the planes are stored in fragment
-// order, so a masked 16-bit half is the fp16 subnormal code * 2^(2*tau - 24)
-// (2-bit planes) or code * 2^(4*(tau & 1) - 24) (4-bit Key planes); the power of
-// two depends only on the tile row and is folded into the score scale (Keys) or
-// the final output (Values).
+// order with every word rotated left by two bits, so a masked 16-bit half is
+// the fp16 subnormal code * 2^(2*tau + 2 - 24) (2-bit planes) or
+// code * 2^(4*(tau & 1) + 2 - 24) (4-bit planes); the power of two depends only
+// on the tile row and is folded into the score scale (Keys) or the final output
+// (Values).  The rotation keeps the codes out of the lowest mantissa bits:
+// measured on the GB300, the PV products of codes in mantissa bits 0-1 kept an
+// error near 2^-13 of the output's scale over an 8192-token sequence, 4 to 8
+// times that of the next two bits up.
 #include "kitty_common.cuh"
 #include "quant_tile.cuh"
 #include "host_common.h"
@@ -50,6 +54,16 @@ constexpr int kDWarps = 4;
 // larger blobs would otherwise allow only 2 CTAs per SM.
 __host__ __device__ constexpr int stages_for(int w) { return w == 4 ? 3 : 4; }
 constexpr int kDMinBlocks = 4;  // resident CTAs per SM the register budget is sized for
+// An unpacked code c of tile-row class tau has the fp16 value
+// c * 2^(row exponent - kCodeExp): the smallest fp16 subnormal is 2^-24, and the
+// planes' two-bit rotation lifts every code by 2^2.
+constexpr int kCodeExp = 22;
+// Query heads per CTA: the 8 columns of an m16n8k16 B operand hold 4 heads as
+// (high, low) pairs.  Larger groups (g = Hq/Hkv up to kMaxGroup) take
+// ceil(g / 4) head-group CTAs per (sequence, kv head, split), adjacent in the
+// grid, which read the same pages (the second read mostly from L2).
+constexpr int kHeadsPerCta = 4;
+constexpr int kMaxGroup = 32;
 constexpr int kDThreads = kDWarps * 32;
 // a flush quantizes the tail in the stage buffers: they must hold the page
 // quantizer's shared state at the smallest blob (n_hi = 0) of either width
@@ -100,7 +114,7 @@ struct DecodeParams {
   int32_t* d_status;
   float sm_log2;  // sm_scale * log2(e)
   uint32_t wait_polls;  // bound of a page wait, in polls of its barrier
-  int pool_pages, max_pages, out_dtype, splits, Hkv, Hq, g, n_hi, blob, in_dtype;
+  int pool_pages, max_pages, out_dtype, splits, Hkv, Hq, g, HG, n_hi, blob, in_dtype;  // HG: head groups
   // Split s of a sequence with np pages covers pages [starts[s], min(np, starts[s+1]));
   // starts[] rises from 0 to starts[splits] = max_pages.  A split holds work only
   // when it holds a page, except split 0, which always runs (it takes the tail
@@ -210,9 +224,9 @@ struct Off {
   static constexpr int vb = kch + 16 * NX, vs = vb + 512 * V, vm = vs + 256, bytes = vm + 256;
 };
 
-// Power of two (exponent + 24) that an unpacked Value code of channel-tile row
-// (m-tile mc, 8-row half rh) carries: 2-bit planes place rows at bit 2*tau
-// (tau = 2*(mc & 1) + rh), 4-bit planes at bit 4*rh.
+// Power of two (exponent + kCodeExp) that an unpacked Value code of
+// channel-tile row (m-tile mc, 8-row half rh) carries: 2-bit planes place rows
+// at bit 2*tau + 2 (tau = 2*(mc & 1) + rh), 4-bit planes at bit 4*rh + 2.
 __host__ __device__ constexpr int vrow_exp(int V, int mc, int rh) {
   return V == 4 ? 4 * rh : 2 * (2 * (mc & 1) + rh);
 }
@@ -252,19 +266,22 @@ __device__ __forceinline__ void rescale(WarpState& w, float pm) {
   }
 }
 
+// Unpack of a rotated 2-bit plane word: tau 0, 1 (codes in mantissa bits 2-3,
+// 4-5) or tau 2, 3 (bits 6-7, 8-9); the word rotated by 8 holds the tile's
+// columns 8..15 in the same places.
 __device__ __forceinline__ void unpack_rows01(uint32_t x, uint32_t* a) {  // tau 0,1
-  const uint32_t x2 = x >> 8;
-  a[0] = x & 0x00030003u; a[1] = x & 0x000C000Cu; a[2] = x2 & 0x00030003u; a[3] = x2 & 0x000C000Cu;
+  const uint32_t x2 = __funnelshift_r(x, x, 8);
+  a[0] = x & 0x000C000Cu; a[1] = x & 0x00300030u; a[2] = x2 & 0x000C000Cu; a[3] = x2 & 0x00300030u;
 }
-// 4-bit planes: one word is one A fragment (rows r, r+8 = nibbles 0, 1 of each
-// byte; the high byte holds the tile's columns 8..15).
+// 4-bit planes: one word is one A fragment (rows r, r+8 = mantissa bits 2-5,
+// 6-9 of each 16-bit half; the word rotated by 8 holds columns 8..15).
 __device__ __forceinline__ void unpack_nib(uint32_t x, uint32_t* a) {
-  const uint32_t x2 = x >> 8;
-  a[0] = x & 0x000F000Fu; a[1] = x & 0x00F000F0u; a[2] = x2 & 0x000F000Fu; a[3] = x2 & 0x00F000F0u;
+  const uint32_t x2 = __funnelshift_r(x, x, 8);
+  a[0] = x & 0x003C003Cu; a[1] = x & 0x03C003C0u; a[2] = x2 & 0x003C003Cu; a[3] = x2 & 0x03C003C0u;
 }
 __device__ __forceinline__ void unpack_rows23(uint32_t x, uint32_t* a) {  // tau 2,3
-  const uint32_t x2 = x >> 8;
-  a[0] = x & 0x00300030u; a[1] = x & 0x00C000C0u; a[2] = x2 & 0x00300030u; a[3] = x2 & 0x00C000C0u;
+  const uint32_t x2 = __funnelshift_r(x, x, 8);
+  a[0] = x & 0x00C000C0u; a[1] = x & 0x03000300u; a[2] = x2 & 0x00C000C0u; a[3] = x2 & 0x03000300u;
 }
 
 // Scores of one staged (page, kv-head) blob, in log2 units: s[2*mt + rh] is
@@ -395,15 +412,19 @@ __device__ __forceinline__ void pair_beta(const uint32_t paA, const uint32_t paB
 }
 
 // Probabilities of one page against the running max, split into a high part
-// with 4 significant bits (exact times a 7-bit Value step) and the rest, as
-// fp16, and transposed into PV B fragments (column 2h = high, 2h+1 = rest).
+// rounded to 4 significant bits (exact times a 7-bit Value step) and the rest
+// (signed, at most 2^-4 of p), as fp16, and transposed into PV B fragments
+// (column 2h = high, 2h+1 = rest).  Rounding the high part rather than
+// truncating it halves the rest, and with it the two fp16 roundings the rest
+// takes (its own and its product with the step).  p <= 1, so the rounded
+// high part stays finite.
 __device__ __forceinline__ void page_probs(WarpState& w, const float (&s)[4], uint32_t (&T)[4]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const float p = ex2(s[i] - w.m);
     w.l += p;
-    const float t = __uint_as_float(__float_as_uint(p) & 0xFFF00000u);  // 4 significant bits
-    T[i] = movmatrix_t(h2_bits(__floats2half2_rn(t, p - t)));          // (high, rest) -> B columns
+    const float t = __uint_as_float((__float_as_uint(p) + 0x00080000u) & 0xFFF00000u);
+    T[i] = movmatrix_t(h2_bits(__floats2half2_rn(t, p - t)));  // (high, rest) -> B columns
   }
 }
 
@@ -425,8 +446,8 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
   }
 
   // ---------------- PV with the Value step folded into this lane's part of P
-  // (high part: exact product; the rest: rounded once, relative 2^-12 of a
-  // term below 2^-3 of p)
+  // (high part: exact product; the rest: rounded once, relative 2^-11 of a
+  // term of at most 2^-4 of p)
   // 2-bit Values: a lane's 8 bytes of group G are words (kt = 0, 1), each
   // holding both m-tiles; 4-bit Values: its 16 bytes are words (kt, m-tile
   // parity), each one A fragment
@@ -540,7 +561,7 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
 #pragma unroll
       for (int rh = 0; rh < 2; ++rh) {
         const int c = 16 * mc + 8 * rh;
-        const float rs = __uint_as_float((uint32_t)(127 - 24 + vrow_exp(V, mc, rh)) << 23);
+        const float rs = __uint_as_float((uint32_t)(127 - kCodeExp + vrow_exp(V, mc, rh)) << 23);
         w.acc[mc][2 * rh] += pi * (bits16_to_f32(ld_s16r(vb + i * 2 * kD + 2 * c), DT) * rs);
       }
   }
@@ -577,7 +598,10 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   extern __shared__ __align__(128) uint8_t dsm[];
   trigger_dependents();  // the combine step may be scheduled once every CTA is running
   const int u = blockIdx.x, s = blockIdx.y;
-  const int b = u / p.Hkv, kvh = u - b * p.Hkv;
+  const int bk = u / p.HG, hgi = u - bk * p.HG;  // (sequence, kv head), head group
+  const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
+  const int h0 = kvh * p.g + kHeadsPerCta * hgi;            // first query head of this CTA
+  const int gh = min(kHeadsPerCta, p.g - kHeadsPerCta * hgi);  // its query heads
   const int tid = threadIdx.x, wid = tid >> 5;
   const Lane L;
   const int lane = L.lane, r = L.r, qq = L.qq;
@@ -595,7 +619,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   float qv[4];
 #pragma unroll
   for (int h = 0; h < 4; ++h)
-    qv[h] = h < p.g ? load16<DT>(p.q + ((size_t)b * p.Hq + (size_t)kvh * p.g + h) * kD + tid) : 0.f;
+    qv[h] = h < gh ? load16<DT>(p.q + ((size_t)b * p.Hq + h0 + h) * kD + tid) : 0.f;
   // the tensor cores take the query as fp16: a value it cannot hold is reported
   // (it would turn the scores of the query group into inf or NaN)
   if (s == 0) {
@@ -607,14 +631,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   const bool lens_ok =
       !(np < 0 || np > p.max_pages || tl < 0 || tl > kPage || (tl > 0 && p.tail_k == nullptr));
   if (!lens_ok) {  // nothing is appended either
-    if (tid == 0 && s == 0 && kvh == 0) set_status(p.d_status, KITTY_ST_BAD_LEN);
+    if (tid == 0 && s == 0 && kvh == 0 && hgi == 0) set_status(p.d_status, KITTY_ST_BAD_LEN);
     np = 0;
     tl = 0;
   }
   if (!split_active(p, s, np)) {
     // no pages here: mark the partials empty (the combine then needs no lengths)
-    if (tid < p.g)
-      p.ws[(((size_t)b * p.Hq + (size_t)kvh * p.g + tid) * p.splits + s) * kPartial] = -INFINITY;
+    if (tid < gh) p.ws[(((size_t)b * p.Hq + h0 + tid) * p.splits + s) * kPartial] = -INFINITY;
     return;
   }
   const int pbeg = sbeg, pend = min(np, send);
@@ -751,7 +774,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   for (int tau = 0; tau < 4; ++tau)
     // a code sits at 2^(2 tau - 24) (2-bit planes) or 2^(4 (tau & 1) - 24) (4-bit)
     kscale[tau] = p.sm_log2 *
-                  __uint_as_float((uint32_t)(127 + 24 - (W == 2 ? 2 * tau : 4 * (tau & 1))) << 23);
+                  __uint_as_float((uint32_t)(127 + kCodeExp - (W == 2 ? 2 * tau : 4 * (tau & 1))) << 23);
 
   WarpState w;
 #pragma unroll
@@ -876,7 +899,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
     for (int i = 0; i < 4; ++i) {
       const int rh = i >> 1;
       const int row = 16 * mc + 8 * rh + r;
-      const float sc = __uint_as_float((uint32_t)(127 + 24 - vrow_exp(V, mc, rh)) << 23);
+      const float sc = __uint_as_float((uint32_t)(127 + kCodeExp - vrow_exp(V, mc, rh)) << 23);
       Ow[row * 8 + 2 * qq + (i & 1)] = w.acc[mc][i] * sc;
     }
   if (r < 4) {
@@ -927,8 +950,8 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   }
 #pragma unroll
   for (int h = 0; h < 4; ++h) {
-    if (h >= p.g) break;
-    const int hq = kvh * p.g + h;
+    if (h >= gh) break;
+    const int hq = h0 + h;
     if (p.splits == 1) {
       store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c,
                 Lsum[h] > 0.f ? Osum[h] / Lsum[h] : 0.f);
@@ -1077,6 +1100,12 @@ size_t decode_smem(int blob, int w) {
   return (size_t)kDWarps * st * blob + kDWarps * st * sizeof(uint64_t) + (4 * kD + 8 * kQx) * 2;
 }
 
+// Head-group CTAs per (sequence, kv head, split): ceil(g / 4).
+int head_groups(const kitty_cfg* cfg) {
+  const int g = cfg->num_q_heads / cfg->num_kv_heads;
+  return (g + kHeadsPerCta - 1) / kHeadsPerCta;
+}
+
 // CTAs of the decode kernel resident at once on the device: kDMinBlocks per SM
 // unless shared memory allows fewer (large n_hi).
 long resident_ctas(int blob, int w) {
@@ -1097,8 +1126,8 @@ struct Schedule {
   int32_t starts[kMaxSplits + 1];
 };
 
-// Split sizes, in dispatch order, for `units` (sequence, kv head) pairs of up to
-// M pages on `slots` resident CTAs.
+// Split sizes, in dispatch order, for the (sequence, kv head, head group) units
+// of up to M pages on `slots` resident CTAs.
 //  * fixed > 0: splits of `fixed` pages (raised to ceil(M / kMaxSplits) if that
 //    is larger), the remainder last.
 //  * fixed = 0: sizes that shrink towards the end of the grid.  Built from the
@@ -1133,12 +1162,12 @@ void plan(const kitty_cfg* cfg, int B, int M, int blob, Schedule* sc) {
   } else {
     const long slots = resident_ctas(blob, cfg->lo_bit);
     const bool hinted = cfg->decode_total_pages > 0;
-    const double rho = (hinted ? 2.0 : 1.0) * (double)B * cfg->num_kv_heads / (double)slots;
-    const long fair = hinted ? (long)cfg->num_kv_heads * cfg->decode_total_pages / slots / 8 * 8
-                             : (1L << 30);
+    const long heads = (long)cfg->num_kv_heads * head_groups(cfg);  // CTAs per sequence and split
+    const double rho = (hinted ? 2.0 : 1.0) * (double)B * heads / (double)slots;
+    const long fair = hinted ? heads * cfg->decode_total_pages / slots / 8 * 8 : (1L << 30);
     const int Ms = cfg->decode_max_pages > 0 ? std::min(M, cfg->decode_max_pages) : M;
-    const double work = hinted ? (double)cfg->num_kv_heads * cfg->decode_total_pages
-                               : (double)B * cfg->num_kv_heads * Ms;  // page-heads (at most)
+    const double work = hinted ? (double)heads * cfg->decode_total_pages
+                               : (double)B * heads * Ms;  // page-heads (at most)
     const int m0 = work < 64.0 * (double)slots ? 32 : 16;
     long T = 0;
     for (int m = m0;; m *= 2) {
@@ -1185,7 +1214,7 @@ size_t workspace_bytes(const kitty_cfg* cfg, int B, const Schedule& sc) {
 
 extern "C" int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pages,
                                  int32_t* splits, int32_t* pages_per_split) {
-  int rc = check_cfg(cfg, true);
+  int rc = check_cfg(cfg, kMaxGroup);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !splits || !pages_per_split) return KITTY_ERR_INVALID_ARG;
   Schedule sc;
@@ -1197,7 +1226,7 @@ extern "C" int kitty_decode_plan(const kitty_cfg* cfg, int32_t B, int32_t max_pa
 
 extern "C" int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pages,
                                             size_t* bytes) {
-  int rc = check_cfg(cfg, true);
+  int rc = check_cfg(cfg, kMaxGroup);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !bytes) return KITTY_ERR_INVALID_ARG;
   Schedule sc;
@@ -1214,7 +1243,7 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
               const void* tail_k, const void* tail_v, const int32_t* tail_len, float sm_scale,
               void* out, int32_t out_dtype, void* workspace, size_t workspace_bytes_in, int32_t B,
               int32_t* d_status, void* stream, const AppendParams& ap) {
-  int rc = check_cfg(cfg, true);
+  int rc = check_cfg(cfg, kMaxGroup);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
   if (out_dtype != KITTY_F32 && out_dtype != KITTY_BF16 && out_dtype != KITTY_F16)
@@ -1254,12 +1283,13 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
   p.Hkv = cfg->num_kv_heads;
   p.Hq = cfg->num_q_heads;
   p.g = cfg->num_q_heads / cfg->num_kv_heads;
+  p.HG = head_groups(cfg);
   p.n_hi = cfg->n_hi;
   p.blob = blob;
   p.in_dtype = cfg->in_dtype;
   const size_t smem = decode_smem(p.blob, cfg->lo_bit);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  dim3 grid((unsigned)B * cfg->num_kv_heads, sc.splits);
+  dim3 grid((unsigned)B * cfg->num_kv_heads * p.HG, sc.splits);
   const int nx = cfg->n_hi / 16, v = v_bits(cfg);
   const cudaError_t e = cfg->in_dtype == KITTY_BF16
       ? (cfg->lo_bit == 4 ? (v == 4 ? launch_decode_nx<KITTY_BF16, 4, 4>(nx, grid, smem, s, p)
@@ -1314,7 +1344,7 @@ extern "C" int kitty_append_decode(const kitty_cfg* cfg, const void* k_new, cons
                                    int32_t pool_pages, float sm_scale, void* out, int32_t out_dtype,
                                    void* workspace, size_t workspace_bytes, int32_t B,
                                    int32_t* d_status, void* stream) {
-  int rc = check_cfg(cfg, true);
+  int rc = check_cfg(cfg, kHeadsPerCta);  // one CTA per (sequence, kv head) owns the append
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
   if (B == 0) return KITTY_OK;

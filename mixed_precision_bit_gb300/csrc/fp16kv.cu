@@ -439,7 +439,7 @@ using namespace kitty;
 
 extern "C" int kitty_f16kv_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob,
                                       size_t* per_page) {
-  const int rc = check_cfg(cfg, false);
+  const int rc = check_cfg(cfg);
   if (rc != KITTY_OK) return rc;
   if (per_head_blob) *per_head_blob = kFBlob;
   if (per_page) *per_page = (size_t)kFBlob * cfg->num_kv_heads;
@@ -449,7 +449,7 @@ extern "C" int kitty_f16kv_page_bytes(const kitty_cfg* cfg, size_t* per_head_blo
 extern "C" int kitty_f16kv_write_pages(const kitty_cfg* cfg, const void* k, const void* v,
                                        int32_t n_pages, const int32_t* page_ids, void* pool,
                                        int32_t pool_pages, int32_t* d_status, void* stream) {
-  const int rc = check_cfg(cfg, false);
+  const int rc = check_cfg(cfg);
   if (rc != KITTY_OK) return rc;
   if (n_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
   if (n_pages == 0) return KITTY_OK;
@@ -468,7 +468,7 @@ extern "C" int kitty_f16kv_append(const kitty_cfg* cfg, const void* k_new, const
                                   int32_t max_pages, int32_t* ctx_len,
                                   const int32_t* new_page_ids, int32_t B, int32_t* d_status,
                                   void* stream) {
-  const int rc = check_cfg(cfg, false);
+  const int rc = check_cfg(cfg);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
   if (B == 0) return KITTY_OK;
@@ -487,7 +487,7 @@ extern "C" int kitty_f16kv_append(const kitty_cfg* cfg, const void* k_new, const
 
 extern "C" int kitty_f16kv_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pages,
                                            size_t* bytes) {
-  const int rc = check_cfg(cfg, true);
+  const int rc = check_cfg(cfg, 4);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || !bytes) return KITTY_ERR_INVALID_ARG;
   int splits = 1, pps = 1;
@@ -502,7 +502,7 @@ extern "C" int kitty_f16kv_decode(const kitty_cfg* cfg, const void* q, const voi
                                   void* out, int32_t out_dtype, void* workspace,
                                   size_t workspace_bytes, int32_t B, int32_t* d_status,
                                   void* stream) {
-  const int rc = check_cfg(cfg, true);
+  const int rc = check_cfg(cfg, 4);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
   if (out_dtype != KITTY_F32 && out_dtype != KITTY_BF16 && out_dtype != KITTY_F16)

@@ -18,7 +18,7 @@ struct kitty_alloc {
 extern "C" int kitty_abi_version(void) { return 5; }
 
 extern "C" int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, size_t* per_page) {
-  const int rc = check_cfg(cfg, false);
+  const int rc = check_cfg(cfg);
   if (rc != KITTY_OK) return rc;
   const size_t b = blob_bytes(cfg->n_hi, cfg->lo_bit, kitty::v_bits(cfg));
   if (per_head_blob) *per_head_blob = b;
@@ -28,7 +28,7 @@ extern "C" int kitty_page_bytes(const kitty_cfg* cfg, size_t* per_head_blob, siz
 
 // hi_fraction * hi_bit + (1 - hi_fraction) * lo_bit, hi_fraction = n_hi / D.
 extern "C" float kitty_avg_bits(const kitty_cfg* cfg) {
-  if (check_cfg(cfg, false) != KITTY_OK) return -1.0f;
+  if (check_cfg(cfg) != KITTY_OK) return -1.0f;
   const double hf = (double)cfg->n_hi / cfg->head_dim;
   return (float)(hf * cfg->hi_bit + (1.0 - hf) * cfg->lo_bit);
 }

@@ -10,8 +10,9 @@ namespace kitty {
 
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// Checks the fixed parameters; decode additionally needs Hq/Hkv <= 4.
-inline int check_cfg(const kitty_cfg* c, bool decode) {
+// Checks the fixed parameters; max_group > 0 also bounds the query group Hq/Hkv
+// (the calls that attend).
+inline int check_cfg(const kitty_cfg* c, int max_group = 0) {
   if (c == nullptr) return KITTY_ERR_INVALID_ARG;
   if (c->num_kv_heads <= 0 || c->num_q_heads <= 0 || c->num_q_heads % c->num_kv_heads != 0)
     return KITTY_ERR_INVALID_ARG;
@@ -31,7 +32,7 @@ inline int check_cfg(const kitty_cfg* c, bool decode) {
   if (c->decode_pages_per_split < 0 || c->decode_total_pages < 0 || c->decode_max_pages < 0 ||
       c->decode_wait_polls < 0)
     return KITTY_ERR_INVALID_ARG;
-  if (decode && c->num_q_heads / c->num_kv_heads > 4) return KITTY_ERR_UNSUPPORTED;
+  if (max_group > 0 && c->num_q_heads / c->num_kv_heads > max_group) return KITTY_ERR_UNSUPPORTED;
   return KITTY_OK;
 }
 

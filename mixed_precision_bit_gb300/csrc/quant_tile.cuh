@@ -424,10 +424,26 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     }
   }
   __syncthreads();
-
+  // Copy out.  The planes' words are stored rotated left by two bits: a code
+  // masked out of its 16-bit half then sits two bits higher in the fp16
+  // mantissa (the decode folds the factor 4 into its scales).  The rotated
+  // words also go back to shared memory, where a fused decode attends to a
+  // flushed page.  Plane boundaries (ks, vbase, vbase + 512 V) are multiples
+  // of 16 bytes.
   uint4* d4 = reinterpret_cast<uint4*>(dst);
-  const uint4* s4 = reinterpret_cast<const uint4*>(sm.blob);
-  for (int i = tid; i < lay.bytes / 16; i += kQThreads) d4[i] = s4[i];
+  uint4* s4 = reinterpret_cast<uint4*>(sm.blob);
+  for (int i = tid; i < lay.bytes / 16; i += kQThreads) {
+    uint4 x = s4[i];
+    const int b = 16 * i;
+    if (b < lay.ks || (b >= lay.vbase && b < lay.vs)) {
+      x.x = __funnelshift_l(x.x, x.x, 2);
+      x.y = __funnelshift_l(x.y, x.y, 2);
+      x.z = __funnelshift_l(x.z, x.z, 2);
+      x.w = __funnelshift_l(x.w, x.w, 2);
+      s4[i] = x;
+    }
+    d4[i] = x;
+  }
   if (tid == 0 && sm.bad) set_status(d_status, sm.bad);
   __syncthreads();
 }

@@ -359,7 +359,7 @@ extern "C" int kitty_quantize_pages(const kitty_cfg* cfg, const void* k, const v
                                     const int32_t* seq_of_page, int32_t n_seqs, float* run_sum,
                                     float* run_sumsq, int32_t* run_count, void* pool,
                                     int32_t pool_pages, int32_t* d_status, void* stream) {
-  int rc = check_cfg(cfg, false);
+  int rc = check_cfg(cfg);
   if (rc != KITTY_OK) return rc;
   if (n_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
   if (n_pages == 0) return KITTY_OK;
@@ -413,7 +413,7 @@ extern "C" int kitty_append_token(const kitty_cfg* cfg, const void* k_new, const
                                   const int32_t* flush_page_ids, int32_t* block_table,
                                   int32_t max_pages, int32_t* num_pages, void* pool,
                                   int32_t pool_pages, int32_t B, int32_t* d_status, void* stream) {
-  int rc = check_cfg(cfg, false);
+  int rc = check_cfg(cfg);
   if (rc != KITTY_OK) return rc;
   if (B < 0 || max_pages < 0 || pool_pages < 0) return KITTY_ERR_INVALID_ARG;
   if (B == 0) return KITTY_OK;

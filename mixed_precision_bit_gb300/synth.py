@@ -130,6 +130,8 @@ def workload(name: str, seed: int = 0) -> Workload:
     qwen3_8b   64 seqs, 32/8 heads, bf16, 8192 tokens (256 pages) + tail U{0..31}, n_hi=16
     long       8 seqs, 32/8 heads, bf16, lengths U[16384, 65536], n_hi=32, channel
                scales redrawn every 4096 tokens
+    llama3_70b 16 seqs, 64/8 heads (query groups of 8), bf16, 8192 tokens (256
+               pages) + tail U{0..31}, n_hi=32
     small_gqa  parity-size GQA case: 3 seqs, 8/2 heads, bf16, ragged lengths
     qwen3_g1, qwen3_g2
                qwen3_8b with 8 / 16 query heads (query groups of 1 and 2): the
@@ -146,6 +148,9 @@ def workload(name: str, seed: int = 0) -> Workload:
     if name == "long":
         L = 16384 + (bits(seed, "long/len", 8) % np.uint64(65536 - 16384 + 1)).astype(np.int64)
         return Workload(name, 8, 32, 8, 32, BF16, L // PAGE, L % PAGE, drift=4096)
+    if name == "llama3_70b":
+        tails = (bits(seed, "llama3_70b/tail", 16) % np.uint64(32)).astype(np.int64)
+        return Workload(name, 16, 64, 8, 32, BF16, np.full(16, 256), tails)
     if name == "small_gqa":
         return Workload(name, 3, 8, 2, 32, BF16, np.array([5, 0, 9]), np.array([7, 3, 31]))
     raise KeyError(name)

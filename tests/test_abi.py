@@ -58,15 +58,27 @@ def test_page_bytes_and_avg_bits(K):
 def test_config_checks(K):
     for bad, code in ((dict(n_hi=8), -2), (dict(head_dim=64), -2), (dict(hi_bit=8), -2),
                       (dict(lo_bit=4), -2), (dict(hi_bit=6, lo_bit=3), -2),
-                      (dict(num_q_heads=12), -1), (dict(in_dtype=7), -1)):
+                      (dict(num_q_heads=12), -1), (dict(in_dtype=7), -1),
+                      (dict(v_bit=4), -2), (dict(v_bit=3, hi_bit=8, lo_bit=4), -2)):
         cfg = K.Config(**{**dict(num_kv_heads=8, num_q_heads=32), **bad})
         with pytest.raises(K.KittyError) as e:
             K.page_bytes(cfg)
         assert e.value.code == code
-    cfg = K.Config(num_kv_heads=8, num_q_heads=64)   # g = 8: quantize ok, decode unsupported
+    # query groups: decode takes g <= 32 (head groups of 4), the fused append + decode g <= 4
+    cfg = K.Config(num_kv_heads=8, num_q_heads=64)   # g = 8
+    K.page_bytes(cfg)
+    assert K.decode_workspace_bytes(cfg, 4, 16) >= 0
+    lib = K.load()
+    rc = lib.kitty_append_decode(ctypes.byref(cfg.c()), *([None] * 11), 16, None, None, 1, 0.1,
+                                 None, 0, None, 0, 1, None, None)
+    assert rc == -2
+    cfg = K.Config(num_kv_heads=1, num_q_heads=33)   # g = 33: quantize ok, decode unsupported
     K.page_bytes(cfg)
     with pytest.raises(K.KittyError):
         K.decode_workspace_bytes(cfg, 4, 16)
+    # 4-bit Values with 4-bit Key planes: the Value plane doubles
+    cfg = K.Config(num_kv_heads=8, num_q_heads=32, n_hi=0, hi_bit=8, lo_bit=4, v_bit=4)
+    assert K.page_bytes(cfg) == (5120, 8 * 5120)
 
 
 def test_allocator(K):

@@ -42,7 +42,7 @@ def _oracle_seq_pool(spec, k, v, running):
 
 
 @pytest.mark.parametrize("name", ["llama3_8b", "qwen3_8b", "long", "budget", "budget_84",
-                                  "budget_kv4"])
+                                  "budget_kv4", "llama3_70b"])
 def test_fullsize_sampled(name):
     import torch
     import bench

@@ -40,6 +40,9 @@ CASES = [
     ("small_gqa", dict(Hq=2, Hkv=2)),            # g = 1
     ("small_gqa", dict(Hq=6, Hkv=3)),            # g = 2
     ("small_gqa", dict(Hq=6, Hkv=2)),            # g = 3
+    ("small_gqa", dict(Hq=16, Hkv=2)),           # g = 8: two head-group CTAs
+    ("small_gqa", dict(Hq=10, Hkv=2, n_hi=16)),  # g = 5: a group of 4 and one of 1
+    ("small_gqa", dict(Hq=12, Hkv=1, dtype=synth.F16)),  # g = 12
     # (hi_bit, lo_bit) = (8, 4): two 4-bit Key planes
     ("tiny", dict(lo_bit=4)),
     ("small_gqa", dict(lo_bit=4)),
@@ -53,6 +56,7 @@ CASES = [
     ("small_gqa", dict(lo_bit=4, v_bit=4)),
     ("small_gqa", dict(lo_bit=4, v_bit=4, n_hi=128, dtype=synth.F16)),
     ("small_gqa", dict(lo_bit=4, v_bit=4, n_hi=16, Hq=6, Hkv=2)),
+    ("small_gqa", dict(lo_bit=4, v_bit=4, n_hi=0, Hq=16, Hkv=2)),
 ]
 
 

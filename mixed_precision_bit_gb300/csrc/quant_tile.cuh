@@ -96,8 +96,9 @@ __device__ __forceinline__ QuantParams qparams(float mn, float mx, int levels, b
 // Codes of four values: code = clamp(rint((x - M) * (1/u)), 0, L), the
 // subtraction and the product rounded to nearest fp32 (two at a time as packed
 // fp32x2 operations, the same roundings), 1/u the correctly rounded
-// reciprocal, rint to the nearest integer (ties to even).  A saturating
-// conversion clamps below at 0, min() above at L.
+// reciprocal, rint to the nearest integer (ties to even).  The conversion to
+// an unsigned integer rounds to nearest even and saturates (a negative
+// quotient gives 0); min() clamps above at L.
 __device__ __forceinline__ void qcode4(const float (&x)[4], const QuantParams& q, int levels,
                                        uint32_t (&code)[4]) {
   float d[4], y[4];
@@ -106,7 +107,30 @@ __device__ __forceinline__ void qcode4(const float (&x)[4], const QuantParams& q
   mul2_rn(y[0], y[1], d[0], d[1], q.ru, q.ru);
   mul2_rn(y[2], y[3], d[2], d[3], q.ru, q.ru);
 #pragma unroll
-  for (int k = 0; k < 4; ++k) code[k] = min(__float2uint_rz(rintf(y[k])), (uint32_t)levels);
+  for (int k = 0; k < 4; ++k) code[k] = min(__float2uint_rn(y[k]), (uint32_t)levels);
+}
+
+// Minimum and maximum of two packed 16-bit values per word (bf16x2 or f16x2):
+// the order of the values, with -0 below +0 as in the fp32 min/max.
+template <int DT>
+__device__ __forceinline__ uint32_t min2_16(uint32_t a, uint32_t b) {
+  if (DT == KITTY_BF16) {
+    const __nv_bfloat162 r = __hmin2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+  const __half2 r = __hmin2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
+}
+template <int DT>
+__device__ __forceinline__ uint32_t max2_16(uint32_t a, uint32_t b) {
+  if (DT == KITTY_BF16) {
+    const __nv_bfloat162 r = __hmax2(*reinterpret_cast<const __nv_bfloat162*>(&a),
+                                     *reinterpret_cast<const __nv_bfloat162*>(&b));
+    return *reinterpret_cast<const uint32_t*>(&r);
+  }
+  const __half2 r = __hmax2(*reinterpret_cast<const __half2*>(&a), *reinterpret_cast<const __half2*>(&b));
+  return *reinterpret_cast<const uint32_t*>(&r);
 }
 
 // One byte of four 2-bit codes, at bits 0, 2, 4, 6.
@@ -319,6 +343,7 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
   {
     const int t = tid >> 2, G = tid & 3;
     float v[kVGroup];
+    uint32_t pmn = 0u, pmx = 0u;  // packed pairwise minima and maxima in the input type
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
       const uint4 w4 = *reinterpret_cast<const uint4*>(&sm.xv[t][G * kVGroup + 8 * k]);
@@ -327,11 +352,13 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
       for (int i = 0; i < 4; ++i) {
         v[8 * k + 2 * i] = bits16_to_f32((uint16_t)(ww[i] & 0xFFFFu), DT);
         v[8 * k + 2 * i + 1] = bits16_to_f32((uint16_t)(ww[i] >> 16), DT);
+        pmn = (k | i) ? min2_16<DT>(pmn, ww[i]) : ww[i];
+        pmx = (k | i) ? max2_16<DT>(pmx, ww[i]) : ww[i];
       }
     }
-    float vmn = v[0], vmx = v[0];
-#pragma unroll
-    for (int i = 1; i < kVGroup; ++i) { vmn = fminf(vmn, v[i]); vmx = fmaxf(vmx, v[i]); }
+    // the min / max of 16-bit values are exact in their own type
+    const float vmn = fminf(bits16_to_f32((uint16_t)(pmn & 0xFFFFu), DT), bits16_to_f32((uint16_t)(pmn >> 16), DT));
+    const float vmx = fmaxf(bits16_to_f32((uint16_t)(pmx & 0xFFFFu), DT), bits16_to_f32((uint16_t)(pmx >> 16), DT));
     constexpr int kVLevels = (1 << V) - 1;
     const QuantParams q = qparams(vmn, vmx, kVLevels, false);
     // Value metadata in fragment order: token 16kt + 8h + 2qq + e at G*32 + qq*8 + kt*4 + h*2 + e

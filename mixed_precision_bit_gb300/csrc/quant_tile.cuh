@@ -23,7 +23,7 @@ constexpr int kMaxBlobWords = (5120 + 17 * kD) / 4;  // largest blob: (8, 4), 4-
 
 constexpr int kRowH = kD + 8;  // 16-bit elements per staged row (16-byte pad: fewer bank conflicts)
 
-struct QuantSmem {
+struct __align__(16) QuantSmem {  // 16-byte vector accesses to xk, xv and blob
   uint16_t xk[kPage][kRowH];  // raw 16-bit inputs, token-major
   uint16_t xv[kPage][kRowH];
   uint32_t blob[kMaxBlobWords];

@@ -113,7 +113,12 @@ class LayerCache:
 
     def step(self, k_new, v_new, flush_ids, q, out, sm_scale=None, stream=None):
         """append(k_new, v_new, flush_ids) then attend(q, out) as one fused launch
-        (plus the split combine)."""
+        (plus the split combine).  The fused call takes query groups of at most 4
+        heads per kv head; larger groups make the two calls."""
+        if self.cfg.num_q_heads // self.cfg.num_kv_heads > 4:
+            self.append(k_new, v_new, flush_ids, stream=stream)
+            self.attend(q, out, sm_scale, stream=stream)
+            return
         sm = 1.0 / math.sqrt(D) if sm_scale is None else sm_scale
         kitty.append_decode(self.cfg, k_new, v_new, q, self.tail_k, self.tail_v, self.tail_len,
                             self.run_sum, self.run_sumsq, self.run_count, flush_ids,

@@ -46,12 +46,15 @@ def _layers(L, B, Hkv, Hq, n_hi, pages, tails, gen):
     return out
 
 
-@pytest.mark.parametrize("graphs,fused", [(True, True), (False, True), (True, False)],
-                         ids=["graphs", "direct", "graphs-unfused"])
-def test_serving_step_matches_per_layer_calls(graphs, fused):
+@pytest.mark.parametrize("graphs,fused,Hq", [(True, True, 8), (False, True, 8), (True, False, 8),
+                                             (True, True, 16)],
+                         ids=["graphs", "direct", "graphs-unfused", "graphs-g8"])
+def test_serving_step_matches_per_layer_calls(graphs, fused, Hq):
+    """Hq = 16 (query groups of 8): the step makes the append and the decode as
+    two calls, and must equal them made directly."""
     import torch
     from mixed_precision_bit_gb300.cache import ServingStep
-    L, B, Hkv, Hq, n_hi = 3, 5, 2, 8, 32
+    L, B, Hkv, n_hi = 3, 5, 2, 32
     pages, tails = [3, 1, 0, 2, 4], [30, 31, 5, 0, 17]
     ref = _layers(L, B, Hkv, Hq, n_hi, pages, tails, torch.Generator("cuda").manual_seed(3))
     new = _layers(L, B, Hkv, Hq, n_hi, pages, tails, torch.Generator("cuda").manual_seed(3))
@@ -77,7 +80,7 @@ def test_serving_step_matches_per_layer_calls(graphs, fused):
             fl = lc.plan_flush()
             flushes += int((fl >= 0).sum())
             fd = torch.from_numpy(fl).cuda()
-            if fused:
+            if fused and Hq // Hkv <= 4:
                 lc.step(k[l], v[l], fd, q[l], d_out)
             else:  # the same two calls (the fused call attends a flushed page in another order)
                 lc.append(k[l], v[l], fd)

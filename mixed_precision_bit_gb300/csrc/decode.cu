@@ -964,13 +964,13 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   }
 }
 
-// Merge the split partials: 32 threads per (sequence, query head) row, four
-// channels a thread (16-byte loads), four rows per 128-thread CTA.  Splits
-// without pages left m = -inf.  In a fused append, the row of query head 0 then
-// does the sequence's append bookkeeping (every decode CTA has read the old
-// lengths by now).  Launched as a programmatic dependent of the decode kernel:
-// it may be scheduled while the decode grid drains, and waits for the whole
-// grid (and its memory) before reading the partials.
+// Merge the split partials of a (sequence, query head) row: the maximum of the
+// partials' m, then L = sum l * 2^(m - max) and O = sum o * 2^(m - max) in split
+// order; splits without pages left m = -inf.  In a fused append, the row of query
+// head 0 then does the sequence's append bookkeeping (every decode CTA has read
+// the old lengths by now).  Both merge kernels are launched as programmatic
+// dependents of the decode kernel: they may be scheduled while the decode grid
+// drains, and wait for the whole grid (and its memory) before reading.
 __device__ __forceinline__ void merge_split(float m, float l, float4 o, float ms, float& L,
                                             float4& O) {
   if (m == -INFINITY) return;  // no pages: l, o were never written
@@ -982,68 +982,110 @@ __device__ __forceinline__ void merge_split(float m, float l, float4 o, float ms
   O.w += o.w * e;
 }
 
-__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int rows) {
-  grid_dependency_wait();
-  const int bh = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
-  if (bh >= rows) return;
-  const int b = bh / p.Hq;
-  const float* base = p.ws + (size_t)bh * p.splits * kPartial;
-  const float4* obase = reinterpret_cast<const float4*>(base + 4) + lane;  // kPartial / 4 apart
-  constexpr int kQ = kPartial / 4;
-  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
-  float ms = -INFINITY, L = 0.f;
-  float4 O = zero;
-  constexpr int kU = 8;
-  if (p.splits <= kU) {
-    // every split's (m, l, o[4 lane..4 lane+3]) in one round of independent loads
-    float m[kU], l[kU];
-    float4 o[kU];
-#pragma unroll
-    for (int s = 0; s < kU; ++s) {
-      m[s] = s < p.splits ? base[s * kPartial] : -INFINITY;
-      l[s] = s < p.splits ? base[s * kPartial + 1] : 0.f;
-      o[s] = s < p.splits ? obase[s * kQ] : zero;
-    }
-#pragma unroll
-    for (int s = 0; s < kU; ++s) ms = fmaxf(ms, m[s]);
-    if (ms != -INFINITY) {
-#pragma unroll
-      for (int s = 0; s < kU; ++s) merge_split(m[s], l[s], o[s], ms, L, O);
-    }
-  } else {
-    // many splits: rounds of independent loads, first for the maxima, then for
-    // the sums, which are added in split order as in the branch above
-    constexpr int kV = 16;
-    for (int s0 = 0; s0 < p.splits; s0 += kV) {
-      float m[kV];
-#pragma unroll
-      for (int k = 0; k < kV; ++k) m[k] = s0 + k < p.splits ? base[(s0 + k) * kPartial] : -INFINITY;
-#pragma unroll
-      for (int k = 0; k < kV; ++k) ms = fmaxf(ms, m[k]);
-    }
-    if (ms != -INFINITY) {
-      for (int s0 = 0; s0 < p.splits; s0 += kU) {
-        float m[kU], l[kU];
-        float4 o[kU];
-#pragma unroll
-        for (int k = 0; k < kU; ++k) {
-          const bool in = s0 + k < p.splits;
-          m[k] = in ? base[(s0 + k) * kPartial] : -INFINITY;
-          l[k] = in ? base[(s0 + k) * kPartial + 1] : 0.f;
-          o[k] = in ? obase[(s0 + k) * kQ] : zero;
-        }
-#pragma unroll
-        for (int k = 0; k < kU; ++k) merge_split(m[k], l[k], o[k], ms, L, O);
-      }
-    }
-  }
+__device__ __forceinline__ void finish_row(const DecodeParams& p, int bh, int lane, float L,
+                                           float4 O) {
   const bool ok = L > 0.f;
-  const float4 r = ok ? make_float4(O.x / L, O.y / L, O.z / L, O.w / L) : zero;
+  const float4 r = ok ? make_float4(O.x / L, O.y / L, O.z / L, O.w / L)
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
   store_out4(p.out, p.out_dtype, (size_t)bh * kD + 4 * lane, r);
+  const int b = bh / p.Hq;
   if (lane == 0 && !ok) set_status(p.d_status, KITTY_ST_EMPTY);
   if (p.ap.k_new != nullptr && lane == 0 && bh - b * p.Hq == 0)
     append_finalize_one(b, p.ap.tail_len, p.ap.flush_page_ids, p.ap.block_table, p.max_pages,
                         p.ap.num_pages, p.pool_pages);
+}
+
+constexpr int kCombineSplits = 8;  // splits one 32-thread row merges in one round of loads
+
+// Up to kCombineSplits splits: 32 threads per row, four channels a thread
+// (16-byte loads), four rows per 128-thread CTA; every split's (m, l, o) in one
+// round of independent loads.
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeParams p, int rows) {
+  grid_dependency_wait();
+  const int bh = blockIdx.x * 4 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (bh >= rows) return;
+  const float* base = p.ws + (size_t)bh * p.splits * kPartial;
+  const float4* obase = reinterpret_cast<const float4*>(base + 4) + lane;  // kPartial / 4 apart
+  constexpr int kQ = kPartial / 4, kU = kCombineSplits;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float m[kU], l[kU];
+  float4 o[kU];
+#pragma unroll
+  for (int s = 0; s < kU; ++s) {
+    m[s] = s < p.splits ? base[s * kPartial] : -INFINITY;
+    l[s] = s < p.splits ? base[s * kPartial + 1] : 0.f;
+    o[s] = s < p.splits ? obase[s * kQ] : zero;
+  }
+  float ms = -INFINITY, L = 0.f;
+  float4 O = zero;
+#pragma unroll
+  for (int s = 0; s < kU; ++s) ms = fmaxf(ms, m[s]);
+  if (ms != -INFINITY) {
+#pragma unroll
+    for (int s = 0; s < kU; ++s) merge_split(m[s], l[s], o[s], ms, L, O);
+  }
+  finish_row(p, bh, lane, L, O);
+}
+
+// More splits (the long-context layers): one 128-thread CTA per row.  Warp w
+// merges splits w, w + 4, w + 8, ... (up to kCombineSplits of them per round of
+// independent loads, with a running maximum across rounds), then warp 0 merges
+// the four warps' results through shared memory.  Two dependent rounds of
+// loads instead of one per 16 splits (maxima) plus one per 8 (sums).
+__global__ void __launch_bounds__(128) combine_wide_kernel(const DecodeParams p, int rows) {
+  grid_dependency_wait();
+  __shared__ float4 wo[4][32];
+  __shared__ float wm[4], wl[4];
+  const int bh = blockIdx.x, wid = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (bh >= rows) return;
+  const float* base = p.ws + (size_t)bh * p.splits * kPartial;
+  const float4* obase = reinterpret_cast<const float4*>(base + 4) + lane;
+  constexpr int kQ = kPartial / 4, kU = kCombineSplits;
+  const float4 zero = make_float4(0.f, 0.f, 0.f, 0.f);
+  float ms = -INFINITY, L = 0.f;
+  float4 O = zero;
+  for (int s0 = wid; s0 < p.splits; s0 += 4 * kU) {
+    float m[kU], l[kU];
+    float4 o[kU];
+#pragma unroll
+    for (int k = 0; k < kU; ++k) {
+      const int s = s0 + 4 * k;
+      const bool in = s < p.splits;
+      m[k] = in ? base[(size_t)s * kPartial] : -INFINITY;
+      l[k] = in ? base[(size_t)s * kPartial + 1] : 0.f;
+      o[k] = in ? obase[(size_t)s * kQ] : zero;
+    }
+    float mr = ms;
+#pragma unroll
+    for (int k = 0; k < kU; ++k) mr = fmaxf(mr, m[k]);
+    if (mr == -INFINITY) continue;
+    if (ms != -INFINITY && mr > ms) {  // rescale the running sums to the new maximum
+      const float e = ex2(ms - mr);
+      L *= e;
+      O.x *= e;
+      O.y *= e;
+      O.z *= e;
+      O.w *= e;
+    }
+    ms = mr;
+#pragma unroll
+    for (int k = 0; k < kU; ++k) merge_split(m[k], l[k], o[k], ms, L, O);
+  }
+  if (lane == 0) {
+    wm[wid] = ms;
+    wl[wid] = L;
+  }
+  wo[wid][lane] = O;
+  __syncthreads();
+  if (wid != 0) return;
+  const float M = fmaxf(fmaxf(wm[0], wm[1]), fmaxf(wm[2], wm[3]));
+  float Lt = 0.f;
+  float4 Ot = zero;
+  if (M != -INFINITY) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) merge_split(wm[w], wl[w], wo[w][lane], M, Lt, Ot);
+  }
+  finish_row(p, bh, lane, Lt, Ot);
 }
 
 // Fused append bookkeeping when there is no combine step (one split).
@@ -1310,9 +1352,14 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
   cudaError_t e2 = cudaSuccess;
   if (sc.splits > 1) {
     const int rows = B * cfg->num_q_heads;
-    lc.gridDim = dim3((unsigned)(rows + 3) / 4);
     lc.blockDim = dim3(128);
-    e2 = cudaLaunchKernelEx(&lc, combine_kernel, p, rows);
+    if (sc.splits <= kCombineSplits) {
+      lc.gridDim = dim3((unsigned)(rows + 3) / 4);
+      e2 = cudaLaunchKernelEx(&lc, combine_kernel, p, rows);
+    } else {
+      lc.gridDim = dim3((unsigned)rows);
+      e2 = cudaLaunchKernelEx(&lc, combine_wide_kernel, p, rows);
+    }
   } else if (ap.k_new != nullptr) {
     lc.gridDim = dim3((unsigned)(B + 127) / 128);
     lc.blockDim = dim3(128);

@@ -571,10 +571,24 @@ def oracle_tokens_per_s(sample, steps, layers):
 
 
 # ------------------------------------------------------------------ profiled traffic
+def kernel_source_digest():
+    """sha256 (first 16 hex digits) of the decode kernel's sources with comments
+    and blank lines removed: a comment edit keeps a profile's counters valid,
+    any code change invalidates them."""
+    import hashlib
+    import re
+    parts = []
+    for f in ("decode.cu", "kitty_common.cuh", "quant_tile.cuh"):
+        src = open(os.path.join(ROOT, "mixed_precision_bit_gb300", "csrc", f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        parts.append("\n".join(l.rstrip() for l in src.splitlines() if l.strip()))
+    return hashlib.sha256("\n".join(parts).encode()).hexdigest()[:16]
+
+
 def profiled_traffic_ratio():
     """DRAM traffic / algorithmic bytes of one decode launch, from the committed ncu
     summary, if that capture was taken on the current kernel source; else None."""
-    import hashlib
     import re
     path = os.path.join(ROOT, "profiles", "decode_kernel_budget_layer.md")
     try:
@@ -582,10 +596,7 @@ def profiled_traffic_ratio():
     except OSError:
         return None
     vals = dict(re.findall(r"^\s*(\w+) = (\w+)\s*$", text, re.M))
-    srcs = [os.path.join(ROOT, "mixed_precision_bit_gb300", "csrc", f)
-            for f in ("decode.cu", "kitty_common.cuh", "quant_tile.cuh")]
-    sha = hashlib.sha256(b"".join(open(f, "rb").read() for f in srcs)).hexdigest()[:16]
-    if vals.get("kernel_source_sha256_16") != sha:
+    if vals.get("kernel_source_sha256_16") != kernel_source_digest():
         return None
     return float(vals["traffic_bytes_per_launch"]) / float(vals["algorithmic_bytes_per_launch"])
 

@@ -6,8 +6,8 @@
 // FlashAttention-style online softmax and PagedAttention block tables (both
 // cited there).
 //
-// One CTA = (kv head, sequence, split); 4 warps, each streaming every 4th page
-// of the split.  Split sizes shrink from the first split to the last and the
+// One CTA = (kv head, sequence, group of up to 4 query heads, split); 4 warps,
+// each streaming every 4th page of the split.  Split sizes shrink from the first split to the last and the
 // grid is split-major, so the CTAs dispatched last are the short ones
 // (longest-processing-time-first order: the grid ends with little idle time on
 // the SMs).  A split's page range does not depend on the sequence length, so a

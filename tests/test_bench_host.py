@@ -39,7 +39,9 @@ def test_traffic_ratio_dropped_when_a_kernel_source_changes(tmp_path, monkeypatc
     for f in SRC:
         p = csrc / f
         original = p.read_bytes()
-        p.write_bytes(original + b"\n")
+        p.write_bytes(original + b"\n// a comment changes no code\n\n")
+        assert bench.profiled_traffic_ratio() == expected, f
+        p.write_bytes(original + b"\nnamespace { constexpr int kUnusedChange = 1; }\n")
         assert bench.profiled_traffic_ratio() is None, f
         p.write_bytes(original)
     assert bench.profiled_traffic_ratio() == expected

@@ -235,9 +235,13 @@ int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pa
  *   out     device [B][Hq][128] of out_dtype (KITTY_F32, KITTY_BF16, KITTY_F16)
  *   workspace device, >= kitty_decode_workspace_bytes, 16-byte aligned (may be
  *   NULL when that size is 0).
+ * Query groups: Hq/Hkv <= 32; a group above 4 heads runs as ceil(g/4) CTAs of
+ * up to 4 query heads each over the same pages.
  * Launches, in stream order: the decode kernel, then (with more than one split)
  * the split combine as a programmatic dependent launch, which may start while
- * the decode grid drains and waits for it before reading the partials.  Both
+ * the decode grid drains and waits for it before reading the partials (32
+ * threads per (sequence, query head) row up to 8 splits; above that, a
+ * 128-thread CTA per row).  Both
  * can be captured in a CUDA graph, also as the first call on a device (that
  * call sets the kernel's shared-memory attributes, which is allowed during
  * capture). */
@@ -334,8 +338,8 @@ int kitty_f16kv_decode(const kitty_cfg* cfg, const void* q, const void* pool, in
                        size_t workspace_bytes, int32_t B, int32_t* d_status, void* stream);
 
 /* Launch shape that kitty_decode_attention uses for this batch shape: number of
- * splits per sequence (at most 256) and the pages in the largest split (for
- * reporting and tests).  Split s covers block-table positions [start_s,
+ * splits per (sequence, kv head, head group) (at most 256) and the pages in the
+ * largest split (for reporting and tests).  Split s covers block-table positions [start_s,
  * start_(s+1)), from position 0 upwards with the largest split first.  A
  * sequence shorter than max_pages leaves its later splits without pages: they
  * write an empty partial, which the merge skips.  Split 0 always runs; it also

@@ -95,14 +95,15 @@ def _signed_zeros(inp):
     return inp
 
 
-@pytest.mark.parametrize("lo_bit", [2, 4])
+@pytest.mark.parametrize("lo_bit,v_bit", [(2, 2), (4, 2), (4, 4)], ids=["42", "84", "84v4"])
 @pytest.mark.parametrize("mode", [0, 1], ids=["page", "running"])
 @pytest.mark.parametrize("dtype", [synth.BF16, synth.F16], ids=["bf16", "f16"])
-def test_quantize_signed_zeros_bit_exact(dtype, mode, lo_bit):
+def test_quantize_signed_zeros_bit_exact(dtype, mode, lo_bit, v_bit):
     """A minimum or maximum that is a signed zero is stored with the sign the
     IEEE 754-2019 minimum and maximum give, whatever the token order: of +0 and
-    -0 the minimum is -0 and the maximum +0."""
-    w = _variant("small_gqa", dtype=dtype, lo_bit=lo_bit)
+    -0 the minimum is -0 and the maximum +0 (Value groups: also with 4-bit
+    Values, whose min and max run on packed 16-bit pairs)."""
+    w = _variant("small_gqa", dtype=dtype, lo_bit=lo_bit, v_bit=v_bit)
     inp = _signed_zeros(synth.host_inputs(w, seed=1))
     pool, run = gpu_quantize(w, inp, mode=mode)
     ref, ref_run, st = oracle_quantize(w, inp, mode=mode)
@@ -112,10 +113,10 @@ def test_quantize_signed_zeros_bit_exact(dtype, mode, lo_bit):
     assert bad.size == 0, "first mismatching bytes at %s" % bad[:8]
 
 
-@pytest.mark.parametrize("lo_bit", [2, 4])
+@pytest.mark.parametrize("lo_bit,v_bit", [(2, 2), (4, 2), (4, 4)], ids=["42", "84", "84v4"])
 @pytest.mark.parametrize("mode", [1, 2], ids=["running", "sequence"])
-def test_quantize_running_bit_exact(mode, lo_bit):
-    w = _variant("small_gqa", pages=np.array([5, 3, 9]), drift=64, lo_bit=lo_bit)
+def test_quantize_running_bit_exact(mode, lo_bit, v_bit):
+    w = _variant("small_gqa", pages=np.array([5, 3, 9]), drift=64, lo_bit=lo_bit, v_bit=v_bit)
     inp = synth.host_inputs(w, seed=2)
     pool, run = gpu_quantize(w, inp, mode=mode)
     ref, (rs, rq, rc), st = oracle_quantize(w, inp, mode=mode)

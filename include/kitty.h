@@ -235,8 +235,9 @@ int kitty_decode_workspace_bytes(const kitty_cfg* cfg, int32_t B, int32_t max_pa
  *   out     device [B][Hq][128] of out_dtype (KITTY_F32, KITTY_BF16, KITTY_F16)
  *   workspace device, >= kitty_decode_workspace_bytes, 16-byte aligned (may be
  *   NULL when that size is 0).
- * Query groups: Hq/Hkv <= 32; a group above 4 heads runs as ceil(g/4) CTAs of
- * up to 4 query heads each over the same pages.
+ * Query groups: Hq/Hkv <= 32.  A group above 4 heads runs as ceil(g/8) CTAs of
+ * up to 8 query heads each in the (4, 2) format with 2-bit Values, else as
+ * ceil(g/4) CTAs of up to 4 query heads each, over the same pages.
  * Launches, in stream order: the decode kernel, then (with more than one split)
  * the split combine as a programmatic dependent launch, which may start while
  * the decode grid drains and waits for it before reading the partials (32

@@ -45,6 +45,8 @@
 #include <atomic>
 #include <cmath>
 #include <mutex>
+#include <type_traits>
+#include <utility>
 
 namespace kitty {
 namespace {
@@ -593,6 +595,97 @@ __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, si
   }
 }
 
+// Merge of the 4 warps' states for query heads hq0 .. hq0 + gh - 1 (gh <= 4):
+// per-warp (m, l, O) to shared memory (the stage buffers), then per channel c =
+// thread; the result goes to the output (one split) or to the split's
+// partials.  Called by all 128 threads; begins with a barrier, so consecutive
+// calls may reuse the same shared memory.
+template <int V>
+__device__ __forceinline__ void merge_warps(WarpState& w, uint8_t* dsm, const DecodeParams& p,
+                                            const int b, const int s, const int h0, const int gh,
+                                            const Lane& L) {
+  const int tid = threadIdx.x, wid = tid >> 5;
+  const int r = L.r, qq = L.qq;
+  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 4);
+  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 8);
+  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 16);
+  __syncthreads();
+  constexpr int kMergeFloats = kD * 8 + 4 * 8 + 8;
+  float* mw = reinterpret_cast<float*>(dsm) + wid * kMergeFloats;
+  float* Ow = mw;            // [128][8]: column 2h = hi, 2h+1 = lo part of head h
+  float* VMw = mw + kD * 8;  // [4][8]
+  float* MLw = VMw + 4 * 8;  // m[4], l[4]
+#pragma unroll
+  for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int rh = i >> 1;
+      const int row = 16 * mc + 8 * rh + r;
+      const float sc = __uint_as_float((uint32_t)(127 + kCodeExp - vrow_exp(V, mc, rh)) << 23);
+      Ow[row * 8 + 2 * qq + (i & 1)] = w.acc[mc][i] * sc;
+    }
+  if (r < 4) {
+    VMw[r * 8 + 2 * qq] = w.vm[0];
+    VMw[r * 8 + 2 * qq + 1] = w.vm[1];
+  }
+  if (r == 0) {
+    MLw[qq] = w.m;
+    MLw[4 + qq] = w.l;
+  }
+  __syncthreads();
+  // per channel c: every warp's (m, l) and its O and Value-minima columns of c,
+  // read as 16-byte vectors; warps are combined in order 0..3
+  const int c = tid;
+  const int G = c >> 5;
+  const float* m0 = reinterpret_cast<const float*>(dsm);
+  float mm[kDWarps][4], e[kDWarps][4], ms[4], Lsum[4], Osum[4];
+#pragma unroll
+  for (int ww = 0; ww < kDWarps; ++ww) {
+    const float4 v = *reinterpret_cast<const float4*>(m0 + ww * kMergeFloats + kD * 8 + 32);
+    mm[ww][0] = v.x; mm[ww][1] = v.y; mm[ww][2] = v.z; mm[ww][3] = v.w;
+  }
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    ms[h] = -INFINITY;
+#pragma unroll
+    for (int ww = 0; ww < kDWarps; ++ww) ms[h] = fmaxf(ms[h], mm[ww][h]);
+    Lsum[h] = 0.f;
+    Osum[h] = 0.f;
+  }
+#pragma unroll
+  for (int ww = 0; ww < kDWarps; ++ww) {
+    const float* base = m0 + ww * kMergeFloats;
+    const float4 l4 = *reinterpret_cast<const float4*>(base + kD * 8 + 36);
+    const float4 o0 = *reinterpret_cast<const float4*>(base + c * 8);
+    const float4 o1 = *reinterpret_cast<const float4*>(base + c * 8 + 4);
+    const float4 v0 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8);
+    const float4 v1 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8 + 4);
+    const float lw[4] = {l4.x, l4.y, l4.z, l4.w};
+    const float o[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
+    const float vmv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      e[ww][h] = (ms[h] == -INFINITY || mm[ww][h] == -INFINITY) ? 0.f : ex2(mm[ww][h] - ms[h]);
+      Lsum[h] += lw[h] * e[ww][h];
+      Osum[h] += (o[2 * h] + o[2 * h + 1] + vmv[2 * h] + vmv[2 * h + 1]) * e[ww][h];
+    }
+  }
+#pragma unroll
+  for (int h = 0; h < 4; ++h) {
+    if (h >= gh) break;
+    const int hq = h0 + h;
+    if (p.splits == 1) {
+      store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c,
+                Lsum[h] > 0.f ? Osum[h] / Lsum[h] : 0.f);
+      if (c == 0 && !(Lsum[h] > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
+    } else {
+      float* part = p.ws + (((size_t)b * p.Hq + hq) * p.splits + s) * kPartial;
+      part[4 + c] = Osum[h];
+      if (c == 0) { part[0] = ms[h]; part[1] = Lsum[h]; }
+    }
+  }
+}
+
 template <int DT, int NX, int W, int V>
 __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const DecodeParams p) {
   extern __shared__ __align__(128) uint8_t dsm[];
@@ -604,7 +697,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   const int gh = min(kHeadsPerCta, p.g - kHeadsPerCta * hgi);  // its query heads
   const int tid = threadIdx.x, wid = tid >> 5;
   const Lane L;
-  const int lane = L.lane, r = L.r, qq = L.qq;
+  const int lane = L.lane, qq = L.qq;
   constexpr int kBlob = Off<NX, W, V>::bytes;
   constexpr int kDStages = stages_for(W);
   const int sbeg = p.starts[s], send = p.starts[s + 1];
@@ -883,85 +976,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   // they reuse the stage buffers, which are idle unless a copy timed out
   if (pbeg == 0 && tl > 0 && !timed_out) tail_tokens<DT, V>(w, p, qs, b, kvh, tl, wid, L, wst);
 
-  // ---- merge the 4 warps: per-warp (m, l, O) to shared memory, then per channel
-  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 4);
-  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 8);
-  w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 16);
-  __syncthreads();
-  constexpr int kMergeFloats = kD * 8 + 4 * 8 + 8;
-  float* mw = reinterpret_cast<float*>(dsm) + wid * kMergeFloats;
-  float* Ow = mw;            // [128][8]: column 2h = hi, 2h+1 = lo part of head h
-  float* VMw = mw + kD * 8;  // [4][8]
-  float* MLw = VMw + 4 * 8;  // m[4], l[4]
-#pragma unroll
-  for (int mc = 0; mc < 8; ++mc)
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int rh = i >> 1;
-      const int row = 16 * mc + 8 * rh + r;
-      const float sc = __uint_as_float((uint32_t)(127 + kCodeExp - vrow_exp(V, mc, rh)) << 23);
-      Ow[row * 8 + 2 * qq + (i & 1)] = w.acc[mc][i] * sc;
-    }
-  if (r < 4) {
-    VMw[r * 8 + 2 * qq] = w.vm[0];
-    VMw[r * 8 + 2 * qq + 1] = w.vm[1];
-  }
-  if (r == 0) {
-    MLw[qq] = w.m;
-    MLw[4 + qq] = w.l;
-  }
-  __syncthreads();
-  // per channel c: every warp's (m, l) and its O and Value-minima columns of c,
-  // read as 16-byte vectors; warps are combined in order 0..3
-  const int c = tid;
-  const int G = c >> 5;
-  const float* m0 = reinterpret_cast<const float*>(dsm);
-  float mm[kDWarps][4], e[kDWarps][4], ms[4], Lsum[4], Osum[4];
-#pragma unroll
-  for (int ww = 0; ww < kDWarps; ++ww) {
-    const float4 v = *reinterpret_cast<const float4*>(m0 + ww * kMergeFloats + kD * 8 + 32);
-    mm[ww][0] = v.x; mm[ww][1] = v.y; mm[ww][2] = v.z; mm[ww][3] = v.w;
-  }
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    ms[h] = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kDWarps; ++ww) ms[h] = fmaxf(ms[h], mm[ww][h]);
-    Lsum[h] = 0.f;
-    Osum[h] = 0.f;
-  }
-#pragma unroll
-  for (int ww = 0; ww < kDWarps; ++ww) {
-    const float* base = m0 + ww * kMergeFloats;
-    const float4 l4 = *reinterpret_cast<const float4*>(base + kD * 8 + 36);
-    const float4 o0 = *reinterpret_cast<const float4*>(base + c * 8);
-    const float4 o1 = *reinterpret_cast<const float4*>(base + c * 8 + 4);
-    const float4 v0 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8);
-    const float4 v1 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8 + 4);
-    const float lw[4] = {l4.x, l4.y, l4.z, l4.w};
-    const float o[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-    const float vmv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      e[ww][h] = (ms[h] == -INFINITY || mm[ww][h] == -INFINITY) ? 0.f : ex2(mm[ww][h] - ms[h]);
-      Lsum[h] += lw[h] * e[ww][h];
-      Osum[h] += (o[2 * h] + o[2 * h + 1] + vmv[2 * h] + vmv[2 * h + 1]) * e[ww][h];
-    }
-  }
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    if (h >= gh) break;
-    const int hq = h0 + h;
-    if (p.splits == 1) {
-      store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c,
-                Lsum[h] > 0.f ? Osum[h] / Lsum[h] : 0.f);
-      if (c == 0 && !(Lsum[h] > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
-    } else {
-      float* part = p.ws + (((size_t)b * p.Hq + hq) * p.splits + s) * kPartial;
-      part[4 + c] = Osum[h];
-      if (c == 0) { part[0] = ms[h]; part[1] = Lsum[h]; }
-    }
-  }
+  merge_warps<V>(w, dsm, p, b, s, h0, gh, L);
 }
 
 // Merge the split partials of a (sequence, query head) row: the maximum of the
@@ -1097,6 +1112,373 @@ __global__ void finalize_kernel(const DecodeParams p, int B) {
                         p.ap.num_pages, p.pool_pages);
 }
 
+// ---------------------------------------------------------------- 8 heads per warp
+// Query groups above 4 in the (4, 2) format: a warp carries two sets of 4 query
+// heads (n-tiles), each its own 8-column B operands and online-softmax state,
+// against every unpacked A fragment, so each code is unpacked once for 8 heads
+// rather than once per head-group CTA.  The query's B fragments sit in a shared
+// table [n-tile][k-step][lane][2 words] (8 bytes a lane: conflict-free loads)
+// instead of registers; the second state costs registers, so 3 CTAs fit per SM.
+constexpr int kDMinBlocks8 = 3;
+constexpr int kQft = 2 * 8 * 32 * 2;  // query B-fragment table, 32-bit words
+
+template <class F, int... I>
+__device__ __forceinline__ void static_for_impl(F&& f, std::integer_sequence<int, I...>) {
+  (f(std::integral_constant<int, I>{}), ...);
+}
+// f(std::integral_constant<int, i>) for i = 0 .. N-1, each i a compile-time constant
+template <int N, class F>
+__device__ __forceinline__ void static_for(F&& f) {
+  static_for_impl(f, std::make_integer_sequence<int, N>{});
+}
+
+// q.M bias of both head sets for a page pair (see pair_beta).
+template <int NX>
+__device__ __forceinline__ void pair_beta8(const uint32_t paA, const uint32_t paB,
+                                           const uint32_t qft_lane, const Lane& L, float sm_log2,
+                                           float (&bA)[2], float (&bB)[2]) {
+  using O = Off<NX, 2, 2>;
+  const uint32_t a_m = ((L.r & 1) ? paB : paA) + 64 * L.qq;
+  const uint4 m0 = ld_s128<O::km>(a_m), m1 = ld_s128<O::km + 16>(a_m);
+  const uint4 m2 = ld_s128<O::km + 32>(a_m), m3 = ld_s128<O::km + 48>(a_m);
+  const uint32_t M[16] = {m0.x, m0.y, m0.z, m0.w, m1.x, m1.y, m1.z, m1.w,
+                          m2.x, m2.y, m2.z, m2.w, m3.x, m3.y, m3.z, m3.w};
+  static_for<2>([&](auto NT) {
+    constexpr int nt = decltype(NT)::value;
+    float cm[4] = {};
+    static_for<8>([&](auto J) {
+      constexpr int j = decltype(J)::value;
+      const uint2 qb = ld_s64<(nt * 8 + j) * 256>(qft_lane);
+      const uint32_t am[4] = {M[2 * j], 0u, M[2 * j + 1], 0u};
+      mma_f16(cm, am, qb.x, qb.y);
+    });
+    const float mine = (cm[0] + cm[1]) * sm_log2;
+    const float other = __shfl_xor_sync(0xFFFFFFFFu, mine, 4);
+    bA[nt] = (L.r & 1) ? other : mine;
+    bB[nt] = (L.r & 1) ? mine : other;
+  });
+}
+
+// Scores of one staged blob for both head sets (see page_scores; 2-bit Key
+// planes): each unpacked A fragment feeds one MMA per head set.
+template <int NX>
+__device__ __forceinline__ void page_scores8(const uint32_t pa, const uint32_t qft_lane,
+                                             const uint32_t (&qxa)[2], const Lane& L,
+                                             const float (&kscale)[4], const float (&beta)[2],
+                                             float (&s)[2][4]) {
+  using O = Off<NX, 2, 2>;
+  const int lane = L.lane, qq = L.qq;
+  const uint32_t a_lane = pa + 32 * lane;  // this lane's 32 bytes of the base plane
+  const uint32_t a_qq = pa + 4 * qq;
+  float cs[2][2][4] = {};
+  const uint4 kb0 = ld_s128<0>(a_lane);
+  const uint4 kb1 = ld_s128<16>(a_lane);
+  const uint32_t kw[8] = {kb0.x, kb0.y, kb0.z, kb0.w, kb1.x, kb1.y, kb1.z, kb1.w};
+  static_for<8>([&](auto J) {
+    constexpr int j = decltype(J)::value;
+    const uint32_t S0 = ld_s32<O::ks + 32 * j>(a_qq), S1 = ld_s32<O::ks + 32 * j + 16>(a_qq);
+    uint32_t a01[4], a23[4];
+    unpack_rows01(kw[j], a01);
+    unpack_rows23(kw[j], a23);
+    static_for<2>([&](auto NT) {
+      constexpr int nt = decltype(NT)::value;
+      const uint2 qb = ld_s64<(nt * 8 + j) * 256>(qft_lane);
+      const uint32_t b0 = hmul2u(qb.x, S0), b1 = hmul2u(qb.y, S1);
+      mma_f16(cs[nt][0], a01, b0, b1);
+      mma_f16(cs[nt][1], a23, b0, b1);
+    });
+  });
+  if (NX > 0) {
+    const uint32_t a_id = pa + 4 * qq;
+    const uint32_t a_x = pa + 4 * NX * lane;
+    static_for<NX>([&](auto JS) {
+      constexpr int js = decltype(JS)::value;
+      const uint32_t ids = ld_s32<O::kch + 16 * js>(a_id);
+      const uint32_t x = ld_s32<O::kx + 4 * js>(a_x);
+      const uint32_t c0 = (ids << 1) & 0xFEu, c1 = (ids >> 7) & 0xFEu;
+      const uint32_t c2 = (ids >> 15) & 0xFEu, c3 = (ids >> 23) & 0xFEu;
+      const uint32_t s01 = ld_s16r(pa + O::ks + c0) | ((uint32_t)ld_s16r(pa + O::ks + c1) << 16);
+      const uint32_t s23 = ld_s16r(pa + O::ks + c2) | ((uint32_t)ld_s16r(pa + O::ks + c3) << 16);
+      uint32_t a01[4], a23[4];
+      unpack_rows01(x, a01);
+      unpack_rows23(x, a23);
+      static_for<2>([&](auto NT) {
+        constexpr int nt = decltype(NT)::value;
+        const uint32_t q01 = ld_s16r(qxa[nt] + c0) | ((uint32_t)ld_s16r(qxa[nt] + c1) << 16);
+        const uint32_t q23 = ld_s16r(qxa[nt] + c2) | ((uint32_t)ld_s16r(qxa[nt] + c3) << 16);
+        const uint32_t b0 = hmul2u(q01, s01), b1 = hmul2u(q23, s23);
+        mma_f16(cs[nt][0], a01, b0, b1);
+        mma_f16(cs[nt][1], a23, b0, b1);
+      });
+    });
+  }
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+      for (int rh = 0; rh < 2; ++rh)
+        s[nt][2 * mt + rh] =
+            fmaf(cs[nt][mt][2 * rh] + cs[nt][mt][2 * rh + 1], kscale[2 * mt + rh], beta[nt]);
+}
+
+// Value minima term and PV of one page for both head sets (2-bit Values): each
+// unpacked A fragment feeds one MMA per head set.
+template <int NX>
+__device__ __forceinline__ void page_pv8(WarpState (&w)[2], const uint32_t pa,
+                                         const uint32_t (&T)[2][4], const Lane& L) {
+  using O = Off<NX, 2, 2>;
+  const int lane = L.lane, r = L.r, qq = L.qq;
+  const uint32_t a_lane = pa + 32 * lane;
+  const uint32_t a_q16 = pa + 16 * qq;
+  {
+    const uint4 vm = ld_s128<O::vm>(pa + 64 * (r & 3) + 16 * qq);
+    const uint32_t am0[4] = {vm.x, 0u, vm.y, 0u};
+    const uint32_t am1[4] = {vm.z, 0u, vm.w, 0u};
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      mma_f16(w[nt].vm, am0, T[nt][0], T[nt][1]);
+      mma_f16(w[nt].vm, am1, T[nt][2], T[nt][3]);
+    }
+  }
+  static_for<4>([&](auto GG) {
+    constexpr int G = decltype(GG)::value;
+    const uint2 vv = ld_s64<O::vb + 8 * G>(a_lane);
+    const uint4 sv = ld_s128<O::vs + 64 * G>(a_q16);
+    const uint32_t S[4] = {sv.x, sv.y, sv.z, sv.w};
+#pragma unroll
+    for (int kt = 0; kt < 2; ++kt) {
+      uint32_t a01[4], a23[4];
+      unpack_rows01(kt ? vv.y : vv.x, a01);
+      unpack_rows23(kt ? vv.y : vv.x, a23);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t bg0 = hmul2u(T[nt][2 * kt], S[2 * kt]);
+        const uint32_t bg1 = hmul2u(T[nt][2 * kt + 1], S[2 * kt + 1]);
+        mma_f16(w[nt].acc[2 * G], a01, bg0, bg1);
+        mma_f16(w[nt].acc[2 * G + 1], a23, bg0, bg1);
+      }
+    }
+  });
+}
+
+// Running max of one head set over a page pair (or one page): scores of head qq
+// of this lane's set, reduced over the 8 lanes that hold the same head.
+__device__ __forceinline__ float head_max(const float (&a)[4], const float (&b)[4], bool hasB) {
+  float pm = fmaxf(fmaxf(a[0], a[1]), fmaxf(a[2], a[3]));
+  if (hasB) pm = fmaxf(pm, fmaxf(fmaxf(b[0], b[1]), fmaxf(b[2], b[3])));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 4));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
+  pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
+  return pm;
+}
+
+// Decode with 8 query heads per CTA (the (4, 2) format, 2-bit Values, plain
+// decode: no fused append).  The same schedule, staging and merge as
+// decode_kernel; per head set the same arithmetic.
+template <int DT, int NX>
+__global__ void __launch_bounds__(kDThreads, kDMinBlocks8) decode8_kernel(const DecodeParams p) {
+  constexpr int W = 2, V = 2;
+  extern __shared__ __align__(128) uint8_t dsm[];
+  trigger_dependents();
+  const int u = blockIdx.x, s = blockIdx.y;
+  const int bk = u / p.HG, hgi = u - bk * p.HG;
+  const int b = bk / p.Hkv, kvh = bk - b * p.Hkv;
+  const int h0 = kvh * p.g + 2 * kHeadsPerCta * hgi;
+  const int gh = min(2 * kHeadsPerCta, p.g - 2 * kHeadsPerCta * hgi);
+  const int tid = threadIdx.x, wid = tid >> 5;
+  const Lane L;
+  const int lane = L.lane, qq = L.qq;
+  constexpr int kBlob = Off<NX, W, V>::bytes;
+  constexpr int kDStages = stages_for(W);
+  const int sbeg = p.starts[s], send = p.starts[s + 1];
+  int np = p.num_pages[b];
+  int tl = p.tail_len != nullptr ? p.tail_len[b] : 0;
+  const int first = sbeg + wid;
+  const int32_t* bt = p.block_table + (size_t)b * p.max_pages;
+  int bt_cache = first + kDWarps * lane < send ? bt[first + kDWarps * lane] : -1;
+  float qv[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h)
+    qv[h] = h < gh ? load16<DT>(p.q + ((size_t)b * p.Hq + h0 + h) * kD + tid) : 0.f;
+  if (s == 0) {
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      if (!(fabsf(qv[h]) <= 65504.0f))
+        set_status(p.d_status, fabsf(qv[h]) < INFINITY ? KITTY_ST_RANGE : KITTY_ST_NONFINITE);
+  }
+  const bool lens_ok =
+      !(np < 0 || np > p.max_pages || tl < 0 || tl > kPage || (tl > 0 && p.tail_k == nullptr));
+  if (!lens_ok) {
+    if (tid == 0 && s == 0 && kvh == 0 && hgi == 0) set_status(p.d_status, KITTY_ST_BAD_LEN);
+    np = 0;
+    tl = 0;
+  }
+  if (!split_active(p, s, np)) {
+    if (tid < gh) p.ws[(((size_t)b * p.Hq + h0 + tid) * p.splits + s) * kPartial] = -INFINITY;
+    return;
+  }
+  const int pbeg = sbeg, pend = min(np, send);
+
+  uint8_t* stages = dsm;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(dsm + kDWarps * kDStages * kBlob);
+  __half* qs = reinterpret_cast<__half*>(bars + kDWarps * kDStages);  // q [8][128]
+  __half* qs4 = qs + 8 * kD;  // q / 2^W: high parts [8][kQx], then low parts [8][kQx]
+  uint32_t* qft = reinterpret_cast<uint32_t*>(qs4 + 16 * kQx);  // [2][8][32][2]
+
+  const int npw = pend > first ? (pend - first + kDWarps - 1) / kDWarps : 0;
+  uint8_t* wst = stages + (size_t)wid * kDStages * kBlob;
+  uint64_t* wbar = bars + wid * kDStages;
+  if (lane == 0) {
+    for (int st = 0; st < kDStages; ++st) mbar_init(&wbar[st], 1);
+    fence_mbar_init();
+  }
+  const uint8_t* head_base = p.pool + (size_t)kvh * kBlob;
+  const size_t page_stride = (size_t)p.Hkv * kBlob;
+  int bt_base = 0;
+  uint32_t valid_mask = 0;
+  const uint32_t stage0 = smem_u32(wst), bar0 = smem_u32(wbar);
+  auto issue = [&](int i) {
+    if (i - bt_base >= 32) {
+      bt_base = i;
+      bt_cache = (i + lane < npw) ? bt[first + (i + lane) * kDWarps] : -1;
+    }
+    const int pid = __shfl_sync(0xFFFFFFFFu, bt_cache, i - bt_base);
+    const int st = i % kDStages;
+    const bool ok = pid >= 0 && pid < p.pool_pages;
+    if (lane == 0) {
+      const uint32_t bar = bar0 + 8 * st;
+      if (ok) {
+        mbar_arrive_expect_tx_s(bar, (uint32_t)kBlob);
+        bulk_g2s_s(stage0 + st * kBlob, head_base + (size_t)pid * page_stride, (uint32_t)kBlob, bar);
+      } else {
+        set_status(p.d_status, KITTY_ST_BAD_PAGE);
+        mbar_arrive_s(bar);
+      }
+    }
+    valid_mask = ok ? (valid_mask | (1u << st)) : (valid_mask & ~(1u << st));
+  };
+  const int pro = min(npw, kDStages);
+  for (int i = 0; i < pro; ++i) issue(i);
+  if (pbeg == 0 && tl > 0 && tid == 0) {
+    const size_t off = ((size_t)b * p.Hkv + kvh) * kPage * kD;
+    l2_prefetch(p.tail_k + off, (uint32_t)tl * kD * 2);
+    l2_prefetch(p.tail_v + off, (uint32_t)tl * kD * 2);
+  }
+
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const __half hv = __float2half_rn(qv[h]);
+    qs[h * kD + tid] = hv;
+    const __half hx = __hmul(hv, __float2half_rn(1.0f / (1 << W)));  // exact: power of two
+    const __half hh = high_part(hx);
+    qs4[h * kQx + tid] = hh;
+    qs4[(8 + h) * kQx + tid] = __hsub(hx, hh);  // exact
+  }
+  __syncthreads();
+  const bool low_col = (lane >> 2) & 1;
+  {  // the B-fragment table (warp wid: k-steps 2 wid, 2 wid + 1 of both head
+     // sets): column 2h takes the high part of q, 2h+1 the rest
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const __half* qh = qs + (4 * nt + (lane >> 3)) * kD;
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        const int j = 2 * wid + jj;
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const __half2 q2 = *reinterpret_cast<const __half2*>(qh + 16 * j + 2 * qq + 8 * e);
+          const __half2 h2 = __halves2half2(high_part(__low2half(q2)), high_part(__high2half(q2)));
+          qft[((nt * 8 + j) * 32 + lane) * 2 + e] = h2_bits(low_col ? __hsub2(q2, h2) : h2);
+        }
+      }
+    }
+  }
+  __syncthreads();
+  const uint32_t qft_lane = smem_u32(qft) + 8 * lane;
+  const uint32_t qxa[2] = {smem_u32(qs4 + ((low_col ? 8 : 0) + (lane >> 3)) * kQx),
+                           smem_u32(qs4 + ((low_col ? 8 : 0) + 4 + (lane >> 3)) * kQx)};
+  float kscale[4];
+#pragma unroll
+  for (int tau = 0; tau < 4; ++tau)
+    kscale[tau] = p.sm_log2 * __uint_as_float((uint32_t)(127 + kCodeExp - 2 * tau) << 23);
+
+  WarpState w[2];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+    for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) w[nt].acc[mc][i] = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) w[nt].vm[i] = 0.f;
+    w[nt].m = kNegBig;
+    w[nt].l = 0.f;
+  }
+  bool timed_out = false;
+  for (int i = 0; i < npw; i += 2) {
+    const bool hasB = i + 1 < npw;
+    bool done = false;
+    for (uint32_t it = 0;; ++it) {
+      done = done || (mbar_test_s(bar0 + 8 * (i % kDStages), (uint32_t)(i / kDStages) & 1u) &&
+                      (!hasB || mbar_test_s(bar0 + 8 * ((i + 1) % kDStages),
+                                            (uint32_t)((i + 1) / kDStages) & 1u)));
+      if (__all_sync(0xFFFFFFFFu, done) || it >= p.wait_polls) break;
+      if (it > 64) __nanosleep(32);
+    }
+    if (!__all_sync(0xFFFFFFFFu, done)) {
+      timed_out = true;
+      if (lane == 0) {
+        set_status(p.d_status, KITTY_ST_TIMEOUT);
+        for (int k = i; k < min(npw, i + kDStages); ++k)
+          mbar_wait_bounded(&wbar[k % kDStages], (uint32_t)(k / kDStages) & 1u, kWaitLimit);
+      }
+      __syncwarp();
+      break;
+    }
+    const int stA = i % kDStages, stB = (i + 1) % kDStages;
+    const bool vA = (valid_mask >> stA) & 1u;
+    const bool vB = hasB && ((valid_mask >> stB) & 1u);
+    const uint32_t paA = stage0 + stA * kBlob;
+    const uint32_t paB = hasB ? stage0 + stB * kBlob : paA;
+    float bA[2], bB[2];
+    pair_beta8<NX>(paA, paB, qft_lane, L, p.sm_log2, bA, bB);
+    float sA[2][4], sB[2][4];
+    page_scores8<NX>(paA, qft_lane, qxa, L, kscale, bA, sA);
+    if (hasB) page_scores8<NX>(paB, qft_lane, qxa, L, kscale, bB, sB);
+    if (!vA || (hasB && !vB)) {  // a page id was out of range (warp-uniform, rare)
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          sA[nt][k] = vA ? sA[nt][k] : -INFINITY;
+          if (hasB) sB[nt][k] = vB ? sB[nt][k] : -INFINITY;
+        }
+    }
+    uint32_t TA[2][4], TB[2][4];
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      rescale(w[nt], head_max(sA[nt], sB[nt], hasB));
+      page_probs(w[nt], sA[nt], TA[nt]);
+      if (hasB) page_probs(w[nt], sB[nt], TB[nt]);
+    }
+    page_pv8<NX>(w, paA, TA, L);
+    if (hasB) page_pv8<NX>(w, paB, TB, L);
+    __syncwarp();
+    if (i + kDStages < npw) issue(i + kDStages);
+    if (i + 1 + kDStages < npw) issue(i + 1 + kDStages);
+  }
+  if (pbeg == 0 && tl > 0 && !timed_out) {
+    tail_tokens<DT, V>(w[0], p, qs, b, kvh, tl, wid, L, wst);
+    if (gh > kHeadsPerCta) {
+      __syncwarp();  // the stage buffer is rewritten
+      tail_tokens<DT, V>(w[1], p, qs + kHeadsPerCta * kD, b, kvh, tl, wid, L, wst);
+    }
+  }
+  merge_warps<V>(w[0], dsm, p, b, s, h0, min(kHeadsPerCta, gh), L);
+  if (gh > kHeadsPerCta) merge_warps<V>(w[1], dsm, p, b, s, h0 + kHeadsPerCta, gh - kHeadsPerCta, L);
+}
+
 template <int DT, int NX, int W, int V>
 cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
   // the shared-memory opt-in is a per-device function attribute (smem is fixed
@@ -1113,6 +1495,37 @@ cudaError_t launch_decode(dim3 grid, size_t smem, cudaStream_t s, const DecodePa
   }
   decode_kernel<DT, NX, W, V><<<grid, kDThreads, smem, s>>>(p);
   return cudaGetLastError();
+}
+
+template <int DT, int NX>
+cudaError_t launch_decode8(dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
+  static std::atomic<uint64_t> opted_in{0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
+  const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t(1) << dev) : 0;
+  if (bit == 0 || (opted_in.load() & bit) == 0) {
+    cudaError_t e = cudaFuncSetAttribute(decode8_kernel<DT, NX>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    opted_in.fetch_or(bit);
+  }
+  decode8_kernel<DT, NX><<<grid, kDThreads, smem, s>>>(p);
+  return cudaGetLastError();
+}
+
+template <int DT>
+cudaError_t launch_decode8_nx(int nx, dim3 grid, size_t smem, cudaStream_t s, const DecodeParams& p) {
+  switch (nx) {
+    case 0: return launch_decode8<DT, 0>(grid, smem, s, p);
+    case 1: return launch_decode8<DT, 1>(grid, smem, s, p);
+    case 2: return launch_decode8<DT, 2>(grid, smem, s, p);
+    case 3: return launch_decode8<DT, 3>(grid, smem, s, p);
+    case 4: return launch_decode8<DT, 4>(grid, smem, s, p);
+    case 5: return launch_decode8<DT, 5>(grid, smem, s, p);
+    case 6: return launch_decode8<DT, 6>(grid, smem, s, p);
+    case 7: return launch_decode8<DT, 7>(grid, smem, s, p);
+    default: return launch_decode8<DT, 8>(grid, smem, s, p);
+  }
 }
 
 template <int DT, int W, int V>
@@ -1137,26 +1550,35 @@ using namespace kitty;
 
 namespace {
 
-size_t decode_smem(int blob, int w) {
-  const int st = stages_for(w);
-  return (size_t)kDWarps * st * blob + kDWarps * st * sizeof(uint64_t) + (4 * kD + 8 * kQx) * 2;
+// Query groups above 4 in the (4, 2) format with 2-bit Values take the
+// 8-heads-per-CTA kernel.
+bool heads8(const kitty_cfg* cfg) {
+  return cfg->num_q_heads / cfg->num_kv_heads > kHeadsPerCta && cfg->lo_bit == 2 && v_bits(cfg) == 2;
 }
 
-// Head-group CTAs per (sequence, kv head, split): ceil(g / 4).
+size_t decode_smem(int blob, int w, bool h8) {
+  const int st = stages_for(w);
+  const size_t q = h8 ? (8 * kD + 16 * kQx) * 2 + kQft * sizeof(uint32_t) : (4 * kD + 8 * kQx) * 2;
+  return (size_t)kDWarps * st * blob + kDWarps * st * sizeof(uint64_t) + q;
+}
+
+// Head-group CTAs per (sequence, kv head, split): ceil(g / 8) on the
+// 8-heads-per-CTA kernel, else ceil(g / 4).
 int head_groups(const kitty_cfg* cfg) {
   const int g = cfg->num_q_heads / cfg->num_kv_heads;
-  return (g + kHeadsPerCta - 1) / kHeadsPerCta;
+  const int per = heads8(cfg) ? 2 * kHeadsPerCta : kHeadsPerCta;
+  return (g + per - 1) / per;
 }
 
-// CTAs of the decode kernel resident at once on the device: kDMinBlocks per SM
-// unless shared memory allows fewer (large n_hi).
-long resident_ctas(int blob, int w) {
+// CTAs of the decode kernel resident at once on the device: kDMinBlocks (or
+// kDMinBlocks8) per SM unless shared memory allows fewer (large n_hi).
+long resident_ctas(int blob, int w, bool h8) {
   int dev = 0, smem_sm = 0;
-  int per_sm = kDMinBlocks;
+  int per_sm = h8 ? kDMinBlocks8 : kDMinBlocks;
   if (cudaGetDevice(&dev) == cudaSuccess &&
       cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) == cudaSuccess &&
       smem_sm > 0) {
-    const long fit = (long)smem_sm / (long)(decode_smem(blob, w) + 1024);
+    const long fit = (long)smem_sm / (long)(decode_smem(blob, w, h8) + 1024);
     per_sm = (int)std::max(1L, std::min<long>(per_sm, fit));
   }
   return (long)sm_count() * per_sm;
@@ -1202,7 +1624,7 @@ void plan(const kitty_cfg* cfg, int B, int M, int blob, Schedule* sc) {
     const int k = (M + c - 1) / c;
     for (int i = 0; i < k; ++i) sz[n++] = i == k - 1 ? M - (k - 1) * c : c;
   } else {
-    const long slots = resident_ctas(blob, cfg->lo_bit);
+    const long slots = resident_ctas(blob, cfg->lo_bit, heads8(cfg));
     const bool hinted = cfg->decode_total_pages > 0;
     const long heads = (long)cfg->num_kv_heads * head_groups(cfg);  // CTAs per sequence and split
     const double rho = (hinted ? 2.0 : 1.0) * (double)B * heads / (double)slots;
@@ -1329,11 +1751,14 @@ int attention(const kitty_cfg* cfg, const void* q, const void* pool, int32_t poo
   p.n_hi = cfg->n_hi;
   p.blob = blob;
   p.in_dtype = cfg->in_dtype;
-  const size_t smem = decode_smem(p.blob, cfg->lo_bit);
+  const bool h8 = heads8(cfg);  // never with a fused append (query groups up to 4 there)
+  const size_t smem = decode_smem(p.blob, cfg->lo_bit, h8);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   dim3 grid((unsigned)B * cfg->num_kv_heads * p.HG, sc.splits);
   const int nx = cfg->n_hi / 16, v = v_bits(cfg);
-  const cudaError_t e = cfg->in_dtype == KITTY_BF16
+  const cudaError_t e = h8 ? (cfg->in_dtype == KITTY_BF16 ? launch_decode8_nx<KITTY_BF16>(nx, grid, smem, s, p)
+                                                          : launch_decode8_nx<KITTY_F16>(nx, grid, smem, s, p))
+      : cfg->in_dtype == KITTY_BF16
       ? (cfg->lo_bit == 4 ? (v == 4 ? launch_decode_nx<KITTY_BF16, 4, 4>(nx, grid, smem, s, p)
                                     : launch_decode_nx<KITTY_BF16, 4, 2>(nx, grid, smem, s, p))
                           : launch_decode_nx<KITTY_BF16, 2, 2>(nx, grid, smem, s, p))

@@ -121,12 +121,13 @@ def test_quantize_finite_bf16_beyond_fp16_range(mode):
 
 @pytest.mark.parametrize("bad,code", [(70000.0, "RANGE"), (float("nan"), "NONFINITE"),
                                       (float("-inf"), "NONFINITE")])
-def test_decode_query_beyond_fp16_range(bad, code):
+@pytest.mark.parametrize("Hq", [8, 16], ids=["g4", "g8"])
+def test_decode_query_beyond_fp16_range(bad, code, Hq):
     """The tensor cores take the query as fp16: a bf16 query element above 65504
     (or non-finite) is reported; an in-range query of the same batch reports
     nothing."""
     import torch
-    w = _w()
+    w = _w(Hq=Hq)
     inp = synth.host_inputs(w, seed=37)
     pool, _ = gpu_quantize(w, inp)
     st = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -137,7 +138,8 @@ def test_decode_query_beyond_fp16_range(bad, code):
     assert int(st.item()) == oracle.ST[code]
 
 
-def test_decode_wait_timeout_reports_and_returns():
+@pytest.mark.parametrize("Hq", [32, 64], ids=["g4", "g8"])
+def test_decode_wait_timeout_reports_and_returns(Hq):
     """A page wait bounded to one poll of its barrier runs out on ordinary copies
     (the pool is evicted from L2 first): KITTY_ST_TIMEOUT is reported, the call
     completes (the CTA drains its copies in flight before it exits), and the
@@ -145,7 +147,7 @@ def test_decode_wait_timeout_reports_and_returns():
     as a call before the timeout."""
     import torch
     from mixed_precision_bit_gb300 import kitty
-    w = dataclasses.replace(synth.workload("small_gqa"), B=16, Hq=32, Hkv=8,
+    w = dataclasses.replace(synth.workload("small_gqa"), B=16, Hq=Hq, Hkv=8,
                             pages=np.full(16, 48), tails=np.full(16, 3))
     inp = synth.host_inputs(w, seed=38)
     pool, _ = gpu_quantize(w, inp)

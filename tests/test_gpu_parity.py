@@ -231,16 +231,18 @@ def test_decode_unaligned_output(out_dtype):
         assert not np.isnan(a).any() and np.array_equal(a, b), pps
 
 
+@pytest.mark.parametrize("Hq", [8, 16], ids=["g4", "g8"])
 @pytest.mark.parametrize("pps", [1, 3, 4, 5, 64])
-def test_decode_split_invariance(pps):
+def test_decode_split_invariance(pps, Hq):
     """Different split-K chunks agree to well inside the tolerance.  They are not
     identical: probabilities enter the tensor cores as fp16 hi/lo pairs relative to
     each warp's running max, so tiny weights fall in the fp16 subnormal range with
     a different absolute rounding per split layout (~1e-5 of RMS observed).  On
     the 64-page sequence the chunk sizes give 64, 22, 16, 13 and 1 splits: the
     merge's several-round path (full and ragged last round), its one-round path
-    and no merge at all; the shorter sequences leave splits without pages."""
-    w = _variant("small_gqa", pages=np.array([37, 1, 64]), tails=np.array([0, 5, 17]))
+    and no merge at all; the shorter sequences leave splits without pages.  With
+    g = 8 the same holds for the kernel that carries 8 query heads per CTA."""
+    w = _variant("small_gqa", Hq=Hq, pages=np.array([37, 1, 64]), tails=np.array([0, 5, 17]))
     inp = synth.host_inputs(w, seed=4)
     pool, _ = gpu_quantize(w, inp)
     a = gpu_decode(w, inp, pool, pps=pps)
@@ -251,9 +253,10 @@ def test_decode_split_invariance(pps):
     assert attn_error(a, ref)[0] <= 0
 
 
-def test_decode_ragged_and_empty():
+@pytest.mark.parametrize("Hq", [8, 16, 12], ids=["g4", "g8", "g6"])
+def test_decode_ragged_and_empty(Hq):
     """Sequences with only a tail, only pages, nothing at all, and a full tail."""
-    w = _variant("small_gqa", B=5, pages=np.array([0, 3, 0, 6, 1]),
+    w = _variant("small_gqa", Hq=Hq, B=5, pages=np.array([0, 3, 0, 6, 1]),
                  tails=np.array([9, 0, 0, 32 - 1, 0]))
     inp = synth.host_inputs(w, seed=5)
     inp["tail_len"][3] = 31
@@ -267,8 +270,9 @@ def test_decode_ragged_and_empty():
     assert attn_error(got, ref)[0] <= 0
 
 
-def test_decode_bad_page_sets_status():
-    w = synth.workload("tiny")
+@pytest.mark.parametrize("Hq", [1, 8], ids=["g1", "g8"])
+def test_decode_bad_page_sets_status(Hq):
+    w = _variant("tiny", Hq=Hq)
     inp = synth.host_inputs(w, seed=6)
     pool, _ = gpu_quantize(w, inp)
     inp["block_table"][0, 3] = 10 ** 6
@@ -360,18 +364,20 @@ def test_determinism():
         assert (oa.view(np.uint64) == ob.view(np.uint64)).all()
 
 
-def test_grouped_heads_equal_single_head_calls():
+@pytest.mark.parametrize("Hq", [8, 16, 10], ids=["g4", "g8", "g5"])
+def test_grouped_heads_equal_single_head_calls(Hq):
     """A kv head's g query heads decoded together agree with g separate one-head
-    calls over the same kv cache: query head hq reads kv head hq / g."""
-    w = _variant("small_gqa", Hq=8, Hkv=2, pages=np.array([12, 5, 20]), tails=np.array([3, 30, 0]))
+    calls over the same kv cache: query head hq reads kv head hq / g.  The split
+    size is fixed, so both sides take the same splits."""
+    w = _variant("small_gqa", Hq=Hq, Hkv=2, pages=np.array([12, 5, 20]), tails=np.array([3, 30, 0]))
     inp = synth.host_inputs(w, seed=13)
     pool, _ = gpu_quantize(w, inp)
-    together = gpu_decode(w, inp, pool)
+    together = gpu_decode(w, inp, pool, pps=4)
     g = w.g
     for h in range(g):
         w1 = dataclasses.replace(w, Hq=w.Hkv)          # one query head per kv head
         inp1 = dict(inp, q=np.ascontiguousarray(inp["q"][:, h::g]))
-        alone = gpu_decode(w1, inp1, pool)
+        alone = gpu_decode(w1, inp1, pool, pps=4)
         ref = together[:, h::g]
         scale = np.sqrt(np.mean(ref ** 2))
         assert np.abs(alone - ref).max() <= 1e-6 * scale, h

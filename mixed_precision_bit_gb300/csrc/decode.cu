@@ -595,93 +595,82 @@ __device__ __noinline__ void flush_tail(QuantSmem* sm, const AppendParams ap, si
   }
 }
 
-// Merge of the 4 warps' states for query heads hq0 .. hq0 + gh - 1 (gh <= 4):
-// per-warp (m, l, O) to shared memory (the stage buffers), then per channel c =
-// thread; the result goes to the output (one split) or to the split's
-// partials.  Called by all 128 threads; begins with a barrier, so consecutive
-// calls may reuse the same shared memory.
-template <int V>
-__device__ __forceinline__ void merge_warps(WarpState& w, uint8_t* dsm, const DecodeParams& p,
-                                            const int b, const int s, const int h0, const int gh,
-                                            const Lane& L) {
-  const int tid = threadIdx.x, wid = tid >> 5;
-  const int r = L.r, qq = L.qq;
+// Merge of the 4 warps' states in fragment layout, in two halves around one
+// block barrier.  merge_put: a warp leaves its O and Value-minima fragments and
+// (m, l) in its own stage buffers (idle after the page loop; 4608 bytes from
+// `scratch`).  merge_get: warp w then merges m-tiles 2w, 2w+1 (channels
+// 32w..32w+31, Value group w) of every warp, in warp order, at the common
+// maximum, and writes those channels of its heads to the output (one split) or
+// to the split's partials.
+constexpr int kMergeBytes = 32 * 16 * 9;  // per warp: 8 O float4 + (vm0, vm1, m, l) per lane
+
+__device__ __forceinline__ void merge_put(WarpState& w, uint8_t* scratch, const Lane& L) {
+  __syncwarp();  // the warp's reads of its buffers (tail rows) are done
   w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 4);
   w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 8);
   w.l += __shfl_xor_sync(0xFFFFFFFFu, w.l, 16);
-  __syncthreads();
-  constexpr int kMergeFloats = kD * 8 + 4 * 8 + 8;
-  float* mw = reinterpret_cast<float*>(dsm) + wid * kMergeFloats;
-  float* Ow = mw;            // [128][8]: column 2h = hi, 2h+1 = lo part of head h
-  float* VMw = mw + kD * 8;  // [4][8]
-  float* MLw = VMw + 4 * 8;  // m[4], l[4]
+  float4* f = reinterpret_cast<float4*>(scratch);
 #pragma unroll
   for (int mc = 0; mc < 8; ++mc)
+    f[mc * 32 + L.lane] = make_float4(w.acc[mc][0], w.acc[mc][1], w.acc[mc][2], w.acc[mc][3]);
+  f[8 * 32 + L.lane] = make_float4(w.vm[0], w.vm[1], w.m, w.l);
+}
+
+// stages: the CTA's stage buffers (warp ww's at + ww * warp_bytes); off: the
+// offset of this head set's scratch within each warp's buffers.
+template <int V>
+__device__ __forceinline__ void merge_get(const uint8_t* stages, const int warp_bytes, const int off,
+                                          const DecodeParams& p, const int b, const int s,
+                                          const int h0, const int gh, const Lane& L) {
+  const int wid = threadIdx.x >> 5;
+  const int r = L.r, qq = L.qq;
+  float4 ml[kDWarps];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int rh = i >> 1;
-      const int row = 16 * mc + 8 * rh + r;
+  for (int ww = 0; ww < kDWarps; ++ww)
+    ml[ww] = reinterpret_cast<const float4*>(stages + ww * warp_bytes + off)[8 * 32 + L.lane];
+  float ms = -INFINITY;
+#pragma unroll
+  for (int ww = 0; ww < kDWarps; ++ww) ms = fmaxf(ms, ml[ww].z);
+  float e[kDWarps], Lsum = 0.f, vmt = 0.f;
+#pragma unroll
+  for (int ww = 0; ww < kDWarps; ++ww) {
+    e[ww] = (ms == -INFINITY || ml[ww].z == -INFINITY) ? 0.f : ex2(ml[ww].z - ms);
+    Lsum += ml[ww].w * e[ww];
+    vmt += (ml[ww].x + ml[ww].y) * e[ww];  // Value group r & 3 of head qq
+  }
+  const float vg = __shfl_sync(0xFFFFFFFFu, vmt, 4 * wid + qq);  // group wid of head qq
+  const int hq = h0 + qq;
+  float* part = p.ws + (((size_t)b * p.Hq + hq) * p.splits + s) * kPartial;
+#pragma unroll
+  for (int k = 0; k < 2; ++k) {
+    const int mc = 2 * wid + k;
+    float a[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ww = 0; ww < kDWarps; ++ww) {
+      const float4 x = reinterpret_cast<const float4*>(stages + ww * warp_bytes + off)[mc * 32 + L.lane];
+      a[0] += x.x * e[ww];
+      a[1] += x.y * e[ww];
+      a[2] += x.z * e[ww];
+      a[3] += x.w * e[ww];
+    }
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh) {
       const float sc = __uint_as_float((uint32_t)(127 + kCodeExp - vrow_exp(V, mc, rh)) << 23);
-      Ow[row * 8 + 2 * qq + (i & 1)] = w.acc[mc][i] * sc;
-    }
-  if (r < 4) {
-    VMw[r * 8 + 2 * qq] = w.vm[0];
-    VMw[r * 8 + 2 * qq + 1] = w.vm[1];
-  }
-  if (r == 0) {
-    MLw[qq] = w.m;
-    MLw[4 + qq] = w.l;
-  }
-  __syncthreads();
-  // per channel c: every warp's (m, l) and its O and Value-minima columns of c,
-  // read as 16-byte vectors; warps are combined in order 0..3
-  const int c = tid;
-  const int G = c >> 5;
-  const float* m0 = reinterpret_cast<const float*>(dsm);
-  float mm[kDWarps][4], e[kDWarps][4], ms[4], Lsum[4], Osum[4];
-#pragma unroll
-  for (int ww = 0; ww < kDWarps; ++ww) {
-    const float4 v = *reinterpret_cast<const float4*>(m0 + ww * kMergeFloats + kD * 8 + 32);
-    mm[ww][0] = v.x; mm[ww][1] = v.y; mm[ww][2] = v.z; mm[ww][3] = v.w;
-  }
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    ms[h] = -INFINITY;
-#pragma unroll
-    for (int ww = 0; ww < kDWarps; ++ww) ms[h] = fmaxf(ms[h], mm[ww][h]);
-    Lsum[h] = 0.f;
-    Osum[h] = 0.f;
-  }
-#pragma unroll
-  for (int ww = 0; ww < kDWarps; ++ww) {
-    const float* base = m0 + ww * kMergeFloats;
-    const float4 l4 = *reinterpret_cast<const float4*>(base + kD * 8 + 36);
-    const float4 o0 = *reinterpret_cast<const float4*>(base + c * 8);
-    const float4 o1 = *reinterpret_cast<const float4*>(base + c * 8 + 4);
-    const float4 v0 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8);
-    const float4 v1 = *reinterpret_cast<const float4*>(base + kD * 8 + G * 8 + 4);
-    const float lw[4] = {l4.x, l4.y, l4.z, l4.w};
-    const float o[8] = {o0.x, o0.y, o0.z, o0.w, o1.x, o1.y, o1.z, o1.w};
-    const float vmv[8] = {v0.x, v0.y, v0.z, v0.w, v1.x, v1.y, v1.z, v1.w};
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      e[ww][h] = (ms[h] == -INFINITY || mm[ww][h] == -INFINITY) ? 0.f : ex2(mm[ww][h] - ms[h]);
-      Lsum[h] += lw[h] * e[ww][h];
-      Osum[h] += (o[2 * h] + o[2 * h + 1] + vmv[2 * h] + vmv[2 * h + 1]) * e[ww][h];
+      const float o = (a[2 * rh] + a[2 * rh + 1]) * sc + vg;
+      const int c = 16 * mc + 8 * rh + r;
+      if (qq < gh) {
+        if (p.splits == 1) store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c,
+                                     Lsum > 0.f ? o / Lsum : 0.f);
+        else part[4 + c] = o;
+      }
     }
   }
-#pragma unroll
-  for (int h = 0; h < 4; ++h) {
-    if (h >= gh) break;
-    const int hq = h0 + h;
+  if (wid == 0 && r == 0 && qq < gh) {
     if (p.splits == 1) {
-      store_out(p.out, p.out_dtype, ((size_t)b * p.Hq + hq) * kD + c,
-                Lsum[h] > 0.f ? Osum[h] / Lsum[h] : 0.f);
-      if (c == 0 && !(Lsum[h] > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
+      if (!(Lsum > 0.f)) set_status(p.d_status, KITTY_ST_EMPTY);
     } else {
-      float* part = p.ws + (((size_t)b * p.Hq + hq) * p.splits + s) * kPartial;
-      part[4 + c] = Osum[h];
-      if (c == 0) { part[0] = ms[h]; part[1] = Lsum[h]; }
+      part[0] = ms;
+      part[1] = Lsum;
     }
   }
 }
@@ -700,6 +689,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   const int lane = L.lane, qq = L.qq;
   constexpr int kBlob = Off<NX, W, V>::bytes;
   constexpr int kDStages = stages_for(W);
+  static_assert(kMergeBytes <= kDStages * kBlob, "merge scratch fits in a warp's stage buffers");
   const int sbeg = p.starts[s], send = p.starts[s + 1];
   // Independent loads first, all in flight together: the lengths, this warp's
   // first 32 block-table entries (up to the split's nominal end, which is
@@ -976,7 +966,11 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   // they reuse the stage buffers, which are idle unless a copy timed out
   if (pbeg == 0 && tl > 0 && !timed_out) tail_tokens<DT, V>(w, p, qs, b, kvh, tl, wid, L, wst);
 
-  merge_warps<V>(w, dsm, p, b, s, h0, gh, L);
+  // a flushed page was read from the first warps' buffers, where the merge now writes
+  if (flush_id >= 0) __syncthreads();
+  merge_put(w, wst, L);
+  __syncthreads();
+  merge_get<V>(stages, kDStages * kBlob, 0, p, b, s, h0, gh, L);
 }
 
 // Merge the split partials of a (sequence, query head) row: the maximum of the
@@ -1291,6 +1285,7 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks8) decode8_kernel(const 
   const int lane = L.lane, qq = L.qq;
   constexpr int kBlob = Off<NX, W, V>::bytes;
   constexpr int kDStages = stages_for(W);
+  static_assert(2 * kMergeBytes <= kDStages * kBlob, "merge scratch fits in a warp's stage buffers");
   const int sbeg = p.starts[s], send = p.starts[s + 1];
   int np = p.num_pages[b];
   int tl = p.tail_len != nullptr ? p.tail_len[b] : 0;
@@ -1475,8 +1470,12 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks8) decode8_kernel(const 
       tail_tokens<DT, V>(w[1], p, qs + kHeadsPerCta * kD, b, kvh, tl, wid, L, wst);
     }
   }
-  merge_warps<V>(w[0], dsm, p, b, s, h0, min(kHeadsPerCta, gh), L);
-  if (gh > kHeadsPerCta) merge_warps<V>(w[1], dsm, p, b, s, h0 + kHeadsPerCta, gh - kHeadsPerCta, L);
+  merge_put(w[0], wst, L);
+  merge_put(w[1], wst + kMergeBytes, L);
+  __syncthreads();
+  merge_get<V>(stages, kDStages * kBlob, 0, p, b, s, h0, min(kHeadsPerCta, gh), L);
+  if (gh > kHeadsPerCta)
+    merge_get<V>(stages, kDStages * kBlob, kMergeBytes, p, b, s, h0 + kHeadsPerCta, gh - kHeadsPerCta, L);
 }
 
 template <int DT, int NX, int W, int V>

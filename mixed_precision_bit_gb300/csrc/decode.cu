@@ -173,6 +173,7 @@ __device__ __forceinline__ uint16_t ld_s16r(uint32_t a) {
   return v;
 }
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(bits_h2(a), bits_h2(b))); }
+__device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) { return h2_bits(__hsub2(bits_h2(a), bits_h2(b))); }
 // The high part of an fp16 value: sign, exponent and the top 3 mantissa bits
 // (4 significant bits).  Times a step of at most 7 significant bits it is exact
 // in fp16, and the rest (value - high part, exact) has at most 7 significant
@@ -556,17 +557,22 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
     if (i < nw) *reinterpret_cast<uint2*>(vbuf + i * 2 * kD + 8 * lane) = vx[i];
   __syncwarp();
   const uint32_t vb = smem_u32(vbuf) + 2 * r;
+  float ta[8][2] = {};  // sum of p * v, scaled by the rows' power of two once at the end
   for (int i = 0; i < nw; ++i) {
     const float pi = __shfl_sync(0xFFFFFFFFu, pr, 4 * i + qq);
 #pragma unroll
     for (int mc = 0; mc < 8; ++mc)
 #pragma unroll
-      for (int rh = 0; rh < 2; ++rh) {
-        const int c = 16 * mc + 8 * rh;
-        const float rs = __uint_as_float((uint32_t)(127 - kCodeExp + vrow_exp(V, mc, rh)) << 23);
-        w.acc[mc][2 * rh] += pi * (bits16_to_f32(ld_s16r(vb + i * 2 * kD + 2 * c), DT) * rs);
-      }
+      for (int rh = 0; rh < 2; ++rh)
+        ta[mc][rh] += pi * bits16_to_f32(ld_s16r(vb + i * 2 * kD + 2 * (16 * mc + 8 * rh)), DT);
   }
+#pragma unroll
+  for (int mc = 0; mc < 8; ++mc)
+#pragma unroll
+    for (int rh = 0; rh < 2; ++rh) {
+      const float rs = __uint_as_float((uint32_t)(127 - kCodeExp + vrow_exp(V, mc, rh)) << 23);
+      w.acc[mc][2 * rh] += ta[mc][rh] * rs;
+    }
 }
 
 // Quantize the full tail of (sequence, kv head) sh into page fid with the
@@ -840,14 +846,21 @@ __global__ void __launch_bounds__(kDThreads, kDMinBlocks) decode_kernel(const De
   const bool low_col = (lane >> 2) & 1;
   uint32_t qf[8][2];
   {
-    const __half* qh = qs + (lane >> 3) * kD;
+    const uint32_t qa = smem_u32(qs + (lane >> 3) * kD + 2 * qq);
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const __half2 q2 = *reinterpret_cast<const __half2*>(qh + 16 * j + 2 * qq + 8 * e);
-        const __half2 h2 = __halves2half2(high_part(__low2half(q2)), high_part(__high2half(q2)));
-        qf[j][e] = h2_bits(low_col ? __hsub2(q2, h2) : h2);
+        uint32_t q2;
+        switch (2 * j + e) {  // compile-time offsets (the loops are unrolled)
+#define KITTY_QF(K) case K: q2 = ld_s32<2 * (16 * (K / 2) + 8 * (K % 2))>(qa); break;
+          KITTY_QF(0) KITTY_QF(1) KITTY_QF(2) KITTY_QF(3) KITTY_QF(4) KITTY_QF(5) KITTY_QF(6) KITTY_QF(7)
+          KITTY_QF(8) KITTY_QF(9) KITTY_QF(10) KITTY_QF(11) KITTY_QF(12) KITTY_QF(13) KITTY_QF(14)
+          default: KITTY_QF(15)
+#undef KITTY_QF
+        }
+        const uint32_t h2 = q2 & 0xFF80FF80u;  // high parts of both halves
+        qf[j][e] = low_col ? hsub2u(q2, h2) : h2;
       }
     }
   }

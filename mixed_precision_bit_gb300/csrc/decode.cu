@@ -7,8 +7,10 @@
 // cited there).
 //
 // One CTA = (kv head, sequence, group of up to 4 query heads, split); 4 warps,
-// each streaming every 4th page of the split.  Split sizes shrink from the first split to the last and the
-// grid is split-major, so the CTAs dispatched last are the short ones
+// each streaming every 4th page of the split.  (Query groups above 4 in the
+// (4, 2) format take decode8_kernel: 8 heads per CTA, two head sets per warp.)
+// Split sizes shrink from the first split to the last and the grid is
+// split-major, so the CTAs dispatched last are the short ones
 // (longest-processing-time-first order: the grid ends with little idle time on
 // the SMs).  A split's page range does not depend on the sequence length, so a
 // CTA requests its lengths, query rows and block-table entries together and
@@ -33,7 +35,9 @@
 // the fp16 subnormal code * 2^(2*tau + 2 - 24) (2-bit planes) or
 // code * 2^(4*(tau & 1) + 2 - 24) (4-bit planes); the power of two depends only
 // on the tile row and is folded into the score scale (Keys) or the final output
-// (Values).  The rotation keeps the codes out of the lowest mantissa bits:
+// (Values).  The 4 warps merge their states in the fragment layout through
+// their own idle stage buffers, each warp finishing a quarter of the channels;
+// splits merge in a separate combine kernel.  The rotation keeps the codes out of the lowest mantissa bits:
 // measured on the GB300, the PV products of codes in mantissa bits 0-1 kept an
 // error near 2^-13 of the output's scale over an 8192-token sequence, 4 to 8
 // times that of the next two bits up.

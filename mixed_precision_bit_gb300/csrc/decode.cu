@@ -497,15 +497,15 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
   }
 }
 
-// Unquantized tail tokens (0..31 per sequence) on the CUDA cores.  Warp wid
-// takes tokens wid, wid+4, ... (at most 8).  All of its K and V rows are
-// loaded at once (8 bytes a lane per row; the rows were prefetched into L2
-// when the CTA started); the 32 (token, head) dot products are reduced across
-// the warp in one transposing butterfly, after which lane 4i+h holds token i
-// of head h, i.e. lane (r, qq) holds token r of its own head; one rescale
-// covers them all.  The V rows pass through the warp's idle stage buffer to
-// reach the accumulator layout, and carry the same per-row power of two as the
-// paged codes.
+// Unquantized tail tokens (0..31 per sequence).  Warp wid takes tokens wid,
+// wid+4, ... (at most 8).  All of its K and V rows are loaded at once (8 bytes
+// a lane per row; the rows were prefetched into L2 when the CTA started); the
+// 32 (token, head) dot products run on the CUDA cores in fp32 and are reduced
+// across the warp in one transposing butterfly, after which lane 4i+h holds
+// token i of head h, i.e. lane (r, qq) holds token r of its own head; one
+// rescale covers them all.  The V rows pass through the warp's idle stage
+// buffer into a tensor-core PV (one MMA per 16 channels), whose result is
+// brought to the paged codes' per-row power of two.
 template <int DT, int V>
 __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* qs, int b, int kvh,
                             int tl, int wid, const Lane& L, uint8_t* vbuf) {
@@ -556,27 +556,34 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
   rescale(w, pm);
   const float pr = r < nw ? ex2(sc - w.m) : 0.f;
   w.l += pr;
+  // PV on the tensor cores in the input type: A = V^T (channels x this warp's
+  // tokens, the rows past nw zero) by transposing ldmatrix from rows padded to
+  // kTailRow bytes (conflict-free), B = p as (high, rest) pairs in the input
+  // type: column n = r takes part r & 1 of head r / 2, k = tokens 2qq, 2qq+1
+  // (tokens 8..15 of the k-step are absent: B's second register is zero)
+  constexpr int kTailRow = 2 * kD + 16;
 #pragma unroll
-  for (int i = 0; i < 8; ++i)
-    if (i < nw) *reinterpret_cast<uint2*>(vbuf + i * 2 * kD + 8 * lane) = vx[i];
+  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(vbuf + i * kTailRow + 8 * lane) = vx[i];
   __syncwarp();
-  const uint32_t vb = smem_u32(vbuf) + 2 * r;
-  float ta[8][2] = {};  // sum of p * v, scaled by the rows' power of two once at the end
-  for (int i = 0; i < nw; ++i) {
-    const float pi = __shfl_sync(0xFFFFFFFFu, pr, 4 * i + qq);
+  const uint32_t u0 = prob_pair<DT>(__shfl_sync(0xFFFFFFFFu, pr, 8 * qq + (r >> 1)));
+  const uint32_t u1 = prob_pair<DT>(__shfl_sync(0xFFFFFFFFu, pr, 8 * qq + 4 + (r >> 1)));
+  const uint32_t b0 = __byte_perm(u0, u1, (r & 1) ? 0x7632u : 0x5410u);
+  const uint32_t va = smem_u32(vbuf) + (lane & 7) * kTailRow + (lane >> 3) * 16;
 #pragma unroll
-    for (int mc = 0; mc < 8; ++mc)
+  for (int g = 0; g < 4; ++g) {
+    uint32_t a4[4];
+    ldsm_x4_t(va + 64 * g, a4);  // channel blocks 4g .. 4g+3 of 8 channels
 #pragma unroll
-      for (int rh = 0; rh < 2; ++rh)
-        ta[mc][rh] += pi * bits16_to_f32(ld_s16r(vb + i * 2 * kD + 2 * (16 * mc + 8 * rh)), DT);
-  }
+    for (int k = 0; k < 2; ++k) {
+      const int mc = 2 * g + k;
+      const uint32_t a[4] = {a4[2 * k], a4[2 * k + 1], 0u, 0u};
+      float c[4] = {0.f, 0.f, 0.f, 0.f};
+      mma16<DT>(c, a, b0, 0u);
 #pragma unroll
-  for (int mc = 0; mc < 8; ++mc)
-#pragma unroll
-    for (int rh = 0; rh < 2; ++rh) {
-      const float rs = __uint_as_float((uint32_t)(127 - kCodeExp + vrow_exp(V, mc, rh)) << 23);
-      w.acc[mc][2 * rh] += ta[mc][rh] * rs;
+      for (int i = 0; i < 4; ++i)  // to the codes' scale: the row's power of two
+        w.acc[mc][i] += c[i] * __uint_as_float((uint32_t)(127 - kCodeExp + vrow_exp(V, mc, i >> 1)) << 23);
     }
+  }
 }
 
 // Quantize the full tail of (sequence, kv head) sh into page fid with the

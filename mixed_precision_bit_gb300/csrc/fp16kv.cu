@@ -58,49 +58,6 @@ __device__ __forceinline__ float ex2f(float x) {
   return y;
 }
 
-// D(16x8 f32) += A(16x16) * B(16x8), both 16-bit of type DT.
-template <int DT>
-__device__ __forceinline__ void mma16(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
-  if (DT == KITTY_BF16) {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  } else {
-    asm volatile(
-        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
-        "{%8,%9}, {%0,%1,%2,%3};"
-        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
-        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
-  }
-}
-
-__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t* a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
-               : "r"(addr));
-}
-__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t* a) {
-  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-               : "=r"(a[0]), "=r"(a[1]), "=r"(a[2]), "=r"(a[3])
-               : "r"(addr));
-}
-
-// (high, rest) of a probability in the 16-bit type: the high part keeps the
-// type's significand (11 bits for fp16, 8 for bf16) exactly, the rest is
-// rounded once.
-template <int DT>
-__device__ __forceinline__ uint32_t prob_pair(float p) {
-  if (DT == KITTY_BF16) {
-    const float t = __uint_as_float(__float_as_uint(p) & 0xFFFF0000u);
-    const __nv_bfloat162 h = __floats2bfloat162_rn(t, p - t);
-    return *reinterpret_cast<const uint32_t*>(&h);
-  }
-  const float t = __uint_as_float(__float_as_uint(p) & 0xFFFFE000u);
-  return h2_bits(__floats2half2_rn(t, p - t));
-}
-
 __device__ __forceinline__ void store_o(void* out, int dt, size_t i, float v) {
   if (dt == KITTY_F32) static_cast<float*>(out)[i] = v;
   else if (dt == KITTY_BF16) static_cast<__nv_bfloat16*>(out)[i] = __float2bfloat16_rn(v);

@@ -1637,6 +1637,9 @@ struct Schedule {
 //    batch (Hkv * total / slots pages), which keeps ragged batches balanced;
 //    without it the factor stays rho (measured on GB300: +2% on the serving
 //    step, +5% on qwen3_8b, +2% on the ragged long-context batch).
+//  * With both hints showing equal lengths (total = B * longest) and the units
+//    filling at most half of the resident CTAs: k = slots / units equal
+//    splits (at least 8 pages each), one wave of equal CTAs.
 void plan(const kitty_cfg* cfg, int B, int M, int blob, Schedule* sc) {
   int sz[kMaxSplits];
   int n = 0;
@@ -1656,31 +1659,42 @@ void plan(const kitty_cfg* cfg, int B, int M, int blob, Schedule* sc) {
     const double work = hinted ? (double)heads * cfg->decode_total_pages
                                : (double)B * heads * Ms;  // page-heads (at most)
     const int m0 = work < 64.0 * (double)slots ? 32 : 16;
-    long T = 0;
-    for (int m = m0;; m *= 2) {
-      n = 0;
-      T = 0;
-      long c = m;
-      while (T < Ms && n < kMaxSplits) {
-        sz[n++] = (int)c;
-        T += c;
-        c = std::max<long>(m, std::min<long>(fair, (long)(rho * (double)T) / 8 * 8));
+    const long units = (long)B * heads;
+    if (hinted && cfg->decode_max_pages > 0 && (long)B * Ms == cfg->decode_total_pages &&
+        2 * units <= slots) {
+      // every sequence holds Ms pages and the units fill at most half of the
+      // resident CTAs: k equal splits make one wave of equal CTAs
+      const int k = (int)std::min<long>(kMaxSplits, slots / units);
+      const int c = std::max(8, (Ms + k - 1) / k);
+      for (int t = 0; t < Ms; t += c) sz[n++] = std::min(c, Ms - t);
+      sz[n - 1] += M - Ms;  // the last split reaches the end of the table
+    } else {
+      long T = 0;
+      for (int m = m0;; m *= 2) {
+        n = 0;
+        T = 0;
+        long c = m;
+        while (T < Ms && n < kMaxSplits) {
+          sz[n++] = (int)c;
+          T += c;
+          c = std::max<long>(m, std::min<long>(fair, (long)(rho * (double)T) / 8 * 8));
+        }
+        if (T >= Ms) break;
       }
-      if (T >= Ms) break;
-    }
-    std::reverse(sz, sz + n);
-    sz[0] -= (int)(T - Ms);
-    sz[n - 1] += M - Ms;  // the last split reaches the end of the table
-    if (n > 1 && sz[0] < sz[1]) {
-      const int tot = sz[0] + sz[1];
-      const int h = (tot / 2 + 7) / 8 * 8;
-      if (h >= tot) {
-        sz[0] = tot;
-        for (int i = 1; i + 1 < n; ++i) sz[i] = sz[i + 1];
-        --n;
-      } else {
-        sz[0] = h;
-        sz[1] = tot - h;
+      std::reverse(sz, sz + n);
+      sz[0] -= (int)(T - Ms);
+      sz[n - 1] += M - Ms;  // the last split reaches the end of the table
+      if (n > 1 && sz[0] < sz[1]) {
+        const int tot = sz[0] + sz[1];
+        const int h = (tot / 2 + 7) / 8 * 8;
+        if (h >= tot) {
+          sz[0] = tot;
+          for (int i = 1; i + 1 < n; ++i) sz[i] = sz[i + 1];
+          --n;
+        } else {
+          sz[0] = h;
+          sz[1] = tot - h;
+        }
       }
     }
   }

@@ -178,6 +178,16 @@ __device__ __forceinline__ uint16_t ld_s16r(uint32_t a) {
 }
 __device__ __forceinline__ uint32_t hmul2u(uint32_t a, uint32_t b) { return h2_bits(__hmul2(bits_h2(a), bits_h2(b))); }
 __device__ __forceinline__ uint32_t hsub2u(uint32_t a, uint32_t b) { return h2_bits(__hsub2(bits_h2(a), bits_h2(b))); }
+// An fp16 pair in the 16-bit input type: unchanged for fp16; for bf16 exact
+// when the values came from bf16 (at most 8 significant bits).
+template <int DT>
+__device__ __forceinline__ uint32_t half2_to16(uint32_t h2) {
+  if (DT == KITTY_BF16) {
+    const __nv_bfloat162 b = __float22bfloat162_rn(__half22float2(bits_h2(h2)));
+    return *reinterpret_cast<const uint32_t*>(&b);
+  }
+  return h2;
+}
 // The high part of an fp16 value: sign, exponent and the top 3 mantissa bits
 // (4 significant bits).  Times a step of at most 7 significant bits it is exact
 // in fp16, and the rest (value - high part, exact) has at most 7 significant
@@ -499,13 +509,12 @@ __device__ __forceinline__ void page_pv(WarpState& w, const uint32_t pa, const u
 
 // Unquantized tail tokens (0..31 per sequence).  Warp wid takes tokens wid,
 // wid+4, ... (at most 8).  All of its K and V rows are loaded at once (8 bytes
-// a lane per row; the rows were prefetched into L2 when the CTA started); the
-// 32 (token, head) dot products run on the CUDA cores in fp32 and are reduced
-// across the warp in one transposing butterfly, after which lane 4i+h holds
-// token i of head h, i.e. lane (r, qq) holds token r of its own head; one
-// rescale covers them all.  The V rows pass through the warp's idle stage
-// buffer into a tensor-core PV (one MMA per 16 channels), whose result is
-// brought to the paged codes' per-row power of two.
+// a lane per row; the rows were prefetched into L2 when the CTA started) and
+// pass through the warp's idle stage buffer to the tensor cores, in the input
+// type: the scores of its tokens against the 4 query heads (8 MMAs; lane
+// (r, qq) gets token r of head qq, so one rescale covers them all), then the
+// PV (one MMA per 16 channels), brought to the paged codes' per-row power of
+// two.
 template <int DT, int V>
 __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* qs, int b, int kvh,
                             int tl, int wid, const Lane& L, uint8_t* vbuf) {
@@ -521,35 +530,50 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
     kx[i] = i < nw ? __ldcg(reinterpret_cast<const uint2*>(p.tail_k + off)) : make_uint2(0u, 0u);
     vx[i] = i < nw ? __ldcg(reinterpret_cast<const uint2*>(p.tail_v + off)) : make_uint2(0u, 0u);
   }
-  float qv[4][4];
-#pragma unroll
-  for (int h = 0; h < 4; ++h)
-#pragma unroll
-    for (int e = 0; e < 4; ++e) qv[h][e] = __half2float(qs[h * kD + 4 * lane + e]);
-  float v[32];
+  // K and V rows through the warp's idle stage buffer, rows padded to kTailRow
+  // bytes (conflict-free ldmatrix); rows past nw are zero
+  constexpr int kTailRow = 2 * kD + 16;
+  uint8_t* kbuf = vbuf + 8 * kTailRow;
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float k0 = bits16_to_f32((uint16_t)(kx[i].x & 0xFFFFu), DT);
-    const float k1 = bits16_to_f32((uint16_t)(kx[i].x >> 16), DT);
-    const float k2 = bits16_to_f32((uint16_t)(kx[i].y & 0xFFFFu), DT);
-    const float k3 = bits16_to_f32((uint16_t)(kx[i].y >> 16), DT);
-#pragma unroll
-    for (int h = 0; h < 4; ++h) v[4 * i + h] = qv[h][0] * k0 + qv[h][1] * k1 + qv[h][2] * k2 + qv[h][3] * k3;
+    *reinterpret_cast<uint2*>(vbuf + i * kTailRow + 8 * lane) = vx[i];
+    *reinterpret_cast<uint2*>(kbuf + i * kTailRow + 8 * lane) = kx[i];
   }
-  // transposing butterfly: after the step with offset o, a lane keeps the half
-  // of the values whose index bit o matches its own lane bit o
+  __syncwarp();
+  // scores on the tensor cores in the input type (the products are exact):
+  // A = the K rows (tokens x channels) by ldmatrix, B = q with head h in
+  // column 2h (odd columns zero), so lane (r, qq) gets token r of head qq
+  float cs[4] = {0.f, 0.f, 0.f, 0.f};
+  {
+    const uint32_t ka = smem_u32(kbuf) + (lane & 7) * kTailRow + (lane >> 3) * 16;
+    const uint32_t qa = smem_u32(qs + (r >> 1) * kD + 2 * qq);
+    const bool qcol = (r & 1) == 0;
 #pragma unroll
-  for (int st = 0; st < 5; ++st) {
-    const int o = 16 >> st;
-    const bool up = (lane & o) != 0;
+    for (int g = 0; g < 4; ++g) {
+      uint32_t a4[4];
+      ldsm_x4(ka + 64 * g, a4);  // channel blocks 4g .. 4g+3 of 8 channels
 #pragma unroll
-    for (int k = 0; k < o; ++k) {
-      const float send = up ? v[k] : v[k + o];
-      const float keep = up ? v[k + o] : v[k];
-      v[k] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, o);
+      for (int k = 0; k < 2; ++k) {
+        const int j = 2 * g + k;  // k-step: channels 16j .. 16j+15
+        const uint32_t a[4] = {a4[2 * k], 0u, a4[2 * k + 1], 0u};
+        uint32_t qb[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          uint32_t h2;
+          switch (2 * j + e) {  // compile-time offsets (the loops are unrolled)
+#define KITTY_QT(K) case K: h2 = ld_s32<2 * (16 * (K / 2) + 8 * (K % 2))>(qa); break;
+            KITTY_QT(0) KITTY_QT(1) KITTY_QT(2) KITTY_QT(3) KITTY_QT(4) KITTY_QT(5) KITTY_QT(6) KITTY_QT(7)
+            KITTY_QT(8) KITTY_QT(9) KITTY_QT(10) KITTY_QT(11) KITTY_QT(12) KITTY_QT(13) KITTY_QT(14)
+            default: KITTY_QT(15)
+#undef KITTY_QT
+          }
+          qb[e] = qcol ? half2_to16<DT>(h2) : 0u;
+        }
+        mma16<DT>(cs, a, qb[0], qb[1]);
+      }
     }
   }
-  const float sc = r < nw ? v[0] * p.sm_log2 : -INFINITY;
+  const float sc = r < nw ? cs[0] * p.sm_log2 : -INFINITY;
   float pm = fmaxf(sc, __shfl_xor_sync(0xFFFFFFFFu, sc, 4));
   pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 8));
   pm = fmaxf(pm, __shfl_xor_sync(0xFFFFFFFFu, pm, 16));
@@ -557,14 +581,9 @@ __device__ void tail_tokens(WarpState& w, const DecodeParams& p, const __half* q
   const float pr = r < nw ? ex2(sc - w.m) : 0.f;
   w.l += pr;
   // PV on the tensor cores in the input type: A = V^T (channels x this warp's
-  // tokens, the rows past nw zero) by transposing ldmatrix from rows padded to
-  // kTailRow bytes (conflict-free), B = p as (high, rest) pairs in the input
+  // tokens) by transposing ldmatrix, B = p as (high, rest) pairs in the input
   // type: column n = r takes part r & 1 of head r / 2, k = tokens 2qq, 2qq+1
   // (tokens 8..15 of the k-step are absent: B's second register is zero)
-  constexpr int kTailRow = 2 * kD + 16;
-#pragma unroll
-  for (int i = 0; i < 8; ++i) *reinterpret_cast<uint2*>(vbuf + i * kTailRow + 8 * lane) = vx[i];
-  __syncwarp();
   const uint32_t u0 = prob_pair<DT>(__shfl_sync(0xFFFFFFFFu, pr, 8 * qq + (r >> 1)));
   const uint32_t u1 = prob_pair<DT>(__shfl_sync(0xFFFFFFFFu, pr, 8 * qq + 4 + (r >> 1)));
   const uint32_t b0 = __byte_perm(u0, u1, (r & 1) ? 0x7632u : 0x5410u);

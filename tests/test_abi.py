@@ -139,6 +139,16 @@ def test_decode_plan_and_workspace(K):
     # a 16 x 128-page batch in a 136-page table: four 32-page splits, the last to the end
     h = K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=16 * 128, decode_max_pages=128)
     assert K.decode_plan(h, 16, 136) == (4, 40)
+    # equal lengths and few units: one wave of equal splits (without a device the
+    # planner counts 148 SMs: 4 resident CTAs each, 3 for 8 query heads per CTA)
+    h = K.Config(num_kv_heads=8, num_q_heads=64, decode_total_pages=16 * 256, decode_max_pages=256)
+    assert K.decode_plan(h, 16, 257) == (3, 86)      # 128 units of 8 heads, 444 slots: 86, 86, 84 + 1
+    h = K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=8 * 256, decode_max_pages=256)
+    assert K.decode_plan(h, 8, 256) == (9, 29)       # 64 units, 592 slots: nine splits of 29 or fewer
+    # the same total with unequal lengths keeps the longest-first sizes (largest first)
+    h = K.Config(num_kv_heads=8, num_q_heads=32, decode_total_pages=8 * 256 - 1, decode_max_pages=256)
+    s, c = K.decode_plan(h, 8, 256)
+    assert (s, c) != (9, 29) and s * c >= 256
     with pytest.raises(K.KittyError):
         K.decode_plan(K.Config(num_kv_heads=8, num_q_heads=32, decode_max_pages=-1), 4, 16)
     cfg.decode_pages_per_split = 1000

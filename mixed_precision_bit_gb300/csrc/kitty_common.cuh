@@ -215,4 +215,14 @@ __device__ __forceinline__ uint32_t prob_pair(float p) {
   return h2_bits(__floats2half2_rn(t, p - t));
 }
 
+// 16-byte asynchronous global-to-shared copy (L2 only), its group commit and wait.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
 }  // namespace kitty

@@ -277,24 +277,38 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
     for (int i = tid; i < lay.bytes / 16; i += kQThreads)
       reinterpret_cast<uint4*>(sm.blob)[i] = make_uint4(0u, 0u, 0u, 0u);
 
-  // ---- stage the raw 16-bit tile (16-byte loads and stores), classify the range
+  // ---- stage the raw 16-bit tile with asynchronous 16-byte copies, the Keys
+  // in one group and the Values in a second, so that the Values land while the
+  // Key statistics run; each thread classifies the range of the chunks it
+  // copied (read back once its group has landed)
+  constexpr int kChunks = kPage * (kD / 8) / kQThreads;  // 16-byte chunks per thread and tensor
   uint32_t amax = 0u;  // per 16-bit half: the largest |input| bits seen
+  auto chunk_max = [&](const uint16_t (*x)[kRowH]) {
 #pragma unroll
-  for (int it = 0; it < kPage * (kD / 8) / kQThreads; ++it) {
+    for (int it = 0; it < kChunks; ++it) {
+      const int idx = tid + it * kQThreads;
+      const uint4 a = *reinterpret_cast<const uint4*>(&x[idx >> 4][(idx & 15) * 8]);
+      amax = __vmaxu2(amax, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
+                                     __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
+    }
+  };
+#pragma unroll
+  for (int it = 0; it < kChunks; ++it) {
     const int idx = tid + it * kQThreads;
     const int t = idx >> 4, ch = (idx & 15) * 8;
-    const uint4 a = *reinterpret_cast<const uint4*>(ksrc + (size_t)t * row_stride + ch);
-    const uint4 b = *reinterpret_cast<const uint4*>(vsrc + (size_t)t * row_stride + ch);
-    *reinterpret_cast<uint4*>(&sm.xk[t][ch]) = a;
-    *reinterpret_cast<uint4*>(&sm.xv[t][ch]) = b;
-    amax = __vmaxu2(amax, __vmaxu2(__vmaxu2(a.x & 0x7FFF7FFFu, a.y & 0x7FFF7FFFu),
-                                   __vmaxu2(a.z & 0x7FFF7FFFu, a.w & 0x7FFF7FFFu)));
-    amax = __vmaxu2(amax, __vmaxu2(__vmaxu2(b.x & 0x7FFF7FFFu, b.y & 0x7FFF7FFFu),
-                                   __vmaxu2(b.z & 0x7FFF7FFFu, b.w & 0x7FFF7FFFu)));
+    cp_async16(smem_u32(&sm.xk[t][ch]), ksrc + (size_t)t * row_stride + ch);
   }
-  __syncthreads();  // tile staged (blob zeroed if so); sm.bad reset by thread 0 is visible
-  const int bad = range_class_of<DT>(max(amax & 0xFFFFu, amax >> 16));
-  if (bad) atomicCAS(&sm.bad, 0, bad);
+  cp_async_commit();
+#pragma unroll
+  for (int it = 0; it < kChunks; ++it) {
+    const int idx = tid + it * kQThreads;
+    const int t = idx >> 4, ch = (idx & 15) * 8;
+    cp_async16(smem_u32(&sm.xv[t][ch]), vsrc + (size_t)t * row_stride + ch);
+  }
+  cp_async_commit();
+  cp_async_wait<1>();  // this thread's Key chunks have landed
+  chunk_max(sm.xk);
+  __syncthreads();  // Key tile staged (blob zeroed if so); sm.bad reset by thread 0 is visible
 
   // ---- Key channel statistics and variance (thread = channel c)
   const int c = tid;
@@ -336,7 +350,13 @@ __device__ void quantize_tile(QuantSmem& sm, const uint16_t* ksrc, const uint16_
       sm.key[c] = var_key(var);
     }
   }
-  __syncthreads();  // keys (or imposed flags) visible
+  cp_async_wait<0>();  // this thread's Value chunks have landed
+  chunk_max(sm.xv);
+  {
+    const int bad = range_class_of<DT>(max(amax & 0xFFFFu, amax >> 16));
+    if (bad) atomicCAS(&sm.bad, 0, bad);
+  }
+  __syncthreads();  // keys (or imposed flags) and the Value tile visible
   if (fixed < 0 && warp == 0) topk_masks(sm.key, sm.boost, n_hi);
 
   // ---- Value quantization: thread 4t+G owns token t, channels 32G..32G+31

@@ -163,15 +163,6 @@ __global__ void __launch_bounds__(kQThreads) seq_scan_kernel(
 // sequence-mode flags are bit-identical to passes A and B.  Thread c = channel c.
 constexpr int kWalkStages = 2;
 
-__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
-}
-
 template <int DT>
 __global__ void __launch_bounds__(kQThreads) seq_walk_kernel(
     const uint16_t* __restrict__ k, const int32_t* page_ids, const int32_t* seq_of_page,
